@@ -1,0 +1,407 @@
+// oracle.cpp -- plain fp64 CPU reference of the shared ViT encoder forward.
+//
+// TEST INFRASTRUCTURE ONLY: used by tests/, the smoke check and the bench's CPU
+// baseline; never by the product path. Shares nothing with the GPU library
+// except the seeded input generator (synth/jepa_synth.h).
+//
+// Each step is written from the jepa.cpp pages (see oracle.h for the page tags):
+// no blocking, fusion or reordering beyond what the definition states; OpenMP
+// only splits independent rows/heads across threads.
+#include "oracle.h"
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#include "../synth/jepa_synth.h"
+
+namespace {
+
+struct Geometry {
+  int C, t, P, gt, gh, gw, Np, prefix, N, K;
+};
+
+bool geometry(const oracle_hparams* hp, int T, int H, int W, Geometry* g) {
+  if (!hp || T <= 0 || H <= 0 || W <= 0) return false;
+  const int t = hp->tubelet_size, P = hp->patch_size;
+  if (t <= 0 || P <= 0 || T % t || H % P || W % P) return false;
+  g->C = hp->in_chans;
+  g->t = t;
+  g->P = P;
+  g->gt = T / t;
+  g->gh = H / P;
+  g->gw = W / P;
+  g->Np = g->gt * g->gh * g->gw;
+  g->prefix = hp->cls_token ? 1 : 0;
+  g->N = g->Np + g->prefix;
+  g->K = g->C * t * P * P;
+  return true;
+}
+
+// pixel (b, frame, c, y, x) of a [B,T,C,H,W] (layout 0) or [B,C,T,H,W] (layout 1) array.
+inline float pixel_at(const float* pix, int layout, int T, int C, int H, int W, int b, int f, int c, int y,
+                      int x) {
+  size_t idx;
+  if (layout == 0)
+    idx = ((((size_t)b * T + f) * C + c) * H + y) * (size_t)W + x;
+  else
+    idx = ((((size_t)b * C + c) * T + f) * H + y) * (size_t)W + x;
+  return pix[idx];
+}
+
+// Synthetic parameter tensor, generated in parallel chunks (the generator is counter-based).
+void gen_param(uint64_t seed, const std::string& name, int bf16, size_t n, std::vector<double>& dst) {
+  dst.assign(n, 0.0);
+  int kind, is_matrix;
+  double a, b;
+  jsynth_param_init(name.c_str(), &kind, &a, &b, &is_matrix);
+  const int round = (bf16 && is_matrix) ? 1 : 0;
+  const size_t chunk = 4096;
+  const long nchunks = (long)((n + chunk - 1) / chunk);
+#pragma omp parallel
+  {
+    std::vector<float> tmp(chunk);
+#pragma omp for schedule(static)
+    for (long c = 0; c < nchunks; ++c) {
+      size_t first = (size_t)c * chunk;
+      size_t len = std::min(chunk, n - first);
+      jsynth_fill(seed, name.c_str(), kind, a, b, round, first, len, tmp.data());
+      for (size_t j = 0; j < len; ++j) dst[first + j] = (double)tmp[j];
+    }
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+int oracle_n_tokens(const oracle_hparams* hp, int T, int H, int W) {
+  Geometry g;
+  if (!geometry(hp, T, H, W, &g)) return -1;
+  return g.N;
+}
+
+// [A] "The shared ViT graph": rows [N, C*T*P*P]; [S] "Token order": i = t*gh*gw + h*gw + w;
+// [C] flatten_patch_conv: C-T-H-W element order; [K]: element order (c, dt, dh, dw).
+int oracle_patchify(const oracle_hparams* hp, const float* pix, int B, int T, int H, int W, int layout,
+                    double* out) {
+  Geometry g;
+  if (!geometry(hp, T, H, W, &g) || B <= 0) return -1;
+#pragma omp parallel for collapse(2) schedule(static)
+  for (int b = 0; b < B; ++b)
+    for (int i = 0; i < g.Np; ++i) {
+      const int tt = i / (g.gh * g.gw), hh = (i % (g.gh * g.gw)) / g.gw, ww = i % g.gw;
+      double* row = out + ((size_t)b * g.Np + i) * g.K;
+      for (int c = 0; c < g.C; ++c)
+        for (int dt = 0; dt < g.t; ++dt)
+          for (int dy = 0; dy < g.P; ++dy)
+            for (int dx = 0; dx < g.P; ++dx) {
+              const int k = ((c * g.t + dt) * g.P + dy) * g.P + dx;
+              row[k] = pixel_at(pix, layout, T, g.C, H, W, b, tt * g.t + dt, c, hh * g.P + dy, ww * g.P + dx);
+            }
+    }
+  return 0;
+}
+
+// The strided Conv3d the patch embedding replaces ([A] "The shared ViT graph"; [K]):
+// kernel = stride = (t, P, P), no padding.
+int oracle_conv3d(const oracle_hparams* hp, const float* pix, int B, int T, int H, int W, int layout,
+                  const double* w, const double* bias, double* out) {
+  Geometry g;
+  if (!geometry(hp, T, H, W, &g) || B <= 0) return -1;
+  const int D = hp->embed_dim;
+#pragma omp parallel for collapse(4) schedule(static)
+  for (int b = 0; b < B; ++b)
+    for (int ot = 0; ot < g.gt; ++ot)
+      for (int oy = 0; oy < g.gh; ++oy)
+        for (int ox = 0; ox < g.gw; ++ox)
+          for (int d = 0; d < D; ++d) {
+            double acc = bias ? bias[d] : 0.0;
+            for (int c = 0; c < g.C; ++c)
+              for (int kt = 0; kt < g.t; ++kt)
+                for (int ky = 0; ky < g.P; ++ky)
+                  for (int kx = 0; kx < g.P; ++kx) {
+                    const double wv = w[((((size_t)d * g.C + c) * g.t + kt) * g.P + ky) * g.P + kx];
+                    acc += wv * (double)pixel_at(pix, layout, T, g.C, H, W, b, ot * g.t + kt, c, oy * g.P + ky,
+                                                 ox * g.P + kx);
+                  }
+            out[((((size_t)b * g.gt + ot) * g.gh + oy) * g.gw + ox) * D + d] = acc;
+          }
+  return 0;
+}
+
+// y = x w^T + b, the ggml_mul_mat of every linear layer ([S] weights stored [out, in]).
+void oracle_linear(const double* x, int M, int K, const double* w, const double* b, int N, double* y) {
+  const int IB = 16;  // rows of x sharing one pass over w (cache reuse only; same sums)
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+  for (int i0 = 0; i0 < M; i0 += IB)
+    for (int j0 = 0; j0 < N; j0 += 64) {
+      const int i1 = std::min(M, i0 + IB), j1 = std::min(N, j0 + 64);
+      for (int j = j0; j < j1; ++j) {
+        const double* wr = w + (size_t)j * K;
+        for (int i = i0; i < i1; ++i) {
+          const double* xr = x + (size_t)i * K;
+          double acc = 0.0;
+#pragma omp simd reduction(+ : acc)
+          for (int k = 0; k < K; ++k) acc += xr[k] * wr[k];
+          y[(size_t)i * N + j] = acc + (b ? b[j] : 0.0);
+        }
+      }
+    }
+}
+
+// LayerNorm: mean, centred biased variance, (x - mu) / sqrt(var + eps) * gamma + beta.
+void oracle_layernorm(const double* x, int M, int D, const double* gamma, const double* beta, double eps,
+                      double* y) {
+#pragma omp parallel for schedule(static)
+  for (int i = 0; i < M; ++i) {
+    const double* xr = x + (size_t)i * D;
+    double mu = 0.0;
+    for (int j = 0; j < D; ++j) mu += xr[j];
+    mu /= D;
+    double var = 0.0;
+    for (int j = 0; j < D; ++j) var += (xr[j] - mu) * (xr[j] - mu);
+    var /= D;
+    const double rstd = 1.0 / std::sqrt(var + eps);
+    for (int j = 0; j < D; ++j) y[(size_t)i * D + j] = (xr[j] - mu) * rstd * gamma[j] + beta[j];
+  }
+}
+
+void oracle_gelu(const double* x, size_t n, double* y) {
+#pragma omp parallel for schedule(static)
+  for (long i = 0; i < (long)n; ++i) y[i] = 0.5 * x[i] * (1.0 + std::erf(x[i] / std::sqrt(2.0)));
+}
+
+// [A] "3-D RoPE": t = i // (gh gw), h = (i % (gh gw)) // gw, w = i % gw; V-JEPA 2.1 rescales
+// h and w (not t) by (rope_ref_grid - 1) / (grid - 1). A grid of one row keeps its position.
+int oracle_rope_positions(const oracle_hparams* hp, int T, int H, int W, double* pos) {
+  Geometry g;
+  if (!geometry(hp, T, H, W, &g)) return -1;
+  const double sh = (hp->rope_interpolate && g.gh > 1) ? (double)(hp->rope_ref_grid - 1) / (double)(g.gh - 1) : 1.0;
+  const double sw = (hp->rope_interpolate && g.gw > 1) ? (double)(hp->rope_ref_grid - 1) / (double)(g.gw - 1) : 1.0;
+  for (int i = 0; i < g.Np; ++i) {
+    pos[3 * i + 0] = (double)(i / (g.gh * g.gw));
+    pos[3 * i + 1] = (double)((i % (g.gh * g.gw)) / g.gw) * sh;
+    pos[3 * i + 2] = (double)(i % g.gw) * sw;
+  }
+  return 0;
+}
+
+// [A] "3-D RoPE": per axis d = 2*((hd//3)//2) dims; omega_k = 1/theta^(2k/d), k < d/2;
+// tiled table[j] = f(pos * omega_{j mod d/2}) (V-JEPA 2), interleaved table[2k] = table[2k+1]
+// = f(pos * omega_k) (V-JEPA 2.1); x cos + rot90(x) sin with rot90(y1, y2) = (-y2, y1), the
+// sign carried in the sin table; prefix (CLS) rows are identity ([S] levjepa note).
+int oracle_rope_tables(const oracle_hparams* hp, int T, int H, int W, double* cos_t, double* sin_t) {
+  Geometry g;
+  if (!geometry(hp, T, H, W, &g)) return -1;
+  const int hd = hp->embed_dim / hp->n_head;
+  const int d = 2 * ((hd / 3) / 2);
+  std::vector<double> pos((size_t)g.Np * 3);
+  oracle_rope_positions(hp, T, H, W, pos.data());
+  for (int n = 0; n < g.N; ++n) {
+    double* cr = cos_t + (size_t)n * hd;
+    double* sr = sin_t + (size_t)n * hd;
+    for (int j = 0; j < hd; ++j) { cr[j] = 1.0; sr[j] = 0.0; }
+    if (n < g.prefix) continue;
+    const int i = n - g.prefix;
+    for (int a = 0; a < 3; ++a)
+      for (int jj = 0; jj < d; ++jj) {
+        const int kidx = (hp->rope_layout == 0) ? (jj % (d / 2)) : (jj / 2);
+        const double omega = 1.0 / std::pow(hp->rope_theta, 2.0 * kidx / d);
+        const double th = pos[3 * i + a] * omega;
+        cr[a * d + jj] = std::cos(th);
+        sr[a * d + jj] = ((jj % 2 == 0) ? -1.0 : 1.0) * std::sin(th);
+      }
+  }
+  return 0;
+}
+
+void oracle_rope_apply(const double* x, int N, int n_head, int hd, const double* cos_t, const double* sin_t,
+                       double* out) {
+#pragma omp parallel for schedule(static)
+  for (int n = 0; n < N; ++n)
+    for (int h = 0; h < n_head; ++h) {
+      const double* xr = x + ((size_t)n * n_head + h) * hd;
+      double* orow = out + ((size_t)n * n_head + h) * hd;
+      const double* cr = cos_t + (size_t)n * hd;
+      const double* sr = sin_t + (size_t)n * hd;
+      for (int j = 0; j < hd; ++j) orow[j] = xr[j] * cr[j] + ((j ^ 1) < hd ? xr[j ^ 1] * sr[j] : 0.0);
+    }
+}
+
+// [S] levjepa note; [A] "Block-causal attention": key j visible to query i iff
+// frame_id(i) >= frame_id(j), frame_id = id // (gh gw) of the patch token; CLS row open,
+// CLS column closed to patch queries.
+int oracle_mask_allow(int attn_mode, int prefix, int frame_tokens, int N, int q, int k) {
+  if (k < 0 || k >= N || q < 0 || q >= N) return 0;
+  if (attn_mode == 0) return 1;
+  if (q < prefix) return 1;
+  if (k < prefix) return 0;
+  return ((q - prefix) / frame_tokens) >= ((k - prefix) / frame_tokens);
+}
+
+// softmax(q k^T / sqrt(hd) + mask) v per head, in fp64, masked keys excluded.
+void oracle_attention(const double* q, const double* k, const double* v, int N, int n_head, int hd,
+                      int attn_mode, int prefix, int frame_tokens, double* o) {
+  const size_t ld = (size_t)n_head * hd;
+  const double scale = 1.0 / std::sqrt((double)hd);
+  for (int h = 0; h < n_head; ++h) {
+#pragma omp parallel
+    {
+      std::vector<double> s(N);
+#pragma omp for schedule(static)
+      for (int i = 0; i < N; ++i) {
+        const double* qi = q + (size_t)i * ld + (size_t)h * hd;
+        double mx = -INFINITY;
+        for (int j = 0; j < N; ++j) {
+          if (!oracle_mask_allow(attn_mode, prefix, frame_tokens, N, i, j)) { s[j] = -INFINITY; continue; }
+          const double* kj = k + (size_t)j * ld + (size_t)h * hd;
+          double acc = 0.0;
+          for (int c = 0; c < hd; ++c) acc += qi[c] * kj[c];
+          s[j] = acc * scale;
+          if (s[j] > mx) mx = s[j];
+        }
+        double sum = 0.0;
+        for (int j = 0; j < N; ++j) {
+          s[j] = (s[j] == -INFINITY) ? 0.0 : std::exp(s[j] - mx);
+          sum += s[j];
+        }
+        double* oi = o + (size_t)i * ld + (size_t)h * hd;
+        for (int c = 0; c < hd; ++c) oi[c] = 0.0;
+        for (int j = 0; j < N; ++j) {
+          if (s[j] == 0.0) continue;
+          const double p = s[j] / sum;
+          const double* vj = v + (size_t)j * ld + (size_t)h * hd;
+          for (int c = 0; c < hd; ++c) oi[c] += p * vj[c];
+        }
+      }
+    }
+  }
+}
+
+// [A] "The shared ViT graph":
+//   tokens = patch_embed(rearranged pixels) [+ pos_embed] [+ cls] [+ modality vec]
+//   for each block: x += attn(ln1(x)); x += ffn(ln2(x))   (pre-LN, GELU(erf), qkv bias)
+//   x = norm(x)
+int oracle_encode(const oracle_hparams* hp, uint64_t seed, int bf16_weights, const float* pix, int B, int T,
+                  int H, int W, int layout, int final_norm, double* out) {
+  Geometry g;
+  if (!geometry(hp, T, H, W, &g) || B <= 0) return -1;
+  const int D = hp->embed_dim, F = hp->ffn_dim, NH = hp->n_head;
+  if (NH <= 0 || D % NH) return -1;
+  const int hd = D / NH;
+  const int N = g.N, Np = g.Np, prefix = g.prefix;
+  if (hp->pos_type == 1 && hp->n_pos_rows != N) return -2;  // learned table must cover every token
+  const size_t MD = (size_t)N * D;
+
+  // ---- patch embedding, prefix and position/modality terms ----
+  std::vector<double> patches((size_t)B * Np * g.K);
+  oracle_patchify(hp, pix, B, T, H, W, layout, patches.data());
+  std::vector<double> wpe, bpe;
+  gen_param(seed, "enc.patch_embed.weight", bf16_weights, (size_t)D * g.K, wpe);
+  gen_param(seed, "enc.patch_embed.bias", bf16_weights, D, bpe);
+  std::vector<double> emb((size_t)B * Np * D);
+  oracle_linear(patches.data(), B * Np, g.K, wpe.data(), bpe.data(), D, emb.data());
+  patches.clear();
+  patches.shrink_to_fit();
+
+  std::vector<double> X((size_t)B * MD, 0.0);
+  std::vector<double> cls, pos, mod;
+  if (hp->cls_token) gen_param(seed, "enc.cls_token", bf16_weights, D, cls);
+  if (hp->pos_type == 1) gen_param(seed, "enc.pos_embed", bf16_weights, (size_t)hp->n_pos_rows * D, pos);
+  if (hp->modality_embed) gen_param(seed, "enc.mod_embed_video", bf16_weights, D, mod);
+  for (int b = 0; b < B; ++b)
+    for (int n = 0; n < N; ++n) {
+      double* xr = X.data() + (size_t)b * MD + (size_t)n * D;
+      for (int c = 0; c < D; ++c) {
+        double v = (n < prefix) ? cls[c] : emb[((size_t)b * Np + (n - prefix)) * D + c];
+        if (hp->pos_type == 1) v += pos[(size_t)n * D + c];  // rows = [CLS?; patches]
+        if (hp->modality_embed) v += mod[c];
+        xr[c] = v;
+      }
+    }
+  emb.clear();
+  emb.shrink_to_fit();
+
+  // ---- RoPE tables (shared by all layers and heads) ----
+  std::vector<double> rc, rs;
+  if (hp->pos_type == 2) {
+    rc.resize((size_t)N * hd);
+    rs.resize((size_t)N * hd);
+    oracle_rope_tables(hp, T, H, W, rc.data(), rs.data());
+  }
+  const int frame_tokens = g.gh * g.gw;
+
+  std::vector<double> h(MD), qkv((size_t)N * 3 * D), q(MD), k(MD), v(MD), o(MD), tmp(MD), u((size_t)N * F);
+  for (int l = 0; l < hp->n_layer; ++l) {
+    const std::string p = "enc.blk." + std::to_string(l) + ".";
+    std::vector<double> ln1w, ln1b, wqkv, bqkv, wout, bout, ln2w, ln2b, wup, bup, wdn, bdn;
+    gen_param(seed, p + "ln1.weight", bf16_weights, D, ln1w);
+    gen_param(seed, p + "ln1.bias", bf16_weights, D, ln1b);
+    gen_param(seed, p + "attn_qkv.weight", bf16_weights, (size_t)3 * D * D, wqkv);
+    gen_param(seed, p + "attn_qkv.bias", bf16_weights, (size_t)3 * D, bqkv);
+    gen_param(seed, p + "attn_out.weight", bf16_weights, (size_t)D * D, wout);
+    gen_param(seed, p + "attn_out.bias", bf16_weights, D, bout);
+    gen_param(seed, p + "ln2.weight", bf16_weights, D, ln2w);
+    gen_param(seed, p + "ln2.bias", bf16_weights, D, ln2b);
+    gen_param(seed, p + "ffn_up.weight", bf16_weights, (size_t)F * D, wup);
+    gen_param(seed, p + "ffn_up.bias", bf16_weights, F, bup);
+    gen_param(seed, p + "ffn_down.weight", bf16_weights, (size_t)D * F, wdn);
+    gen_param(seed, p + "ffn_down.bias", bf16_weights, D, bdn);
+
+    for (int b = 0; b < B; ++b) {
+      double* x = X.data() + (size_t)b * MD;
+      // x += attn(ln1(x)): fused qkv rows [q; k; v] ([S] attn_qkv), heads contiguous in each.
+      oracle_layernorm(x, N, D, ln1w.data(), ln1b.data(), hp->ln_eps, h.data());
+      oracle_linear(h.data(), N, D, wqkv.data(), bqkv.data(), 3 * D, qkv.data());
+      for (int n = 0; n < N; ++n)
+        for (int c = 0; c < D; ++c) {
+          q[(size_t)n * D + c] = qkv[(size_t)n * 3 * D + c];
+          k[(size_t)n * D + c] = qkv[(size_t)n * 3 * D + D + c];
+          v[(size_t)n * D + c] = qkv[(size_t)n * 3 * D + 2 * D + c];
+        }
+      if (hp->pos_type == 2) {  // on q and k, not v, after the projection and before scaling
+        oracle_rope_apply(q.data(), N, NH, hd, rc.data(), rs.data(), tmp.data());
+        q.swap(tmp);
+        oracle_rope_apply(k.data(), N, NH, hd, rc.data(), rs.data(), tmp.data());
+        k.swap(tmp);
+      }
+      oracle_attention(q.data(), k.data(), v.data(), N, NH, hd, hp->attn_mode, prefix, frame_tokens, o.data());
+      oracle_linear(o.data(), N, D, wout.data(), bout.data(), D, tmp.data());
+      for (size_t i = 0; i < MD; ++i) x[i] += tmp[i];
+      // x += ffn(ln2(x)) with GELU(erf)
+      oracle_layernorm(x, N, D, ln2w.data(), ln2b.data(), hp->ln_eps, h.data());
+      oracle_linear(h.data(), N, D, wup.data(), bup.data(), F, u.data());
+      oracle_gelu(u.data(), u.size(), u.data());
+      oracle_linear(u.data(), N, F, wdn.data(), bdn.data(), D, tmp.data());
+      for (size_t i = 0; i < MD; ++i) x[i] += tmp[i];
+    }
+  }
+
+  if (final_norm) {
+    std::vector<double> nw, nb;
+    gen_param(seed, "enc.norm.weight", bf16_weights, D, nw);
+    gen_param(seed, "enc.norm.bias", bf16_weights, D, nb);
+    for (int b = 0; b < B; ++b)
+      oracle_layernorm(X.data() + (size_t)b * MD, N, D, nw.data(), nb.data(), hp->ln_eps, out + (size_t)b * MD);
+  } else {
+    std::memcpy(out, X.data(), X.size() * sizeof(double));
+  }
+  return 0;
+}
+
+}  // extern "C"

@@ -1,0 +1,102 @@
+/*
+ * oracle.h -- plain, slow, fp64 CPU reference of the shared ViT encoder forward.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing in the product library includes, links or
+ * calls this code; only the tests, the smoke check and the bench's CPU-baseline
+ * leg use it. It shares no code with the GPU path except the seeded input
+ * generator (synth/jepa_synth.h).
+ *
+ * Every function follows a passage of the jepa.cpp pages:
+ *   [S] = jepa.cpp "GGUF schema (v1)"      (tensor table, token order, family notes)
+ *   [A] = jepa.cpp "Architecture"          (shared ViT graph, 3-D RoPE, block-causal attention)
+ *   [C] = jepa.cpp "Converter"             (conv flattening, qkv fusing, hfvit/levjepa maps)
+ *   [K] = SkyVision.cpp README, V-JEPA 2 section (tubelet packing order, tiled-RoPE quirk)
+ *
+ * All arithmetic is double precision; bf16 inputs (weights of the bf16 mode)
+ * enter as their exact values.
+ */
+#ifndef JEPA_ORACLE_H
+#define JEPA_ORACLE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Encoder hyper-parameters, mirroring the jepa.enc.* keys of [S] "Encoder". */
+typedef struct {
+  int embed_dim, n_layer, n_head, ffn_dim;
+  int patch_size, tubelet_size, in_chans;
+  double ln_eps, rope_theta;
+  int pos_type;         /* 0 none, 1 learned table, 2 rope3d */
+  int rope_layout;      /* 0 tiled (V-JEPA 2), 1 interleaved (V-JEPA 2.1) */
+  int rope_interpolate; /* V-JEPA 2.1 interpolate_rope */
+  int rope_ref_grid;    /* 256 / patch_size */
+  int cls_token;        /* prepend enc.cls_token */
+  int modality_embed;   /* add enc.mod_embed_video to every token */
+  int attn_mode;        /* 0 full, 1 block_causal */
+  int n_pos_rows;       /* rows of enc.pos_embed (learned only) */
+} oracle_hparams;
+
+/* Number of tokens of one item: (T/t)(H/P)(W/P) + cls. Returns -1 if a size is not divisible. */
+int oracle_n_tokens(const oracle_hparams* hp, int T, int H, int W);
+
+/* Pixel -> patch rows ([A] "The shared ViT graph"; [S] "Token order"; [K] tubelet packing).
+ * pix: [B,T,C,H,W] (layout 0) or [B,C,T,H,W] (layout 1), float.
+ * out: [B*Np, C*t*P*P], element k = ((c*t + dt)*P + dy)*P + dx, token i = (tt*gh + hh)*gw + ww. */
+int oracle_patchify(const oracle_hparams* hp, const float* pix, int B, int T, int H, int W, int layout,
+                    double* out);
+
+/* Brute-force strided 3-D convolution (kernel = stride = (t, P, P)), the operation the
+ * rearrangement + matmul replaces ([A] "The shared ViT graph").
+ * w: [D, C, t, P, P]; out: [B, gt, gh, gw, D]. */
+int oracle_conv3d(const oracle_hparams* hp, const float* pix, int B, int T, int H, int W, int layout,
+                  const double* w, const double* bias, double* out);
+
+/* y = x w^T + b; x [M,K], w [N,K] (PyTorch row-major, [S] tensor table), b [N] or NULL. */
+void oracle_linear(const double* x, int M, int K, const double* w, const double* b, int N, double* y);
+
+/* LayerNorm over rows: centred two-pass biased variance, eps inside the sqrt ([A] "Attention and precision"). */
+void oracle_layernorm(const double* x, int M, int D, const double* gamma, const double* beta, double eps,
+                      double* y);
+
+/* GELU(erf): 0.5 x (1 + erf(x / sqrt 2)) ([S] jepa.enc.act = gelu_erf). */
+void oracle_gelu(const double* x, size_t n, double* y);
+
+/* Per-patch-token RoPE positions (t, h, w) ([A] "3-D RoPE"), with interpolate_rope
+ * scaling of h and w by (ref-1)/(g-1). pos: [Np, 3]. */
+int oracle_rope_positions(const oracle_hparams* hp, int T, int H, int W, double* pos);
+
+/* cos / signed-sin tables [N, hd] for all N tokens (prefix rows are identity), so that
+ * rope(x)[j] = x[j] cos[j] + x[j^1] sin[j] for j < 3d and x[j] for the rest. */
+int oracle_rope_tables(const oracle_hparams* hp, int T, int H, int W, double* cos_t, double* sin_t);
+
+/* Apply the tables to x [N, H*hd] in place-free form (q and k of every head). */
+void oracle_rope_apply(const double* x, int N, int n_head, int hd, const double* cos_t, const double* sin_t,
+                       double* out);
+
+/* Is key k visible to query q? attn_mode 0: every k < N. attn_mode 1 (block-causal,
+ * [S] levjepa note; [A] "Block-causal attention"): prefix rows see everything, prefix
+ * columns are closed to patch queries, patch keys visible iff frame(q) >= frame(k). */
+int oracle_mask_allow(int attn_mode, int prefix, int frame_tokens, int N, int q, int k);
+
+/* Softmax attention per head: o = softmax(q k^T / sqrt(hd) + mask) v.
+ * q, k, v, o: [N, H*hd], heads contiguous ([A] "Attention and precision"). */
+void oracle_attention(const double* q, const double* k, const double* v, int N, int n_head, int hd,
+                      int attn_mode, int prefix, int frame_tokens, double* o);
+
+/* The whole encoder ([A] "The shared ViT graph") for B items with synthetic weights of
+ * `seed` (bf16_weights != 0 rounds the matrix weights to bf16, as the bf16 model holds them).
+ * out: [B, N, D]; final_norm = 0 returns the residual stream before enc.norm. */
+int oracle_encode(const oracle_hparams* hp, uint64_t seed, int bf16_weights, const float* pix, int B, int T,
+                  int H, int W, int layout, int final_norm, double* out);
+
+/* Number of OpenMP threads the oracle uses. */
+int oracle_num_threads(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
