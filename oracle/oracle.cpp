@@ -4,9 +4,10 @@
 // baseline; never by the product path. Shares nothing with the GPU library
 // except the seeded input generator (synth/jepa_synth.h).
 //
-// Each step is written from the jepa.cpp pages (see oracle.h for the page tags):
-// no blocking, fusion or reordering beyond what the definition states; OpenMP
-// only splits independent rows/heads across threads.
+// Each step is written from the jepa.cpp pages (see oracle.h for the page tags),
+// with no fusion and no reordering of the method's steps. OpenMP only splits
+// independent rows / heads across threads; the row blocking of oracle_linear and
+// the vectorised dot products change nothing but the rounding order of the sums.
 #include "oracle.h"
 
 #include <cmath>
@@ -271,6 +272,7 @@ void oracle_attention(const double* q, const double* k, const double* v, int N, 
           if (!oracle_mask_allow(attn_mode, prefix, frame_tokens, N, i, j)) { s[j] = -INFINITY; continue; }
           const double* kj = k + (size_t)j * ld + (size_t)h * hd;
           double acc = 0.0;
+#pragma omp simd reduction(+ : acc)
           for (int c = 0; c < hd; ++c) acc += qi[c] * kj[c];
           s[j] = acc * scale;
           if (s[j] > mx) mx = s[j];
