@@ -1,0 +1,235 @@
+/*
+ * jepa.h -- C ABI of the GB300 (sm_103a) ViT encoder library (libjepa_gb300.so).
+ *
+ * The library runs the forward pass of the shared ViT encoder graph of the jepa.cpp
+ * pages ("Architecture", section "The shared ViT graph"):
+ *
+ *   tokens = patch_embed(rearranged pixels) [+ pos_embed] [+ cls] [+ modality vec]
+ *   for each block:  x += attn(ln1(x));  x += ffn(ln2(x))    (pre-LN, GELU(erf), qkv bias)
+ *   x = norm(x)
+ *
+ * on hand-written CUDA kernels: a pixel->patch rearrangement, tcgen05/TMEM GEMMs fed by TMA
+ * (patch embed, fused QKV with bias + 3-D RoPE, out-projection + residual, FFN up + GELU,
+ * FFN down + residual), a tcgen05 flash-attention kernel (full or block-causal), LayerNorm,
+ * and an fp32 SIMT path for the fp32 mode. Weights are synthetic (seeded), laid out under
+ * the GGUF schema's enc.* names and shapes ("GGUF schema (v1)", Encoder tensors).
+ *
+ * Conventions (shared by every entry point):
+ *  - Every function returns jepa_status; on failure a human-readable reason is kept in a
+ *    thread-local buffer (jepa_error_text), and nothing is clamped or defaulted silently
+ *    ("Architecture", Robustness).
+ *  - Pointers named d_* are device pointers (cudaMalloc / torch CUDA memory) on the model's
+ *    device; pointers named h_* are host pointers. The caller owns every buffer it passes;
+ *    the library owns the weights (jepa_model) and the workspace (jepa_context).
+ *  - Launches are asynchronous on the context's (or the op's) stream. Argument errors are
+ *    returned synchronously. A bounded device-side wait that gives up (a kernel that could
+ *    not make progress within its time limit) is reported as JEPA_E_TIMEOUT by the next
+ *    jepa_context_sync / jepa_device_status.
+ *  - Thread contract ("Architecture", Robustness): a jepa_model is immutable after load and
+ *    may be shared by any number of threads; a jepa_context belongs to one thread at a time.
+ *  - Layouts are row-major (C order). bf16 = bfloat16 stored as uint16_t bit patterns.
+ */
+#ifndef JEPA_H
+#define JEPA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct jepa_model jepa_model;
+typedef struct jepa_context jepa_context;
+
+typedef enum {
+  JEPA_OK = 0,
+  JEPA_E_INVALID_ARG = 1, /* a null pointer, a non-positive or non-divisible size */
+  JEPA_E_UNSUPPORTED = 2, /* a valid request this build cannot run (e.g. head_dim not 64) */
+  JEPA_E_BUDGET = 3,      /* the workspace would exceed the caller's byte budget, or the context's max shape */
+  JEPA_E_OOM = 4,         /* cudaMalloc failed */
+  JEPA_E_CUDA = 5,        /* a CUDA runtime call failed */
+  JEPA_E_TIMEOUT = 6      /* a device-side bounded wait expired; the context is still usable */
+} jepa_status;
+
+typedef enum { JEPA_FP32 = 0, JEPA_BF16 = 1 } jepa_dtype;
+typedef enum { JEPA_POS_NONE = 0, JEPA_POS_LEARNED = 1, JEPA_POS_ROPE3D = 2 } jepa_pos_type;
+typedef enum { JEPA_ROPE_TILED = 0, JEPA_ROPE_INTERLEAVED = 1 } jepa_rope_layout;
+typedef enum { JEPA_ATTN_FULL = 0, JEPA_ATTN_BLOCK_CAUSAL = 1 } jepa_attn_mode;
+typedef enum { JEPA_LAYOUT_TCHW = 0, JEPA_LAYOUT_CTHW = 1 } jepa_pixel_layout;
+
+/* Encoder hyper-parameters, mirroring the jepa.enc.* keys ("GGUF schema (v1)", Encoder).
+ *  pos_type        JEPA_POS_LEARNED: enc.pos_embed [n_pos_rows, D], rows = [CLS?; patches]
+ *                  JEPA_POS_ROPE3D : 3-D RoPE on q and k ("Architecture", 3-D RoPE)
+ *  rope_layout     tiled (V-JEPA 2) or interleaved (V-JEPA 2.1) cos/sin table layout
+ *  rope_interpolate, rope_ref_grid   V-JEPA 2.1: h, w rescaled by (ref-1)/(grid-1)
+ *  cls_token       prepend enc.cls_token (no position information for it)
+ *  modality_embed  add enc.mod_embed_video to every token (V-JEPA 2.1)
+ *  attn_mode       full, or LeVJEPA's block-causal mask ("Architecture", Block-causal attention)
+ *  img_size, n_frames  training geometry (informational; jepa_encode takes the clip's own T,H,W) */
+typedef struct {
+  int32_t embed_dim, n_layer, n_head, ffn_dim;
+  int32_t patch_size, tubelet_size, img_size, n_frames, in_chans;
+  float ln_eps, rope_theta;
+  int32_t pos_type, rope_layout, rope_interpolate, rope_ref_grid;
+  int32_t cls_token, modality_embed, attn_mode, n_pos_rows;
+} jepa_hparams;
+
+/* ------------------------------------------------------------------ configuration */
+
+/* Fill *out with a named workload's hyper-parameters. Names:
+ *  "hfvit_ti14"      ViT-Ti/14 image encoder, learned pos + CLS (hfvit / LeWM encoder shape)
+ *  "vjepa2_vitl16"   V-JEPA 2 ViT-L/16, tubelet 2, tiled 3-D RoPE
+ *  "vjepa2_1_vitl16" V-JEPA 2.1 ViT-L/16, interleaved RoPE, interpolate_rope (ref grid 16), modality vector
+ *  "levjepa_vitl16"  LeVJEPA ViT-L/16, tubelet 1, CLS, tiled RoPE, block-causal
+ *  "vjepa2_vitg16"   V-JEPA 2 ViT-g/16 (embed 1408, 40 layers, 22 heads, ffn 6144)
+ * Unknown name -> JEPA_E_INVALID_ARG. */
+jepa_status jepa_preset(const char* name, jepa_hparams* out);
+
+/* Range and invariant checks of "Architecture", Robustness (what the loader validates):
+ * sizes in range, embed_dim % n_head == 0, even head width on a RoPE model, rope_interpolate
+ * with a ref grid, ln_eps in [0, 1], rope_theta > 0, a learned table with rows. */
+jepa_status jepa_hparams_validate(const jepa_hparams* hp);
+
+/* Tokens of one item of a T x H x W clip: (T/t)(H/P)(W/P) + cls ("GGUF schema (v1)", Token order).
+ * Refuses sizes that are not divisible by the tubelet / patch (no cropping). */
+jepa_status jepa_n_tokens(const jepa_hparams* hp, int32_t T, int32_t H, int32_t W, int32_t* n_out);
+
+/* ------------------------------------------------------------------ model */
+
+/* Synthesise every enc.* tensor of `hp` from `seed` (synth/jepa_synth.h recipe: matrices
+ * N(0,0.02), biases 0.01 N(0,1), LN gamma 1+0.1 N(0,1), beta 0.01 N(0,1), cls/pos/modality
+ * N(0,0.02)) and upload it to CUDA device `device`. dtype JEPA_BF16 stores the matrix weights
+ * (patch_embed, attn_qkv, attn_out, ffn_up, ffn_down) as bf16 and computes in bf16 with fp32
+ * accumulation; JEPA_FP32 keeps everything fp32. Norms, biases and vectors stay fp32 in both
+ * ("GGUF schema (v1)", Quantization rules). The returned model is immutable. */
+jepa_status jepa_model_load(const jepa_hparams* hp, uint64_t seed, int32_t dtype, int32_t device,
+                            jepa_model** out);
+void jepa_model_free(jepa_model* m);
+jepa_status jepa_model_hparams(const jepa_model* m, jepa_hparams* out);
+
+/* Copy the enc.* tensor `name` (e.g. "enc.blk.3.attn_qkv.weight") to host memory as float:
+ * n_elems must equal the tensor's element count (shape per the GGUF schema, PyTorch row-major).
+ * Synchronous. Unknown name -> JEPA_E_INVALID_ARG. */
+jepa_status jepa_model_tensor(const jepa_model* m, const char* name, float* h_dst, size_t n_elems);
+
+/* ------------------------------------------------------------------ context */
+
+/* Allocate a workspace for clips of up to max_batch items of max_frames x max_height x max_width
+ * ("Architecture", The engine in one page: jepa_context_new allocates a compute arena).
+ * max_workspace_bytes = 0 means 8 GiB. Over budget -> JEPA_E_BUDGET (refused, not allocated).
+ * The context starts on its own non-blocking stream of the model's device. */
+jepa_status jepa_context_new(const jepa_model* m, int32_t max_batch, int32_t max_frames, int32_t max_height,
+                             int32_t max_width, size_t max_workspace_bytes, jepa_context** out);
+void jepa_context_free(jepa_context* c);
+/* Use `stream` (a cudaStream_t, e.g. torch.cuda.current_stream().cuda_stream) for all launches. */
+jepa_status jepa_context_set_stream(jepa_context* c, void* stream);
+/* enable != 0: capture the encode launch sequence of a (shape, pixel ptr, token ptr) key into a
+ * CUDA graph on first use and replay it afterwards ("Architecture", GPU backend: graph replay).
+ * The context stream must then not be the legacy default stream. */
+jepa_status jepa_context_set_graph(jepa_context* c, int32_t enable);
+jepa_status jepa_context_workspace_bytes(const jepa_context* c, size_t* out);
+/* Kernel launches one jepa_encode of this shape issues (graph replay counts the kernels inside). */
+jepa_status jepa_context_launches(const jepa_context* c, int32_t B, int32_t T, int32_t H, int32_t W,
+                                  int32_t* n_out);
+
+/* Encode B clips. d_pixels: float [B,T,C,H,W] (layout JEPA_LAYOUT_TCHW) or [B,C,T,H,W]
+ * (JEPA_LAYOUT_CTHW, the NCTHW tensor of "Architecture", Video ingest), already normalised.
+ * d_tokens: float [B, N, embed_dim], N from jepa_n_tokens, after the final norm. Items never
+ * mix ("Architecture", Batching). Asynchronous on the context stream. Shapes beyond the context's
+ * max -> JEPA_E_BUDGET; not divisible -> JEPA_E_INVALID_ARG. A 16-byte aligned d_pixels takes the
+ * vectorised rearrangement. */
+jepa_status jepa_encode(jepa_context* c, const float* d_pixels, int32_t B, int32_t T, int32_t H, int32_t W,
+                        int32_t layout, float* d_tokens);
+
+/* Same with HOST buffers: copies h_pixels to the device, encodes, copies the tokens back and
+ * waits. Pinned host memory makes the copies asynchronous DMA; pageable memory also works. */
+jepa_status jepa_encode_host(jepa_context* c, const float* h_pixels, int32_t B, int32_t T, int32_t H,
+                             int32_t W, int32_t layout, float* h_tokens);
+
+/* Wait for the context stream and report device-side errors (JEPA_E_TIMEOUT) raised since the
+ * last check. */
+jepa_status jepa_context_sync(jepa_context* c);
+
+/* ------------------------------------------------------------------ stage entry points
+ * The kernels the encoder runs, callable one at a time (tests compare each against the oracle).
+ * `stream` is a cudaStream_t (NULL = legacy default stream). Device errors of these calls are
+ * reported by jepa_device_status. */
+
+/* Rearrange pixels into patch rows ("Architecture", The shared ViT graph; element order
+ * (c, dt, dy, dx), token order (t, h, w)). d_out: [B*Np, C*t*P*P] float (out_dtype JEPA_FP32)
+ * or bf16 (JEPA_BF16). */
+jepa_status jepa_op_patchify(const float* d_pixels, int32_t B, int32_t T, int32_t C, int32_t H, int32_t W,
+                             int32_t tubelet, int32_t patch, int32_t layout, int32_t out_dtype, void* d_out,
+                             void* stream);
+
+/* LayerNorm over rows with a centred two-pass variance ("Architecture", Attention and precision):
+ * d_y = (x - mean) / sqrt(var + eps) * gamma + beta; d_x float [M, D]; d_y float or bf16 [M, D].
+ * D must be a multiple of 4 and at most 2048. */
+jepa_status jepa_op_layernorm(const float* d_x, int32_t M, int32_t D, const float* d_gamma,
+                              const float* d_beta, float eps, int32_t out_dtype, void* d_y, void* stream);
+
+/* What a GEMM does with its accumulator tile (the fused epilogues of the encoder). */
+typedef enum {
+  JEPA_EPI_BIAS = 0,          /* out[m,n] = acc + bias[n]                                   */
+  JEPA_EPI_BIAS_GELU = 1,     /* out[m,n] = GELU_erf(acc + bias[n])                         */
+  JEPA_EPI_BIAS_RESIDUAL = 2, /* out[m,n] += acc + bias[n]   (out is the fp32 residual X)    */
+  JEPA_EPI_QKV_ROPE = 3,      /* out = acc + bias, then 3-D RoPE on the q and k columns      */
+  JEPA_EPI_PATCH_EMBED = 4    /* X[b*rows_per_item + prefix + i] = acc + bias (+pos) (+vec)  */
+} jepa_epi_kind;
+
+typedef struct {
+  int32_t kind;               /* jepa_epi_kind */
+  const float* d_bias;        /* [N] fp32, required */
+  void* d_out;                /* [M, N] (or the remapped rows of PATCH_EMBED); bf16 for BIAS, BIAS_GELU
+                                 and QKV_ROPE in the bf16 path, fp32 otherwise */
+  /* QKV_ROPE: rows are tokens of items of rows_per_item tokens whose first `prefix` rows are
+   * not rotated; columns are [q | k | v] of n_head heads of head_dim each; d_rope is the table
+   * of jepa_op_rope_table for the item's patch grid (NULL: no rotation). */
+  const float* d_rope;
+  int32_t rows_per_item, prefix, n_head, head_dim, rope_layout;
+  /* PATCH_EMBED: input row m is patch i = m % patches_per_item of item b = m / patches_per_item. */
+  int32_t patches_per_item;
+  const float* d_pos;         /* [rows_per_item, N] learned table (rows = [prefix; patches]) or NULL */
+  const float* d_vec;         /* [N] vector added to every patch row (modality) or NULL */
+} jepa_epilogue;
+
+/* out = epilogue(x w^T): d_x [M, K], d_w [N, K] (PyTorch Linear layout), both fp32 (dtype
+ * JEPA_FP32, SIMT kernel) or both bf16 (JEPA_BF16, tcgen05 kernel: K % 64 == 0, N % 64 == 0,
+ * 16-byte aligned operands). */
+jepa_status jepa_op_linear(int32_t dtype, const void* d_x, int32_t M, int32_t K, const void* d_w, int32_t N,
+                           const jepa_epilogue* epi, void* stream);
+
+/* 3-D RoPE cos/sin table of one item's patch grid ("Architecture", 3-D RoPE):
+ * d_table float [Np, 3, d/2, 2] with (cos, sin) of pos_axis * theta^(-2k/d), d = 2*((hd/3)/2),
+ * positions (t, h, w) of patch i (h, w rescaled for rope_interpolate). */
+jepa_status jepa_op_rope_table(const jepa_hparams* hp, int32_t T, int32_t H, int32_t W, float* d_table,
+                               void* stream);
+
+/* Softmax attention per (item, head): o = softmax(q k^T / sqrt(head_dim) + mask) v.
+ * d_qkv: [B*N, 3*n_head*head_dim] ([q | k | v] columns, heads contiguous), d_out: [B*N, n_head*head_dim];
+ * fp32 (dtype JEPA_FP32) or bf16 (JEPA_BF16: tcgen05 flash kernel); head_dim 64.
+ * attn_mode JEPA_ATTN_BLOCK_CAUSAL: the first `prefix` rows see every key, prefix columns are
+ * closed to the other rows, and patch key j is visible to patch query i iff
+ * (i - prefix) / frame_tokens >= (j - prefix) / frame_tokens. */
+jepa_status jepa_op_attention(int32_t dtype, const void* d_qkv, int32_t B, int32_t N, int32_t n_head,
+                              int32_t head_dim, int32_t attn_mode, int32_t prefix, int32_t frame_tokens,
+                              void* d_out, void* stream);
+
+/* Device-side error word of the stage entry points: JEPA_OK, or JEPA_E_TIMEOUT if a bounded wait
+ * gave up since the last call (the word is cleared). Synchronises the device. */
+jepa_status jepa_device_status(void);
+
+/* Runs one kernel whose mbarrier wait can never complete, with a wait limit of `limit_us`
+ * microseconds, and returns what the host then reads (JEPA_E_TIMEOUT when the limit works).
+ * Exercises the failure path of every bounded wait without faulting or hanging the GPU. */
+jepa_status jepa_debug_wait_timeout(int32_t limit_us);
+
+/* Thread-local text of the last failure of this thread, and its reset. */
+const char* jepa_error_text(void);
+void jepa_error_reset(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* JEPA_H */

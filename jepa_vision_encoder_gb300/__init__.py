@@ -1,0 +1,268 @@
+"""GB300 (sm_103a) forward pass of the shared ViT encoder of the JEPA family.
+
+A thin Python layer over the C ABI of include/jepa.h (libjepa_gb300.so): it passes torch
+tensors' device pointers and a CUDA stream; every step of the encoder runs in the library's
+CUDA kernels. Importing works without a GPU; calls that launch kernels need one.
+
+    import jepa_vision_encoder_gb300 as jv
+    model = jv.Model.preset("vjepa2_vitl16", seed=0, dtype="bf16")
+    ctx = jv.Context(model, max_batch=1, frames=16, height=256, width=256)
+    tokens = ctx.encode(pixels)          # pixels: float32 CUDA tensor [B, T, 3, H, W]
+"""
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import (ATTN_BLOCK_CAUSAL, ATTN_FULL, BF16, EPI_BIAS, EPI_BIAS_GELU, EPI_BIAS_RESIDUAL,
+                   EPI_PATCH_EMBED, EPI_QKV_ROPE, FP32, LAYOUT_CTHW, LAYOUT_TCHW, POS_LEARNED, POS_NONE,
+                   POS_ROPE3D, ROPE_INTERLEAVED, ROPE_TILED, Epilogue, HParams, JepaError, check, lib)
+
+__all__ = ["Model", "Context", "HParams", "JepaError", "preset", "hparams", "n_tokens", "ops", "lib"]
+
+PRESETS = ("hfvit_ti14", "vjepa2_vitl16", "vjepa2_1_vitl16", "levjepa_vitl16", "vjepa2_vitg16")
+
+
+def _dtype_code(dtype) -> int:
+    if dtype in (BF16, "bf16", torch.bfloat16):
+        return BF16
+    if dtype in (FP32, "fp32", "f32", torch.float32):
+        return FP32
+    raise ValueError(f"unknown dtype {dtype!r}")
+
+
+def preset(name: str) -> HParams:
+    hp = HParams()
+    check(lib().jepa_preset(name.encode(), ctypes.byref(hp)))
+    return hp
+
+
+def hparams(**kw) -> HParams:
+    hp = HParams()
+    hp.in_chans = 3
+    hp.ln_eps = 1e-6
+    hp.rope_theta = 10000.0
+    for k, v in kw.items():
+        setattr(hp, k, v)
+    return hp
+
+
+def n_tokens(hp: HParams, T: int, H: int, W: int) -> int:
+    n = ctypes.c_int32()
+    check(lib().jepa_n_tokens(ctypes.byref(hp), T, H, W, ctypes.byref(n)))
+    return n.value
+
+
+def _stream_ptr(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t: torch.Tensor):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _clip_dims(pixels: torch.Tensor, layout: int):
+    if layout == LAYOUT_TCHW:
+        return pixels.shape[0], pixels.shape[1], pixels.shape[3], pixels.shape[4]
+    return pixels.shape[0], pixels.shape[2], pixels.shape[3], pixels.shape[4]
+
+
+class Model:
+    """Synthetic-weight encoder resident on one GPU (immutable; shareable across threads)."""
+
+    def __init__(self, hp: HParams, seed: int = 0, dtype="bf16", device: int = 0):
+        self.hp = hp
+        self.seed = seed
+        self.dtype = _dtype_code(dtype)
+        self.device = device
+        h = ctypes.c_void_p()
+        check(lib().jepa_model_load(ctypes.byref(hp), seed, self.dtype, device, ctypes.byref(h)))
+        self._h = h
+
+    @classmethod
+    def preset(cls, name: str, seed: int = 0, dtype="bf16", device: int = 0, **overrides):
+        hp = preset(name)
+        for k, v in overrides.items():
+            setattr(hp, k, v)
+        return cls(hp, seed=seed, dtype=dtype, device=device)
+
+    def tensor(self, name: str, shape) -> torch.Tensor:
+        """An enc.* tensor copied to host memory as float32."""
+        n = 1
+        for s in shape:
+            n *= s
+        out = torch.empty(n, dtype=torch.float32)
+        check(lib().jepa_model_tensor(self._h, name.encode(), ctypes.c_void_p(out.data_ptr()), n))
+        return out.reshape(shape)
+
+    def n_tokens(self, T, H, W) -> int:
+        return n_tokens(self.hp, T, H, W)
+
+    def close(self):
+        if getattr(self, "_h", None):
+            lib().jepa_model_free(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class Context:
+    """Workspace for clips up to (max_batch, frames, height, width); one thread at a time.
+
+    Kernels run on `stream` if one is given (the caller orders its own work around it), else
+    on a side stream the context owns: encode() then waits for torch's current stream before
+    launching and makes the current stream wait for the encode, so torch code before and after
+    is ordered with it (and CUDA-graph capture never touches the legacy default stream).
+    """
+
+    def __init__(self, model: Model, max_batch: int, frames: int, height: int, width: int,
+                 max_workspace_bytes: int = 0, stream=None, graph: bool = False):
+        self.model = model
+        h = ctypes.c_void_p()
+        check(lib().jepa_context_new(model._h, max_batch, frames, height, width, max_workspace_bytes,
+                                     ctypes.byref(h)))
+        self._h = h
+        self._own = stream is None
+        self.stream = torch.cuda.Stream(device=model.device) if stream is None else stream
+        check(lib().jepa_context_set_stream(self._h, ctypes.c_void_p(self.stream.cuda_stream)))
+        if graph:
+            check(lib().jepa_context_set_graph(self._h, 1))
+
+    def _enter(self):
+        if self._own:
+            self.stream.wait_stream(torch.cuda.current_stream(self.stream.device))
+
+    def _leave(self):
+        if self._own:
+            torch.cuda.current_stream(self.stream.device).wait_stream(self.stream)
+
+    def set_graph(self, enable: bool):
+        check(lib().jepa_context_set_graph(self._h, int(enable)))
+
+    @property
+    def workspace_bytes(self) -> int:
+        n = ctypes.c_size_t()
+        check(lib().jepa_context_workspace_bytes(self._h, ctypes.byref(n)))
+        return n.value
+
+    def launches(self, B, T, H, W) -> int:
+        n = ctypes.c_int32()
+        check(lib().jepa_context_launches(self._h, B, T, H, W, ctypes.byref(n)))
+        return n.value
+
+    def encode(self, pixels: torch.Tensor, out: torch.Tensor = None, layout: int = LAYOUT_TCHW) -> torch.Tensor:
+        """pixels: contiguous float32 CUDA tensor [B,T,C,H,W] (layout 0) or [B,C,T,H,W] (layout 1)."""
+        assert pixels.is_cuda and pixels.dtype == torch.float32 and pixels.is_contiguous()
+        B, T, H, W = _clip_dims(pixels, layout)
+        N = self.model.n_tokens(T, H, W)
+        if out is None:
+            out = torch.empty((B, N, self.model.hp.embed_dim), dtype=torch.float32, device=pixels.device)
+        self._enter()
+        check(lib().jepa_encode(self._h, _ptr(pixels), B, T, H, W, layout, _ptr(out)))
+        self._leave()
+        return out
+
+    def encode_host(self, pixels: torch.Tensor, out: torch.Tensor = None, layout: int = LAYOUT_TCHW) -> torch.Tensor:
+        """Host (CPU, ideally pinned) float32 pixels in, host tokens out; synchronous."""
+        assert not pixels.is_cuda and pixels.dtype == torch.float32 and pixels.is_contiguous()
+        B, T, H, W = _clip_dims(pixels, layout)
+        N = self.model.n_tokens(T, H, W)
+        if out is None:
+            out = torch.empty((B, N, self.model.hp.embed_dim), dtype=torch.float32)
+        check(lib().jepa_encode_host(self._h, _ptr(pixels), B, T, H, W, layout, _ptr(out)))
+        return out
+
+    def sync(self):
+        check(lib().jepa_context_sync(self._h))
+
+    def close(self):
+        if getattr(self, "_h", None):
+            lib().jepa_context_free(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class ops:
+    """The encoder's kernels one at a time (same kernels the encode path launches)."""
+
+    @staticmethod
+    def patchify(pixels: torch.Tensor, tubelet: int, patch: int, layout: int = LAYOUT_TCHW, dtype="bf16"):
+        if layout == LAYOUT_TCHW:
+            B, T, C, H, W = pixels.shape
+        else:
+            B, C, T, H, W = pixels.shape
+        rows = B * (T // tubelet) * (H // patch) * (W // patch)
+        K = C * tubelet * patch * patch
+        code = _dtype_code(dtype)
+        out = torch.empty((rows, K), dtype=torch.bfloat16 if code == BF16 else torch.float32, device=pixels.device)
+        check(lib().jepa_op_patchify(_ptr(pixels), B, T, C, H, W, tubelet, patch, layout, code, _ptr(out),
+                                     _stream_ptr()))
+        return out
+
+    @staticmethod
+    def layernorm(x: torch.Tensor, gamma, beta, eps: float, dtype="fp32"):
+        M, D = x.shape
+        code = _dtype_code(dtype)
+        y = torch.empty((M, D), dtype=torch.bfloat16 if code == BF16 else torch.float32, device=x.device)
+        check(lib().jepa_op_layernorm(_ptr(x), M, D, _ptr(gamma), _ptr(beta), eps, code, _ptr(y), _stream_ptr()))
+        return y
+
+    @staticmethod
+    def linear(x: torch.Tensor, w: torch.Tensor, bias: torch.Tensor, out: torch.Tensor, kind: int = EPI_BIAS,
+               rope: torch.Tensor = None, rows_per_item: int = 1, prefix: int = 0, n_head: int = 0,
+               head_dim: int = 0, rope_layout: int = 0, patches_per_item: int = 1, pos: torch.Tensor = None,
+               vec: torch.Tensor = None):
+        M, K = x.shape
+        N = w.shape[0]
+        code = BF16 if x.dtype == torch.bfloat16 else FP32
+        e = Epilogue()
+        e.kind = kind
+        e.d_bias = bias.data_ptr()
+        e.d_out = out.data_ptr()
+        e.d_rope = rope.data_ptr() if rope is not None else None
+        e.rows_per_item = rows_per_item
+        e.prefix = prefix
+        e.n_head = n_head
+        e.head_dim = head_dim
+        e.rope_layout = rope_layout
+        e.patches_per_item = patches_per_item
+        e.d_pos = pos.data_ptr() if pos is not None else None
+        e.d_vec = vec.data_ptr() if vec is not None else None
+        check(lib().jepa_op_linear(code, _ptr(x), M, K, _ptr(w), N, ctypes.byref(e), _stream_ptr()))
+        return out
+
+    @staticmethod
+    def rope_table(hp: HParams, T: int, H: int, W: int, device="cuda"):
+        hd = hp.embed_dim // hp.n_head
+        d = 2 * ((hd // 3) // 2)
+        gt, gh, gw = T // hp.tubelet_size, H // hp.patch_size, W // hp.patch_size
+        table = torch.empty((gt * gh * gw, 3, d // 2, 2), dtype=torch.float32, device=device)
+        check(lib().jepa_op_rope_table(ctypes.byref(hp), T, H, W, _ptr(table), _stream_ptr()))
+        return table
+
+    @staticmethod
+    def attention(qkv: torch.Tensor, B: int, N: int, n_head: int, head_dim: int = 64, attn_mode: int = ATTN_FULL,
+                  prefix: int = 0, frame_tokens: int = 1):
+        code = BF16 if qkv.dtype == torch.bfloat16 else FP32
+        out = torch.empty((B * N, n_head * head_dim), dtype=qkv.dtype, device=qkv.device)
+        check(lib().jepa_op_attention(code, _ptr(qkv), B, N, n_head, head_dim, attn_mode, prefix, frame_tokens,
+                                      _ptr(out), _stream_ptr()))
+        return out
+
+    @staticmethod
+    def device_status():
+        return lib().jepa_device_status()
+
+    @staticmethod
+    def wait_timeout_probe(limit_us: int) -> int:
+        return lib().jepa_debug_wait_timeout(limit_us)

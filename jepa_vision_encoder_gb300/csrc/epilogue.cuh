@@ -1,0 +1,139 @@
+// epilogue.cuh -- what a GEMM does with a row fragment of its fp32 accumulator: the fused
+// bias / GELU(erf) / residual / 3-D RoPE / patch-embedding row remap of the encoder.
+//
+// A fragment is E consecutive columns n0 .. n0+E-1 (n0 even, E even) of output row m, held
+// by one thread. Both the tcgen05 GEMM (E = 32 from one TMEM load) and the fp32 SIMT GEMM
+// (E = 4) call epi_fragment, so the two precisions share one definition of each epilogue.
+#pragma once
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace jepa {
+
+enum EpiKind : int { kEpiBias = 0, kEpiGelu = 1, kEpiResidual = 2, kEpiQkvRope = 3, kEpiPatch = 4 };
+
+struct EpiArgs {
+  int kind;
+  int M, N;
+  const float* bias;      // [N]
+  void* out;              // bf16 or fp32, leading dimension N (PATCH: D = N, remapped rows)
+  // 3-D RoPE ("Architecture", 3-D RoPE): rows are tokens of items of rows_per_item tokens,
+  // the first `prefix` of which are not rotated; q columns [0, D), k columns [D, 2D).
+  const float2* rope;     // [Np, 3, dh] (cos, sin) of the item's patch grid
+  int rows_per_item, prefix, n_head, head_dim, rope_layout, rope_d;
+  // patch embedding: input row m = patch i of item b (i = m % patches_per_item)
+  int patches_per_item;
+  const float* pos;       // [rows_per_item, N] or null
+  const float* vec;       // [N] or null
+};
+
+__device__ __forceinline__ float gelu_erf(float x) { return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f)); }
+
+// OUT_BF16 selects bf16 storage of BIAS / GELU / QKV_ROPE (the bf16 path); RESIDUAL and PATCH
+// always store fp32 (the residual stream).
+template <int E, bool OUT_BF16>
+__device__ __forceinline__ void epi_fragment(const EpiArgs& a, int m, int n0, float (&v)[E]) {
+  if (m >= a.M) return;
+#pragma unroll
+  for (int e = 0; e < E; ++e) v[e] += (n0 + e < a.N) ? __ldg(a.bias + n0 + e) : 0.0f;
+
+  if (a.kind == kEpiGelu) {
+#pragma unroll
+    for (int e = 0; e < E; ++e) v[e] = gelu_erf(v[e]);
+  } else if (a.kind == kEpiQkvRope && a.rope != nullptr) {
+    const int D = a.n_head * a.head_dim;
+    const int p = m % a.rows_per_item;
+    if (p >= a.prefix) {
+      const int i = p - a.prefix;
+      const int d = a.rope_d, dh = d >> 1;
+      const float2* row = a.rope + (size_t)i * 3 * dh;
+      float r[E];
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const int n = n0 + e;
+        r[e] = v[e];
+        if (n < 2 * D) {
+          const int j = (n % D) % a.head_dim;  // dim inside the head
+          if (j < 3 * d) {
+            const int axis = j / d, jj = j - axis * d;
+            const int k = (a.rope_layout == 0) ? (jj % dh) : (jj >> 1);
+            const float2 cs = __ldg(row + axis * dh + k);
+            // x cos + rot90(x) sin, rot90(y1, y2) = (-y2, y1) on (even, odd) pairs
+            const float partner = v[e ^ 1];
+            r[e] = (jj & 1) ? fmaf(v[e], cs.x, partner * cs.y) : fmaf(v[e], cs.x, -partner * cs.y);
+          }
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < E; ++e) v[e] = r[e];
+    }
+  }
+
+  if (a.kind == kEpiResidual) {
+    float* out = reinterpret_cast<float*>(a.out) + (size_t)m * a.N + n0;
+    if (n0 + E <= a.N && (E % 4) == 0) {
+#pragma unroll
+      for (int e = 0; e < E; e += 4) {
+        float4 x = *reinterpret_cast<float4*>(out + e);
+        x.x += v[e];
+        x.y += v[e + 1];
+        x.z += v[e + 2];
+        x.w += v[e + 3];
+        *reinterpret_cast<float4*>(out + e) = x;
+      }
+    } else {
+      for (int e = 0; e < E && n0 + e < a.N; ++e) out[e] += v[e];
+    }
+    return;
+  }
+  if (a.kind == kEpiPatch) {
+    const int b = m / a.patches_per_item, i = m % a.patches_per_item;
+    const int row = a.prefix + i;
+    float* out = reinterpret_cast<float*>(a.out) + ((size_t)b * a.rows_per_item + row) * a.N + n0;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      if (n0 + e < a.N) {
+        float x = v[e];
+        if (a.pos) x += __ldg(a.pos + (size_t)row * a.N + n0 + e);
+        if (a.vec) x += __ldg(a.vec + n0 + e);
+        v[e] = x;
+      }
+    }
+    if (n0 + E <= a.N && (E % 4) == 0) {
+#pragma unroll
+      for (int e = 0; e < E; e += 4) *reinterpret_cast<float4*>(out + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+    } else {
+      for (int e = 0; e < E && n0 + e < a.N; ++e) out[e] = v[e];
+    }
+    return;
+  }
+  // BIAS / GELU / QKV_ROPE store
+  if (OUT_BF16) {
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out) + (size_t)m * a.N + n0;
+    if (n0 + E <= a.N && (E % 8) == 0) {
+#pragma unroll
+      for (int e = 0; e < E; e += 8) {
+        uint4 w;
+        w.x = pack_bf16x2(v[e], v[e + 1]);
+        w.y = pack_bf16x2(v[e + 2], v[e + 3]);
+        w.z = pack_bf16x2(v[e + 4], v[e + 5]);
+        w.w = pack_bf16x2(v[e + 6], v[e + 7]);
+        *reinterpret_cast<uint4*>(out + e) = w;
+      }
+    } else {
+      for (int e = 0; e < E && n0 + e < a.N; ++e) out[e] = __float2bfloat16_rn(v[e]);
+    }
+  } else {
+    float* out = reinterpret_cast<float*>(a.out) + (size_t)m * a.N + n0;
+    if (n0 + E <= a.N && (E % 4) == 0) {
+#pragma unroll
+      for (int e = 0; e < E; e += 4) *reinterpret_cast<float4*>(out + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+    } else {
+      for (int e = 0; e < E && n0 + e < a.N; ++e) out[e] = v[e];
+    }
+  }
+}
+
+}  // namespace jepa

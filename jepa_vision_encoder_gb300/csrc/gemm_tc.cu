@@ -1,0 +1,242 @@
+// gemm_tc.cu -- persistent tcgen05 GEMM for sm_103a: out = epilogue(A[M,K] B[N,K]^T), bf16
+// operands, fp32 accumulation in tensor memory. Every linear layer of the encoder runs here
+// ("Architecture", The shared ViT graph: patch embed, fused qkv, out-projection, FFN).
+//
+// Warp roles (192 threads, one CTA per SM, grid = min(tiles, SMs), tiles strided over CTAs):
+//   warp 0      TMA producer: A tile 128x64 and B tile BNx64 per stage (128-byte swizzle)
+//   warp 1      MMA issuer: 4 x tcgen05.mma (M=128, N=BN, K=16) per stage into one of two
+//               TMEM accumulators (2 x BN columns), so the epilogue of tile i overlaps the
+//               main loop of tile i+1
+//   warps 2..5  epilogue: tcgen05.ld 32 columns at a time from their TMEM lane quarter, then the
+//               fused bias / GELU / RoPE / residual / row remap of epilogue.cuh, stored from registers.
+// Every mbarrier wait is bounded (ptx.cuh); on the way out the producer drains its loads and the
+// MMA thread waits for its MMAs before TMEM is freed.
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace jepa {
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;  // one 128-byte swizzle atom of bf16 along K
+
+template <int BN>
+struct GemmCfg {
+  static constexpr int kStages = (BN == 256) ? 4 : (BN == 128 ? 6 : 8);
+  static constexpr int kABytes = kBM * kBK * 2;
+  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kTmemCols = 2 * BN;
+  static constexpr int kBarBytes = 256;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
+};
+
+template <int BN, bool OUT_BF16>
+__global__ void __launch_bounds__(192, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, EpiArgs epi,
+                   int M, int N, int K, int* err, uint64_t limit_ns) {
+  using C = GemmCfg<BN>;
+  constexpr int S = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + S * C::kABytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * C::kStageBytes);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + S;
+  uint64_t* tfull = bars + 2 * S;
+  uint64_t* tempty = bars + 2 * S + 2;
+  uint64_t* mma_done = bars + 2 * S + 4;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int num_m = (M + kBM - 1) / kBM, num_n = N / BN, num_k = K / kBK;
+  const int num_tiles = num_m * num_n;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(full + s), 1);
+      mbar_init(smem_u32(empty + s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(smem_u32(tfull + a), 1);
+      mbar_init(smem_u32(tempty + a), 4);
+    }
+    mbar_init(smem_u32(mma_done), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const WaitCtl wc{abort_flag, err, limit_ns};
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, armed = 0, armed_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        const int m0 = (tile % num_m) * kBM, n0 = (tile / num_m) * BN;
+        for (int kb = 0; kb < num_k; ++kb) {
+          if (!mbar_wait(smem_u32(empty + stage), phase ^ 1u, wc)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_u32(full + stage);
+          mbar_arrive_expect_tx(fb, C::kStageBytes);
+          tma_load_2d(smem_u32(sA + stage * C::kABytes), &tmA, fb, kb * kBK, m0);
+          tma_load_2d(smem_u32(sB + stage * C::kBBytes), &tmB, fb, kb * kBK, n0);
+          armed |= 1u << stage;
+          armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      for (int s = 0; s < S; ++s)
+        if (armed & (1u << s)) mbar_drain(smem_u32(full + s), (armed_phase >> s) & 1u, limit_ns, err);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN, 0, 0);
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        if (!mbar_wait(smem_u32(tempty + acc), acc_phase ^ 1u, wc)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < num_k; ++kb) {
+          if (!mbar_wait(smem_u32(full + stage), phase, wc)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA + stage * C::kABytes), b0 = smem_u32(sB + stage * C::kBBytes);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            const uint64_t ad = smem_desc_sw128(a0 + k * 32, 1024, 1024);
+            const uint64_t bd = smem_desc_sw128(b0 + k * 32, 1024, 1024);
+            mma_ss(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+          }
+          mma_commit(smem_u32(empty + stage));
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(smem_u32(tfull + acc));
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      mma_commit(smem_u32(mma_done));
+      mbar_drain(smem_u32(mma_done), 0, limit_ns, err);
+    }
+  } else {
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      const int m0 = (tile % num_m) * kBM, n0 = (tile / num_m) * BN;
+      if (!mbar_wait(smem_u32(tfull + acc), acc_phase, wc)) break;
+      tc_fence_after();
+      const int m = m0 + q * 32 + lane;
+      const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(trow + c * 32, r);
+        tmem_ld_wait();
+        float v[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
+        epi_fragment<32, OUT_BF16>(epi, m, n0 + c * 32, v);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(tempty + acc));
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+int gemm_tc_pick_bn(int M, int N) {
+  const int sms = num_sms();
+  const int num_m = (M + kBM - 1) / kBM;
+  // The widest tile whose tiling still gives (nearly) every SM work; narrower tiles for the
+  // small-N layers at small M, where 128x256 tiles would leave most SMs idle.
+  if (N % 256 == 0 && num_m * (N / 256) >= sms) return 256;
+  if (N % 128 == 0 && num_m * (N / 128) >= sms / 2) return 128;
+  if (N % 64 == 0) return 64;
+  return N % 128 == 0 ? 128 : 256;
+}
+
+template <int BN, bool OUT_BF16>
+static cudaError_t launch_bn(const CUtensorMap& tmA, const CUtensorMap& tmB, const EpiArgs& epi, int M, int N,
+                             int K, int* err, uint64_t limit_ns, cudaStream_t s) {
+  using C = GemmCfg<BN>;
+  const int tiles = ((M + kBM - 1) / kBM) * (N / BN);
+  const int grid = tiles < num_sms() ? tiles : num_sms();
+  gemm_tc_kernel<BN, OUT_BF16><<<grid, 192, C::kSmemBytes, s>>>(tmA, tmB, epi, M, N, K, err, limit_ns);
+  return cudaGetLastError();
+}
+
+template <int BN, bool OUT_BF16>
+static cudaError_t set_smem_attr() {
+  return cudaFuncSetAttribute(gemm_tc_kernel<BN, OUT_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              GemmCfg<BN>::kSmemBytes);
+}
+
+cudaError_t gemm_tc_init_attributes() {
+  cudaError_t e = set_smem_attr<256, true>();
+  if (e == cudaSuccess) e = set_smem_attr<256, false>();
+  if (e == cudaSuccess) e = set_smem_attr<128, true>();
+  if (e == cudaSuccess) e = set_smem_attr<128, false>();
+  if (e == cudaSuccess) e = set_smem_attr<64, true>();
+  if (e == cudaSuccess) e = set_smem_attr<64, false>();
+  return e;
+}
+
+cudaError_t gemm_tc_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, int BN, const EpiArgs& epi, int M,
+                           int N, int K, int* err, uint64_t limit_ns, cudaStream_t s) {
+  if (M <= 0) return cudaSuccess;
+  const bool bf16_out = !(epi.kind == kEpiResidual || epi.kind == kEpiPatch);
+  switch (BN) {
+    case 256:
+      return bf16_out ? launch_bn<256, true>(tmA, tmB, epi, M, N, K, err, limit_ns, s)
+                      : launch_bn<256, false>(tmA, tmB, epi, M, N, K, err, limit_ns, s);
+    case 128:
+      return bf16_out ? launch_bn<128, true>(tmA, tmB, epi, M, N, K, err, limit_ns, s)
+                      : launch_bn<128, false>(tmA, tmB, epi, M, N, K, err, limit_ns, s);
+    case 64:
+      return bf16_out ? launch_bn<64, true>(tmA, tmB, epi, M, N, K, err, limit_ns, s)
+                      : launch_bn<64, false>(tmA, tmB, epi, M, N, K, err, limit_ns, s);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace jepa

@@ -1,0 +1,57 @@
+// kernels.h -- host-side launchers of the CUDA kernels (internal to libjepa_gb300.so).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "epilogue.cuh"
+
+namespace jepa {
+
+// Encodes a 2-D bf16 tensor map (row-major [rows, cols], 128-byte swizzle, box = box_rows x 64).
+// Returns false if the driver refuses the map.
+bool make_tmap_2d_bf16(CUtensorMap* tm, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows);
+// 3-D map of a [B][N][cols] bf16 array with box 64 x box_rows x 1 (attention Q/K/V tiles).
+bool make_tmap_3d_bf16(CUtensorMap* tm, const void* ptr, uint64_t B, uint64_t N, uint64_t cols, uint32_t box_rows);
+
+int num_sms();
+// Sets the dynamic shared-memory limits of the tcgen05 kernels (once per process; call before
+// any stream capture).
+cudaError_t tc_kernels_init();
+uint64_t default_wait_limit_ns();
+
+// tcgen05 GEMM: out = epilogue(A[M,K] * B[N,K]^T), bf16 operands. tmA box 128x64, tmB box BNx64
+// where BN = gemm_tc_pick_bn(M, N).
+int gemm_tc_pick_bn(int M, int N);
+cudaError_t gemm_tc_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, int BN, const EpiArgs& epi, int M,
+                           int N, int K, int* err, uint64_t limit_ns, cudaStream_t s);
+
+// fp32 SIMT GEMM with the same epilogues.
+cudaError_t gemm_simt_launch(const float* A, const float* Bw, const EpiArgs& epi, int M, int N, int K,
+                             cudaStream_t s);
+
+// tcgen05 flash attention over qkv [B][N][3*H*64] bf16 (3-D tensor map, box 64 x 128).
+struct AttnParams {
+  int B, N, H, head_dim;
+  int attn_mode, prefix, frame_tokens;
+  void* out;  // [B*N, H*head_dim]
+};
+cudaError_t attention_tc_launch(const CUtensorMap& tmQKV, const AttnParams& p, int* err, uint64_t limit_ns,
+                                cudaStream_t s);
+// fp32 attention (SIMT, online softmax).
+cudaError_t attention_simt_launch(const float* qkv, const AttnParams& p, cudaStream_t s);
+
+// Element-wise / row kernels.
+cudaError_t patchify_launch(const float* pix, int B, int T, int C, int H, int W, int t, int P, int layout,
+                            bool out_bf16, void* out, cudaStream_t s);
+cudaError_t layernorm_launch(const float* x, int M, int D, const float* g, const float* b, float eps,
+                             bool out_bf16, void* y, cudaStream_t s);
+cudaError_t rope_table_launch(int gt, int gh, int gw, int head_dim, float theta, int interpolate, int ref_grid,
+                              float2* table, cudaStream_t s);
+// X rows b*N + r for r < prefix: cls (+ pos[r]) (+ vec).
+cudaError_t prefix_rows_launch(float* X, int B, int N, int D, const float* cls, const float* pos,
+                               const float* vec, cudaStream_t s);
+// A kernel whose wait can never complete (failure-path check of the bounded waits).
+cudaError_t wait_timeout_probe_launch(int* err, uint64_t limit_ns, cudaStream_t s);
+
+}  // namespace jepa

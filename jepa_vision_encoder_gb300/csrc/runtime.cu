@@ -1,0 +1,904 @@
+// runtime.cu -- the C ABI of include/jepa.h: hyper-parameter validation, synthetic model
+// load (enc.* tensors of the GGUF schema, uploaded once), the context workspace, and the
+// launch sequence of one encode ("Architecture", The shared ViT graph):
+//
+//   patchify -> patch GEMM (+bias, +pos / modality, CLS row offset) [-> CLS prefix rows]
+//   per layer: LN1 -> QKV GEMM (+bias, 3-D RoPE on q/k) -> attention -> out GEMM (+bias, +=X)
+//              LN2 -> FFN-up GEMM (+bias, GELU) -> FFN-down GEMM (+bias, +=X)
+//   final LN -> tokens (fp32)
+//
+// bf16 models run the tcgen05 GEMM and flash-attention kernels; fp32 models the SIMT ones.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <thread>
+#include <vector>
+
+#include "jepa.h"
+#include "jepa_synth.h"
+#include "kernels.h"
+
+using namespace jepa;
+
+// ------------------------------------------------------------------ errors
+namespace {
+thread_local std::string t_err;
+
+jepa_status fail(jepa_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  t_err = buf;
+  return s;
+}
+
+#define CUDA_TRY(expr)                                                                         \
+  do {                                                                                         \
+    cudaError_t e_ = (expr);                                                                   \
+    if (e_ != cudaSuccess)                                                                     \
+      return fail(e_ == cudaErrorMemoryAllocation ? JEPA_E_OOM : JEPA_E_CUDA, "%s: %s (%s:%d)", \
+                  #expr, cudaGetErrorString(e_), __FILE__, __LINE__);                         \
+  } while (0)
+
+constexpr size_t kDefaultBudget = 8ull << 30;  // 8 GiB, the default arena ceiling of the pages
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int rope_d(int head_dim) { return 2 * ((head_dim / 3) / 2); }
+
+}  // namespace
+
+extern "C" const char* jepa_error_text(void) { return t_err.c_str(); }
+extern "C" void jepa_error_reset(void) { t_err.clear(); }
+
+// ------------------------------------------------------------------ hyper-parameters
+extern "C" jepa_status jepa_preset(const char* name, jepa_hparams* out) {
+  if (!name || !out) return fail(JEPA_E_INVALID_ARG, "jepa_preset: null argument");
+  jepa_hparams h;
+  memset(&h, 0, sizeof h);
+  h.in_chans = 3;
+  h.ln_eps = 1e-6f;
+  h.rope_theta = 10000.0f;
+  const std::string n(name);
+  if (n == "hfvit_ti14") {
+    h.embed_dim = 192; h.n_layer = 12; h.n_head = 3; h.ffn_dim = 768;
+    h.patch_size = 14; h.tubelet_size = 1; h.img_size = 224; h.n_frames = 1;
+    h.pos_type = JEPA_POS_LEARNED; h.cls_token = 1; h.n_pos_rows = 257;
+  } else if (n == "vjepa2_vitl16") {
+    h.embed_dim = 1024; h.n_layer = 24; h.n_head = 16; h.ffn_dim = 4096;
+    h.patch_size = 16; h.tubelet_size = 2; h.img_size = 256; h.n_frames = 16;
+    h.pos_type = JEPA_POS_ROPE3D; h.rope_layout = JEPA_ROPE_TILED;
+  } else if (n == "vjepa2_1_vitl16") {
+    h.embed_dim = 1024; h.n_layer = 24; h.n_head = 16; h.ffn_dim = 4096;
+    h.patch_size = 16; h.tubelet_size = 2; h.img_size = 384; h.n_frames = 16;
+    h.pos_type = JEPA_POS_ROPE3D; h.rope_layout = JEPA_ROPE_INTERLEAVED;
+    h.rope_interpolate = 1; h.rope_ref_grid = 256 / 16; h.modality_embed = 1;
+  } else if (n == "levjepa_vitl16") {
+    h.embed_dim = 1024; h.n_layer = 24; h.n_head = 16; h.ffn_dim = 4096;
+    h.patch_size = 16; h.tubelet_size = 1; h.img_size = 256; h.n_frames = 16;
+    h.pos_type = JEPA_POS_ROPE3D; h.rope_layout = JEPA_ROPE_TILED; h.cls_token = 1;
+    h.attn_mode = JEPA_ATTN_BLOCK_CAUSAL;
+  } else if (n == "vjepa2_vitg16") {
+    h.embed_dim = 1408; h.n_layer = 40; h.n_head = 22; h.ffn_dim = 6144;
+    h.patch_size = 16; h.tubelet_size = 2; h.img_size = 256; h.n_frames = 64;
+    h.pos_type = JEPA_POS_ROPE3D; h.rope_layout = JEPA_ROPE_TILED;
+  } else {
+    return fail(JEPA_E_INVALID_ARG, "jepa_preset: unknown preset '%s'", name);
+  }
+  *out = h;
+  return JEPA_OK;
+}
+
+extern "C" jepa_status jepa_hparams_validate(const jepa_hparams* hp) {
+  if (!hp) return fail(JEPA_E_INVALID_ARG, "hparams: null");
+  auto in = [](int v, int lo, int hi) { return v >= lo && v <= hi; };
+  if (!in(hp->embed_dim, 1, 65536)) return fail(JEPA_E_INVALID_ARG, "embed_dim %d outside [1, 65536]", hp->embed_dim);
+  if (!in(hp->n_layer, 1, 1024)) return fail(JEPA_E_INVALID_ARG, "n_layer %d outside [1, 1024]", hp->n_layer);
+  if (!in(hp->n_head, 1, 1024)) return fail(JEPA_E_INVALID_ARG, "n_head %d outside [1, 1024]", hp->n_head);
+  if (!in(hp->ffn_dim, 1, 1 << 20)) return fail(JEPA_E_INVALID_ARG, "ffn_dim %d outside [1, 2^20]", hp->ffn_dim);
+  if (!in(hp->patch_size, 1, 1024)) return fail(JEPA_E_INVALID_ARG, "patch_size %d outside [1, 1024]", hp->patch_size);
+  if (!in(hp->tubelet_size, 1, 1024)) return fail(JEPA_E_INVALID_ARG, "tubelet_size %d outside [1, 1024]", hp->tubelet_size);
+  if (!in(hp->in_chans, 1, 1024)) return fail(JEPA_E_INVALID_ARG, "in_chans %d outside [1, 1024]", hp->in_chans);
+  if (hp->img_size != 0 && !in(hp->img_size, 1, 65536)) return fail(JEPA_E_INVALID_ARG, "img_size %d outside [1, 65536]", hp->img_size);
+  if (hp->n_frames != 0 && !in(hp->n_frames, 1, 65536)) return fail(JEPA_E_INVALID_ARG, "n_frames %d outside [1, 65536]", hp->n_frames);
+  if (!std::isfinite(hp->ln_eps) || hp->ln_eps < 0.0f || hp->ln_eps > 1.0f)
+    return fail(JEPA_E_INVALID_ARG, "ln_eps %g not finite in [0, 1]", (double)hp->ln_eps);
+  if (!in(hp->pos_type, 0, 2)) return fail(JEPA_E_INVALID_ARG, "pos_type %d unknown", hp->pos_type);
+  if (!in(hp->rope_layout, 0, 1)) return fail(JEPA_E_INVALID_ARG, "rope_layout %d unknown", hp->rope_layout);
+  if (!in(hp->attn_mode, 0, 1)) return fail(JEPA_E_INVALID_ARG, "attn_mode %d unknown", hp->attn_mode);
+  if (hp->embed_dim % hp->n_head) return fail(JEPA_E_INVALID_ARG, "embed_dim %d not divisible by n_head %d", hp->embed_dim, hp->n_head);
+  const int hd = hp->embed_dim / hp->n_head;
+  if (hp->pos_type == JEPA_POS_ROPE3D) {
+    if (!std::isfinite(hp->rope_theta) || hp->rope_theta <= 0.0f)
+      return fail(JEPA_E_INVALID_ARG, "rope_theta %g must be finite and > 0", (double)hp->rope_theta);
+    if (hd % 2) return fail(JEPA_E_INVALID_ARG, "odd head width %d on a 3-D RoPE model (it rotates pairs)", hd);
+    if (hp->rope_interpolate && hp->rope_ref_grid < 1)
+      return fail(JEPA_E_INVALID_ARG, "rope_interpolate without a rope_ref_grid to rescale from");
+  }
+  if (hp->pos_type == JEPA_POS_LEARNED && !in(hp->n_pos_rows, 1, 1 << 22))
+    return fail(JEPA_E_INVALID_ARG, "learned position table needs n_pos_rows in [1, 2^22] (got %d)", hp->n_pos_rows);
+  return JEPA_OK;
+}
+
+namespace {
+struct Geo {
+  int gt, gh, gw, Np, prefix, N, K;
+};
+jepa_status geometry(const jepa_hparams* hp, int T, int H, int W, Geo* g) {
+  if (T <= 0 || H <= 0 || W <= 0) return fail(JEPA_E_INVALID_ARG, "clip size %dx%dx%d must be positive", T, H, W);
+  if (T % hp->tubelet_size || H % hp->patch_size || W % hp->patch_size)
+    return fail(JEPA_E_INVALID_ARG, "clip %dx%dx%d not divisible by tubelet %d / patch %d", T, H, W,
+                hp->tubelet_size, hp->patch_size);
+  g->gt = T / hp->tubelet_size;
+  g->gh = H / hp->patch_size;
+  g->gw = W / hp->patch_size;
+  const long long np = (long long)g->gt * g->gh * g->gw;
+  if (np + 1 > (1ll << 22)) return fail(JEPA_E_INVALID_ARG, "token count %lld above 2^22", np);
+  g->Np = (int)np;
+  g->prefix = hp->cls_token ? 1 : 0;
+  g->N = g->Np + g->prefix;
+  g->K = hp->in_chans * hp->tubelet_size * hp->patch_size * hp->patch_size;
+  return JEPA_OK;
+}
+}  // namespace
+
+extern "C" jepa_status jepa_n_tokens(const jepa_hparams* hp, int32_t T, int32_t H, int32_t W, int32_t* n_out) {
+  if (!hp || !n_out) return fail(JEPA_E_INVALID_ARG, "jepa_n_tokens: null argument");
+  jepa_status s = jepa_hparams_validate(hp);
+  if (s != JEPA_OK) return s;
+  Geo g;
+  s = geometry(hp, T, H, W, &g);
+  if (s != JEPA_OK) return s;
+  *n_out = g.N;
+  return JEPA_OK;
+}
+
+// ------------------------------------------------------------------ model
+namespace {
+struct TensorRec {
+  std::string name;
+  size_t offset;  // in the arena
+  size_t n;
+  bool bf16;
+};
+struct LayerW {
+  const float *ln1_w, *ln1_b, *b_qkv, *b_out, *ln2_w, *ln2_b, *b_up, *b_down;
+  const void *w_qkv, *w_out, *w_up, *w_down;
+  CUtensorMap tm_qkv[3], tm_out[3], tm_up[3], tm_down[3];  // box rows 64 / 128 / 256
+};
+int bn_slot(int bn) { return bn == 64 ? 0 : (bn == 128 ? 1 : 2); }
+}  // namespace
+
+struct jepa_model {
+  jepa_hparams hp;
+  int dtype = 0, device = 0;
+  uint64_t seed = 0;
+  uint8_t* arena = nullptr;
+  size_t arena_bytes = 0;
+  std::vector<TensorRec> tensors;
+  const void* w_patch = nullptr;
+  const float *b_patch = nullptr, *pos = nullptr, *cls = nullptr, *mod = nullptr, *norm_w = nullptr, *norm_b = nullptr;
+  std::vector<LayerW> layers;
+  CUtensorMap tm_patch[3];
+  int K = 0;
+  const TensorRec* find(const char* name) const {
+    for (const auto& t : tensors)
+      if (t.name == name) return &t;
+    return nullptr;
+  }
+};
+
+namespace {
+// Fill `n` values of tensor `name` (the synth recipe) using all host cores.
+void synth_parallel(uint64_t seed, const std::string& name, int bf16_matrices, size_t n, float* dst) {
+  int kind, is_matrix;
+  double a, b;
+  jsynth_param_init(name.c_str(), &kind, &a, &b, &is_matrix);
+  const int round = (bf16_matrices && is_matrix) ? 1 : 0;
+  unsigned nt = std::max(1u, std::thread::hardware_concurrency());
+  if (n < 65536) nt = 1;
+  std::vector<std::thread> th;
+  const size_t per = (n + nt - 1) / nt;
+  for (unsigned t = 0; t < nt; ++t) {
+    const size_t first = (size_t)t * per;
+    if (first >= n) break;
+    const size_t len = std::min(per, n - first);
+    th.emplace_back([=] { jsynth_fill(seed, name.c_str(), kind, a, b, round, first, len, dst + first); });
+  }
+  for (auto& x : th) x.join();
+}
+}  // namespace
+
+extern "C" jepa_status jepa_model_load(const jepa_hparams* hp, uint64_t seed, int32_t dtype, int32_t device,
+                                       jepa_model** out) {
+  if (!hp || !out) return fail(JEPA_E_INVALID_ARG, "jepa_model_load: null argument");
+  *out = nullptr;
+  jepa_status st = jepa_hparams_validate(hp);
+  if (st != JEPA_OK) return st;
+  if (dtype != JEPA_FP32 && dtype != JEPA_BF16) return fail(JEPA_E_INVALID_ARG, "dtype %d unknown", dtype);
+  const int D = hp->embed_dim, F = hp->ffn_dim, L = hp->n_layer;
+  const int hd = D / hp->n_head;
+  const int K = hp->in_chans * hp->tubelet_size * hp->patch_size * hp->patch_size;
+  if (hd != 64) return fail(JEPA_E_UNSUPPORTED, "head_dim %d: the attention kernels are built for 64", hd);
+  if (D % 4 || D > 2048) return fail(JEPA_E_UNSUPPORTED, "embed_dim %d: LayerNorm needs a multiple of 4 up to 2048", D);
+  if (F % 4) return fail(JEPA_E_UNSUPPORTED, "ffn_dim %d must be a multiple of 4", F);
+  if (dtype == JEPA_BF16 && (D % 64 || F % 64 || K % 64))
+    return fail(JEPA_E_UNSUPPORTED, "bf16 GEMMs need embed %d, ffn %d and patch K %d to be multiples of 64", D, F, K);
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev)
+    return fail(JEPA_E_CUDA, "CUDA device %d not available (%d devices)", device, ndev);
+  CUDA_TRY(cudaSetDevice(device));
+
+  jepa_model* m = new jepa_model();
+  m->hp = *hp;
+  m->dtype = dtype;
+  m->device = device;
+  m->seed = seed;
+  m->K = K;
+  const bool bf = dtype == JEPA_BF16;
+  // tensor table, in GGUF enc.* names and PyTorch row-major shapes
+  auto add = [&](const std::string& name, size_t n, bool matrix) {
+    TensorRec r;
+    r.name = name;
+    r.n = n;
+    r.bf16 = bf && matrix;
+    r.offset = 0;
+    m->tensors.push_back(r);
+  };
+  add("enc.patch_embed.weight", (size_t)D * K, true);
+  add("enc.patch_embed.bias", D, false);
+  if (hp->pos_type == JEPA_POS_LEARNED) add("enc.pos_embed", (size_t)hp->n_pos_rows * D, false);
+  if (hp->cls_token) add("enc.cls_token", D, false);
+  if (hp->modality_embed) add("enc.mod_embed_video", D, false);
+  for (int l = 0; l < L; ++l) {
+    const std::string p = "enc.blk." + std::to_string(l) + ".";
+    add(p + "ln1.weight", D, false);
+    add(p + "ln1.bias", D, false);
+    add(p + "attn_qkv.weight", (size_t)3 * D * D, true);
+    add(p + "attn_qkv.bias", (size_t)3 * D, false);
+    add(p + "attn_out.weight", (size_t)D * D, true);
+    add(p + "attn_out.bias", D, false);
+    add(p + "ln2.weight", D, false);
+    add(p + "ln2.bias", D, false);
+    add(p + "ffn_up.weight", (size_t)F * D, true);
+    add(p + "ffn_up.bias", F, false);
+    add(p + "ffn_down.weight", (size_t)D * F, true);
+    add(p + "ffn_down.bias", D, false);
+  }
+  add("enc.norm.weight", D, false);
+  add("enc.norm.bias", D, false);
+  size_t off = 0, largest = 0;
+  for (auto& t : m->tensors) {
+    t.offset = off;
+    off = align256(off + t.n * (t.bf16 ? 2 : 4));
+    largest = std::max(largest, t.n);
+  }
+  m->arena_bytes = off;
+  cudaError_t e = cudaMalloc(&m->arena, off);
+  if (e != cudaSuccess) {
+    delete m;
+    return fail(JEPA_E_OOM, "weights: cudaMalloc(%zu bytes) failed: %s", off, cudaGetErrorString(e));
+  }
+  std::vector<float> host(largest);
+  std::vector<uint16_t> hbits;
+  for (const auto& t : m->tensors) {
+    synth_parallel(seed, t.name, bf ? 1 : 0, t.n, host.data());
+    if (t.bf16) {
+      hbits.resize(t.n);
+      for (size_t i = 0; i < t.n; ++i) hbits[i] = jsynth_f32_to_bf16_bits(host[i]);
+      e = cudaMemcpy(m->arena + t.offset, hbits.data(), t.n * 2, cudaMemcpyHostToDevice);
+    } else {
+      e = cudaMemcpy(m->arena + t.offset, host.data(), t.n * 4, cudaMemcpyHostToDevice);
+    }
+    if (e != cudaSuccess) {
+      jepa_model_free(m);
+      return fail(JEPA_E_CUDA, "weights upload: %s", cudaGetErrorString(e));
+    }
+  }
+  auto ptr = [&](const std::string& name) -> void* { return m->arena + m->find(name.c_str())->offset; };
+  auto fptr = [&](const std::string& name) -> const float* { return reinterpret_cast<const float*>(ptr(name)); };
+  m->w_patch = ptr("enc.patch_embed.weight");
+  m->b_patch = fptr("enc.patch_embed.bias");
+  if (hp->pos_type == JEPA_POS_LEARNED) m->pos = fptr("enc.pos_embed");
+  if (hp->cls_token) m->cls = fptr("enc.cls_token");
+  if (hp->modality_embed) m->mod = fptr("enc.mod_embed_video");
+  m->norm_w = fptr("enc.norm.weight");
+  m->norm_b = fptr("enc.norm.bias");
+  m->layers.resize(L);
+  bool maps_ok = true;
+  const uint32_t boxes[3] = {64, 128, 256};
+  for (int s = 0; s < 3 && bf; ++s) maps_ok &= make_tmap_2d_bf16(&m->tm_patch[s], m->w_patch, D, K, boxes[s]);
+  for (int l = 0; l < L; ++l) {
+    const std::string p = "enc.blk." + std::to_string(l) + ".";
+    LayerW& w = m->layers[l];
+    w.ln1_w = fptr(p + "ln1.weight");
+    w.ln1_b = fptr(p + "ln1.bias");
+    w.w_qkv = ptr(p + "attn_qkv.weight");
+    w.b_qkv = fptr(p + "attn_qkv.bias");
+    w.w_out = ptr(p + "attn_out.weight");
+    w.b_out = fptr(p + "attn_out.bias");
+    w.ln2_w = fptr(p + "ln2.weight");
+    w.ln2_b = fptr(p + "ln2.bias");
+    w.w_up = ptr(p + "ffn_up.weight");
+    w.b_up = fptr(p + "ffn_up.bias");
+    w.w_down = ptr(p + "ffn_down.weight");
+    w.b_down = fptr(p + "ffn_down.bias");
+    for (int s = 0; s < 3 && bf; ++s) {
+      maps_ok &= make_tmap_2d_bf16(&w.tm_qkv[s], w.w_qkv, 3 * D, D, boxes[s]);
+      maps_ok &= make_tmap_2d_bf16(&w.tm_out[s], w.w_out, D, D, boxes[s]);
+      maps_ok &= make_tmap_2d_bf16(&w.tm_up[s], w.w_up, F, D, boxes[s]);
+      maps_ok &= make_tmap_2d_bf16(&w.tm_down[s], w.w_down, D, F, boxes[s]);
+    }
+  }
+  if (!maps_ok) {
+    jepa_model_free(m);
+    return fail(JEPA_E_CUDA, "cuTensorMapEncodeTiled refused a weight tensor map");
+  }
+  *out = m;
+  return JEPA_OK;
+}
+
+extern "C" void jepa_model_free(jepa_model* m) {
+  if (!m) return;
+  if (m->arena) {
+    cudaSetDevice(m->device);
+    cudaFree(m->arena);
+  }
+  delete m;
+}
+
+extern "C" jepa_status jepa_model_hparams(const jepa_model* m, jepa_hparams* out) {
+  if (!m || !out) return fail(JEPA_E_INVALID_ARG, "jepa_model_hparams: null argument");
+  *out = m->hp;
+  return JEPA_OK;
+}
+
+extern "C" jepa_status jepa_model_tensor(const jepa_model* m, const char* name, float* h_dst, size_t n_elems) {
+  if (!m || !name || !h_dst) return fail(JEPA_E_INVALID_ARG, "jepa_model_tensor: null argument");
+  const TensorRec* t = m->find(name);
+  if (!t) return fail(JEPA_E_INVALID_ARG, "jepa_model_tensor: no tensor named '%s'", name);
+  if (t->n != n_elems) return fail(JEPA_E_INVALID_ARG, "tensor '%s' has %zu elements, not %zu", name, t->n, n_elems);
+  CUDA_TRY(cudaSetDevice(m->device));
+  if (t->bf16) {
+    std::vector<uint16_t> bits(t->n);
+    CUDA_TRY(cudaMemcpy(bits.data(), m->arena + t->offset, t->n * 2, cudaMemcpyDeviceToHost));
+    for (size_t i = 0; i < t->n; ++i) h_dst[i] = jsynth_bf16_bits_to_f32(bits[i]);
+  } else {
+    CUDA_TRY(cudaMemcpy(h_dst, m->arena + t->offset, t->n * 4, cudaMemcpyDeviceToHost));
+  }
+  return JEPA_OK;
+}
+
+// ------------------------------------------------------------------ context
+struct jepa_context {
+  const jepa_model* m = nullptr;
+  cudaStream_t stream = nullptr;
+  bool own_stream = false;
+  int max_B = 0, max_T = 0, max_H = 0, max_W = 0;
+  long long max_rows = 0, max_prows = 0, max_np = 0, max_pix = 0;
+  uint8_t* ws = nullptr;
+  size_t ws_bytes = 0;
+  float* X = nullptr;
+  void *Xn = nullptr, *qkv = nullptr, *ao = nullptr, *Hh = nullptr, *Pm = nullptr;
+  float2* rope = nullptr;
+  float *pix_stage = nullptr, *tok_stage = nullptr;
+  int* err = nullptr;
+  // per-shape state
+  int kB = -1, kT = -1, kH = -1, kW = -1;
+  CUtensorMap tm_Pm, tm_Xn, tm_ao, tm_Hh, tm_qkv3;
+  int bn_patch = 0, bn_qkv = 0, bn_out = 0, bn_up = 0, bn_down = 0;
+  // graph replay
+  bool use_graph = false;
+  cudaGraphExec_t gexec = nullptr;
+  int gB = -1, gT = -1, gH = -1, gW = -1, glayout = -1;
+  const float* gpix = nullptr;
+  float* gtok = nullptr;
+};
+
+namespace {
+size_t ws_layout(const jepa_model* m, long long rows, long long prows, long long np, long long pix, jepa_context* c) {
+  const jepa_hparams& hp = m->hp;
+  const size_t D = hp.embed_dim, F = hp.ffn_dim, K = m->K;
+  const size_t es = m->dtype == JEPA_BF16 ? 2 : 4;
+  const int dh = rope_d(D / hp.n_head) / 2;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align256(off + bytes);
+    return o;
+  };
+  const size_t oX = take(rows * D * 4), oXn = take(rows * D * es), oQ = take(rows * 3 * D * es),
+               oA = take(rows * D * es), oH = take(rows * F * es), oP = take(prows * K * es),
+               oR = take((size_t)np * 3 * std::max(dh, 1) * sizeof(float2)), oPix = take(pix * 4),
+               oTok = take(rows * D * 4), oErr = take(sizeof(int));
+  if (c) {
+    c->X = reinterpret_cast<float*>(c->ws + oX);
+    c->Xn = c->ws + oXn;
+    c->qkv = c->ws + oQ;
+    c->ao = c->ws + oA;
+    c->Hh = c->ws + oH;
+    c->Pm = c->ws + oP;
+    c->rope = reinterpret_cast<float2*>(c->ws + oR);
+    c->pix_stage = reinterpret_cast<float*>(c->ws + oPix);
+    c->tok_stage = reinterpret_cast<float*>(c->ws + oTok);
+    c->err = reinterpret_cast<int*>(c->ws + oErr);
+  }
+  return off;
+}
+}  // namespace
+
+extern "C" jepa_status jepa_context_new(const jepa_model* m, int32_t max_batch, int32_t max_frames,
+                                        int32_t max_height, int32_t max_width, size_t max_workspace_bytes,
+                                        jepa_context** out) {
+  if (!m || !out) return fail(JEPA_E_INVALID_ARG, "jepa_context_new: null argument");
+  *out = nullptr;
+  if (max_batch <= 0) return fail(JEPA_E_INVALID_ARG, "max_batch %d must be positive", max_batch);
+  Geo g;
+  jepa_status st = geometry(&m->hp, max_frames, max_height, max_width, &g);
+  if (st != JEPA_OK) return st;
+  const long long rows = (long long)max_batch * g.N, prows = (long long)max_batch * g.Np;
+  const long long pix = (long long)max_batch * max_frames * m->hp.in_chans * max_height * max_width;
+  const size_t need = ws_layout(m, rows, prows, g.Np, pix, nullptr);
+  const size_t budget = max_workspace_bytes ? max_workspace_bytes : kDefaultBudget;
+  if (need > budget)
+    return fail(JEPA_E_BUDGET, "workspace of %zu bytes for %d x (%dx%dx%d) exceeds the budget of %zu bytes", need,
+                max_batch, max_frames, max_height, max_width, budget);
+  CUDA_TRY(cudaSetDevice(m->device));
+  if (m->dtype == JEPA_BF16) CUDA_TRY(tc_kernels_init());
+  jepa_context* c = new jepa_context();
+  c->m = m;
+  c->max_B = max_batch;
+  c->max_T = max_frames;
+  c->max_H = max_height;
+  c->max_W = max_width;
+  c->max_rows = rows;
+  c->max_prows = prows;
+  c->max_np = g.Np;
+  c->max_pix = pix;
+  cudaError_t e = cudaMalloc(&c->ws, need);
+  if (e != cudaSuccess) {
+    delete c;
+    return fail(JEPA_E_OOM, "workspace: cudaMalloc(%zu bytes) failed: %s", need, cudaGetErrorString(e));
+  }
+  c->ws_bytes = need;
+  ws_layout(m, rows, prows, g.Np, pix, c);
+  e = cudaStreamCreateWithFlags(&c->stream, cudaStreamNonBlocking);
+  if (e != cudaSuccess) {
+    cudaFree(c->ws);
+    delete c;
+    return fail(JEPA_E_CUDA, "cudaStreamCreate: %s", cudaGetErrorString(e));
+  }
+  c->own_stream = true;
+  cudaMemset(c->err, 0, sizeof(int));
+  *out = c;
+  return JEPA_OK;
+}
+
+extern "C" void jepa_context_free(jepa_context* c) {
+  if (!c) return;
+  cudaSetDevice(c->m->device);
+  if (c->stream) cudaStreamSynchronize(c->stream);
+  if (c->gexec) cudaGraphExecDestroy(c->gexec);
+  if (c->own_stream && c->stream) cudaStreamDestroy(c->stream);
+  if (c->ws) cudaFree(c->ws);
+  delete c;
+}
+
+extern "C" jepa_status jepa_context_set_stream(jepa_context* c, void* stream) {
+  if (!c) return fail(JEPA_E_INVALID_ARG, "jepa_context_set_stream: null context");
+  CUDA_TRY(cudaSetDevice(c->m->device));
+  CUDA_TRY(cudaStreamSynchronize(c->stream));
+  if (c->own_stream) cudaStreamDestroy(c->stream);
+  c->stream = reinterpret_cast<cudaStream_t>(stream);
+  c->own_stream = false;
+  if (c->gexec) {  // a graph recorded for another stream is dropped
+    cudaGraphExecDestroy(c->gexec);
+    c->gexec = nullptr;
+  }
+  return JEPA_OK;
+}
+
+extern "C" jepa_status jepa_context_set_graph(jepa_context* c, int32_t enable) {
+  if (!c) return fail(JEPA_E_INVALID_ARG, "jepa_context_set_graph: null context");
+  c->use_graph = enable != 0;
+  return JEPA_OK;
+}
+
+extern "C" jepa_status jepa_context_workspace_bytes(const jepa_context* c, size_t* out) {
+  if (!c || !out) return fail(JEPA_E_INVALID_ARG, "jepa_context_workspace_bytes: null argument");
+  *out = c->ws_bytes;
+  return JEPA_OK;
+}
+
+namespace {
+int launches_per_encode(const jepa_model* m) {
+  return 2 + (m->hp.cls_token ? 1 : 0) + 7 * m->hp.n_layer + 1;
+}
+
+jepa_status check_shape(jepa_context* c, const float* pix, int B, int T, int H, int W, int layout, const void* tok,
+                        Geo* g) {
+  if (!pix || !tok) return fail(JEPA_E_INVALID_ARG, "jepa_encode: null pixel or token pointer");
+  if (layout != JEPA_LAYOUT_TCHW && layout != JEPA_LAYOUT_CTHW) return fail(JEPA_E_INVALID_ARG, "layout %d unknown", layout);
+  if (B <= 0) return fail(JEPA_E_INVALID_ARG, "batch %d must be positive", B);
+  jepa_status st = geometry(&c->m->hp, T, H, W, g);
+  if (st != JEPA_OK) return st;
+  if (B > c->max_B || T > c->max_T || H > c->max_H || W > c->max_W || (long long)B * g->N > c->max_rows ||
+      (long long)B * g->Np > c->max_prows)
+    return fail(JEPA_E_BUDGET, "clip batch %d x %dx%dx%d exceeds the context's maximum %d x %dx%dx%d", B, T, H, W,
+                c->max_B, c->max_T, c->max_H, c->max_W);
+  if (c->m->hp.pos_type == JEPA_POS_LEARNED && g->N != c->m->hp.n_pos_rows)
+    return fail(JEPA_E_UNSUPPORTED, "learned position table has %d rows, the clip has %d tokens", c->m->hp.n_pos_rows,
+                g->N);
+  return JEPA_OK;
+}
+
+// Per-shape set-up: tensor maps over the workspace, GEMM tile widths, the RoPE table.
+jepa_status prepare_shape(jepa_context* c, int B, int T, int H, int W, const Geo& g) {
+  if (c->kB == B && c->kT == T && c->kH == H && c->kW == W) return JEPA_OK;
+  const jepa_model* m = c->m;
+  const jepa_hparams& hp = m->hp;
+  const int D = hp.embed_dim, F = hp.ffn_dim;
+  const long long M = (long long)B * g.N, Mp = (long long)B * g.Np;
+  if (m->dtype == JEPA_BF16) {
+    bool ok = true;
+    ok &= make_tmap_2d_bf16(&c->tm_Pm, c->Pm, Mp, m->K, 128);
+    ok &= make_tmap_2d_bf16(&c->tm_Xn, c->Xn, M, D, 128);
+    ok &= make_tmap_2d_bf16(&c->tm_ao, c->ao, M, D, 128);
+    ok &= make_tmap_2d_bf16(&c->tm_Hh, c->Hh, M, F, 128);
+    ok &= make_tmap_3d_bf16(&c->tm_qkv3, c->qkv, B, g.N, 3 * D, 128);
+    if (!ok) return fail(JEPA_E_CUDA, "cuTensorMapEncodeTiled refused a workspace tensor map");
+    c->bn_patch = gemm_tc_pick_bn((int)Mp, D);
+    c->bn_qkv = gemm_tc_pick_bn((int)M, 3 * D);
+    c->bn_out = gemm_tc_pick_bn((int)M, D);
+    c->bn_up = gemm_tc_pick_bn((int)M, F);
+    c->bn_down = gemm_tc_pick_bn((int)M, D);
+  }
+  if (hp.pos_type == JEPA_POS_ROPE3D) {
+    CUDA_TRY(rope_table_launch(g.gt, g.gh, g.gw, D / hp.n_head, hp.rope_theta, hp.rope_interpolate,
+                               hp.rope_ref_grid, c->rope, c->stream));
+  }
+  c->kB = B;
+  c->kT = T;
+  c->kH = H;
+  c->kW = W;
+  return JEPA_OK;
+}
+
+EpiArgs make_epi(int kind, int M, int N, const float* bias, void* out) {
+  EpiArgs e;
+  memset(&e, 0, sizeof e);
+  e.kind = kind;
+  e.M = M;
+  e.N = N;
+  e.bias = bias;
+  e.out = out;
+  e.rows_per_item = 1;
+  e.patches_per_item = 1;
+  return e;
+}
+
+// The launch sequence of one encode (no host synchronisation inside: graph-capturable).
+jepa_status launch_encode(jepa_context* c, const float* pix, int B, int T, int H, int W, int layout, float* tok,
+                          const Geo& g) {
+  const jepa_model* m = c->m;
+  const jepa_hparams& hp = m->hp;
+  const bool bf = m->dtype == JEPA_BF16;
+  const int D = hp.embed_dim, F = hp.ffn_dim, L = hp.n_layer, NH = hp.n_head, hd = D / NH;
+  const int M = B * g.N, Mp = B * g.Np;
+  cudaStream_t s = c->stream;
+  const uint64_t lim = default_wait_limit_ns();
+
+  CUDA_TRY(patchify_launch(pix, B, T, hp.in_chans, H, W, hp.tubelet_size, hp.patch_size, layout, bf, c->Pm, s));
+  EpiArgs pe = make_epi(kEpiPatch, Mp, D, m->b_patch, c->X);
+  pe.patches_per_item = g.Np;
+  pe.rows_per_item = g.N;
+  pe.prefix = g.prefix;
+  pe.pos = m->pos;
+  pe.vec = m->mod;
+  if (bf)
+    CUDA_TRY(gemm_tc_launch(c->tm_Pm, m->tm_patch[bn_slot(c->bn_patch)], c->bn_patch, pe, Mp, D, m->K, c->err, lim, s));
+  else
+    CUDA_TRY(gemm_simt_launch(reinterpret_cast<const float*>(c->Pm), reinterpret_cast<const float*>(m->w_patch), pe,
+                              Mp, D, m->K, s));
+  if (g.prefix) CUDA_TRY(prefix_rows_launch(c->X, B, g.N, D, m->cls, m->pos, m->mod, s));
+
+  AttnParams ap;
+  ap.B = B;
+  ap.N = g.N;
+  ap.H = NH;
+  ap.head_dim = hd;
+  ap.attn_mode = hp.attn_mode;
+  ap.prefix = g.prefix;
+  ap.frame_tokens = g.gh * g.gw;
+  ap.out = c->ao;
+
+  for (int l = 0; l < L; ++l) {
+    const LayerW& w = m->layers[l];
+    CUDA_TRY(layernorm_launch(c->X, M, D, w.ln1_w, w.ln1_b, hp.ln_eps, bf, c->Xn, s));
+    EpiArgs qe = make_epi(kEpiQkvRope, M, 3 * D, w.b_qkv, c->qkv);
+    qe.rows_per_item = g.N;
+    qe.prefix = g.prefix;
+    qe.n_head = NH;
+    qe.head_dim = hd;
+    qe.rope_layout = hp.rope_layout;
+    qe.rope_d = rope_d(hd);
+    qe.rope = hp.pos_type == JEPA_POS_ROPE3D ? c->rope : nullptr;
+    EpiArgs oe = make_epi(kEpiResidual, M, D, w.b_out, c->X);
+    EpiArgs ue = make_epi(kEpiGelu, M, F, w.b_up, c->Hh);
+    EpiArgs de = make_epi(kEpiResidual, M, D, w.b_down, c->X);
+    if (bf) {
+      CUDA_TRY(gemm_tc_launch(c->tm_Xn, w.tm_qkv[bn_slot(c->bn_qkv)], c->bn_qkv, qe, M, 3 * D, D, c->err, lim, s));
+      CUDA_TRY(attention_tc_launch(c->tm_qkv3, ap, c->err, lim, s));
+      CUDA_TRY(gemm_tc_launch(c->tm_ao, w.tm_out[bn_slot(c->bn_out)], c->bn_out, oe, M, D, D, c->err, lim, s));
+      CUDA_TRY(layernorm_launch(c->X, M, D, w.ln2_w, w.ln2_b, hp.ln_eps, true, c->Xn, s));
+      CUDA_TRY(gemm_tc_launch(c->tm_Xn, w.tm_up[bn_slot(c->bn_up)], c->bn_up, ue, M, F, D, c->err, lim, s));
+      CUDA_TRY(gemm_tc_launch(c->tm_Hh, w.tm_down[bn_slot(c->bn_down)], c->bn_down, de, M, D, F, c->err, lim, s));
+    } else {
+      const float* Xn = reinterpret_cast<const float*>(c->Xn);
+      CUDA_TRY(gemm_simt_launch(Xn, reinterpret_cast<const float*>(w.w_qkv), qe, M, 3 * D, D, s));
+      CUDA_TRY(attention_simt_launch(reinterpret_cast<const float*>(c->qkv), ap, s));
+      CUDA_TRY(gemm_simt_launch(reinterpret_cast<const float*>(c->ao), reinterpret_cast<const float*>(w.w_out), oe, M,
+                                D, D, s));
+      CUDA_TRY(layernorm_launch(c->X, M, D, w.ln2_w, w.ln2_b, hp.ln_eps, false, c->Xn, s));
+      CUDA_TRY(gemm_simt_launch(Xn, reinterpret_cast<const float*>(w.w_up), ue, M, F, D, s));
+      CUDA_TRY(gemm_simt_launch(reinterpret_cast<const float*>(c->Hh), reinterpret_cast<const float*>(w.w_down), de,
+                                M, D, F, s));
+    }
+  }
+  CUDA_TRY(layernorm_launch(c->X, M, D, m->norm_w, m->norm_b, hp.ln_eps, false, tok, s));
+  return JEPA_OK;
+}
+}  // namespace
+
+extern "C" jepa_status jepa_context_launches(const jepa_context* c, int32_t B, int32_t T, int32_t H, int32_t W,
+                                             int32_t* n_out) {
+  if (!c || !n_out) return fail(JEPA_E_INVALID_ARG, "jepa_context_launches: null argument");
+  if (B <= 0) return fail(JEPA_E_INVALID_ARG, "batch %d must be positive", B);
+  Geo g;
+  jepa_status st = geometry(&c->m->hp, T, H, W, &g);
+  if (st != JEPA_OK) return st;
+  *n_out = launches_per_encode(c->m);
+  return JEPA_OK;
+}
+
+extern "C" jepa_status jepa_encode(jepa_context* c, const float* d_pixels, int32_t B, int32_t T, int32_t H,
+                                   int32_t W, int32_t layout, float* d_tokens) {
+  if (!c) return fail(JEPA_E_INVALID_ARG, "jepa_encode: null context");
+  Geo g;
+  jepa_status st = check_shape(c, d_pixels, B, T, H, W, layout, d_tokens, &g);
+  if (st != JEPA_OK) return st;
+  CUDA_TRY(cudaSetDevice(c->m->device));
+  st = prepare_shape(c, B, T, H, W, g);
+  if (st != JEPA_OK) return st;
+  if (!c->use_graph) return launch_encode(c, d_pixels, B, T, H, W, layout, d_tokens, g);
+
+  const bool hit = c->gexec && c->gB == B && c->gT == T && c->gH == H && c->gW == W && c->glayout == layout &&
+                   c->gpix == d_pixels && c->gtok == d_tokens;
+  if (!hit) {
+    if (c->gexec) {
+      cudaGraphExecDestroy(c->gexec);
+      c->gexec = nullptr;
+    }
+    cudaGraph_t graph = nullptr;
+    CUDA_TRY(cudaStreamBeginCapture(c->stream, cudaStreamCaptureModeThreadLocal));
+    st = launch_encode(c, d_pixels, B, T, H, W, layout, d_tokens, g);
+    cudaError_t e = cudaStreamEndCapture(c->stream, &graph);
+    if (st != JEPA_OK) {
+      if (graph) cudaGraphDestroy(graph);
+      return st;
+    }
+    if (e != cudaSuccess) return fail(JEPA_E_CUDA, "graph capture: %s", cudaGetErrorString(e));
+    e = cudaGraphInstantiate(&c->gexec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (e != cudaSuccess) return fail(JEPA_E_CUDA, "graph instantiate: %s", cudaGetErrorString(e));
+    c->gB = B;
+    c->gT = T;
+    c->gH = H;
+    c->gW = W;
+    c->glayout = layout;
+    c->gpix = d_pixels;
+    c->gtok = d_tokens;
+  }
+  CUDA_TRY(cudaGraphLaunch(c->gexec, c->stream));
+  return JEPA_OK;
+}
+
+extern "C" jepa_status jepa_encode_host(jepa_context* c, const float* h_pixels, int32_t B, int32_t T, int32_t H,
+                                        int32_t W, int32_t layout, float* h_tokens) {
+  if (!c) return fail(JEPA_E_INVALID_ARG, "jepa_encode_host: null context");
+  Geo g;
+  jepa_status st = check_shape(c, h_pixels, B, T, H, W, layout, h_tokens, &g);
+  if (st != JEPA_OK) return st;
+  CUDA_TRY(cudaSetDevice(c->m->device));
+  const size_t pix_bytes = (size_t)B * T * c->m->hp.in_chans * H * W * sizeof(float);
+  const size_t tok_bytes = (size_t)B * g.N * c->m->hp.embed_dim * sizeof(float);
+  CUDA_TRY(cudaMemcpyAsync(c->pix_stage, h_pixels, pix_bytes, cudaMemcpyHostToDevice, c->stream));
+  st = jepa_encode(c, c->pix_stage, B, T, H, W, layout, c->tok_stage);
+  if (st != JEPA_OK) return st;
+  CUDA_TRY(cudaMemcpyAsync(h_tokens, c->tok_stage, tok_bytes, cudaMemcpyDeviceToHost, c->stream));
+  return jepa_context_sync(c);
+}
+
+extern "C" jepa_status jepa_context_sync(jepa_context* c) {
+  if (!c) return fail(JEPA_E_INVALID_ARG, "jepa_context_sync: null context");
+  CUDA_TRY(cudaSetDevice(c->m->device));
+  CUDA_TRY(cudaStreamSynchronize(c->stream));
+  int h_err = 0;
+  CUDA_TRY(cudaMemcpy(&h_err, c->err, sizeof(int), cudaMemcpyDeviceToHost));
+  if (h_err) {
+    CUDA_TRY(cudaMemset(c->err, 0, sizeof(int)));
+    return fail(JEPA_E_TIMEOUT, "a device-side wait gave up (error word %d)", h_err);
+  }
+  return JEPA_OK;
+}
+
+// ------------------------------------------------------------------ stage entry points
+namespace {
+std::mutex g_op_mu;
+int* g_op_err = nullptr;  // device error word of the stage entry points (one per process)
+
+jepa_status op_err_word(int** out) {
+  std::lock_guard<std::mutex> lk(g_op_mu);
+  if (!g_op_err) {
+    CUDA_TRY(cudaMalloc(&g_op_err, sizeof(int)));
+    CUDA_TRY(cudaMemset(g_op_err, 0, sizeof(int)));
+  }
+  *out = g_op_err;
+  return JEPA_OK;
+}
+}  // namespace
+
+extern "C" jepa_status jepa_op_patchify(const float* d_pixels, int32_t B, int32_t T, int32_t C, int32_t H, int32_t W,
+                                        int32_t tubelet, int32_t patch, int32_t layout, int32_t out_dtype, void* d_out,
+                                        void* stream) {
+  if (!d_pixels || !d_out) return fail(JEPA_E_INVALID_ARG, "jepa_op_patchify: null pointer");
+  if (B <= 0 || T <= 0 || C <= 0 || H <= 0 || W <= 0 || tubelet <= 0 || patch <= 0)
+    return fail(JEPA_E_INVALID_ARG, "jepa_op_patchify: non-positive size");
+  if (T % tubelet || H % patch || W % patch) return fail(JEPA_E_INVALID_ARG, "jepa_op_patchify: sizes not divisible");
+  if (layout != 0 && layout != 1) return fail(JEPA_E_INVALID_ARG, "layout %d unknown", layout);
+  CUDA_TRY(patchify_launch(d_pixels, B, T, C, H, W, tubelet, patch, layout, out_dtype == JEPA_BF16, d_out,
+                           reinterpret_cast<cudaStream_t>(stream)));
+  return JEPA_OK;
+}
+
+extern "C" jepa_status jepa_op_layernorm(const float* d_x, int32_t M, int32_t D, const float* d_gamma,
+                                         const float* d_beta, float eps, int32_t out_dtype, void* d_y, void* stream) {
+  if (!d_x || !d_gamma || !d_beta || !d_y) return fail(JEPA_E_INVALID_ARG, "jepa_op_layernorm: null pointer");
+  if (M < 0 || D <= 0 || D % 4 || D > 2048) return fail(JEPA_E_INVALID_ARG, "jepa_op_layernorm: bad size M %d D %d", M, D);
+  CUDA_TRY(layernorm_launch(d_x, M, D, d_gamma, d_beta, eps, out_dtype == JEPA_BF16, d_y,
+                            reinterpret_cast<cudaStream_t>(stream)));
+  return JEPA_OK;
+}
+
+extern "C" jepa_status jepa_op_linear(int32_t dtype, const void* d_x, int32_t M, int32_t K, const void* d_w, int32_t N,
+                                      const jepa_epilogue* epi, void* stream) {
+  if (!d_x || !d_w || !epi || !epi->d_bias || !epi->d_out) return fail(JEPA_E_INVALID_ARG, "jepa_op_linear: null pointer");
+  if (M < 0 || K <= 0 || N <= 0) return fail(JEPA_E_INVALID_ARG, "jepa_op_linear: bad size %d x %d x %d", M, K, N);
+  if (epi->kind < 0 || epi->kind > JEPA_EPI_PATCH_EMBED) return fail(JEPA_E_INVALID_ARG, "epilogue kind %d", epi->kind);
+  EpiArgs e = make_epi(epi->kind, M, N, epi->d_bias, epi->d_out);
+  if (epi->kind == JEPA_EPI_QKV_ROPE) {
+    if (epi->n_head <= 0 || epi->head_dim <= 0 || 3 * epi->n_head * epi->head_dim != N || epi->head_dim % 2 ||
+        epi->rows_per_item <= 0 || epi->prefix < 0)
+      return fail(JEPA_E_INVALID_ARG, "QKV_ROPE epilogue: inconsistent heads/rows");
+    e.rope = reinterpret_cast<const float2*>(epi->d_rope);
+    e.rows_per_item = epi->rows_per_item;
+    e.prefix = epi->prefix;
+    e.n_head = epi->n_head;
+    e.head_dim = epi->head_dim;
+    e.rope_layout = epi->rope_layout;
+    e.rope_d = rope_d(epi->head_dim);
+  }
+  if (epi->kind == JEPA_EPI_PATCH_EMBED) {
+    if (epi->patches_per_item <= 0 || epi->rows_per_item < epi->patches_per_item + epi->prefix || epi->prefix < 0)
+      return fail(JEPA_E_INVALID_ARG, "PATCH_EMBED epilogue: inconsistent rows");
+    e.patches_per_item = epi->patches_per_item;
+    e.rows_per_item = epi->rows_per_item;
+    e.prefix = epi->prefix;
+    e.pos = epi->d_pos;
+    e.vec = epi->d_vec;
+  }
+  if (N % 4) return fail(JEPA_E_INVALID_ARG, "GEMM epilogues need N %% 4 == 0 (N %d)", N);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (dtype == JEPA_FP32) {
+    CUDA_TRY(gemm_simt_launch(reinterpret_cast<const float*>(d_x), reinterpret_cast<const float*>(d_w), e, M, N, K, s));
+    return JEPA_OK;
+  }
+  if (dtype != JEPA_BF16) return fail(JEPA_E_INVALID_ARG, "dtype %d unknown", dtype);
+  if (K % 64 || N % 64) return fail(JEPA_E_UNSUPPORTED, "bf16 GEMM needs K %% 64 == 0 and N %% 64 == 0 (K %d, N %d)", K, N);
+  if ((reinterpret_cast<uintptr_t>(d_x) | reinterpret_cast<uintptr_t>(d_w)) & 15)
+    return fail(JEPA_E_INVALID_ARG, "bf16 GEMM operands must be 16-byte aligned");
+  if (M == 0) return JEPA_OK;
+  CUDA_TRY(tc_kernels_init());
+  int* err = nullptr;
+  jepa_status st = op_err_word(&err);
+  if (st != JEPA_OK) return st;
+  const int bn = gemm_tc_pick_bn(M, N);
+  CUtensorMap ta, tb;
+  if (!make_tmap_2d_bf16(&ta, d_x, M, K, 128) || !make_tmap_2d_bf16(&tb, d_w, N, K, bn))
+    return fail(JEPA_E_CUDA, "cuTensorMapEncodeTiled refused an operand");
+  CUDA_TRY(gemm_tc_launch(ta, tb, bn, e, M, N, K, err, default_wait_limit_ns(), s));
+  return JEPA_OK;
+}
+
+extern "C" jepa_status jepa_op_rope_table(const jepa_hparams* hp, int32_t T, int32_t H, int32_t W, float* d_table,
+                                          void* stream) {
+  if (!hp || !d_table) return fail(JEPA_E_INVALID_ARG, "jepa_op_rope_table: null pointer");
+  jepa_status st = jepa_hparams_validate(hp);
+  if (st != JEPA_OK) return st;
+  Geo g;
+  st = geometry(hp, T, H, W, &g);
+  if (st != JEPA_OK) return st;
+  CUDA_TRY(rope_table_launch(g.gt, g.gh, g.gw, hp->embed_dim / hp->n_head, hp->rope_theta, hp->rope_interpolate,
+                             hp->rope_ref_grid, reinterpret_cast<float2*>(d_table), reinterpret_cast<cudaStream_t>(stream)));
+  return JEPA_OK;
+}
+
+extern "C" jepa_status jepa_op_attention(int32_t dtype, const void* d_qkv, int32_t B, int32_t N, int32_t n_head,
+                                         int32_t head_dim, int32_t attn_mode, int32_t prefix, int32_t frame_tokens,
+                                         void* d_out, void* stream) {
+  if (!d_qkv || !d_out) return fail(JEPA_E_INVALID_ARG, "jepa_op_attention: null pointer");
+  if (B <= 0 || N <= 0 || n_head <= 0) return fail(JEPA_E_INVALID_ARG, "jepa_op_attention: bad size");
+  if (attn_mode != 0 && attn_mode != 1) return fail(JEPA_E_INVALID_ARG, "attn_mode %d unknown", attn_mode);
+  if (attn_mode == 1 && (frame_tokens <= 0 || prefix < 0)) return fail(JEPA_E_INVALID_ARG, "block-causal needs frame_tokens > 0");
+  if (head_dim != 64) return fail(JEPA_E_UNSUPPORTED, "attention kernels are built for head_dim 64 (got %d)", head_dim);
+  AttnParams p;
+  p.B = B;
+  p.N = N;
+  p.H = n_head;
+  p.head_dim = head_dim;
+  p.attn_mode = attn_mode;
+  p.prefix = prefix;
+  p.frame_tokens = frame_tokens;
+  p.out = d_out;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (dtype == JEPA_FP32) {
+    CUDA_TRY(attention_simt_launch(reinterpret_cast<const float*>(d_qkv), p, s));
+    return JEPA_OK;
+  }
+  if (dtype != JEPA_BF16) return fail(JEPA_E_INVALID_ARG, "dtype %d unknown", dtype);
+  if (reinterpret_cast<uintptr_t>(d_qkv) & 15) return fail(JEPA_E_INVALID_ARG, "qkv must be 16-byte aligned");
+  CUDA_TRY(tc_kernels_init());
+  int* err = nullptr;
+  jepa_status st = op_err_word(&err);
+  if (st != JEPA_OK) return st;
+  CUtensorMap tm;
+  if (!make_tmap_3d_bf16(&tm, d_qkv, B, N, 3 * n_head * 64, 128)) return fail(JEPA_E_CUDA, "cuTensorMapEncodeTiled refused qkv");
+  CUDA_TRY(attention_tc_launch(tm, p, err, default_wait_limit_ns(), s));
+  return JEPA_OK;
+}
+
+extern "C" jepa_status jepa_device_status(void) {
+  CUDA_TRY(cudaDeviceSynchronize());
+  int* err = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_op_mu);
+    err = g_op_err;
+  }
+  if (!err) return JEPA_OK;
+  int h = 0;
+  CUDA_TRY(cudaMemcpy(&h, err, sizeof(int), cudaMemcpyDeviceToHost));
+  if (h) {
+    CUDA_TRY(cudaMemset(err, 0, sizeof(int)));
+    return fail(JEPA_E_TIMEOUT, "a device-side wait gave up (error word %d)", h);
+  }
+  return JEPA_OK;
+}
+
+extern "C" jepa_status jepa_debug_wait_timeout(int32_t limit_us) {
+  if (limit_us <= 0 || limit_us > 1000000) return fail(JEPA_E_INVALID_ARG, "limit_us %d outside (0, 1e6]", limit_us);
+  int* err = nullptr;
+  jepa_status st = op_err_word(&err);
+  if (st != JEPA_OK) return st;
+  CUDA_TRY(wait_timeout_probe_launch(err, (uint64_t)limit_us * 1000ull, nullptr));
+  return jepa_device_status();
+}

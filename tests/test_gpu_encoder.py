@@ -1,0 +1,178 @@
+"""Whole-encoder parity of the GPU path against the oracle (GPU only).
+
+Bars (per workload dtype):
+  fp32: max |y - ref| / max |ref| <= 1e-4
+  bf16: per-token cosine >= 0.9999 and max |y - ref| <= 3e-2 (outputs are unit-scale after the norm)
+Small cases run the live oracle (2 layers, a few hundred tokens, several tiles + ragged tail);
+full-size cases compare sampled rows with tests/golden/full_<workload>.npz, written by
+tests/golden/make_full_goldens.py from the oracle alone.
+"""
+import os
+import threading
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from configs import WORKLOADS, small
+
+jv = pytest.importorskip("jepa_vision_encoder_gb300")
+pytestmark = pytest.mark.gpu
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+PRESET = {
+    "hfvit_ti14_224": "hfvit_ti14",
+    "vjepa2_vitl16_16x256": "vjepa2_vitl16",
+    "vjepa2_1_vitl16_16x384": "vjepa2_1_vitl16",
+    "levjepa_vitl16_16x256": "levjepa_vitl16",
+    "vjepa2_vitg16_64x256": "vjepa2_vitg16",
+}
+
+
+def check_bar(got, ref, dtype, what=""):
+    got = np.asarray(got, dtype=np.float64).reshape(-1, ref.shape[-1])
+    ref = np.asarray(ref, dtype=np.float64).reshape(-1, ref.shape[-1])
+    err = np.abs(got - ref)
+    cos = (got * ref).sum(-1) / (np.linalg.norm(got, axis=-1) * np.linalg.norm(ref, axis=-1))
+    if dtype == "fp32":
+        rel = err.max() / np.abs(ref).max()
+        assert rel <= 1e-4, f"{what}: max rel err {rel:.3e}"
+    else:
+        assert cos.min() >= 0.9999, f"{what}: min token cosine {cos.min():.7f}"
+        assert err.max() <= 3e-2, f"{what}: max abs err {err.max():.3e}"
+    return err.max(), cos.min()
+
+
+def make(name, n_layer=None, batch=1, T=None, H=None, W=None, graph=False):
+    cfg, dtype, _, (T0, H0, W0) = WORKLOADS[name]
+    kw = {} if n_layer is None else {"n_layer": n_layer}
+    model = jv.Model.preset(PRESET[name], seed=0, dtype=dtype, **kw)
+    ctx = jv.Context(model, batch, T or T0, H or H0, W or W0, graph=graph)
+    return model, ctx
+
+
+@pytest.mark.parametrize("name", list(WORKLOADS))
+def test_small_encoder_matches_oracle(name):
+    cfg, dtype, (T, H, W) = small(name)
+    B = 2
+    model, ctx = make(name, n_layer=cfg.n_layer, batch=B, T=T, H=H, W=W)
+    pix = synth.pixels(0, (B, T, 3, H, W))
+    out = ctx.encode(torch.from_numpy(pix).cuda())
+    ctx.sync()
+    ref = oracle.encode(cfg, 0, dtype == "bf16", pix)
+    check_bar(out.cpu().numpy(), ref, dtype, name)
+
+
+def test_weights_are_the_generator_bits():
+    model = jv.Model.preset("vjepa2_vitl16", seed=0, dtype="bf16", n_layer=1)
+    for name, shape in [("enc.blk.0.attn_qkv.weight", (3072, 1024)), ("enc.blk.0.ln1.weight", (1024,)),
+                        ("enc.patch_embed.bias", (1024,))]:
+        assert np.array_equal(model.tensor(name, shape).numpy(), synth.param(0, name, shape, True))
+
+
+def test_layouts_agree_bit_exact():
+    name = "vjepa2_vitl16_16x256"
+    cfg, dtype, (T, H, W) = small(name)
+    model, ctx = make(name, n_layer=2, batch=1, T=T, H=H, W=W)
+    pix = synth.pixels(1, (1, T, 3, H, W))
+    a = ctx.encode(torch.from_numpy(pix).cuda()).clone()
+    b = ctx.encode(torch.from_numpy(np.ascontiguousarray(pix.transpose(0, 2, 1, 3, 4))).cuda(), layout=jv.LAYOUT_CTHW)
+    ctx.sync()
+    assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("name", ["vjepa2_vitl16_16x256", "levjepa_vitl16_16x256", "hfvit_ti14_224"])
+def test_batch_items_equal_single_calls(name):
+    cfg, dtype, (T, H, W) = small(name)
+    B = 3
+    model, ctx = make(name, n_layer=2, batch=B, T=T, H=H, W=W)
+    pix = torch.from_numpy(synth.pixels(2, (B, T, 3, H, W))).cuda()
+    full = ctx.encode(pix).clone()
+    for b in range(B):
+        one = ctx.encode(pix[b:b + 1].contiguous()).clone()
+        assert torch.equal(full[b:b + 1], one), f"item {b}"
+    ctx.sync()
+
+
+def test_graph_replay_and_host_api_match_eager():
+    name = "levjepa_vitl16_16x256"
+    cfg, dtype, (T, H, W) = small(name)
+    model, ctx = make(name, n_layer=2, batch=2, T=T, H=H, W=W)
+    pix_h = torch.from_numpy(synth.pixels(3, (2, T, 3, H, W)))
+    eager = ctx.encode(pix_h.cuda()).clone()
+    ctx.set_graph(True)
+    pix_d = pix_h.cuda()
+    out = torch.empty_like(eager)
+    for _ in range(3):
+        ctx.encode(pix_d, out)
+    ctx.sync()
+    assert torch.equal(out, eager)
+    host = ctx.encode_host(pix_h.pin_memory())
+    assert torch.equal(host, eager.cpu())
+
+
+def test_two_threads_two_contexts_bit_identical():
+    name = "vjepa2_1_vitl16_16x384"
+    cfg, dtype, (T, H, W) = small(name)
+    model = jv.Model.preset(PRESET[name], seed=0, dtype=dtype, n_layer=2)
+    pix = torch.from_numpy(synth.pixels(4, (1, T, 3, H, W)))
+    results = {}
+
+    def run(i):
+        ctx = jv.Context(model, 1, T, H, W)
+        results[i] = ctx.encode_host(pix)
+        ctx.close()
+
+    th = [threading.Thread(target=run, args=(i,)) for i in range(2)]
+    for t in th:
+        t.start()
+    for t in th:
+        t.join()
+    assert torch.equal(results[0], results[1])
+
+
+def test_refusals():
+    model = jv.Model.preset("vjepa2_vitl16", seed=0, dtype="bf16", n_layer=1)
+    with pytest.raises(jv.JepaError) as e:
+        jv.Context(model, 64, 64, 512, 512, max_workspace_bytes=1 << 30)
+    assert e.value.status == jv._lib.E_BUDGET
+    ctx = jv.Context(model, 1, 4, 64, 64)
+    with pytest.raises(jv.JepaError) as e:
+        ctx.encode(torch.zeros((2, 4, 3, 64, 64), device="cuda"))
+    assert e.value.status == jv._lib.E_BUDGET
+    with pytest.raises(jv.JepaError) as e:
+        ctx.encode(torch.zeros((1, 3, 3, 64, 64), device="cuda"))
+    assert e.value.status == jv._lib.E_INVALID_ARG
+    hf = jv.Model.preset("hfvit_ti14", seed=0, dtype="fp32", n_layer=1)
+    c2 = jv.Context(hf, 1, 1, 112, 112)
+    with pytest.raises(jv.JepaError) as e:   # learned table of 257 rows, clip of 65 tokens
+        c2.encode(torch.zeros((1, 1, 3, 112, 112), device="cuda"))
+    assert e.value.status == jv._lib.E_UNSUPPORTED
+    with pytest.raises(jv.JepaError) as e:
+        jv.Model.preset("vjepa2_vitl16", seed=0, dtype="bf16", n_layer=1, n_head=8)   # head_dim 128
+    assert e.value.status == jv._lib.E_UNSUPPORTED
+
+
+def golden_cases():
+    return [n for n in WORKLOADS if os.path.exists(os.path.join(GOLDEN, f"full_{n}.npz"))]
+
+
+@pytest.mark.parametrize("name", golden_cases())
+def test_full_size_sampled_rows_match_oracle(name):
+    g = np.load(os.path.join(GOLDEN, f"full_{name}.npz"))
+    cfg, dtype, batches, (T, H, W) = WORKLOADS[name]
+    B = int(g["batch"])
+    model, ctx = make(name, batch=B)
+    pix = torch.from_numpy(synth.pixels(int(g["seed"]), (B, T, 3, H, W))).cuda()
+    out = ctx.encode(pix)
+    ctx.sync()
+    rows = torch.from_numpy(g["rows"]).long().cuda()
+    for j, b in enumerate(g["items"]):
+        got = out[int(b)][rows].cpu().numpy()
+        check_bar(got, g["tokens"][j].astype(np.float64), dtype, f"{name} item {b}")
+    if B > 1:   # every item of the full batch equals its single-item encode
+        one = jv.Context(model, 1, T, H, W)
+        for b in range(B):
+            assert torch.equal(one.encode(pix[b:b + 1].contiguous()), out[b:b + 1]), f"item {b}"
