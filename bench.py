@@ -1,0 +1,355 @@
+#!/usr/bin/env python3
+"""Encoder throughput on GB300: tokens/s and TFLOP/s of the shared ViT encoder forward.
+
+Workload: V-JEPA 2 ViT-L/16, one 16 x 256 x 256 clip per GPU (2048 tokens), bf16 weights and
+activations with fp32 accumulation, synthetic seeded weights and pixels. A step is one
+jepa_encode of the clip (patchify, patch GEMM, 24 blocks, final norm) on inputs resident in HBM.
+
+    python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+
+Timing: W untimed steps, then K steps, each bracketed by CUDA events on the context stream,
+with a 256 MiB write between steps to flush L2 (outside the events); barrier + synchronize
+around the timed region; the max over ranks of the device time. Per-kernel durations come from
+the library's event hook over the same steps. One JSON line on rank 0.
+
+--impl reference times the oracle (the plain fp64 CPU encoder) on the host cores instead.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "encoder tokens/s and TFLOP/s (fraction of bf16 peak), ViT-L 16×256² video"
+WORKLOAD = dict(preset="vjepa2_vitl16", T=16, H=256, W=256)
+FLUSH_BYTES = 256 << 20  # > 129 MB of L2
+
+# Per-launch DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of a kernel class, from an
+# ncu capture summarised under profiles/; `sha1` is the hash of the kernel's source file when the
+# counters were taken (a changed kernel reports traffic null until it is captured again).
+NCU_TRAFFIC = {}
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--batch", type=int, default=1, help="clips per GPU per step")
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args(argv)
+
+
+# ------------------------------------------------------------------ distributed plumbing
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def reduce_max(value: float, device=None) -> float:
+    """Max of a scalar over ranks (identity without torch.distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(device=None):
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device])
+        else:
+            dist.barrier()
+
+
+# ------------------------------------------------------------------ measured peaks and clocks
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+CLOCK_FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+                "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+                "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while the timed region runs."""
+
+    def __init__(self, device_index: int, interval_ms: int = 50):
+        self.cmd = ["nvidia-smi", "-i", str(device_index), "--query-gpu=" + ",".join(CLOCK_FIELDS),
+                    "--format=csv,noheader,nounits", "-lms", str(interval_ms)]
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)  # let the first sample land before the timed region starts
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < len(CLOCK_FIELDS):
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ oracle timing (host cores)
+def oracle_layer_times(n_tokens_hint=None):
+    """Time the oracle on the workload clip with 1 and 2 transformer layers; returns
+    (t1, t2, tokens, threads). Full-depth time = t1 + (L - 1) (t2 - t1)."""
+    import numpy as np
+    from dataclasses import replace
+    import oracle
+    import synth
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from configs import WORKLOADS
+    cfg, _, _, (T, H, W) = WORKLOADS["vjepa2_vitl16_16x256"]
+    pix = synth.pixels(0, (1, T, 3, H, W))
+    times = []
+    for nl in (1, 2):
+        t0 = time.perf_counter()
+        oracle.encode(replace(cfg, n_layer=nl), 0, True, pix)
+        times.append(time.perf_counter() - t0)
+    return times[0], times[1], oracle.n_tokens(cfg, T, H, W), oracle.num_threads(), cfg.n_layer
+
+
+def cpu_baseline():
+    t1, t2, N, threads, L = oracle_layer_times()
+    per_layer = max(t2 - t1, 1e-9)
+    full = t1 + (L - 1) * per_layer
+    return {"value": N / full, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"fp64 oracle encodes of the same 2048-token clip with 1 and 2 of the {L} layers "
+                      f"({t1:.2f} s, {t2:.2f} s); full-depth time {full:.1f} s extrapolated linearly per layer"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    from dataclasses import replace
+    import synth
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from configs import WORKLOADS
+    cfg, _, _, (T, H, W) = WORKLOADS["vjepa2_vitl16_16x256"]
+    pix = synth.pixels(0, (1, T, 3, H, W))
+    one = replace(cfg, n_layer=1)
+    # calibration: the per-layer cost (2 layers minus 1 layer)
+    t1, t2, N, threads, L = oracle_layer_times()
+    per_layer = max(t2 - t1, 1e-9)
+    for _ in range(args.warmup):
+        oracle.encode(one, 0, True, pix)
+    full_times = []
+    t_start = time.perf_counter()
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.encode(one, 0, True, pix)
+        full_times.append((time.perf_counter() - t0) + (L - 1) * per_layer)
+    wall = time.perf_counter() - t_start
+    mean_full = statistics.mean(full_times)
+    value = N / mean_full
+    sample = (f"each step: the fp64 oracle on the 2048-token clip with 1 of the {L} layers; the other {L - 1} "
+              f"layers added at the calibrated per-layer time {per_layer:.2f} s")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * mean_full, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "V-JEPA 2 ViT-L/16 16x256x256 clip (2048 tokens), batch 1",
+                       "wall_s_sampled_steps": wall},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ our arm
+def source_sha1(kernel_class: str):
+    files = {"attention": "attention_tc.cu", "layernorm": "rowops.cu", "layernorm_final": "rowops.cu",
+             "patchify": "rowops.cu"}
+    name = files.get(kernel_class, "gemm_tc.cu")
+    with open(os.path.join(ROOT, "jepa_vision_encoder_gb300", "csrc", name), "rb") as f:
+        return hashlib.sha1(f.read()).hexdigest()
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group(backend="nccl" if torch.cuda.is_available() else "gloo")
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    import jepa_vision_encoder_gb300 as jv
+    import synth
+
+    B, T, H, W = args.batch, WORKLOAD["T"], WORKLOAD["H"], WORKLOAD["W"]
+    model = jv.Model.preset(WORKLOAD["preset"], seed=0, dtype="bf16", device=local)
+    ctx = jv.Context(model, B, T, H, W)
+    N = model.n_tokens(T, H, W)
+    D = model.hp.embed_dim
+    pix_h = torch.from_numpy(synth.pixels(rank, (B, T, 3, H, W)))
+    pix = pix_h.cuda()
+    out = torch.empty((B, N, D), dtype=torch.float32, device="cuda")
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    stream = ctx.stream
+    peaks = measured_peaks()
+
+    with torch.cuda.stream(stream):
+        ctx.set_profiling(True)
+        for _ in range(args.warmup):
+            flush.zero_()
+            ctx.encode(pix, out)
+        ctx.sync()
+        ctx.profile(reset=True)
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        torch.cuda.synchronize()
+        barrier(local)
+        torch.cuda.synchronize()
+        with ClockSampler(local) as clk:
+            for i in range(args.steps):
+                flush.zero_()
+                starts[i].record(stream)
+                ctx.encode(pix, out)
+                ends[i].record(stream)
+            torch.cuda.synchronize()
+        barrier(local)
+        torch.cuda.synchronize()
+        ctx.sync()
+        step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+        prof = ctx.profile(reset=True)
+        ctx.set_profiling(False)
+
+        # graph replay of the same step, for comparison (not the headline)
+        ctx.set_graph(True)
+        for _ in range(3):
+            ctx.encode(pix, out)
+        g_ms = []
+        for _ in range(min(args.steps, 20)):
+            flush.zero_()
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s0.record(stream)
+            ctx.encode(pix, out)
+            s1.record(stream)
+            g_ms.append((s0, s1))
+        torch.cuda.synchronize()
+        graph_ms = statistics.mean(a.elapsed_time(b) for a, b in g_ms)
+        ctx.set_graph(False)
+
+    total_ms = reduce_max(sum(step_ms), device="cuda" if world > 1 else None)
+    ms_per_step = total_ms / args.steps
+    tokens_per_step = world * B * N
+    value = tokens_per_step * args.steps / (total_ms / 1e3)
+    flops_per_step = sum(v["flops"] for v in prof.values()) / args.steps  # per GPU
+    tflops = world * flops_per_step * args.steps / (total_ms / 1e3) / 1e12
+
+    # dominant kernel class of the timed region
+    name, st = max(prof.items(), key=lambda kv: kv[1]["total_ms"])
+    avg_ms = st["total_ms"] / st["launches"]
+    if st["flops"] > 0:
+        achieved = st["flops"] / st["launches"] / (avg_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"], "kernel": name,
+                "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"]}
+    else:
+        achieved = st["bytes"] / st["launches"] / (avg_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "kernel": name}
+    rec = NCU_TRAFFIC.get(name)
+    roof["traffic"] = rec["bytes_per_launch"] if rec and rec.get("sha1") == source_sha1(name) else None
+    roof["peak_source"] = peaks["source"]
+    kernels = {k: {"launches": v["launches"], "avg_us": 1e3 * v["total_ms"] / v["launches"],
+                   "share": v["total_ms"] / max(sum(x["total_ms"] for x in prof.values()), 1e-9),
+                   **({"tflops": v["flops"] / (v["total_ms"] / 1e3) / 1e12} if v["flops"] else {}),
+                   **({"gbs": v["bytes"] / (v["total_ms"] / 1e3) / 1e9} if v["bytes"] else {})}
+               for k, v in prof.items()}
+
+    # end to end through the C ABI with host buffers (pinned), copies inside the timed region
+    pin_in = pix_h.pin_memory()
+    pin_out = torch.empty((B, N, D), dtype=torch.float32).pin_memory()
+    ctx.encode_host(pin_in, pin_out)
+    e2e_steps = min(args.steps, 20)
+    barrier(local)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        ctx.encode_host(pin_in, pin_out)
+    e2e_s = reduce_max(time.perf_counter() - t0, device="cuda" if world > 1 else None)
+    e2e = {"value": tokens_per_step * e2e_steps / e2e_s, "unit": "tokens/s",
+           "h2d_bytes_per_step": pin_in.numel() * 4, "d2h_bytes_per_step": pin_out.numel() * 4}
+
+    launches = ctx.launches(B, T, H, W)
+    line = None
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": f"V-JEPA 2 ViT-L/16 16x256x256 clip ({N} tokens) x {B} per GPU",
+                           "tokens_per_step": tokens_per_step, "global_batch": world * B, "seq_len": N,
+                           "parallelism": f"replicas x{world} (independent clips, no collective)",
+                           "l2": "flushed (256 MiB write) between steps", "weights": "seeded synthetic"},
+                "tflops": tflops, "frac_of_bf16_peak": tflops / (world * peaks["bf16_tflops"]),
+                "graph_ms_per_step": graph_ms,
+                "roofline": roof, "kernels": kernels,
+                "e2e": e2e, "gpu_launches": launches * args.steps,
+                "clocks": {k: v for k, v in clk.summary().items()}}
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline()
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

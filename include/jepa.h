@@ -151,6 +151,22 @@ jepa_status jepa_encode_host(jepa_context* c, const float* h_pixels, int32_t B, 
  * last check. */
 jepa_status jepa_context_sync(jepa_context* c);
 
+/* Per-kernel timing of the encode launch sequence (the measurement side of "Architecture",
+ * Tools: jepa-bench). With profiling on, every launch of jepa_encode is bracketed by CUDA events
+ * recorded on the context stream (graph replay is bypassed while it is on). */
+typedef struct {
+  char name[24];          /* kernel class: "patchify", "gemm_patch", "ln", "gemm_qkv", "attention", ... */
+  int32_t launches;       /* launches accumulated since the last reset */
+  float total_ms;         /* sum of their event-measured durations */
+  double flops;           /* algorithmic flops of those launches (GEMMs: 2MNK; attention: 4 hd V) */
+  double bytes;           /* algorithmic HBM bytes of those launches (memory-bound kernels) */
+} jepa_kernel_stat;
+jepa_status jepa_context_set_profiling(jepa_context* c, int32_t enable);
+/* Synchronises the context stream, folds the recorded events into at most `max` classes of
+ * out[], sets *n_out, and clears the accumulators when reset != 0. */
+jepa_status jepa_context_profile(jepa_context* c, jepa_kernel_stat* out, int32_t max, int32_t* n_out,
+                                 int32_t reset);
+
 /* ------------------------------------------------------------------ stage entry points
  * The kernels the encoder runs, callable one at a time (tests compare each against the oracle).
  * `stream` is a cudaStream_t (NULL = legacy default stream). Device errors of these calls are

@@ -180,6 +180,18 @@ class Context:
     def sync(self):
         check(lib().jepa_context_sync(self._h))
 
+    def set_profiling(self, enable: bool):
+        check(lib().jepa_context_set_profiling(self._h, int(enable)))
+
+    def profile(self, reset: bool = True) -> dict:
+        """Per-kernel-class event timings accumulated since the last reset:
+        {name: {"launches", "total_ms", "flops", "bytes"}} (synchronises the context stream)."""
+        buf = (_lib.KernelStat * 16)()
+        n = ctypes.c_int32()
+        check(lib().jepa_context_profile(self._h, buf, 16, ctypes.byref(n), int(reset)))
+        return {buf[i].name.decode(): {"launches": buf[i].launches, "total_ms": buf[i].total_ms,
+                                       "flops": buf[i].flops, "bytes": buf[i].bytes} for i in range(n.value)}
+
     def close(self):
         if getattr(self, "_h", None):
             lib().jepa_context_free(self._h)

@@ -44,6 +44,11 @@ class Epilogue(ctypes.Structure):
     ]
 
 
+class KernelStat(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 24), ("launches", ctypes.c_int32), ("total_ms", ctypes.c_float),
+                ("flops", ctypes.c_double), ("bytes", ctypes.c_double)]
+
+
 # name -> (restype, argtypes); the exported surface of include/jepa.h
 _P, _I, _U64, _SZ, _F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_uint64, ctypes.c_size_t, ctypes.c_float
 _HP = ctypes.POINTER(HParams)
@@ -64,6 +69,8 @@ SIGNATURES = {
     "jepa_encode": (_I, [_P, _P, _I, _I, _I, _I, _I, _P]),
     "jepa_encode_host": (_I, [_P, _P, _I, _I, _I, _I, _I, _P]),
     "jepa_context_sync": (_I, [_P]),
+    "jepa_context_set_profiling": (_I, [_P, _I]),
+    "jepa_context_profile": (_I, [_P, ctypes.POINTER(KernelStat), _I, ctypes.POINTER(ctypes.c_int32), _I]),
     "jepa_op_patchify": (_I, [_P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P]),
     "jepa_op_layernorm": (_I, [_P, _I, _I, _P, _P, _F, _I, _P, _P]),
     "jepa_op_linear": (_I, [_I, _P, _I, _I, _P, _I, ctypes.POINTER(Epilogue), _P]),

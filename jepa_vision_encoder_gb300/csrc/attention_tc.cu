@@ -216,9 +216,12 @@ __global__ void __launch_bounds__(192, 2) attn_tc_kernel(const __grid_constant__
           break;
         }
         tc_fence_after();
-        if (m_new > m_run) {
-          const float alpha = ex2_approx(m_run - m_new);
-          l_run *= alpha;
+        // The rescale is decided per row, but the TMEM ld/st are warp-collective (.sync.aligned):
+        // the whole warp rescales when any of its rows needs it, the others with alpha = 1.
+        const bool need = m_new > m_run;
+        const float alpha = need ? ex2_approx(m_run - m_new) : 1.0f;
+        l_run *= alpha;
+        if (__any_sync(0xffffffffu, need)) {
 #pragma unroll 1
           for (int c = 0; c < kHD / 16; ++c) {
             uint32_t ov[16];
@@ -259,7 +262,9 @@ __global__ void __launch_bounds__(192, 2) attn_tc_kernel(const __grid_constant__
       tc_fence_before();
       mbar_arrive(smem_u32(p_full));
     }
-    if (ok && num_kt > 0 && mbar_wait(smem_u32(o_done), (uint32_t)((num_kt - 1) & 1), wc)) {
+    bool store = ok && num_kt > 0 && mbar_wait(smem_u32(o_done), (uint32_t)((num_kt - 1) & 1), wc);
+    store = __all_sync(0xffffffffu, store);  // the TMEM loads below are warp-collective
+    if (store) {
       tc_fence_after();
       const float inv = (l_run > 0.0f) ? 1.0f / l_run : 0.0f;
       __nv_bfloat16* dst = a.out + ((size_t)b * a.N + q) * a.D + h * kHD;

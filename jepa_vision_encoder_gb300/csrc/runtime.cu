@@ -403,6 +403,14 @@ struct jepa_context {
   int gB = -1, gT = -1, gH = -1, gW = -1, glayout = -1;
   const float* gpix = nullptr;
   float* gtok = nullptr;
+  // per-kernel profiling (events on the context stream)
+  bool profiling = false;
+  std::vector<cudaEvent_t> ev_pool;
+  size_t ev_used = 0;
+  struct Rec { int cls; size_t e0, e1; double flops, bytes; };
+  std::vector<Rec> recs;
+  int prof_launches[16] = {};
+  double prof_ms[16] = {}, prof_flops[16] = {}, prof_bytes[16] = {};
 };
 
 namespace {
@@ -489,6 +497,7 @@ extern "C" void jepa_context_free(jepa_context* c) {
   cudaSetDevice(c->m->device);
   if (c->stream) cudaStreamSynchronize(c->stream);
   if (c->gexec) cudaGraphExecDestroy(c->gexec);
+  for (cudaEvent_t e : c->ev_pool) cudaEventDestroy(e);
   if (c->own_stream && c->stream) cudaStreamDestroy(c->stream);
   if (c->ws) cudaFree(c->ws);
   delete c;
@@ -587,6 +596,43 @@ EpiArgs make_epi(int kind, int M, int N, const float* bias, void* out) {
   return e;
 }
 
+// Kernel classes of the profiling hook.
+enum ProfClass { kPPatchify, kPGemmPatch, kPPrefix, kPLn, kPGemmQkv, kPAttention, kPGemmOut, kPGemmUp, kPGemmDown,
+                 kPLnFinal, kPClasses };
+const char* kProfNames[kPClasses] = {"patchify", "gemm_patch", "prefix_rows", "layernorm", "gemm_qkv",
+                                     "attention", "gemm_out", "gemm_up", "gemm_down", "layernorm_final"};
+
+size_t prof_event(jepa_context* c) {
+  if (c->ev_used == c->ev_pool.size()) {
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) return (size_t)-1;
+    c->ev_pool.push_back(e);
+  }
+  return c->ev_used++;
+}
+
+// Runs `launch`, bracketed by two events when profiling is on.
+template <class F>
+cudaError_t prof(jepa_context* c, int cls, double flops, double bytes, F&& launch) {
+  if (!c->profiling) return launch();
+  const size_t e0 = prof_event(c), e1 = prof_event(c);
+  if (e0 == (size_t)-1 || e1 == (size_t)-1) return cudaErrorMemoryAllocation;
+  cudaEventRecord(c->ev_pool[e0], c->stream);
+  const cudaError_t r = launch();
+  cudaEventRecord(c->ev_pool[e1], c->stream);
+  c->recs.push_back({cls, e0, e1, flops, bytes});
+  return r;
+}
+
+// Visible (query, key) pairs of one item: N^2 for full attention; for block-causal, every
+// patch query of frame f sees the (f + 1) frame_tokens patch keys before it, a prefix row sees N.
+double visible_pairs(int attn_mode, int prefix, int frames, int frame_tokens, int N) {
+  if (attn_mode == 0) return (double)N * N;
+  double v = (double)prefix * N;
+  for (int f = 0; f < frames; ++f) v += (double)frame_tokens * (f + 1) * frame_tokens;
+  return v;
+}
+
 // The launch sequence of one encode (no host synchronisation inside: graph-capturable).
 jepa_status launch_encode(jepa_context* c, const float* pix, int B, int T, int H, int W, int layout, float* tok,
                           const Geo& g) {
@@ -597,20 +643,29 @@ jepa_status launch_encode(jepa_context* c, const float* pix, int B, int T, int H
   const int M = B * g.N, Mp = B * g.Np;
   cudaStream_t s = c->stream;
   const uint64_t lim = default_wait_limit_ns();
+  const double es = bf ? 2.0 : 4.0;                       // bytes of a GEMM operand element
+  const double dM = M, dMp = Mp, dD = D, dF = F, dK = m->K;
+  const double ln_bytes = dM * dD * (4.0 + es);           // read X fp32, write the normalised rows
+  const double attn_flops = 4.0 * hd * NH * B *
+                            visible_pairs(hp.attn_mode, g.prefix, g.gt, g.gh * g.gw, g.N);
 
-  CUDA_TRY(patchify_launch(pix, B, T, hp.in_chans, H, W, hp.tubelet_size, hp.patch_size, layout, bf, c->Pm, s));
+  CUDA_TRY(prof(c, kPPatchify, 0.0, (double)B * T * hp.in_chans * H * W * 4.0 + dMp * dK * es, [&] {
+    return patchify_launch(pix, B, T, hp.in_chans, H, W, hp.tubelet_size, hp.patch_size, layout, bf, c->Pm, s);
+  }));
   EpiArgs pe = make_epi(kEpiPatch, Mp, D, m->b_patch, c->X);
   pe.patches_per_item = g.Np;
   pe.rows_per_item = g.N;
   pe.prefix = g.prefix;
   pe.pos = m->pos;
   pe.vec = m->mod;
-  if (bf)
-    CUDA_TRY(gemm_tc_launch(c->tm_Pm, m->tm_patch[bn_slot(c->bn_patch)], c->bn_patch, pe, Mp, D, m->K, c->err, lim, s));
-  else
-    CUDA_TRY(gemm_simt_launch(reinterpret_cast<const float*>(c->Pm), reinterpret_cast<const float*>(m->w_patch), pe,
-                              Mp, D, m->K, s));
-  if (g.prefix) CUDA_TRY(prefix_rows_launch(c->X, B, g.N, D, m->cls, m->pos, m->mod, s));
+  CUDA_TRY(prof(c, kPGemmPatch, 2.0 * dMp * dD * dK, 0.0, [&] {
+    return bf ? gemm_tc_launch(c->tm_Pm, m->tm_patch[bn_slot(c->bn_patch)], c->bn_patch, pe, Mp, D, m->K, c->err, lim, s)
+              : gemm_simt_launch(reinterpret_cast<const float*>(c->Pm), reinterpret_cast<const float*>(m->w_patch), pe,
+                                 Mp, D, m->K, s);
+  }));
+  if (g.prefix)
+    CUDA_TRY(prof(c, kPPrefix, 0.0, (double)B * D * 4.0,
+                  [&] { return prefix_rows_launch(c->X, B, g.N, D, m->cls, m->pos, m->mod, s); }));
 
   AttnParams ap;
   ap.B = B;
@@ -624,7 +679,8 @@ jepa_status launch_encode(jepa_context* c, const float* pix, int B, int T, int H
 
   for (int l = 0; l < L; ++l) {
     const LayerW& w = m->layers[l];
-    CUDA_TRY(layernorm_launch(c->X, M, D, w.ln1_w, w.ln1_b, hp.ln_eps, bf, c->Xn, s));
+    CUDA_TRY(prof(c, kPLn, 0.0, ln_bytes,
+                  [&] { return layernorm_launch(c->X, M, D, w.ln1_w, w.ln1_b, hp.ln_eps, bf, c->Xn, s); }));
     EpiArgs qe = make_epi(kEpiQkvRope, M, 3 * D, w.b_qkv, c->qkv);
     qe.rows_per_item = g.N;
     qe.prefix = g.prefix;
@@ -636,26 +692,34 @@ jepa_status launch_encode(jepa_context* c, const float* pix, int B, int T, int H
     EpiArgs oe = make_epi(kEpiResidual, M, D, w.b_out, c->X);
     EpiArgs ue = make_epi(kEpiGelu, M, F, w.b_up, c->Hh);
     EpiArgs de = make_epi(kEpiResidual, M, D, w.b_down, c->X);
-    if (bf) {
-      CUDA_TRY(gemm_tc_launch(c->tm_Xn, w.tm_qkv[bn_slot(c->bn_qkv)], c->bn_qkv, qe, M, 3 * D, D, c->err, lim, s));
-      CUDA_TRY(attention_tc_launch(c->tm_qkv3, ap, c->err, lim, s));
-      CUDA_TRY(gemm_tc_launch(c->tm_ao, w.tm_out[bn_slot(c->bn_out)], c->bn_out, oe, M, D, D, c->err, lim, s));
-      CUDA_TRY(layernorm_launch(c->X, M, D, w.ln2_w, w.ln2_b, hp.ln_eps, true, c->Xn, s));
-      CUDA_TRY(gemm_tc_launch(c->tm_Xn, w.tm_up[bn_slot(c->bn_up)], c->bn_up, ue, M, F, D, c->err, lim, s));
-      CUDA_TRY(gemm_tc_launch(c->tm_Hh, w.tm_down[bn_slot(c->bn_down)], c->bn_down, de, M, D, F, c->err, lim, s));
-    } else {
-      const float* Xn = reinterpret_cast<const float*>(c->Xn);
-      CUDA_TRY(gemm_simt_launch(Xn, reinterpret_cast<const float*>(w.w_qkv), qe, M, 3 * D, D, s));
-      CUDA_TRY(attention_simt_launch(reinterpret_cast<const float*>(c->qkv), ap, s));
-      CUDA_TRY(gemm_simt_launch(reinterpret_cast<const float*>(c->ao), reinterpret_cast<const float*>(w.w_out), oe, M,
-                                D, D, s));
-      CUDA_TRY(layernorm_launch(c->X, M, D, w.ln2_w, w.ln2_b, hp.ln_eps, false, c->Xn, s));
-      CUDA_TRY(gemm_simt_launch(Xn, reinterpret_cast<const float*>(w.w_up), ue, M, F, D, s));
-      CUDA_TRY(gemm_simt_launch(reinterpret_cast<const float*>(c->Hh), reinterpret_cast<const float*>(w.w_down), de,
-                                M, D, F, s));
-    }
+    const float* Xn = reinterpret_cast<const float*>(c->Xn);
+    CUDA_TRY(prof(c, kPGemmQkv, 2.0 * dM * 3.0 * dD * dD, 0.0, [&] {
+      return bf ? gemm_tc_launch(c->tm_Xn, w.tm_qkv[bn_slot(c->bn_qkv)], c->bn_qkv, qe, M, 3 * D, D, c->err, lim, s)
+                : gemm_simt_launch(Xn, reinterpret_cast<const float*>(w.w_qkv), qe, M, 3 * D, D, s);
+    }));
+    CUDA_TRY(prof(c, kPAttention, attn_flops, 0.0, [&] {
+      return bf ? attention_tc_launch(c->tm_qkv3, ap, c->err, lim, s)
+                : attention_simt_launch(reinterpret_cast<const float*>(c->qkv), ap, s);
+    }));
+    CUDA_TRY(prof(c, kPGemmOut, 2.0 * dM * dD * dD, 0.0, [&] {
+      return bf ? gemm_tc_launch(c->tm_ao, w.tm_out[bn_slot(c->bn_out)], c->bn_out, oe, M, D, D, c->err, lim, s)
+                : gemm_simt_launch(reinterpret_cast<const float*>(c->ao), reinterpret_cast<const float*>(w.w_out), oe,
+                                   M, D, D, s);
+    }));
+    CUDA_TRY(prof(c, kPLn, 0.0, ln_bytes,
+                  [&] { return layernorm_launch(c->X, M, D, w.ln2_w, w.ln2_b, hp.ln_eps, bf, c->Xn, s); }));
+    CUDA_TRY(prof(c, kPGemmUp, 2.0 * dM * dF * dD, 0.0, [&] {
+      return bf ? gemm_tc_launch(c->tm_Xn, w.tm_up[bn_slot(c->bn_up)], c->bn_up, ue, M, F, D, c->err, lim, s)
+                : gemm_simt_launch(Xn, reinterpret_cast<const float*>(w.w_up), ue, M, F, D, s);
+    }));
+    CUDA_TRY(prof(c, kPGemmDown, 2.0 * dM * dD * dF, 0.0, [&] {
+      return bf ? gemm_tc_launch(c->tm_Hh, w.tm_down[bn_slot(c->bn_down)], c->bn_down, de, M, D, F, c->err, lim, s)
+                : gemm_simt_launch(reinterpret_cast<const float*>(c->Hh), reinterpret_cast<const float*>(w.w_down), de,
+                                   M, D, F, s);
+    }));
   }
-  CUDA_TRY(layernorm_launch(c->X, M, D, m->norm_w, m->norm_b, hp.ln_eps, false, tok, s));
+  CUDA_TRY(prof(c, kPLnFinal, 0.0, dM * dD * 8.0,
+                [&] { return layernorm_launch(c->X, M, D, m->norm_w, m->norm_b, hp.ln_eps, false, tok, s); }));
   return JEPA_OK;
 }
 }  // namespace
@@ -680,7 +744,7 @@ extern "C" jepa_status jepa_encode(jepa_context* c, const float* d_pixels, int32
   CUDA_TRY(cudaSetDevice(c->m->device));
   st = prepare_shape(c, B, T, H, W, g);
   if (st != JEPA_OK) return st;
-  if (!c->use_graph) return launch_encode(c, d_pixels, B, T, H, W, layout, d_tokens, g);
+  if (!c->use_graph || c->profiling) return launch_encode(c, d_pixels, B, T, H, W, layout, d_tokens, g);
 
   const bool hit = c->gexec && c->gB == B && c->gT == T && c->gH == H && c->gW == W && c->glayout == layout &&
                    c->gpix == d_pixels && c->gtok == d_tokens;
@@ -738,6 +802,51 @@ extern "C" jepa_status jepa_context_sync(jepa_context* c) {
   if (h_err) {
     CUDA_TRY(cudaMemset(c->err, 0, sizeof(int)));
     return fail(JEPA_E_TIMEOUT, "a device-side wait gave up (error word %d)", h_err);
+  }
+  return JEPA_OK;
+}
+
+extern "C" jepa_status jepa_context_set_profiling(jepa_context* c, int32_t enable) {
+  if (!c) return fail(JEPA_E_INVALID_ARG, "jepa_context_set_profiling: null context");
+  c->profiling = enable != 0;
+  return JEPA_OK;
+}
+
+extern "C" jepa_status jepa_context_profile(jepa_context* c, jepa_kernel_stat* out, int32_t max, int32_t* n_out,
+                                            int32_t reset) {
+  if (!c || !n_out || (max > 0 && !out)) return fail(JEPA_E_INVALID_ARG, "jepa_context_profile: null argument");
+  CUDA_TRY(cudaSetDevice(c->m->device));
+  CUDA_TRY(cudaStreamSynchronize(c->stream));
+  for (const auto& r : c->recs) {
+    float ms = 0.0f;
+    CUDA_TRY(cudaEventElapsedTime(&ms, c->ev_pool[r.e0], c->ev_pool[r.e1]));
+    c->prof_launches[r.cls] += 1;
+    c->prof_ms[r.cls] += ms;
+    c->prof_flops[r.cls] += r.flops;
+    c->prof_bytes[r.cls] += r.bytes;
+  }
+  c->recs.clear();
+  c->ev_used = 0;
+  int n = 0;
+  for (int k = 0; k < kPClasses; ++k) {
+    if (!c->prof_launches[k]) continue;
+    if (n < max) {
+      jepa_kernel_stat& st = out[n];
+      memset(&st, 0, sizeof st);
+      snprintf(st.name, sizeof st.name, "%s", kProfNames[k]);
+      st.launches = c->prof_launches[k];
+      st.total_ms = (float)c->prof_ms[k];
+      st.flops = c->prof_flops[k];
+      st.bytes = c->prof_bytes[k];
+    }
+    ++n;
+  }
+  *n_out = n;
+  if (reset) {
+    for (int k = 0; k < kPClasses; ++k) {
+      c->prof_launches[k] = 0;
+      c->prof_ms[k] = c->prof_flops[k] = c->prof_bytes[k] = 0.0;
+    }
   }
   return JEPA_OK;
 }
