@@ -2,19 +2,20 @@
 // fp32 softmax and accumulation: o = softmax(q k^T / sqrt(64) + mask) v per (item, head)
 // ("Architecture", Attention and precision; Block-causal attention).
 //
-// One CTA = one tile of 128 queries of one (item, head); two CTAs per SM (256 TMEM columns
-// and ~82 KB of shared memory each), so one CTA's softmax overlaps the other's MMAs.
-//   warp 0      TMA: the Q tile once, then K and V tiles of 128 keys into a 2-stage ring
-//               (3-D tensor map over qkv [B][N][3D]: rows beyond N read as zeros)
-//   warp 1      MMA: S = Q K^T (4 x M128 N128 K16, both K-major) into TMEM columns [0,128);
-//               after the softmax has written P, O += P V (8 x M128 N64 K16, P read from TMEM
-//               columns [128,192), V MN-major in shared memory) into columns [192,256)
-//   warps 2..5  softmax, one query row per thread (TMEM lane): pass 1 row max of S, pass 2
-//               p = 2^(s*log2e/8 - m) stored to TMEM as bf16; the running max only moves when
-//               a tile raises it by more than 2^8, and then O is rescaled in TMEM; at the end
-//               o = O / l is written as bf16.
-// Block-causal: a query tile only visits keys below the last frame its rows can see, and the
-// per-element predicate runs only on tiles that straddle a frame edge, the CLS row/column or N.
+// One CTA = two tiles of 128 queries (Q0, Q1) of one (item, head), one CTA per SM:
+//   warps 0..3  softmax of Q0, warps 4..7 softmax of Q1: one query row per thread (TMEM lane).
+//               Pass 1 takes the row max of S; pass 2 writes p = 2^(s*log2e/8 - m) to TMEM as
+//               bf16. The running max only moves when a tile raises it by more than 2^8, and then
+//               the warp rescales its O rows in TMEM. At the end o = O / l is stored as bf16.
+//   warp 8      TMA: Q0 and Q1 once, then K and V tiles of 128 keys into a 3-stage ring
+//               (3-D tensor map over qkv [B][N][3D]: rows beyond N read as zeros).
+//   warp 9      MMA, interleaving the two tiles so the tensor core works on one tile while the
+//               other tile's softmax runs:  ... PV0(j), S0(j+1), PV1(j), S1(j+1) ...
+//               S = Q K^T: M128 N128 K16 x4 (both K-major); O += P V: M128 N64 K16 x8 with P
+//               read from TMEM and V MN-major in shared memory.
+// TMEM (512 columns): S0 [0,128) S1 [128,256) P0 [256,320) P1 [320,384) O0 [384,448) O1 [448,512).
+// Block-causal: a CTA only visits keys below the last frame its rows can see, and the per-element
+// predicate runs only on tiles that straddle a frame edge, the CLS row/column or N.
 #include <cuda_bf16.h>
 
 #include <mutex>
@@ -26,15 +27,16 @@ namespace jepa {
 
 namespace {
 
-constexpr int kQT = 128;  // queries per CTA
+constexpr int kQT = 128;  // queries per tile (per softmax warpgroup)
 constexpr int kKT = 128;  // keys per tile
 constexpr int kHD = 64;
 constexpr int kTileBytes = kQT * kHD * 2;  // 16 KB: one 128 x 64 bf16 tile
-constexpr int kKvStages = 2;
-constexpr int kSmemBytes = 1024 + kTileBytes * (1 + 2 * kKvStages) + 256;
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColS = 0, kColP = 128, kColO = 192;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units: p stays below 2^8 between rescales
+constexpr int kKvStages = 3;
+constexpr int kSmemBytes = 1024 + kTileBytes * (2 + 2 * kKvStages) + 256;
+constexpr int kThreads = 320;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0, kColP = 256, kColO = 384;  // + 128 / 64 / 64 per tile
+constexpr float kRescaleThreshold = 8.0f;                 // log2 units: p stays below 2^8 between rescales
 
 struct AttnDev {
   int N, H, D;
@@ -56,34 +58,35 @@ __device__ __forceinline__ void row_window(const AttnDev& a, int q, int& lo, int
   }
 }
 
-__global__ void __launch_bounds__(192, 2) attn_tc_kernel(const __grid_constant__ CUtensorMap tm, AttnDev a) {
+// Last key (exclusive) any query in [q_begin, q_end) can see.
+__device__ __forceinline__ int keys_needed(const AttnDev& a, int q_begin, int q_end) {
+  if (a.attn_mode != 1 || q_begin < a.prefix) return a.N;
+  const int q_last = min(q_end, a.N) - 1;
+  if (q_last < q_begin) return 0;
+  return min(a.N, a.prefix + ((q_last - a.prefix) / a.frame_tokens + 1) * a.frame_tokens);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_constant__ CUtensorMap tm, AttnDev a) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
-  uint8_t* sQ = smem;
-  uint8_t* sK = smem + kTileBytes;                    // kKvStages tiles
-  uint8_t* sV = smem + kTileBytes * (1 + kKvStages);  // kKvStages tiles
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kTileBytes * (1 + 2 * kKvStages));
+  uint8_t* sQ = smem;                                 // 2 tiles
+  uint8_t* sK = smem + 2 * kTileBytes;                // kKvStages tiles
+  uint8_t* sV = smem + (2 + kKvStages) * kTileBytes;  // kKvStages tiles
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (2 + 2 * kKvStages) * kTileBytes);
   uint64_t* q_full = bars;
   uint64_t* kv_full = bars + 1;
   uint64_t* kv_empty = bars + 1 + kKvStages;
-  uint64_t* s_full = bars + 1 + 2 * kKvStages;
-  uint64_t* p_full = s_full + 1;
-  uint64_t* o_done = s_full + 2;
-  uint64_t* mma_done = s_full + 3;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 4);
+  uint64_t* s_full = bars + 1 + 2 * kKvStages;  // [2]
+  uint64_t* p_full = s_full + 2;                // [2]
+  uint64_t* o_done = s_full + 4;                // [2]
+  uint64_t* mma_done = s_full + 6;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 7);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int q0 = blockIdx.x * kQT, h = blockIdx.y, b = blockIdx.z;
-
-  // Key range of this query tile: a tile holding a prefix (CLS) row sees every key.
-  int kv_end = a.N;
-  if (a.attn_mode == 1 && q0 >= a.prefix) {
-    const int q_last = min(q0 + kQT - 1, a.N - 1);
-    kv_end = min(a.N, a.prefix + ((q_last - a.prefix) / a.frame_tokens + 1) * a.frame_tokens);
-  }
-  const int num_kt = (kv_end + kKT - 1) / kKT;
+  const int q0 = blockIdx.x * 2 * kQT, h = blockIdx.y, b = blockIdx.z;
+  const int num_kt = (keys_needed(a, q0, q0 + 2 * kQT) + kKT - 1) / kKT;
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(q_full), 1);
@@ -91,15 +94,17 @@ __global__ void __launch_bounds__(192, 2) attn_tc_kernel(const __grid_constant__
       mbar_init(smem_u32(kv_full + s), 1);
       mbar_init(smem_u32(kv_empty + s), 1);
     }
-    mbar_init(smem_u32(s_full), 1);
-    mbar_init(smem_u32(p_full), 128);
-    mbar_init(smem_u32(o_done), 1);
+    for (int g = 0; g < 2; ++g) {
+      mbar_init(smem_u32(s_full + g), 1);
+      mbar_init(smem_u32(p_full + g), 128);
+      mbar_init(smem_u32(o_done + g), 1);
+    }
     mbar_init(smem_u32(mma_done), 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tm);
   }
-  if (warp == 1) {
+  if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
@@ -109,11 +114,12 @@ __global__ void __launch_bounds__(192, 2) attn_tc_kernel(const __grid_constant__
   const uint32_t tmem = *tmem_slot;
   const WaitCtl wc{abort_flag, a.err, a.limit_ns};
 
-  if (warp == 0) {
+  if (warp == 8) {
     if (lane == 0) {
       const uint32_t qb = smem_u32(q_full);
-      mbar_arrive_expect_tx(qb, kTileBytes);
+      mbar_arrive_expect_tx(qb, 2 * kTileBytes);
       tma_load_3d(smem_u32(sQ), &tm, qb, h * kHD, q0, b);
+      tma_load_3d(smem_u32(sQ + kTileBytes), &tm, qb, h * kHD, q0 + kQT, b);
       int stage = 0;
       uint32_t phase = 0, armed = 0, armed_phase = 0;
       for (int j = 0; j < num_kt; ++j) {
@@ -133,61 +139,87 @@ __global__ void __launch_bounds__(192, 2) attn_tc_kernel(const __grid_constant__
       for (int s = 0; s < kKvStages; ++s)
         if (armed & (1u << s)) mbar_drain(smem_u32(kv_full + s), (armed_phase >> s) & 1u, a.limit_ns, a.err);
     }
-  } else if (warp == 1) {
+  } else if (warp == 9) {
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, kKT, 0, 0);
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, kHD, 0, 1);
-      bool ok = mbar_wait(smem_u32(q_full), 0, wc);
-      int stage = 0;
-      uint32_t phase = 0;
-      const uint32_t q_addr = smem_u32(sQ);
-      for (int j = 0; j < num_kt && ok; ++j) {
-        if (!mbar_wait(smem_u32(kv_full + stage), phase, wc)) break;
-        tc_fence_after();
-        const uint32_t k_addr = smem_u32(sK + stage * kTileBytes), v_addr = smem_u32(sV + stage * kTileBytes);
+      const uint32_t qa[2] = {smem_u32(sQ), smem_u32(sQ + kTileBytes)};
+      auto issue_s = [&](int g, int st) {
+        const uint32_t k_addr = smem_u32(sK + st * kTileBytes);
 #pragma unroll
         for (int k = 0; k < kHD / 16; ++k)
-          mma_ss(tmem + kColS, smem_desc_sw128(q_addr + k * 32, 1024, 1024),
+          mma_ss(tmem + kColS + g * 128, smem_desc_sw128(qa[g] + k * 32, 1024, 1024),
                  smem_desc_sw128(k_addr + k * 32, 1024, 1024), idesc_s, k != 0 ? 1u : 0u);
-        mma_commit(smem_u32(s_full));
-        if (!mbar_wait(smem_u32(p_full), (uint32_t)(j & 1), wc)) break;
-        tc_fence_after();
+        mma_commit(smem_u32(s_full + g));
+      };
+      auto issue_pv = [&](int g, int st, int j) {
+        const uint32_t v_addr = smem_u32(sV + st * kTileBytes);
 #pragma unroll
         for (int k = 0; k < kKT / 16; ++k)
-          mma_ts(tmem + kColO, tmem + kColP + k * 8, smem_desc_sw128(v_addr + k * 2048, 1024, 1024), idesc_o,
-                 (j > 0 || k > 0) ? 1u : 0u);
-        mma_commit(smem_u32(o_done));
-        mma_commit(smem_u32(kv_empty + stage));
-        if (++stage == kKvStages) {
-          stage = 0;
-          phase ^= 1u;
+          mma_ts(tmem + kColO + g * 64, tmem + kColP + g * 64 + k * 8,
+                 smem_desc_sw128(v_addr + k * 2048, 1024, 1024), idesc_o, (j > 0 || k > 0) ? 1u : 0u);
+        mma_commit(smem_u32(o_done + g));
+      };
+      bool ok = num_kt > 0 && mbar_wait(smem_u32(q_full), 0, wc) && mbar_wait(smem_u32(kv_full), 0, wc);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0, 0);
+        issue_s(1, 0);
+      }
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int j = 0; j < num_kt && ok; ++j) {
+        const int nst = (stage + 1 == kKvStages) ? 0 : stage + 1;
+        const uint32_t nph = (stage + 1 == kKvStages) ? (phase ^ 1u) : phase;
+        const bool more = j + 1 < num_kt;
+        // tile 0: P0 V(j), then S0 of the next key tile
+        if (!(ok = mbar_wait(smem_u32(p_full), (uint32_t)(j & 1), wc))) break;
+        tc_fence_after();
+        issue_pv(0, stage, j);
+        if (more) {
+          if (!(ok = mbar_wait(smem_u32(kv_full + nst), nph, wc))) break;
+          tc_fence_after();
+          issue_s(0, nst);
         }
+        // tile 1
+        if (!(ok = mbar_wait(smem_u32(p_full + 1), (uint32_t)(j & 1), wc))) break;
+        tc_fence_after();
+        issue_pv(1, stage, j);
+        mma_commit(smem_u32(kv_empty + stage));  // K(j), V(j) no longer read once these complete
+        if (more) issue_s(1, nst);
+        stage = nst;
+        phase = nph;
       }
       mma_commit(smem_u32(mma_done));
       mbar_drain(smem_u32(mma_done), 0, a.limit_ns, a.err);
     }
   } else {
+    const int g = warp >> 2;                 // which query tile
     const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;  // query row inside the tile = TMEM lane
-    const int q = q0 + r;
-    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+    const int r = quarter * 32 + lane;       // query row inside the tile = TMEM lane
+    const int qt0 = q0 + g * kQT;            // first query of this tile
+    const int q = qt0 + r;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t tS = tmem + lane_off + kColS + g * 128;
+    const uint32_t tP = tmem + lane_off + kColP + g * 64;
+    const uint32_t tO = tmem + lane_off + kColO + g * 64;
     int lo, hi;
     row_window(a, q, lo, hi);
     const float sc = a.scale_log2;
+    // uniform per warpgroup: the tile's query span for the mask classification
+    const int q_first = max(qt0, a.prefix), q_last = min(qt0 + kQT - 1, a.N - 1);
+    const int f_min = (a.attn_mode == 1 && q_last >= q_first) ? (q_first - a.prefix) / a.frame_tokens : 0;
     float m_run = -INFINITY, l_run = 0.0f;
     bool ok = true;
     for (int j = 0; j < num_kt; ++j) {
       const int k0 = j * kKT;
-      // uniform per CTA: does this tile need the element predicate?
       bool masked = (k0 + kKT > a.N);
       if (a.attn_mode == 1) {
-        const int q_first = max(q0, a.prefix), q_last = min(q0 + kQT - 1, a.N - 1);
-        const int f_min = (q_first - a.prefix) / a.frame_tokens;
         const int k_last = min(k0 + kKT - 1, a.N - 1);
         const int fk_max = (k_last - a.prefix) / a.frame_tokens;
-        masked = masked || q0 < a.prefix || k0 < a.prefix || fk_max > f_min || q_last < q_first;
+        masked = masked || qt0 < a.prefix || k0 < a.prefix || fk_max > f_min || q_last < q_first;
       }
-      if (!mbar_wait(smem_u32(s_full), (uint32_t)(j & 1), wc)) {
+      if (!mbar_wait(smem_u32(s_full + g), (uint32_t)(j & 1), wc)) {
         ok = false;
         break;
       }
@@ -197,21 +229,25 @@ __global__ void __launch_bounds__(192, 2) attn_tc_kernel(const __grid_constant__
 #pragma unroll 1
       for (int c = 0; c < kKT / 32; ++c) {
         uint32_t rr[32];
-        tmem_ld32(lane_base + kColS + c * 32, rr);
-        tmem_ld_wait();
+        tmem_ld32(tS + c * 32, rr);
+        tmem_ld_wait(rr);
+        if (masked) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int key = k0 + c * 32 + e;
-          const float s = __uint_as_float(rr[e]);
-          if (!masked || (key >= lo && key < hi)) mx = fmaxf(mx, s);
+          for (int e = 0; e < 32; ++e) {
+            const int key = k0 + c * 32 + e;
+            if (key >= lo && key < hi) mx = fmaxf(mx, __uint_as_float(rr[e]));
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(rr[e]));
         }
       }
       const float m_tile = mx * sc;
       float m_new = m_run;
       if (j == 0 || m_tile > m_run + kRescaleThreshold) m_new = fmaxf(m_run, m_tile);
-      // O and P are free once the previous P V has completed
       if (j > 0) {
-        if (!mbar_wait(smem_u32(o_done), (uint32_t)((j - 1) & 1), wc)) {
+        // O and P of this tile are free once its previous P V has completed
+        if (!mbar_wait(smem_u32(o_done + g), (uint32_t)((j - 1) & 1), wc)) {
           ok = false;
           break;
         }
@@ -225,11 +261,11 @@ __global__ void __launch_bounds__(192, 2) attn_tc_kernel(const __grid_constant__
 #pragma unroll 1
           for (int c = 0; c < kHD / 16; ++c) {
             uint32_t ov[16];
-            tmem_ld16(lane_base + kColO + c * 16, ov);
-            tmem_ld_wait();
+            tmem_ld16(tO + c * 16, ov);
+            tmem_ld_wait(ov);
 #pragma unroll
             for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-            tmem_st16(lane_base + kColO + c * 16, ov);
+            tmem_st16(tO + c * 16, ov);
           }
         }
       }
@@ -240,29 +276,29 @@ __global__ void __launch_bounds__(192, 2) attn_tc_kernel(const __grid_constant__
 #pragma unroll 1
       for (int c = 0; c < kKT / 32; ++c) {
         uint32_t rr[32];
-        tmem_ld32(lane_base + kColS + c * 32, rr);
-        tmem_ld_wait();
+        tmem_ld32(tS + c * 32, rr);
+        tmem_ld_wait(rr);
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const int key = k0 + c * 32 + e;
           float p0 = ex2_approx(fmaf(__uint_as_float(rr[e]), sc, -base));
           float p1 = ex2_approx(fmaf(__uint_as_float(rr[e + 1]), sc, -base));
           if (masked) {
+            const int key = k0 + c * 32 + e;
             if (!(key >= lo && key < hi)) p0 = 0.0f;
             if (!(key + 1 >= lo && key + 1 < hi)) p1 = 0.0f;
           }
           lsum += p0 + p1;
           pk[e >> 1] = pack_bf16x2(p0, p1);
         }
-        tmem_st16(lane_base + kColP + c * 16, pk);
+        tmem_st16(tP + c * 16, pk);
       }
       l_run += lsum;
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(smem_u32(p_full));
+      mbar_arrive(smem_u32(p_full + g));
     }
-    bool store = ok && num_kt > 0 && mbar_wait(smem_u32(o_done), (uint32_t)((num_kt - 1) & 1), wc);
+    bool store = ok && num_kt > 0 && mbar_wait(smem_u32(o_done + g), (uint32_t)((num_kt - 1) & 1), wc);
     store = __all_sync(0xffffffffu, store);  // the TMEM loads below are warp-collective
     if (store) {
       tc_fence_after();
@@ -271,8 +307,8 @@ __global__ void __launch_bounds__(192, 2) attn_tc_kernel(const __grid_constant__
 #pragma unroll 1
       for (int c = 0; c < kHD / 32; ++c) {
         uint32_t ov[32];
-        tmem_ld32(lane_base + kColO + c * 32, ov);
-        tmem_ld_wait();
+        tmem_ld32(tO + c * 32, ov);
+        tmem_ld_wait(ov);
         if (q < a.N) {
           uint4 w[4];
           uint32_t* wp = reinterpret_cast<uint32_t*>(w);
@@ -288,7 +324,7 @@ __global__ void __launch_bounds__(192, 2) attn_tc_kernel(const __grid_constant__
     tc_fence_before();
   }
   __syncthreads();
-  if (warp == 1) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -324,8 +360,8 @@ cudaError_t attention_tc_launch(const CUtensorMap& tmQKV, const AttnParams& p, i
   a.scale_log2 = 1.4426950408889634f / 8.0f;  // log2(e) / sqrt(64)
   a.err = err;
   a.limit_ns = limit_ns;
-  dim3 grid((p.N + kQT - 1) / kQT, p.H, p.B);
-  attn_tc_kernel<<<grid, 192, kSmemBytes, s>>>(tmQKV, a);
+  dim3 grid((p.N + 2 * kQT - 1) / (2 * kQT), p.H, p.B);
+  attn_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(tmQKV, a);
   return cudaGetLastError();
 }
 

@@ -31,24 +31,75 @@ struct EpiArgs {
 
 __device__ __forceinline__ float gelu_erf(float x) { return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f)); }
 
+// 3-D RoPE on 32 consecutive columns of one head of width 64 starting at head dim J0 (0 or 32):
+// d = 2*((64/3)/2) = 20 rotated dims per axis (t: 0-19, h: 20-39, w: 40-59), 60-63 untouched.
+// Every index is a compile-time constant; LAYOUT 0 = tiled (frequency j mod 10), 1 = interleaved
+// (frequency j / 2). row = the token's table [3][10] of (cos, sin).
+template <int J0, int LAYOUT>
+__device__ __forceinline__ void rope_hd64_chunk(float (&v)[32], const float2* __restrict__ row) {
+#pragma unroll
+  for (int e = 0; e < 32; e += 2) {
+    constexpr int kD = 20, kDh = 10;
+    const int j = J0 + e;  // even dim inside the head
+    if (j < 3 * kD) {
+      const int axis = j / kD, jj = j - axis * kD;
+      const int k0 = LAYOUT == 0 ? (jj % kDh) : (jj >> 1);
+      const int k1 = LAYOUT == 0 ? ((jj + 1) % kDh) : ((jj + 1) >> 1);
+      const float2 c0 = __ldg(row + axis * kDh + k0);
+      const float2 c1 = __ldg(row + axis * kDh + k1);
+      const float x0 = v[e], x1 = v[e + 1];
+      // x cos + rot90(x) sin, rot90(y1, y2) = (-y2, y1): each member uses its own angle
+      v[e] = fmaf(x0, c0.x, -x1 * c0.y);
+      v[e + 1] = fmaf(x1, c1.x, x0 * c1.y);
+    }
+  }
+}
+
 // OUT_BF16 selects bf16 storage of BIAS / GELU / QKV_ROPE (the bf16 path); RESIDUAL and PATCH
 // always store fp32 (the residual stream).
 template <int E, bool OUT_BF16>
 __device__ __forceinline__ void epi_fragment(const EpiArgs& a, int m, int n0, float (&v)[E]) {
   if (m >= a.M) return;
+  if ((E % 4) == 0 && n0 + E <= a.N && (n0 & 3) == 0) {
+    const float4* b4 = reinterpret_cast<const float4*>(a.bias + n0);
 #pragma unroll
-  for (int e = 0; e < E; ++e) v[e] += (n0 + e < a.N) ? __ldg(a.bias + n0 + e) : 0.0f;
+    for (int e = 0; e < E; e += 4) {
+      const float4 b = __ldg(b4 + e / 4);
+      v[e] += b.x;
+      v[e + 1] += b.y;
+      v[e + 2] += b.z;
+      v[e + 3] += b.w;
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < E; ++e) v[e] += (n0 + e < a.N) ? __ldg(a.bias + n0 + e) : 0.0f;
+  }
 
   if (a.kind == kEpiGelu) {
 #pragma unroll
     for (int e = 0; e < E; ++e) v[e] = gelu_erf(v[e]);
   } else if (a.kind == kEpiQkvRope && a.rope != nullptr) {
-    const int D = a.n_head * a.head_dim;
     const int p = m % a.rows_per_item;
-    if (p >= a.prefix) {
-      const int i = p - a.prefix;
+    bool done = p < a.prefix;  // prefix (CLS) rows are not rotated
+    if constexpr (E == 32) {
+      // tcgen05 GEMM fast path: a 32-column chunk is one half of one head of width 64
+      if (!done && a.head_dim == 64 && (n0 & 31) == 0) {
+        if (n0 < 2 * a.n_head * 64) {
+          const float2* row = a.rope + (size_t)(p - a.prefix) * 30;
+          const bool upper = (n0 & 63) != 0;
+          if (a.rope_layout == 0) {
+            if (upper) rope_hd64_chunk<32, 0>(v, row); else rope_hd64_chunk<0, 0>(v, row);
+          } else {
+            if (upper) rope_hd64_chunk<32, 1>(v, row); else rope_hd64_chunk<0, 1>(v, row);
+          }
+        }
+        done = true;
+      }
+    }
+    if (!done) {  // any even head width, any fragment (the fp32 SIMT GEMM)
+      const int D = a.n_head * a.head_dim;
       const int d = a.rope_d, dh = d >> 1;
-      const float2* row = a.rope + (size_t)i * 3 * dh;
+      const float2* row = a.rope + (size_t)(p - a.prefix) * 3 * dh;
       float r[E];
 #pragma unroll
       for (int e = 0; e < E; ++e) {

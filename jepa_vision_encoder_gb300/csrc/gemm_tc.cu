@@ -2,13 +2,15 @@
 // operands, fp32 accumulation in tensor memory. Every linear layer of the encoder runs here
 // ("Architecture", The shared ViT graph: patch embed, fused qkv, out-projection, FFN).
 //
-// Warp roles (192 threads, one CTA per SM, grid = min(tiles, SMs), tiles strided over CTAs):
+// Warp roles (320 threads, one CTA per SM, grid = min(tiles, SMs), tiles strided over CTAs):
 //   warp 0      TMA producer: A tile 128x64 and B tile BNx64 per stage (128-byte swizzle)
 //   warp 1      MMA issuer: 4 x tcgen05.mma (M=128, N=BN, K=16) per stage into one of two
 //               TMEM accumulators (2 x BN columns), so the epilogue of tile i overlaps the
 //               main loop of tile i+1
-//   warps 2..5  epilogue: tcgen05.ld 32 columns at a time from their TMEM lane quarter, then the
-//               fused bias / GELU / RoPE / residual / row remap of epilogue.cuh, stored from registers.
+//   warps 2..9  epilogue: two warps per TMEM lane quarter, each taking half of the tile's columns,
+//               32 at a time (the next tcgen05.ld in flight while one chunk is processed), then
+//               the fused bias / GELU / RoPE / residual / row remap of epilogue.cuh, stored from
+//               registers.
 // Every mbarrier wait is bounded (ptx.cuh); on the way out the producer drains its loads and the
 // MMA thread waits for its MMAs before TMEM is freed.
 #include <cuda_bf16.h>
@@ -20,6 +22,8 @@ namespace jepa {
 
 constexpr int kBM = 128;
 constexpr int kBK = 64;  // one 128-byte swizzle atom of bf16 along K
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 
 template <int BN>
 struct GemmCfg {
@@ -33,7 +37,7 @@ struct GemmCfg {
 };
 
 template <int BN, bool OUT_BF16>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, EpiArgs epi,
                    int M, int N, int K, int* err, uint64_t limit_ns) {
   using C = GemmCfg<BN>;
@@ -63,7 +67,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(tfull + a), 1);
-      mbar_init(smem_u32(tempty + a), 4);
+      mbar_init(smem_u32(tempty + a), kEpiWarps);
     }
     mbar_init(smem_u32(mma_done), 1);
     *abort_flag = 0;
@@ -148,7 +152,9 @@ __global__ void __launch_bounds__(192, 1)
       mbar_drain(smem_u32(mma_done), 0, limit_ns, err);
     }
   } else {
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int q = warp & 3;                        // TMEM lane quarter this warp may access
+    constexpr int kChunks = BN / 32 / 2;           // 32-column chunks per warp (half the tile)
+    const int c0 = ((warp - 2) >> 2) * kChunks;    // first chunk of this warp's half
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
@@ -157,15 +163,16 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_after();
       const int m = m0 + q * 32 + lane;
       const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(trow + c * 32, r);
-        tmem_ld_wait();
+      uint32_t r[2][32];
+      tmem_ld32(trow + c0 * 32, r[0]);
+#pragma unroll
+      for (int i = 0; i < kChunks; ++i) {
+        tmem_ld_wait(r[i & 1]);
+        if (i + 1 < kChunks) tmem_ld32(trow + (c0 + i + 1) * 32, r[(i + 1) & 1]);
         float v[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
-        epi_fragment<32, OUT_BF16>(epi, m, n0 + c * 32, v);
+        for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[i & 1][e]);
+        epi_fragment<32, OUT_BF16>(epi, m, n0 + (c0 + i) * 32, v);
       }
       tc_fence_before();
       __syncwarp();
@@ -200,7 +207,7 @@ static cudaError_t launch_bn(const CUtensorMap& tmA, const CUtensorMap& tmB, con
   using C = GemmCfg<BN>;
   const int tiles = ((M + kBM - 1) / kBM) * (N / BN);
   const int grid = tiles < num_sms() ? tiles : num_sms();
-  gemm_tc_kernel<BN, OUT_BF16><<<grid, 192, C::kSmemBytes, s>>>(tmA, tmB, epi, M, N, K, err, limit_ns);
+  gemm_tc_kernel<BN, OUT_BF16><<<grid, kThreads, C::kSmemBytes, s>>>(tmA, tmB, epi, M, N, K, err, limit_ns);
   return cudaGetLastError();
 }
 

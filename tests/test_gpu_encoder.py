@@ -140,15 +140,15 @@ def test_refusals():
     assert e.value.status == jv._lib.E_BUDGET
     ctx = jv.Context(model, 1, 4, 64, 64)
     with pytest.raises(jv.JepaError) as e:
-        ctx.encode(torch.zeros((2, 4, 3, 64, 64), device="cuda"))
+        ctx.encode(torch.zeros((2, 4, 3, 64, 64), dtype=torch.float32, device="cuda"))
     assert e.value.status == jv._lib.E_BUDGET
     with pytest.raises(jv.JepaError) as e:
-        ctx.encode(torch.zeros((1, 3, 3, 64, 64), device="cuda"))
+        ctx.encode(torch.zeros((1, 3, 3, 64, 64), dtype=torch.float32, device="cuda"))
     assert e.value.status == jv._lib.E_INVALID_ARG
     hf = jv.Model.preset("hfvit_ti14", seed=0, dtype="fp32", n_layer=1)
     c2 = jv.Context(hf, 1, 1, 112, 112)
     with pytest.raises(jv.JepaError) as e:   # learned table of 257 rows, clip of 65 tokens
-        c2.encode(torch.zeros((1, 1, 3, 112, 112), device="cuda"))
+        c2.encode(torch.zeros((1, 1, 3, 112, 112), dtype=torch.float32, device="cuda"))
     assert e.value.status == jv._lib.E_UNSUPPORTED
     with pytest.raises(jv.JepaError) as e:
         jv.Model.preset("vjepa2_vitl16", seed=0, dtype="bf16", n_layer=1, n_head=8)   # head_dim 128

@@ -129,7 +129,7 @@ def test_linear_fp32(M, N, K, kind):
     x, w, bias = rnd((M, K), 8), rnd((N, K), 9, 0.05), rnd(N, 10, 0.1)
     acc = oracle.linear(x, w)
     init = rnd((M, N), 11)
-    out = torch.from_numpy(init).to(DEV) if kind == jv.EPI_BIAS_RESIDUAL else torch.empty((M, N), device=DEV)
+    out = torch.from_numpy(init).to(DEV) if kind == jv.EPI_BIAS_RESIDUAL else torch.empty((M, N), dtype=torch.float32, device=DEV)
     ref = ref_epilogue(kind, acc, bias, init)
     jv.ops.linear(torch.from_numpy(x).to(DEV), torch.from_numpy(w).to(DEV), torch.from_numpy(bias).to(DEV), out, kind)
     assert np.abs(f64(out) - ref).max() <= 1e-5 * np.abs(ref).max()
@@ -179,7 +179,7 @@ def test_qkv_rope_epilogue(case, dtype):
         out = torch.empty((M, 3 * D), dtype=torch.bfloat16, device=DEV)
     else:
         xt, wt = torch.from_numpy(x), torch.from_numpy(w)
-        out = torch.empty((M, 3 * D), device=DEV)
+        out = torch.empty((M, 3 * D), dtype=torch.float32, device=DEV)
     table = jv.ops.rope_table(hp, T, H, W)
     jv.ops.linear(xt.to(DEV), wt.to(DEV), torch.from_numpy(bias).to(DEV), out, jv.EPI_QKV_ROPE, rope=table,
                   rows_per_item=N, prefix=cfg.cls_token, n_head=n_head, head_dim=64, rope_layout=cfg.rope_layout)
@@ -293,7 +293,7 @@ def test_bounded_wait_reports_timeout_and_device_stays_usable():
     x = bf16_exact(rnd((128, 64), 60))
     w = bf16_exact(rnd((64, 64), 61))
     out = torch.empty((128, 64), dtype=torch.bfloat16, device=DEV)
-    jv.ops.linear(x.to(DEV), w.to(DEV), torch.zeros(64, device=DEV), out)
+    jv.ops.linear(x.to(DEV), w.to(DEV), torch.zeros(64, dtype=torch.float32, device=DEV), out)
     torch.cuda.synchronize()
     ref = oracle.linear(f64(x), f64(w))
     assert np.all(np.abs(f64(out) - ref) <= bf16_bound(ref, 64))

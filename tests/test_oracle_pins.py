@@ -21,7 +21,6 @@ import synth
 from oracle import Config
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "printed_values.json")
-torch.set_default_dtype(torch.float64)
 
 
 def tiny_video(**kw):
