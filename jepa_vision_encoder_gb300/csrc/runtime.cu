@@ -409,6 +409,11 @@ struct jepa_context {
   size_t ev_used = 0;
   struct Rec { int cls; size_t e0, e1; double flops, bytes; };
   std::vector<Rec> recs;
+  // events recorded inside a captured graph (re-recorded by every replay, folded after each)
+  bool capturing = false, gprof = false, gpending = false;
+  std::vector<cudaEvent_t> gev;
+  size_t gev_used = 0;
+  std::vector<Rec> grecs;
   int prof_launches[16] = {};
   double prof_ms[16] = {}, prof_flops[16] = {}, prof_bytes[16] = {};
 };
@@ -498,6 +503,7 @@ extern "C" void jepa_context_free(jepa_context* c) {
   if (c->stream) cudaStreamSynchronize(c->stream);
   if (c->gexec) cudaGraphExecDestroy(c->gexec);
   for (cudaEvent_t e : c->ev_pool) cudaEventDestroy(e);
+  for (cudaEvent_t e : c->gev) cudaEventDestroy(e);
   if (c->own_stream && c->stream) cudaStreamDestroy(c->stream);
   if (c->ws) cudaFree(c->ws);
   delete c;
@@ -603,6 +609,7 @@ const char* kProfNames[kPClasses] = {"patchify", "gemm_patch", "prefix_rows", "l
                                      "attention", "gemm_out", "gemm_up", "gemm_down", "layernorm_final"};
 
 size_t prof_event(jepa_context* c) {
+  if (c->capturing) return c->gev_used < c->gev.size() ? c->gev_used++ : (size_t)-1;  // created before capture
   if (c->ev_used == c->ev_pool.size()) {
     cudaEvent_t e;
     if (cudaEventCreate(&e) != cudaSuccess) return (size_t)-1;
@@ -617,11 +624,30 @@ cudaError_t prof(jepa_context* c, int cls, double flops, double bytes, F&& launc
   if (!c->profiling) return launch();
   const size_t e0 = prof_event(c), e1 = prof_event(c);
   if (e0 == (size_t)-1 || e1 == (size_t)-1) return cudaErrorMemoryAllocation;
-  cudaEventRecord(c->ev_pool[e0], c->stream);
+  std::vector<cudaEvent_t>& pool = c->capturing ? c->gev : c->ev_pool;
+  cudaEventRecord(pool[e0], c->stream);
   const cudaError_t r = launch();
-  cudaEventRecord(c->ev_pool[e1], c->stream);
-  c->recs.push_back({cls, e0, e1, flops, bytes});
+  cudaEventRecord(pool[e1], c->stream);
+  (c->capturing ? c->grecs : c->recs).push_back({cls, e0, e1, flops, bytes});
   return r;
+}
+
+// Adds the durations of the last graph replay's recorded events to the accumulators.
+cudaError_t fold_graph_events(jepa_context* c) {
+  if (!c->gpending) return cudaSuccess;
+  cudaError_t e = cudaStreamSynchronize(c->stream);
+  if (e != cudaSuccess) return e;
+  for (const auto& r : c->grecs) {
+    float ms = 0.0f;
+    e = cudaEventElapsedTime(&ms, c->gev[r.e0], c->gev[r.e1]);
+    if (e != cudaSuccess) return e;
+    c->prof_launches[r.cls] += 1;
+    c->prof_ms[r.cls] += ms;
+    c->prof_flops[r.cls] += r.flops;
+    c->prof_bytes[r.cls] += r.bytes;
+  }
+  c->gpending = false;
+  return cudaSuccess;
 }
 
 // Visible (query, key) pairs of one item: N^2 for full attention; for block-causal, every
@@ -744,18 +770,31 @@ extern "C" jepa_status jepa_encode(jepa_context* c, const float* d_pixels, int32
   CUDA_TRY(cudaSetDevice(c->m->device));
   st = prepare_shape(c, B, T, H, W, g);
   if (st != JEPA_OK) return st;
-  if (!c->use_graph || c->profiling) return launch_encode(c, d_pixels, B, T, H, W, layout, d_tokens, g);
+  if (!c->use_graph) return launch_encode(c, d_pixels, B, T, H, W, layout, d_tokens, g);
 
+  CUDA_TRY(fold_graph_events(c));  // the previous replay's events are about to be re-recorded
   const bool hit = c->gexec && c->gB == B && c->gT == T && c->gH == H && c->gW == W && c->glayout == layout &&
-                   c->gpix == d_pixels && c->gtok == d_tokens;
+                   c->gpix == d_pixels && c->gtok == d_tokens && c->gprof == c->profiling;
   if (!hit) {
     if (c->gexec) {
       cudaGraphExecDestroy(c->gexec);
       c->gexec = nullptr;
     }
+    c->grecs.clear();
+    c->gev_used = 0;
+    if (c->profiling) {  // two events per launch, created outside the capture
+      const size_t need = 2 * (size_t)launches_per_encode(c->m);
+      while (c->gev.size() < need) {
+        cudaEvent_t e;
+        CUDA_TRY(cudaEventCreate(&e));
+        c->gev.push_back(e);
+      }
+    }
     cudaGraph_t graph = nullptr;
     CUDA_TRY(cudaStreamBeginCapture(c->stream, cudaStreamCaptureModeThreadLocal));
+    c->capturing = true;
     st = launch_encode(c, d_pixels, B, T, H, W, layout, d_tokens, g);
+    c->capturing = false;
     cudaError_t e = cudaStreamEndCapture(c->stream, &graph);
     if (st != JEPA_OK) {
       if (graph) cudaGraphDestroy(graph);
@@ -772,8 +811,10 @@ extern "C" jepa_status jepa_encode(jepa_context* c, const float* d_pixels, int32
     c->glayout = layout;
     c->gpix = d_pixels;
     c->gtok = d_tokens;
+    c->gprof = c->profiling;
   }
   CUDA_TRY(cudaGraphLaunch(c->gexec, c->stream));
+  c->gpending = c->gprof;
   return JEPA_OK;
 }
 
@@ -817,6 +858,7 @@ extern "C" jepa_status jepa_context_profile(jepa_context* c, jepa_kernel_stat* o
   if (!c || !n_out || (max > 0 && !out)) return fail(JEPA_E_INVALID_ARG, "jepa_context_profile: null argument");
   CUDA_TRY(cudaSetDevice(c->m->device));
   CUDA_TRY(cudaStreamSynchronize(c->stream));
+  CUDA_TRY(fold_graph_events(c));
   for (const auto& r : c->recs) {
     float ms = 0.0f;
     CUDA_TRY(cudaEventElapsedTime(&ms, c->ev_pool[r.e0], c->ev_pool[r.e1]));
