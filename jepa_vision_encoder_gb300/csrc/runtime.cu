@@ -625,9 +625,11 @@ cudaError_t prof(jepa_context* c, int cls, double flops, double bytes, F&& launc
   const size_t e0 = prof_event(c), e1 = prof_event(c);
   if (e0 == (size_t)-1 || e1 == (size_t)-1) return cudaErrorMemoryAllocation;
   std::vector<cudaEvent_t>& pool = c->capturing ? c->gev : c->ev_pool;
-  cudaEventRecord(pool[e0], c->stream);
+  // inside a capture the records become external event nodes, re-recorded by every replay
+  const unsigned flags = c->capturing ? cudaEventRecordExternal : cudaEventRecordDefault;
+  cudaEventRecordWithFlags(pool[e0], c->stream, flags);
   const cudaError_t r = launch();
-  cudaEventRecord(pool[e1], c->stream);
+  cudaEventRecordWithFlags(pool[e1], c->stream, flags);
   (c->capturing ? c->grecs : c->recs).push_back({cls, e0, e1, flops, bytes});
   return r;
 }
