@@ -190,16 +190,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Tile choice by a small cost model: waves of tiles times the per-SM work of one tile divided
+// by the fraction of the tensor peak that tile shape sustains (measured: 1-SM 128x256 0.62,
+// 128x128 0.48, 128x64 0.29 of peak with TMA-fed operands; the 2-SM 256x256 pair form is
+// assumed at 0.85). Returns 64, 128, 256, or kPairTile for the 2-SM kernel.
 int gemm_tc_pick_bn(int M, int N) {
   const int sms = num_sms();
-  const int num_m = (M + kBM - 1) / kBM;
-  // The widest tile whose tiling still gives (nearly) every SM work; narrower tiles for the
-  // small-N layers at small M, where 128x256 tiles would leave most SMs idle.
-  if (N % 256 == 0 && num_m * (N / 256) >= sms) return 256;
-  if (N % 128 == 0 && num_m * (N / 128) >= sms / 2) return 128;
-  if (N % 64 == 0) return 64;
-  return N % 128 == 0 ? 128 : 256;
+  const int num_m = (M + kBM - 1) / kBM, num_m2 = (M + 2 * kBM - 1) / (2 * kBM);
+  int best = 0;
+  double best_cost = 1e30;
+  const struct { int bn; double eff; } one[] = {{256, 0.62}, {128, 0.48}, {64, 0.29}};
+  for (const auto& c : one) {
+    if (N % c.bn) continue;
+    const long long tiles = (long long)num_m * (N / c.bn);
+    const double cost = (double)((tiles + sms - 1) / sms) * c.bn / c.eff;
+    if (cost < best_cost) best_cost = cost, best = c.bn;
+  }
+  if (N % 256 == 0 && sms >= 2) {
+    const long long pair_tiles = (long long)num_m2 * (N / 256);
+    const int pairs = gemm_tc2_max_pairs();
+    const double cost = (double)((pair_tiles + pairs - 1) / pairs) * 256 / 0.85;
+    if (cost < best_cost) best_cost = cost, best = kPairTile;
+  }
+  return best ? best : 64;
 }
+
+int gemm_tc_b_box(int bn) { return bn == kPairTile ? 128 : bn; }
 
 template <int BN, bool OUT_BF16>
 static cudaError_t launch_bn(const CUtensorMap& tmA, const CUtensorMap& tmB, const EpiArgs& epi, int M, int N,
@@ -217,8 +233,11 @@ static cudaError_t set_smem_attr() {
                               GemmCfg<BN>::kSmemBytes);
 }
 
+cudaError_t gemm_tc2_init_attributes();
+
 cudaError_t gemm_tc_init_attributes() {
-  cudaError_t e = set_smem_attr<256, true>();
+  cudaError_t e = gemm_tc2_init_attributes();
+  if (e == cudaSuccess) e = set_smem_attr<256, true>();
   if (e == cudaSuccess) e = set_smem_attr<256, false>();
   if (e == cudaSuccess) e = set_smem_attr<128, true>();
   if (e == cudaSuccess) e = set_smem_attr<128, false>();
@@ -230,6 +249,7 @@ cudaError_t gemm_tc_init_attributes() {
 cudaError_t gemm_tc_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, int BN, const EpiArgs& epi, int M,
                            int N, int K, int* err, uint64_t limit_ns, cudaStream_t s) {
   if (M <= 0) return cudaSuccess;
+  if (BN == kPairTile) return gemm_tc2_launch(tmA, tmB, epi, M, N, K, err, limit_ns, s);
   const bool bf16_out = !(epi.kind == kEpiResidual || epi.kind == kEpiPatch);
   switch (BN) {
     case 256:

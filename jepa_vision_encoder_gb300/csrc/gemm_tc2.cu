@@ -1,0 +1,257 @@
+// gemm_tc2.cu -- the 2-SM form of the tcgen05 GEMM: out = epilogue(A[M,K] B[N,K]^T) with
+// 256 x 256 tiles computed by a cluster of two CTAs on two SMs (tcgen05 cta_group::2).
+//
+// Each CTA of the pair loads, per 64-wide K block, its own 128 rows of A and its own 128 of the
+// tile's 256 columns of B (32 KB per stage instead of the 48 KB a 1-SM 128 x 256 tile needs per SM),
+// so the operand traffic into each SM's shared memory drops by a third at the same tensor work.
+// Only the even CTA issues the MMAs (M = 256: rows 0-127 land in its TMEM, 128-255 in the peer's).
+//
+// Per CTA (320 threads, one CTA per SM, grid = 2 x pairs, tiles strided over pairs):
+//   warp 0      TMA producer of this CTA's halves; completion on its own barrier
+//   warp 1      even CTA: MMA issuer; odd CTA: forwards "stage landed" to the even CTA with a
+//               remote mbarrier arrive (so every copy completes on the barrier of the CTA it
+//               writes to, and each CTA can drain its own copies on the way out)
+//   warps 2..9  epilogue of this CTA's 128 rows (two warps per TMEM lane quarter, half the
+//               columns each), releasing the accumulator with an arrive on the even CTA.
+// Stage and accumulator hand-offs from the even CTA use multicast commits to both CTAs.
+// Every wait is bounded; both CTAs meet at a cluster barrier before TMEM is freed.
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace jepa {
+
+namespace {
+
+constexpr int kTileM = 256;   // rows per pair tile (128 per CTA)
+constexpr int kTileN = 256;   // columns per pair tile (MMA N; 128 B-rows per CTA)
+constexpr int kBK = 64;
+constexpr int kStages = 6;
+constexpr int kHalfBytes = 128 * kBK * 2;            // 16 KB: 128 rows x 64 bf16
+constexpr int kStageBytes = 2 * kHalfBytes;          // A half + B half
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr uint32_t kTmemCols = 2 * kTileN;           // two accumulators
+constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 512;
+
+template <bool OUT_BF16>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, EpiArgs epi,
+                    int M, int N, int K, int* err, uint64_t limit_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  uint8_t* sA = smem;                              // kStages x 16 KB
+  uint8_t* sB = smem + kStages * kHalfBytes;       // kStages x 16 KB
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint64_t* full = bars;                           // own copies landed
+  uint64_t* empty = bars + kStages;                // stage free (multicast from the even CTA)
+  uint64_t* pfull = bars + 2 * kStages;            // even CTA: the odd CTA's copies landed
+  uint64_t* tfull = bars + 3 * kStages;            // accumulator ready (multicast)
+  uint64_t* tempty = bars + 3 * kStages + 2;       // even CTA: accumulator drained by both CTAs
+  uint64_t* mma_done = bars + 3 * kStages + 4;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * kStages + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int pair = blockIdx.x >> 1, num_pairs = gridDim.x >> 1;
+  const int num_m = (M + kTileM - 1) / kTileM, num_n = N / kTileN, num_k = K / kBK;
+  const int num_tiles = num_m * num_n;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(full + s), 1);
+      mbar_init(smem_u32(empty + s), 1);
+      mbar_init(smem_u32(pfull + s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(smem_u32(tfull + a), 1);
+      mbar_init(smem_u32(tempty + a), 2 * kEpiWarps);
+    }
+    mbar_init(smem_u32(mma_done), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // both CTAs' barriers exist before any remote arrive or multicast
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const WaitCtl wc{abort_flag, err, limit_ns};
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, armed = 0, armed_phase = 0;
+      bool ok = true;
+      for (int tile = pair; tile < num_tiles && ok; tile += num_pairs) {
+        const int m0 = (tile % num_m) * kTileM + (int)rank * 128, n0 = (tile / num_m) * kTileN + (int)rank * 128;
+        for (int kb = 0; kb < num_k; ++kb) {
+          if (!mbar_wait(smem_u32(empty + stage), phase ^ 1u, wc)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_u32(full + stage);
+          mbar_arrive_expect_tx(fb, kStageBytes);
+          tma_load_2d(smem_u32(sA + stage * kHalfBytes), &tmA, fb, kb * kBK, m0);
+          tma_load_2d(smem_u32(sB + stage * kHalfBytes), &tmB, fb, kb * kBK, n0);
+          armed |= 1u << stage;
+          armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      for (int s = 0; s < kStages; ++s)
+        if (armed & (1u << s)) mbar_drain(smem_u32(full + s), (armed_phase >> s) & 1u, limit_ns, err);
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 1) {
+      // odd CTA: tell the even CTA when each of this CTA's stages has landed
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = pair; tile < num_tiles && ok; tile += num_pairs) {
+        for (int kb = 0; kb < num_k; ++kb) {
+          if (!mbar_wait(smem_u32(full + stage), phase, wc)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_remote(mapa_shared(smem_u32(pfull + stage), 0));
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    } else if (lane == 0) {
+      // even CTA: the MMA issuer of the pair
+      constexpr uint32_t idesc = idesc_bf16_f32(kTileM, kTileN, 0, 0);
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = pair; tile < num_tiles && ok; tile += num_pairs) {
+        if (!mbar_wait(smem_u32(tempty + acc), acc_phase ^ 1u, wc)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kTileN);
+        for (int kb = 0; kb < num_k; ++kb) {
+          if (!mbar_wait(smem_u32(full + stage), phase, wc) || !mbar_wait(smem_u32(pfull + stage), phase, wc)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA + stage * kHalfBytes), b0 = smem_u32(sB + stage * kHalfBytes);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)
+            mma_ss_pair(d_tmem, smem_desc_sw128(a0 + k * 32, 1024, 1024), smem_desc_sw128(b0 + k * 32, 1024, 1024),
+                        idesc, (kb | k) != 0 ? 1u : 0u);
+          mma_commit_pair_mc(smem_u32(empty + stage), 0x3);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit_pair_mc(smem_u32(tfull + acc), 0x3);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      mma_commit_pair_mc(smem_u32(mma_done), 0x1);
+      mbar_drain(smem_u32(mma_done), 0, limit_ns, err);
+    }
+  } else {
+    const int q = warp & 3;                    // TMEM lane quarter this warp may access
+    constexpr int kChunks = kTileN / 32 / 2;   // 32-column chunks per warp (half the columns)
+    const int c0 = ((warp - 2) >> 2) * kChunks;
+    const uint32_t tempty_even = mapa_shared(smem_u32(tempty), 0);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = pair; tile < num_tiles; tile += num_pairs) {
+      const int m0 = (tile % num_m) * kTileM + (int)rank * 128, n0 = (tile / num_m) * kTileN;
+      if (!mbar_wait(smem_u32(tfull + acc), acc_phase, wc)) break;
+      tc_fence_after();
+      const int m = m0 + q * 32 + lane;
+      const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kTileN);
+      uint32_t r[2][32];
+      tmem_ld32(trow + c0 * 32, r[0]);
+#pragma unroll
+      for (int i = 0; i < kChunks; ++i) {
+        tmem_ld_wait(r[i & 1]);
+        if (i + 1 < kChunks) tmem_ld32(trow + (c0 + i + 1) * 32, r[(i + 1) & 1]);
+        float v[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[i & 1][e]);
+        epi_fragment<32, OUT_BF16>(epi, m, n0 + (c0 + i) * 32, v);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(tempty_even + (uint32_t)(acc * sizeof(uint64_t)));
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // the pair's MMAs are drained and both epilogues are done with TMEM
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace
+
+cudaError_t gemm_tc2_init_attributes() {
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc2_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gemm_tc2_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  return e;
+}
+
+// Cluster pairs that can be resident at once (the GPCs may not pair up every SM).
+int gemm_tc2_max_pairs() {
+  static int cached = 0;
+  if (cached == 0) {
+    int n = 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (num_sms() / 2), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_tc2_kernel<true>, &cfg) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = num_sms() / 2;
+    }
+    cached = n < num_sms() / 2 ? n : num_sms() / 2;
+  }
+  return cached;
+}
+
+cudaError_t gemm_tc2_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const EpiArgs& epi, int M, int N, int K,
+                            int* err, uint64_t limit_ns, cudaStream_t s) {
+  if (M <= 0) return cudaSuccess;
+  if (N % kTileN || K % kBK) return cudaErrorInvalidValue;
+  const int tiles = ((M + kTileM - 1) / kTileM) * (N / kTileN);
+  const int max_pairs = gemm_tc2_max_pairs();
+  const int pairs = tiles < max_pairs ? tiles : max_pairs;
+  const bool bf16_out = !(epi.kind == kEpiResidual || epi.kind == kEpiPatch);
+  if (bf16_out)
+    gemm_tc2_kernel<true><<<2 * pairs, kThreads, kSmemBytes, s>>>(tmA, tmB, epi, M, N, K, err, limit_ns);
+  else
+    gemm_tc2_kernel<false><<<2 * pairs, kThreads, kSmemBytes, s>>>(tmA, tmB, epi, M, N, K, err, limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace jepa

@@ -20,9 +20,15 @@ int num_sms();
 cudaError_t tc_kernels_init();
 uint64_t default_wait_limit_ns();
 
-// tcgen05 GEMM: out = epilogue(A[M,K] * B[N,K]^T), bf16 operands. tmA box 128x64, tmB box BNx64
-// where BN = gemm_tc_pick_bn(M, N).
+// tcgen05 GEMM: out = epilogue(A[M,K] * B[N,K]^T), bf16 operands. tmA box 128x64, tmB box
+// gemm_tc_b_box(BN) x 64 where BN = gemm_tc_pick_bn(M, N); BN == kPairTile selects the 2-SM
+// (cluster pair) kernel with 256 x 256 tiles.
+constexpr int kPairTile = 512;
 int gemm_tc_pick_bn(int M, int N);
+int gemm_tc_b_box(int bn);
+int gemm_tc2_max_pairs();
+cudaError_t gemm_tc2_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const EpiArgs& epi, int M, int N, int K,
+                            int* err, uint64_t limit_ns, cudaStream_t s);
 cudaError_t gemm_tc_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, int BN, const EpiArgs& epi, int M,
                            int N, int K, int* err, uint64_t limit_ns, cudaStream_t s);
 

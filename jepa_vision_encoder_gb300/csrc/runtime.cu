@@ -176,7 +176,7 @@ struct LayerW {
   const void *w_qkv, *w_out, *w_up, *w_down;
   CUtensorMap tm_qkv[3], tm_out[3], tm_up[3], tm_down[3];  // box rows 64 / 128 / 256
 };
-int bn_slot(int bn) { return bn == 64 ? 0 : (bn == 128 ? 1 : 2); }
+int bn_slot(int bn) { return bn == 64 ? 0 : ((bn == 128 || bn == kPairTile) ? 1 : 2); }
 }  // namespace
 
 struct jepa_model {
@@ -637,6 +637,7 @@ cudaError_t prof(jepa_context* c, int cls, double flops, double bytes, F&& launc
 // Adds the durations of the last graph replay's recorded events to the accumulators.
 cudaError_t fold_graph_events(jepa_context* c) {
   if (!c->gpending) return cudaSuccess;
+  c->gpending = false;  // folded at most once, even when the driver refuses the timing
   cudaError_t e = cudaStreamSynchronize(c->stream);
   if (e != cudaSuccess) return e;
   for (const auto& r : c->grecs) {
@@ -977,7 +978,7 @@ extern "C" jepa_status jepa_op_linear(int32_t dtype, const void* d_x, int32_t M,
   if (st != JEPA_OK) return st;
   const int bn = gemm_tc_pick_bn(M, N);
   CUtensorMap ta, tb;
-  if (!make_tmap_2d_bf16(&ta, d_x, M, K, 128) || !make_tmap_2d_bf16(&tb, d_w, N, K, bn))
+  if (!make_tmap_2d_bf16(&ta, d_x, M, K, 128) || !make_tmap_2d_bf16(&tb, d_w, N, K, gemm_tc_b_box(bn)))
     return fail(JEPA_E_CUDA, "cuTensorMapEncodeTiled refused an operand");
   CUDA_TRY(gemm_tc_launch(ta, tb, bn, e, M, N, K, err, default_wait_limit_ns(), s));
   return JEPA_OK;
