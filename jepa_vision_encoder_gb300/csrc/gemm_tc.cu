@@ -192,8 +192,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // Tile choice by a small cost model: waves of tiles times the per-SM work of one tile divided
 // by the fraction of the tensor peak that tile shape sustains (measured: 1-SM 128x256 0.62,
-// 128x128 0.48, 128x64 0.29 of peak with TMA-fed operands; the 2-SM 256x256 pair form is
-// assumed at 0.85). Returns 64, 128, 256, or kPairTile for the 2-SM kernel.
+// 128x128 0.48, 128x64 0.29 of peak with TMA-fed operands; the 2-SM 256x256 pair form 0.75).
+// Returns 64, 128, 256, or kPairTile for the 2-SM kernel.
 int gemm_tc_pick_bn(int M, int N) {
   const int sms = num_sms();
   const int num_m = (M + kBM - 1) / kBM, num_m2 = (M + 2 * kBM - 1) / (2 * kBM);
@@ -209,7 +209,7 @@ int gemm_tc_pick_bn(int M, int N) {
   if (N % 256 == 0 && sms >= 2) {
     const long long pair_tiles = (long long)num_m2 * (N / 256);
     const int pairs = gemm_tc2_max_pairs();
-    const double cost = (double)((pair_tiles + pairs - 1) / pairs) * 256 / 0.85;
+    const double cost = (double)((pair_tiles + pairs - 1) / pairs) * 256 / 0.75;
     if (cost < best_cost) best_cost = cost, best = kPairTile;
   }
   return best ? best : 64;

@@ -7,14 +7,14 @@
 // Only the even CTA issues the MMAs (M = 256: rows 0-127 land in its TMEM, 128-255 in the peer's).
 //
 // Per CTA (320 threads, one CTA per SM, grid = 2 x pairs, tiles strided over pairs):
-//   warp 0      TMA producer of this CTA's halves; completion on its own barrier
-//   warp 1      even CTA: MMA issuer; odd CTA: forwards "stage landed" to the even CTA with a
-//               remote mbarrier arrive (so every copy completes on the barrier of the CTA it
-//               writes to, and each CTA can drain its own copies on the way out)
+//   warp 0      TMA producer of this CTA's halves; every copy of the pair completes on the even
+//               CTA's stage barrier, which the even CTA arms with the bytes of both halves
+//   warp 1      even CTA: MMA issuer (odd CTA: idle)
 //   warps 2..9  epilogue of this CTA's 128 rows (two warps per TMEM lane quarter, half the
 //               columns each), releasing the accumulator with an arrive on the even CTA.
 // Stage and accumulator hand-offs from the even CTA use multicast commits to both CTAs.
-// Every wait is bounded; both CTAs meet at a cluster barrier before TMEM is freed.
+// Every wait is bounded; the even CTA drains every stage phase it armed (both CTAs' copies)
+// and its MMAs, then both CTAs meet at a cluster barrier before TMEM is freed.
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -47,7 +47,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
   uint64_t* full = bars;                           // own copies landed
   uint64_t* empty = bars + kStages;                // stage free (multicast from the even CTA)
-  uint64_t* pfull = bars + 2 * kStages;            // even CTA: the odd CTA's copies landed
+  // bars + 2 * kStages .. + 3 * kStages: unused (keeps the layout of the barrier block)
   uint64_t* tfull = bars + 3 * kStages;            // accumulator ready (multicast)
   uint64_t* tempty = bars + 3 * kStages + 2;       // even CTA: accumulator drained by both CTAs
   uint64_t* mma_done = bars + 3 * kStages + 4;
@@ -64,7 +64,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(full + s), 1);
       mbar_init(smem_u32(empty + s), 1);
-      mbar_init(smem_u32(pfull + s), 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(tfull + a), 1);
@@ -89,6 +88,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
+      // Both CTAs load their halves; every copy completes on the even CTA's stage barrier,
+      // which the even CTA arms with the bytes of both halves (tx-count may run ahead of the
+      // arm within a phase: the phase cannot complete before the even CTA's arrive).
       int stage = 0;
       uint32_t phase = 0, armed = 0, armed_phase = 0;
       bool ok = true;
@@ -99,10 +101,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          const uint32_t fb = smem_u32(full + stage);
-          mbar_arrive_expect_tx(fb, kStageBytes);
-          tma_load_2d(smem_u32(sA + stage * kHalfBytes), &tmA, fb, kb * kBK, m0);
-          tma_load_2d(smem_u32(sB + stage * kHalfBytes), &tmB, fb, kb * kBK, n0);
+          const uint32_t fb_even = mapa_shared(smem_u32(full + stage), 0);
+          if (rank == 0) mbar_arrive_expect_tx(smem_u32(full + stage), 2 * kStageBytes);
+          tma_load_2d_pair(smem_u32(sA + stage * kHalfBytes), &tmA, fb_even, kb * kBK, m0);
+          tma_load_2d_pair(smem_u32(sB + stage * kHalfBytes), &tmB, fb_even, kb * kBK, n0);
           armed |= 1u << stage;
           armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
           if (++stage == kStages) {
@@ -111,29 +113,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
       }
-      for (int s = 0; s < kStages; ++s)
-        if (armed & (1u << s)) mbar_drain(smem_u32(full + s), (armed_phase >> s) & 1u, limit_ns, err);
+      // the even CTA drains every phase it armed (its own and the odd CTA's copies)
+      if (rank == 0)
+        for (int s = 0; s < kStages; ++s)
+          if (armed & (1u << s)) mbar_drain(smem_u32(full + s), (armed_phase >> s) & 1u, limit_ns, err);
     }
   } else if (warp == 1) {
-    if (lane == 0 && rank == 1) {
-      // odd CTA: tell the even CTA when each of this CTA's stages has landed
-      int stage = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-      for (int tile = pair; tile < num_tiles && ok; tile += num_pairs) {
-        for (int kb = 0; kb < num_k; ++kb) {
-          if (!mbar_wait(smem_u32(full + stage), phase, wc)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_remote(mapa_shared(smem_u32(pfull + stage), 0));
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-      }
-    } else if (lane == 0) {
+    if (lane == 0 && rank == 0) {
       // even CTA: the MMA issuer of the pair
       constexpr uint32_t idesc = idesc_bf16_f32(kTileM, kTileN, 0, 0);
       int stage = 0, acc = 0;
@@ -144,7 +130,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kTileN);
         for (int kb = 0; kb < num_k; ++kb) {
-          if (!mbar_wait(smem_u32(full + stage), phase, wc) || !mbar_wait(smem_u32(pfull + stage), phase, wc)) {
+          if (!mbar_wait(smem_u32(full + stage), phase, wc)) {
             ok = false;
             break;
           }

@@ -106,6 +106,17 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tm,
       : "memory");
 }
 
+// Load into this CTA's shared memory, completing on an mbarrier of either CTA of the pair
+// (`bar` is a shared::cluster address, e.g. the even CTA's barrier from mapa).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* tm, uint32_t bar, int32_t x,
+                                                 int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05
 // TMEM allocation (whole warp). Writes the TMEM base address to shared memory at `dst`.
 __device__ __forceinline__ void tmem_alloc(uint32_t dst, uint32_t ncols) {
