@@ -241,6 +241,28 @@ jepa_status jepa_device_status(void);
  * Exercises the failure path of every bounded wait without faulting or hanging the GPU. */
 jepa_status jepa_debug_wait_timeout(int32_t limit_us);
 
+/* ------------------------------------------------------------------ allocation-free encode
+ * The jepa.cpp pages have no counterpart to this entry point. It serves callers that cannot
+ * allocate device memory at all: a host program whose device memory is owned by a fixed pool or
+ * by another framework's allocator, or a loop where a cudaMalloc (which may synchronise the
+ * whole device) is not allowed. It runs the same kernels as jepa_encode, but its workspace is
+ * one scratch array of JEPA_NOALLOC_SCRATCH_BYTES (64 MiB) compiled into the library, so every
+ * GPU that loads the library holds that array until the process exits.
+ *  - The call allocates nothing (no cudaMalloc, no cudaFree, no allocating library routine);
+ *    it uses the model from jepa_model_load and the caller's pixel and token buffers as given.
+ *  - A clip batch whose workspace does not fit in the array is refused with JEPA_E_BUDGET before
+ *    anything is launched (one 16 x 256 x 256 ViT-L/16 clip fits; jepa_context_new has no such cap).
+ *  - The first call on a device looks up the array's address on that device (set-up); make that
+ *    first call before any CUDA stream capture.
+ *  - All calls share the one array, which keeps whatever the last call left in it; calls whose
+ *    work overlaps on the GPU (other streams, other threads) race on it: serialise them.
+ *  - The call is synchronous: it launches on `stream` (a cudaStream_t, NULL = legacy default),
+ *    waits for it, and returns JEPA_E_TIMEOUT if a device-side bounded wait gave up.
+ * Other arguments as jepa_encode. */
+#define JEPA_NOALLOC_SCRATCH_BYTES (64ull << 20)
+jepa_status jepa_encode_noalloc(const jepa_model* m, const float* d_pixels, int32_t B, int32_t T, int32_t H,
+                                int32_t W, int32_t layout, float* d_tokens, void* stream);
+
 /* Thread-local text of the last failure of this thread, and its reset. */
 const char* jepa_error_text(void);
 void jepa_error_reset(void);

@@ -99,6 +99,16 @@ class Model:
     def n_tokens(self, T, H, W) -> int:
         return n_tokens(self.hp, T, H, W)
 
+    def encode_noalloc(self, pixels: torch.Tensor, out: torch.Tensor, layout: int = LAYOUT_TCHW) -> torch.Tensor:
+        """Encode into the caller's `out` with the library's fixed scratch array as workspace
+        (no device allocation); synchronous on torch's current stream. Calls must not overlap."""
+        assert pixels.is_cuda and pixels.dtype == torch.float32 and pixels.is_contiguous()
+        assert out.is_cuda and out.dtype == torch.float32 and out.is_contiguous()
+        B, T, H, W = _clip_dims(pixels, layout)
+        assert out.numel() == B * self.n_tokens(T, H, W) * self.hp.embed_dim
+        check(lib().jepa_encode_noalloc(self._h, _ptr(pixels), B, T, H, W, layout, _ptr(out), _stream_ptr()))
+        return out
+
     def close(self):
         if getattr(self, "_h", None):
             lib().jepa_model_free(self._h)

@@ -78,6 +78,7 @@ SIGNATURES = {
     "jepa_op_attention": (_I, [_I, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P]),
     "jepa_device_status": (_I, []),
     "jepa_debug_wait_timeout": (_I, [_I]),
+    "jepa_encode_noalloc": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P]),
     "jepa_error_text": (ctypes.c_char_p, []),
     "jepa_error_reset": (None, []),
 }

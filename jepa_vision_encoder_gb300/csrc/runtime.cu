@@ -1056,3 +1056,81 @@ extern "C" jepa_status jepa_debug_wait_timeout(int32_t limit_us) {
   CUDA_TRY(wait_timeout_probe_launch(err, (uint64_t)limit_us * 1000ull, nullptr));
   return jepa_device_status();
 }
+
+// ------------------------------------------------------------------ allocation-free encode
+// For callers that cannot allocate device memory: the encode workspace lives in one fixed
+// scratch array of this file instead of a context's cudaMalloc'd arena. The launch sequence is
+// the one jepa_encode runs, over a jepa_context that only views the array.
+namespace {
+static __device__ __align__(256) uint8_t g_noalloc_scratch[JEPA_NOALLOC_SCRATCH_BYTES];
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+uint8_t* g_noalloc_base[kNoAllocMaxDevices] = {};  // the array's device address, per device
+
+// Set-up, once per device with that device current: the host-side name of the array is only a
+// stand-in, so its device address is looked up and kept.
+jepa_status noalloc_scratch(int device, uint8_t** out) {
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_base[device]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p)
+      return fail(JEPA_E_CUDA, "jepa_encode_noalloc: scratch array address on device %d: %s", device,
+                  cudaGetErrorString(e));
+    g_noalloc_base[device] = reinterpret_cast<uint8_t*>(p);
+  }
+  *out = g_noalloc_base[device];
+  return JEPA_OK;
+}
+}  // namespace
+
+extern "C" jepa_status jepa_encode_noalloc(const jepa_model* m, const float* d_pixels, int32_t B, int32_t T,
+                                           int32_t H, int32_t W, int32_t layout, float* d_tokens, void* stream) {
+  if (!m) return fail(JEPA_E_INVALID_ARG, "jepa_encode_noalloc: null model");
+  if (!d_pixels || !d_tokens) return fail(JEPA_E_INVALID_ARG, "jepa_encode_noalloc: null pixel or token pointer");
+  if (layout != JEPA_LAYOUT_TCHW && layout != JEPA_LAYOUT_CTHW) return fail(JEPA_E_INVALID_ARG, "layout %d unknown", layout);
+  if (B <= 0) return fail(JEPA_E_INVALID_ARG, "batch %d must be positive", B);
+  Geo g;
+  jepa_status st = geometry(&m->hp, T, H, W, &g);
+  if (st != JEPA_OK) return st;
+  if (m->hp.pos_type == JEPA_POS_LEARNED && g.N != m->hp.n_pos_rows)
+    return fail(JEPA_E_UNSUPPORTED, "learned position table has %d rows, the clip has %d tokens", m->hp.n_pos_rows, g.N);
+  if (m->device < 0 || m->device >= kNoAllocMaxDevices)
+    return fail(JEPA_E_UNSUPPORTED, "jepa_encode_noalloc: device %d beyond %d", m->device, kNoAllocMaxDevices);
+  const long long rows = (long long)B * g.N, prows = (long long)B * g.Np;
+  const size_t need = ws_layout(m, rows, prows, g.Np, 0, nullptr);
+  if (need > JEPA_NOALLOC_SCRATCH_BYTES)
+    return fail(JEPA_E_BUDGET, "jepa_encode_noalloc: %d x %dx%dx%d needs %zu bytes of scratch, the array holds %llu",
+                B, T, H, W, need, (unsigned long long)JEPA_NOALLOC_SCRATCH_BYTES);
+  CUDA_TRY(cudaSetDevice(m->device));
+  uint8_t* base = nullptr;
+  st = noalloc_scratch(m->device, &base);
+  if (st != JEPA_OK) return st;
+  if (m->dtype == JEPA_BF16) CUDA_TRY(tc_kernels_init());
+
+  jepa_context c;  // a view over the scratch array: owns nothing, frees nothing
+  c.m = m;
+  c.stream = reinterpret_cast<cudaStream_t>(stream);
+  c.own_stream = false;
+  c.max_B = B;
+  c.max_T = T;
+  c.max_H = H;
+  c.max_W = W;
+  c.max_rows = rows;
+  c.max_prows = prows;
+  c.max_np = g.Np;
+  c.max_pix = 0;
+  c.ws = base;
+  c.ws_bytes = need;
+  ws_layout(m, rows, prows, g.Np, 0, &c);
+  CUDA_TRY(cudaMemsetAsync(c.err, 0, sizeof(int), c.stream));  // the array keeps the last call's word
+  st = prepare_shape(&c, B, T, H, W, g);
+  if (st != JEPA_OK) return st;
+  st = launch_encode(&c, d_pixels, B, T, H, W, layout, d_tokens, g);
+  if (st != JEPA_OK) return st;
+  int h_err = 0;
+  CUDA_TRY(cudaMemcpyAsync(&h_err, c.err, sizeof(int), cudaMemcpyDeviceToHost, c.stream));
+  CUDA_TRY(cudaStreamSynchronize(c.stream));
+  if (h_err) return fail(JEPA_E_TIMEOUT, "jepa_encode_noalloc: a device-side wait gave up (error word %d)", h_err);
+  return JEPA_OK;
+}
