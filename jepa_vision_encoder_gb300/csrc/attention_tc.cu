@@ -4,9 +4,11 @@
 //
 // One CTA = two tiles of 128 queries (Q0, Q1) of one (item, head), one CTA per SM:
 //   warps 0..3  softmax of Q0, warps 4..7 softmax of Q1: one query row per thread (TMEM lane).
-//               Pass 1 takes the row max of S; pass 2 writes p = 2^(s*log2e/8 - m) to TMEM as
-//               bf16. The running max only moves when a tile raises it by more than 2^8, and then
-//               the warp rescales its O rows in TMEM. At the end o = O / l is stored as bf16.
+//               The thread reads its 128 scores from TMEM once, takes their max (independent
+//               three-input max chains) and writes p = 2^(s*log2e/8 - m) to TMEM as bf16 pairs
+//               (packed two-lane FMA for the scaling, two-lane adds for the row sum). The
+//               running max only moves when a tile raises it by more than 2^8, and then the
+//               warp rescales its O rows in TMEM. At the end o = O / l is stored as bf16.
 //   warp 8      TMA: Q0 and Q1 once, then K and V tiles of 128 keys into a 3-stage ring
 //               (3-D tensor map over qkv [B][N][3D]: rows beyond N read as zeros).
 //   warp 9      MMA, interleaving the two tiles so the tensor core works on one tile while the
@@ -224,25 +226,32 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         break;
       }
       tc_fence_after();
-      // pass 1: row max of the raw scores
-      float mx = -INFINITY;
-#pragma unroll 1
-      for (int c = 0; c < kKT / 32; ++c) {
-        uint32_t rr[32];
-        tmem_ld32(tS + c * 32, rr);
-        tmem_ld_wait(rr);
-        if (masked) {
+      // the thread's 128 raw scores, read from TMEM once
+      uint32_t s[kKT / 32][32];
+#pragma unroll
+      for (int c = 0; c < kKT / 32; ++c) tmem_ld32(tS + c * 32, s[c]);
+      tmem_ld_wait(s[0]);
+#pragma unroll
+      for (int c = 1; c < kKT / 32; ++c) tmem_ld_bind(s[c]);
+      if (masked) {  // invisible keys score -inf: they lose the max and give p = 0
+#pragma unroll
+        for (int c = 0; c < kKT / 32; ++c)
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const int key = k0 + c * 32 + e;
-            if (key >= lo && key < hi) mx = fmaxf(mx, __uint_as_float(rr[e]));
+            if (!(key >= lo && key < hi)) s[c][e] = __float_as_uint(-INFINITY);
           }
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(rr[e]));
-        }
       }
-      const float m_tile = mx * sc;
+      // row max: four independent chains of three-input max
+      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int c = 0; c < kKT / 32; ++c)
+#pragma unroll
+        for (int e = 0; e < 32; e += 8)
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            mx4[t] = fmax3(mx4[t], __uint_as_float(s[c][e + 2 * t]), __uint_as_float(s[c][e + 2 * t + 1]));
+      const float m_tile = fmax3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3])) * sc;
       float m_new = m_run;
       if (j == 0 || m_tile > m_run + kRescaleThreshold) m_new = fmaxf(m_run, m_tile);
       if (j > 0) {
@@ -271,29 +280,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       }
       m_run = m_new;
       const float base = (m_run == -INFINITY) ? 0.0f : m_run;
-      // pass 2: p = 2^(s*sc - m) as bf16 pairs into the P columns
-      float lsum = 0.0f;
-#pragma unroll 1
+      // p = 2^(s*sc - m) two keys at a time, as bf16 pairs into the P columns
+      const float2 sc2 = make_float2(sc, sc), nb2 = make_float2(-base, -base);
+      float2 ls2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
+#pragma unroll
       for (int c = 0; c < kKT / 32; ++c) {
-        uint32_t rr[32];
-        tmem_ld32(tS + c * 32, rr);
-        tmem_ld_wait(rr);
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          float p0 = ex2_approx(fmaf(__uint_as_float(rr[e]), sc, -base));
-          float p1 = ex2_approx(fmaf(__uint_as_float(rr[e + 1]), sc, -base));
-          if (masked) {
-            const int key = k0 + c * 32 + e;
-            if (!(key >= lo && key < hi)) p0 = 0.0f;
-            if (!(key + 1 >= lo && key + 1 < hi)) p1 = 0.0f;
-          }
-          lsum += p0 + p1;
-          pk[e >> 1] = pack_bf16x2(p0, p1);
+          const float2 x =
+              __ffma2_rn(make_float2(__uint_as_float(s[c][e]), __uint_as_float(s[c][e + 1])), sc2, nb2);
+          const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+          ls2[(e >> 1) & 1] = __fadd2_rn(ls2[(e >> 1) & 1], p);
+          pk[e >> 1] = pack_bf16x2(p.x, p.y);
         }
         tmem_st16(tP + c * 16, pk);
       }
-      l_run += lsum;
+      l_run += (ls2[0].x + ls2[1].x) + (ls2[0].y + ls2[1].y);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(smem_u32(p_full + g));

@@ -2,8 +2,10 @@
 // bias / GELU(erf) / residual / 3-D RoPE / patch-embedding row remap of the encoder.
 //
 // A fragment is E consecutive columns n0 .. n0+E-1 (n0 even, E even) of output row m, held
-// by one thread. Both the tcgen05 GEMM (E = 32 from one TMEM load) and the fp32 SIMT GEMM
-// (E = 4) call epi_fragment, so the two precisions share one definition of each epilogue.
+// by one thread. The fp32 SIMT GEMM (E = 4) and the patch embedding of the tcgen05 GEMMs call
+// epi_fragment, which stores from registers; the other tcgen05 epilogues run the same bias /
+// GELU / RoPE arithmetic (epi_math_tc) on 32-column chunks and store through shared memory and
+// TMA (EpiStage).
 #pragma once
 #include <cuda_bf16.h>
 #include <cstdint>
@@ -55,6 +57,34 @@ __device__ __forceinline__ void rope_hd64_chunk(float (&v)[32], const float2* __
   }
 }
 
+// 3-D RoPE on E consecutive columns n0.. (n0 even) of token row p of an item, any even head width:
+// q columns [0, D) and k columns [D, 2D) are rotated, v columns pass.
+template <int E>
+__device__ __forceinline__ void rope_generic(const EpiArgs& a, int p, int n0, float (&v)[E]) {
+  const int D = a.n_head * a.head_dim;
+  const int d = a.rope_d, dh = d >> 1;
+  const float2* row = a.rope + (size_t)(p - a.prefix) * 3 * dh;
+  float r[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int n = n0 + e;
+    r[e] = v[e];
+    if (n < 2 * D) {
+      const int j = (n % D) % a.head_dim;  // dim inside the head
+      if (j < 3 * d) {
+        const int axis = j / d, jj = j - axis * d;
+        const int k = (a.rope_layout == 0) ? (jj % dh) : (jj >> 1);
+        const float2 cs = __ldg(row + axis * dh + k);
+        // x cos + rot90(x) sin, rot90(y1, y2) = (-y2, y1) on (even, odd) pairs
+        const float partner = v[e ^ 1];
+        r[e] = (jj & 1) ? fmaf(v[e], cs.x, partner * cs.y) : fmaf(v[e], cs.x, -partner * cs.y);
+      }
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < E; ++e) v[e] = r[e];
+}
+
 // OUT_BF16 selects bf16 storage of BIAS / GELU / QKV_ROPE (the bf16 path); RESIDUAL and PATCH
 // always store fp32 (the residual stream).
 template <int E, bool OUT_BF16>
@@ -96,30 +126,7 @@ __device__ __forceinline__ void epi_fragment(const EpiArgs& a, int m, int n0, fl
         done = true;
       }
     }
-    if (!done) {  // any even head width, any fragment (the fp32 SIMT GEMM)
-      const int D = a.n_head * a.head_dim;
-      const int d = a.rope_d, dh = d >> 1;
-      const float2* row = a.rope + (size_t)(p - a.prefix) * 3 * dh;
-      float r[E];
-#pragma unroll
-      for (int e = 0; e < E; ++e) {
-        const int n = n0 + e;
-        r[e] = v[e];
-        if (n < 2 * D) {
-          const int j = (n % D) % a.head_dim;  // dim inside the head
-          if (j < 3 * d) {
-            const int axis = j / d, jj = j - axis * d;
-            const int k = (a.rope_layout == 0) ? (jj % dh) : (jj >> 1);
-            const float2 cs = __ldg(row + axis * dh + k);
-            // x cos + rot90(x) sin, rot90(y1, y2) = (-y2, y1) on (even, odd) pairs
-            const float partner = v[e ^ 1];
-            r[e] = (jj & 1) ? fmaf(v[e], cs.x, partner * cs.y) : fmaf(v[e], cs.x, -partner * cs.y);
-          }
-        }
-      }
-#pragma unroll
-      for (int e = 0; e < E; ++e) v[e] = r[e];
-    }
+    if (!done) rope_generic<E>(a, p, n0, v);  // any even head width, any fragment (the fp32 SIMT GEMM)
   }
 
   if (a.kind == kEpiResidual) {
@@ -183,6 +190,106 @@ __device__ __forceinline__ void epi_fragment(const EpiArgs& a, int m, int n0, fl
       for (int e = 0; e < E; e += 4) *reinterpret_cast<float4*>(out + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
     } else {
       for (int e = 0; e < E && n0 + e < a.N; ++e) out[e] = v[e];
+    }
+  }
+}
+
+
+// ---------------------------------------------------------------- tensor-core GEMM epilogues
+// The tcgen05 GEMMs take the epilogue kind as a template argument (EK) so each kernel holds only
+// its own arithmetic. epi_math_tc applies the bias and then GELU or 3-D RoPE to 32 consecutive
+// columns n0.. of row m; the caller stages the result in shared memory and stores it with TMA.
+template <int EK>
+__device__ __forceinline__ void epi_math_tc(const EpiArgs& a, int m, int n0, float (&v)[32]) {
+  const float4* b4 = reinterpret_cast<const float4*>(a.bias + n0);  // n0 is warp-uniform: broadcast
+#pragma unroll
+  for (int e = 0; e < 32; e += 4) {
+    const float4 b = __ldg(b4 + e / 4);
+    v[e] += b.x;
+    v[e + 1] += b.y;
+    v[e + 2] += b.z;
+    v[e + 3] += b.w;
+  }
+  if constexpr (EK == kEpiGelu) {
+#pragma unroll
+    for (int e = 0; e < 32; ++e) v[e] = gelu_erf(v[e]);
+  } else if constexpr (EK == kEpiQkvRope) {
+    const int p = m % a.rows_per_item;
+    if (a.rope != nullptr && p >= a.prefix && n0 < 2 * a.n_head * a.head_dim) {
+      if (a.head_dim == 64) {
+        const float2* row = a.rope + (size_t)(p - a.prefix) * 30;
+        const bool upper = (n0 & 63) != 0;
+        if (a.rope_layout == 0) {
+          if (upper) rope_hd64_chunk<32, 0>(v, row); else rope_hd64_chunk<0, 0>(v, row);
+        } else {
+          if (upper) rope_hd64_chunk<32, 1>(v, row); else rope_hd64_chunk<0, 1>(v, row);
+        }
+      } else {
+        rope_generic<32>(a, p, n0, v);  // any even head width
+      }
+    }
+  }
+}
+
+// A warp's ring of two 2 KB shared-memory buffers, each 32 rows (one per lane) x 64 bytes, laid
+// out with the 64-byte TMA swizzle (16-byte unit u of row r at u ^ ((r >> 1) & 3)), so the
+// lanes' 16-byte writes hit distinct banks. put() stores the piece through the output tensor
+// map (box 64 bytes x 32 rows) at column x, row y, or adds it into global memory (fp32).
+struct EpiStage {
+  uint8_t* base;  // 1024-byte aligned, 4 KB
+  uint32_t n;     // pieces issued by this warp
+
+  __device__ __forceinline__ void put(int lane, const uint32_t (&w)[16], const CUtensorMap* tm, int x, int y,
+                                      bool add) {
+    uint8_t* buf = base + (n & 1u) * 2048u;
+    if (n >= 2) {  // the store issued two pieces ago read this buffer
+      if (lane == 0) bulk_wait_read<1>();
+      __syncwarp();
+    }
+    uint4* row = reinterpret_cast<uint4*>(buf + lane * 64);
+    const int sw = (lane >> 1) & 3;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) row[u ^ sw] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      if (add)
+        tma_reduce_add_2d(tm, smem_u32(buf), x, y);
+      else
+        tma_store_2d(tm, smem_u32(buf), x, y);
+      bulk_commit();
+    }
+    ++n;
+  }
+  // Every store of this warp complete (before the kernel exits).
+  __device__ __forceinline__ void finish(int lane) {
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+};
+
+// One 32-column chunk of row m (= first row y0 of the warp's slab + lane) of a tensor-core GEMM:
+// math, then staged store (bf16: one piece) or staged fp32 add into the residual stream (two).
+template <int EK>
+__device__ __forceinline__ void epi_chunk_tc(const EpiArgs& a, const CUtensorMap* tm_out, EpiStage& st, int lane,
+                                             int y0, int n0, float (&v)[32]) {
+  if constexpr (EK == kEpiPatch) {
+    epi_fragment<32, false>(a, y0 + lane, n0, v);
+  } else {
+    epi_math_tc<EK>(a, y0 + lane, n0, v);
+    if constexpr (EK == kEpiResidual) {
+      uint32_t w[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(v[e]);
+      st.put(lane, w, tm_out, n0, y0, true);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(v[16 + e]);
+      st.put(lane, w, tm_out, n0 + 16, y0, true);
+    } else {
+      uint32_t w[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) w[e] = pack_bf16x2(v[2 * e], v[2 * e + 1]);
+      st.put(lane, w, tm_out, n0, y0, false);
     }
   }
 }

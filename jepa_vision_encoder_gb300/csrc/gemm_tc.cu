@@ -9,8 +9,10 @@
 //               main loop of tile i+1
 //   warps 2..9  epilogue: two warps per TMEM lane quarter, each taking half of the tile's columns,
 //               32 at a time (the next tcgen05.ld in flight while one chunk is processed), then
-//               the fused bias / GELU / RoPE / residual / row remap of epilogue.cuh, stored from
-//               registers.
+//               the fused bias / GELU / RoPE of epilogue.cuh; each 32-row x 64-byte piece goes
+//               through a per-warp pair of swizzled shared-memory buffers to a TMA store (bf16
+//               outputs) or a TMA fp32 add into the residual stream. The patch embedding (rows
+//               remapped per item) stores from registers.
 // Every mbarrier wait is bounded (ptx.cuh); on the way out the producer drains its loads and the
 // MMA thread waits for its MMAs before TMEM is freed.
 #include <cuda_bf16.h>
@@ -32,14 +34,16 @@ struct GemmCfg {
   static constexpr int kBBytes = BN * kBK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kTmemCols = 2 * BN;
+  static constexpr int kEpiBytes = kEpiWarps * 4096;  // two 2 KB staging buffers per epilogue warp
   static constexpr int kBarBytes = 256;
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kEpiBytes + kBarBytes;
 };
 
-template <int BN, bool OUT_BF16>
+template <int BN, int EK>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, EpiArgs epi,
-                   int M, int N, int K, int* err, uint64_t limit_ns) {
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmO, EpiArgs epi, int M, int N, int K, int* err,
+                   uint64_t limit_ns) {
   using C = GemmCfg<BN>;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -47,7 +51,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = smem_raw + pad;
   uint8_t* sA = smem;
   uint8_t* sB = smem + S * C::kABytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * C::kStageBytes);
+  uint8_t* sEpi = smem + S * C::kStageBytes;  // kEpiWarps x 4 KB
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sEpi + C::kEpiBytes);
   uint64_t* full = bars;
   uint64_t* empty = bars + S;
   uint64_t* tfull = bars + 2 * S;
@@ -74,6 +79,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
+    if (EK != kEpiPatch) prefetch_tmap(&tmO);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
@@ -155,13 +161,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;                        // TMEM lane quarter this warp may access
     constexpr int kChunks = BN / 32 / 2;           // 32-column chunks per warp (half the tile)
     const int c0 = ((warp - 2) >> 2) * kChunks;    // first chunk of this warp's half
+    EpiStage stage{sEpi + (warp - 2) * 4096, 0};
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       const int m0 = (tile % num_m) * kBM, n0 = (tile / num_m) * BN;
       if (!mbar_wait(smem_u32(tfull + acc), acc_phase, wc)) break;
       tc_fence_after();
-      const int m = m0 + q * 32 + lane;
+      const int y0 = m0 + q * 32;
       const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
       uint32_t r[2][32];
       tmem_ld32(trow + c0 * 32, r[0]);
@@ -172,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float v[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[i & 1][e]);
-        epi_fragment<32, OUT_BF16>(epi, m, n0 + (c0 + i) * 32, v);
+        epi_chunk_tc<EK>(epi, &tmO, stage, lane, y0, n0 + (c0 + i) * 32, v);
       }
       tc_fence_before();
       __syncwarp();
@@ -182,6 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc_phase ^= 1u;
       }
     }
+    stage.finish(lane);
   }
   __syncthreads();
   if (warp == 1) {
@@ -217,52 +225,62 @@ int gemm_tc_pick_bn(int M, int N) {
 
 int gemm_tc_b_box(int bn) { return bn == kPairTile ? 128 : bn; }
 
-template <int BN, bool OUT_BF16>
-static cudaError_t launch_bn(const CUtensorMap& tmA, const CUtensorMap& tmB, const EpiArgs& epi, int M, int N,
-                             int K, int* err, uint64_t limit_ns, cudaStream_t s) {
+template <int BN, int EK>
+static cudaError_t launch_bn(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmO,
+                             const EpiArgs& epi, int M, int N, int K, int* err, uint64_t limit_ns, cudaStream_t s) {
   using C = GemmCfg<BN>;
   const int tiles = ((M + kBM - 1) / kBM) * (N / BN);
   const int grid = tiles < num_sms() ? tiles : num_sms();
-  gemm_tc_kernel<BN, OUT_BF16><<<grid, kThreads, C::kSmemBytes, s>>>(tmA, tmB, epi, M, N, K, err, limit_ns);
+  gemm_tc_kernel<BN, EK><<<grid, kThreads, C::kSmemBytes, s>>>(tmA, tmB, tmO, epi, M, N, K, err, limit_ns);
   return cudaGetLastError();
 }
 
-template <int BN, bool OUT_BF16>
+template <int BN>
+static cudaError_t launch_kind(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmO,
+                               const EpiArgs& epi, int M, int N, int K, int* err, uint64_t limit_ns, cudaStream_t s) {
+  switch (epi.kind) {
+    case kEpiBias: return launch_bn<BN, kEpiBias>(tmA, tmB, tmO, epi, M, N, K, err, limit_ns, s);
+    case kEpiGelu: return launch_bn<BN, kEpiGelu>(tmA, tmB, tmO, epi, M, N, K, err, limit_ns, s);
+    case kEpiResidual: return launch_bn<BN, kEpiResidual>(tmA, tmB, tmO, epi, M, N, K, err, limit_ns, s);
+    case kEpiQkvRope: return launch_bn<BN, kEpiQkvRope>(tmA, tmB, tmO, epi, M, N, K, err, limit_ns, s);
+    case kEpiPatch: return launch_bn<BN, kEpiPatch>(tmA, tmB, tmO, epi, M, N, K, err, limit_ns, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <int BN>
 static cudaError_t set_smem_attr() {
-  return cudaFuncSetAttribute(gemm_tc_kernel<BN, OUT_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              GemmCfg<BN>::kSmemBytes);
+  cudaError_t e = cudaSuccess;
+  auto set = [&](const void* f) {
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, GemmCfg<BN>::kSmemBytes);
+  };
+  set((const void*)gemm_tc_kernel<BN, kEpiBias>);
+  set((const void*)gemm_tc_kernel<BN, kEpiGelu>);
+  set((const void*)gemm_tc_kernel<BN, kEpiResidual>);
+  set((const void*)gemm_tc_kernel<BN, kEpiQkvRope>);
+  set((const void*)gemm_tc_kernel<BN, kEpiPatch>);
+  return e;
 }
 
 cudaError_t gemm_tc2_init_attributes();
 
 cudaError_t gemm_tc_init_attributes() {
   cudaError_t e = gemm_tc2_init_attributes();
-  if (e == cudaSuccess) e = set_smem_attr<256, true>();
-  if (e == cudaSuccess) e = set_smem_attr<256, false>();
-  if (e == cudaSuccess) e = set_smem_attr<128, true>();
-  if (e == cudaSuccess) e = set_smem_attr<128, false>();
-  if (e == cudaSuccess) e = set_smem_attr<64, true>();
-  if (e == cudaSuccess) e = set_smem_attr<64, false>();
+  if (e == cudaSuccess) e = set_smem_attr<256>();
+  if (e == cudaSuccess) e = set_smem_attr<128>();
+  if (e == cudaSuccess) e = set_smem_attr<64>();
   return e;
 }
 
-cudaError_t gemm_tc_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, int BN, const EpiArgs& epi, int M,
-                           int N, int K, int* err, uint64_t limit_ns, cudaStream_t s) {
+cudaError_t gemm_tc_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmO, int BN,
+                           const EpiArgs& epi, int M, int N, int K, int* err, uint64_t limit_ns, cudaStream_t s) {
   if (M <= 0) return cudaSuccess;
-  if (BN == kPairTile) return gemm_tc2_launch(tmA, tmB, epi, M, N, K, err, limit_ns, s);
-  const bool bf16_out = !(epi.kind == kEpiResidual || epi.kind == kEpiPatch);
+  if (BN == kPairTile) return gemm_tc2_launch(tmA, tmB, tmO, epi, M, N, K, err, limit_ns, s);
   switch (BN) {
-    case 256:
-      return bf16_out ? launch_bn<256, true>(tmA, tmB, epi, M, N, K, err, limit_ns, s)
-                      : launch_bn<256, false>(tmA, tmB, epi, M, N, K, err, limit_ns, s);
-    case 128:
-      return bf16_out ? launch_bn<128, true>(tmA, tmB, epi, M, N, K, err, limit_ns, s)
-                      : launch_bn<128, false>(tmA, tmB, epi, M, N, K, err, limit_ns, s);
-    case 64:
-      return bf16_out ? launch_bn<64, true>(tmA, tmB, epi, M, N, K, err, limit_ns, s)
-                      : launch_bn<64, false>(tmA, tmB, epi, M, N, K, err, limit_ns, s);
-    default:
-      return cudaErrorInvalidValue;
+    case 256: return launch_kind<256>(tmA, tmB, tmO, epi, M, N, K, err, limit_ns, s);
+    case 128: return launch_kind<128>(tmA, tmB, tmO, epi, M, N, K, err, limit_ns, s);
+    case 64: return launch_kind<64>(tmA, tmB, tmO, epi, M, N, K, err, limit_ns, s);
+    default: return cudaErrorInvalidValue;
   }
 }
 

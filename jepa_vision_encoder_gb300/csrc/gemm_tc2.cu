@@ -11,7 +11,8 @@
 //               CTA's stage barrier, which the even CTA arms with the bytes of both halves
 //   warp 1      even CTA: MMA issuer (odd CTA: idle)
 //   warps 2..9  epilogue of this CTA's 128 rows (two warps per TMEM lane quarter, half the
-//               columns each), releasing the accumulator with an arrive on the even CTA.
+//               columns each, stored through swizzled shared memory with TMA as in the 1-SM
+//               kernel), releasing the accumulator with an arrive on the even CTA.
 // Stage and accumulator hand-offs from the even CTA use multicast commits to both CTAs.
 // Every wait is bounded; the even CTA drains every stage phase it armed (both CTAs' copies)
 // and its MMAs, then both CTAs meet at a cluster barrier before TMEM is freed.
@@ -33,18 +34,21 @@ constexpr int kStageBytes = 2 * kHalfBytes;          // A half + B half
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t kTmemCols = 2 * kTileN;           // two accumulators
-constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 512;
+constexpr int kEpiBytes = kEpiWarps * 4096;          // two 2 KB staging buffers per epilogue warp
+constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kEpiBytes + 512;
 
-template <bool OUT_BF16>
+template <int EK>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, EpiArgs epi,
-                    int M, int N, int K, int* err, uint64_t limit_ns) {
+    gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmO, EpiArgs epi, int M, int N, int K, int* err,
+                    uint64_t limit_ns) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
   uint8_t* sA = smem;                              // kStages x 16 KB
   uint8_t* sB = smem + kStages * kHalfBytes;       // kStages x 16 KB
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint8_t* sEpi = smem + kStages * kStageBytes;    // kEpiWarps x 4 KB
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sEpi + kEpiBytes);
   uint64_t* full = bars;                           // own copies landed
   uint64_t* empty = bars + kStages;                // stage free (multicast from the even CTA)
   // bars + 2 * kStages .. + 3 * kStages: unused (keeps the layout of the barrier block)
@@ -74,6 +78,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     fence_mbar_init();
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
+    if (EK != kEpiPatch) prefetch_tmap(&tmO);
   }
   if (warp == 1) {
     tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
@@ -161,13 +166,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     constexpr int kChunks = kTileN / 32 / 2;   // 32-column chunks per warp (half the columns)
     const int c0 = ((warp - 2) >> 2) * kChunks;
     const uint32_t tempty_even = mapa_shared(smem_u32(tempty), 0);
+    EpiStage stage{sEpi + (warp - 2) * 4096, 0};
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = pair; tile < num_tiles; tile += num_pairs) {
       const int m0 = (tile % num_m) * kTileM + (int)rank * 128, n0 = (tile / num_m) * kTileN;
       if (!mbar_wait(smem_u32(tfull + acc), acc_phase, wc)) break;
       tc_fence_after();
-      const int m = m0 + q * 32 + lane;
+      const int y0 = m0 + q * 32;
       const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kTileN);
       uint32_t r[2][32];
       tmem_ld32(trow + c0 * 32, r[0]);
@@ -178,7 +184,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         float v[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[i & 1][e]);
-        epi_fragment<32, OUT_BF16>(epi, m, n0 + (c0 + i) * 32, v);
+        epi_chunk_tc<EK>(epi, &tmO, stage, lane, y0, n0 + (c0 + i) * 32, v);
       }
       tc_fence_before();
       __syncwarp();
@@ -188,6 +194,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         acc_phase ^= 1u;
       }
     }
+    stage.finish(lane);
   }
   tc_fence_before();
   __syncthreads();
@@ -201,9 +208,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 }  // namespace
 
 cudaError_t gemm_tc2_init_attributes() {
-  cudaError_t e = cudaFuncSetAttribute(gemm_tc2_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(gemm_tc2_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  cudaError_t e = cudaSuccess;
+  auto set = [&](const void* f) {
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  };
+  set((const void*)gemm_tc2_kernel<kEpiBias>);
+  set((const void*)gemm_tc2_kernel<kEpiGelu>);
+  set((const void*)gemm_tc2_kernel<kEpiResidual>);
+  set((const void*)gemm_tc2_kernel<kEpiQkvRope>);
+  set((const void*)gemm_tc2_kernel<kEpiPatch>);
   return e;
 }
 
@@ -216,7 +229,7 @@ int gemm_tc2_max_pairs() {
     cfg.gridDim = dim3(2 * (num_sms() / 2), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = kSmemBytes;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_tc2_kernel<true>, &cfg) != cudaSuccess || n <= 0) {
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_tc2_kernel<kEpiBias>, &cfg) != cudaSuccess || n <= 0) {
       cudaGetLastError();
       n = num_sms() / 2;
     }
@@ -225,18 +238,26 @@ int gemm_tc2_max_pairs() {
   return cached;
 }
 
-cudaError_t gemm_tc2_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const EpiArgs& epi, int M, int N, int K,
-                            int* err, uint64_t limit_ns, cudaStream_t s) {
+cudaError_t gemm_tc2_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmO,
+                            const EpiArgs& epi, int M, int N, int K, int* err, uint64_t limit_ns, cudaStream_t s) {
   if (M <= 0) return cudaSuccess;
   if (N % kTileN || K % kBK) return cudaErrorInvalidValue;
   const int tiles = ((M + kTileM - 1) / kTileM) * (N / kTileN);
   const int max_pairs = gemm_tc2_max_pairs();
   const int pairs = tiles < max_pairs ? tiles : max_pairs;
-  const bool bf16_out = !(epi.kind == kEpiResidual || epi.kind == kEpiPatch);
-  if (bf16_out)
-    gemm_tc2_kernel<true><<<2 * pairs, kThreads, kSmemBytes, s>>>(tmA, tmB, epi, M, N, K, err, limit_ns);
-  else
-    gemm_tc2_kernel<false><<<2 * pairs, kThreads, kSmemBytes, s>>>(tmA, tmB, epi, M, N, K, err, limit_ns);
+  const dim3 grid(2 * pairs), block(kThreads);
+  switch (epi.kind) {
+    case kEpiBias: gemm_tc2_kernel<kEpiBias><<<grid, block, kSmemBytes, s>>>(tmA, tmB, tmO, epi, M, N, K, err, limit_ns); break;
+    case kEpiGelu: gemm_tc2_kernel<kEpiGelu><<<grid, block, kSmemBytes, s>>>(tmA, tmB, tmO, epi, M, N, K, err, limit_ns); break;
+    case kEpiResidual:
+      gemm_tc2_kernel<kEpiResidual><<<grid, block, kSmemBytes, s>>>(tmA, tmB, tmO, epi, M, N, K, err, limit_ns);
+      break;
+    case kEpiQkvRope:
+      gemm_tc2_kernel<kEpiQkvRope><<<grid, block, kSmemBytes, s>>>(tmA, tmB, tmO, epi, M, N, K, err, limit_ns);
+      break;
+    case kEpiPatch: gemm_tc2_kernel<kEpiPatch><<<grid, block, kSmemBytes, s>>>(tmA, tmB, tmO, epi, M, N, K, err, limit_ns); break;
+    default: return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
 }
 

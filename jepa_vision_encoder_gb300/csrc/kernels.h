@@ -11,6 +11,9 @@ namespace jepa {
 // Encodes a 2-D bf16 tensor map (row-major [rows, cols], 128-byte swizzle, box = box_rows x 64).
 // Returns false if the driver refuses the map.
 bool make_tmap_2d_bf16(CUtensorMap* tm, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows);
+// GEMM output map: row-major [rows, cols] of bf16 (elem_bytes 2) or fp32 (4), box 32 rows x 64
+// bytes with the 64-byte swizzle (the epilogue's staging layout).
+bool make_tmap_2d_out(CUtensorMap* tm, const void* ptr, uint64_t rows, uint64_t cols, int elem_bytes);
 // 3-D map of a [B][N][cols] bf16 array with box 64 x box_rows x 1 (attention Q/K/V tiles).
 bool make_tmap_3d_bf16(CUtensorMap* tm, const void* ptr, uint64_t B, uint64_t N, uint64_t cols, uint32_t box_rows);
 
@@ -22,15 +25,16 @@ uint64_t default_wait_limit_ns();
 
 // tcgen05 GEMM: out = epilogue(A[M,K] * B[N,K]^T), bf16 operands. tmA box 128x64, tmB box
 // gemm_tc_b_box(BN) x 64 where BN = gemm_tc_pick_bn(M, N); BN == kPairTile selects the 2-SM
-// (cluster pair) kernel with 256 x 256 tiles.
+// (cluster pair) kernel with 256 x 256 tiles. tmO = make_tmap_2d_out over epi.out (bf16 for
+// BIAS / GELU / QKV_ROPE, fp32 for RESIDUAL; unused for PATCH, which stores from registers).
 constexpr int kPairTile = 512;
 int gemm_tc_pick_bn(int M, int N);
 int gemm_tc_b_box(int bn);
 int gemm_tc2_max_pairs();
-cudaError_t gemm_tc2_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const EpiArgs& epi, int M, int N, int K,
-                            int* err, uint64_t limit_ns, cudaStream_t s);
-cudaError_t gemm_tc_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, int BN, const EpiArgs& epi, int M,
-                           int N, int K, int* err, uint64_t limit_ns, cudaStream_t s);
+cudaError_t gemm_tc2_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmO,
+                            const EpiArgs& epi, int M, int N, int K, int* err, uint64_t limit_ns, cudaStream_t s);
+cudaError_t gemm_tc_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmO, int BN,
+                           const EpiArgs& epi, int M, int N, int K, int* err, uint64_t limit_ns, cudaStream_t s);
 
 // fp32 SIMT GEMM with the same epilogues.
 cudaError_t gemm_simt_launch(const float* A, const float* Bw, const EpiArgs& epi, int M, int N, int K,
