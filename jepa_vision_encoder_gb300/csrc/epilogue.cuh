@@ -23,7 +23,9 @@ struct EpiArgs {
   void* out;              // bf16 or fp32, leading dimension N (PATCH: D = N, remapped rows)
   // 3-D RoPE ("Architecture", 3-D RoPE): rows are tokens of items of rows_per_item tokens,
   // the first `prefix` of which are not rotated; q columns [0, D), k columns [D, 2D).
-  const float2* rope;     // [Np, 3, dh] (cos, sin) of the item's patch grid
+  const float2* rope;     // [Np, 3, dh] (cos, sin) of the item's patch grid, or
+  const float2* rope_axes;  // [gt + gh + gw, dh]: the t rows, then h, then w (used when not null)
+  int rope_gt, rope_gh, rope_gw;
   int rows_per_item, prefix, n_head, head_dim, rope_layout, rope_d;
   // patch embedding: input row m = patch i of item b (i = m % patches_per_item)
   int patches_per_item;
@@ -33,12 +35,49 @@ struct EpiArgs {
 
 __device__ __forceinline__ float gelu_erf(float x) { return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f)); }
 
+// GELU of the bf16 tensor-core epilogue, two values at a time in packed fp32 arithmetic.
+// q = Phi(-|x|) = erfc(z) / 2 with z = |x| / sqrt(2) is evaluated as exp(-z^2) * sum_k c_k z^k, a
+// fit of the scaled complementary error function (gelu_fit.py in this directory prints the
+// coefficients and the bound |q - Phi(-|x|)| <= 1.1e-6, far below bf16 rounding); z is clamped
+// at 7.5, where exp(-z^2) < 1e-24. Then GELU(x) = x (1 - q) for x >= 0 and x q for x < 0.
+__device__ __forceinline__ float2 gelu_fast2(float2 x) {
+  constexpr float c[9] = {5.0000000000e-01f, -5.6412470331e-01f, 4.9878799230e-01f, -3.6839867682e-01f,
+                          2.2596099097e-01f, -1.0779897437e-01f, 3.5892620358e-02f, -7.1522320417e-03f,
+                          6.2728129318e-04f};
+  constexpr float kRsqrt2 = 0.70710678118654752f, kNegLog2e = -1.4426950408889634f;
+  const float2 z = make_float2(fminf(fabsf(x.x) * kRsqrt2, 7.5f), fminf(fabsf(x.y) * kRsqrt2, 7.5f));
+  const float2 zz = __fmul2_rn(z, z);
+  float2 p = make_float2(c[8], c[8]);
+#pragma unroll
+  for (int k = 7; k >= 0; --k) p = __ffma2_rn(p, z, make_float2(c[k], c[k]));
+  const float2 q = __fmul2_rn(p, make_float2(ex2_approx(zz.x * kNegLog2e), ex2_approx(zz.y * kNegLog2e)));
+  const float2 f = make_float2(x.x >= 0.0f ? 1.0f - q.x : q.x, x.y >= 0.0f ? 1.0f - q.y : q.y);
+  return __fmul2_rn(x, f);
+}
+
+// The (cos, sin) rows (dh entries each) of the t, h and w axes of token row p of an item.
+__device__ __forceinline__ void rope_axis_rows(const EpiArgs& a, int p, int dh, const float2* (&r)[3]) {
+  const int pp = p - a.prefix;
+  if (a.rope_axes != nullptr) {
+    const int hw = a.rope_gh * a.rope_gw;
+    const int t = pp / hw, rem = pp - t * hw, h = rem / a.rope_gw, w = rem - h * a.rope_gw;
+    r[0] = a.rope_axes + (size_t)t * dh;
+    r[1] = a.rope_axes + (size_t)(a.rope_gt + h) * dh;
+    r[2] = a.rope_axes + (size_t)(a.rope_gt + a.rope_gh + w) * dh;
+  } else {
+    const float2* row = a.rope + (size_t)pp * 3 * dh;
+    r[0] = row;
+    r[1] = row + dh;
+    r[2] = row + 2 * dh;
+  }
+}
+
 // 3-D RoPE on 32 consecutive columns of one head of width 64 starting at head dim J0 (0 or 32):
 // d = 2*((64/3)/2) = 20 rotated dims per axis (t: 0-19, h: 20-39, w: 40-59), 60-63 untouched.
 // Every index is a compile-time constant; LAYOUT 0 = tiled (frequency j mod 10), 1 = interleaved
-// (frequency j / 2). row = the token's table [3][10] of (cos, sin).
+// (frequency j / 2). r = the token's (cos, sin) rows of its three axes, 10 entries each.
 template <int J0, int LAYOUT>
-__device__ __forceinline__ void rope_hd64_chunk(float (&v)[32], const float2* __restrict__ row) {
+__device__ __forceinline__ void rope_hd64_chunk(float (&v)[32], const float2* const (&r)[3]) {
 #pragma unroll
   for (int e = 0; e < 32; e += 2) {
     constexpr int kD = 20, kDh = 10;
@@ -47,8 +86,8 @@ __device__ __forceinline__ void rope_hd64_chunk(float (&v)[32], const float2* __
       const int axis = j / kD, jj = j - axis * kD;
       const int k0 = LAYOUT == 0 ? (jj % kDh) : (jj >> 1);
       const int k1 = LAYOUT == 0 ? ((jj + 1) % kDh) : ((jj + 1) >> 1);
-      const float2 c0 = __ldg(row + axis * kDh + k0);
-      const float2 c1 = __ldg(row + axis * kDh + k1);
+      const float2 c0 = __ldg(r[axis] + k0);
+      const float2 c1 = __ldg(r[axis] + k1);
       const float x0 = v[e], x1 = v[e + 1];
       // x cos + rot90(x) sin, rot90(y1, y2) = (-y2, y1): each member uses its own angle
       v[e] = fmaf(x0, c0.x, -x1 * c0.y);
@@ -63,7 +102,8 @@ template <int E>
 __device__ __forceinline__ void rope_generic(const EpiArgs& a, int p, int n0, float (&v)[E]) {
   const int D = a.n_head * a.head_dim;
   const int d = a.rope_d, dh = d >> 1;
-  const float2* row = a.rope + (size_t)(p - a.prefix) * 3 * dh;
+  const float2* rows[3];
+  rope_axis_rows(a, p, dh, rows);
   float r[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) {
@@ -74,7 +114,7 @@ __device__ __forceinline__ void rope_generic(const EpiArgs& a, int p, int n0, fl
       if (j < 3 * d) {
         const int axis = j / d, jj = j - axis * d;
         const int k = (a.rope_layout == 0) ? (jj % dh) : (jj >> 1);
-        const float2 cs = __ldg(row + axis * dh + k);
+        const float2 cs = __ldg(rows[axis] + k);
         // x cos + rot90(x) sin, rot90(y1, y2) = (-y2, y1) on (even, odd) pairs
         const float partner = v[e ^ 1];
         r[e] = (jj & 1) ? fmaf(v[e], cs.x, partner * cs.y) : fmaf(v[e], cs.x, -partner * cs.y);
@@ -108,19 +148,20 @@ __device__ __forceinline__ void epi_fragment(const EpiArgs& a, int m, int n0, fl
   if (a.kind == kEpiGelu) {
 #pragma unroll
     for (int e = 0; e < E; ++e) v[e] = gelu_erf(v[e]);
-  } else if (a.kind == kEpiQkvRope && a.rope != nullptr) {
+  } else if (a.kind == kEpiQkvRope && (a.rope != nullptr || a.rope_axes != nullptr)) {
     const int p = m % a.rows_per_item;
     bool done = p < a.prefix;  // prefix (CLS) rows are not rotated
     if constexpr (E == 32) {
       // tcgen05 GEMM fast path: a 32-column chunk is one half of one head of width 64
       if (!done && a.head_dim == 64 && (n0 & 31) == 0) {
         if (n0 < 2 * a.n_head * 64) {
-          const float2* row = a.rope + (size_t)(p - a.prefix) * 30;
+          const float2* rows[3];
+          rope_axis_rows(a, p, 10, rows);
           const bool upper = (n0 & 63) != 0;
           if (a.rope_layout == 0) {
-            if (upper) rope_hd64_chunk<32, 0>(v, row); else rope_hd64_chunk<0, 0>(v, row);
+            if (upper) rope_hd64_chunk<32, 0>(v, rows); else rope_hd64_chunk<0, 0>(v, rows);
           } else {
-            if (upper) rope_hd64_chunk<32, 1>(v, row); else rope_hd64_chunk<0, 1>(v, row);
+            if (upper) rope_hd64_chunk<32, 1>(v, rows); else rope_hd64_chunk<0, 1>(v, rows);
           }
         }
         done = true;
@@ -205,24 +246,31 @@ __device__ __forceinline__ void epi_math_tc(const EpiArgs& a, int m, int n0, flo
 #pragma unroll
   for (int e = 0; e < 32; e += 4) {
     const float4 b = __ldg(b4 + e / 4);
-    v[e] += b.x;
-    v[e + 1] += b.y;
-    v[e + 2] += b.z;
-    v[e + 3] += b.w;
+    const float2 lo = __fadd2_rn(make_float2(v[e], v[e + 1]), make_float2(b.x, b.y));
+    const float2 hi = __fadd2_rn(make_float2(v[e + 2], v[e + 3]), make_float2(b.z, b.w));
+    v[e] = lo.x;
+    v[e + 1] = lo.y;
+    v[e + 2] = hi.x;
+    v[e + 3] = hi.y;
   }
   if constexpr (EK == kEpiGelu) {
 #pragma unroll
-    for (int e = 0; e < 32; ++e) v[e] = gelu_erf(v[e]);
+    for (int e = 0; e < 32; e += 2) {
+      const float2 g = gelu_fast2(make_float2(v[e], v[e + 1]));
+      v[e] = g.x;
+      v[e + 1] = g.y;
+    }
   } else if constexpr (EK == kEpiQkvRope) {
     const int p = m % a.rows_per_item;
-    if (a.rope != nullptr && p >= a.prefix && n0 < 2 * a.n_head * a.head_dim) {
+    if ((a.rope != nullptr || a.rope_axes != nullptr) && p >= a.prefix && n0 < 2 * a.n_head * a.head_dim) {
       if (a.head_dim == 64) {
-        const float2* row = a.rope + (size_t)(p - a.prefix) * 30;
+        const float2* rows[3];
+        rope_axis_rows(a, p, 10, rows);
         const bool upper = (n0 & 63) != 0;
         if (a.rope_layout == 0) {
-          if (upper) rope_hd64_chunk<32, 0>(v, row); else rope_hd64_chunk<0, 0>(v, row);
+          if (upper) rope_hd64_chunk<32, 0>(v, rows); else rope_hd64_chunk<0, 0>(v, rows);
         } else {
-          if (upper) rope_hd64_chunk<32, 1>(v, row); else rope_hd64_chunk<0, 1>(v, row);
+          if (upper) rope_hd64_chunk<32, 1>(v, rows); else rope_hd64_chunk<0, 1>(v, rows);
         }
       } else {
         rope_generic<32>(a, p, n0, v);  // any even head width
@@ -291,6 +339,102 @@ __device__ __forceinline__ void epi_chunk_tc(const EpiArgs& a, const CUtensorMap
       for (int e = 0; e < 16; ++e) w[e] = pack_bf16x2(v[2 * e], v[2 * e + 1]);
       st.put(lane, w, tm_out, n0, y0, false);
     }
+  }
+}
+
+// RoPE of one 32-column half (J0 = 0: head dims 0-31, J0 = 32: dims 32-63) of a width-64 head,
+// with the row's (cos, sin) values already in registers: cs[axis][k].
+template <int J0, int LAYOUT>
+__device__ __forceinline__ void rope_hd64_regs(float (&v)[32], const float2 (&cs)[3][10]) {
+#pragma unroll
+  for (int e = 0; e < 32; e += 2) {
+    constexpr int kD = 20, kDh = 10;
+    const int j = J0 + e;
+    if (j < 3 * kD) {
+      const int axis = j / kD, jj = j - axis * kD;
+      const int k0 = LAYOUT == 0 ? (jj % kDh) : (jj >> 1);
+      const int k1 = LAYOUT == 0 ? ((jj + 1) % kDh) : ((jj + 1) >> 1);
+      const float x0 = v[e], x1 = v[e + 1];
+      v[e] = fmaf(x0, cs[axis][k0].x, -x1 * cs[axis][k0].y);
+      v[e + 1] = fmaf(x1, cs[axis][k1].x, x0 * cs[axis][k1].y);
+    }
+  }
+}
+
+// QKV epilogue of a warp whose chunks are all head halves J0 (chunks 2i + J0/32 of the tile): the
+// row's (cos, sin) values for the two axes those dims use are loaded once per tile, then every
+// chunk rotates from registers.
+template <int J0, int NCHUNK>
+__device__ __forceinline__ void epi_warp_qkv_hd64(const EpiArgs& a, const CUtensorMap* tm, EpiStage& st, int lane,
+                                                  uint32_t trow, int y0, int n_tile0) {
+  constexpr int kA0 = J0 == 0 ? 0 : 1;  // axes touched by this half: t, h (J0 = 0) or h, w (J0 = 32)
+  const int p = (y0 + lane) % a.rows_per_item;
+  const bool rot = (a.rope != nullptr || a.rope_axes != nullptr) && p >= a.prefix;
+  float2 cs[3][10];
+#pragma unroll
+  for (int ax = 0; ax < 3; ++ax)
+#pragma unroll
+    for (int k = 0; k < 10; ++k) cs[ax][k] = make_float2(1.0f, 0.0f);
+  if (rot) {
+    const float2* rows[3];
+    rope_axis_rows(a, p, 10, rows);
+#pragma unroll
+    for (int ax = kA0; ax < kA0 + 2; ++ax)
+#pragma unroll
+      for (int k = 0; k < 10; ++k) cs[ax][k] = __ldg(rows[ax] + k);
+  }
+  const int qk_cols = 2 * a.n_head * 64;
+  uint32_t r[2][32];
+  tmem_ld32(trow + (J0 / 32) * 32, r[0]);
+#pragma unroll
+  for (int i = 0; i < NCHUNK; ++i) {
+    const int c = 2 * i + J0 / 32;
+    tmem_ld_wait(r[i & 1]);
+    if (i + 1 < NCHUNK) tmem_ld32(trow + (c + 2) * 32, r[(i + 1) & 1]);
+    float v[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[i & 1][e]);
+    const int n0 = n_tile0 + c * 32;
+    epi_math_tc<kEpiBias>(a, y0 + lane, n0, v);
+    if (n0 < qk_cols) {  // q and k columns rotate (warp-uniform); v columns pass
+      if (a.rope_layout == 0)
+        rope_hd64_regs<J0, 0>(v, cs);
+      else
+        rope_hd64_regs<J0, 1>(v, cs);
+    }
+    uint32_t w[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) w[e] = pack_bf16x2(v[2 * e], v[2 * e + 1]);
+    st.put(lane, w, tm, n0, y0, false);
+  }
+}
+
+// The epilogue of one warp for one accumulator tile: NCHUNK 32-column chunks of its 32 TMEM lanes
+// (rows y0 .. y0+31), the next tcgen05.ld in flight while a chunk is processed. half selects which
+// chunks: 0 or 1 of the warp pair sharing the lane quarter.
+template <int EK, int NCHUNK>
+__device__ __forceinline__ void epi_warp_tile(const EpiArgs& a, const CUtensorMap* tm, EpiStage& st, int lane,
+                                              uint32_t trow, int y0, int n_tile0, int half) {
+  if constexpr (EK == kEpiQkvRope) {
+    if (a.head_dim == 64) {  // heads never straddle a 64-column boundary: chunk parity = head half
+      if (half == 0)
+        epi_warp_qkv_hd64<0, NCHUNK>(a, tm, st, lane, trow, y0, n_tile0);
+      else
+        epi_warp_qkv_hd64<32, NCHUNK>(a, tm, st, lane, trow, y0, n_tile0);
+      return;
+    }
+  }
+  const int c0 = half * NCHUNK;
+  uint32_t r[2][32];
+  tmem_ld32(trow + c0 * 32, r[0]);
+#pragma unroll
+  for (int i = 0; i < NCHUNK; ++i) {
+    tmem_ld_wait(r[i & 1]);
+    if (i + 1 < NCHUNK) tmem_ld32(trow + (c0 + i + 1) * 32, r[(i + 1) & 1]);
+    float v[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[i & 1][e]);
+    epi_chunk_tc<EK>(a, tm, st, lane, y0, n_tile0 + (c0 + i) * 32, v);
   }
 }
 

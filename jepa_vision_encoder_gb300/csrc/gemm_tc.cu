@@ -7,8 +7,10 @@
 //   warp 1      MMA issuer: 4 x tcgen05.mma (M=128, N=BN, K=16) per stage into one of two
 //               TMEM accumulators (2 x BN columns), so the epilogue of tile i overlaps the
 //               main loop of tile i+1
-//   warps 2..9  epilogue: two warps per TMEM lane quarter, each taking half of the tile's columns,
-//               32 at a time (the next tcgen05.ld in flight while one chunk is processed), then
+//   warps 2..9  epilogue: two warps per TMEM lane quarter, each taking half of the tile's columns
+//               (for QKV, alternate 32-column chunks, so a warp meets one half of every head and
+//               keeps that half's RoPE (cos, sin) row in registers), 32 columns at a time (the
+//               next tcgen05.ld in flight while one chunk is processed), then
 //               the fused bias / GELU / RoPE of epilogue.cuh; each 32-row x 64-byte piece goes
 //               through a per-warp pair of swizzled shared-memory buffers to a TMA store (bf16
 //               outputs) or a TMA fp32 add into the residual stream. The patch embedding (rows
@@ -160,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     const int q = warp & 3;                        // TMEM lane quarter this warp may access
     constexpr int kChunks = BN / 32 / 2;           // 32-column chunks per warp (half the tile)
-    const int c0 = ((warp - 2) >> 2) * kChunks;    // first chunk of this warp's half
+    const int half = (warp - 2) >> 2;              // which of the two warps on this lane quarter
     EpiStage stage{sEpi + (warp - 2) * 4096, 0};
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -170,17 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int y0 = m0 + q * 32;
       const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-      uint32_t r[2][32];
-      tmem_ld32(trow + c0 * 32, r[0]);
-#pragma unroll
-      for (int i = 0; i < kChunks; ++i) {
-        tmem_ld_wait(r[i & 1]);
-        if (i + 1 < kChunks) tmem_ld32(trow + (c0 + i + 1) * 32, r[(i + 1) & 1]);
-        float v[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[i & 1][e]);
-        epi_chunk_tc<EK>(epi, &tmO, stage, lane, y0, n0 + (c0 + i) * 32, v);
-      }
+      epi_warp_tile<EK, kChunks>(epi, &tmO, stage, lane, trow, y0, n0, half);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(tempty + acc));

@@ -164,7 +164,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else {
     const int q = warp & 3;                    // TMEM lane quarter this warp may access
     constexpr int kChunks = kTileN / 32 / 2;   // 32-column chunks per warp (half the columns)
-    const int c0 = ((warp - 2) >> 2) * kChunks;
+    const int half = (warp - 2) >> 2;  // which of the two warps on this lane quarter
     const uint32_t tempty_even = mapa_shared(smem_u32(tempty), 0);
     EpiStage stage{sEpi + (warp - 2) * 4096, 0};
     int acc = 0;
@@ -175,17 +175,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int y0 = m0 + q * 32;
       const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kTileN);
-      uint32_t r[2][32];
-      tmem_ld32(trow + c0 * 32, r[0]);
-#pragma unroll
-      for (int i = 0; i < kChunks; ++i) {
-        tmem_ld_wait(r[i & 1]);
-        if (i + 1 < kChunks) tmem_ld32(trow + (c0 + i + 1) * 32, r[(i + 1) & 1]);
-        float v[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[i & 1][e]);
-        epi_chunk_tc<EK>(epi, &tmO, stage, lane, y0, n0 + (c0 + i) * 32, v);
-      }
+      epi_warp_tile<EK, kChunks>(epi, &tmO, stage, lane, trow, y0, n0, half);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(tempty_even + (uint32_t)(acc * sizeof(uint64_t)));

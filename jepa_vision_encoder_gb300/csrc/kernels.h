@@ -58,6 +58,9 @@ cudaError_t layernorm_launch(const float* x, int M, int D, const float* g, const
                              bool out_bf16, void* y, cudaStream_t s);
 cudaError_t rope_table_launch(int gt, int gh, int gw, int head_dim, float theta, int interpolate, int ref_grid,
                               float2* table, cudaStream_t s);
+// The same entries factored per axis: [gt + gh + gw][d/2] (t rows, then h, then w).
+cudaError_t rope_axes_launch(int gt, int gh, int gw, int head_dim, float theta, int interpolate, int ref_grid,
+                             float2* axes, cudaStream_t s);
 // X rows b*N + r for r < prefix: cls (+ pos[r]) (+ vec).
 cudaError_t prefix_rows_launch(float* X, int B, int N, int D, const float* cls, const float* pos,
                                const float* vec, cudaStream_t s);

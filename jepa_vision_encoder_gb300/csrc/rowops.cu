@@ -186,31 +186,52 @@ cudaError_t layernorm_launch(const float* x, int M, int D, const float* g, const
 // ------------------------------------------------------------------ 3-D RoPE table
 // ("Architecture", 3-D RoPE): patch i at (t, h, w) = (i / (gh gw), (i % (gh gw)) / gw, i % gw),
 // h and w rescaled by (ref - 1) / (g - 1) under interpolate_rope; omega_k = theta^(-2k/d).
-// table[i][axis][k] = (cos, sin)(pos_axis * omega_k), computed in double.
+// table[i][axis][k] = (cos, sin)(pos_axis * omega_k), computed in double. The encoder itself uses
+// the factored form axes[c][k] over the t coordinates, then h, then w (gt + gh + gw rows): the
+// same entries, computed by the same function, in 3 KB instead of one row per token.
 namespace {
+__device__ __forceinline__ float2 rope_entry(int axis, int coord, int g, int d, int k, double theta, int interp,
+                                             int ref) {
+  double pos = (double)coord;
+  if (axis > 0 && interp && g > 1) pos *= (double)(ref - 1) / (double)(g - 1);
+  const double omega = 1.0 / pow(theta, 2.0 * k / (double)d);
+  double sn, cs;
+  sincos(pos * omega, &sn, &cs);
+  return make_float2((float)cs, (float)sn);
+}
+
 __global__ void rope_table_kernel(int gt, int gh, int gw, int d, double theta, int interp, int ref,
                                   float2* __restrict__ table) {
   const int dh = d / 2;
   const int total = gt * gh * gw * 3 * dh;
   for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += gridDim.x * blockDim.x) {
     const int k = idx % dh, axis = (idx / dh) % 3, i = idx / (3 * dh);
-    double pos;
-    if (axis == 0) {
-      pos = (double)(i / (gh * gw));
-    } else if (axis == 1) {
-      pos = (double)((i % (gh * gw)) / gw);
-      if (interp && gh > 1) pos *= (double)(ref - 1) / (double)(gh - 1);
-    } else {
-      pos = (double)(i % gw);
-      if (interp && gw > 1) pos *= (double)(ref - 1) / (double)(gw - 1);
-    }
-    const double omega = 1.0 / pow(theta, 2.0 * k / (double)d);
-    double sn, cs;
-    sincos(pos * omega, &sn, &cs);
-    table[idx] = make_float2((float)cs, (float)sn);
+    const int coord = axis == 0 ? i / (gh * gw) : (axis == 1 ? (i % (gh * gw)) / gw : i % gw);
+    table[idx] = rope_entry(axis, coord, axis == 0 ? gt : (axis == 1 ? gh : gw), d, k, theta, interp, ref);
+  }
+}
+
+__global__ void rope_axes_kernel(int gt, int gh, int gw, int d, double theta, int interp, int ref,
+                                 float2* __restrict__ axes) {
+  const int dh = d / 2;
+  const int total = (gt + gh + gw) * dh;
+  for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += gridDim.x * blockDim.x) {
+    const int k = idx % dh, row = idx / dh;
+    const int axis = row < gt ? 0 : (row < gt + gh ? 1 : 2);
+    const int coord = axis == 0 ? row : (axis == 1 ? row - gt : row - gt - gh);
+    axes[idx] = rope_entry(axis, coord, axis == 0 ? gt : (axis == 1 ? gh : gw), d, k, theta, interp, ref);
   }
 }
 }  // namespace
+
+cudaError_t rope_axes_launch(int gt, int gh, int gw, int head_dim, float theta, int interpolate, int ref_grid,
+                             float2* axes, cudaStream_t s) {
+  const int d = 2 * ((head_dim / 3) / 2);
+  const int total = (gt + gh + gw) * (d / 2);
+  if (total <= 0) return cudaSuccess;
+  rope_axes_kernel<<<grid_for(total, 256), 256, 0, s>>>(gt, gh, gw, d, (double)theta, interpolate, ref_grid, axes);
+  return cudaGetLastError();
+}
 
 cudaError_t rope_table_launch(int gt, int gh, int gw, int head_dim, float theta, int interpolate, int ref_grid,
                               float2* table, cudaStream_t s) {

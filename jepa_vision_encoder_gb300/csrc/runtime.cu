@@ -583,8 +583,8 @@ jepa_status prepare_shape(jepa_context* c, int B, int T, int H, int W, const Geo
     c->bn_down = gemm_tc_pick_bn((int)M, D);
   }
   if (hp.pos_type == JEPA_POS_ROPE3D) {
-    CUDA_TRY(rope_table_launch(g.gt, g.gh, g.gw, D / hp.n_head, hp.rope_theta, hp.rope_interpolate,
-                               hp.rope_ref_grid, c->rope, c->stream));
+    CUDA_TRY(rope_axes_launch(g.gt, g.gh, g.gw, D / hp.n_head, hp.rope_theta, hp.rope_interpolate,
+                              hp.rope_ref_grid, c->rope, c->stream));
   }
   c->kB = B;
   c->kT = T;
@@ -721,7 +721,10 @@ jepa_status launch_encode(jepa_context* c, const float* pix, int B, int T, int H
     qe.head_dim = hd;
     qe.rope_layout = hp.rope_layout;
     qe.rope_d = rope_d(hd);
-    qe.rope = hp.pos_type == JEPA_POS_ROPE3D ? c->rope : nullptr;
+    qe.rope_axes = hp.pos_type == JEPA_POS_ROPE3D ? c->rope : nullptr;
+    qe.rope_gt = g.gt;
+    qe.rope_gh = g.gh;
+    qe.rope_gw = g.gw;
     EpiArgs oe = make_epi(kEpiResidual, M, D, w.b_out, c->X);
     EpiArgs ue = make_epi(kEpiGelu, M, F, w.b_up, c->Hh);
     EpiArgs de = make_epi(kEpiResidual, M, D, w.b_down, c->X);
