@@ -11,8 +11,9 @@
 //               warp rescales its O rows in TMEM. At the end o = O / l is stored as bf16.
 //   warp 8      TMA: Q0 and Q1 once, then K and V tiles of 128 keys into a 3-stage ring
 //               (3-D tensor map over qkv [B][N][3D]: rows beyond N read as zeros).
-//   warp 9      MMA, interleaving the two tiles so the tensor core works on one tile while the
-//               other tile's softmax runs:  ... PV0(j), S0(j+1), PV1(j), S1(j+1) ...
+//   warp 9      MMA, per tile g and key tile j: S_g(j+1) = Q_g K(j+1)^T as soon as warpgroup g has
+//               read S_g(j) into registers (so the next scores are ready when its softmax ends),
+//               then O_g += P_g(j) V(j) once P_g(j) is in TMEM; the two tiles alternate.
 //               S = Q K^T: M128 N128 K16 x4 (both K-major); O += P V: M128 N64 K16 x8 with P
 //               read from TMEM and V MN-major in shared memory.
 // TMEM (512 columns): S0 [0,128) S1 [128,256) P0 [256,320) P1 [320,384) O0 [384,448) O1 [448,512).
@@ -83,7 +84,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   uint64_t* p_full = s_full + 2;                // [2]
   uint64_t* o_done = s_full + 4;                // [2]
   uint64_t* mma_done = s_full + 6;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 7);
+  uint64_t* s_free = s_full + 7;                // [2]: the warpgroup has read S into registers
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 9);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -100,6 +102,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       mbar_init(smem_u32(s_full + g), 1);
       mbar_init(smem_u32(p_full + g), 128);
       mbar_init(smem_u32(o_done + g), 1);
+      mbar_init(smem_u32(s_free + g), 4);
     }
     mbar_init(smem_u32(mma_done), 1);
     *abort_flag = 0;
@@ -145,21 +148,24 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, kKT, 0, 0);
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, kHD, 0, 1);
-      const uint32_t qa[2] = {smem_u32(sQ), smem_u32(sQ + kTileBytes)};
+      // descriptors built once; a K step or a stage only moves the start address (the issue
+      // loop stays short enough to keep the tensor pipe fed with these small MMAs)
+      const uint64_t q_desc = smem_desc_sw128(smem_u32(sQ), 1024, 1024);
+      const uint64_t k_desc = smem_desc_sw128(smem_u32(sK), 1024, 1024);
+      const uint64_t v_desc = smem_desc_sw128(smem_u32(sV), 1024, 1024);
       auto issue_s = [&](int g, int st) {
-        const uint32_t k_addr = smem_u32(sK + st * kTileBytes);
+        const uint64_t qd = desc_advance(q_desc, g * kTileBytes), kd = desc_advance(k_desc, st * kTileBytes);
+        const uint32_t d = tmem + kColS + g * 128;
 #pragma unroll
-        for (int k = 0; k < kHD / 16; ++k)
-          mma_ss(tmem + kColS + g * 128, smem_desc_sw128(qa[g] + k * 32, 1024, 1024),
-                 smem_desc_sw128(k_addr + k * 32, 1024, 1024), idesc_s, k != 0 ? 1u : 0u);
+        for (int k = 0; k < kHD / 16; ++k) mma_ss(d, desc_advance(qd, k * 32), desc_advance(kd, k * 32), idesc_s, k != 0);
         mma_commit(smem_u32(s_full + g));
       };
       auto issue_pv = [&](int g, int st, int j) {
-        const uint32_t v_addr = smem_u32(sV + st * kTileBytes);
+        const uint64_t vd = desc_advance(v_desc, st * kTileBytes);
+        const uint32_t d = tmem + kColO + g * 64, p = tmem + kColP + g * 64;
 #pragma unroll
         for (int k = 0; k < kKT / 16; ++k)
-          mma_ts(tmem + kColO + g * 64, tmem + kColP + g * 64 + k * 8,
-                 smem_desc_sw128(v_addr + k * 2048, 1024, 1024), idesc_o, (j > 0 || k > 0) ? 1u : 0u);
+          mma_ts(d, p + k * 8, desc_advance(vd, k * 2048), idesc_o, (j > 0 || k > 0) ? 1u : 0u);
         mma_commit(smem_u32(o_done + g));
       };
       bool ok = num_kt > 0 && mbar_wait(smem_u32(q_full), 0, wc) && mbar_wait(smem_u32(kv_full), 0, wc);
@@ -174,21 +180,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         const int nst = (stage + 1 == kKvStages) ? 0 : stage + 1;
         const uint32_t nph = (stage + 1 == kKvStages) ? (phase ^ 1u) : phase;
         const bool more = j + 1 < num_kt;
-        // tile 0: P0 V(j), then S0 of the next key tile
-        if (!(ok = mbar_wait(smem_u32(p_full), (uint32_t)(j & 1), wc))) break;
-        tc_fence_after();
-        issue_pv(0, stage, j);
-        if (more) {
-          if (!(ok = mbar_wait(smem_u32(kv_full + nst), nph, wc))) break;
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+          // S_g(j+1) as soon as the warpgroup holds S_g(j) in registers (while it computes P),
+          // then P_g(j) V(j) once P is in TMEM
+          if (more) {
+            if (!(ok = mbar_wait(smem_u32(s_free + g), (uint32_t)(j & 1), wc))) break;
+            if (g == 0 && !(ok = mbar_wait(smem_u32(kv_full + nst), nph, wc))) break;
+            tc_fence_after();
+            issue_s(g, nst);
+          }
+          if (!(ok = mbar_wait(smem_u32(p_full + g), (uint32_t)(j & 1), wc))) break;
           tc_fence_after();
-          issue_s(0, nst);
+          issue_pv(g, stage, j);
         }
-        // tile 1
-        if (!(ok = mbar_wait(smem_u32(p_full + 1), (uint32_t)(j & 1), wc))) break;
-        tc_fence_after();
-        issue_pv(1, stage, j);
+        if (!ok) break;
         mma_commit(smem_u32(kv_empty + stage));  // K(j), V(j) no longer read once these complete
-        if (more) issue_s(1, nst);
         stage = nst;
         phase = nph;
       }
@@ -233,6 +240,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       tmem_ld_wait(s[0]);
 #pragma unroll
       for (int c = 1; c < kKT / 32; ++c) tmem_ld_bind(s[c]);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(s_free + g));  // the MMA warp may overwrite S now
       if (masked) {  // invisible keys score -inf: they lose the max and give p = 0
 #pragma unroll
         for (int c = 0; c < kKT / 32; ++c)

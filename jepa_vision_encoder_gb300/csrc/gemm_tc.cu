@@ -123,6 +123,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN, 0, 0);
+      const uint64_t a_desc = smem_desc_sw128(smem_u32(sA), 1024, 1024);  // stage 0; stages and K
+      const uint64_t b_desc = smem_desc_sw128(smem_u32(sB), 1024, 1024);  // steps move the address
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
@@ -136,13 +138,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(sA + stage * C::kABytes), b0 = smem_u32(sB + stage * C::kBBytes);
+          const uint64_t ad = desc_advance(a_desc, stage * C::kABytes), bd = desc_advance(b_desc, stage * C::kBBytes);
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k) {
-            const uint64_t ad = smem_desc_sw128(a0 + k * 32, 1024, 1024);
-            const uint64_t bd = smem_desc_sw128(b0 + k * 32, 1024, 1024);
-            mma_ss(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
-          }
+          for (int k = 0; k < kBK / 16; ++k)
+            mma_ss(d_tmem, desc_advance(ad, k * 32), desc_advance(bd, k * 32), idesc, (kb | k) != 0 ? 1u : 0u);
           mma_commit(smem_u32(empty + stage));
           if (++stage == S) {
             stage = 0;

@@ -127,6 +127,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (lane == 0 && rank == 0) {
       // even CTA: the MMA issuer of the pair
       constexpr uint32_t idesc = idesc_bf16_f32(kTileM, kTileN, 0, 0);
+      const uint64_t a_desc = smem_desc_sw128(smem_u32(sA), 1024, 1024);  // stage 0; stages and K
+      const uint64_t b_desc = smem_desc_sw128(smem_u32(sB), 1024, 1024);  // steps move the address
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
@@ -140,11 +142,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(sA + stage * kHalfBytes), b0 = smem_u32(sB + stage * kHalfBytes);
+          const uint64_t ad = desc_advance(a_desc, stage * kHalfBytes), bd = desc_advance(b_desc, stage * kHalfBytes);
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k)
-            mma_ss_pair(d_tmem, smem_desc_sw128(a0 + k * 32, 1024, 1024), smem_desc_sw128(b0 + k * 32, 1024, 1024),
-                        idesc, (kb | k) != 0 ? 1u : 0u);
+            mma_ss_pair(d_tmem, desc_advance(ad, k * 32), desc_advance(bd, k * 32), idesc, (kb | k) != 0 ? 1u : 0u);
           mma_commit_pair_mc(smem_u32(empty + stage), 0x3);
           if (++stage == kStages) {
             stage = 0;

@@ -256,6 +256,10 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
+// The descriptor of the same layout `bytes` further on (a multiple of 16): only the start-address
+// field changes, and it cannot carry out of its 14 bits for addresses inside shared memory.
+__device__ __forceinline__ uint64_t desc_advance(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
+
 // Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator (bits 4-5 = 1),
 // A and B bf16 (bits 7-9 = 1, 10-12 = 1), A/B major (bits 15, 16: 0 = K-major, 1 = MN-major),
 // N >> 3 (bits 17-22), M >> 4 (bits 24-28).
