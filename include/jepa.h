@@ -128,6 +128,11 @@ jepa_status jepa_context_set_stream(jepa_context* c, void* stream);
  * CUDA graph on first use and replay it afterwards ("Architecture", GPU backend: graph replay).
  * The context stream must then not be the legacy default stream. */
 jepa_status jepa_context_set_graph(jepa_context* c, int32_t enable);
+/* enable != 0 (the default): the encode's kernels go out as programmatic dependent launches, so
+ * each kernel's set-up (barriers, TMEM, tensor-map prefetch) overlaps the end of the previous
+ * one; every kernel waits for its predecessor before touching shared data, so results do not
+ * change. Launches are ordinary while per-kernel profiling is on. */
+jepa_status jepa_context_set_pdl(jepa_context* c, int32_t enable);
 jepa_status jepa_context_workspace_bytes(const jepa_context* c, size_t* out);
 /* Kernel launches one jepa_encode of this shape issues (graph replay counts the kernels inside). */
 jepa_status jepa_context_launches(const jepa_context* c, int32_t B, int32_t T, int32_t H, int32_t W,

@@ -154,6 +154,10 @@ class Context:
     def set_graph(self, enable: bool):
         check(lib().jepa_context_set_graph(self._h, int(enable)))
 
+    def set_pdl(self, enable: bool):
+        """Programmatic dependent launches between the encode's kernels (on by default)."""
+        check(lib().jepa_context_set_pdl(self._h, int(enable)))
+
     @property
     def workspace_bytes(self) -> int:
         n = ctypes.c_size_t()

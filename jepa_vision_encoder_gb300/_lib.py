@@ -64,6 +64,7 @@ SIGNATURES = {
     "jepa_context_free": (None, [_P]),
     "jepa_context_set_stream": (_I, [_P, _P]),
     "jepa_context_set_graph": (_I, [_P, _I]),
+    "jepa_context_set_pdl": (_I, [_P, _I]),
     "jepa_context_workspace_bytes": (_I, [_P, ctypes.POINTER(_SZ)]),
     "jepa_context_launches": (_I, [_P, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_int32)]),
     "jepa_encode": (_I, [_P, _P, _I, _I, _I, _I, _I, _P]),

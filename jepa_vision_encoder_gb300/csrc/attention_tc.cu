@@ -118,6 +118,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtl wc{abort_flag, a.err, a.limit_ns};
+  pdl_trigger();
+  pdl_wait();  // qkv comes from the previous kernel; the output may still be read by older ones
 
   if (warp == 8) {
     if (lane == 0) {
@@ -374,8 +376,7 @@ cudaError_t attention_tc_launch(const CUtensorMap& tmQKV, const AttnParams& p, i
   a.err = err;
   a.limit_ns = limit_ns;
   dim3 grid((p.N + 2 * kQT - 1) / (2 * kQT), p.H, p.B);
-  attn_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(tmQKV, a);
-  return cudaGetLastError();
+  return launch_kernel(attn_tc_kernel, grid, dim3(kThreads), kSmemBytes, s, tmQKV, a);
 }
 
 }  // namespace jepa

@@ -2,7 +2,8 @@
 // operands, fp32 accumulation in tensor memory. Every linear layer of the encoder runs here
 // ("Architecture", The shared ViT graph: patch embed, fused qkv, out-projection, FFN).
 //
-// Warp roles (320 threads, one CTA per SM, grid = min(tiles, SMs), tiles strided over CTAs):
+// Warp roles (320 threads, one CTA per SM, grid = min(tiles, SMs), tiles strided over CTAs and
+// numbered N-fastest, so the CTAs working at the same time share rows of A and sweep the weights):
 //   warp 0      TMA producer: A tile 128x64 and B tile BNx64 per stage (128-byte swizzle)
 //   warp 1      MMA issuer: 4 x tcgen05.mma (M=128, N=BN, K=16) per stage into one of two
 //               TMEM accumulators (2 x BN columns), so the epilogue of tile i overlaps the
@@ -92,6 +93,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const WaitCtl wc{abort_flag, err, limit_ns};
+  pdl_trigger();
+  pdl_wait();  // A and the residual stream come from earlier kernels
 
   if (warp == 0) {
     if (lane == 0) {
@@ -99,7 +102,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0, armed = 0, armed_phase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        const int m0 = (tile % num_m) * kBM, n0 = (tile / num_m) * BN;
+        const int m0 = (tile / num_n) * kBM, n0 = (tile % num_n) * BN;
         for (int kb = 0; kb < num_k; ++kb) {
           if (!mbar_wait(smem_u32(empty + stage), phase ^ 1u, wc)) {
             ok = false;
@@ -166,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-      const int m0 = (tile % num_m) * kBM, n0 = (tile / num_m) * BN;
+      const int m0 = (tile / num_n) * kBM, n0 = (tile % num_n) * BN;
       if (!mbar_wait(smem_u32(tfull + acc), acc_phase, wc)) break;
       tc_fence_after();
       const int y0 = m0 + q * 32;
@@ -222,8 +225,8 @@ static cudaError_t launch_bn(const CUtensorMap& tmA, const CUtensorMap& tmB, con
   using C = GemmCfg<BN>;
   const int tiles = ((M + kBM - 1) / kBM) * (N / BN);
   const int grid = tiles < num_sms() ? tiles : num_sms();
-  gemm_tc_kernel<BN, EK><<<grid, kThreads, C::kSmemBytes, s>>>(tmA, tmB, tmO, epi, M, N, K, err, limit_ns);
-  return cudaGetLastError();
+  return launch_kernel(gemm_tc_kernel<BN, EK>, dim3(grid), dim3(kThreads), C::kSmemBytes, s, tmA, tmB, tmO, epi, M, N,
+                       K, err, limit_ns);
 }
 
 template <int BN>

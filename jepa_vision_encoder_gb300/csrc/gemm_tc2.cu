@@ -2,9 +2,12 @@
 // 256 x 256 tiles computed by a cluster of two CTAs on two SMs (tcgen05 cta_group::2).
 //
 // Each CTA of the pair loads, per 64-wide K block, its own 128 rows of A and its own 128 of the
-// tile's 256 columns of B (32 KB per stage instead of the 48 KB a 1-SM 128 x 256 tile needs per SM),
-// so the operand traffic into each SM's shared memory drops by a third at the same tensor work.
-// Only the even CTA issues the MMAs (M = 256: rows 0-127 land in its TMEM, 128-255 in the peer's).
+// tile's 256 columns of B (32 KB per stage instead of the 48 KB a 1-SM 128 x 256 tile needs per
+// SM), so the operand traffic into each SM's shared memory drops by a third at the same tensor
+// work. Only the even CTA issues the MMAs (M = 256: rows 0-127 land in its TMEM, 128-255 in the
+// peer's). (A 256 x 128 pair tile, measured, was slower than both this and the 1-SM tiles at
+// every encoder shape.) Tiles are numbered N-fastest: the pairs working at the same time share rows of A (read from
+// HBM once) and sweep the weights B, which stay in L2.
 //
 // Per CTA (320 threads, one CTA per SM, grid = 2 x pairs, tiles strided over pairs):
 //   warp 0      TMA producer of this CTA's halves; every copy of the pair completes on the even
@@ -26,28 +29,35 @@ namespace jepa {
 namespace {
 
 constexpr int kTileM = 256;   // rows per pair tile (128 per CTA)
-constexpr int kTileN = 256;   // columns per pair tile (MMA N; 128 B-rows per CTA)
 constexpr int kBK = 64;
-constexpr int kStages = 6;
-constexpr int kHalfBytes = 128 * kBK * 2;            // 16 KB: 128 rows x 64 bf16
-constexpr int kStageBytes = 2 * kHalfBytes;          // A half + B half
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
-constexpr uint32_t kTmemCols = 2 * kTileN;           // two accumulators
 constexpr int kEpiBytes = kEpiWarps * 4096;          // two 2 KB staging buffers per epilogue warp
-constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kEpiBytes + 512;
 
-template <int EK>
+template <int TN>
+struct PairCfg {
+  static constexpr int kBRows = TN / 2;              // B rows each CTA loads
+  static constexpr int kABytes = 128 * kBK * 2;      // 16 KB: 128 rows x 64 bf16
+  static constexpr int kBBytes = kBRows * kBK * 2;   // 16 KB (TN 256) or 8 KB (TN 128)
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = (6 * 32768) / kStageBytes;  // 6 or 8: 192 KB of operand stages
+  static constexpr uint32_t kTmemCols = 2 * TN;      // two accumulators
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kEpiBytes + 512;
+};
+
+template <int TN, int EK>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmO, EpiArgs epi, int M, int N, int K, int* err,
                     uint64_t limit_ns) {
+  using C = PairCfg<TN>;
+  constexpr int kStages = C::kStages, kTileN = TN;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
   uint8_t* sA = smem;                              // kStages x 16 KB
-  uint8_t* sB = smem + kStages * kHalfBytes;       // kStages x 16 KB
-  uint8_t* sEpi = smem + kStages * kStageBytes;    // kEpiWarps x 4 KB
+  uint8_t* sB = smem + kStages * C::kABytes;       // kStages x kBBytes
+  uint8_t* sEpi = smem + kStages * C::kStageBytes; // kEpiWarps x 4 KB
   uint64_t* bars = reinterpret_cast<uint64_t*>(sEpi + kEpiBytes);
   uint64_t* full = bars;                           // own copies landed
   uint64_t* empty = bars + kStages;                // stage free (multicast from the even CTA)
@@ -81,7 +91,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (EK != kEpiPatch) prefetch_tmap(&tmO);
   }
   if (warp == 1) {
-    tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+    tmem_alloc_pair(smem_u32(tmem_slot), C::kTmemCols);
     tmem_relinquish_pair();
   }
   tc_fence_before();
@@ -90,6 +100,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const WaitCtl wc{abort_flag, err, limit_ns};
+  pdl_trigger();
+  pdl_wait();  // A and the residual stream come from earlier kernels
 
   if (warp == 0) {
     if (lane == 0) {
@@ -100,16 +112,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t phase = 0, armed = 0, armed_phase = 0;
       bool ok = true;
       for (int tile = pair; tile < num_tiles && ok; tile += num_pairs) {
-        const int m0 = (tile % num_m) * kTileM + (int)rank * 128, n0 = (tile / num_m) * kTileN + (int)rank * 128;
+        const int m0 = (tile / num_n) * kTileM + (int)rank * 128, n0 = (tile % num_n) * kTileN + (int)rank * C::kBRows;
         for (int kb = 0; kb < num_k; ++kb) {
           if (!mbar_wait(smem_u32(empty + stage), phase ^ 1u, wc)) {
             ok = false;
             break;
           }
           const uint32_t fb_even = mapa_shared(smem_u32(full + stage), 0);
-          if (rank == 0) mbar_arrive_expect_tx(smem_u32(full + stage), 2 * kStageBytes);
-          tma_load_2d_pair(smem_u32(sA + stage * kHalfBytes), &tmA, fb_even, kb * kBK, m0);
-          tma_load_2d_pair(smem_u32(sB + stage * kHalfBytes), &tmB, fb_even, kb * kBK, n0);
+          if (rank == 0) mbar_arrive_expect_tx(smem_u32(full + stage), 2 * C::kStageBytes);
+          tma_load_2d_pair(smem_u32(sA + stage * C::kABytes), &tmA, fb_even, kb * kBK, m0);
+          tma_load_2d_pair(smem_u32(sB + stage * C::kBBytes), &tmB, fb_even, kb * kBK, n0);
           armed |= 1u << stage;
           armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
           if (++stage == kStages) {
@@ -142,7 +154,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint64_t ad = desc_advance(a_desc, stage * kHalfBytes), bd = desc_advance(b_desc, stage * kHalfBytes);
+          const uint64_t ad = desc_advance(a_desc, stage * C::kABytes), bd = desc_advance(b_desc, stage * C::kBBytes);
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k)
             mma_ss_pair(d_tmem, desc_advance(ad, k * 32), desc_advance(bd, k * 32), idesc, (kb | k) != 0 ? 1u : 0u);
@@ -171,7 +183,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = pair; tile < num_tiles; tile += num_pairs) {
-      const int m0 = (tile % num_m) * kTileM + (int)rank * 128, n0 = (tile / num_m) * kTileN;
+      const int m0 = (tile / num_n) * kTileM + (int)rank * 128, n0 = (tile % num_n) * kTileN;
       if (!mbar_wait(smem_u32(tfull + acc), acc_phase, wc)) break;
       tc_fence_after();
       const int y0 = m0 + q * 32;
@@ -192,24 +204,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cluster_sync_all();  // the pair's MMAs are drained and both epilogues are done with TMEM
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc_pair(tmem_base, kTmemCols);
+    tmem_dealloc_pair(tmem_base, C::kTmemCols);
+  }
+}
+
+template <int TN>
+cudaError_t set_pair_attrs() {
+  cudaError_t e = cudaSuccess;
+  auto set = [&](const void* f) {
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, PairCfg<TN>::kSmemBytes);
+  };
+  set((const void*)gemm_tc2_kernel<TN, kEpiBias>);
+  set((const void*)gemm_tc2_kernel<TN, kEpiGelu>);
+  set((const void*)gemm_tc2_kernel<TN, kEpiResidual>);
+  set((const void*)gemm_tc2_kernel<TN, kEpiQkvRope>);
+  set((const void*)gemm_tc2_kernel<TN, kEpiPatch>);
+  return e;
+}
+
+template <int TN, int EK>
+cudaError_t launch_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmO, const EpiArgs& epi,
+                        int M, int N, int K, int* err, uint64_t limit_ns, cudaStream_t s) {
+  const int tiles = ((M + kTileM - 1) / kTileM) * (N / TN);
+  const int max_pairs = gemm_tc2_max_pairs();
+  const int pairs = tiles < max_pairs ? tiles : max_pairs;
+  return launch_kernel(gemm_tc2_kernel<TN, EK>, dim3(2 * pairs), dim3(kThreads), PairCfg<TN>::kSmemBytes, s, tmA, tmB,
+                       tmO, epi, M, N, K, err, limit_ns);
+}
+
+template <int TN>
+cudaError_t launch_pair_kind(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmO,
+                             const EpiArgs& epi, int M, int N, int K, int* err, uint64_t limit_ns, cudaStream_t s) {
+  switch (epi.kind) {
+    case kEpiBias: return launch_pair<TN, kEpiBias>(tmA, tmB, tmO, epi, M, N, K, err, limit_ns, s);
+    case kEpiGelu: return launch_pair<TN, kEpiGelu>(tmA, tmB, tmO, epi, M, N, K, err, limit_ns, s);
+    case kEpiResidual: return launch_pair<TN, kEpiResidual>(tmA, tmB, tmO, epi, M, N, K, err, limit_ns, s);
+    case kEpiQkvRope: return launch_pair<TN, kEpiQkvRope>(tmA, tmB, tmO, epi, M, N, K, err, limit_ns, s);
+    case kEpiPatch: return launch_pair<TN, kEpiPatch>(tmA, tmB, tmO, epi, M, N, K, err, limit_ns, s);
+    default: return cudaErrorInvalidValue;
   }
 }
 
 }  // namespace
 
-cudaError_t gemm_tc2_init_attributes() {
-  cudaError_t e = cudaSuccess;
-  auto set = [&](const void* f) {
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  };
-  set((const void*)gemm_tc2_kernel<kEpiBias>);
-  set((const void*)gemm_tc2_kernel<kEpiGelu>);
-  set((const void*)gemm_tc2_kernel<kEpiResidual>);
-  set((const void*)gemm_tc2_kernel<kEpiQkvRope>);
-  set((const void*)gemm_tc2_kernel<kEpiPatch>);
-  return e;
-}
+cudaError_t gemm_tc2_init_attributes() { return set_pair_attrs<256>(); }
 
 // Cluster pairs that can be resident at once (the GPCs may not pair up every SM).
 int gemm_tc2_max_pairs() {
@@ -219,8 +258,8 @@ int gemm_tc2_max_pairs() {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * (num_sms() / 2), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_tc2_kernel<kEpiBias>, &cfg) != cudaSuccess || n <= 0) {
+    cfg.dynamicSmemBytes = PairCfg<256>::kSmemBytes;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_tc2_kernel<256, kEpiBias>, &cfg) != cudaSuccess || n <= 0) {
       cudaGetLastError();
       n = num_sms() / 2;
     }
@@ -232,24 +271,8 @@ int gemm_tc2_max_pairs() {
 cudaError_t gemm_tc2_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmO,
                             const EpiArgs& epi, int M, int N, int K, int* err, uint64_t limit_ns, cudaStream_t s) {
   if (M <= 0) return cudaSuccess;
-  if (N % kTileN || K % kBK) return cudaErrorInvalidValue;
-  const int tiles = ((M + kTileM - 1) / kTileM) * (N / kTileN);
-  const int max_pairs = gemm_tc2_max_pairs();
-  const int pairs = tiles < max_pairs ? tiles : max_pairs;
-  const dim3 grid(2 * pairs), block(kThreads);
-  switch (epi.kind) {
-    case kEpiBias: gemm_tc2_kernel<kEpiBias><<<grid, block, kSmemBytes, s>>>(tmA, tmB, tmO, epi, M, N, K, err, limit_ns); break;
-    case kEpiGelu: gemm_tc2_kernel<kEpiGelu><<<grid, block, kSmemBytes, s>>>(tmA, tmB, tmO, epi, M, N, K, err, limit_ns); break;
-    case kEpiResidual:
-      gemm_tc2_kernel<kEpiResidual><<<grid, block, kSmemBytes, s>>>(tmA, tmB, tmO, epi, M, N, K, err, limit_ns);
-      break;
-    case kEpiQkvRope:
-      gemm_tc2_kernel<kEpiQkvRope><<<grid, block, kSmemBytes, s>>>(tmA, tmB, tmO, epi, M, N, K, err, limit_ns);
-      break;
-    case kEpiPatch: gemm_tc2_kernel<kEpiPatch><<<grid, block, kSmemBytes, s>>>(tmA, tmB, tmO, epi, M, N, K, err, limit_ns); break;
-    default: return cudaErrorInvalidValue;
-  }
-  return cudaGetLastError();
+  if (N % 256 || K % kBK) return cudaErrorInvalidValue;
+  return launch_pair_kind<256>(tmA, tmB, tmO, epi, M, N, K, err, limit_ns, s);
 }
 
 }  // namespace jepa

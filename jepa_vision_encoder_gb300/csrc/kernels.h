@@ -6,7 +6,32 @@
 
 #include "epilogue.cuh"
 
+#include <utility>
+
 namespace jepa {
+
+// Launch mode of the calling thread: while set (the encoder's launch sequence), kernels go out as
+// programmatic dependent launches, so each one's set-up overlaps the end of the previous kernel.
+bool& pdl_launches();
+
+// Launches `kernel` on `s`, programmatic when pdl_launches() is set.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                          Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  if (pdl_launches()) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Encodes a 2-D bf16 tensor map (row-major [rows, cols], 128-byte swizzle, box = box_rows x 64).
 // Returns false if the driver refuses the map.

@@ -24,6 +24,14 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// Every kernel of the encoder calls pdl_trigger() once its own set-up is done (the next kernel in
+// the stream may then be scheduled while this one runs; it cannot start before every block of
+// this grid has triggered or exited) and pdl_wait() before it reads data an earlier kernel wrote
+// or writes data an earlier kernel reads. Both are no-ops when the launch was not programmatic.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");

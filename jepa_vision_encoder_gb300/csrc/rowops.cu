@@ -29,6 +29,8 @@ __device__ __forceinline__ size_t pix_index(int layout, int T, int C, int H, int
 // Needs P % 8 == 0 and W % 4 == 0 (16-byte aligned pixel runs).
 __global__ void patchify_bf16_v8_kernel(const float* __restrict__ pix, int B, int T, int C, int H, int W, int t,
                                         int P, int layout, __nv_bfloat16* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   const int gt = T / t, gh = H / P, gw = W / P;
   const int K = C * t * P * P;
   const int chunks_per_row = K / 8;
@@ -57,6 +59,8 @@ __global__ void patchify_bf16_v8_kernel(const float* __restrict__ pix, int B, in
 template <bool BF16>
 __global__ void patchify_scalar_kernel(const float* __restrict__ pix, int B, int T, int C, int H, int W, int t,
                                        int P, int layout, void* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   const int gt = T / t, gh = H / P, gw = W / P;
   const int K = C * t * P * P;
   const long long total = (long long)B * gt * gh * gw * K;
@@ -91,14 +95,11 @@ cudaError_t patchify_launch(const float* pix, int B, int T, int C, int H, int W,
   const int K = C * t * P * P;
   if (rows <= 0) return cudaSuccess;
   if (out_bf16 && P % 8 == 0 && W % 4 == 0 && (reinterpret_cast<uintptr_t>(pix) & 15) == 0) {
-    patchify_bf16_v8_kernel<<<grid_for(rows * (K / 8), 256), 256, 0, s>>>(
-        pix, B, T, C, H, W, t, P, layout, reinterpret_cast<__nv_bfloat16*>(out));
-  } else if (out_bf16) {
-    patchify_scalar_kernel<true><<<grid_for(rows * K, 256), 256, 0, s>>>(pix, B, T, C, H, W, t, P, layout, out);
-  } else {
-    patchify_scalar_kernel<false><<<grid_for(rows * K, 256), 256, 0, s>>>(pix, B, T, C, H, W, t, P, layout, out);
+    return launch_kernel(patchify_bf16_v8_kernel, dim3(grid_for(rows * (K / 8), 256)), dim3(256), 0, s, pix, B, T, C,
+                         H, W, t, P, layout, reinterpret_cast<__nv_bfloat16*>(out));
   }
-  return cudaGetLastError();
+  return launch_kernel(out_bf16 ? patchify_scalar_kernel<true> : patchify_scalar_kernel<false>,
+                       dim3(grid_for(rows * K, 256)), dim3(256), 0, s, pix, B, T, C, H, W, t, P, layout, out);
 }
 
 // ------------------------------------------------------------------ LayerNorm
@@ -110,6 +111,8 @@ template <int V, bool BF16>
 __global__ void __launch_bounds__(256) layernorm_kernel(const float* __restrict__ x, int M, int D,
                                                         const float* __restrict__ g, const float* __restrict__ bta,
                                                         float eps, void* __restrict__ y) {
+  pdl_trigger();
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row = blockIdx.x * 8 + warp;
   if (row >= M) return;
@@ -162,11 +165,8 @@ template <int V>
 cudaError_t ln_v(const float* x, int M, int D, const float* g, const float* b, float eps, bool bf16, void* y,
                  cudaStream_t s) {
   const int grid = (M + 7) / 8;
-  if (bf16)
-    layernorm_kernel<V, true><<<grid, 256, 0, s>>>(x, M, D, g, b, eps, y);
-  else
-    layernorm_kernel<V, false><<<grid, 256, 0, s>>>(x, M, D, g, b, eps, y);
-  return cudaGetLastError();
+  return launch_kernel(bf16 ? layernorm_kernel<V, true> : layernorm_kernel<V, false>, dim3(grid), dim3(256), 0, s, x,
+                       M, D, g, b, eps, y);
 }
 
 }  // namespace
@@ -246,6 +246,8 @@ cudaError_t rope_table_launch(int gt, int gh, int gw, int head_dim, float theta,
 namespace {
 __global__ void prefix_rows_kernel(float* X, int B, int N, int D, const float* cls, const float* pos,
                                    const float* vec) {
+  pdl_trigger();
+  pdl_wait();
   const int b = blockIdx.x;
   for (int c = threadIdx.x; c < D; c += blockDim.x) {
     float v = cls[c];
@@ -259,8 +261,7 @@ __global__ void prefix_rows_kernel(float* X, int B, int N, int D, const float* c
 cudaError_t prefix_rows_launch(float* X, int B, int N, int D, const float* cls, const float* pos, const float* vec,
                                cudaStream_t s) {
   if (B <= 0) return cudaSuccess;
-  prefix_rows_kernel<<<B, 256, 0, s>>>(X, B, N, D, cls, pos, vec);
-  return cudaGetLastError();
+  return launch_kernel(prefix_rows_kernel, dim3(B), dim3(256), 0, s, X, B, N, D, cls, pos, vec);
 }
 
 // ------------------------------------------------------------------ bounded-wait probe
@@ -353,6 +354,11 @@ int num_sms() {
     cached.store(v);
   }
   return v;
+}
+
+bool& pdl_launches() {
+  thread_local bool on = false;
+  return on;
 }
 
 uint64_t default_wait_limit_ns() { return 1000000000ull; }  // 1 s: far above any legitimate wait

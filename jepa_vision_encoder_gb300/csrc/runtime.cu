@@ -400,6 +400,7 @@ struct jepa_context {
   int bn_patch = 0, bn_qkv = 0, bn_out = 0, bn_up = 0, bn_down = 0;
   // graph replay
   bool use_graph = false;
+  bool use_pdl = true;  // programmatic dependent launches in the encode sequence
   cudaGraphExec_t gexec = nullptr;
   int gB = -1, gT = -1, gH = -1, gW = -1, glayout = -1;
   const float* gpix = nullptr;
@@ -411,7 +412,7 @@ struct jepa_context {
   struct Rec { int cls; size_t e0, e1; double flops, bytes; };
   std::vector<Rec> recs;
   // events recorded inside a captured graph (re-recorded by every replay, folded after each)
-  bool capturing = false, gprof = false, gpending = false;
+  bool capturing = false, gprof = false, gpending = false, gpdl = false;
   std::vector<cudaEvent_t> gev;
   size_t gev_used = 0;
   std::vector<Rec> grecs;
@@ -527,6 +528,12 @@ extern "C" jepa_status jepa_context_set_stream(jepa_context* c, void* stream) {
 extern "C" jepa_status jepa_context_set_graph(jepa_context* c, int32_t enable) {
   if (!c) return fail(JEPA_E_INVALID_ARG, "jepa_context_set_graph: null context");
   c->use_graph = enable != 0;
+  return JEPA_OK;
+}
+
+extern "C" jepa_status jepa_context_set_pdl(jepa_context* c, int32_t enable) {
+  if (!c) return fail(JEPA_E_INVALID_ARG, "jepa_context_set_pdl: null context");
+  c->use_pdl = enable != 0;
   return JEPA_OK;
 }
 
@@ -677,6 +684,12 @@ jepa_status launch_encode(jepa_context* c, const float* pix, int B, int T, int H
   cudaStream_t s = c->stream;
   const uint64_t lim = default_wait_limit_ns();
   const double es = bf ? 2.0 : 4.0;                       // bytes of a GEMM operand element
+  // programmatic launches for this sequence (not between profiling events)
+  struct PdlScope {
+    bool prev;
+    explicit PdlScope(bool on) : prev(pdl_launches()) { pdl_launches() = on; }
+    ~PdlScope() { pdl_launches() = prev; }
+  } pdl_scope(c->use_pdl && !c->profiling);
   const double dM = M, dMp = Mp, dD = D, dF = F, dK = m->K;
   const double ln_bytes = dM * dD * (4.0 + es);           // read X fp32, write the normalised rows
   const double attn_flops = 4.0 * hd * NH * B *
@@ -784,7 +797,7 @@ extern "C" jepa_status jepa_encode(jepa_context* c, const float* d_pixels, int32
 
   CUDA_TRY(fold_graph_events(c));  // the previous replay's events are about to be re-recorded
   const bool hit = c->gexec && c->gB == B && c->gT == T && c->gH == H && c->gW == W && c->glayout == layout &&
-                   c->gpix == d_pixels && c->gtok == d_tokens && c->gprof == c->profiling;
+                   c->gpix == d_pixels && c->gtok == d_tokens && c->gprof == c->profiling && c->gpdl == c->use_pdl;
   if (!hit) {
     if (c->gexec) {
       cudaGraphExecDestroy(c->gexec);
@@ -822,6 +835,7 @@ extern "C" jepa_status jepa_encode(jepa_context* c, const float* d_pixels, int32
     c->gpix = d_pixels;
     c->gtok = d_tokens;
     c->gprof = c->profiling;
+    c->gpdl = c->use_pdl;
   }
   CUDA_TRY(cudaGraphLaunch(c->gexec, c->stream));
   c->gpending = c->gprof;

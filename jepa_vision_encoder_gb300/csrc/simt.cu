@@ -4,6 +4,7 @@
 #include <cuda_bf16.h>
 
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace jepa {
 
@@ -17,6 +18,8 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const float* __restrict_
                                                         EpiArgs epi, int M, int N, int K) {
   __shared__ float As[kTK][kTM + 4];
   __shared__ float Bs[kTK][kTN + 4];
+  pdl_trigger();
+  pdl_wait();
   const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
   const int m0 = blockIdx.y * kTM, n0 = blockIdx.x * kTN;
   float acc[4][4] = {};
@@ -59,6 +62,8 @@ constexpr int kSQ = 128, kSK = 64, kSHD = 64;
 __global__ void __launch_bounds__(kSQ) attn_simt_kernel(const float* __restrict__ qkv, AttnParams p) {
   __shared__ float Ks[kSK][kSHD];
   __shared__ float Vs[kSK][kSHD];
+  pdl_trigger();
+  pdl_wait();
   const int h = blockIdx.y, b = blockIdx.z;
   const int D = p.H * kSHD, ld = 3 * D;
   const int q = blockIdx.x * kSQ + threadIdx.x;
@@ -128,8 +133,7 @@ cudaError_t gemm_simt_launch(const float* A, const float* Bw, const EpiArgs& epi
                              cudaStream_t s) {
   if (M <= 0) return cudaSuccess;
   dim3 grid((N + kTN - 1) / kTN, (M + kTM - 1) / kTM);
-  gemm_simt_kernel<<<grid, 256, 0, s>>>(A, Bw, epi, M, N, K);
-  return cudaGetLastError();
+  return launch_kernel(gemm_simt_kernel, grid, dim3(256), 0, s, A, Bw, epi, M, N, K);
 }
 
 cudaError_t attention_simt_launch(const float* qkv, const AttnParams& p, cudaStream_t s) {
@@ -138,8 +142,7 @@ cudaError_t attention_simt_launch(const float* qkv, const AttnParams& p, cudaStr
   AttnParams q = p;
   if (q.frame_tokens <= 0) q.frame_tokens = 1;
   dim3 grid((p.N + kSQ - 1) / kSQ, p.H, p.B);
-  attn_simt_kernel<<<grid, kSQ, 0, s>>>(qkv, q);
-  return cudaGetLastError();
+  return launch_kernel(attn_simt_kernel, grid, dim3(kSQ), 0, s, qkv, q);
 }
 
 }  // namespace jepa

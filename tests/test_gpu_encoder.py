@@ -113,6 +113,24 @@ def test_graph_replay_and_host_api_match_eager():
     assert torch.equal(host, eager.cpu())
 
 
+@pytest.mark.parametrize("name", ["vjepa2_vitl16_16x256", "hfvit_ti14_224"])
+def test_programmatic_launches_change_nothing(name):
+    # the same kernels with and without programmatic dependent launch, eager and graph replay
+    cfg, dtype, (T, H, W) = small(name)
+    model, ctx = make(name, n_layer=cfg.n_layer, batch=2, T=T, H=H, W=W)
+    pix = torch.from_numpy(synth.pixels(5, (2, T, 3, H, W))).cuda()
+    ctx.set_pdl(False)
+    ref = ctx.encode(pix).clone()
+    ctx.set_pdl(True)
+    out = ctx.encode(pix).clone()
+    ctx.set_graph(True)
+    for _ in range(2):
+        graph_out = ctx.encode(pix).clone()
+    ctx.sync()
+    assert torch.equal(out, ref)
+    assert torch.equal(graph_out, ref)
+
+
 def test_two_threads_two_contexts_bit_identical():
     name = "vjepa2_1_vitl16_16x384"
     cfg, dtype, (T, H, W) = small(name)
