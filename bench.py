@@ -1,11 +1,13 @@
 #!/usr/bin/env python3
 """Encoder throughput on GB300: tokens/s and TFLOP/s of the shared ViT encoder forward.
 
-Workload: V-JEPA 2 ViT-L/16, one 16 x 256 x 256 clip per GPU (2048 tokens), bf16 weights and
-activations with fp32 accumulation, synthetic seeded weights and pixels. A step is one
-jepa_encode of the clip (patchify, patch GEMM, 24 blocks, final norm) on inputs resident in HBM.
+Workload: V-JEPA 2 ViT-L/16 on 16 x 256 x 256 clips (2048 tokens each), eight clips per GPU per
+step by default (--batch), bf16 weights and activations with fp32 accumulation, synthetic seeded
+weights and pixels. A step is one jepa_encode of the batch (patchify, patch GEMM, 24 blocks,
+final norm) on inputs resident in HBM. The line also carries the same clip at batch 1 ("batch1"),
+timed the same way.
 
-    python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+    python bench.py [--gpus N --steps K --warmup W] [--batch B] [--impl reference]
 
 Timing: W untimed steps, then K steps replaying one CUDA graph of the encode, each bracketed by
 CUDA events on the context stream, with a 256 MiB write between steps to flush L2 (outside the
@@ -32,10 +34,17 @@ METRIC = "encoder tokens/s and TFLOP/s (fraction of bf16 peak), ViT-L 16×256² 
 WORKLOAD = dict(preset="vjepa2_vitl16", T=16, H=256, W=256)
 FLUSH_BYTES = 256 << 20  # > 129 MB of L2
 
-# Per-launch DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of a kernel class, from an
-# ncu capture summarised under profiles/; `sha1` is the hash of the kernel's source file when the
-# counters were taken (a changed kernel reports traffic null until it is captured again).
-NCU_TRAFFIC = {}
+# Per-launch DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of a kernel class, from the
+# batch-1 ncu captures of the 2048-token clip; `sha1` is the hash of the class's source files when
+# the counters were taken (a changed kernel reports traffic null until it is captured again).
+NCU_TRAFFIC = {
+    "attention": {"bytes_per_launch": 12.63e6, "batch": 1, "sha1": "1511a9089fe720105e8fd5525f9926fedd8eca90"},
+    "layernorm": {"bytes_per_launch": 8.41e6, "batch": 1, "sha1": "8b7cd377f622007f9d31328489c2f31b9a9b7484"},
+    "gemm_qkv": {"bytes_per_launch": 10.58e6, "batch": 1, "sha1": "399fa54a5c822b7bd74f2d95c23de3da22870726"},
+    "gemm_up": {"bytes_per_launch": 12.65e6, "batch": 1, "sha1": "399fa54a5c822b7bd74f2d95c23de3da22870726"},
+    "gemm_out": {"bytes_per_launch": 14.70e6, "batch": 1, "sha1": "399fa54a5c822b7bd74f2d95c23de3da22870726"},
+    "gemm_down": {"bytes_per_launch": 33.58e6, "batch": 1, "sha1": "399fa54a5c822b7bd74f2d95c23de3da22870726"},
+}
 
 
 def parse_args(argv=None):
@@ -43,7 +52,7 @@ def parse_args(argv=None):
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=50)
     p.add_argument("--warmup", type=int, default=5)
-    p.add_argument("--batch", type=int, default=1, help="clips per GPU per step")
+    p.add_argument("--batch", type=int, default=8, help="clips per GPU per step")
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true")
     return p.parse_args(argv)
@@ -193,12 +202,15 @@ def run_reference(args):
     wall = time.perf_counter() - t_start
     mean_full = statistics.mean(full_times)
     value = N / mean_full
-    sample = (f"each step: the fp64 oracle on the 2048-token clip with 1 of the {L} layers; the other {L - 1} "
-              f"layers added at the calibrated per-layer time {per_layer:.2f} s")
+    B = args.batch
+    sample = (f"each step: the fp64 oracle on one 2048-token clip with 1 of the {L} layers; the other {L - 1} "
+              f"layers added at the calibrated per-layer time {per_layer:.2f} s; the {B} clips of a step are "
+              f"independent, so a step costs {B} such clips")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * mean_full, "higher_is_better": True,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * mean_full * B, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "V-JEPA 2 ViT-L/16 16x256x256 clip (2048 tokens), batch 1",
+            "config": {"workload": f"V-JEPA 2 ViT-L/16 16x256x256 clip ({N} tokens) x {B} per GPU",
+                       "tokens_per_step": B * N, "global_batch": B, "seq_len": N,
                        "wall_s_sampled_steps": wall},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -207,12 +219,46 @@ def run_reference(args):
 
 
 # ------------------------------------------------------------------ our arm
+KERNEL_SOURCES = {
+    "attention": ("attention_tc.cu", "ptx.cuh"),
+    "layernorm": ("rowops.cu", "ptx.cuh"), "layernorm_final": ("rowops.cu", "ptx.cuh"),
+    "patchify": ("rowops.cu", "ptx.cuh"),
+}
+GEMM_SOURCES = ("gemm_tc.cu", "gemm_tc2.cu", "epilogue.cuh", "ptx.cuh")
+
+
 def source_sha1(kernel_class: str):
-    files = {"attention": "attention_tc.cu", "layernorm": "rowops.cu", "layernorm_final": "rowops.cu",
-             "patchify": "rowops.cu"}
-    name = files.get(kernel_class, "gemm_tc.cu")
-    with open(os.path.join(ROOT, "jepa_vision_encoder_gb300", "csrc", name), "rb") as f:
-        return hashlib.sha1(f.read()).hexdigest()
+    """sha1 over the source files the kernel class is built from."""
+    h = hashlib.sha1()
+    for name in KERNEL_SOURCES.get(kernel_class, GEMM_SOURCES):
+        with open(os.path.join(ROOT, "jepa_vision_encoder_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def time_graph_steps(jv, model, B, steps, warmup, flush, rank):
+    """ms per step of graph-replayed encodes of B clips (L2 flushed between steps)."""
+    import torch
+    import synth
+    T, H, W = WORKLOAD["T"], WORKLOAD["H"], WORKLOAD["W"]
+    ctx = jv.Context(model, B, T, H, W, graph=True)
+    pix = torch.from_numpy(synth.pixels(rank, (B, T, 3, H, W))).cuda()
+    out = torch.empty((B, model.n_tokens(T, H, W), model.hp.embed_dim), dtype=torch.float32, device="cuda")
+    with torch.cuda.stream(ctx.stream):
+        for _ in range(warmup):
+            flush.zero_()
+            ctx.encode(pix, out)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        torch.cuda.synchronize()
+        for e0, e1 in ev:
+            flush.zero_()
+            e0.record(ctx.stream)
+            ctx.encode(pix, out)
+            e1.record(ctx.stream)
+        torch.cuda.synchronize()
+    ctx.sync()
+    ctx.close()
+    return statistics.mean(a.elapsed_time(b) for a, b in ev)
 
 
 def run_ours(args):
@@ -330,7 +376,9 @@ def run_ours(args):
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "kernel": name}
     rec = NCU_TRAFFIC.get(name)
-    roof["traffic"] = rec["bytes_per_launch"] if rec and rec.get("sha1") == source_sha1(name) else None
+    # counters were taken at batch 1: other batches report null
+    roof["traffic"] = (rec["bytes_per_launch"]
+                       if rec and rec.get("sha1") == source_sha1(name) and B == rec["batch"] else None)
     roof["peak_source"] = peaks["source"]
     kernels = {k: {"launches": v["launches"], "avg_us": 1e3 * v["total_ms"] / v["launches"],
                    "share": v["total_ms"] / max(sum(x["total_ms"] for x in prof.values()), 1e-9),
@@ -352,6 +400,15 @@ def run_ours(args):
            "h2d_bytes_per_step": pin_in.numel() * 4, "d2h_bytes_per_step": pin_out.numel() * 4}
 
     launches = ctx.launches(B, T, H, W)
+    # the same clip at batch 1 (latency case of the workload), measured the same way
+    b1 = None
+    if B != 1:
+        ms1 = reduce_max(time_graph_steps(jv, model, 1, min(args.steps, 50), args.warmup, flush, rank),
+                         device="cuda" if world > 1 else None)
+        fl1 = flops_per_step / B
+        b1 = {"ms_per_step": ms1, "value": world * N / (ms1 / 1e3), "unit": "tokens/s",
+              "tflops": world * fl1 / (ms1 / 1e3) / 1e12,
+              "frac_of_bf16_peak": fl1 / (ms1 / 1e3) / 1e12 / peaks["bf16_tflops"]}
     line = None
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -364,7 +421,7 @@ def run_ours(args):
                 "tflops": tflops, "frac_of_bf16_peak": tflops / (world * peaks["bf16_tflops"]),
                 "eager_ms_per_step": eager_ms, "launch_mode": launch_mode,
                 "roofline": roof, "kernels": kernels,
-                "e2e": e2e, "gpu_launches": launches * args.steps,
+                "e2e": e2e, "gpu_launches": launches * args.steps, "batch1": b1,
                 "clocks": {k: v for k, v in clk.summary().items()},
                 "profiled_pass": {"ms_per_step": p0.elapsed_time(p1) / args.steps,
                                   "clocks": clk_prof.summary()}}
