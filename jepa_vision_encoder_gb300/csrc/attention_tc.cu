@@ -6,14 +6,14 @@
 //   warps 0..3  softmax of Q0, warps 4..7 softmax of Q1: one query row per thread (TMEM lane).
 //               The thread reads its 128 scores from TMEM once, takes their max (independent
 //               three-input max chains) and writes p = 2^(s*log2e/8 - m) to TMEM as bf16 pairs
-//               (packed two-lane FMA for the scaling, two-lane adds for the row sum). The
+//               (packed two-lane FMA for the scaling, four two-lane chains for the row sum). The
 //               running max only moves when a tile raises it by more than 2^8, and then the
 //               warp rescales its O rows in TMEM. At the end o = O / l is stored as bf16.
 //   warp 8      TMA: Q0 and Q1 once, then K and V tiles of 128 keys into a 3-stage ring
 //               (3-D tensor map over qkv [B][N][3D]: rows beyond N read as zeros).
-//   warp 9      MMA, per tile g and key tile j: S_g(j+1) = Q_g K(j+1)^T as soon as warpgroup g has
-//               read S_g(j) into registers (so the next scores are ready when its softmax ends),
-//               then O_g += P_g(j) V(j) once P_g(j) is in TMEM; the two tiles alternate.
+//   warp 9      MMA, per key tile j: S_g(j+1) = Q_g K(j+1)^T for both tiles as soon as warpgroup g
+//               has read S_g(j) into registers (so the next scores are ready when its softmax
+//               ends), then O_g += P_g(j) V(j) for both tiles once P_g(j) is in TMEM.
 //               S = Q K^T: M128 N128 K16 x4 (both K-major); O += P V: M128 N64 K16 x8 with P
 //               read from TMEM and V MN-major in shared memory.
 // TMEM (512 columns): S0 [0,128) S1 [128,256) P0 [256,320) P1 [320,384) O0 [384,448) O1 [448,512).
@@ -182,16 +182,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         const int nst = (stage + 1 == kKvStages) ? 0 : stage + 1;
         const uint32_t nph = (stage + 1 == kKvStages) ? (phase ^ 1u) : phase;
         const bool more = j + 1 < num_kt;
+        // S_g(j+1) as soon as warpgroup g holds S_g(j) in registers (while it computes P), for
+        // both tiles, then P_g(j) V(j) once P is in TMEM: neither tile's next scores wait
+        // behind the other tile's softmax
+        if (more) {
+          ok = mbar_wait(smem_u32(kv_full + nst), nph, wc);
 #pragma unroll
-        for (int g = 0; g < 2; ++g) {
-          // S_g(j+1) as soon as the warpgroup holds S_g(j) in registers (while it computes P),
-          // then P_g(j) V(j) once P is in TMEM
-          if (more) {
+          for (int g = 0; g < 2 && ok; ++g) {
             if (!(ok = mbar_wait(smem_u32(s_free + g), (uint32_t)(j & 1), wc))) break;
-            if (g == 0 && !(ok = mbar_wait(smem_u32(kv_full + nst), nph, wc))) break;
             tc_fence_after();
             issue_s(g, nst);
           }
+        }
+#pragma unroll
+        for (int g = 0; g < 2 && ok; ++g) {
           if (!(ok = mbar_wait(smem_u32(p_full + g), (uint32_t)(j & 1), wc))) break;
           tc_fence_after();
           issue_pv(g, stage, j);
@@ -294,7 +298,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       const float base = (m_run == -INFINITY) ? 0.0f : m_run;
       // p = 2^(s*sc - m) two keys at a time, as bf16 pairs into the P columns
       const float2 sc2 = make_float2(sc, sc), nb2 = make_float2(-base, -base);
-      float2 ls2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
+      float2 ls2[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
+                       make_float2(0.0f, 0.0f)};  // four short chains for the row sum
 #pragma unroll
       for (int c = 0; c < kKT / 32; ++c) {
         uint32_t pk[16];
@@ -303,12 +308,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           const float2 x =
               __ffma2_rn(make_float2(__uint_as_float(s[c][e]), __uint_as_float(s[c][e + 1])), sc2, nb2);
           const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-          ls2[(e >> 1) & 1] = __fadd2_rn(ls2[(e >> 1) & 1], p);
+          ls2[(e >> 1) & 3] = __fadd2_rn(ls2[(e >> 1) & 3], p);
           pk[e >> 1] = pack_bf16x2(p.x, p.y);
         }
         tmem_st16(tP + c * 16, pk);
       }
-      l_run += (ls2[0].x + ls2[1].x) + (ls2[0].y + ls2[1].y);
+      const float2 l01 = __fadd2_rn(ls2[0], ls2[1]), l23 = __fadd2_rn(ls2[2], ls2[3]);
+      l_run += (l01.x + l23.x) + (l01.y + l23.y);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(smem_u32(p_full + g));
