@@ -322,7 +322,31 @@ template <int EK>
 __device__ __forceinline__ void epi_chunk_tc(const EpiArgs& a, const CUtensorMap* tm_out, EpiStage& st, int lane,
                                              int y0, int n0, float (&v)[32]) {
   if constexpr (EK == kEpiPatch) {
-    epi_fragment<32, false>(a, y0 + lane, n0, v);
+    if (a.prefix == 0 && a.rows_per_item == a.patches_per_item && a.pos == nullptr) {
+      // output rows are the patch rows (no CLS, no learned table): bias (+ modality vector),
+      // then the same staged TMA store as the other epilogues, in fp32
+      epi_math_tc<EK>(a, y0 + lane, n0, v);
+      if (a.vec != nullptr) {
+        const float4* v4 = reinterpret_cast<const float4*>(a.vec + n0);
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const float4 m = __ldg(v4 + e / 4);
+          v[e] += m.x;
+          v[e + 1] += m.y;
+          v[e + 2] += m.z;
+          v[e + 3] += m.w;
+        }
+      }
+      uint32_t w[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(v[e]);
+      st.put(lane, w, tm_out, n0, y0, false);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(v[16 + e]);
+      st.put(lane, w, tm_out, n0 + 16, y0, false);
+    } else {
+      epi_fragment<32, false>(a, y0 + lane, n0, v);  // rows remapped per item: stores from registers
+    }
   } else {
     epi_math_tc<EK>(a, y0 + lane, n0, v);
     if constexpr (EK == kEpiResidual) {

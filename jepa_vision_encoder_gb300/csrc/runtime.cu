@@ -1002,9 +1002,11 @@ extern "C" jepa_status jepa_op_linear(int32_t dtype, const void* d_x, int32_t M,
   if (!make_tmap_2d_bf16(&ta, d_x, M, K, 128) || !make_tmap_2d_bf16(&tb, d_w, N, K, gemm_tc_b_box(bn)))
     return fail(JEPA_E_CUDA, "cuTensorMapEncodeTiled refused an operand");
   memset(&to, 0, sizeof to);
-  if (e.kind != kEpiPatch) {
+  // the patch embedding stores through TMA too when its rows are the patch rows themselves
+  const bool patch_tma = e.kind == kEpiPatch && e.prefix == 0 && e.rows_per_item == e.patches_per_item && !e.pos;
+  if (e.kind != kEpiPatch || patch_tma) {
     if (reinterpret_cast<uintptr_t>(e.out) & 15) return fail(JEPA_E_INVALID_ARG, "bf16 GEMM output must be 16-byte aligned");
-    if (!make_tmap_2d_out(&to, e.out, M, N, e.kind == kEpiResidual ? 4 : 2))
+    if (!make_tmap_2d_out(&to, e.out, M, N, (e.kind == kEpiResidual || e.kind == kEpiPatch) ? 4 : 2))
       return fail(JEPA_E_CUDA, "cuTensorMapEncodeTiled refused the output");
   }
   CUDA_TRY(gemm_tc_launch(ta, tb, to, bn, e, M, N, K, err, default_wait_limit_ns(), s));
