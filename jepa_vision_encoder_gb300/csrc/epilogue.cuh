@@ -301,8 +301,8 @@ struct EpiStage {
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
-      if (add)
-        tma_reduce_add_2d(tm, smem_u32(buf), x, y);
+      if (add)  // the residual stream is read again by the next LayerNorm: keep it in L2
+        tma_reduce_add_2d_hint(tm, smem_u32(buf), x, y, l2_policy_evict_last());
       else
         tma_store_2d(tm, smem_u32(buf), x, y);
       bulk_commit();

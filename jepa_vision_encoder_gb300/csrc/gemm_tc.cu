@@ -98,6 +98,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
+      const uint64_t a_policy = l2_policy_evict_first();
       int stage = 0;
       uint32_t phase = 0, armed = 0, armed_phase = 0;
       bool ok = true;
@@ -110,7 +111,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const uint32_t fb = smem_u32(full + stage);
           mbar_arrive_expect_tx(fb, C::kStageBytes);
-          tma_load_2d(smem_u32(sA + stage * C::kABytes), &tmA, fb, kb * kBK, m0);
+          if (EK == kEpiResidual)  // A (attention output, FFN hidden) is read once: let it go first
+            tma_load_2d_hint(smem_u32(sA + stage * C::kABytes), &tmA, fb, kb * kBK, m0, a_policy);
+          else
+            tma_load_2d(smem_u32(sA + stage * C::kABytes), &tmA, fb, kb * kBK, m0);
           tma_load_2d(smem_u32(sB + stage * C::kBBytes), &tmB, fb, kb * kBK, n0);
           armed |= 1u << stage;
           armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);

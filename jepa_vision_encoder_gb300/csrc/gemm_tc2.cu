@@ -108,6 +108,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // Both CTAs load their halves; every copy completes on the even CTA's stage barrier,
       // which the even CTA arms with the bytes of both halves (tx-count may run ahead of the
       // arm within a phase: the phase cannot complete before the even CTA's arrive).
+      const uint64_t a_policy = l2_policy_evict_first();
       int stage = 0;
       uint32_t phase = 0, armed = 0, armed_phase = 0;
       bool ok = true;
@@ -120,7 +121,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           const uint32_t fb_even = mapa_shared(smem_u32(full + stage), 0);
           if (rank == 0) mbar_arrive_expect_tx(smem_u32(full + stage), 2 * C::kStageBytes);
-          tma_load_2d_pair(smem_u32(sA + stage * C::kABytes), &tmA, fb_even, kb * kBK, m0);
+          if (EK == kEpiResidual)  // A (attention output, FFN hidden) is read once: let it go first
+            tma_load_2d_pair_hint(smem_u32(sA + stage * C::kABytes), &tmA, fb_even, kb * kBK, m0, a_policy);
+          else
+            tma_load_2d_pair(smem_u32(sA + stage * C::kABytes), &tmA, fb_even, kb * kBK, m0);
           tma_load_2d_pair(smem_u32(sB + stage * C::kBBytes), &tmB, fb_even, kb * kBK, n0);
           armed |= 1u << stage;
           armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
