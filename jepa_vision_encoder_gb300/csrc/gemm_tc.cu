@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      const uint64_t a_policy = l2_policy_evict_first();
+      const uint64_t a_policy = l2_policy_evict_first(), b_policy = l2_policy_evict_last();
       int stage = 0;
       uint32_t phase = 0, armed = 0, armed_phase = 0;
       bool ok = true;
@@ -115,7 +115,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d_hint(smem_u32(sA + stage * C::kABytes), &tmA, fb, kb * kBK, m0, a_policy);
           else
             tma_load_2d(smem_u32(sA + stage * C::kABytes), &tmA, fb, kb * kBK, m0);
-          tma_load_2d(smem_u32(sB + stage * C::kBBytes), &tmB, fb, kb * kBK, n0);
+          tma_load_2d_hint(smem_u32(sB + stage * C::kBBytes), &tmB, fb, kb * kBK, n0, b_policy);  // weights: every M tile
           armed |= 1u << stage;
           armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
           if (++stage == S) {

@@ -108,7 +108,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // Both CTAs load their halves; every copy completes on the even CTA's stage barrier,
       // which the even CTA arms with the bytes of both halves (tx-count may run ahead of the
       // arm within a phase: the phase cannot complete before the even CTA's arrive).
-      const uint64_t a_policy = l2_policy_evict_first();
+      const uint64_t a_policy = l2_policy_evict_first(), b_policy = l2_policy_evict_last();
       int stage = 0;
       uint32_t phase = 0, armed = 0, armed_phase = 0;
       bool ok = true;
@@ -125,7 +125,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tma_load_2d_pair_hint(smem_u32(sA + stage * C::kABytes), &tmA, fb_even, kb * kBK, m0, a_policy);
           else
             tma_load_2d_pair(smem_u32(sA + stage * C::kABytes), &tmA, fb_even, kb * kBK, m0);
-          tma_load_2d_pair(smem_u32(sB + stage * C::kBBytes), &tmB, fb_even, kb * kBK, n0);
+          tma_load_2d_pair_hint(smem_u32(sB + stage * C::kBBytes), &tmB, fb_even, kb * kBK, n0, b_policy);  // weights: every M tile
           armed |= 1u << stage;
           armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
           if (++stage == kStages) {
