@@ -239,13 +239,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         break;
       }
       tc_fence_after();
-      // the thread's 128 raw scores, read from TMEM once
-      uint32_t s[kKT / 32][32];
-#pragma unroll
-      for (int c = 0; c < kKT / 32; ++c) tmem_ld32(tS + c * 32, s[c]);
-      tmem_ld_wait(s[0]);
-#pragma unroll
-      for (int c = 1; c < kKT / 32; ++c) tmem_ld_bind(s[c]);
+      // the thread's 128 raw scores, read from TMEM in one load
+      uint32_t sr[kKT];
+      tmem_ld128(tS, sr);
+      tmem_ld_wait(sr);
+      uint32_t (&s)[kKT / 32][32] = *reinterpret_cast<uint32_t (*)[kKT / 32][32]>(&sr);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(s_free + g));  // the MMA warp may overwrite S now
@@ -300,19 +298,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       const float2 sc2 = make_float2(sc, sc), nb2 = make_float2(-base, -base);
       float2 ls2[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
                        make_float2(0.0f, 0.0f)};  // four short chains for the row sum
+      uint32_t pk[kKT / 2];
 #pragma unroll
       for (int c = 0; c < kKT / 32; ++c) {
-        uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           const float2 x =
               __ffma2_rn(make_float2(__uint_as_float(s[c][e]), __uint_as_float(s[c][e + 1])), sc2, nb2);
           const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
           ls2[(e >> 1) & 3] = __fadd2_rn(ls2[(e >> 1) & 3], p);
-          pk[e >> 1] = pack_bf16x2(p.x, p.y);
+          pk[c * 16 + (e >> 1)] = pack_bf16x2(p.x, p.y);
         }
-        tmem_st16(tP + c * 16, pk);
       }
+      tmem_st64(tP, pk);
       const float2 l01 = __fadd2_rn(ls2[0], ls2[1]), l23 = __fadd2_rn(ls2[2], ls2[3]);
       l_run += (l01.x + l23.x) + (l01.y + l23.y);
       tmem_st_wait();
