@@ -34,16 +34,16 @@ METRIC = "encoder tokens/s and TFLOP/s (fraction of bf16 peak), ViT-L 16×256² 
 WORKLOAD = dict(preset="vjepa2_vitl16", T=16, H=256, W=256)
 FLUSH_BYTES = 256 << 20  # > 129 MB of L2
 
-# Per-launch DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of a kernel class, from the
-# batch-1 ncu captures of the 2048-token clip; `sha1` is the hash of the class's source files when
+# Per-launch DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of a kernel class, from ncu
+# captures of the 2048-token clips at 8 per GPU; `sha1` is the hash of the class's source files when
 # the counters were taken (a changed kernel reports traffic null until it is captured again).
-NCU_TRAFFIC = {
-    "attention": {"bytes_per_launch": 12.63e6, "batch": 1, "sha1": "1511a9089fe720105e8fd5525f9926fedd8eca90"},
-    "layernorm": {"bytes_per_launch": 8.41e6, "batch": 1, "sha1": "8b7cd377f622007f9d31328489c2f31b9a9b7484"},
-    "gemm_qkv": {"bytes_per_launch": 10.58e6, "batch": 1, "sha1": "399fa54a5c822b7bd74f2d95c23de3da22870726"},
-    "gemm_up": {"bytes_per_launch": 12.65e6, "batch": 1, "sha1": "399fa54a5c822b7bd74f2d95c23de3da22870726"},
-    "gemm_out": {"bytes_per_launch": 14.70e6, "batch": 1, "sha1": "399fa54a5c822b7bd74f2d95c23de3da22870726"},
-    "gemm_down": {"bytes_per_launch": 33.58e6, "batch": 1, "sha1": "399fa54a5c822b7bd74f2d95c23de3da22870726"},
+NCU_TRAFFIC = {  # (kernel class, clips per GPU): bytes per launch, source hash at capture
+    ("attention", 8): {"bytes_per_launch": 112.78e6, "sha1": "58a1e95f818e157373e6c71370eda112659e7ff6"},
+    ("layernorm", 8): {"bytes_per_launch": 68.98e6, "sha1": "39f959c935d12366f5b46a566e219d3edf4e75d6"},
+    ("gemm_qkv", 8): {"bytes_per_launch": 85.51e6, "sha1": "492471294b0890c32ea3405750fc2b5f7a07768d"},
+    ("gemm_out", 8): {"bytes_per_launch": 102.86e6, "sha1": "492471294b0890c32ea3405750fc2b5f7a07768d"},
+    ("gemm_up", 8): {"bytes_per_launch": 120.41e6, "sha1": "492471294b0890c32ea3405750fc2b5f7a07768d"},
+    ("gemm_down", 8): {"bytes_per_launch": 217.99e6, "sha1": "492471294b0890c32ea3405750fc2b5f7a07768d"},
 }
 
 
@@ -375,10 +375,8 @@ def run_ours(args):
         achieved = st["bytes"] / st["launches"] / (avg_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "kernel": name}
-    rec = NCU_TRAFFIC.get(name)
-    # counters were taken at batch 1: other batches report null
-    roof["traffic"] = (rec["bytes_per_launch"]
-                       if rec and rec.get("sha1") == source_sha1(name) and B == rec["batch"] else None)
+    rec = NCU_TRAFFIC.get((name, B))  # null for other batches or changed sources
+    roof["traffic"] = rec["bytes_per_launch"] if rec and rec.get("sha1") == source_sha1(name) else None
     roof["peak_source"] = peaks["source"]
     kernels = {k: {"launches": v["launches"], "avg_us": 1e3 * v["total_ms"] / v["launches"],
                    "share": v["total_ms"] / max(sum(x["total_ms"] for x in prof.values()), 1e-9),
