@@ -28,7 +28,8 @@ class OracleHParams(ctypes.Structure):
         ("in_chans", ctypes.c_int), ("ln_eps", ctypes.c_double), ("rope_theta", ctypes.c_double),
         ("pos_type", ctypes.c_int), ("rope_layout", ctypes.c_int), ("rope_interpolate", ctypes.c_int),
         ("rope_ref_grid", ctypes.c_int), ("cls_token", ctypes.c_int), ("modality_embed", ctypes.c_int),
-        ("attn_mode", ctypes.c_int), ("n_pos_rows", ctypes.c_int),
+        ("attn_mode", ctypes.c_int), ("n_pos_rows", ctypes.c_int), ("img_size", ctypes.c_int),
+        ("n_frames", ctypes.c_int), ("sincos_w_first", ctypes.c_int), ("sincos_uniform_power", ctypes.c_int),
     ]
 
 
@@ -44,7 +45,7 @@ class Config:
     in_chans: int = 3
     ln_eps: float = 1e-6
     rope_theta: float = 10000.0
-    pos_type: int = 0          # 0 none, 1 learned, 2 rope3d
+    pos_type: int = 0          # 0 none, 1 learned, 2 rope3d, 3 sincos2d, 4 sincos3d
     rope_layout: int = 0       # 0 tiled, 1 interleaved
     rope_interpolate: int = 0
     rope_ref_grid: int = 0
@@ -52,6 +53,10 @@ class Config:
     modality_embed: int = 0
     attn_mode: int = 0         # 0 full, 1 block_causal
     n_pos_rows: int = 0
+    img_size: int = 0          # training crop and frames: the grid a sin-cos table is baked for
+    n_frames: int = 0
+    sincos_w_first: int = 0    # sincos2d halves [w | h] (HF I-JEPA order)
+    sincos_uniform_power: int = 0
 
     def struct(self) -> OracleHParams:
         return OracleHParams(**asdict(self))
@@ -97,6 +102,11 @@ def lib():
         L.oracle_rope_tables.argtypes = [hp, I, I, I, P, P]
         L.oracle_rope_apply.argtypes = [P, I, I, I, P, P, P]
         L.oracle_rope_apply.restype = None
+        L.oracle_sincos_2d.argtypes = [I, I, I, I, P]
+        L.oracle_sincos_3d.argtypes = [I, I, I, I, I, P]
+        L.oracle_interp_trilinear.argtypes = [P, I, I, I, I, I, I, I, P]
+        L.oracle_interp_bicubic.argtypes = [P, I, I, I, I, I, P]
+        L.oracle_pos_table.argtypes = [hp, I, I, I, P]
         L.oracle_mask_allow.argtypes = [I, I, I, I, I, I]
         L.oracle_attention.argtypes = [P, P, P, I, I, I, I, I, I, P]
         L.oracle_attention.restype = None
@@ -210,6 +220,53 @@ def rope_apply(x, n_head, cos_t, sin_t) -> np.ndarray:
     hd = x.shape[1] // n_head
     out = np.empty_like(x)
     lib().oracle_rope_apply(x.ctypes.data, N, n_head, hd, cos_t.ctypes.data, sin_t.ctypes.data, out.ctypes.data)
+    return out
+
+
+def sincos_2d(gh, gw, D, w_first=False) -> np.ndarray:
+    """2-D sin-cos table [gh*gw, D], halves [h | w] (or [w | h] when w_first)."""
+    out = np.empty((gh * gw, D), dtype=np.float64)
+    if lib().oracle_sincos_2d(gh, gw, D, int(w_first), out.ctypes.data) != 0:
+        raise ValueError(f"sincos_2d refused width {D}")
+    return out
+
+
+def sincos_3d(gt, gh, gw, D, uniform_power=False) -> np.ndarray:
+    """3-D sin-cos table [gt*gh*gw, D], parts [t | h | w]."""
+    out = np.empty((gt * gh * gw, D), dtype=np.float64)
+    if lib().oracle_sincos_3d(gt, gh, gw, D, int(uniform_power), out.ctypes.data) != 0:
+        raise ValueError(f"sincos_3d refused width {D}")
+    return out
+
+
+def interp_trilinear(src, size) -> np.ndarray:
+    """src [st, sh, sw, D] -> [dt, dh, dw, D] (pixel-centre aligned)."""
+    src = _f64(src)
+    st, sh, sw, D = src.shape
+    dt, dh, dw = size
+    out = np.empty((dt, dh, dw, D), dtype=np.float64)
+    assert lib().oracle_interp_trilinear(src.ctypes.data, st, sh, sw, D, dt, dh, dw, out.ctypes.data) == 0
+    return out
+
+
+def interp_bicubic(src, size) -> np.ndarray:
+    """src [sh, sw, D] -> [dh, dw, D] (pixel-centre aligned, Keys a = -0.75)."""
+    src = _f64(src)
+    sh, sw, D = src.shape
+    dh, dw = size
+    out = np.empty((dh, dw, D), dtype=np.float64)
+    assert lib().oracle_interp_bicubic(src.ctypes.data, sh, sw, D, dh, dw, out.ctypes.data) == 0
+    return out
+
+
+def pos_table(cfg: Config, T, H, W) -> np.ndarray:
+    """The sin-cos table a T x H x W clip adds to its patch rows, [Np, D]."""
+    gt, gh, gw, _ = geometry(cfg, T, H, W)
+    out = np.empty((gt * gh * gw, cfg.embed_dim), dtype=np.float64)
+    s = cfg.struct()
+    rc = lib().oracle_pos_table(ctypes.byref(s), T, H, W, out.ctypes.data)
+    if rc != 0:
+        raise ValueError(f"oracle_pos_table refused the configuration (code {rc})")
     return out
 
 

@@ -244,6 +244,163 @@ void oracle_rope_apply(const double* x, int N, int n_head, int hd, const double*
     }
 }
 
+// ---- fixed sin-cos position tables ([S] "Encoder": sincos2d / sincos3d; [R] sincos_2d, sincos_3d) ----
+
+// One axis of even width d: column k < d/2 is sin(p w_k), column d/2 + k is cos(p w_k), with the
+// d/2 frequencies w_k = 10000^(-k / (d/2)) falling geometrically from 1 towards 1/10000.
+static void sincos_axis(int d, double p, double* out) {
+  const int half = d / 2;
+  for (int k = 0; k < half; ++k) {
+    const double w = std::pow(10000.0, -(double)k / (double)half);
+    out[k] = std::sin(p * w);
+    out[half + k] = std::cos(p * w);
+  }
+}
+
+int oracle_sincos_2d(int gh, int gw, int D, int w_first, double* out) {
+  if (gh <= 0 || gw <= 0 || D <= 0 || D % 4) return -1;
+  const int half = D / 2;
+  for (int i = 0; i < gh * gw; ++i) {
+    const int h = i / gw, w = i % gw;
+    double* row = out + (size_t)i * D;
+    sincos_axis(half, w_first ? w : h, row);
+    sincos_axis(half, w_first ? h : w, row + half);
+  }
+  return 0;
+}
+
+int oracle_sincos_3d(int gt, int gh, int gw, int D, int uniform_power, double* out) {
+  if (gt <= 0 || gh <= 0 || gw <= 0 || D <= 0) return -1;
+  int dt, dh, dw;
+  if (uniform_power) {
+    dt = dh = dw = 2 * ((D + 5) / 6);  // 2 ceil(D / 6)
+  } else {
+    if (D % 8) return -1;
+    dt = D / 2;
+    dh = dw = D / 4;
+  }
+  std::vector<double> full((size_t)(dt + dh + dw));
+  for (int i = 0; i < gt * gh * gw; ++i) {
+    const int t = i / (gh * gw), h = (i / gw) % gh, w = i % gw;
+    sincos_axis(dt, t, full.data());
+    sincos_axis(dh, h, full.data() + dt);
+    sincos_axis(dw, w, full.data() + dt + dh);
+    std::memcpy(out + (size_t)i * D, full.data(), (size_t)D * sizeof(double));  // cut to D columns
+  }
+  return 0;
+}
+
+// Pixel-centre source coordinate of output index o on an axis resized from n_in to n_out samples.
+static double resize_coord(int o, int n_in, int n_out) { return (o + 0.5) * ((double)n_in / (double)n_out) - 0.5; }
+
+// Linear blend on one axis: the two input indices and their weights.
+static void linear_taps(int o, int n_in, int n_out, int idx[2], double wt[2]) {
+  double c = resize_coord(o, n_in, n_out);
+  if (c < 0.0) c = 0.0;
+  int i0 = (int)std::floor(c);
+  if (i0 > n_in - 1) i0 = n_in - 1;
+  const double l1 = c - i0;
+  idx[0] = i0;
+  idx[1] = std::min(i0 + 1, n_in - 1);
+  wt[0] = 1.0 - l1;
+  wt[1] = l1;
+}
+
+// Keys' cubic convolution kernel with a = -0.75.
+static double keys_cubic(double x) {
+  const double a = -0.75;
+  x = std::fabs(x);
+  if (x <= 1.0) return ((a + 2.0) * x - (a + 3.0)) * x * x + 1.0;
+  if (x < 2.0) return ((a * x - 5.0 * a) * x + 8.0 * a) * x - 4.0 * a;
+  return 0.0;
+}
+
+// Cubic taps on one axis: samples floor(c)-1 .. floor(c)+2, clamped to the axis.
+static void cubic_taps(int o, int n_in, int n_out, int idx[4], double wt[4]) {
+  const double c = resize_coord(o, n_in, n_out);
+  const int i0 = (int)std::floor(c);
+  for (int j = 0; j < 4; ++j) {
+    const int s = i0 - 1 + j;
+    idx[j] = std::min(std::max(s, 0), n_in - 1);
+    wt[j] = keys_cubic(c - s);
+  }
+}
+
+int oracle_interp_trilinear(const double* src, int st, int sh, int sw, int D, int dt, int dh, int dw, double* dst) {
+  if (st <= 0 || sh <= 0 || sw <= 0 || D <= 0 || dt <= 0 || dh <= 0 || dw <= 0) return -1;
+#pragma omp parallel for collapse(3) schedule(static)
+  for (int t = 0; t < dt; ++t)
+    for (int h = 0; h < dh; ++h)
+      for (int w = 0; w < dw; ++w) {
+        int it[2], ih[2], iw[2];
+        double at[2], ah[2], aw[2];
+        linear_taps(t, st, dt, it, at);
+        linear_taps(h, sh, dh, ih, ah);
+        linear_taps(w, sw, dw, iw, aw);
+        double* out = dst + (((size_t)t * dh + h) * dw + w) * D;
+        for (int c = 0; c < D; ++c) out[c] = 0.0;
+        for (int a = 0; a < 2; ++a)
+          for (int b = 0; b < 2; ++b)
+            for (int e = 0; e < 2; ++e) {
+              const double wt = at[a] * ah[b] * aw[e];
+              const double* in = src + (((size_t)it[a] * sh + ih[b]) * sw + iw[e]) * D;
+              for (int c = 0; c < D; ++c) out[c] += wt * in[c];
+            }
+      }
+  return 0;
+}
+
+int oracle_interp_bicubic(const double* src, int sh, int sw, int D, int dh, int dw, double* dst) {
+  if (sh <= 0 || sw <= 0 || D <= 0 || dh <= 0 || dw <= 0) return -1;
+#pragma omp parallel for collapse(2) schedule(static)
+  for (int h = 0; h < dh; ++h)
+    for (int w = 0; w < dw; ++w) {
+      int ih[4], iw[4];
+      double ah[4], aw[4];
+      cubic_taps(h, sh, dh, ih, ah);
+      cubic_taps(w, sw, dw, iw, aw);
+      double* out = dst + ((size_t)h * dw + w) * D;
+      for (int c = 0; c < D; ++c) out[c] = 0.0;
+      for (int a = 0; a < 4; ++a)
+        for (int b = 0; b < 4; ++b) {
+          const double wt = ah[a] * aw[b];
+          const double* in = src + ((size_t)ih[a] * sw + iw[b]) * D;
+          for (int c = 0; c < D; ++c) out[c] += wt * in[c];
+        }
+    }
+  return 0;
+}
+
+// [S] "Encoder": the table is baked for the training grid; other grids get it resized (bicubic for
+// the 2-D image table, trilinear for the 3-D video table).
+int oracle_pos_table(const oracle_hparams* hp, int T, int H, int W, double* out) {
+  Geometry g;
+  if (!geometry(hp, T, H, W, &g)) return -1;
+  const int D = hp->embed_dim;
+  if (hp->pos_type != 3 && hp->pos_type != 4) return -1;
+  if (hp->img_size <= 0 || hp->img_size % hp->patch_size) return -1;
+  const int gh0 = hp->img_size / hp->patch_size, gw0 = gh0;
+  if (hp->pos_type == 3) {
+    if (g.gt != 1) return -2;  // a 2-D table has no time axis
+    std::vector<double> t0((size_t)gh0 * gw0 * D);
+    if (oracle_sincos_2d(gh0, gw0, D, hp->sincos_w_first, t0.data())) return -1;
+    if (g.gh == gh0 && g.gw == gw0) {
+      std::memcpy(out, t0.data(), t0.size() * sizeof(double));
+      return 0;
+    }
+    return oracle_interp_bicubic(t0.data(), gh0, gw0, D, g.gh, g.gw, out);
+  }
+  if (hp->n_frames <= 0 || hp->n_frames % hp->tubelet_size) return -1;
+  const int gt0 = hp->n_frames / hp->tubelet_size;
+  std::vector<double> t0((size_t)gt0 * gh0 * gw0 * D);
+  if (oracle_sincos_3d(gt0, gh0, gw0, D, hp->sincos_uniform_power, t0.data())) return -1;
+  if (g.gt == gt0 && g.gh == gh0 && g.gw == gw0) {
+    std::memcpy(out, t0.data(), t0.size() * sizeof(double));
+    return 0;
+  }
+  return oracle_interp_trilinear(t0.data(), gt0, gh0, gw0, D, g.gt, g.gh, g.gw, out);
+}
+
 // [S] levjepa note; [A] "Block-causal attention": key j visible to query i iff
 // frame_id(i) >= frame_id(j), frame_id = id // (gh gw) of the patch token; CLS row open,
 // CLS column closed to patch queries.
@@ -308,6 +465,7 @@ int oracle_encode(const oracle_hparams* hp, uint64_t seed, int bf16_weights, con
   const int hd = D / NH;
   const int N = g.N, Np = g.Np, prefix = g.prefix;
   if (hp->pos_type == 1 && hp->n_pos_rows != N) return -2;  // learned table must cover every token
+  if ((hp->pos_type == 3 || hp->pos_type == 4) && prefix) return -2;  // sin-cos tables cover patch rows only
   const size_t MD = (size_t)N * D;
 
   // ---- patch embedding, prefix and position/modality terms ----
@@ -325,6 +483,11 @@ int oracle_encode(const oracle_hparams* hp, uint64_t seed, int bf16_weights, con
   std::vector<double> cls, pos, mod;
   if (hp->cls_token) gen_param(seed, "enc.cls_token", bf16_weights, D, cls);
   if (hp->pos_type == 1) gen_param(seed, "enc.pos_embed", bf16_weights, (size_t)hp->n_pos_rows * D, pos);
+  if (hp->pos_type == 3 || hp->pos_type == 4) {
+    pos.resize((size_t)Np * D);
+    const int rc = oracle_pos_table(hp, T, H, W, pos.data());
+    if (rc) return rc;
+  }
   if (hp->modality_embed) gen_param(seed, "enc.mod_embed_video", bf16_weights, D, mod);
   for (int b = 0; b < B; ++b)
     for (int n = 0; n < N; ++n) {
@@ -332,6 +495,7 @@ int oracle_encode(const oracle_hparams* hp, uint64_t seed, int bf16_weights, con
       for (int c = 0; c < D; ++c) {
         double v = (n < prefix) ? cls[c] : emb[((size_t)b * Np + (n - prefix)) * D + c];
         if (hp->pos_type == 1) v += pos[(size_t)n * D + c];  // rows = [CLS?; patches]
+        if (hp->pos_type == 3 || hp->pos_type == 4) v += pos[(size_t)n * D + c];  // patch rows, no prefix
         if (hp->modality_embed) v += mod[c];
         xr[c] = v;
       }

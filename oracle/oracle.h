@@ -11,6 +11,7 @@
  *   [A] = jepa.cpp "Architecture"          (shared ViT graph, 3-D RoPE, block-causal attention)
  *   [C] = jepa.cpp "Converter"             (conv flattening, qkv fusing, hfvit/levjepa maps)
  *   [K] = SkyVision.cpp README, V-JEPA 2 section (tubelet packing order, tiled-RoPE quirk)
+ *   [R] = jepa.cpp "Converter" reference table (sincos_2d / sincos_3d helpers, ijepa table order)
  *
  * All arithmetic is double precision; bf16 inputs (weights of the bf16 mode)
  * enter as their exact values.
@@ -30,7 +31,7 @@ typedef struct {
   int embed_dim, n_layer, n_head, ffn_dim;
   int patch_size, tubelet_size, in_chans;
   double ln_eps, rope_theta;
-  int pos_type;         /* 0 none, 1 learned table, 2 rope3d */
+  int pos_type;         /* 0 none, 1 learned table, 2 rope3d, 3 sincos2d, 4 sincos3d */
   int rope_layout;      /* 0 tiled (V-JEPA 2), 1 interleaved (V-JEPA 2.1) */
   int rope_interpolate; /* V-JEPA 2.1 interpolate_rope */
   int rope_ref_grid;    /* 256 / patch_size */
@@ -38,6 +39,10 @@ typedef struct {
   int modality_embed;   /* add enc.mod_embed_video to every token */
   int attn_mode;        /* 0 full, 1 block_causal */
   int n_pos_rows;       /* rows of enc.pos_embed (learned only) */
+  int img_size;         /* training crop: the sin-cos table covers (img/P) x (img/P) ... */
+  int n_frames;         /* ... x (frames/t) positions */
+  int sincos_w_first;   /* sincos2d halves ordered [w | h] (HF I-JEPA) instead of [h | w] */
+  int sincos_uniform_power; /* sincos3d: three equal axis widths 2*ceil(D/6), cut to D */
 } oracle_hparams;
 
 /* Number of tokens of one item: (T/t)(H/P)(W/P) + cls. Returns -1 if a size is not divisible. */
@@ -76,6 +81,35 @@ int oracle_rope_tables(const oracle_hparams* hp, int T, int H, int W, double* co
 /* Apply the tables to x [N, H*hd] in place-free form (q and k of every head). */
 void oracle_rope_apply(const double* x, int N, int n_head, int hd, const double* cos_t, const double* sin_t,
                        double* out);
+
+/* Fixed sin-cos position tables ([S] "Encoder": sincos2d / sincos3d, baked at conversion for the
+ * training grid; [R] sincos_2d, sincos_3d). One axis of even width d maps position p to
+ * [sin(p w_0) .. sin(p w_{d/2-1}), cos(p w_0) .. cos(p w_{d/2-1})], w_k = 10000^(-k/(d/2)).
+ * sincos_2d: rows i = h*gw + w, columns [axis(h) | axis(w)] of width D/2 each, or [axis(w) | axis(h)]
+ *   when w_first (the order of the HF I-JEPA table). D % 4 == 0. out: [gh*gw, D].
+ * sincos_3d: rows i = (t*gh + h)*gw + w, columns [axis(t) | axis(h) | axis(w)] of widths
+ *   (D/2, D/4, D/4), or 2*ceil(D/6) each when uniform_power, the row then cut to its first D
+ *   columns. out: [gt*gh*gw, D]. Returns -1 on a width the split cannot take. */
+int oracle_sincos_2d(int gh, int gw, int D, int w_first, double* out);
+int oracle_sincos_3d(int gt, int gh, int gw, int D, int uniform_power, double* out);
+
+/* Resizing a position table to another grid ([S] "Encoder": the runtime interpolates the
+ * training-grid table for other grids; [S] ijepa note: as HF does). Pixel-centre alignment
+ * (align_corners off): output index o of an axis resized from n_in to n_out samples reads the
+ * input at c = (o + 1/2) n_in / n_out - 1/2.
+ * trilinear: src [st, sh, sw, D] -> dst [dt, dh, dw, D]; per axis c is clamped at 0 and the two
+ *   neighbours floor(c), floor(c)+1 (the latter clamped to n_in-1) are blended linearly.
+ * bicubic: src [sh, sw, D] -> dst [dh, dw, D]; per axis the four samples floor(c)-1 .. floor(c)+2
+ *   (indices clamped to [0, n_in-1]) are weighted by Keys' cubic convolution kernel, a = -0.75.
+ * Returns -1 on a non-positive size. */
+int oracle_interp_trilinear(const double* src, int st, int sh, int sw, int D, int dt, int dh, int dw, double* dst);
+int oracle_interp_bicubic(const double* src, int sh, int sw, int D, int dh, int dw, double* dst);
+
+/* The position table one clip adds to its patch rows, [gt*gh*gw, D], for pos_type 3 / 4: the
+ * sin-cos table of the training grid ((n_frames/t) x (img/P) x (img/P); one frame for sincos2d),
+ * resized to the clip's grid when they differ (bicubic for sincos2d, trilinear for sincos3d).
+ * Returns -1 on a bad size, -2 when the table cannot serve the clip (sincos2d on several frames). */
+int oracle_pos_table(const oracle_hparams* hp, int T, int H, int W, double* out);
 
 /* Is key k visible to query q? attn_mode 0: every k < N. attn_mode 1 (block-causal,
  * [S] levjepa note; [A] "Block-causal attention"): prefix rows see everything, prefix

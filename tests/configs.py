@@ -1,9 +1,12 @@
-"""The five workloads of the encoder (synthetic inputs), in the jepa.enc.* vocabulary.
+"""The workloads of the encoder (synthetic inputs), in the jepa.enc.* vocabulary.
 
 Shapes follow the pages' ViT-Ti/L/g image and video workloads:
   hfvit Ti/14 224^2 image (fp32), V-JEPA 2 ViT-L/16 16x256^2 video (bf16, batch 1 and 8),
   V-JEPA 2.1 ViT-L/16 16x384^2 (interleaved RoPE + interpolate_rope + modality vector),
-  LeVJEPA ViT-L/16 16x256^2 tubelet 1 (CLS + block-causal), V-JEPA 2 ViT-g/16 64x256^2.
+  LeVJEPA ViT-L/16 16x256^2 tubelet 1 (CLS + block-causal), V-JEPA 2 ViT-g/16 64x256^2,
+  and the two fixed-table families at ViT-L/16 width: V-JEPA with its 3-D sin-cos table baked
+  for 16x224^2 and resized (trilinear) to a 16x256^2 clip, I-JEPA with its [w | h] 2-D table
+  baked for 224^2 and resized (bicubic) to 256^2 images, 8 per call.
 `small()` shrinks a workload (frames, image size, depth) so the oracle finishes in
 seconds while the geometry still spans several 128-row tiles with a ragged tail.
 """
@@ -19,6 +22,10 @@ VJEPA2_1_L16 = Config(embed_dim=1024, n_layer=24, n_head=16, ffn_dim=4096, patch
                       pos_type=2, rope_layout=1, rope_interpolate=1, rope_ref_grid=16, modality_embed=1)
 LEVJEPA_L16 = Config(embed_dim=1024, n_layer=24, n_head=16, ffn_dim=4096, patch_size=16, tubelet_size=1,
                      pos_type=2, rope_layout=0, cls_token=1, attn_mode=1)
+VJEPA_L16 = Config(embed_dim=1024, n_layer=24, n_head=16, ffn_dim=4096, patch_size=16, tubelet_size=2,
+                   pos_type=4, img_size=224, n_frames=16, sincos_uniform_power=1)
+IJEPA_L16 = Config(embed_dim=1024, n_layer=24, n_head=16, ffn_dim=4096, patch_size=16, tubelet_size=1,
+                   pos_type=3, img_size=224, n_frames=1, sincos_w_first=1)
 VJEPA2_G16 = Config(embed_dim=1408, n_layer=40, n_head=22, ffn_dim=6144, patch_size=16, tubelet_size=2,
                     pos_type=2, rope_layout=0)
 
@@ -45,4 +52,8 @@ def small(name: str, n_layer: int = 2):
         return replace(cfg, n_layer=n_layer), dtype, (3, 160, 144)      # 3x10x9 + CLS = 271 tokens
     if name == "vjepa2_vitg16_64x256":
         return replace(cfg, n_layer=n_layer), dtype, (4, 160, 192)      # 2x10x12 = 240 tokens
+    if name == "vjepa_vitl16_16x256":   # table baked for 2x12x12, resized to 2x13x11 = 286 tokens
+        return replace(cfg, n_layer=n_layer, n_frames=4, img_size=192), dtype, (4, 208, 176)
+    if name == "ijepa_vitl16_256":      # table baked for 14x14, resized to 17x15 = 255 tokens
+        return replace(cfg, n_layer=n_layer), dtype, (1, 272, 240)
     raise KeyError(name)
