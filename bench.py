@@ -7,7 +7,12 @@ weights and pixels. A step is one jepa_encode of the batch (patchify, patch GEMM
 final norm) on inputs resident in HBM. The line also carries the same clip at batch 1 ("batch1"),
 timed the same way.
 
-    python bench.py [--gpus N --steps K --warmup W] [--batch B] [--impl reference]
+--workload picks one of the fixed-table families instead: V-JEPA ViT-L/16 16 x 256 x 256 clips
+whose 3-D sin-cos table is baked for 16 x 224 x 224 and resized (trilinear), or I-JEPA-style
+ViT-L/16 256 x 256 images whose 2-D table is baked for 224 x 224 and resized (bicubic). Their
+lines add the one-off table kernels' times ("pos_table").
+
+    python bench.py [--gpus N --steps K --warmup W] [--batch B] [--workload NAME] [--impl reference]
 
 Timing: W untimed steps, then K steps replaying one CUDA graph of the encode, each bracketed by
 CUDA events on the context stream, with a 256 MiB write between steps to flush L2 (outside the
@@ -31,19 +36,31 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "encoder tokens/s and TFLOP/s (fraction of bf16 peak), ViT-L 16×256² video"
-WORKLOAD = dict(preset="vjepa2_vitl16", T=16, H=256, W=256)
+BENCH_WORKLOADS = {
+    "vjepa2_vitl16_16x256": dict(preset="vjepa2_vitl16", T=16, H=256, W=256, batch=8, metric=METRIC,
+                                 label="V-JEPA 2 ViT-L/16 16x256x256 clip"),
+    "vjepa_vitl16_16x256": dict(preset="vjepa_vitl16", T=16, H=256, W=256, batch=8,
+                                metric="encoder tokens/s and TFLOP/s, V-JEPA ViT-L/16 16×256² video, 3-D sin-cos table",
+                                label="V-JEPA ViT-L/16 16x256x256 clip (3-D sin-cos table baked for 16x224x224, "
+                                      "resized trilinear)"),
+    "ijepa_vitl16_256": dict(preset="ijepa_vitl16", T=1, H=256, W=256, batch=64,
+                             metric="encoder tokens/s and TFLOP/s, I-JEPA-style ViT-L/16 256² image, 2-D sin-cos table",
+                             label="I-JEPA-style ViT-L/16 256x256 image (2-D [w|h] sin-cos table baked for 224x224, "
+                                   "resized bicubic)"),
+}
+HEADLINE = "vjepa2_vitl16_16x256"
 FLUSH_BYTES = 256 << 20  # > 129 MB of L2
 
 # Per-launch DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of a kernel class, from ncu
 # captures of the 2048-token clips at 8 per GPU; `sha1` is the hash of the class's source files when
 # the counters were taken (a changed kernel reports traffic null until it is captured again).
-NCU_TRAFFIC = {  # (kernel class, clips per GPU): bytes per launch, source hash at capture
-    ("attention", 8): {"bytes_per_launch": 112.78e6, "sha1": "58a1e95f818e157373e6c71370eda112659e7ff6"},
-    ("layernorm", 8): {"bytes_per_launch": 68.98e6, "sha1": "39f959c935d12366f5b46a566e219d3edf4e75d6"},
-    ("gemm_qkv", 8): {"bytes_per_launch": 85.51e6, "sha1": "492471294b0890c32ea3405750fc2b5f7a07768d"},
-    ("gemm_out", 8): {"bytes_per_launch": 102.86e6, "sha1": "492471294b0890c32ea3405750fc2b5f7a07768d"},
-    ("gemm_up", 8): {"bytes_per_launch": 120.41e6, "sha1": "492471294b0890c32ea3405750fc2b5f7a07768d"},
-    ("gemm_down", 8): {"bytes_per_launch": 217.99e6, "sha1": "492471294b0890c32ea3405750fc2b5f7a07768d"},
+NCU_TRAFFIC = {  # (workload, kernel class, clips per GPU): bytes per launch, source hash at capture
+    (HEADLINE, "attention", 8): {"bytes_per_launch": 112.78e6, "sha1": "58a1e95f818e157373e6c71370eda112659e7ff6"},
+    (HEADLINE, "layernorm", 8): {"bytes_per_launch": 68.98e6, "sha1": "39f959c935d12366f5b46a566e219d3edf4e75d6"},
+    (HEADLINE, "gemm_qkv", 8): {"bytes_per_launch": 85.51e6, "sha1": "492471294b0890c32ea3405750fc2b5f7a07768d"},
+    (HEADLINE, "gemm_out", 8): {"bytes_per_launch": 102.86e6, "sha1": "492471294b0890c32ea3405750fc2b5f7a07768d"},
+    (HEADLINE, "gemm_up", 8): {"bytes_per_launch": 120.41e6, "sha1": "492471294b0890c32ea3405750fc2b5f7a07768d"},
+    (HEADLINE, "gemm_down", 8): {"bytes_per_launch": 217.99e6, "sha1": "492471294b0890c32ea3405750fc2b5f7a07768d"},
 }
 
 
@@ -52,7 +69,8 @@ def parse_args(argv=None):
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=50)
     p.add_argument("--warmup", type=int, default=5)
-    p.add_argument("--batch", type=int, default=8, help="clips per GPU per step")
+    p.add_argument("--batch", type=int, default=None, help="clips per GPU per step (default: the workload's)")
+    p.add_argument("--workload", choices=sorted(BENCH_WORKLOADS), default=HEADLINE)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true")
     return p.parse_args(argv)
@@ -148,7 +166,7 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ oracle timing (host cores)
-def oracle_layer_times(n_tokens_hint=None):
+def oracle_layer_times(workload=HEADLINE):
     """Time the oracle on the workload clip with 1 and 2 transformer layers; returns
     (t1, t2, tokens, threads). Full-depth time = t1 + (L - 1) (t2 - t1)."""
     import numpy as np
@@ -157,7 +175,7 @@ def oracle_layer_times(n_tokens_hint=None):
     import synth
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     from configs import WORKLOADS
-    cfg, _, _, (T, H, W) = WORKLOADS["vjepa2_vitl16_16x256"]
+    cfg, _, _, (T, H, W) = WORKLOADS[workload]
     pix = synth.pixels(0, (1, T, 3, H, W))
     times = []
     for nl in (1, 2):
@@ -167,12 +185,12 @@ def oracle_layer_times(n_tokens_hint=None):
     return times[0], times[1], oracle.n_tokens(cfg, T, H, W), oracle.num_threads(), cfg.n_layer
 
 
-def cpu_baseline():
-    t1, t2, N, threads, L = oracle_layer_times()
+def cpu_baseline(workload=HEADLINE):
+    t1, t2, N, threads, L = oracle_layer_times(workload)
     per_layer = max(t2 - t1, 1e-9)
     full = t1 + (L - 1) * per_layer
     return {"value": N / full, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-            "sample": f"fp64 oracle encodes of the same 2048-token clip with 1 and 2 of the {L} layers "
+            "sample": f"fp64 oracle encodes of the same {N}-token item with 1 and 2 of the {L} layers "
                       f"({t1:.2f} s, {t2:.2f} s); full-depth time {full:.1f} s extrapolated linearly per layer"}
 
 
@@ -185,11 +203,12 @@ def run_reference(args):
     import synth
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     from configs import WORKLOADS
-    cfg, _, _, (T, H, W) = WORKLOADS["vjepa2_vitl16_16x256"]
+    wl = BENCH_WORKLOADS[args.workload]
+    cfg, _, _, (T, H, W) = WORKLOADS[args.workload]
     pix = synth.pixels(0, (1, T, 3, H, W))
     one = replace(cfg, n_layer=1)
     # calibration: the per-layer cost (2 layers minus 1 layer)
-    t1, t2, N, threads, L = oracle_layer_times()
+    t1, t2, N, threads, L = oracle_layer_times(args.workload)
     per_layer = max(t2 - t1, 1e-9)
     for _ in range(args.warmup):
         oracle.encode(one, 0, True, pix)
@@ -202,14 +221,14 @@ def run_reference(args):
     wall = time.perf_counter() - t_start
     mean_full = statistics.mean(full_times)
     value = N / mean_full
-    B = args.batch
-    sample = (f"each step: the fp64 oracle on one 2048-token clip with 1 of the {L} layers; the other {L - 1} "
-              f"layers added at the calibrated per-layer time {per_layer:.2f} s; the {B} clips of a step are "
-              f"independent, so a step costs {B} such clips")
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+    B = args.batch or wl["batch"]
+    sample = (f"each step: the fp64 oracle on one {N}-token item with 1 of the {L} layers; the other {L - 1} "
+              f"layers added at the calibrated per-layer time {per_layer:.2f} s; the {B} items of a step are "
+              f"independent, so a step costs {B} such items")
+    line = {"impl": "reference", "metric": wl["metric"], "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * mean_full * B, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": f"V-JEPA 2 ViT-L/16 16x256x256 clip ({N} tokens) x {B} per GPU",
+            "config": {"workload": f"{wl['label']} ({N} tokens) x {B} per GPU",
                        "tokens_per_step": B * N, "global_batch": B, "seq_len": N,
                        "wall_s_sampled_steps": wall},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample},
@@ -236,11 +255,11 @@ def source_sha1(kernel_class: str):
     return h.hexdigest()
 
 
-def time_graph_steps(jv, model, B, steps, warmup, flush, rank):
+def time_graph_steps(jv, model, wl, B, steps, warmup, flush, rank):
     """ms per step of graph-replayed encodes of B clips (L2 flushed between steps)."""
     import torch
     import synth
-    T, H, W = WORKLOAD["T"], WORKLOAD["H"], WORKLOAD["W"]
+    T, H, W = wl["T"], wl["H"], wl["W"]
     ctx = jv.Context(model, B, T, H, W, graph=True)
     pix = torch.from_numpy(synth.pixels(rank, (B, T, 3, H, W))).cuda()
     out = torch.empty((B, model.n_tokens(T, H, W), model.hp.embed_dim), dtype=torch.float32, device="cuda")
@@ -261,6 +280,42 @@ def time_graph_steps(jv, model, B, steps, warmup, flush, rank):
     return statistics.mean(a.elapsed_time(b) for a, b in ev)
 
 
+def time_pos_tables(jv, model, T, H, W, reps=20):
+    """The one-off table kernels of a fixed-table model: the training-grid table (at load) and its
+    resize to the clip grid (once per clip shape), each timed alone with CUDA events."""
+    import torch
+    hp = model.hp
+    three = hp.pos_type == jv.POS_SINCOS3D
+    grid0 = ((hp.n_frames // hp.tubelet_size) if three else 1, hp.img_size // hp.patch_size, hp.img_size // hp.patch_size)
+    grid1 = (T // hp.tubelet_size, H // hp.patch_size, W // hp.patch_size)
+    D = hp.embed_dim
+    mode = jv.RESIZE_TRILINEAR if three else jv.RESIZE_BICUBIC
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return 1e3 * e0.elapsed_time(e1) / reps
+
+    base = jv.ops.sincos_table(hp.pos_type, *grid0, D, bool(hp.sincos_w_first), bool(hp.sincos_uniform_power))
+    us_table = timed(lambda: jv.ops.sincos_table(hp.pos_type, *grid0, D, bool(hp.sincos_w_first),
+                                                 bool(hp.sincos_uniform_power)))
+    us_resize = timed(lambda: jv.ops.pos_resize(base, grid0, grid1, mode))
+    rows0, rows1 = grid0[0] * grid0[1] * grid0[2], grid1[0] * grid1[1] * grid1[2]
+    resize_bytes = 4.0 * D * (rows0 + rows1)   # the source table once, the resized table once
+    return {"train_grid": list(grid0), "clip_grid": list(grid1),
+            "table_us": us_table, "table_bytes": 4.0 * D * rows0,
+            "resize_us": us_resize, "resize_mode": "trilinear" if three else "bicubic",
+            "resize_bytes": resize_bytes, "resize_gbs": resize_bytes / (us_resize * 1e-6) / 1e9,
+            "note": "outside the step: the table is baked at load, the resize runs once per clip shape; "
+                    "both tables fit in L2, timed back to back without a flush"}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -274,8 +329,9 @@ def run_ours(args):
     import jepa_vision_encoder_gb300 as jv
     import synth
 
-    B, T, H, W = args.batch, WORKLOAD["T"], WORKLOAD["H"], WORKLOAD["W"]
-    model = jv.Model.preset(WORKLOAD["preset"], seed=0, dtype="bf16", device=local)
+    wl = BENCH_WORKLOADS[args.workload]
+    B, T, H, W = args.batch or wl["batch"], wl["T"], wl["H"], wl["W"]
+    model = jv.Model.preset(wl["preset"], seed=0, dtype="bf16", device=local)
     ctx = jv.Context(model, B, T, H, W)
     N = model.n_tokens(T, H, W)
     D = model.hp.embed_dim
@@ -375,7 +431,7 @@ def run_ours(args):
         achieved = st["bytes"] / st["launches"] / (avg_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "kernel": name}
-    rec = NCU_TRAFFIC.get((name, B))  # null for other batches or changed sources
+    rec = NCU_TRAFFIC.get((args.workload, name, B))  # null for other workloads, batches or changed sources
     roof["traffic"] = rec["bytes_per_launch"] if rec and rec.get("sha1") == source_sha1(name) else None
     roof["peak_source"] = peaks["source"]
     kernels = {k: {"launches": v["launches"], "avg_us": 1e3 * v["total_ms"] / v["launches"],
@@ -401,18 +457,19 @@ def run_ours(args):
     # the same clip at batch 1 (latency case of the workload), measured the same way
     b1 = None
     if B != 1:
-        ms1 = reduce_max(time_graph_steps(jv, model, 1, min(args.steps, 50), args.warmup, flush, rank),
+        ms1 = reduce_max(time_graph_steps(jv, model, wl, 1, min(args.steps, 50), args.warmup, flush, rank),
                          device="cuda" if world > 1 else None)
         fl1 = flops_per_step / B
         b1 = {"ms_per_step": ms1, "value": world * N / (ms1 / 1e3), "unit": "tokens/s",
               "tflops": world * fl1 / (ms1 / 1e3) / 1e12,
               "frac_of_bf16_peak": fl1 / (ms1 / 1e3) / 1e12 / peaks["bf16_tflops"]}
+    pos_table = time_pos_tables(jv, model, T, H, W) if model.hp.pos_type in (jv.POS_SINCOS2D, jv.POS_SINCOS3D) else None
     line = None
     if rank == 0:
-        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        line = {"metric": wl["metric"], "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-                "config": {"workload": f"V-JEPA 2 ViT-L/16 16x256x256 clip ({N} tokens) x {B} per GPU",
+                "config": {"workload": f"{wl['label']} ({N} tokens) x {B} per GPU",
                            "tokens_per_step": tokens_per_step, "global_batch": world * B, "seq_len": N,
                            "parallelism": f"replicas x{world} (independent clips, no collective)",
                            "l2": "flushed (256 MiB write) between steps", "weights": "seeded synthetic"},
@@ -423,8 +480,10 @@ def run_ours(args):
                 "clocks": {k: v for k, v in clk.summary().items()},
                 "profiled_pass": {"ms_per_step": p0.elapsed_time(p1) / args.steps,
                                   "clocks": clk_prof.summary()}}
+        if pos_table:
+            line["pos_table"] = pos_table
         if world == 1 and not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline()
+            line["cpu_baseline"] = cpu_baseline(args.workload)
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

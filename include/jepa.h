@@ -53,7 +53,14 @@ typedef enum {
 } jepa_status;
 
 typedef enum { JEPA_FP32 = 0, JEPA_BF16 = 1 } jepa_dtype;
-typedef enum { JEPA_POS_NONE = 0, JEPA_POS_LEARNED = 1, JEPA_POS_ROPE3D = 2 } jepa_pos_type;
+typedef enum {
+  JEPA_POS_NONE = 0,
+  JEPA_POS_LEARNED = 1,
+  JEPA_POS_ROPE3D = 2,
+  JEPA_POS_SINCOS2D = 3, /* fixed 2-D sin-cos table (I-JEPA) */
+  JEPA_POS_SINCOS3D = 4  /* fixed 3-D sin-cos table (V-JEPA) */
+} jepa_pos_type;
+typedef enum { JEPA_RESIZE_TRILINEAR = 0, JEPA_RESIZE_BICUBIC = 1 } jepa_resize_mode;
 typedef enum { JEPA_ROPE_TILED = 0, JEPA_ROPE_INTERLEAVED = 1 } jepa_rope_layout;
 typedef enum { JEPA_ATTN_FULL = 0, JEPA_ATTN_BLOCK_CAUSAL = 1 } jepa_attn_mode;
 typedef enum { JEPA_LAYOUT_TCHW = 0, JEPA_LAYOUT_CTHW = 1 } jepa_pixel_layout;
@@ -61,18 +68,28 @@ typedef enum { JEPA_LAYOUT_TCHW = 0, JEPA_LAYOUT_CTHW = 1 } jepa_pixel_layout;
 /* Encoder hyper-parameters, mirroring the jepa.enc.* keys ("GGUF schema (v1)", Encoder).
  *  pos_type        JEPA_POS_LEARNED: enc.pos_embed [n_pos_rows, D], rows = [CLS?; patches]
  *                  JEPA_POS_ROPE3D : 3-D RoPE on q and k ("Architecture", 3-D RoPE)
+ *                  JEPA_POS_SINCOS2D / SINCOS3D: enc.pos_embed is the fixed sin-cos table of the
+ *                  training grid (img_size/P)^2 (x n_frames/t for 3-D), baked at load; a clip of
+ *                  another grid adds that table resized to its own grid, bicubic for 2-D and
+ *                  trilinear for 3-D ("GGUF schema (v1)", Encoder: sincos tables). Patch rows
+ *                  only: no CLS token; a 2-D table serves single-frame clips only.
  *  rope_layout     tiled (V-JEPA 2) or interleaved (V-JEPA 2.1) cos/sin table layout
  *  rope_interpolate, rope_ref_grid   V-JEPA 2.1: h, w rescaled by (ref-1)/(grid-1)
  *  cls_token       prepend enc.cls_token (no position information for it)
  *  modality_embed  add enc.mod_embed_video to every token (V-JEPA 2.1)
  *  attn_mode       full, or LeVJEPA's block-causal mask ("Architecture", Block-causal attention)
- *  img_size, n_frames  training geometry (informational; jepa_encode takes the clip's own T,H,W) */
+ *  img_size, n_frames  training geometry: the grid a sin-cos table is baked for (otherwise
+ *                  informational; jepa_encode takes the clip's own T,H,W)
+ *  sincos_w_first  2-D table halves ordered [w | h] (the HF I-JEPA table) instead of [h | w]
+ *  sincos_uniform_power  3-D table with three equal axis widths 2*ceil(D/6), cut to D, instead
+ *                  of (D/2, D/4, D/4) ("Converter", sincos_3d(..., uniform_power)) */
 typedef struct {
   int32_t embed_dim, n_layer, n_head, ffn_dim;
   int32_t patch_size, tubelet_size, img_size, n_frames, in_chans;
   float ln_eps, rope_theta;
   int32_t pos_type, rope_layout, rope_interpolate, rope_ref_grid;
   int32_t cls_token, modality_embed, attn_mode, n_pos_rows;
+  int32_t sincos_w_first, sincos_uniform_power;
 } jepa_hparams;
 
 /* ------------------------------------------------------------------ configuration */
@@ -83,12 +100,18 @@ typedef struct {
  *  "vjepa2_1_vitl16" V-JEPA 2.1 ViT-L/16, interleaved RoPE, interpolate_rope (ref grid 16), modality vector
  *  "levjepa_vitl16"  LeVJEPA ViT-L/16, tubelet 1, CLS, tiled RoPE, block-causal
  *  "vjepa2_vitg16"   V-JEPA 2 ViT-g/16 (embed 1408, 40 layers, 22 heads, ffn 6144)
+ *  "vjepa_vitl16"    V-JEPA ViT-L/16, tubelet 2, 3-D sin-cos table (uniform power) baked for 16x224^2
+ *  "ijepa_vitl16"    I-JEPA-style image encoder at ViT-L/16 width, [w | h] 2-D sin-cos table baked
+ *                    for 224^2 (the released I-JEPA widths have head_dim 80 / 88, which this
+ *                    build refuses)
  * Unknown name -> JEPA_E_INVALID_ARG. */
 jepa_status jepa_preset(const char* name, jepa_hparams* out);
 
 /* Range and invariant checks of "Architecture", Robustness (what the loader validates):
  * sizes in range, embed_dim % n_head == 0, even head width on a RoPE model, rope_interpolate
- * with a ref grid, ln_eps in [0, 1], rope_theta > 0, a learned table with rows. */
+ * with a ref grid, ln_eps in [0, 1], rope_theta > 0, a learned table with rows, a sin-cos table
+ * with a training grid (img_size a multiple of the patch; for 3-D n_frames a multiple of the
+ * tubelet) and a width its split can take (2-D: D % 4 == 0; 3-D: D % 8 == 0 unless uniform). */
 jepa_status jepa_hparams_validate(const jepa_hparams* hp);
 
 /* Tokens of one item of a T x H x W clip: (T/t)(H/P)(W/P) + cls ("GGUF schema (v1)", Token order).
@@ -226,6 +249,30 @@ jepa_status jepa_op_linear(int32_t dtype, const void* d_x, int32_t M, int32_t K,
  * positions (t, h, w) of patch i (h, w rescaled for rope_interpolate). */
 jepa_status jepa_op_rope_table(const jepa_hparams* hp, int32_t T, int32_t H, int32_t W, float* d_table,
                                void* stream);
+
+/* Fixed sin-cos position table ("GGUF schema (v1)", Encoder: sincos tables; "Converter",
+ * sincos_2d / sincos_3d). One axis of even width d maps position p to
+ * [sin(p w_0) .. sin(p w_{d/2-1}), cos(p w_0) .. cos(p w_{d/2-1})], w_k = 10000^(-k/(d/2)).
+ *  kind JEPA_POS_SINCOS2D: gt must be 1; row i = h*gw + w holds [axis(h) | axis(w)], each D/2
+ *       wide, or [axis(w) | axis(h)] when w_first. D % 4 == 0.
+ *  kind JEPA_POS_SINCOS3D: row i = (t*gh + h)*gw + w holds [axis(t) | axis(h) | axis(w)] of
+ *       widths (D/2, D/4, D/4) (D % 8 == 0), or 2*ceil(D/6) each when uniform_power, cut to D.
+ * d_table: device float [gt*gh*gw, D], written on `stream` (values computed in double, stored
+ * as float). Bad sizes or kind -> JEPA_E_INVALID_ARG. */
+jepa_status jepa_op_sincos_table(int32_t kind, int32_t gt, int32_t gh, int32_t gw, int32_t D, int32_t w_first,
+                                 int32_t uniform_power, float* d_table, void* stream);
+
+/* Resize a position table to another grid ("GGUF schema (v1)", Encoder: the runtime interpolates
+ * the training-grid table for other grids, as HF does), with pixel-centre alignment: output
+ * index o of an axis of n_in -> n_out samples reads the input at c = (o + 1/2) n_in/n_out - 1/2.
+ *  JEPA_RESIZE_TRILINEAR: src [st, sh, sw, D] -> dst [dt, dh, dw, D]; per axis c clamped at 0,
+ *       samples floor(c) and floor(c)+1 (clamped to n_in-1) blended linearly.
+ *  JEPA_RESIZE_BICUBIC: per frame (st == dt), [sh, sw, D] -> [dh, dw, D]; per axis the samples
+ *       floor(c)-1 .. floor(c)+2 (clamped to the axis) weighted by Keys' cubic kernel, a = -0.75.
+ * d_src, d_dst: device float, 16-byte aligned, D % 4 == 0, not overlapping; arithmetic in float.
+ * Bad sizes, mode or alignment -> JEPA_E_INVALID_ARG. */
+jepa_status jepa_op_pos_resize(const float* d_src, int32_t st, int32_t sh, int32_t sw, int32_t D, int32_t mode,
+                               float* d_dst, int32_t dt, int32_t dh, int32_t dw, void* stream);
 
 /* Softmax attention per (item, head): o = softmax(q k^T / sqrt(head_dim) + mask) v.
  * d_qkv: [B*N, 3*n_head*head_dim] ([q | k | v] columns, heads contiguous), d_out: [B*N, n_head*head_dim];

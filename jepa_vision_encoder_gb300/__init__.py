@@ -16,11 +16,13 @@ import torch
 from . import _lib
 from ._lib import (ATTN_BLOCK_CAUSAL, ATTN_FULL, BF16, EPI_BIAS, EPI_BIAS_GELU, EPI_BIAS_RESIDUAL,
                    EPI_PATCH_EMBED, EPI_QKV_ROPE, FP32, LAYOUT_CTHW, LAYOUT_TCHW, POS_LEARNED, POS_NONE,
-                   POS_ROPE3D, ROPE_INTERLEAVED, ROPE_TILED, Epilogue, HParams, JepaError, check, lib)
+                   POS_ROPE3D, POS_SINCOS2D, POS_SINCOS3D, RESIZE_BICUBIC, RESIZE_TRILINEAR, ROPE_INTERLEAVED,
+                   ROPE_TILED, Epilogue, HParams, JepaError, check, lib)
 
 __all__ = ["Model", "Context", "HParams", "JepaError", "preset", "hparams", "n_tokens", "ops", "lib"]
 
-PRESETS = ("hfvit_ti14", "vjepa2_vitl16", "vjepa2_1_vitl16", "levjepa_vitl16", "vjepa2_vitg16")
+PRESETS = ("hfvit_ti14", "vjepa2_vitl16", "vjepa2_1_vitl16", "levjepa_vitl16", "vjepa2_vitg16", "vjepa_vitl16",
+           "ijepa_vitl16")
 
 
 def _dtype_code(dtype) -> int:
@@ -275,6 +277,25 @@ class ops:
         table = torch.empty((gt * gh * gw, 3, d // 2, 2), dtype=torch.float32, device=device)
         check(lib().jepa_op_rope_table(ctypes.byref(hp), T, H, W, _ptr(table), _stream_ptr()))
         return table
+
+    @staticmethod
+    def sincos_table(kind: int, gt: int, gh: int, gw: int, D: int, w_first: bool = False,
+                     uniform_power: bool = False, device="cuda"):
+        """Fixed sin-cos position table [gt*gh*gw, D] (kind POS_SINCOS2D with gt == 1, or POS_SINCOS3D)."""
+        table = torch.empty((gt * gh * gw, D), dtype=torch.float32, device=device)
+        check(lib().jepa_op_sincos_table(kind, gt, gh, gw, D, int(w_first), int(uniform_power), _ptr(table),
+                                         _stream_ptr()))
+        return table
+
+    @staticmethod
+    def pos_resize(table: torch.Tensor, src_grid, dst_grid, mode: int = RESIZE_TRILINEAR):
+        """Resize a [st*sh*sw, D] float table to [dt*dh*dw, D] (trilinear, or bicubic per frame)."""
+        st, sh, sw = src_grid
+        dt, dh, dw = dst_grid
+        D = table.shape[-1]
+        out = torch.empty((dt * dh * dw, D), dtype=torch.float32, device=table.device)
+        check(lib().jepa_op_pos_resize(_ptr(table), st, sh, sw, D, mode, _ptr(out), dt, dh, dw, _stream_ptr()))
+        return out
 
     @staticmethod
     def attention(qkv: torch.Tensor, B: int, N: int, n_head: int, head_dim: int = 64, attn_mode: int = ATTN_FULL,

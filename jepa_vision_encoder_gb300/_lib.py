@@ -13,7 +13,8 @@ OK, E_INVALID_ARG, E_UNSUPPORTED, E_BUDGET, E_OOM, E_CUDA, E_TIMEOUT = range(7)
 STATUS_NAMES = {0: "JEPA_OK", 1: "JEPA_E_INVALID_ARG", 2: "JEPA_E_UNSUPPORTED", 3: "JEPA_E_BUDGET",
                 4: "JEPA_E_OOM", 5: "JEPA_E_CUDA", 6: "JEPA_E_TIMEOUT"}
 FP32, BF16 = 0, 1
-POS_NONE, POS_LEARNED, POS_ROPE3D = 0, 1, 2
+POS_NONE, POS_LEARNED, POS_ROPE3D, POS_SINCOS2D, POS_SINCOS3D = 0, 1, 2, 3, 4
+RESIZE_TRILINEAR, RESIZE_BICUBIC = 0, 1
 ROPE_TILED, ROPE_INTERLEAVED = 0, 1
 ATTN_FULL, ATTN_BLOCK_CAUSAL = 0, 1
 LAYOUT_TCHW, LAYOUT_CTHW = 0, 1
@@ -29,6 +30,7 @@ class HParams(ctypes.Structure):
         ("pos_type", ctypes.c_int32), ("rope_layout", ctypes.c_int32), ("rope_interpolate", ctypes.c_int32),
         ("rope_ref_grid", ctypes.c_int32), ("cls_token", ctypes.c_int32), ("modality_embed", ctypes.c_int32),
         ("attn_mode", ctypes.c_int32), ("n_pos_rows", ctypes.c_int32),
+        ("sincos_w_first", ctypes.c_int32), ("sincos_uniform_power", ctypes.c_int32),
     ]
 
     def as_dict(self):
@@ -76,6 +78,8 @@ SIGNATURES = {
     "jepa_op_layernorm": (_I, [_P, _I, _I, _P, _P, _F, _I, _P, _P]),
     "jepa_op_linear": (_I, [_I, _P, _I, _I, _P, _I, ctypes.POINTER(Epilogue), _P]),
     "jepa_op_rope_table": (_I, [_HP, _I, _I, _I, _P, _P]),
+    "jepa_op_sincos_table": (_I, [_I, _I, _I, _I, _I, _I, _I, _P, _P]),
+    "jepa_op_pos_resize": (_I, [_P, _I, _I, _I, _I, _I, _P, _I, _I, _I, _P]),
     "jepa_op_attention": (_I, [_I, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P]),
     "jepa_device_status": (_I, []),
     "jepa_debug_wait_timeout": (_I, [_I]),

@@ -322,10 +322,22 @@ template <int EK>
 __device__ __forceinline__ void epi_chunk_tc(const EpiArgs& a, const CUtensorMap* tm_out, EpiStage& st, int lane,
                                              int y0, int n0, float (&v)[32]) {
   if constexpr (EK == kEpiPatch) {
-    if (a.prefix == 0 && a.rows_per_item == a.patches_per_item && a.pos == nullptr) {
-      // output rows are the patch rows (no CLS, no learned table): bias (+ modality vector),
-      // then the same staged TMA store as the other epilogues, in fp32
+    if (a.prefix == 0 && a.rows_per_item == a.patches_per_item) {
+      // output rows are the patch rows (no CLS): bias (+ position row) (+ modality vector), then
+      // the same staged TMA store as the other epilogues, in fp32
       epi_math_tc<EK>(a, y0 + lane, n0, v);
+      if (a.pos != nullptr) {  // row i of the item's table (a fixed table: patch rows only)
+        const float4* p4 =
+            reinterpret_cast<const float4*>(a.pos + (size_t)((y0 + lane) % a.patches_per_item) * a.N + n0);
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const float4 q = __ldg(p4 + e / 4);
+          v[e] += q.x;
+          v[e + 1] += q.y;
+          v[e + 2] += q.z;
+          v[e + 3] += q.w;
+        }
+      }
       if (a.vec != nullptr) {
         const float4* v4 = reinterpret_cast<const float4*>(a.vec + n0);
 #pragma unroll

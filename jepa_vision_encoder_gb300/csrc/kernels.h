@@ -89,6 +89,13 @@ cudaError_t rope_axes_launch(int gt, int gh, int gw, int head_dim, float theta, 
 // X rows b*N + r for r < prefix: cls (+ pos[r]) (+ vec).
 cudaError_t prefix_rows_launch(float* X, int B, int N, int D, const float* cls, const float* pos,
                                const float* vec, cudaStream_t s);
+// Fixed sin-cos position table [gt*gh*gw, D] (kind 0: 2-D with gt == 1, kind 1: 3-D) and its
+// resizing (mode 0 trilinear, mode 1 bicubic per frame) to another grid.
+bool sincos_widths(int kind, int D, int uniform_power, int* d0, int* d1, int* d2);
+cudaError_t sincos_table_launch(int kind, int gt, int gh, int gw, int D, int w_first, int uniform_power, float* out,
+                                cudaStream_t s);
+cudaError_t pos_resize_launch(const float* src, int st, int sh, int sw, int D, int mode, float* dst, int dt, int dh,
+                              int dw, cudaStream_t s);
 // A kernel whose wait can never complete (failure-path check of the bounded waits).
 cudaError_t wait_timeout_probe_launch(int* err, uint64_t limit_ns, cudaStream_t s);
 

@@ -92,6 +92,14 @@ extern "C" jepa_status jepa_preset(const char* name, jepa_hparams* out) {
     h.embed_dim = 1408; h.n_layer = 40; h.n_head = 22; h.ffn_dim = 6144;
     h.patch_size = 16; h.tubelet_size = 2; h.img_size = 256; h.n_frames = 64;
     h.pos_type = JEPA_POS_ROPE3D; h.rope_layout = JEPA_ROPE_TILED;
+  } else if (n == "vjepa_vitl16") {
+    h.embed_dim = 1024; h.n_layer = 24; h.n_head = 16; h.ffn_dim = 4096;
+    h.patch_size = 16; h.tubelet_size = 2; h.img_size = 224; h.n_frames = 16;
+    h.pos_type = JEPA_POS_SINCOS3D; h.sincos_uniform_power = 1;
+  } else if (n == "ijepa_vitl16") {
+    h.embed_dim = 1024; h.n_layer = 24; h.n_head = 16; h.ffn_dim = 4096;
+    h.patch_size = 16; h.tubelet_size = 1; h.img_size = 224; h.n_frames = 1;
+    h.pos_type = JEPA_POS_SINCOS2D; h.sincos_w_first = 1;
   } else {
     return fail(JEPA_E_INVALID_ARG, "jepa_preset: unknown preset '%s'", name);
   }
@@ -113,7 +121,7 @@ extern "C" jepa_status jepa_hparams_validate(const jepa_hparams* hp) {
   if (hp->n_frames != 0 && !in(hp->n_frames, 1, 65536)) return fail(JEPA_E_INVALID_ARG, "n_frames %d outside [1, 65536]", hp->n_frames);
   if (!std::isfinite(hp->ln_eps) || hp->ln_eps < 0.0f || hp->ln_eps > 1.0f)
     return fail(JEPA_E_INVALID_ARG, "ln_eps %g not finite in [0, 1]", (double)hp->ln_eps);
-  if (!in(hp->pos_type, 0, 2)) return fail(JEPA_E_INVALID_ARG, "pos_type %d unknown", hp->pos_type);
+  if (!in(hp->pos_type, 0, 4)) return fail(JEPA_E_INVALID_ARG, "pos_type %d unknown", hp->pos_type);
   if (!in(hp->rope_layout, 0, 1)) return fail(JEPA_E_INVALID_ARG, "rope_layout %d unknown", hp->rope_layout);
   if (!in(hp->attn_mode, 0, 1)) return fail(JEPA_E_INVALID_ARG, "attn_mode %d unknown", hp->attn_mode);
   if (hp->embed_dim % hp->n_head) return fail(JEPA_E_INVALID_ARG, "embed_dim %d not divisible by n_head %d", hp->embed_dim, hp->n_head);
@@ -127,6 +135,22 @@ extern "C" jepa_status jepa_hparams_validate(const jepa_hparams* hp) {
   }
   if (hp->pos_type == JEPA_POS_LEARNED && !in(hp->n_pos_rows, 1, 1 << 22))
     return fail(JEPA_E_INVALID_ARG, "learned position table needs n_pos_rows in [1, 2^22] (got %d)", hp->n_pos_rows);
+  if (hp->pos_type == JEPA_POS_SINCOS2D || hp->pos_type == JEPA_POS_SINCOS3D) {
+    const bool three = hp->pos_type == JEPA_POS_SINCOS3D;
+    if (hp->img_size < hp->patch_size || hp->img_size % hp->patch_size)
+      return fail(JEPA_E_INVALID_ARG, "a sin-cos table needs img_size %d to be a multiple of patch %d", hp->img_size,
+                  hp->patch_size);
+    if (three && (hp->n_frames < hp->tubelet_size || hp->n_frames % hp->tubelet_size))
+      return fail(JEPA_E_INVALID_ARG, "a 3-D sin-cos table needs n_frames %d to be a multiple of tubelet %d",
+                  hp->n_frames, hp->tubelet_size);
+    int d0, d1, d2;
+    if (!sincos_widths(three ? 1 : 0, hp->embed_dim, hp->sincos_uniform_power, &d0, &d1, &d2))
+      return fail(JEPA_E_INVALID_ARG, "embed_dim %d cannot be split into the %s sin-cos axes", hp->embed_dim,
+                  three ? "3-D" : "2-D");
+    const long long rows = (long long)(three ? hp->n_frames / hp->tubelet_size : 1) *
+                           (hp->img_size / hp->patch_size) * (hp->img_size / hp->patch_size);
+    if (rows > (1ll << 22)) return fail(JEPA_E_INVALID_ARG, "sin-cos training grid of %lld rows above 2^22", rows);
+  }
   return JEPA_OK;
 }
 
@@ -150,6 +174,14 @@ jepa_status geometry(const jepa_hparams* hp, int T, int H, int W, Geo* g) {
   g->K = hp->in_chans * hp->tubelet_size * hp->patch_size * hp->patch_size;
   return JEPA_OK;
 }
+
+bool is_sincos(const jepa_hparams& hp) { return hp.pos_type == JEPA_POS_SINCOS2D || hp.pos_type == JEPA_POS_SINCOS3D; }
+
+// The grid a sin-cos table is baked for: (n_frames/t) x (img/P) x (img/P), one frame for 2-D.
+void sincos_train_grid(const jepa_hparams& hp, int* gt, int* gh, int* gw) {
+  *gt = hp.pos_type == JEPA_POS_SINCOS3D ? hp.n_frames / hp.tubelet_size : 1;
+  *gh = *gw = hp.img_size / hp.patch_size;
+}
 }  // namespace
 
 extern "C" jepa_status jepa_n_tokens(const jepa_hparams* hp, int32_t T, int32_t H, int32_t W, int32_t* n_out) {
@@ -170,6 +202,7 @@ struct TensorRec {
   size_t offset;  // in the arena
   size_t n;
   bool bf16;
+  bool fixed;     // computed by a kernel (sin-cos table), not drawn from the generator
 };
 struct LayerW {
   const float *ln1_w, *ln1_b, *b_qkv, *b_out, *ln2_w, *ln2_b, *b_up, *b_down;
@@ -234,6 +267,8 @@ extern "C" jepa_status jepa_model_load(const jepa_hparams* hp, uint64_t seed, in
   if (F % 4) return fail(JEPA_E_UNSUPPORTED, "ffn_dim %d must be a multiple of 4", F);
   if (dtype == JEPA_BF16 && (D % 64 || F % 64 || K % 64))
     return fail(JEPA_E_UNSUPPORTED, "bf16 GEMMs need embed %d, ffn %d and patch K %d to be multiples of 64", D, F, K);
+  if (is_sincos(*hp) && hp->cls_token)
+    return fail(JEPA_E_UNSUPPORTED, "a sin-cos table with a CLS token (the tables cover patch rows only)");
   int ndev = 0;
   if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev)
     return fail(JEPA_E_CUDA, "CUDA device %d not available (%d devices)", device, ndev);
@@ -247,17 +282,23 @@ extern "C" jepa_status jepa_model_load(const jepa_hparams* hp, uint64_t seed, in
   m->K = K;
   const bool bf = dtype == JEPA_BF16;
   // tensor table, in GGUF enc.* names and PyTorch row-major shapes
-  auto add = [&](const std::string& name, size_t n, bool matrix) {
+  auto add = [&](const std::string& name, size_t n, bool matrix, bool fixed = false) {
     TensorRec r;
     r.name = name;
     r.n = n;
     r.bf16 = bf && matrix;
+    r.fixed = fixed;
     r.offset = 0;
     m->tensors.push_back(r);
   };
   add("enc.patch_embed.weight", (size_t)D * K, true);
   add("enc.patch_embed.bias", D, false);
   if (hp->pos_type == JEPA_POS_LEARNED) add("enc.pos_embed", (size_t)hp->n_pos_rows * D, false);
+  int pgt = 0, pgh = 0, pgw = 0;  // training grid of a sin-cos table
+  if (is_sincos(*hp)) {
+    sincos_train_grid(*hp, &pgt, &pgh, &pgw);
+    add("enc.pos_embed", (size_t)pgt * pgh * pgw * D, false, true);
+  }
   if (hp->cls_token) add("enc.cls_token", D, false);
   if (hp->modality_embed) add("enc.mod_embed_video", D, false);
   for (int l = 0; l < L; ++l) {
@@ -292,6 +333,7 @@ extern "C" jepa_status jepa_model_load(const jepa_hparams* hp, uint64_t seed, in
   std::vector<float> host(largest);
   std::vector<uint16_t> hbits;
   for (const auto& t : m->tensors) {
+    if (t.fixed) continue;
     synth_parallel(seed, t.name, bf ? 1 : 0, t.n, host.data());
     if (t.bf16) {
       hbits.resize(t.n);
@@ -310,6 +352,17 @@ extern "C" jepa_status jepa_model_load(const jepa_hparams* hp, uint64_t seed, in
   m->w_patch = ptr("enc.patch_embed.weight");
   m->b_patch = fptr("enc.patch_embed.bias");
   if (hp->pos_type == JEPA_POS_LEARNED) m->pos = fptr("enc.pos_embed");
+  if (is_sincos(*hp)) {  // the converter's table of the training grid, baked here on the device
+    float* tab = reinterpret_cast<float*>(ptr("enc.pos_embed"));
+    e = sincos_table_launch(hp->pos_type == JEPA_POS_SINCOS3D ? 1 : 0, pgt, pgh, pgw, D, hp->sincos_w_first,
+                            hp->sincos_uniform_power, tab, nullptr);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+      jepa_model_free(m);
+      return fail(JEPA_E_CUDA, "sin-cos table: %s", cudaGetErrorString(e));
+    }
+    m->pos = tab;
+  }
   if (hp->cls_token) m->cls = fptr("enc.cls_token");
   if (hp->modality_embed) m->mod = fptr("enc.mod_embed_video");
   m->norm_w = fptr("enc.norm.weight");
@@ -391,6 +444,8 @@ struct jepa_context {
   float* X = nullptr;
   void *Xn = nullptr, *qkv = nullptr, *ao = nullptr, *Hh = nullptr, *Pm = nullptr;
   float2* rope = nullptr;
+  float* pos_buf = nullptr;         // a sin-cos table resized to the current clip grid
+  const float* pos_clip = nullptr;  // the table the patch rows add: the model's, or pos_buf
   float *pix_stage = nullptr, *tok_stage = nullptr;
   int* err = nullptr;
   // per-shape state
@@ -434,7 +489,8 @@ size_t ws_layout(const jepa_model* m, long long rows, long long prows, long long
   };
   const size_t oX = take(rows * D * 4), oXn = take(rows * D * es), oQ = take(rows * 3 * D * es),
                oA = take(rows * D * es), oH = take(rows * F * es), oP = take(prows * K * es),
-               oR = take((size_t)np * 3 * std::max(dh, 1) * sizeof(float2)), oPix = take(pix * 4),
+               oR = take((size_t)np * 3 * std::max(dh, 1) * sizeof(float2)),
+               oPos = take(is_sincos(hp) ? (size_t)np * D * 4 : 0), oPix = take(pix * 4),
                oTok = take(rows * D * 4), oErr = take(sizeof(int));
   if (c) {
     c->X = reinterpret_cast<float*>(c->ws + oX);
@@ -444,6 +500,7 @@ size_t ws_layout(const jepa_model* m, long long rows, long long prows, long long
     c->Hh = c->ws + oH;
     c->Pm = c->ws + oP;
     c->rope = reinterpret_cast<float2*>(c->ws + oR);
+    c->pos_buf = is_sincos(hp) ? reinterpret_cast<float*>(c->ws + oPos) : nullptr;
     c->pix_stage = reinterpret_cast<float*>(c->ws + oPix);
     c->tok_stage = reinterpret_cast<float*>(c->ws + oTok);
     c->err = reinterpret_cast<int*>(c->ws + oErr);
@@ -562,6 +619,8 @@ jepa_status check_shape(jepa_context* c, const float* pix, int B, int T, int H, 
   if (c->m->hp.pos_type == JEPA_POS_LEARNED && g->N != c->m->hp.n_pos_rows)
     return fail(JEPA_E_UNSUPPORTED, "learned position table has %d rows, the clip has %d tokens", c->m->hp.n_pos_rows,
                 g->N);
+  if (c->m->hp.pos_type == JEPA_POS_SINCOS2D && g->gt != 1)
+    return fail(JEPA_E_UNSUPPORTED, "a 2-D sin-cos table serves single-frame clips (the clip has %d)", g->gt);
   return JEPA_OK;
 }
 
@@ -592,6 +651,16 @@ jepa_status prepare_shape(jepa_context* c, int B, int T, int H, int W, const Geo
   if (hp.pos_type == JEPA_POS_ROPE3D) {
     CUDA_TRY(rope_axes_launch(g.gt, g.gh, g.gw, D / hp.n_head, hp.rope_theta, hp.rope_interpolate,
                               hp.rope_ref_grid, c->rope, c->stream));
+  }
+  c->pos_clip = m->pos;
+  if (is_sincos(hp)) {  // the training-grid table, resized when the clip's grid differs
+    int gt0, gh0, gw0;
+    sincos_train_grid(hp, &gt0, &gh0, &gw0);
+    if (g.gt != gt0 || g.gh != gh0 || g.gw != gw0) {
+      const int mode = hp.pos_type == JEPA_POS_SINCOS3D ? JEPA_RESIZE_TRILINEAR : JEPA_RESIZE_BICUBIC;
+      CUDA_TRY(pos_resize_launch(m->pos, gt0, gh0, gw0, D, mode, c->pos_buf, g.gt, g.gh, g.gw, c->stream));
+      c->pos_clip = c->pos_buf;
+    }
   }
   c->kB = B;
   c->kT = T;
@@ -702,7 +771,7 @@ jepa_status launch_encode(jepa_context* c, const float* pix, int B, int T, int H
   pe.patches_per_item = g.Np;
   pe.rows_per_item = g.N;
   pe.prefix = g.prefix;
-  pe.pos = m->pos;
+  pe.pos = c->pos_clip;
   pe.vec = m->mod;
   CUDA_TRY(prof(c, kPGemmPatch, 2.0 * dMp * dD * dK, 0.0, [&] {
     return bf ? gemm_tc_launch(c->tm_Pm, m->tm_patch[bn_slot(c->bn_patch)], c->tm_o_x, c->bn_patch, pe, Mp, D, m->K, c->err, lim, s)
@@ -1003,7 +1072,7 @@ extern "C" jepa_status jepa_op_linear(int32_t dtype, const void* d_x, int32_t M,
     return fail(JEPA_E_CUDA, "cuTensorMapEncodeTiled refused an operand");
   memset(&to, 0, sizeof to);
   // the patch embedding stores through TMA too when its rows are the patch rows themselves
-  const bool patch_tma = e.kind == kEpiPatch && e.prefix == 0 && e.rows_per_item == e.patches_per_item && !e.pos;
+  const bool patch_tma = e.kind == kEpiPatch && e.prefix == 0 && e.rows_per_item == e.patches_per_item;
   if (e.kind != kEpiPatch || patch_tma) {
     if (reinterpret_cast<uintptr_t>(e.out) & 15) return fail(JEPA_E_INVALID_ARG, "bf16 GEMM output must be 16-byte aligned");
     if (!make_tmap_2d_out(&to, e.out, M, N, (e.kind == kEpiResidual || e.kind == kEpiPatch) ? 4 : 2))
@@ -1023,6 +1092,40 @@ extern "C" jepa_status jepa_op_rope_table(const jepa_hparams* hp, int32_t T, int
   if (st != JEPA_OK) return st;
   CUDA_TRY(rope_table_launch(g.gt, g.gh, g.gw, hp->embed_dim / hp->n_head, hp->rope_theta, hp->rope_interpolate,
                              hp->rope_ref_grid, reinterpret_cast<float2*>(d_table), reinterpret_cast<cudaStream_t>(stream)));
+  return JEPA_OK;
+}
+
+extern "C" jepa_status jepa_op_sincos_table(int32_t kind, int32_t gt, int32_t gh, int32_t gw, int32_t D,
+                                            int32_t w_first, int32_t uniform_power, float* d_table, void* stream) {
+  if (!d_table) return fail(JEPA_E_INVALID_ARG, "jepa_op_sincos_table: null pointer");
+  if (kind != JEPA_POS_SINCOS2D && kind != JEPA_POS_SINCOS3D)
+    return fail(JEPA_E_INVALID_ARG, "jepa_op_sincos_table: kind %d is not a sin-cos table", kind);
+  const int k = kind == JEPA_POS_SINCOS3D ? 1 : 0;
+  if (gt <= 0 || gh <= 0 || gw <= 0 || (k == 0 && gt != 1) || (long long)gt * gh * gw > (1ll << 22))
+    return fail(JEPA_E_INVALID_ARG, "jepa_op_sincos_table: grid %dx%dx%d", gt, gh, gw);
+  int d0, d1, d2;
+  if (!sincos_widths(k, D, uniform_power, &d0, &d1, &d2))
+    return fail(JEPA_E_INVALID_ARG, "jepa_op_sincos_table: width %d cannot be split", D);
+  CUDA_TRY(sincos_table_launch(k, gt, gh, gw, D, w_first, uniform_power, d_table, reinterpret_cast<cudaStream_t>(stream)));
+  return JEPA_OK;
+}
+
+extern "C" jepa_status jepa_op_pos_resize(const float* d_src, int32_t st, int32_t sh, int32_t sw, int32_t D,
+                                          int32_t mode, float* d_dst, int32_t dt, int32_t dh, int32_t dw, void* stream) {
+  if (!d_src || !d_dst) return fail(JEPA_E_INVALID_ARG, "jepa_op_pos_resize: null pointer");
+  if (mode != JEPA_RESIZE_TRILINEAR && mode != JEPA_RESIZE_BICUBIC)
+    return fail(JEPA_E_INVALID_ARG, "jepa_op_pos_resize: mode %d unknown", mode);
+  if (st <= 0 || sh <= 0 || sw <= 0 || dt <= 0 || dh <= 0 || dw <= 0 || D <= 0 || D % 4)
+    return fail(JEPA_E_INVALID_ARG, "jepa_op_pos_resize: bad size (%dx%dx%d -> %dx%dx%d, D %d)", st, sh, sw, dt, dh,
+                dw, D);
+  if (mode == JEPA_RESIZE_BICUBIC && st != dt)
+    return fail(JEPA_E_INVALID_ARG, "jepa_op_pos_resize: bicubic resizes each frame (st %d != dt %d)", st, dt);
+  if ((reinterpret_cast<uintptr_t>(d_src) | reinterpret_cast<uintptr_t>(d_dst)) & 15)
+    return fail(JEPA_E_INVALID_ARG, "jepa_op_pos_resize: tables must be 16-byte aligned");
+  const size_t sb = (size_t)st * sh * sw * D * 4, db = (size_t)dt * dh * dw * D * 4;
+  const uintptr_t s0 = reinterpret_cast<uintptr_t>(d_src), d0 = reinterpret_cast<uintptr_t>(d_dst);
+  if (s0 < d0 + db && d0 < s0 + sb) return fail(JEPA_E_INVALID_ARG, "jepa_op_pos_resize: source and output overlap");
+  CUDA_TRY(pos_resize_launch(d_src, st, sh, sw, D, mode, d_dst, dt, dh, dw, reinterpret_cast<cudaStream_t>(stream)));
   return JEPA_OK;
 }
 
@@ -1124,6 +1227,8 @@ extern "C" jepa_status jepa_encode_noalloc(const jepa_model* m, const float* d_p
   if (st != JEPA_OK) return st;
   if (m->hp.pos_type == JEPA_POS_LEARNED && g.N != m->hp.n_pos_rows)
     return fail(JEPA_E_UNSUPPORTED, "learned position table has %d rows, the clip has %d tokens", m->hp.n_pos_rows, g.N);
+  if (m->hp.pos_type == JEPA_POS_SINCOS2D && g.gt != 1)
+    return fail(JEPA_E_UNSUPPORTED, "a 2-D sin-cos table serves single-frame clips (the clip has %d)", g.gt);
   if (m->device < 0 || m->device >= kNoAllocMaxDevices)
     return fail(JEPA_E_UNSUPPORTED, "jepa_encode_noalloc: device %d beyond %d", m->device, kNoAllocMaxDevices);
   const long long rows = (long long)B * g.N, prows = (long long)B * g.Np;

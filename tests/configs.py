@@ -36,6 +36,8 @@ WORKLOADS = {
     "vjepa2_1_vitl16_16x384": (VJEPA2_1_L16, "bf16", (1,), (16, 384, 384)),
     "levjepa_vitl16_16x256": (LEVJEPA_L16, "bf16", (2,), (16, 256, 256)),
     "vjepa2_vitg16_64x256": (VJEPA2_G16, "bf16", (1,), (64, 256, 256)),
+    "vjepa_vitl16_16x256": (VJEPA_L16, "bf16", (1,), (16, 256, 256)),
+    "ijepa_vitl16_256": (IJEPA_L16, "bf16", (8,), (1, 256, 256)),
 }
 
 

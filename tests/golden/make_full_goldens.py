@@ -1,4 +1,4 @@
-"""Write sampled oracle outputs of the five full-size workloads to tests/golden/full_<name>.npz.
+"""Write sampled oracle outputs of the full-size workloads to tests/golden/full_<name>.npz.
 
 Calls only the oracle (and the shared input generator). For each workload and each
 sampled item the whole fp64 encoder runs on the CPU; the file keeps a fixed set of token

@@ -44,6 +44,8 @@ PRESET_OF = {
     "vjepa2_1_vitl16_16x384": "vjepa2_1_vitl16",
     "levjepa_vitl16_16x256": "levjepa_vitl16",
     "vjepa2_vitg16_64x256": "vjepa2_vitg16",
+    "vjepa_vitl16_16x256": "vjepa_vitl16",
+    "ijepa_vitl16_256": "ijepa_vitl16",
 }
 
 
@@ -53,8 +55,10 @@ def test_presets_match_workloads(workload):
     hp = jv.preset(PRESET_OF[workload])
     for k in ("embed_dim", "n_layer", "n_head", "ffn_dim", "patch_size", "tubelet_size", "in_chans", "pos_type",
               "rope_layout", "rope_interpolate", "rope_ref_grid", "cls_token", "modality_embed", "attn_mode",
-              "n_pos_rows"):
+              "n_pos_rows", "sincos_w_first", "sincos_uniform_power"):
         assert getattr(hp, k) == getattr(cfg, k), k
+    if cfg.pos_type in (_lib.POS_SINCOS2D, _lib.POS_SINCOS3D):   # the grid the table is baked for
+        assert (hp.img_size, hp.n_frames) == (cfg.img_size, cfg.n_frames)
     assert abs(hp.ln_eps - cfg.ln_eps) < 1e-12 and hp.rope_theta == cfg.rope_theta
     assert jv.lib().jepa_hparams_validate(ctypes.byref(hp)) == 0
     import oracle
@@ -92,6 +96,11 @@ def test_refusals_by_name():
         ("hfvit_ti14", dict(n_pos_rows=0), "n_pos_rows"),
         ("vjepa2_vitl16", dict(attn_mode=7), "attn_mode"),
         ("vjepa2_vitl16", dict(rope_theta=-1.0), "rope_theta"),
+        ("vjepa2_vitl16", dict(pos_type=5), "pos_type"),
+        ("vjepa_vitl16", dict(img_size=200), "multiple of patch"),
+        ("vjepa_vitl16", dict(n_frames=15), "multiple of tubelet"),
+        ("vjepa_vitl16", dict(embed_dim=1028, n_head=4, sincos_uniform_power=0), "sin-cos axes"),
+        ("ijepa_vitl16", dict(embed_dim=1026, n_head=18), "sin-cos axes"),
     ]
     for name, kw, frag in cases:
         bad = jv.preset(name)

@@ -28,6 +28,8 @@ PRESET = {
     "vjepa2_1_vitl16_16x384": "vjepa2_1_vitl16",
     "levjepa_vitl16_16x256": "levjepa_vitl16",
     "vjepa2_vitg16_64x256": "vjepa2_vitg16",
+    "vjepa_vitl16_16x256": "vjepa_vitl16",
+    "ijepa_vitl16_256": "ijepa_vitl16",
 }
 
 
@@ -45,9 +47,11 @@ def check_bar(got, ref, dtype, what=""):
     return err.max(), cos.min()
 
 
-def make(name, n_layer=None, batch=1, T=None, H=None, W=None, graph=False):
-    cfg, dtype, _, (T0, H0, W0) = WORKLOADS[name]
+def make(name, n_layer=None, batch=1, T=None, H=None, W=None, graph=False, cfg=None):
+    cfg0, dtype, _, (T0, H0, W0) = WORKLOADS[name]
     kw = {} if n_layer is None else {"n_layer": n_layer}
+    if cfg is not None and cfg.pos_type in (jv.POS_SINCOS2D, jv.POS_SINCOS3D):   # the grid the table is baked for
+        kw.update(img_size=cfg.img_size, n_frames=cfg.n_frames)
     model = jv.Model.preset(PRESET[name], seed=0, dtype=dtype, **kw)
     ctx = jv.Context(model, batch, T or T0, H or H0, W or W0, graph=graph)
     return model, ctx
@@ -57,7 +61,7 @@ def make(name, n_layer=None, batch=1, T=None, H=None, W=None, graph=False):
 def test_small_encoder_matches_oracle(name):
     cfg, dtype, (T, H, W) = small(name)
     B = 2
-    model, ctx = make(name, n_layer=cfg.n_layer, batch=B, T=T, H=H, W=W)
+    model, ctx = make(name, n_layer=cfg.n_layer, batch=B, T=T, H=H, W=W, cfg=cfg)
     pix = synth.pixels(0, (B, T, 3, H, W))
     out = ctx.encode(torch.from_numpy(pix).cuda())
     ctx.sync()

@@ -199,7 +199,7 @@ def test_qkv_rope_epilogue(case, dtype):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
-@pytest.mark.parametrize("prefix,use_pos,use_vec", [(0, False, True), (1, True, False)])
+@pytest.mark.parametrize("prefix,use_pos,use_vec", [(0, False, True), (1, True, False), (0, True, True)])
 def test_patch_embed_epilogue(dtype, prefix, use_pos, use_vec):
     B, Np, K, D = 3, 130, 192, 256
     N = Np + prefix
