@@ -66,6 +66,38 @@ class Config:
         return self.embed_dim // self.n_head
 
 
+class OraclePredHParams(ctypes.Structure):
+    _fields_ = [
+        ("embed_dim", ctypes.c_int), ("n_layer", ctypes.c_int), ("n_head", ctypes.c_int),
+        ("ffn_dim", ctypes.c_int), ("enc_dim", ctypes.c_int), ("out_dim", ctypes.c_int),
+        ("n_mask_tokens", ctypes.c_int), ("mask_index", ctypes.c_int), ("ln_eps", ctypes.c_double),
+        ("rope_theta", ctypes.c_double), ("rope_layout", ctypes.c_int),
+    ]
+
+
+@dataclass
+class PredConfig:
+    """Masked-predictor hyper-parameters in the jepa.pred.* vocabulary."""
+    embed_dim: int
+    n_layer: int
+    n_head: int
+    ffn_dim: int
+    enc_dim: int
+    out_dim: int
+    n_mask_tokens: int = 10
+    mask_index: int = 1
+    ln_eps: float = 1e-6
+    rope_theta: float = 10000.0
+    rope_layout: int = 0
+
+    def struct(self) -> OraclePredHParams:
+        return OraclePredHParams(**asdict(self))
+
+    @property
+    def head_dim(self) -> int:
+        return self.embed_dim // self.n_head
+
+
 def build(force: bool = False) -> str:
     """Compile liboracle.so in place (g++, OpenMP, contraction off for the generator)."""
     src = os.path.join(_HERE, "oracle.cpp")
@@ -107,6 +139,10 @@ def lib():
         L.oracle_interp_trilinear.argtypes = [P, I, I, I, I, I, I, I, P]
         L.oracle_interp_bicubic.argtypes = [P, I, I, I, I, I, P]
         L.oracle_pos_table.argtypes = [hp, I, I, I, P]
+        L.oracle_rope_tables_pos.argtypes = [I, ctypes.c_double, I, P, I, P, P]
+        L.oracle_rope_tables_pos.restype = None
+        L.oracle_predict.argtypes = [ctypes.POINTER(OraclePredHParams), ctypes.c_uint64, I, P, I, I, P, I, P, I,
+                                     I, I, P]
         L.oracle_mask_allow.argtypes = [I, I, I, I, I, I]
         L.oracle_attention.argtypes = [P, P, P, I, I, I, I, I, I, P]
         L.oracle_attention.restype = None
@@ -267,6 +303,32 @@ def pos_table(cfg: Config, T, H, W) -> np.ndarray:
     rc = lib().oracle_pos_table(ctypes.byref(s), T, H, W, out.ctypes.data)
     if rc != 0:
         raise ValueError(f"oracle_pos_table refused the configuration (code {rc})")
+    return out
+
+
+def rope_tables_pos(hd, theta, layout, pos):
+    """cos / signed-sin tables [n, hd] at explicit positions pos [n, 3]."""
+    pos = _f64(pos)
+    n = pos.shape[0]
+    c = np.empty((n, hd), dtype=np.float64)
+    s_ = np.empty((n, hd), dtype=np.float64)
+    lib().oracle_rope_tables_pos(hd, float(theta), layout, pos.ctypes.data, n, c.ctypes.data, s_.ctypes.data)
+    return c, s_
+
+
+def predict(pcfg: PredConfig, seed: int, bf16_weights: bool, enc, ctx_ids, tgt_ids, grid) -> np.ndarray:
+    """Masked predictor: enc [B, n_enc, enc_dim], ctx_ids [B, n_ctx], tgt_ids [B, n_tgt], grid (gh, gw)
+    -> [B, n_tgt, out_dim] fp64."""
+    enc = _f64(enc)
+    B, n_enc, _ = enc.shape
+    ctx = np.ascontiguousarray(ctx_ids, dtype=np.int32).reshape(B, -1)
+    tgt = np.ascontiguousarray(tgt_ids, dtype=np.int32).reshape(B, -1)
+    out = np.empty((B, tgt.shape[1], pcfg.out_dim), dtype=np.float64)
+    s = pcfg.struct()
+    rc = lib().oracle_predict(ctypes.byref(s), seed, int(bf16_weights), enc.ctypes.data, B, n_enc, ctx.ctypes.data,
+                              ctx.shape[1], tgt.ctypes.data, tgt.shape[1], grid[0], grid[1], out.ctypes.data)
+    if rc != 0:
+        raise ValueError(f"oracle_predict refused the configuration (code {rc})")
     return out
 
 

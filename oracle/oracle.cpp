@@ -10,6 +10,7 @@
 // the vectorised dot products change nothing but the rounding order of the sums.
 #include "oracle.h"
 
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -206,28 +207,37 @@ int oracle_rope_positions(const oracle_hparams* hp, int T, int H, int W, double*
 // tiled table[j] = f(pos * omega_{j mod d/2}) (V-JEPA 2), interleaved table[2k] = table[2k+1]
 // = f(pos * omega_k) (V-JEPA 2.1); x cos + rot90(x) sin with rot90(y1, y2) = (-y2, y1), the
 // sign carried in the sin table; prefix (CLS) rows are identity ([S] levjepa note).
-int oracle_rope_tables(const oracle_hparams* hp, int T, int H, int W, double* cos_t, double* sin_t) {
-  Geometry g;
-  if (!geometry(hp, T, H, W, &g)) return -1;
-  const int hd = hp->embed_dim / hp->n_head;
+void oracle_rope_tables_pos(int hd, double theta, int layout, const double* pos, int n, double* cos_t,
+                            double* sin_t) {
   const int d = 2 * ((hd / 3) / 2);
-  std::vector<double> pos((size_t)g.Np * 3);
-  oracle_rope_positions(hp, T, H, W, pos.data());
-  for (int n = 0; n < g.N; ++n) {
-    double* cr = cos_t + (size_t)n * hd;
-    double* sr = sin_t + (size_t)n * hd;
+  for (int i = 0; i < n; ++i) {
+    double* cr = cos_t + (size_t)i * hd;
+    double* sr = sin_t + (size_t)i * hd;
     for (int j = 0; j < hd; ++j) { cr[j] = 1.0; sr[j] = 0.0; }
-    if (n < g.prefix) continue;
-    const int i = n - g.prefix;
     for (int a = 0; a < 3; ++a)
       for (int jj = 0; jj < d; ++jj) {
-        const int kidx = (hp->rope_layout == 0) ? (jj % (d / 2)) : (jj / 2);
-        const double omega = 1.0 / std::pow(hp->rope_theta, 2.0 * kidx / d);
+        const int kidx = (layout == 0) ? (jj % (d / 2)) : (jj / 2);
+        const double omega = 1.0 / std::pow(theta, 2.0 * kidx / d);
         const double th = pos[3 * i + a] * omega;
         cr[a * d + jj] = std::cos(th);
         sr[a * d + jj] = ((jj % 2 == 0) ? -1.0 : 1.0) * std::sin(th);
       }
   }
+}
+
+int oracle_rope_tables(const oracle_hparams* hp, int T, int H, int W, double* cos_t, double* sin_t) {
+  Geometry g;
+  if (!geometry(hp, T, H, W, &g)) return -1;
+  const int hd = hp->embed_dim / hp->n_head;
+  std::vector<double> pos((size_t)g.Np * 3);
+  oracle_rope_positions(hp, T, H, W, pos.data());
+  for (int n = 0; n < g.prefix; ++n)  // prefix (CLS) rows: identity
+    for (int j = 0; j < hd; ++j) {
+      cos_t[(size_t)n * hd + j] = 1.0;
+      sin_t[(size_t)n * hd + j] = 0.0;
+    }
+  oracle_rope_tables_pos(hd, hp->rope_theta, hp->rope_layout, pos.data(), g.Np, cos_t + (size_t)g.prefix * hd,
+                         sin_t + (size_t)g.prefix * hd);
   return 0;
 }
 
@@ -452,6 +462,72 @@ void oracle_attention(const double* q, const double* k, const double* v, int N, 
   }
 }
 
+}  // extern "C"
+
+namespace {
+// The weights of one pre-LN block under `prefix` ("enc.blk.{l}." or "pred.blk.{l}.": [S] the
+// predictor blocks have the encoder's layout).
+struct BlockW {
+  std::vector<double> ln1w, ln1b, wqkv, bqkv, wout, bout, ln2w, ln2b, wup, bup, wdn, bdn;
+  void gen(uint64_t seed, const std::string& p, int bf16_weights, int D, int F) {
+    gen_param(seed, p + "ln1.weight", bf16_weights, D, ln1w);
+    gen_param(seed, p + "ln1.bias", bf16_weights, D, ln1b);
+    gen_param(seed, p + "attn_qkv.weight", bf16_weights, (size_t)3 * D * D, wqkv);
+    gen_param(seed, p + "attn_qkv.bias", bf16_weights, (size_t)3 * D, bqkv);
+    gen_param(seed, p + "attn_out.weight", bf16_weights, (size_t)D * D, wout);
+    gen_param(seed, p + "attn_out.bias", bf16_weights, D, bout);
+    gen_param(seed, p + "ln2.weight", bf16_weights, D, ln2w);
+    gen_param(seed, p + "ln2.bias", bf16_weights, D, ln2b);
+    gen_param(seed, p + "ffn_up.weight", bf16_weights, (size_t)F * D, wup);
+    gen_param(seed, p + "ffn_up.bias", bf16_weights, F, bup);
+    gen_param(seed, p + "ffn_down.weight", bf16_weights, (size_t)D * F, wdn);
+    gen_param(seed, p + "ffn_down.bias", bf16_weights, D, bdn);
+  }
+};
+
+struct BlockScratch {
+  std::vector<double> h, qkv, q, k, v, o, tmp, u;
+  BlockScratch(int N, int D, int F)
+      : h((size_t)N * D), qkv((size_t)N * 3 * D), q((size_t)N * D), k((size_t)N * D), v((size_t)N * D),
+        o((size_t)N * D), tmp((size_t)N * D), u((size_t)N * F) {}
+};
+
+// One block on the N rows x [N, D] of one item, in place ([A] "The shared ViT graph"):
+// x += out(attn(rope(qkv(ln1(x))))); x += down(GELU(up(ln2(x)))). rc / rs: RoPE tables [N, hd]
+// applied to q and k (not v) after the projection and before scaling, or null for none.
+void block_forward(const BlockW& w, double* x, int N, int D, int NH, int F, double eps, const double* rc,
+                   const double* rs, int attn_mode, int prefix, int frame_tokens, BlockScratch& s) {
+  const int hd = D / NH;
+  const size_t MD = (size_t)N * D;
+  // x += attn(ln1(x)): fused qkv rows [q; k; v] ([S] attn_qkv), heads contiguous in each.
+  oracle_layernorm(x, N, D, w.ln1w.data(), w.ln1b.data(), eps, s.h.data());
+  oracle_linear(s.h.data(), N, D, w.wqkv.data(), w.bqkv.data(), 3 * D, s.qkv.data());
+  for (int n = 0; n < N; ++n)
+    for (int c = 0; c < D; ++c) {
+      s.q[(size_t)n * D + c] = s.qkv[(size_t)n * 3 * D + c];
+      s.k[(size_t)n * D + c] = s.qkv[(size_t)n * 3 * D + D + c];
+      s.v[(size_t)n * D + c] = s.qkv[(size_t)n * 3 * D + 2 * D + c];
+    }
+  if (rc) {
+    oracle_rope_apply(s.q.data(), N, NH, hd, rc, rs, s.tmp.data());
+    s.q.swap(s.tmp);
+    oracle_rope_apply(s.k.data(), N, NH, hd, rc, rs, s.tmp.data());
+    s.k.swap(s.tmp);
+  }
+  oracle_attention(s.q.data(), s.k.data(), s.v.data(), N, NH, hd, attn_mode, prefix, frame_tokens, s.o.data());
+  oracle_linear(s.o.data(), N, D, w.wout.data(), w.bout.data(), D, s.tmp.data());
+  for (size_t i = 0; i < MD; ++i) x[i] += s.tmp[i];
+  // x += ffn(ln2(x)) with GELU(erf)
+  oracle_layernorm(x, N, D, w.ln2w.data(), w.ln2b.data(), eps, s.h.data());
+  oracle_linear(s.h.data(), N, D, w.wup.data(), w.bup.data(), F, s.u.data());
+  oracle_gelu(s.u.data(), (size_t)N * F, s.u.data());
+  oracle_linear(s.u.data(), N, F, w.wdn.data(), w.bdn.data(), D, s.tmp.data());
+  for (size_t i = 0; i < MD; ++i) x[i] += s.tmp[i];
+}
+}  // namespace
+
+extern "C" {
+
 // [A] "The shared ViT graph":
 //   tokens = patch_embed(rearranged pixels) [+ pos_embed] [+ cls] [+ modality vec]
 //   for each block: x += attn(ln1(x)); x += ffn(ln2(x))   (pre-LN, GELU(erf), qkv bias)
@@ -512,50 +588,13 @@ int oracle_encode(const oracle_hparams* hp, uint64_t seed, int bf16_weights, con
   }
   const int frame_tokens = g.gh * g.gw;
 
-  std::vector<double> h(MD), qkv((size_t)N * 3 * D), q(MD), k(MD), v(MD), o(MD), tmp(MD), u((size_t)N * F);
+  BlockScratch sc(N, D, F);
   for (int l = 0; l < hp->n_layer; ++l) {
-    const std::string p = "enc.blk." + std::to_string(l) + ".";
-    std::vector<double> ln1w, ln1b, wqkv, bqkv, wout, bout, ln2w, ln2b, wup, bup, wdn, bdn;
-    gen_param(seed, p + "ln1.weight", bf16_weights, D, ln1w);
-    gen_param(seed, p + "ln1.bias", bf16_weights, D, ln1b);
-    gen_param(seed, p + "attn_qkv.weight", bf16_weights, (size_t)3 * D * D, wqkv);
-    gen_param(seed, p + "attn_qkv.bias", bf16_weights, (size_t)3 * D, bqkv);
-    gen_param(seed, p + "attn_out.weight", bf16_weights, (size_t)D * D, wout);
-    gen_param(seed, p + "attn_out.bias", bf16_weights, D, bout);
-    gen_param(seed, p + "ln2.weight", bf16_weights, D, ln2w);
-    gen_param(seed, p + "ln2.bias", bf16_weights, D, ln2b);
-    gen_param(seed, p + "ffn_up.weight", bf16_weights, (size_t)F * D, wup);
-    gen_param(seed, p + "ffn_up.bias", bf16_weights, F, bup);
-    gen_param(seed, p + "ffn_down.weight", bf16_weights, (size_t)D * F, wdn);
-    gen_param(seed, p + "ffn_down.bias", bf16_weights, D, bdn);
-
-    for (int b = 0; b < B; ++b) {
-      double* x = X.data() + (size_t)b * MD;
-      // x += attn(ln1(x)): fused qkv rows [q; k; v] ([S] attn_qkv), heads contiguous in each.
-      oracle_layernorm(x, N, D, ln1w.data(), ln1b.data(), hp->ln_eps, h.data());
-      oracle_linear(h.data(), N, D, wqkv.data(), bqkv.data(), 3 * D, qkv.data());
-      for (int n = 0; n < N; ++n)
-        for (int c = 0; c < D; ++c) {
-          q[(size_t)n * D + c] = qkv[(size_t)n * 3 * D + c];
-          k[(size_t)n * D + c] = qkv[(size_t)n * 3 * D + D + c];
-          v[(size_t)n * D + c] = qkv[(size_t)n * 3 * D + 2 * D + c];
-        }
-      if (hp->pos_type == 2) {  // on q and k, not v, after the projection and before scaling
-        oracle_rope_apply(q.data(), N, NH, hd, rc.data(), rs.data(), tmp.data());
-        q.swap(tmp);
-        oracle_rope_apply(k.data(), N, NH, hd, rc.data(), rs.data(), tmp.data());
-        k.swap(tmp);
-      }
-      oracle_attention(q.data(), k.data(), v.data(), N, NH, hd, hp->attn_mode, prefix, frame_tokens, o.data());
-      oracle_linear(o.data(), N, D, wout.data(), bout.data(), D, tmp.data());
-      for (size_t i = 0; i < MD; ++i) x[i] += tmp[i];
-      // x += ffn(ln2(x)) with GELU(erf)
-      oracle_layernorm(x, N, D, ln2w.data(), ln2b.data(), hp->ln_eps, h.data());
-      oracle_linear(h.data(), N, D, wup.data(), bup.data(), F, u.data());
-      oracle_gelu(u.data(), u.size(), u.data());
-      oracle_linear(u.data(), N, F, wdn.data(), bdn.data(), D, tmp.data());
-      for (size_t i = 0; i < MD; ++i) x[i] += tmp[i];
-    }
+    BlockW w;
+    w.gen(seed, "enc.blk." + std::to_string(l) + ".", bf16_weights, D, F);
+    for (int b = 0; b < B; ++b)
+      block_forward(w, X.data() + (size_t)b * MD, N, D, NH, F, hp->ln_eps, hp->pos_type == 2 ? rc.data() : nullptr,
+                    rs.data(), hp->attn_mode, prefix, frame_tokens, sc);
   }
 
   if (final_norm) {
@@ -566,6 +605,78 @@ int oracle_encode(const oracle_hparams* hp, uint64_t seed, int bf16_weights, con
       oracle_layernorm(X.data() + (size_t)b * MD, N, D, nw.data(), nb.data(), hp->ln_eps, out + (size_t)b * MD);
   } else {
     std::memcpy(out, X.data(), X.size() * sizeof(double));
+  }
+  return 0;
+}
+
+// [S] "Predictor": pred.embed [pred_dim, enc_dim], pred.mask_tokens [n, pred_dim], pred.blk.{i}
+// (the encoder block layout), pred.norm, pred.proj [out_dim, pred_dim]. [K] masked-latent
+// predictor: context features -> embed -> append mask tokens -> order by position -> stack (own
+// RoPE table) -> LN -> restore order, take the targets -> proj.
+int oracle_predict(const oracle_pred_hparams* hp, uint64_t seed, int bf16_weights, const double* enc, int B,
+                   int n_enc, const int* ctx_ids, int n_ctx, const int* tgt_ids, int n_tgt, int gh, int gw,
+                   double* out) {
+  if (!hp || B <= 0 || n_ctx < 0 || n_tgt <= 0 || n_enc <= 0 || gh <= 0 || gw <= 0) return -1;
+  const int P = hp->embed_dim, E = hp->enc_dim, O = hp->out_dim, NH = hp->n_head, F = hp->ffn_dim;
+  if (NH <= 0 || P % NH || hp->n_mask_tokens <= 0 || hp->mask_index < 0) return -1;
+  const int hd = P / NH, N = n_ctx + n_tgt;
+  for (int i = 0; i < B * n_ctx; ++i)
+    if (ctx_ids[i] < 0 || ctx_ids[i] >= n_enc) return -1;
+  for (int i = 0; i < B * n_tgt; ++i)
+    if (tgt_ids[i] < 0) return -1;
+
+  std::vector<double> we, be, mt, nw, nb, wp, bp;
+  gen_param(seed, "pred.embed.weight", bf16_weights, (size_t)P * E, we);
+  gen_param(seed, "pred.embed.bias", bf16_weights, P, be);
+  gen_param(seed, "pred.mask_tokens", bf16_weights, (size_t)hp->n_mask_tokens * P, mt);
+  const double* mask_tok = mt.data() + (size_t)(hp->mask_index % hp->n_mask_tokens) * P;
+
+  // per item: the token rows in position order, the order itself, and the RoPE tables
+  std::vector<double> X((size_t)B * N * P), rc((size_t)B * N * hd), rs((size_t)B * N * hd);
+  std::vector<int> order((size_t)B * N);
+  for (int b = 0; b < B; ++b) {
+    std::vector<double> ctx((size_t)n_ctx * E), emb((size_t)n_ctx * P);
+    for (int s = 0; s < n_ctx; ++s)
+      std::memcpy(&ctx[(size_t)s * E], enc + ((size_t)b * n_enc + ctx_ids[b * n_ctx + s]) * E, E * sizeof(double));
+    if (n_ctx) oracle_linear(ctx.data(), n_ctx, E, we.data(), be.data(), P, emb.data());
+    std::vector<int> ids(N);
+    for (int s = 0; s < N; ++s) ids[s] = s < n_ctx ? ctx_ids[b * n_ctx + s] : tgt_ids[b * n_tgt + (s - n_ctx)];
+    int* ord = order.data() + (size_t)b * N;
+    for (int s = 0; s < N; ++s) ord[s] = s;
+    std::stable_sort(ord, ord + N, [&](int a, int c) { return ids[a] < ids[c]; });
+    std::vector<double> pos((size_t)N * 3);
+    for (int r = 0; r < N; ++r) {
+      const int s = ord[r], id = ids[s];
+      const double* src = s < n_ctx ? &emb[(size_t)s * P] : mask_tok;
+      std::memcpy(&X[((size_t)b * N + r) * P], src, P * sizeof(double));
+      pos[3 * r + 0] = (double)(id / (gh * gw));
+      pos[3 * r + 1] = (double)((id % (gh * gw)) / gw);
+      pos[3 * r + 2] = (double)(id % gw);
+    }
+    oracle_rope_tables_pos(hd, hp->rope_theta, hp->rope_layout, pos.data(), N, rc.data() + (size_t)b * N * hd,
+                           rs.data() + (size_t)b * N * hd);
+  }
+
+  BlockScratch sc(N, P, F);
+  for (int l = 0; l < hp->n_layer; ++l) {
+    BlockW w;
+    w.gen(seed, "pred.blk." + std::to_string(l) + ".", bf16_weights, P, F);
+    for (int b = 0; b < B; ++b)
+      block_forward(w, X.data() + (size_t)b * N * P, N, P, NH, F, hp->ln_eps, rc.data() + (size_t)b * N * hd,
+                    rs.data() + (size_t)b * N * hd, 0, 0, 1, sc);
+  }
+
+  gen_param(seed, "pred.norm.weight", bf16_weights, P, nw);
+  gen_param(seed, "pred.norm.bias", bf16_weights, P, nb);
+  gen_param(seed, "pred.proj.weight", bf16_weights, (size_t)O * P, wp);
+  gen_param(seed, "pred.proj.bias", bf16_weights, O, bp);
+  for (int b = 0; b < B; ++b) {
+    std::vector<double> y((size_t)N * P), back((size_t)N * P), tgt((size_t)n_tgt * P);
+    oracle_layernorm(X.data() + (size_t)b * N * P, N, P, nw.data(), nb.data(), hp->ln_eps, y.data());
+    const int* ord = order.data() + (size_t)b * N;
+    for (int r = 0; r < N; ++r) std::memcpy(&back[(size_t)ord[r] * P], &y[(size_t)r * P], P * sizeof(double));
+    std::memcpy(tgt.data(), &back[(size_t)n_ctx * P], (size_t)n_tgt * P * sizeof(double));
+    oracle_linear(tgt.data(), n_tgt, P, wp.data(), bp.data(), O, out + (size_t)b * n_tgt * O);
   }
   return 0;
 }

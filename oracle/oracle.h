@@ -111,6 +111,11 @@ int oracle_interp_bicubic(const double* src, int sh, int sw, int D, int dh, int 
  * Returns -1 on a bad size, -2 when the table cannot serve the clip (sincos2d on several frames). */
 int oracle_pos_table(const oracle_hparams* hp, int T, int H, int W, double* out);
 
+/* cos / signed-sin tables [n, hd] of n tokens at explicit (t, h, w) positions pos [n, 3], the
+ * same rule as oracle_rope_tables (no prefix rows). */
+void oracle_rope_tables_pos(int hd, double theta, int layout, const double* pos, int n, double* cos_t,
+                            double* sin_t);
+
 /* Is key k visible to query q? attn_mode 0: every k < N. attn_mode 1 (block-causal,
  * [S] levjepa note; [A] "Block-causal attention"): prefix rows see everything, prefix
  * columns are closed to patch queries, patch keys visible iff frame(q) >= frame(k). */
@@ -126,6 +131,28 @@ void oracle_attention(const double* q, const double* k, const double* v, int N, 
  * out: [B, N, D]; final_norm = 0 returns the residual stream before enc.norm. */
 int oracle_encode(const oracle_hparams* hp, uint64_t seed, int bf16_weights, const float* pix, int B, int T,
                   int H, int W, int layout, int final_norm, double* out);
+
+/* Masked-latent predictor hyper-parameters (jepa.pred.* of [S] "Predictor"). */
+typedef struct {
+  int embed_dim, n_layer, n_head, ffn_dim; /* predictor width, depth, heads, ffn (V-JEPA 2: 384/12/12/1536) */
+  int enc_dim, out_dim;                    /* pred.embed input width, pred.proj output width */
+  int n_mask_tokens, mask_index;           /* rows of pred.mask_tokens; the row targets take (mod n) */
+  double ln_eps, rope_theta;
+  int rope_layout;                         /* 0 tiled (V-JEPA 2), 1 interleaved */
+} oracle_pred_hparams;
+
+/* The masked predictor ([S] "Predictor" tensor table; [K] V-JEPA 2 section, masked-latent
+ * predictor): per item, the encoder tokens at the context ids are projected by pred.embed, a
+ * mask token (row mask_index mod n_mask_tokens of pred.mask_tokens) stands at each target id,
+ * the tokens are put in order of position id (stable), run through the pred.blk stack (the
+ * encoder's block with 3-D RoPE at the ids' positions, full attention), normalised by
+ * pred.norm, put back in their input order, and the target rows projected by pred.proj.
+ * Position id -> (t, h, w) = (id / (gh gw), (id mod gh gw) / gw, id mod gw).
+ * enc [B, n_enc, enc_dim]; ctx_ids [B, n_ctx] in [0, n_enc); tgt_ids [B, n_tgt] >= 0;
+ * out [B, n_tgt, out_dim]. Returns -1 on a bad size or id. */
+int oracle_predict(const oracle_pred_hparams* hp, uint64_t seed, int bf16_weights, const double* enc, int B,
+                   int n_enc, const int* ctx_ids, int n_ctx, const int* tgt_ids, int n_tgt, int gh, int gw,
+                   double* out);
 
 /* Number of OpenMP threads the oracle uses. */
 int oracle_num_threads(void);

@@ -165,7 +165,9 @@ static inline void jsynth_fill(uint64_t seed, const char* name, int kind, double
  * LayerNorm beta            0.01 * N(0,1)
  * cls / pos / modality      N(0, 0.02)
  * pixels                    U(-2, 2), stream "input.pixels" of seed + 1
- * jsynth_param_init() maps a GGUF enc.* tensor name to its (kind, a, b, is_matrix). */
+ * jsynth_param_init() maps a GGUF tensor name (enc.*, pred.*, head.*) to its (kind, a, b, is_matrix):
+ * LayerNorm gains (ln1 / ln2 / *norm / ln_kv weights) 1 + 0.1 N(0,1), biases 0.01 N(0,1), other
+ * weights (matrices) N(0, 0.02), everything else (tokens, tables, vectors) N(0, 0.02). */
 static inline int jsynth_ends_with(const char* s, const char* suffix) {
   size_t ls = strlen(s), lf = strlen(suffix);
   return ls >= lf && memcmp(s + ls - lf, suffix, lf) == 0;
@@ -175,7 +177,7 @@ static inline void jsynth_param_init(const char* name, int* kind, double* a, dou
   *kind = JSYNTH_NORMAL;
   *is_matrix = 0;
   if (jsynth_ends_with(name, "ln1.weight") || jsynth_ends_with(name, "ln2.weight") ||
-      strcmp(name, "enc.norm.weight") == 0) {
+      jsynth_ends_with(name, "norm.weight") || jsynth_ends_with(name, "ln_kv.weight")) {
     *a = 1.0; *b = 0.1;
   } else if (jsynth_ends_with(name, ".bias")) {
     *a = 0.0; *b = 0.01;
