@@ -7,7 +7,10 @@ weights and pixels. A step is one jepa_encode of the batch (patchify, patch GEMM
 final norm) on inputs resident in HBM. The line also carries the same clip at batch 1 ("batch1"),
 timed the same way.
 
---workload picks one of the fixed-table families instead: V-JEPA ViT-L/16 16 x 256 x 256 clips
+--workload vjepa2_vitl16_predictor times the V-JEPA 2 masked predictor instead (12 layers of
+width 384 over the 2048 tokens of each clip: the first 1024 as context, the last 1024 as
+targets, the split of the pages' predictor example), eight clips per step, on encoder tokens
+resident in HBM. --workload also picks one of the fixed-table families: V-JEPA ViT-L/16 16 x 256 x 256 clips
 whose 3-D sin-cos table is baked for 16 x 224 x 224 and resized (trilinear), or I-JEPA-style
 ViT-L/16 256 x 256 images whose 2-D table is baked for 224 x 224 and resized (bicubic). Their
 lines add the one-off table kernels' times ("pos_table").
@@ -48,6 +51,8 @@ BENCH_WORKLOADS = {
                              label="I-JEPA-style ViT-L/16 256x256 image (2-D [w|h] sin-cos table baked for 224x224, "
                                    "resized bicubic)"),
 }
+PREDICTOR = "vjepa2_vitl16_predictor"
+PRED_METRIC = "masked predictor tokens/s and TFLOP/s, V-JEPA 2 ViT-L predictor over 16×256² clips"
 HEADLINE = "vjepa2_vitl16_16x256"
 FLUSH_BYTES = 256 << 20  # > 129 MB of L2
 
@@ -70,7 +75,7 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=50)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--batch", type=int, default=None, help="clips per GPU per step (default: the workload's)")
-    p.add_argument("--workload", choices=sorted(BENCH_WORKLOADS), default=HEADLINE)
+    p.add_argument("--workload", choices=sorted(BENCH_WORKLOADS) + [PREDICTOR], default=HEADLINE)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true")
     return p.parse_args(argv)
@@ -194,10 +199,213 @@ def cpu_baseline(workload=HEADLINE):
                       f"({t1:.2f} s, {t2:.2f} s); full-depth time {full:.1f} s extrapolated linearly per layer"}
 
 
+def pred_inputs(B, seed=0):
+    """Encoder tokens N(0, 1) from the shared generator and the pages' half / half split."""
+    import numpy as np
+    import synth
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from configs import PRED_VJEPA2_L16, PRED_WORKLOAD
+    grid, n_ctx, n_tgt = PRED_WORKLOAD["grid"], PRED_WORKLOAD["n_ctx"], PRED_WORKLOAD["n_tgt"]
+    n_pos = grid[0] * grid[1] * grid[2]
+    enc = synth.fill(seed, "input.enc_tokens", synth.NORMAL, 0.0, 1.0, (B, n_pos, PRED_VJEPA2_L16.enc_dim))
+    ctx = np.tile(np.arange(n_ctx, dtype=np.int32), (B, 1))
+    tgt = np.tile(np.arange(n_ctx, n_ctx + n_tgt, dtype=np.int32), (B, 1))
+    return enc, ctx, tgt, grid, PRED_VJEPA2_L16
+
+
+def pred_oracle_layer_times():
+    """The oracle predictor on one clip's tokens with 1 and 2 layers: (t1, t2, tokens, threads, L)."""
+    from dataclasses import replace
+    import oracle
+    enc, ctx, tgt, grid, cfg = pred_inputs(1)
+    times = []
+    for nl in (1, 2):
+        t0 = time.perf_counter()
+        oracle.predict(replace(cfg, n_layer=nl), 0, True, enc, ctx, tgt, grid[1:])
+        times.append(time.perf_counter() - t0)
+    return times[0], times[1], ctx.shape[1] + tgt.shape[1], oracle.num_threads(), cfg.n_layer
+
+
+def pred_cpu_baseline():
+    t1, t2, N, threads, L = pred_oracle_layer_times()
+    per_layer = max(t2 - t1, 1e-9)
+    full = t1 + (L - 1) * per_layer
+    return {"value": N / full, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"fp64 oracle predictor on one clip's {N} tokens with 1 and 2 of the {L} layers "
+                      f"({t1:.2f} s, {t2:.2f} s); full-depth time {full:.1f} s extrapolated linearly per layer"}
+
+
+def run_reference_predictor(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from dataclasses import replace
+    import oracle
+    enc, ctx, tgt, grid, cfg = pred_inputs(1)
+    t1, t2, N, threads, L = pred_oracle_layer_times()
+    per_layer = max(t2 - t1, 1e-9)
+    one = replace(cfg, n_layer=1)
+    for _ in range(args.warmup):
+        oracle.predict(one, 0, True, enc, ctx, tgt, grid[1:])
+    full_times = []
+    t_start = time.perf_counter()
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.predict(one, 0, True, enc, ctx, tgt, grid[1:])
+        full_times.append((time.perf_counter() - t0) + (L - 1) * per_layer)
+    wall = time.perf_counter() - t_start
+    mean_full = statistics.mean(full_times)
+    value = N / mean_full
+    B = args.batch or 8
+    sample = (f"each step: the fp64 oracle predictor on one clip's {N} tokens with 1 of the {L} layers; the other "
+              f"{L - 1} layers added at the calibrated per-layer time {per_layer:.2f} s; the {B} clips of a step are "
+              f"independent, so a step costs {B} such clips")
+    line = {"impl": "reference", "metric": PRED_METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * mean_full * B, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"V-JEPA 2 ViT-L masked predictor, {N} tokens per clip (1024 context + 1024 "
+                                   f"targets) x {B} per GPU", "tokens_per_step": B * N, "global_batch": B,
+                       "seq_len": N, "wall_s_sampled_steps": wall},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_predictor(args):
+    """The masked predictor: one step = one jepa_predict of B clips' tokens (graph replay)."""
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group(backend="nccl" if torch.cuda.is_available() else "gloo")
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    import jepa_vision_encoder_gb300 as jv
+
+    B = args.batch or 8
+    enc_h, ctx_h, tgt_h, grid, cfg = pred_inputs(B, seed=rank)
+    pred = jv.Predictor.preset("vjepa2_vitl16", seed=0, device=local)
+    n_ctx, n_tgt = ctx_h.shape[1], tgt_h.shape[1]
+    N = n_ctx + n_tgt
+    pc = jv.PredContext(pred, B, n_ctx, n_tgt)
+    enc, ctx, tgt = (torch.from_numpy(a).cuda() for a in (enc_h, ctx_h, tgt_h))
+    out = torch.empty((B, n_tgt, cfg.out_dim), dtype=torch.float32, device="cuda")
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    stream = pc.stream
+    peaks = measured_peaks()
+    with torch.cuda.stream(stream):
+        pc.set_graph(True)
+        for _ in range(args.warmup):
+            flush.zero_()
+            pc.predict(enc, ctx, tgt, grid, out)
+        pc.sync()
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        torch.cuda.synchronize()
+        barrier(local)
+        torch.cuda.synchronize()
+        with ClockSampler(local) as clk:
+            for i in range(args.steps):
+                flush.zero_()
+                starts[i].record(stream)
+                pc.predict(enc, ctx, tgt, grid, out)
+                ends[i].record(stream)
+            torch.cuda.synchronize()
+        barrier(local)
+        torch.cuda.synchronize()
+        pc.sync()
+        step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+        # per-kernel durations: eager launches with events around each kernel
+        pc.set_profiling(True)
+        for _ in range(2):
+            pc.predict(enc, ctx, tgt, grid, out)
+        pc.profile(reset=True)
+        p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        p0.record(stream)
+        for _ in range(args.steps):
+            flush.zero_()
+            pc.predict(enc, ctx, tgt, grid, out)
+        p1.record(stream)
+        torch.cuda.synchronize()
+        prof = pc.profile(reset=True)
+        pc.set_profiling(False)
+    total_ms = reduce_max(sum(step_ms), device="cuda" if world > 1 else None)
+    ms_per_step = total_ms / args.steps
+    tokens_per_step = world * B * N
+    value = tokens_per_step * args.steps / (total_ms / 1e3)
+    flops_per_step = sum(v["flops"] for v in prof.values()) / args.steps
+    tflops = world * flops_per_step * args.steps / (total_ms / 1e3) / 1e12
+    name, st = max(prof.items(), key=lambda kv: kv[1]["total_ms"])
+    avg_ms = st["total_ms"] / st["launches"]
+    if st["flops"] > 0:
+        achieved = st["flops"] / st["launches"] / (avg_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"], "kernel": name,
+                "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"]}
+    else:
+        achieved = st["bytes"] / st["launches"] / (avg_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "kernel": name}
+    rec = NCU_TRAFFIC.get((args.workload, name, B))
+    roof["traffic"] = rec["bytes_per_launch"] if rec and rec.get("sha1") == source_sha1(name) else None
+    roof["peak_source"] = peaks["source"]
+    tot = max(sum(x["total_ms"] for x in prof.values()), 1e-9)
+    kernels = {k: {"launches": v["launches"], "avg_us": 1e3 * v["total_ms"] / v["launches"], "share": v["total_ms"] / tot,
+                   **({"tflops": v["flops"] / (v["total_ms"] / 1e3) / 1e12} if v["flops"] else {}),
+                   **({"gbs": v["bytes"] / (v["total_ms"] / 1e3) / 1e9} if v["bytes"] else {})}
+               for k, v in prof.items()}
+    # end to end: encoder tokens and ids from pinned host memory, predictions back, every step
+    pin = [torch.from_numpy(a).pin_memory() for a in (enc_h, ctx_h, tgt_h)]
+    pin_out = torch.empty((B, n_tgt, cfg.out_dim), dtype=torch.float32).pin_memory()
+    e2e_steps = min(args.steps, 20)
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            enc.copy_(pin[0], non_blocking=True)
+            ctx.copy_(pin[1], non_blocking=True)
+            tgt.copy_(pin[2], non_blocking=True)
+            pc.predict(enc, ctx, tgt, grid, out)
+            pin_out.copy_(out, non_blocking=True)
+        pc.sync()
+    e2e_step()
+    barrier(local)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2e_s = reduce_max(time.perf_counter() - t0, device="cuda" if world > 1 else None)
+    e2e = {"value": tokens_per_step * e2e_steps / e2e_s, "unit": "tokens/s",
+           "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in pin),
+           "d2h_bytes_per_step": pin_out.numel() * 4}
+    if rank == 0:
+        line = {"metric": PRED_METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": f"V-JEPA 2 ViT-L masked predictor, {N} tokens per clip ({n_ctx} context + "
+                                       f"{n_tgt} targets) x {B} per GPU", "tokens_per_step": tokens_per_step,
+                           "global_batch": world * B, "seq_len": N,
+                           "parallelism": f"replicas x{world} (independent clips, no collective)",
+                           "l2": "flushed (256 MiB write) between steps", "weights": "seeded synthetic"},
+                "tflops": tflops, "frac_of_bf16_peak": tflops / (world * peaks["bf16_tflops"]),
+                "launch_mode": "CUDA graph replay of the predictor", "roofline": roof, "kernels": kernels,
+                "e2e": e2e, "gpu_launches": pc.launches(n_ctx) * args.steps,
+                "clocks": clk.summary(), "profiled_pass": {"ms_per_step": p0.elapsed_time(p1) / args.steps}}
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = pred_cpu_baseline()
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
+    if args.workload == PREDICTOR:
+        return run_reference_predictor(args)
     import oracle
     from dataclasses import replace
     import synth
@@ -494,6 +702,8 @@ def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload == PREDICTOR:
+        return run_predictor(args)
     return run_ours(args)
 
 

@@ -236,6 +236,12 @@ typedef struct {
   int32_t patches_per_item;
   const float* d_pos;         /* [rows_per_item, N] learned table (rows = [prefix; patches]) or NULL */
   const float* d_vec;         /* [N] vector added to every patch row (modality) or NULL */
+  /* QKV_ROPE, optional: d_rope_ids [M] gives every row's patch index (its position in d_rope's
+   * grid) in place of its place in its item (token sequences that are not the grid in order);
+   * qkv_pad64 (bf16, head_dim 32 only) stores head h of q, k and v at columns 64h .. 64h+31 of
+   * a [M, 3*n_head*64] output whose other columns the caller keeps at zero. */
+  const int32_t* d_rope_ids;
+  int32_t qkv_pad64;
 } jepa_epilogue;
 
 /* out = epilogue(x w^T): d_x [M, K], d_w [N, K] (PyTorch Linear layout), both fp32 (dtype
@@ -277,6 +283,10 @@ jepa_status jepa_op_pos_resize(const float* d_src, int32_t st, int32_t sh, int32
 /* Softmax attention per (item, head): o = softmax(q k^T / sqrt(head_dim) + mask) v.
  * d_qkv: [B*N, 3*n_head*head_dim] ([q | k | v] columns, heads contiguous), d_out: [B*N, n_head*head_dim];
  * fp32 (dtype JEPA_FP32) or bf16 (JEPA_BF16: tcgen05 flash kernel); head_dim 64.
+ * bf16 also takes head_dim 32 (the masked predictor's heads) in a zero-padded layout: d_qkv is
+ * [B*N, 3*n_head*64] with head h of q, k and v in columns 64h .. 64h+31 of its third and zeros in
+ * 64h+32 .. 64h+63 (the layout a QKV_ROPE epilogue with qkv_pad64 writes); d_out stays compact,
+ * [B*N, n_head*32]; the scale is 1/sqrt(32).
  * attn_mode JEPA_ATTN_BLOCK_CAUSAL: the first `prefix` rows see every key, prefix columns are
  * closed to the other rows, and patch key j is visible to patch query i iff
  * (i - prefix) / frame_tokens >= (j - prefix) / frame_tokens. */
@@ -316,6 +326,77 @@ jepa_status jepa_encode_noalloc(const jepa_model* m, const float* d_pixels, int3
                                 int32_t W, int32_t layout, float* d_tokens, void* stream);
 
 /* Thread-local text of the last failure of this thread, and its reset. */
+/* ------------------------------------------------------------------ masked predictor
+ *
+ * The masked-latent predictor of V-JEPA 2 ("GGUF schema (v1)", Predictor: pred.* tensors; the
+ * SkyVision V-JEPA 2 notes, masked-latent predictor): per item, the encoder tokens at the context
+ * ids are projected by pred.embed (enc_dim -> embed_dim), a mask token (row mask_index mod
+ * n_mask_tokens of pred.mask_tokens) stands at each target id, the sequence runs through
+ * n_layer pre-LN blocks of the encoder's layout (pred.blk.*) with 3-D RoPE at the ids'
+ * positions and full attention, pred.norm, and the target rows are projected by pred.proj
+ * (embed_dim -> out_dim). The pages order the tokens by position id before the blocks and
+ * restore the order after pred.norm; with full attention and per-token positions that order
+ * changes no result, so the library keeps the input order [context ; targets]. */
+typedef struct jepa_predictor jepa_predictor;
+typedef struct jepa_pred_context jepa_pred_context;
+
+/* jepa.pred.* hyper-parameters. head_dim = embed_dim / n_head must be 32 or 64. */
+typedef struct {
+  int32_t embed_dim, n_layer, n_head, ffn_dim; /* V-JEPA 2: 384, 12, 12, 1536 */
+  int32_t enc_dim, out_dim;                    /* pred.embed input width, pred.proj output width */
+  int32_t n_mask_tokens, mask_index;           /* 10 (V-JEPA 2); the row the targets take (1 by default) */
+  float ln_eps, rope_theta;
+  int32_t rope_layout;                         /* JEPA_ROPE_TILED (V-JEPA 2) or JEPA_ROPE_INTERLEAVED */
+} jepa_pred_hparams;
+
+/* "vjepa2_vitl16": the V-JEPA 2 ViT-L predictor (384 wide, 12 layers, 12 heads of 32, ffn 1536,
+ * enc and out 1024, 10 mask tokens, mask index 1: transformers never passes another index,
+ * per the pages). Unknown name -> JEPA_E_INVALID_ARG. */
+jepa_status jepa_pred_preset(const char* name, jepa_pred_hparams* out);
+jepa_status jepa_pred_hparams_validate(const jepa_pred_hparams* hp);
+
+/* Synthesise every pred.* tensor (the enc.* recipe of jepa_model_load) and upload it to `device`;
+ * bf16 only (dtype JEPA_FP32 -> JEPA_E_UNSUPPORTED). Immutable, shareable. */
+jepa_status jepa_pred_load(const jepa_pred_hparams* hp, uint64_t seed, int32_t dtype, int32_t device,
+                           jepa_predictor** out);
+void jepa_pred_free(jepa_predictor* p);
+/* Copy pred.* tensor `name` to host floats (n_elems must match), as jepa_model_tensor. */
+jepa_status jepa_pred_tensor(const jepa_predictor* p, const char* name, float* h_dst, size_t n_elems);
+
+/* Workspace for up to max_batch items of max_ctx context and max_tgt target tokens
+ * (max_workspace_bytes 0 = 8 GiB; over budget -> JEPA_E_BUDGET). Own non-blocking stream. */
+jepa_status jepa_pred_context_new(const jepa_predictor* p, int32_t max_batch, int32_t max_ctx, int32_t max_tgt,
+                                  size_t max_workspace_bytes, jepa_pred_context** out);
+void jepa_pred_context_free(jepa_pred_context* c);
+jepa_status jepa_pred_context_set_stream(jepa_pred_context* c, void* stream);
+/* enable != 0: capture the launch sequence of a (shape, pointers) key into a CUDA graph on first
+ * use and replay it afterwards. */
+jepa_status jepa_pred_context_set_graph(jepa_pred_context* c, int32_t enable);
+/* Events around every launch (eager launches only while on); jepa_pred_context_profile folds them
+ * per kernel class as jepa_context_profile does. */
+jepa_status jepa_pred_context_set_profiling(jepa_pred_context* c, int32_t enable);
+jepa_status jepa_pred_context_profile(jepa_pred_context* c, jepa_kernel_stat* out, int32_t max, int32_t* n_out,
+                                      int32_t reset);
+/* Kernel launches of one jepa_predict of this shape. */
+jepa_status jepa_pred_context_launches(const jepa_pred_context* c, int32_t n_ctx, int32_t* n_out);
+
+/* Predict B items, asynchronously on the context stream.
+ *  d_enc:     device float [B, n_enc, enc_dim], the encoder's output tokens (no prefix rows)
+ *  d_ctx_ids: device int32 [B, n_ctx], context token indices in [0, n_enc) and < gt*gh*gw
+ *  d_tgt_ids: device int32 [B, n_tgt], target positions in [0, gt*gh*gw); an id may repeat and
+ *             may also be a context id (the pages' all-to-all default)
+ *  gt, gh, gw: the position grid the ids index (id -> t = id / (gh gw), h = id % (gh gw) / gw,
+ *             w = id % gw; the pages decode predictor ids on the fixed img_size/patch grid)
+ *  d_out:     device float [B, n_tgt, out_dim], 16-byte aligned
+ * n_ctx may be 0; n_tgt >= 1; enc_dim % 8 == 0. An id out of range is replaced by 0 on the device
+ * and reported as JEPA_E_INVALID_ARG by the next jepa_pred_context_sync. */
+jepa_status jepa_predict(jepa_pred_context* c, const float* d_enc, int32_t B, int32_t n_enc, const int32_t* d_ctx_ids,
+                         int32_t n_ctx, const int32_t* d_tgt_ids, int32_t n_tgt, int32_t gt, int32_t gh, int32_t gw,
+                         float* d_out);
+/* Wait for the context stream; JEPA_E_INVALID_ARG if an id was out of range, JEPA_E_TIMEOUT if a
+ * bounded wait gave up (the word is cleared). */
+jepa_status jepa_pred_context_sync(jepa_pred_context* c);
+
 const char* jepa_error_text(void);
 void jepa_error_reset(void);
 

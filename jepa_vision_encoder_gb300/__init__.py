@@ -17,9 +17,10 @@ from . import _lib
 from ._lib import (ATTN_BLOCK_CAUSAL, ATTN_FULL, BF16, EPI_BIAS, EPI_BIAS_GELU, EPI_BIAS_RESIDUAL,
                    EPI_PATCH_EMBED, EPI_QKV_ROPE, FP32, LAYOUT_CTHW, LAYOUT_TCHW, POS_LEARNED, POS_NONE,
                    POS_ROPE3D, POS_SINCOS2D, POS_SINCOS3D, RESIZE_BICUBIC, RESIZE_TRILINEAR, ROPE_INTERLEAVED,
-                   ROPE_TILED, Epilogue, HParams, JepaError, check, lib)
+                   ROPE_TILED, Epilogue, HParams, JepaError, PredHParams, check, lib)
 
-__all__ = ["Model", "Context", "HParams", "JepaError", "preset", "hparams", "n_tokens", "ops", "lib"]
+__all__ = ["Model", "Context", "HParams", "JepaError", "preset", "hparams", "n_tokens", "ops", "lib", "Predictor",
+           "PredContext", "PredHParams", "pred_preset"]
 
 PRESETS = ("hfvit_ti14", "vjepa2_vitl16", "vjepa2_1_vitl16", "levjepa_vitl16", "vjepa2_vitg16", "vjepa_vitl16",
            "ijepa_vitl16")
@@ -220,6 +221,119 @@ class Context:
             pass
 
 
+def pred_preset(name: str) -> PredHParams:
+    hp = PredHParams()
+    check(lib().jepa_pred_preset(name.encode(), ctypes.byref(hp)))
+    return hp
+
+
+class Predictor:
+    """Synthetic-weight masked-latent predictor (pred.* tensors) resident on one GPU, bf16."""
+
+    def __init__(self, hp: PredHParams, seed: int = 0, dtype="bf16", device: int = 0):
+        self.hp = hp
+        self.seed = seed
+        self.device = device
+        h = ctypes.c_void_p()
+        check(lib().jepa_pred_load(ctypes.byref(hp), seed, _dtype_code(dtype), device, ctypes.byref(h)))
+        self._h = h
+
+    @classmethod
+    def preset(cls, name: str, seed: int = 0, dtype="bf16", device: int = 0, **overrides):
+        hp = pred_preset(name)
+        for k, v in overrides.items():
+            setattr(hp, k, v)
+        return cls(hp, seed=seed, dtype=dtype, device=device)
+
+    def tensor(self, name: str, shape) -> torch.Tensor:
+        """A pred.* tensor copied to host memory as float32."""
+        n = 1
+        for s in shape:
+            n *= s
+        out = torch.empty(n, dtype=torch.float32)
+        check(lib().jepa_pred_tensor(self._h, name.encode(), ctypes.c_void_p(out.data_ptr()), n))
+        return out.reshape(shape)
+
+    def close(self):
+        if getattr(self, "_h", None):
+            lib().jepa_pred_free(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class PredContext:
+    """Workspace for up to max_batch items of max_ctx context and max_tgt target tokens; streams
+    as Context (an own side stream ordered with torch's current stream, or the given `stream`)."""
+
+    def __init__(self, pred: Predictor, max_batch: int, max_ctx: int, max_tgt: int, max_workspace_bytes: int = 0,
+                 stream=None, graph: bool = False):
+        self.pred = pred
+        h = ctypes.c_void_p()
+        check(lib().jepa_pred_context_new(pred._h, max_batch, max_ctx, max_tgt, max_workspace_bytes, ctypes.byref(h)))
+        self._h = h
+        self._own = stream is None
+        self.stream = torch.cuda.Stream(device=pred.device) if stream is None else stream
+        check(lib().jepa_pred_context_set_stream(self._h, ctypes.c_void_p(self.stream.cuda_stream)))
+        if graph:
+            check(lib().jepa_pred_context_set_graph(self._h, 1))
+
+    def set_graph(self, enable: bool):
+        check(lib().jepa_pred_context_set_graph(self._h, int(enable)))
+
+    def set_profiling(self, enable: bool):
+        check(lib().jepa_pred_context_set_profiling(self._h, int(enable)))
+
+    def launches(self, n_ctx: int) -> int:
+        n = ctypes.c_int32()
+        check(lib().jepa_pred_context_launches(self._h, n_ctx, ctypes.byref(n)))
+        return n.value
+
+    def predict(self, enc: torch.Tensor, ctx_ids: torch.Tensor, tgt_ids: torch.Tensor, grid, out: torch.Tensor = None):
+        """enc: float32 CUDA [B, n_enc, enc_dim]; ctx_ids / tgt_ids: int32 CUDA [B, n]; grid (gt, gh, gw)."""
+        assert enc.is_cuda and enc.dtype == torch.float32 and enc.is_contiguous()
+        assert tgt_ids.dtype == torch.int32 and tgt_ids.is_contiguous()
+        assert ctx_ids.dtype == torch.int32 and ctx_ids.is_contiguous()
+        B, n_enc, _ = enc.shape
+        n_ctx, n_tgt = ctx_ids.shape[-1], tgt_ids.shape[-1]
+        if out is None:
+            out = torch.empty((B, n_tgt, self.pred.hp.out_dim), dtype=torch.float32, device=enc.device)
+        if self._own:
+            self.stream.wait_stream(torch.cuda.current_stream(self.stream.device))
+        ctx_ptr = ctypes.c_void_p(ctx_ids.data_ptr() if n_ctx else 0)
+        check(lib().jepa_predict(self._h, _ptr(enc), B, n_enc, ctx_ptr, n_ctx, _ptr(tgt_ids), n_tgt, grid[0], grid[1],
+                                 grid[2], _ptr(out)))
+        if self._own:
+            torch.cuda.current_stream(self.stream.device).wait_stream(self.stream)
+        return out
+
+    def sync(self):
+        check(lib().jepa_pred_context_sync(self._h))
+
+    def profile(self, reset: bool = True) -> dict:
+        """Per-kernel-class event timings (profiling on: eager launches), as Context.profile."""
+        buf = (_lib.KernelStat * 16)()
+        n = ctypes.c_int32()
+        check(lib().jepa_pred_context_profile(self._h, buf, 16, ctypes.byref(n), int(reset)))
+        return {buf[i].name.decode(): {"launches": buf[i].launches, "total_ms": buf[i].total_ms,
+                                       "flops": buf[i].flops, "bytes": buf[i].bytes} for i in range(n.value)}
+
+    def close(self):
+        if getattr(self, "_h", None):
+            lib().jepa_pred_context_free(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
 class ops:
     """The encoder's kernels one at a time (same kernels the encode path launches)."""
 
@@ -249,7 +363,7 @@ class ops:
     def linear(x: torch.Tensor, w: torch.Tensor, bias: torch.Tensor, out: torch.Tensor, kind: int = EPI_BIAS,
                rope: torch.Tensor = None, rows_per_item: int = 1, prefix: int = 0, n_head: int = 0,
                head_dim: int = 0, rope_layout: int = 0, patches_per_item: int = 1, pos: torch.Tensor = None,
-               vec: torch.Tensor = None):
+               vec: torch.Tensor = None, rope_ids: torch.Tensor = None, qkv_pad64: bool = False):
         M, K = x.shape
         N = w.shape[0]
         code = BF16 if x.dtype == torch.bfloat16 else FP32
@@ -266,6 +380,8 @@ class ops:
         e.patches_per_item = patches_per_item
         e.d_pos = pos.data_ptr() if pos is not None else None
         e.d_vec = vec.data_ptr() if vec is not None else None
+        e.d_rope_ids = rope_ids.data_ptr() if rope_ids is not None else None
+        e.qkv_pad64 = int(qkv_pad64)
         check(lib().jepa_op_linear(code, _ptr(x), M, K, _ptr(w), N, ctypes.byref(e), _stream_ptr()))
         return out
 

@@ -43,7 +43,20 @@ class Epilogue(ctypes.Structure):
         ("d_rope", ctypes.c_void_p), ("rows_per_item", ctypes.c_int32), ("prefix", ctypes.c_int32),
         ("n_head", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("rope_layout", ctypes.c_int32),
         ("patches_per_item", ctypes.c_int32), ("d_pos", ctypes.c_void_p), ("d_vec", ctypes.c_void_p),
+        ("d_rope_ids", ctypes.c_void_p), ("qkv_pad64", ctypes.c_int32),
     ]
+
+
+class PredHParams(ctypes.Structure):
+    _fields_ = [
+        ("embed_dim", ctypes.c_int32), ("n_layer", ctypes.c_int32), ("n_head", ctypes.c_int32),
+        ("ffn_dim", ctypes.c_int32), ("enc_dim", ctypes.c_int32), ("out_dim", ctypes.c_int32),
+        ("n_mask_tokens", ctypes.c_int32), ("mask_index", ctypes.c_int32), ("ln_eps", ctypes.c_float),
+        ("rope_theta", ctypes.c_float), ("rope_layout", ctypes.c_int32),
+    ]
+
+    def as_dict(self):
+        return {k: getattr(self, k) for k, _ in self._fields_}
 
 
 class KernelStat(ctypes.Structure):
@@ -54,6 +67,7 @@ class KernelStat(ctypes.Structure):
 # name -> (restype, argtypes); the exported surface of include/jepa.h
 _P, _I, _U64, _SZ, _F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_uint64, ctypes.c_size_t, ctypes.c_float
 _HP = ctypes.POINTER(HParams)
+_PHP = ctypes.POINTER(PredHParams)
 SIGNATURES = {
     "jepa_preset": (_I, [ctypes.c_char_p, _HP]),
     "jepa_hparams_validate": (_I, [_HP]),
@@ -84,6 +98,20 @@ SIGNATURES = {
     "jepa_device_status": (_I, []),
     "jepa_debug_wait_timeout": (_I, [_I]),
     "jepa_encode_noalloc": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P]),
+    "jepa_pred_preset": (_I, [ctypes.c_char_p, _PHP]),
+    "jepa_pred_hparams_validate": (_I, [_PHP]),
+    "jepa_pred_load": (_I, [_PHP, _U64, _I, _I, ctypes.POINTER(_P)]),
+    "jepa_pred_free": (None, [_P]),
+    "jepa_pred_tensor": (_I, [_P, ctypes.c_char_p, _P, _SZ]),
+    "jepa_pred_context_new": (_I, [_P, _I, _I, _I, _SZ, ctypes.POINTER(_P)]),
+    "jepa_pred_context_free": (None, [_P]),
+    "jepa_pred_context_set_stream": (_I, [_P, _P]),
+    "jepa_pred_context_set_graph": (_I, [_P, _I]),
+    "jepa_pred_context_set_profiling": (_I, [_P, _I]),
+    "jepa_pred_context_profile": (_I, [_P, ctypes.POINTER(KernelStat), _I, ctypes.POINTER(ctypes.c_int32), _I]),
+    "jepa_pred_context_launches": (_I, [_P, _I, ctypes.POINTER(ctypes.c_int32)]),
+    "jepa_predict": (_I, [_P, _P, _I, _I, _P, _I, _P, _I, _I, _I, _I, _P]),
+    "jepa_pred_context_sync": (_I, [_P]),
     "jepa_error_text": (ctypes.c_char_p, []),
     "jepa_error_reset": (None, []),
 }

@@ -16,8 +16,9 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libjepa_gb300.so")
-SOURCES = ["runtime.cu", "gemm_tc.cu", "gemm_tc2.cu", "attention_tc.cu", "simt.cu", "rowops.cu", "postab.cu"]
-HEADERS = ["ptx.cuh", "epilogue.cuh", "kernels.h"]
+SOURCES = ["runtime.cu", "gemm_tc.cu", "gemm_tc2.cu", "attention_tc.cu", "simt.cu", "rowops.cu", "postab.cu",
+           "predictor.cu"]
+HEADERS = ["ptx.cuh", "epilogue.cuh", "kernels.h", "internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

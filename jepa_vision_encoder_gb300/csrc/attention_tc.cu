@@ -44,6 +44,7 @@ constexpr float kRescaleThreshold = 8.0f;                 // log2 units: p stays
 struct AttnDev {
   int N, H, D;
   int attn_mode, prefix, frame_tokens;
+  int out_hd;  // output columns per head (64, or 32 for zero-padded heads of width 32)
   __nv_bfloat16* out;
   float scale_log2;
   int* err;
@@ -322,9 +323,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     if (store) {
       tc_fence_after();
       const float inv = (l_run > 0.0f) ? 1.0f / l_run : 0.0f;
-      __nv_bfloat16* dst = a.out + ((size_t)b * a.N + q) * a.D + h * kHD;
+      __nv_bfloat16* dst = a.out + ((size_t)b * a.N + q) * (a.H * a.out_hd) + h * a.out_hd;
 #pragma unroll 1
-      for (int c = 0; c < kHD / 32; ++c) {
+      for (int c = 0; c < a.out_hd / 32; ++c) {
         uint32_t ov[32];
         tmem_ld32(tO + c * 32, ov);
         tmem_ld_wait(ov);
@@ -366,7 +367,7 @@ cudaError_t tc_kernels_init() {
 
 cudaError_t attention_tc_launch(const CUtensorMap& tmQKV, const AttnParams& p, int* err, uint64_t limit_ns,
                                 cudaStream_t s) {
-  if (p.head_dim != kHD) return cudaErrorInvalidValue;
+  if (p.head_dim != kHD || (p.real_hd != 64 && p.real_hd != 32)) return cudaErrorInvalidValue;
   if (p.B <= 0 || p.N <= 0) return cudaSuccess;
   AttnDev a;
   a.N = p.N;
@@ -376,7 +377,8 @@ cudaError_t attention_tc_launch(const CUtensorMap& tmQKV, const AttnParams& p, i
   a.prefix = p.prefix;
   a.frame_tokens = p.frame_tokens > 0 ? p.frame_tokens : 1;
   a.out = reinterpret_cast<__nv_bfloat16*>(p.out);
-  a.scale_log2 = 1.4426950408889634f / 8.0f;  // log2(e) / sqrt(64)
+  a.out_hd = p.real_hd;
+  a.scale_log2 = 1.4426950408889634f / sqrtf((float)p.real_hd);  // log2(e) / sqrt(head width)
   a.err = err;
   a.limit_ns = limit_ns;
   dim3 grid((p.N + 2 * kQT - 1) / (2 * kQT), p.H, p.B);

@@ -27,6 +27,12 @@ struct EpiArgs {
   const float2* rope_axes;  // [gt + gh + gw, dh]: the t rows, then h, then w (used when not null)
   int rope_gt, rope_gh, rope_gw;
   int rows_per_item, prefix, n_head, head_dim, rope_layout, rope_d;
+  // optional: the patch position id of every output row m (rope_ids[m]), for token sequences that
+  // are not the patch grid in order (the masked predictor's context and target tokens)
+  const int* rope_ids;
+  // head_dim 32 only: store each 32-column head at a 64-column pitch (the upper 32 columns of a
+  // head stay as they are: zero), the layout the width-64 attention kernel reads
+  int qkv_pad64;
   // patch embedding: input row m = patch i of item b (i = m % patches_per_item)
   int patches_per_item;
   const float* pos;       // [rows_per_item, N] or null
@@ -55,9 +61,10 @@ __device__ __forceinline__ float2 gelu_fast2(float2 x) {
   return __fmul2_rn(x, f);
 }
 
-// The (cos, sin) rows (dh entries each) of the t, h and w axes of token row p of an item.
-__device__ __forceinline__ void rope_axis_rows(const EpiArgs& a, int p, int dh, const float2* (&r)[3]) {
-  const int pp = p - a.prefix;
+// The (cos, sin) rows (dh entries each) of the t, h and w axes of output row m, row p of its item.
+__device__ __forceinline__ void rope_axis_rows(const EpiArgs& a, int m, int p, int dh, const float2* (&r)[3]) {
+  // rows past M (the ragged tail of the last tile, never stored) must not read past rope_ids
+  const int pp = a.rope_ids != nullptr ? (m < a.M ? __ldg(a.rope_ids + m) : 0) : p - a.prefix;
   if (a.rope_axes != nullptr) {
     const int hw = a.rope_gh * a.rope_gw;
     const int t = pp / hw, rem = pp - t * hw, h = rem / a.rope_gw, w = rem - h * a.rope_gw;
@@ -99,11 +106,11 @@ __device__ __forceinline__ void rope_hd64_chunk(float (&v)[32], const float2* co
 // 3-D RoPE on E consecutive columns n0.. (n0 even) of token row p of an item, any even head width:
 // q columns [0, D) and k columns [D, 2D) are rotated, v columns pass.
 template <int E>
-__device__ __forceinline__ void rope_generic(const EpiArgs& a, int p, int n0, float (&v)[E]) {
+__device__ __forceinline__ void rope_generic(const EpiArgs& a, int m, int p, int n0, float (&v)[E]) {
   const int D = a.n_head * a.head_dim;
   const int d = a.rope_d, dh = d >> 1;
   const float2* rows[3];
-  rope_axis_rows(a, p, dh, rows);
+  rope_axis_rows(a, m, p, dh, rows);
   float r[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) {
@@ -156,7 +163,7 @@ __device__ __forceinline__ void epi_fragment(const EpiArgs& a, int m, int n0, fl
       if (!done && a.head_dim == 64 && (n0 & 31) == 0) {
         if (n0 < 2 * a.n_head * 64) {
           const float2* rows[3];
-          rope_axis_rows(a, p, 10, rows);
+          rope_axis_rows(a, m, p, 10, rows);
           const bool upper = (n0 & 63) != 0;
           if (a.rope_layout == 0) {
             if (upper) rope_hd64_chunk<32, 0>(v, rows); else rope_hd64_chunk<0, 0>(v, rows);
@@ -167,7 +174,7 @@ __device__ __forceinline__ void epi_fragment(const EpiArgs& a, int m, int n0, fl
         done = true;
       }
     }
-    if (!done) rope_generic<E>(a, p, n0, v);  // any even head width, any fragment (the fp32 SIMT GEMM)
+    if (!done) rope_generic<E>(a, m, p, n0, v);  // any even head width, any fragment (the fp32 SIMT GEMM)
   }
 
   if (a.kind == kEpiResidual) {
@@ -265,7 +272,7 @@ __device__ __forceinline__ void epi_math_tc(const EpiArgs& a, int m, int n0, flo
     if ((a.rope != nullptr || a.rope_axes != nullptr) && p >= a.prefix && n0 < 2 * a.n_head * a.head_dim) {
       if (a.head_dim == 64) {
         const float2* rows[3];
-        rope_axis_rows(a, p, 10, rows);
+        rope_axis_rows(a, m, p, 10, rows);
         const bool upper = (n0 & 63) != 0;
         if (a.rope_layout == 0) {
           if (upper) rope_hd64_chunk<32, 0>(v, rows); else rope_hd64_chunk<0, 0>(v, rows);
@@ -273,7 +280,7 @@ __device__ __forceinline__ void epi_math_tc(const EpiArgs& a, int m, int n0, flo
           if (upper) rope_hd64_chunk<32, 1>(v, rows); else rope_hd64_chunk<0, 1>(v, rows);
         }
       } else {
-        rope_generic<32>(a, p, n0, v);  // any even head width
+        rope_generic<32>(a, m, p, n0, v);  // any even head width
       }
     }
   }
@@ -373,7 +380,8 @@ __device__ __forceinline__ void epi_chunk_tc(const EpiArgs& a, const CUtensorMap
       uint32_t w[16];
 #pragma unroll
       for (int e = 0; e < 16; ++e) w[e] = pack_bf16x2(v[2 * e], v[2 * e + 1]);
-      st.put(lane, w, tm_out, n0, y0, false);
+      // a padded QKV output puts head n0 / 32 (width 32) at column 64 * (n0 / 32)
+      st.put(lane, w, tm_out, (EK == kEpiQkvRope && a.qkv_pad64) ? (n0 >> 5) << 6 : n0, y0, false);
     }
   }
 }
@@ -413,7 +421,7 @@ __device__ __forceinline__ void epi_warp_qkv_hd64(const EpiArgs& a, const CUtens
     for (int k = 0; k < 10; ++k) cs[ax][k] = make_float2(1.0f, 0.0f);
   if (rot) {
     const float2* rows[3];
-    rope_axis_rows(a, p, 10, rows);
+    rope_axis_rows(a, y0 + lane, p, 10, rows);
 #pragma unroll
     for (int ax = kA0; ax < kA0 + 2; ++ax)
 #pragma unroll
@@ -445,6 +453,71 @@ __device__ __forceinline__ void epi_warp_qkv_hd64(const EpiArgs& a, const CUtens
   }
 }
 
+// 3-D RoPE of one head of width 32 held in v: d = 2*((32/3)/2) = 10 rotated dims per axis (t: 0-9,
+// h: 10-19, w: 20-29), 30-31 untouched; 5 frequencies per axis, so in the tiled layout the odd
+// member of a pair wraps (frequency (jj + 1) mod 5). cs = the row's (cos, sin) values, cs[axis][k].
+template <int LAYOUT>
+__device__ __forceinline__ void rope_hd32_regs(float (&v)[32], const float2 (&cs)[3][5]) {
+#pragma unroll
+  for (int e = 0; e < 30; e += 2) {
+    constexpr int kD = 10, kDh = 5;
+    const int axis = e / kD, jj = e - axis * kD;
+    const int k0 = LAYOUT == 0 ? (jj % kDh) : (jj >> 1);
+    const int k1 = LAYOUT == 0 ? ((jj + 1) % kDh) : ((jj + 1) >> 1);
+    const float x0 = v[e], x1 = v[e + 1];
+    v[e] = fmaf(x0, cs[axis][k0].x, -x1 * cs[axis][k0].y);
+    v[e + 1] = fmaf(x1, cs[axis][k1].x, x0 * cs[axis][k1].y);
+  }
+}
+
+// QKV epilogue of a warp for heads of width 32 (every 32-column chunk is one head): the row's 15
+// (cos, sin) values are loaded once per tile, each q / k chunk rotates from registers, and a
+// padded output puts head n0 / 32 at column 64 * (n0 / 32).
+template <int NCHUNK>
+__device__ __forceinline__ void epi_warp_qkv_hd32(const EpiArgs& a, const CUtensorMap* tm, EpiStage& st, int lane,
+                                                  uint32_t trow, int y0, int n_tile0, int half) {
+  const int m = y0 + lane;
+  const int p = m % a.rows_per_item;
+  const bool rot = (a.rope != nullptr || a.rope_axes != nullptr) && p >= a.prefix;
+  float2 cs[3][5];
+#pragma unroll
+  for (int ax = 0; ax < 3; ++ax)
+#pragma unroll
+    for (int k = 0; k < 5; ++k) cs[ax][k] = make_float2(1.0f, 0.0f);
+  if (rot) {
+    const float2* rows[3];
+    rope_axis_rows(a, m, p, 5, rows);
+#pragma unroll
+    for (int ax = 0; ax < 3; ++ax)
+#pragma unroll
+      for (int k = 0; k < 5; ++k) cs[ax][k] = __ldg(rows[ax] + k);
+  }
+  const int qk_cols = 2 * a.n_head * 32;
+  const int c0 = half * NCHUNK;
+  uint32_t r[2][32];
+  tmem_ld32(trow + c0 * 32, r[0]);
+#pragma unroll
+  for (int i = 0; i < NCHUNK; ++i) {
+    tmem_ld_wait(r[i & 1]);
+    if (i + 1 < NCHUNK) tmem_ld32(trow + (c0 + i + 1) * 32, r[(i + 1) & 1]);
+    float v[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[i & 1][e]);
+    const int n0 = n_tile0 + (c0 + i) * 32;
+    epi_math_tc<kEpiBias>(a, m, n0, v);
+    if (n0 < qk_cols) {  // q and k heads rotate (warp-uniform); v heads pass
+      if (a.rope_layout == 0)
+        rope_hd32_regs<0>(v, cs);
+      else
+        rope_hd32_regs<1>(v, cs);
+    }
+    uint32_t w[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) w[e] = pack_bf16x2(v[2 * e], v[2 * e + 1]);
+    st.put(lane, w, tm, a.qkv_pad64 ? (n0 >> 5) << 6 : n0, y0, false);
+  }
+}
+
 // The epilogue of one warp for one accumulator tile: NCHUNK 32-column chunks of its 32 TMEM lanes
 // (rows y0 .. y0+31), the next tcgen05.ld in flight while a chunk is processed. half selects which
 // chunks: 0 or 1 of the warp pair sharing the lane quarter.
@@ -457,6 +530,10 @@ __device__ __forceinline__ void epi_warp_tile(const EpiArgs& a, const CUtensorMa
         epi_warp_qkv_hd64<0, NCHUNK>(a, tm, st, lane, trow, y0, n_tile0);
       else
         epi_warp_qkv_hd64<32, NCHUNK>(a, tm, st, lane, trow, y0, n_tile0);
+      return;
+    }
+    if (a.head_dim == 32) {
+      epi_warp_qkv_hd32<NCHUNK>(a, tm, st, lane, trow, y0, n_tile0, half);
       return;
     }
   }

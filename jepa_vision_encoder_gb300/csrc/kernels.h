@@ -69,7 +69,11 @@ cudaError_t gemm_simt_launch(const float* A, const float* Bw, const EpiArgs& epi
 struct AttnParams {
   int B, N, H, head_dim;
   int attn_mode, prefix, frame_tokens;
-  void* out;  // [B*N, H*head_dim]
+  void* out;  // [B*N, H*real_hd]
+  // Heads narrower than the kernel's 64 columns arrive zero-padded to 64 (q, k and v of head h at
+  // columns 64h .. 64h+63, the first real_hd of them real): the scores are scaled by
+  // 1/sqrt(real_hd) and only the real_hd output columns of each head are written.
+  int real_hd = 64;
 };
 cudaError_t attention_tc_launch(const CUtensorMap& tmQKV, const AttnParams& p, int* err, uint64_t limit_ns,
                                 cudaStream_t s);

@@ -24,6 +24,7 @@
 
 #include "jepa.h"
 #include "jepa_synth.h"
+#include "internal.h"
 #include "kernels.h"
 
 using namespace jepa;
@@ -31,8 +32,9 @@ using namespace jepa;
 // ------------------------------------------------------------------ errors
 namespace {
 thread_local std::string t_err;
+}  // namespace
 
-jepa_status fail(jepa_status s, const char* fmt, ...) {
+jepa_status jepa::fail(jepa_status s, const char* fmt, ...) {
   char buf[512];
   va_list ap;
   va_start(ap, fmt);
@@ -41,22 +43,6 @@ jepa_status fail(jepa_status s, const char* fmt, ...) {
   t_err = buf;
   return s;
 }
-
-#define CUDA_TRY(expr)                                                                         \
-  do {                                                                                         \
-    cudaError_t e_ = (expr);                                                                   \
-    if (e_ != cudaSuccess)                                                                     \
-      return fail(e_ == cudaErrorMemoryAllocation ? JEPA_E_OOM : JEPA_E_CUDA, "%s: %s (%s:%d)", \
-                  #expr, cudaGetErrorString(e_), __FILE__, __LINE__);                         \
-  } while (0)
-
-constexpr size_t kDefaultBudget = 8ull << 30;  // 8 GiB, the default arena ceiling of the pages
-
-size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
-
-int rope_d(int head_dim) { return 2 * ((head_dim / 3) / 2); }
-
-}  // namespace
 
 extern "C" const char* jepa_error_text(void) { return t_err.c_str(); }
 extern "C" void jepa_error_reset(void) { t_err.clear(); }
@@ -231,9 +217,8 @@ struct jepa_model {
   }
 };
 
-namespace {
 // Fill `n` values of tensor `name` (the synth recipe) using all host cores.
-void synth_parallel(uint64_t seed, const std::string& name, int bf16_matrices, size_t n, float* dst) {
+void jepa::synth_parallel(uint64_t seed, const std::string& name, int bf16_matrices, size_t n, float* dst) {
   int kind, is_matrix;
   double a, b;
   jsynth_param_init(name.c_str(), &kind, &a, &b, &is_matrix);
@@ -250,7 +235,6 @@ void synth_parallel(uint64_t seed, const std::string& name, int bf16_matrices, s
   }
   for (auto& x : th) x.join();
 }
-}  // namespace
 
 extern "C" jepa_status jepa_model_load(const jepa_hparams* hp, uint64_t seed, int32_t dtype, int32_t device,
                                        jepa_model** out) {
@@ -1035,6 +1019,10 @@ extern "C" jepa_status jepa_op_linear(int32_t dtype, const void* d_x, int32_t M,
         epi->rows_per_item <= 0 || epi->prefix < 0)
       return fail(JEPA_E_INVALID_ARG, "QKV_ROPE epilogue: inconsistent heads/rows");
     e.rope = reinterpret_cast<const float2*>(epi->d_rope);
+    e.rope_ids = epi->d_rope_ids;
+    e.qkv_pad64 = epi->qkv_pad64 ? 1 : 0;
+    if (e.qkv_pad64 && (dtype != JEPA_BF16 || epi->head_dim != 32))
+      return fail(JEPA_E_INVALID_ARG, "QKV_ROPE epilogue: qkv_pad64 needs the bf16 path and head_dim 32");
     e.rows_per_item = epi->rows_per_item;
     e.prefix = epi->prefix;
     e.n_head = epi->n_head;
@@ -1075,7 +1063,8 @@ extern "C" jepa_status jepa_op_linear(int32_t dtype, const void* d_x, int32_t M,
   const bool patch_tma = e.kind == kEpiPatch && e.prefix == 0 && e.rows_per_item == e.patches_per_item;
   if (e.kind != kEpiPatch || patch_tma) {
     if (reinterpret_cast<uintptr_t>(e.out) & 15) return fail(JEPA_E_INVALID_ARG, "bf16 GEMM output must be 16-byte aligned");
-    if (!make_tmap_2d_out(&to, e.out, M, N, (e.kind == kEpiResidual || e.kind == kEpiPatch) ? 4 : 2))
+    const int out_cols = e.qkv_pad64 ? 3 * e.n_head * 64 : N;  // padded heads: 64 columns each
+    if (!make_tmap_2d_out(&to, e.out, M, out_cols, (e.kind == kEpiResidual || e.kind == kEpiPatch) ? 4 : 2))
       return fail(JEPA_E_CUDA, "cuTensorMapEncodeTiled refused the output");
   }
   CUDA_TRY(gemm_tc_launch(ta, tb, to, bn, e, M, N, K, err, default_wait_limit_ns(), s));
@@ -1136,12 +1125,15 @@ extern "C" jepa_status jepa_op_attention(int32_t dtype, const void* d_qkv, int32
   if (B <= 0 || N <= 0 || n_head <= 0) return fail(JEPA_E_INVALID_ARG, "jepa_op_attention: bad size");
   if (attn_mode != 0 && attn_mode != 1) return fail(JEPA_E_INVALID_ARG, "attn_mode %d unknown", attn_mode);
   if (attn_mode == 1 && (frame_tokens <= 0 || prefix < 0)) return fail(JEPA_E_INVALID_ARG, "block-causal needs frame_tokens > 0");
-  if (head_dim != 64) return fail(JEPA_E_UNSUPPORTED, "attention kernels are built for head_dim 64 (got %d)", head_dim);
+  if (head_dim != 64 && !(head_dim == 32 && dtype == JEPA_BF16))
+    return fail(JEPA_E_UNSUPPORTED, "attention kernels are built for head_dim 64 (32 zero-padded in bf16; got %d)",
+                head_dim);
   AttnParams p;
   p.B = B;
   p.N = N;
   p.H = n_head;
-  p.head_dim = head_dim;
+  p.head_dim = 64;
+  p.real_hd = head_dim;
   p.attn_mode = attn_mode;
   p.prefix = prefix;
   p.frame_tokens = frame_tokens;

@@ -59,3 +59,12 @@ def small(name: str, n_layer: int = 2):
     if name == "ijepa_vitl16_256":      # table baked for 14x14, resized to 17x15 = 255 tokens
         return replace(cfg, n_layer=n_layer), dtype, (1, 272, 240)
     raise KeyError(name)
+
+# The V-JEPA 2 ViT-L masked predictor (jepa.pred.*): 12 layers of width 384, 12 heads of 32,
+# over the 8 x 16 x 16 position grid of a 16 x 256^2 clip; the pages' worked predictor example
+# takes the first half of the tokens as context and the second half as targets.
+from oracle import PredConfig  # noqa: E402
+
+PRED_VJEPA2_L16 = PredConfig(embed_dim=384, n_layer=12, n_head=12, ffn_dim=1536, enc_dim=1024, out_dim=1024,
+                             n_mask_tokens=10, mask_index=1)
+PRED_WORKLOAD = dict(grid=(8, 16, 16), n_ctx=1024, n_tgt=1024, batches=(1, 8))

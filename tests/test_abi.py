@@ -65,6 +65,24 @@ def test_presets_match_workloads(workload):
     assert jv.n_tokens(hp, T, H, W) == oracle.n_tokens(cfg, T, H, W)
 
 
+def test_predictor_preset_matches_its_config():
+    from configs import PRED_VJEPA2_L16
+    hp = jv.pred_preset("vjepa2_vitl16")
+    for k in ("embed_dim", "n_layer", "n_head", "ffn_dim", "enc_dim", "out_dim", "n_mask_tokens", "mask_index",
+              "rope_layout"):
+        assert getattr(hp, k) == getattr(PRED_VJEPA2_L16, k), k
+    assert jv.lib().jepa_pred_hparams_validate(ctypes.byref(hp)) == 0
+    L = jv.lib()
+    for kw, frag in [(dict(n_head=7), "not divisible"), (dict(embed_dim=33 * 12), "odd"), (dict(mask_index=-1), "mask_index"),
+                     (dict(rope_layout=3), "rope_layout"), (dict(n_layer=0), "n_layer")]:
+        bad = jv.pred_preset("vjepa2_vitl16")
+        for k, v in kw.items():
+            setattr(bad, k, v)
+        expect(L.jepa_pred_hparams_validate(ctypes.byref(bad)), _lib.E_INVALID_ARG, frag)
+    expect(L.jepa_pred_preset(b"nope", ctypes.byref(hp)), _lib.E_INVALID_ARG, "unknown preset")
+    expect(L.jepa_predict(None, None, 1, 1, None, 0, None, 1, 1, 1, 1, None), _lib.E_INVALID_ARG)
+
+
 def test_token_counts():
     assert jv.n_tokens(jv.preset("vjepa2_vitg16"), 64, 256, 256) == 8192
     hp = jv.preset("levjepa_vitl16")
