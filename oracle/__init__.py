@@ -98,6 +98,25 @@ class PredConfig:
         return self.embed_dim // self.n_head
 
 
+class OracleHeadHParams(ctypes.Structure):
+    _fields_ = [("embed_dim", ctypes.c_int), ("n_head", ctypes.c_int), ("ffn_dim", ctypes.c_int),
+                ("n_pool_layers", ctypes.c_int), ("n_classes", ctypes.c_int), ("ln_eps", ctypes.c_double)]
+
+
+@dataclass
+class HeadConfig:
+    """Attentive-pool head hyper-parameters in the jepa.head.* vocabulary."""
+    embed_dim: int
+    n_head: int
+    ffn_dim: int
+    n_pool_layers: int = 3
+    n_classes: int = 174
+    ln_eps: float = 1e-6
+
+    def struct(self) -> OracleHeadHParams:
+        return OracleHeadHParams(**asdict(self))
+
+
 def build(force: bool = False) -> str:
     """Compile liboracle.so in place (g++, OpenMP, contraction off for the generator)."""
     src = os.path.join(_HERE, "oracle.cpp")
@@ -143,6 +162,10 @@ def lib():
         L.oracle_rope_tables_pos.restype = None
         L.oracle_predict.argtypes = [ctypes.POINTER(OraclePredHParams), ctypes.c_uint64, I, P, I, I, P, I, P, I,
                                      I, I, P]
+        L.oracle_cross_attention.argtypes = [P, I, P, P, I, I, I, P]
+        L.oracle_cross_attention.restype = None
+        L.oracle_attentive_head.argtypes = [ctypes.POINTER(OracleHeadHParams), ctypes.c_uint64, I, P, I, I, P, P]
+        L.oracle_pool.argtypes = [P, I, I, I, I, I, P]
         L.oracle_mask_allow.argtypes = [I, I, I, I, I, I]
         L.oracle_attention.argtypes = [P, P, P, I, I, I, I, I, I, P]
         L.oracle_attention.restype = None
@@ -329,6 +352,40 @@ def predict(pcfg: PredConfig, seed: int, bf16_weights: bool, enc, ctx_ids, tgt_i
                               ctx.shape[1], tgt.ctypes.data, tgt.shape[1], grid[0], grid[1], out.ctypes.data)
     if rc != 0:
         raise ValueError(f"oracle_predict refused the configuration (code {rc})")
+    return out
+
+
+def cross_attention(q, k, v, n_head) -> np.ndarray:
+    """q [Nq, H*hd], k, v [Nk, H*hd] -> [Nq, H*hd]."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    hd = q.shape[1] // n_head
+    o = np.empty_like(q)
+    lib().oracle_cross_attention(q.ctypes.data, q.shape[0], k.ctypes.data, v.ctypes.data, k.shape[0], n_head, hd,
+                                 o.ctypes.data)
+    return o
+
+
+def attentive_head(hcfg: HeadConfig, seed: int, bf16_weights: bool, tokens):
+    """tokens [B, N, D] -> (pooled [B, D], logits [B, n_classes]) fp64."""
+    tokens = _f64(tokens)
+    B, N, D = tokens.shape
+    pooled = np.empty((B, D), dtype=np.float64)
+    logits = np.empty((B, hcfg.n_classes), dtype=np.float64)
+    s = hcfg.struct()
+    rc = lib().oracle_attentive_head(ctypes.byref(s), seed, int(bf16_weights), tokens.ctypes.data, B, N,
+                                     pooled.ctypes.data, logits.ctypes.data)
+    if rc != 0:
+        raise ValueError(f"oracle_attentive_head refused the configuration (code {rc})")
+    return pooled, logits
+
+
+def pool(tokens, prefix: int, mode: int) -> np.ndarray:
+    """tokens [B, N, D] -> [B, D]: mode 0 mean of the patch tokens, mode 1 the CLS row."""
+    tokens = _f64(tokens)
+    B, N, D = tokens.shape
+    out = np.empty((B, D), dtype=np.float64)
+    if lib().oracle_pool(tokens.ctypes.data, B, N, D, prefix, mode, out.ctypes.data) != 0:
+        raise ValueError("oracle_pool refused the arguments")
     return out
 
 

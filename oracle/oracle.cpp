@@ -681,4 +681,113 @@ int oracle_predict(const oracle_pred_hparams* hp, uint64_t seed, int bf16_weight
   return 0;
 }
 
+void oracle_cross_attention(const double* q, int Nq, const double* k, const double* v, int Nk, int n_head, int hd,
+                            double* o) {
+  const int D = n_head * hd;
+  const double scale = 1.0 / std::sqrt((double)hd);
+#pragma omp parallel for collapse(2) schedule(static)
+  for (int h = 0; h < n_head; ++h)
+    for (int i = 0; i < Nq; ++i) {
+      std::vector<double> s(Nk);
+      const double* qi = q + (size_t)i * D + (size_t)h * hd;
+      double mx = -INFINITY;
+      for (int j = 0; j < Nk; ++j) {
+        const double* kj = k + (size_t)j * D + (size_t)h * hd;
+        double acc = 0.0;
+        for (int c = 0; c < hd; ++c) acc += qi[c] * kj[c];
+        s[j] = acc * scale;
+        mx = std::max(mx, s[j]);
+      }
+      double sum = 0.0;
+      for (int j = 0; j < Nk; ++j) {
+        s[j] = std::exp(s[j] - mx);
+        sum += s[j];
+      }
+      double* oi = o + (size_t)i * D + (size_t)h * hd;
+      for (int c = 0; c < hd; ++c) oi[c] = 0.0;
+      for (int j = 0; j < Nk; ++j) {
+        const double p = s[j] / sum;
+        const double* vj = v + (size_t)j * D + (size_t)h * hd;
+        for (int c = 0; c < hd; ++c) oi[c] += p * vj[c];
+      }
+    }
+}
+
+// [S] "Head": head.blk.{i} (encoder block layout, run first), head.query [1, D], head.xattn.ln_kv
+// (keys / values only), head.xattn.q / k / v with bias (no output projection), head.xattn.ln2,
+// head.xattn.ffn_up / ffn_down, head.cls [n_classes, D] (no final norm). [K] attentive pooler:
+// pre-norm self-attention layers without RoPE or mask over the whole token stream, then the
+// learned query's cross attention, query residual + MLP; the classifier on the pooled token.
+int oracle_attentive_head(const oracle_head_hparams* hp, uint64_t seed, int bf16_weights, const double* tokens, int B,
+                          int N, double* pooled, double* logits) {
+  if (!hp || B <= 0 || N <= 0 || hp->n_head <= 0 || hp->embed_dim % hp->n_head || hp->n_pool_layers < 0 ||
+      hp->n_classes <= 0)
+    return -1;
+  const int D = hp->embed_dim, F = hp->ffn_dim, NH = hp->n_head, C = hp->n_classes;
+  const int hd = D / NH;
+  const size_t MD = (size_t)N * D;
+  std::vector<double> X(tokens, tokens + (size_t)B * MD);
+  BlockScratch sc(N, D, F);
+  for (int l = 0; l < hp->n_pool_layers; ++l) {
+    BlockW w;
+    w.gen(seed, "head.blk." + std::to_string(l) + ".", bf16_weights, D, F);
+    for (int b = 0; b < B; ++b)
+      block_forward(w, X.data() + (size_t)b * MD, N, D, NH, F, hp->ln_eps, nullptr, nullptr, 0, 0, 1, sc);
+  }
+  std::vector<double> query, lkw, lkb, wq, bq, wk, bk, wv, bv, l2w, l2b, wup, bup, wdn, bdn, wc, bc;
+  gen_param(seed, "head.query", bf16_weights, D, query);
+  gen_param(seed, "head.xattn.ln_kv.weight", bf16_weights, D, lkw);
+  gen_param(seed, "head.xattn.ln_kv.bias", bf16_weights, D, lkb);
+  gen_param(seed, "head.xattn.q.weight", bf16_weights, (size_t)D * D, wq);
+  gen_param(seed, "head.xattn.q.bias", bf16_weights, D, bq);
+  gen_param(seed, "head.xattn.k.weight", bf16_weights, (size_t)D * D, wk);
+  gen_param(seed, "head.xattn.k.bias", bf16_weights, D, bk);
+  gen_param(seed, "head.xattn.v.weight", bf16_weights, (size_t)D * D, wv);
+  gen_param(seed, "head.xattn.v.bias", bf16_weights, D, bv);
+  gen_param(seed, "head.xattn.ln2.weight", bf16_weights, D, l2w);
+  gen_param(seed, "head.xattn.ln2.bias", bf16_weights, D, l2b);
+  gen_param(seed, "head.xattn.ffn_up.weight", bf16_weights, (size_t)F * D, wup);
+  gen_param(seed, "head.xattn.ffn_up.bias", bf16_weights, F, bup);
+  gen_param(seed, "head.xattn.ffn_down.weight", bf16_weights, (size_t)D * F, wdn);
+  gen_param(seed, "head.xattn.ffn_down.bias", bf16_weights, D, bdn);
+  gen_param(seed, "head.cls.weight", bf16_weights, (size_t)C * D, wc);
+  gen_param(seed, "head.cls.bias", bf16_weights, C, bc);
+  std::vector<double> q(D), kv(MD), k(MD), v(MD), o(D), x(D), h(D), u(F), t(D);
+  oracle_linear(query.data(), 1, D, wq.data(), bq.data(), D, q.data());  // the raw query token, no LN
+  for (int b = 0; b < B; ++b) {
+    oracle_layernorm(X.data() + (size_t)b * MD, N, D, lkw.data(), lkb.data(), hp->ln_eps, kv.data());
+    oracle_linear(kv.data(), N, D, wk.data(), bk.data(), D, k.data());
+    oracle_linear(kv.data(), N, D, wv.data(), bv.data(), D, v.data());
+    oracle_cross_attention(q.data(), 1, k.data(), v.data(), N, NH, hd, o.data());
+    for (int c = 0; c < D; ++c) x[c] = query[c] + o[c];  // no output projection; the query is the residual
+    oracle_layernorm(x.data(), 1, D, l2w.data(), l2b.data(), hp->ln_eps, h.data());
+    oracle_linear(h.data(), 1, D, wup.data(), bup.data(), F, u.data());
+    oracle_gelu(u.data(), F, u.data());
+    oracle_linear(u.data(), 1, F, wdn.data(), bdn.data(), D, t.data());
+    for (int c = 0; c < D; ++c) x[c] += t[c];
+    if (pooled) std::memcpy(pooled + (size_t)b * D, x.data(), D * sizeof(double));
+    if (logits) oracle_linear(x.data(), 1, D, wc.data(), bc.data(), C, logits + (size_t)b * C);
+  }
+  return 0;
+}
+
+int oracle_pool(const double* tokens, int B, int N, int D, int prefix, int mode, double* out) {
+  if (B <= 0 || N <= 0 || D <= 0 || prefix < 0 || prefix >= N) return -1;
+  if (mode == 1 && prefix < 1) return -1;
+  if (mode != 0 && mode != 1) return -1;
+  for (int b = 0; b < B; ++b) {
+    const double* t = tokens + (size_t)b * N * D;
+    double* o = out + (size_t)b * D;
+    if (mode == 1) {
+      std::memcpy(o, t, D * sizeof(double));
+      continue;
+    }
+    for (int c = 0; c < D; ++c) o[c] = 0.0;
+    for (int n = prefix; n < N; ++n)
+      for (int c = 0; c < D; ++c) o[c] += t[(size_t)n * D + c];
+    for (int c = 0; c < D; ++c) o[c] /= (double)(N - prefix);
+  }
+  return 0;
+}
+
 }  // extern "C"

@@ -154,6 +154,34 @@ int oracle_predict(const oracle_pred_hparams* hp, uint64_t seed, int bf16_weight
                    int n_enc, const int* ctx_ids, int n_ctx, const int* tgt_ids, int n_tgt, int gh, int gw,
                    double* out);
 
+/* Attention of Nq query rows over Nk key / value rows per head, o = softmax(q k^T / sqrt(hd)) v
+ * (no mask): q [Nq, H*hd], k, v [Nk, H*hd], o [Nq, H*hd], heads contiguous. */
+void oracle_cross_attention(const double* q, int Nq, const double* k, const double* v, int Nk, int n_head, int hd,
+                            double* o);
+
+/* Attentive-pool head hyper-parameters (jepa.head.* of [S] "Head"). */
+typedef struct {
+  int embed_dim, n_head, ffn_dim, n_pool_layers, n_classes;
+  double ln_eps;
+} oracle_head_hparams;
+
+/* The attentive-pool head and classifier ([S] "Head" tensor table; [K] V-JEPA 2 section, the
+ * attentive pooler and the classifier): n_pool_layers pre-LN self-attention blocks over all
+ * tokens (the encoder block's layout, head.blk.*, no RoPE, no mask), then one learned query
+ * (head.query) attends to the tokens: keys and values are projected (head.xattn.k / .v) from
+ * the tokens after head.xattn.ln_kv, the query (head.xattn.q) from the raw query token, there is
+ * no output projection, and the query is the residual: x = query + attn; x += down(GELU(up(
+ * ln2(x)))) (head.xattn.ffn_*). pooled = x; logits = x head.cls^T + bias (no final norm).
+ * tokens [B, N, D]; pooled [B, D] and logits [B, n_classes] (either may be NULL). */
+int oracle_attentive_head(const oracle_head_hparams* hp, uint64_t seed, int bf16_weights, const double* tokens, int B,
+                          int N, double* pooled, double* logits);
+
+/* Pooled features of [B, N, D] tokens whose first `prefix` rows are prefix (CLS) tokens:
+ * mode 0 = the mean of the N - prefix patch tokens ([S] ijepa note: the feature is the mean of
+ * the patch tokens), mode 1 = row 0, the CLS token ([C] hfvit / levjepa: the CLS token).
+ * out [B, D]. Returns -1 on a bad size or mode (mode 1 needs prefix >= 1). */
+int oracle_pool(const double* tokens, int B, int N, int D, int prefix, int mode, double* out);
+
 /* Number of OpenMP threads the oracle uses. */
 int oracle_num_threads(void);
 
