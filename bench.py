@@ -7,7 +7,10 @@ weights and pixels. A step is one jepa_encode of the batch (patchify, patch GEMM
 final norm) on inputs resident in HBM. The line also carries the same clip at batch 1 ("batch1"),
 timed the same way.
 
---workload vjepa2_vitl16_predictor times the V-JEPA 2 masked predictor instead (12 layers of
+--workload vjepa2_vitl16_ssv2_head times the V-JEPA 2 SSv2 attentive-pool head + 174-way classifier
+over the 2048 encoder tokens of each clip (3 pooler layers, the cross attention of one query,
+the MLP and the classifier), eight clips per step. --workload vjepa2_vitl16_predictor times the
+V-JEPA 2 masked predictor instead (12 layers of
 width 384 over the 2048 tokens of each clip: the first 1024 as context, the last 1024 as
 targets, the split of the pages' predictor example), eight clips per step, on encoder tokens
 resident in HBM. --workload also picks one of the fixed-table families: V-JEPA ViT-L/16 16 x 256 x 256 clips
@@ -52,6 +55,8 @@ BENCH_WORKLOADS = {
                                    "resized bicubic)"),
 }
 PREDICTOR = "vjepa2_vitl16_predictor"
+HEADW = "vjepa2_vitl16_ssv2_head"
+HEAD_METRIC = "attentive-pool head tokens/s and TFLOP/s, V-JEPA 2 ViT-L SSv2 classifier head over 16×256² clips"
 PRED_METRIC = "masked predictor tokens/s and TFLOP/s, V-JEPA 2 ViT-L predictor over 16×256² clips"
 HEADLINE = "vjepa2_vitl16_16x256"
 FLUSH_BYTES = 256 << 20  # > 129 MB of L2
@@ -75,7 +80,7 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=50)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--batch", type=int, default=None, help="clips per GPU per step (default: the workload's)")
-    p.add_argument("--workload", choices=sorted(BENCH_WORKLOADS) + [PREDICTOR], default=HEADLINE)
+    p.add_argument("--workload", choices=sorted(BENCH_WORKLOADS) + [PREDICTOR, HEADW], default=HEADLINE)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true")
     return p.parse_args(argv)
@@ -235,36 +240,64 @@ def pred_cpu_baseline():
                       f"({t1:.2f} s, {t2:.2f} s); full-depth time {full:.1f} s extrapolated linearly per layer"}
 
 
-def run_reference_predictor(args):
+def head_inputs(B, seed=0):
+    """Encoder tokens N(0, 1) from the shared generator for the head workload."""
+    import synth
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from configs import HEAD_VJEPA2_L16_SSV2, HEAD_WORKLOAD
+    N = HEAD_WORKLOAD["tokens"]
+    return synth.fill(seed, "input.enc_tokens", synth.NORMAL, 0.0, 1.0, (B, N, HEAD_VJEPA2_L16_SSV2.embed_dim)), \
+        HEAD_VJEPA2_L16_SSV2
+
+
+def head_oracle_layer_times():
+    """The oracle head on one clip's tokens with 1 and 2 pooler layers: (t1, t2, tokens, threads, L)."""
+    from dataclasses import replace
+    import oracle
+    tok, cfg = head_inputs(1)
+    times = []
+    for nl in (1, 2):
+        t0 = time.perf_counter()
+        oracle.attentive_head(replace(cfg, n_pool_layers=nl), 0, True, tok)
+        times.append(time.perf_counter() - t0)
+    return times[0], times[1], tok.shape[1], oracle.num_threads(), cfg.n_pool_layers
+
+
+def head_cpu_baseline():
+    t1, t2, N, threads, L = head_oracle_layer_times()
+    full = t1 + (L - 1) * max(t2 - t1, 1e-9)
+    return {"value": N / full, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"fp64 oracle head on one clip's {N} tokens with 1 and 2 of the {L} pooler layers "
+                      f"({t1:.2f} s, {t2:.2f} s); full-depth time {full:.1f} s extrapolated linearly per layer"}
+
+
+def run_reference_layers(args, times, one_layer, metric, label):
+    """The reference arm of a head-side workload: the oracle with one layer per step, the other
+    layers added at the per-layer time calibrated from the 1- and 2-layer runs."""
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
-    from dataclasses import replace
-    import oracle
-    enc, ctx, tgt, grid, cfg = pred_inputs(1)
-    t1, t2, N, threads, L = pred_oracle_layer_times()
+    t1, t2, N, threads, L = times
     per_layer = max(t2 - t1, 1e-9)
-    one = replace(cfg, n_layer=1)
     for _ in range(args.warmup):
-        oracle.predict(one, 0, True, enc, ctx, tgt, grid[1:])
+        one_layer()
     full_times = []
     t_start = time.perf_counter()
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        oracle.predict(one, 0, True, enc, ctx, tgt, grid[1:])
+        one_layer()
         full_times.append((time.perf_counter() - t0) + (L - 1) * per_layer)
     wall = time.perf_counter() - t_start
     mean_full = statistics.mean(full_times)
     value = N / mean_full
     B = args.batch or 8
-    sample = (f"each step: the fp64 oracle predictor on one clip's {N} tokens with 1 of the {L} layers; the other "
-              f"{L - 1} layers added at the calibrated per-layer time {per_layer:.2f} s; the {B} clips of a step are "
+    sample = (f"each step: the fp64 oracle on one clip's {N} tokens with 1 of the {L} layers; the other {L - 1} "
+              f"layers added at the calibrated per-layer time {per_layer:.2f} s; the {B} clips of a step are "
               f"independent, so a step costs {B} such clips")
-    line = {"impl": "reference", "metric": PRED_METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+    line = {"impl": "reference", "metric": metric, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * mean_full * B, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": f"V-JEPA 2 ViT-L masked predictor, {N} tokens per clip (1024 context + 1024 "
-                                   f"targets) x {B} per GPU", "tokens_per_step": B * N, "global_batch": B,
+            "config": {"workload": f"{label} x {B} per GPU", "tokens_per_step": B * N, "global_batch": B,
                        "seq_len": N, "wall_s_sampled_steps": wall},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -272,8 +305,44 @@ def run_reference_predictor(args):
     return 0
 
 
-def run_predictor(args):
-    """The masked predictor: one step = one jepa_predict of B clips' tokens (graph replay)."""
+def run_reference_predictor(args):
+    from dataclasses import replace
+    import oracle
+    enc, ctx, tgt, grid, cfg = pred_inputs(1)
+    one = replace(cfg, n_layer=1)
+    return run_reference_layers(args, pred_oracle_layer_times(),
+                                lambda: oracle.predict(one, 0, True, enc, ctx, tgt, grid[1:]), PRED_METRIC,
+                                f"V-JEPA 2 ViT-L masked predictor, {ctx.shape[1] + tgt.shape[1]} tokens per clip "
+                                f"({ctx.shape[1]} context + {tgt.shape[1]} targets)")
+
+
+def run_reference_head(args):
+    from dataclasses import replace
+    import oracle
+    tok, cfg = head_inputs(1)
+    one = replace(cfg, n_pool_layers=1)
+    return run_reference_layers(args, head_oracle_layer_times(), lambda: oracle.attentive_head(one, 0, True, tok),
+                                HEAD_METRIC, f"V-JEPA 2 ViT-L SSv2 attentive-pool head + classifier, {tok.shape[1]} "
+                                             f"tokens per clip")
+
+
+class SeqBench:
+    """What run_sequence needs of a head-side workload (predictor, attentive-pool head)."""
+    metric = label = ""
+    tokens_per_step = launches = h2d_bytes = d2h_bytes = 0
+    stream = None
+
+    def step(self):               # one step on inputs resident in HBM, issued on self.stream
+        raise NotImplementedError
+
+    def e2e_step(self):           # host inputs in, host results out, synchronous
+        raise NotImplementedError
+
+
+def run_sequence(args, wl, make):
+    """Time a head-side workload the way run_ours times the encoder: W warm-up steps, K steps of
+    graph replay bracketed by CUDA events (L2 flushed between steps), then K eager steps with the
+    context's per-kernel events (roofline and kernel table), then K' end-to-end steps."""
     import torch
     import torch.distributed as dist
 
@@ -285,23 +354,17 @@ def run_predictor(args):
     torch.cuda.set_device(local)
     import jepa_vision_encoder_gb300 as jv
 
-    B = args.batch or 8
-    enc_h, ctx_h, tgt_h, grid, cfg = pred_inputs(B, seed=rank)
-    pred = jv.Predictor.preset("vjepa2_vitl16", seed=0, device=local)
-    n_ctx, n_tgt = ctx_h.shape[1], tgt_h.shape[1]
-    N = n_ctx + n_tgt
-    pc = jv.PredContext(pred, B, n_ctx, n_tgt)
-    enc, ctx, tgt = (torch.from_numpy(a).cuda() for a in (enc_h, ctx_h, tgt_h))
-    out = torch.empty((B, n_tgt, cfg.out_dim), dtype=torch.float32, device="cuda")
+    B = args.batch or wl["batch"]
+    w = make(jv, B, rank, local)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
-    stream = pc.stream
+    stream = w.stream
     peaks = measured_peaks()
     with torch.cuda.stream(stream):
-        pc.set_graph(True)
+        w.ctx.set_graph(True)
         for _ in range(args.warmup):
             flush.zero_()
-            pc.predict(enc, ctx, tgt, grid, out)
-        pc.sync()
+            w.step()
+        w.ctx.sync()
         starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
         ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
         torch.cuda.synchronize()
@@ -311,30 +374,29 @@ def run_predictor(args):
             for i in range(args.steps):
                 flush.zero_()
                 starts[i].record(stream)
-                pc.predict(enc, ctx, tgt, grid, out)
+                w.step()
                 ends[i].record(stream)
             torch.cuda.synchronize()
         barrier(local)
         torch.cuda.synchronize()
-        pc.sync()
+        w.ctx.sync()
         step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
-        # per-kernel durations: eager launches with events around each kernel
-        pc.set_profiling(True)
+        w.ctx.set_profiling(True)
         for _ in range(2):
-            pc.predict(enc, ctx, tgt, grid, out)
-        pc.profile(reset=True)
+            w.step()
+        w.ctx.profile(reset=True)
         p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         p0.record(stream)
         for _ in range(args.steps):
             flush.zero_()
-            pc.predict(enc, ctx, tgt, grid, out)
+            w.step()
         p1.record(stream)
         torch.cuda.synchronize()
-        prof = pc.profile(reset=True)
-        pc.set_profiling(False)
+        prof = w.ctx.profile(reset=True)
+        w.ctx.set_profiling(False)
     total_ms = reduce_max(sum(step_ms), device="cuda" if world > 1 else None)
     ms_per_step = total_ms / args.steps
-    tokens_per_step = world * B * N
+    tokens_per_step = world * w.tokens_per_step
     value = tokens_per_step * args.steps / (total_ms / 1e3)
     flops_per_step = sum(v["flops"] for v in prof.values()) / args.steps
     tflops = world * flops_per_step * args.steps / (total_ms / 1e3) / 1e12
@@ -357,47 +419,104 @@ def run_predictor(args):
                    **({"tflops": v["flops"] / (v["total_ms"] / 1e3) / 1e12} if v["flops"] else {}),
                    **({"gbs": v["bytes"] / (v["total_ms"] / 1e3) / 1e9} if v["bytes"] else {})}
                for k, v in prof.items()}
-    # end to end: encoder tokens and ids from pinned host memory, predictions back, every step
-    pin = [torch.from_numpy(a).pin_memory() for a in (enc_h, ctx_h, tgt_h)]
-    pin_out = torch.empty((B, n_tgt, cfg.out_dim), dtype=torch.float32).pin_memory()
     e2e_steps = min(args.steps, 20)
-
-    def e2e_step():
-        with torch.cuda.stream(stream):
-            enc.copy_(pin[0], non_blocking=True)
-            ctx.copy_(pin[1], non_blocking=True)
-            tgt.copy_(pin[2], non_blocking=True)
-            pc.predict(enc, ctx, tgt, grid, out)
-            pin_out.copy_(out, non_blocking=True)
-        pc.sync()
-    e2e_step()
+    w.e2e_step()
     barrier(local)
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
-        e2e_step()
+        w.e2e_step()
     e2e_s = reduce_max(time.perf_counter() - t0, device="cuda" if world > 1 else None)
-    e2e = {"value": tokens_per_step * e2e_steps / e2e_s, "unit": "tokens/s",
-           "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in pin),
-           "d2h_bytes_per_step": pin_out.numel() * 4}
+    e2e = {"value": tokens_per_step * e2e_steps / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": w.h2d_bytes,
+           "d2h_bytes_per_step": w.d2h_bytes}
     if rank == 0:
-        line = {"metric": PRED_METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        line = {"metric": w.metric, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-                "config": {"workload": f"V-JEPA 2 ViT-L masked predictor, {N} tokens per clip ({n_ctx} context + "
-                                       f"{n_tgt} targets) x {B} per GPU", "tokens_per_step": tokens_per_step,
-                           "global_batch": world * B, "seq_len": N,
-                           "parallelism": f"replicas x{world} (independent clips, no collective)",
+                "config": {"workload": w.label, "tokens_per_step": tokens_per_step, "global_batch": world * B,
+                           "seq_len": w.seq_len, "parallelism": f"replicas x{world} (independent clips, no collective)",
                            "l2": "flushed (256 MiB write) between steps", "weights": "seeded synthetic"},
                 "tflops": tflops, "frac_of_bf16_peak": tflops / (world * peaks["bf16_tflops"]),
-                "launch_mode": "CUDA graph replay of the predictor", "roofline": roof, "kernels": kernels,
-                "e2e": e2e, "gpu_launches": pc.launches(n_ctx) * args.steps,
-                "clocks": clk.summary(), "profiled_pass": {"ms_per_step": p0.elapsed_time(p1) / args.steps}}
+                "launch_mode": "CUDA graph replay", "roofline": roof, "kernels": kernels, "e2e": e2e,
+                "gpu_launches": w.launches * args.steps, "clocks": clk.summary(),
+                "profiled_pass": {"ms_per_step": p0.elapsed_time(p1) / args.steps}}
         if world == 1 and not args.no_cpu_baseline:
-            line["cpu_baseline"] = pred_cpu_baseline()
+            line["cpu_baseline"] = w.cpu_baseline()
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def make_predictor(jv, B, rank, local):
+    """The V-JEPA 2 masked predictor over B clips' tokens (the pages' half / half split)."""
+    import torch
+    enc_h, ctx_h, tgt_h, grid, cfg = pred_inputs(B, seed=rank)
+    w = SeqBench()
+    pred = jv.Predictor.preset("vjepa2_vitl16", seed=0, device=local)
+    n_ctx, n_tgt = ctx_h.shape[1], tgt_h.shape[1]
+    w.ctx = jv.PredContext(pred, B, n_ctx, n_tgt)
+    w.stream = w.ctx.stream
+    enc, ctx, tgt = (torch.from_numpy(a).cuda() for a in (enc_h, ctx_h, tgt_h))
+    out = torch.empty((B, n_tgt, cfg.out_dim), dtype=torch.float32, device="cuda")
+    pin = [torch.from_numpy(a).pin_memory() for a in (enc_h, ctx_h, tgt_h)]
+    pin_out = torch.empty((B, n_tgt, cfg.out_dim), dtype=torch.float32).pin_memory()
+    w.step = lambda: w.ctx.predict(enc, ctx, tgt, grid, out)
+
+    def e2e_step():
+        with torch.cuda.stream(w.stream):
+            enc.copy_(pin[0], non_blocking=True)
+            ctx.copy_(pin[1], non_blocking=True)
+            tgt.copy_(pin[2], non_blocking=True)
+            w.ctx.predict(enc, ctx, tgt, grid, out)
+            pin_out.copy_(out, non_blocking=True)
+        w.ctx.sync()
+    w.e2e_step = e2e_step
+    w.h2d_bytes = sum(t.numel() * t.element_size() for t in pin)
+    w.d2h_bytes = pin_out.numel() * 4
+    w.seq_len = n_ctx + n_tgt
+    w.tokens_per_step = B * w.seq_len
+    w.launches = w.ctx.launches(n_ctx)
+    w.metric = PRED_METRIC
+    w.label = (f"V-JEPA 2 ViT-L masked predictor, {w.seq_len} tokens per clip ({n_ctx} context + {n_tgt} targets) "
+               f"x {B} per GPU")
+    w.cpu_baseline = pred_cpu_baseline
+    w.keep = (pred, enc, ctx, tgt, out, pin, pin_out)
+    return w
+
+
+def make_head(jv, B, rank, local):
+    """The V-JEPA 2 ViT-L SSv2 attentive-pool head + classifier over B clips' encoder tokens."""
+    import torch
+    tok_h, cfg = head_inputs(B, seed=rank)
+    w = SeqBench()
+    head = jv.Head.preset("vjepa2_vitl16_ssv2", seed=0, device=local)
+    N = tok_h.shape[1]
+    w.ctx = jv.HeadContext(head, B, N)
+    w.stream = w.ctx.stream
+    tok = torch.from_numpy(tok_h).cuda()
+    pooled = torch.empty((B, cfg.embed_dim), dtype=torch.float32, device="cuda")
+    logits = torch.empty((B, cfg.n_classes), dtype=torch.float32, device="cuda")
+    pin = torch.from_numpy(tok_h).pin_memory()
+    pin_logits = torch.empty((B, cfg.n_classes), dtype=torch.float32).pin_memory()
+    w.step = lambda: w.ctx.forward(tok, pooled, logits)
+
+    def e2e_step():
+        with torch.cuda.stream(w.stream):
+            tok.copy_(pin, non_blocking=True)
+            w.ctx.forward(tok, pooled, logits)
+            pin_logits.copy_(logits, non_blocking=True)
+        w.ctx.sync()
+    w.e2e_step = e2e_step
+    w.h2d_bytes = pin.numel() * 4
+    w.d2h_bytes = pin_logits.numel() * 4
+    w.seq_len = N
+    w.tokens_per_step = B * N
+    w.launches = w.ctx.launches(True)
+    w.metric = HEAD_METRIC
+    w.label = f"V-JEPA 2 ViT-L SSv2 attentive-pool head + 174-way classifier, {N} tokens per clip x {B} per GPU"
+    w.cpu_baseline = head_cpu_baseline
+    w.keep = (head, tok, pooled, logits, pin, pin_logits)
+    return w
 
 
 def run_reference(args):
@@ -406,6 +525,8 @@ def run_reference(args):
         return 0
     if args.workload == PREDICTOR:
         return run_reference_predictor(args)
+    if args.workload == HEADW:
+        return run_reference_head(args)
     import oracle
     from dataclasses import replace
     import synth
@@ -703,7 +824,9 @@ def main(argv=None):
     if args.impl == "reference":
         return run_reference(args)
     if args.workload == PREDICTOR:
-        return run_predictor(args)
+        return run_sequence(args, {"batch": 8}, make_predictor)
+    if args.workload == HEADW:
+        return run_sequence(args, {"batch": 8}, make_head)
     return run_ours(args)
 
 

@@ -397,6 +397,64 @@ jepa_status jepa_predict(jepa_pred_context* c, const float* d_enc, int32_t B, in
  * bounded wait gave up (the word is cleared). */
 jepa_status jepa_pred_context_sync(jepa_pred_context* c);
 
+/* ------------------------------------------------------------------ attentive-pool head, pooling
+ *
+ * The attentive-pool head and classifier of the V-JEPA 2 video classifiers ("GGUF schema (v1)",
+ * Head: head.* tensors; the SkyVision V-JEPA 2 notes, attentive pooler and classifier):
+ * n_pool_layers pre-LN self-attention blocks of the encoder's layout (head.blk.*, no RoPE, no mask)
+ * over all tokens, then one learned query (head.query) attends to the tokens: keys and values
+ * are projected from the tokens after head.xattn.ln_kv, the query from the raw query token, there
+ * is no output projection and the query is the residual (x = query + attn); then
+ * x += ffn_down(GELU(ffn_up(ln2(x)))). pooled = x (the head's embedding); logits = x head.cls^T
+ * + bias, with no final norm. */
+typedef struct jepa_head jepa_head;
+typedef struct jepa_head_context jepa_head_context;
+
+/* jepa.head.* hyper-parameters; head_dim = embed_dim / n_head is 32, 64 or 128 (64 when
+ * n_pool_layers > 0). */
+typedef struct {
+  int32_t embed_dim, n_head, ffn_dim, n_pool_layers, n_classes;
+  float ln_eps;
+} jepa_head_hparams;
+
+/* "vjepa2_vitl16_ssv2": the V-JEPA 2 ViT-L SSv2 classifier head (1024 wide, 16 heads, ffn 4096,
+ * 3 pooler layers, 174 classes). Unknown name -> JEPA_E_INVALID_ARG. */
+jepa_status jepa_head_preset(const char* name, jepa_head_hparams* out);
+jepa_status jepa_head_hparams_validate(const jepa_head_hparams* hp);
+/* Synthesise every head.* tensor (the enc.* recipe) and upload it to `device`; bf16 only. */
+jepa_status jepa_head_load(const jepa_head_hparams* hp, uint64_t seed, int32_t dtype, int32_t device, jepa_head** out);
+void jepa_head_free(jepa_head* h);
+jepa_status jepa_head_tensor(const jepa_head* h, const char* name, float* h_dst, size_t n_elems);
+
+/* Workspace for up to max_batch items of max_tokens tokens (at most 32768; budget 0 = 8 GiB). */
+jepa_status jepa_head_context_new(const jepa_head* h, int32_t max_batch, int32_t max_tokens, size_t max_workspace_bytes,
+                                  jepa_head_context** out);
+void jepa_head_context_free(jepa_head_context* c);
+jepa_status jepa_head_context_set_stream(jepa_head_context* c, void* stream);
+jepa_status jepa_head_context_set_graph(jepa_head_context* c, int32_t enable);
+jepa_status jepa_head_context_set_profiling(jepa_head_context* c, int32_t enable);
+jepa_status jepa_head_context_profile(jepa_head_context* c, jepa_kernel_stat* out, int32_t max, int32_t* n_out,
+                                      int32_t reset);
+/* Kernel launches of one jepa_head_forward (with_logits != 0: the classifier too). */
+jepa_status jepa_head_context_launches(const jepa_head_context* c, int32_t with_logits, int32_t* n_out);
+
+/* Run the head on B items of N encoder tokens, asynchronously on the context stream.
+ *  d_tokens: device float [B, N, embed_dim] (the encoder's output; read only), 16-byte aligned
+ *  d_pooled: device float [B, embed_dim] or NULL;  d_logits: device float [B, n_classes] or NULL
+ *  (at least one of the two). */
+jepa_status jepa_head_forward(jepa_head_context* c, const float* d_tokens, int32_t B, int32_t N, float* d_pooled,
+                              float* d_logits);
+/* Wait for the context stream; JEPA_E_TIMEOUT if a bounded wait gave up. */
+jepa_status jepa_head_context_sync(jepa_head_context* c);
+
+/* Pooled features of encoder tokens: JEPA_POOL_MEAN = the mean of the patch tokens, rows
+ * [prefix, N) ("GGUF schema (v1)", ijepa note: the feature is the mean of the patch tokens);
+ * JEPA_POOL_CLS = row 0, the CLS token (hfvit / levjepa; needs prefix >= 1).
+ * d_tokens: device float [B, N, D], d_out: device float [B, D], both 16-byte aligned, D % 4 == 0. */
+typedef enum { JEPA_POOL_MEAN = 0, JEPA_POOL_CLS = 1 } jepa_pool_mode;
+jepa_status jepa_op_pool(int32_t mode, const float* d_tokens, int32_t B, int32_t N, int32_t D, int32_t prefix,
+                         float* d_out, void* stream);
+
 const char* jepa_error_text(void);
 void jepa_error_reset(void);
 

@@ -17,10 +17,11 @@ from . import _lib
 from ._lib import (ATTN_BLOCK_CAUSAL, ATTN_FULL, BF16, EPI_BIAS, EPI_BIAS_GELU, EPI_BIAS_RESIDUAL,
                    EPI_PATCH_EMBED, EPI_QKV_ROPE, FP32, LAYOUT_CTHW, LAYOUT_TCHW, POS_LEARNED, POS_NONE,
                    POS_ROPE3D, POS_SINCOS2D, POS_SINCOS3D, RESIZE_BICUBIC, RESIZE_TRILINEAR, ROPE_INTERLEAVED,
-                   ROPE_TILED, Epilogue, HParams, JepaError, PredHParams, check, lib)
+                   ROPE_TILED, POOL_CLS, POOL_MEAN, Epilogue, HeadHParams, HParams, JepaError, PredHParams, check,
+                   lib)
 
 __all__ = ["Model", "Context", "HParams", "JepaError", "preset", "hparams", "n_tokens", "ops", "lib", "Predictor",
-           "PredContext", "PredHParams", "pred_preset"]
+           "PredContext", "PredHParams", "pred_preset", "Head", "HeadContext", "HeadHParams", "head_preset"]
 
 PRESETS = ("hfvit_ti14", "vjepa2_vitl16", "vjepa2_1_vitl16", "levjepa_vitl16", "vjepa2_vitg16", "vjepa_vitl16",
            "ijepa_vitl16")
@@ -334,6 +335,117 @@ class PredContext:
             pass
 
 
+def head_preset(name: str) -> HeadHParams:
+    hp = HeadHParams()
+    check(lib().jepa_head_preset(name.encode(), ctypes.byref(hp)))
+    return hp
+
+
+class Head:
+    """Synthetic-weight attentive-pool head + classifier (head.* tensors) on one GPU, bf16."""
+
+    def __init__(self, hp: HeadHParams, seed: int = 0, dtype="bf16", device: int = 0):
+        self.hp = hp
+        self.seed = seed
+        self.device = device
+        h = ctypes.c_void_p()
+        check(lib().jepa_head_load(ctypes.byref(hp), seed, _dtype_code(dtype), device, ctypes.byref(h)))
+        self._h = h
+
+    @classmethod
+    def preset(cls, name: str, seed: int = 0, dtype="bf16", device: int = 0, **overrides):
+        hp = head_preset(name)
+        for k, v in overrides.items():
+            setattr(hp, k, v)
+        return cls(hp, seed=seed, dtype=dtype, device=device)
+
+    def tensor(self, name: str, shape) -> torch.Tensor:
+        """A head.* tensor copied to host memory as float32."""
+        n = 1
+        for s in shape:
+            n *= s
+        out = torch.empty(n, dtype=torch.float32)
+        check(lib().jepa_head_tensor(self._h, name.encode(), ctypes.c_void_p(out.data_ptr()), n))
+        return out.reshape(shape)
+
+    def close(self):
+        if getattr(self, "_h", None):
+            lib().jepa_head_free(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class HeadContext:
+    """Workspace for up to max_batch items of max_tokens tokens; streams as Context."""
+
+    def __init__(self, head: Head, max_batch: int, max_tokens: int, max_workspace_bytes: int = 0, stream=None,
+                 graph: bool = False):
+        self.head = head
+        h = ctypes.c_void_p()
+        check(lib().jepa_head_context_new(head._h, max_batch, max_tokens, max_workspace_bytes, ctypes.byref(h)))
+        self._h = h
+        self._own = stream is None
+        self.stream = torch.cuda.Stream(device=head.device) if stream is None else stream
+        check(lib().jepa_head_context_set_stream(self._h, ctypes.c_void_p(self.stream.cuda_stream)))
+        if graph:
+            check(lib().jepa_head_context_set_graph(self._h, 1))
+
+    def set_graph(self, enable: bool):
+        check(lib().jepa_head_context_set_graph(self._h, int(enable)))
+
+    def set_profiling(self, enable: bool):
+        check(lib().jepa_head_context_set_profiling(self._h, int(enable)))
+
+    def launches(self, with_logits: bool = True) -> int:
+        n = ctypes.c_int32()
+        check(lib().jepa_head_context_launches(self._h, int(with_logits), ctypes.byref(n)))
+        return n.value
+
+    def forward(self, tokens: torch.Tensor, pooled: torch.Tensor = None, logits: torch.Tensor = None,
+                want_pooled: bool = True, want_logits: bool = True):
+        """tokens: float32 CUDA [B, N, D] -> (pooled [B, D], logits [B, n_classes])."""
+        assert tokens.is_cuda and tokens.dtype == torch.float32 and tokens.is_contiguous()
+        B, N, D = tokens.shape
+        if pooled is None and want_pooled:
+            pooled = torch.empty((B, D), dtype=torch.float32, device=tokens.device)
+        if logits is None and want_logits:
+            logits = torch.empty((B, self.head.hp.n_classes), dtype=torch.float32, device=tokens.device)
+        if self._own:
+            self.stream.wait_stream(torch.cuda.current_stream(self.stream.device))
+        check(lib().jepa_head_forward(self._h, _ptr(tokens), B, N,
+                                      ctypes.c_void_p(pooled.data_ptr() if pooled is not None else 0),
+                                      ctypes.c_void_p(logits.data_ptr() if logits is not None else 0)))
+        if self._own:
+            torch.cuda.current_stream(self.stream.device).wait_stream(self.stream)
+        return pooled, logits
+
+    def sync(self):
+        check(lib().jepa_head_context_sync(self._h))
+
+    def profile(self, reset: bool = True) -> dict:
+        buf = (_lib.KernelStat * 16)()
+        n = ctypes.c_int32()
+        check(lib().jepa_head_context_profile(self._h, buf, 16, ctypes.byref(n), int(reset)))
+        return {buf[i].name.decode(): {"launches": buf[i].launches, "total_ms": buf[i].total_ms,
+                                       "flops": buf[i].flops, "bytes": buf[i].bytes} for i in range(n.value)}
+
+    def close(self):
+        if getattr(self, "_h", None):
+            lib().jepa_head_context_free(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
 class ops:
     """The encoder's kernels one at a time (same kernels the encode path launches)."""
 
@@ -420,6 +532,14 @@ class ops:
         out = torch.empty((B * N, n_head * head_dim), dtype=qkv.dtype, device=qkv.device)
         check(lib().jepa_op_attention(code, _ptr(qkv), B, N, n_head, head_dim, attn_mode, prefix, frame_tokens,
                                       _ptr(out), _stream_ptr()))
+        return out
+
+    @staticmethod
+    def pool(tokens: torch.Tensor, prefix: int = 0, mode: int = POOL_MEAN):
+        """tokens float32 CUDA [B, N, D] -> [B, D]: the mean of rows [prefix, N), or row 0 (POOL_CLS)."""
+        B, N, D = tokens.shape
+        out = torch.empty((B, D), dtype=torch.float32, device=tokens.device)
+        check(lib().jepa_op_pool(mode, _ptr(tokens), B, N, D, prefix, _ptr(out), _stream_ptr()))
         return out
 
     @staticmethod

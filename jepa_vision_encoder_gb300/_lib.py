@@ -15,6 +15,7 @@ STATUS_NAMES = {0: "JEPA_OK", 1: "JEPA_E_INVALID_ARG", 2: "JEPA_E_UNSUPPORTED", 
 FP32, BF16 = 0, 1
 POS_NONE, POS_LEARNED, POS_ROPE3D, POS_SINCOS2D, POS_SINCOS3D = 0, 1, 2, 3, 4
 RESIZE_TRILINEAR, RESIZE_BICUBIC = 0, 1
+POOL_MEAN, POOL_CLS = 0, 1
 ROPE_TILED, ROPE_INTERLEAVED = 0, 1
 ATTN_FULL, ATTN_BLOCK_CAUSAL = 0, 1
 LAYOUT_TCHW, LAYOUT_CTHW = 0, 1
@@ -59,6 +60,14 @@ class PredHParams(ctypes.Structure):
         return {k: getattr(self, k) for k, _ in self._fields_}
 
 
+class HeadHParams(ctypes.Structure):
+    _fields_ = [("embed_dim", ctypes.c_int32), ("n_head", ctypes.c_int32), ("ffn_dim", ctypes.c_int32),
+                ("n_pool_layers", ctypes.c_int32), ("n_classes", ctypes.c_int32), ("ln_eps", ctypes.c_float)]
+
+    def as_dict(self):
+        return {k: getattr(self, k) for k, _ in self._fields_}
+
+
 class KernelStat(ctypes.Structure):
     _fields_ = [("name", ctypes.c_char * 24), ("launches", ctypes.c_int32), ("total_ms", ctypes.c_float),
                 ("flops", ctypes.c_double), ("bytes", ctypes.c_double)]
@@ -68,6 +77,7 @@ class KernelStat(ctypes.Structure):
 _P, _I, _U64, _SZ, _F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_uint64, ctypes.c_size_t, ctypes.c_float
 _HP = ctypes.POINTER(HParams)
 _PHP = ctypes.POINTER(PredHParams)
+_HHP = ctypes.POINTER(HeadHParams)
 SIGNATURES = {
     "jepa_preset": (_I, [ctypes.c_char_p, _HP]),
     "jepa_hparams_validate": (_I, [_HP]),
@@ -112,6 +122,21 @@ SIGNATURES = {
     "jepa_pred_context_launches": (_I, [_P, _I, ctypes.POINTER(ctypes.c_int32)]),
     "jepa_predict": (_I, [_P, _P, _I, _I, _P, _I, _P, _I, _I, _I, _I, _P]),
     "jepa_pred_context_sync": (_I, [_P]),
+    "jepa_head_preset": (_I, [ctypes.c_char_p, _HHP]),
+    "jepa_head_hparams_validate": (_I, [_HHP]),
+    "jepa_head_load": (_I, [_HHP, _U64, _I, _I, ctypes.POINTER(_P)]),
+    "jepa_head_free": (None, [_P]),
+    "jepa_head_tensor": (_I, [_P, ctypes.c_char_p, _P, _SZ]),
+    "jepa_head_context_new": (_I, [_P, _I, _I, _SZ, ctypes.POINTER(_P)]),
+    "jepa_head_context_free": (None, [_P]),
+    "jepa_head_context_set_stream": (_I, [_P, _P]),
+    "jepa_head_context_set_graph": (_I, [_P, _I]),
+    "jepa_head_context_set_profiling": (_I, [_P, _I]),
+    "jepa_head_context_profile": (_I, [_P, ctypes.POINTER(KernelStat), _I, ctypes.POINTER(ctypes.c_int32), _I]),
+    "jepa_head_context_launches": (_I, [_P, _I, ctypes.POINTER(ctypes.c_int32)]),
+    "jepa_head_forward": (_I, [_P, _P, _I, _I, _P, _P]),
+    "jepa_head_context_sync": (_I, [_P]),
+    "jepa_op_pool": (_I, [_I, _P, _I, _I, _I, _I, _P, _P]),
     "jepa_error_text": (ctypes.c_char_p, []),
     "jepa_error_reset": (None, []),
 }

@@ -17,8 +17,8 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libjepa_gb300.so")
 SOURCES = ["runtime.cu", "gemm_tc.cu", "gemm_tc2.cu", "attention_tc.cu", "simt.cu", "rowops.cu", "postab.cu",
-           "predictor.cu"]
-HEADERS = ["ptx.cuh", "epilogue.cuh", "kernels.h", "internal.h"]
+           "predictor.cu", "head.cu"]
+HEADERS = ["ptx.cuh", "epilogue.cuh", "kernels.h", "internal.h", "seq.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

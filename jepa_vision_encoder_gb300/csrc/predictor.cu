@@ -27,6 +27,7 @@
 #include "jepa_synth.h"
 #include "kernels.h"
 #include "ptx.cuh"
+#include "seq.h"
 
 using namespace jepa;
 
@@ -154,8 +155,7 @@ const char* kQNames[kQClasses] = {"pred_ids", "pred_gather_ctx", "gemm_embed", "
 
 struct jepa_pred_context {
   const jepa_predictor* p = nullptr;
-  cudaStream_t stream = nullptr;
-  bool own_stream = false;
+  SeqRunner run;
   int max_B = 0, max_ctx = 0, max_tgt = 0;
   uint8_t* ws = nullptr;
   size_t ws_bytes = 0;
@@ -169,21 +169,6 @@ struct jepa_pred_context {
   float* kout = nullptr;
   CUtensorMap tm_A, tm_Xn, tm_ao, tm_Hh, tm_Y, tm_qkv3, tm_o_qkv, tm_o_hh, tm_o_x, tm_o_out;
   int bn_embed = 0, bn_qkv = 0, bn_out = 0, bn_up = 0, bn_down = 0, bn_proj = 0;
-  // graph replay
-  bool use_graph = false;
-  cudaGraphExec_t gexec = nullptr;
-  const float* genc = nullptr;
-  const int *gctx = nullptr, *gtgt = nullptr;
-  float* gout = nullptr;
-  int gkey[8] = {-1, -1, -1, -1, -1, -1, -1, -1};
-  // profiling (eager launches only)
-  bool profiling = false;
-  std::vector<cudaEvent_t> ev;
-  size_t ev_used = 0;
-  struct Ev { int cls; size_t e0, e1; double flops, bytes; };
-  std::vector<Ev> recs;
-  int prof_launches[kQClasses] = {};
-  double prof_ms[kQClasses] = {}, prof_flops[kQClasses] = {}, prof_bytes[kQClasses] = {};
 };
 
 // ------------------------------------------------------------------ hyper-parameters
@@ -436,13 +421,17 @@ extern "C" jepa_status jepa_pred_context_new(const jepa_predictor* p, int32_t ma
   pred_ws_layout(p, max_batch, max_ctx, max_tgt, kMaxRopeRows, c);
   // the padded head columns of qkv are never written: they stay zero from here on
   e = cudaMemset(c->ws, 0, need);
-  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->stream, cudaStreamNonBlocking);
   if (e != cudaSuccess) {
     cudaFree(c->ws);
     delete c;
     return fail(JEPA_E_CUDA, "predictor context: %s", cudaGetErrorString(e));
   }
-  c->own_stream = true;
+  const jepa_status st = c->run.init(kQClasses);
+  if (st != JEPA_OK) {
+    cudaFree(c->ws);
+    delete c;
+    return st;
+  }
   *out = c;
   return JEPA_OK;
 }
@@ -450,10 +439,7 @@ extern "C" jepa_status jepa_pred_context_new(const jepa_predictor* p, int32_t ma
 extern "C" void jepa_pred_context_free(jepa_pred_context* c) {
   if (!c) return;
   cudaSetDevice(c->p->device);
-  if (c->stream) cudaStreamSynchronize(c->stream);
-  if (c->gexec) cudaGraphExecDestroy(c->gexec);
-  for (cudaEvent_t e : c->ev) cudaEventDestroy(e);
-  if (c->own_stream && c->stream) cudaStreamDestroy(c->stream);
+  c->run.destroy();
   if (c->ws) cudaFree(c->ws);
   delete c;
 }
@@ -461,26 +447,18 @@ extern "C" void jepa_pred_context_free(jepa_pred_context* c) {
 extern "C" jepa_status jepa_pred_context_set_stream(jepa_pred_context* c, void* stream) {
   if (!c) return fail(JEPA_E_INVALID_ARG, "jepa_pred_context_set_stream: null context");
   CUDA_TRY(cudaSetDevice(c->p->device));
-  CUDA_TRY(cudaStreamSynchronize(c->stream));
-  if (c->own_stream) cudaStreamDestroy(c->stream);
-  c->stream = reinterpret_cast<cudaStream_t>(stream);
-  c->own_stream = false;
-  if (c->gexec) {
-    cudaGraphExecDestroy(c->gexec);
-    c->gexec = nullptr;
-  }
-  return JEPA_OK;
+  return c->run.set_stream(stream);
 }
 
 extern "C" jepa_status jepa_pred_context_set_graph(jepa_pred_context* c, int32_t enable) {
   if (!c) return fail(JEPA_E_INVALID_ARG, "jepa_pred_context_set_graph: null context");
-  c->use_graph = enable != 0;
+  c->run.use_graph = enable != 0;
   return JEPA_OK;
 }
 
 extern "C" jepa_status jepa_pred_context_set_profiling(jepa_pred_context* c, int32_t enable) {
   if (!c) return fail(JEPA_E_INVALID_ARG, "jepa_pred_context_set_profiling: null context");
-  c->profiling = enable != 0;
+  c->run.profiling = enable != 0;
   return JEPA_OK;
 }
 
@@ -514,7 +492,7 @@ jepa_status pred_prepare(jepa_pred_context* c, int B, int n_ctx, int n_tgt, int 
   c->bn_up = gemm_tc_pick_bn((int)M, F);
   c->bn_down = gemm_tc_pick_bn((int)M, P);
   c->bn_proj = gemm_tc_pick_bn((int)Mt, O);
-  CUDA_TRY(rope_axes_launch(gt, gh, gw, P / hp.n_head, hp.rope_theta, 0, 0, c->rope, c->stream));
+  CUDA_TRY(rope_axes_launch(gt, gh, gw, P / hp.n_head, hp.rope_theta, 0, 0, c->rope, c->run.stream));
   c->kB = B;
   c->kC = n_ctx;
   c->kT = n_tgt;
@@ -538,58 +516,38 @@ EpiArgs epi_of(int kind, int M, int N, const float* bias, void* out) {
   return e;
 }
 
-template <class Fn>
-cudaError_t timed(jepa_pred_context* c, int cls, double flops, double bytes, Fn&& launch) {
-  if (!c->profiling) return launch();
-  while (c->ev.size() < c->ev_used + 2) {
-    cudaEvent_t e;
-    cudaError_t r = cudaEventCreate(&e);
-    if (r != cudaSuccess) return r;
-    c->ev.push_back(e);
-  }
-  const size_t e0 = c->ev_used++, e1 = c->ev_used++;
-  cudaEventRecord(c->ev[e0], c->stream);
-  const cudaError_t r = launch();
-  cudaEventRecord(c->ev[e1], c->stream);
-  c->recs.push_back({cls, e0, e1, flops, bytes});
-  return r;
-}
-
 jepa_status pred_launch(jepa_pred_context* c, const float* enc, int B, int n_enc, const int* ctx, int n_ctx,
                         const int* tgt, int n_tgt, int gt, int gh, int gw, float* out) {
   const jepa_predictor* p = c->p;
   const jepa_pred_hparams& hp = p->hp;
   const int P = hp.embed_dim, F = hp.ffn_dim, E = hp.enc_dim, O = hp.out_dim, NH = hp.n_head, hd = P / NH;
   const int n_total = n_ctx + n_tgt, M = B * n_total, Mc = B * n_ctx, Mt = B * n_tgt;
-  cudaStream_t s = c->stream;
+  cudaStream_t s = c->run.stream;
   const uint64_t lim = default_wait_limit_ns();
-  struct PdlScope {
-    bool prev;
-    explicit PdlScope(bool on) : prev(pdl_launches()) { pdl_launches() = on; }
-    ~PdlScope() { pdl_launches() = prev; }
-  } pdl_scope(!c->profiling);
+  PdlScope pdl_scope(!c->run.profiling);
+  auto timed = [c](int cls, double fl, double by, auto&& launch) { return c->run.timed(cls, fl, by, launch); };
   const double dM = M, dP = P, dF = F;
   const double ln_bytes = dM * dP * 6.0;
 
-  CUDA_TRY(timed(c, kQIds, 0.0, (double)M * 8.0, [&] {
+  CUDA_TRY(timed(kQIds, 0.0, (double)M * 8.0, [&] {
     return launch_kernel(pred_ids_kernel, dim3(blocks_for(M, 256)), dim3(256), 0, s, ctx, n_ctx, tgt, n_tgt, B, n_enc,
                          gt * gh * gw, c->ids, c->err);
   }));
   if (n_ctx > 0) {
-    CUDA_TRY(timed(c, kQGather, 0.0, (double)Mc * E * 6.0, [&] {
+    CUDA_TRY(timed(kQGather, 0.0, (double)Mc * E * 6.0, [&] {
       return launch_kernel(pred_gather_ctx_kernel, dim3(blocks_for((long long)Mc * (E / 8), 256)), dim3(256), 0, s,
                            enc, n_enc, E, (const int*)c->ids, n_total, n_ctx, B, reinterpret_cast<__nv_bfloat16*>(c->A));
     }));
     EpiArgs ee = epi_of(kEpiPatch, Mc, P, p->b_embed, c->X);  // row s of item b -> X row b*n_total + s
     ee.patches_per_item = n_ctx;
     ee.rows_per_item = n_total;
-    CUDA_TRY(timed(c, kQEmbed, 2.0 * Mc * dP * E, 0.0, [&] {
+    CUDA_TRY(timed(kQEmbed, 2.0 * Mc * dP * E, 0.0, [&] {
       return gemm_tc_launch(c->tm_A, p->tm_embed[slot(c->bn_embed)], c->tm_o_x, c->bn_embed, ee, Mc, P, E, c->err,
                             lim, s);
     }));
   }
   const float* token = p->mask_tokens + (size_t)(hp.mask_index % hp.n_mask_tokens) * P;
-  CUDA_TRY(timed(c, kQFill, 0.0, (double)Mt * P * 4.0, [&] {
+  CUDA_TRY(timed(kQFill, 0.0, (double)Mt * P * 4.0, [&] {
     return launch_kernel(pred_fill_targets_kernel, dim3(blocks_for((long long)Mt * (P / 4), 256)), dim3(256), 0, s,
                          c->X, B, n_total, n_ctx, P, token);
   }));
@@ -622,27 +580,27 @@ jepa_status pred_launch(jepa_pred_context* c, const float* enc, int B, int n_enc
     EpiArgs oe = epi_of(kEpiResidual, M, P, w.b_out, c->X);
     EpiArgs ue = epi_of(kEpiGelu, M, F, w.b_up, c->Hh);
     EpiArgs de = epi_of(kEpiResidual, M, P, w.b_down, c->X);
-    CUDA_TRY(timed(c, kQLn, 0.0, ln_bytes,
+    CUDA_TRY(timed(kQLn, 0.0, ln_bytes,
                    [&] { return layernorm_launch(c->X, M, P, w.ln1_w, w.ln1_b, hp.ln_eps, true, c->Xn, s); }));
-    CUDA_TRY(timed(c, kQQkv, 2.0 * dM * 3.0 * dP * dP, 0.0, [&] {
+    CUDA_TRY(timed(kQQkv, 2.0 * dM * 3.0 * dP * dP, 0.0, [&] {
       return gemm_tc_launch(c->tm_Xn, w.tm_qkv[slot(c->bn_qkv)], c->tm_o_qkv, c->bn_qkv, qe, M, 3 * P, P, c->err, lim, s);
     }));
-    CUDA_TRY(timed(c, kQAttn, attn_flops, 0.0, [&] { return attention_tc_launch(c->tm_qkv3, ap, c->err, lim, s); }));
-    CUDA_TRY(timed(c, kQOut, 2.0 * dM * dP * dP, 0.0, [&] {
+    CUDA_TRY(timed(kQAttn, attn_flops, 0.0, [&] { return attention_tc_launch(c->tm_qkv3, ap, c->err, lim, s); }));
+    CUDA_TRY(timed(kQOut, 2.0 * dM * dP * dP, 0.0, [&] {
       return gemm_tc_launch(c->tm_ao, w.tm_out[slot(c->bn_out)], c->tm_o_x, c->bn_out, oe, M, P, P, c->err, lim, s);
     }));
-    CUDA_TRY(timed(c, kQLn, 0.0, ln_bytes,
+    CUDA_TRY(timed(kQLn, 0.0, ln_bytes,
                    [&] { return layernorm_launch(c->X, M, P, w.ln2_w, w.ln2_b, hp.ln_eps, true, c->Xn, s); }));
-    CUDA_TRY(timed(c, kQUp, 2.0 * dM * dF * dP, 0.0, [&] {
+    CUDA_TRY(timed(kQUp, 2.0 * dM * dF * dP, 0.0, [&] {
       return gemm_tc_launch(c->tm_Xn, w.tm_up[slot(c->bn_up)], c->tm_o_hh, c->bn_up, ue, M, F, P, c->err, lim, s);
     }));
-    CUDA_TRY(timed(c, kQDown, 2.0 * dM * dP * dF, 0.0, [&] {
+    CUDA_TRY(timed(kQDown, 2.0 * dM * dP * dF, 0.0, [&] {
       return gemm_tc_launch(c->tm_Hh, w.tm_down[slot(c->bn_down)], c->tm_o_x, c->bn_down, de, M, P, F, c->err, lim, s);
     }));
   }
-  CUDA_TRY(timed(c, kQLnFinal, 0.0, ln_bytes,
+  CUDA_TRY(timed(kQLnFinal, 0.0, ln_bytes,
                  [&] { return layernorm_launch(c->X, M, P, p->norm_w, p->norm_b, hp.ln_eps, true, c->Xn, s); }));
-  CUDA_TRY(timed(c, kQGatherTgt, 0.0, (double)Mt * P * 4.0, [&] {
+  CUDA_TRY(timed(kQGatherTgt, 0.0, (double)Mt * P * 4.0, [&] {
     return launch_kernel(pred_gather_tgt_kernel, dim3(blocks_for((long long)Mt * (P / 8), 256)), dim3(256), 0, s,
                          reinterpret_cast<const __nv_bfloat16*>(c->Xn), B, n_total, n_ctx, P,
                          reinterpret_cast<__nv_bfloat16*>(c->Y));
@@ -650,7 +608,7 @@ jepa_status pred_launch(jepa_pred_context* c, const float* enc, int B, int n_enc
   EpiArgs pe = epi_of(kEpiPatch, Mt, O, p->b_proj, out);  // rows are the output rows: fp32 TMA store
   pe.patches_per_item = n_tgt;
   pe.rows_per_item = n_tgt;
-  CUDA_TRY(timed(c, kQProj, 2.0 * Mt * (double)O * P, 0.0, [&] {
+  CUDA_TRY(timed(kQProj, 2.0 * Mt * (double)O * P, 0.0, [&] {
     return gemm_tc_launch(c->tm_Y, p->tm_proj[slot(c->bn_proj)], c->tm_o_out, c->bn_proj, pe, Mt, O, P, c->err, lim, s);
   }));
   return JEPA_OK;
@@ -683,88 +641,22 @@ extern "C" jepa_status jepa_predict(jepa_pred_context* c, const float* d_enc, in
   CUDA_TRY(cudaSetDevice(c->p->device));
   jepa_status st = pred_prepare(c, B, n_ctx, n_tgt, gt, gh, gw, d_out);
   if (st != JEPA_OK) return st;
-  if (!c->use_graph || c->profiling)
-    return pred_launch(c, d_enc, B, n_enc, d_ctx_ids, n_ctx, d_tgt_ids, n_tgt, gt, gh, gw, d_out);
-  const int key[8] = {B, n_enc, n_ctx, n_tgt, gt, gh, gw, 0};
-  const bool hit = c->gexec && !memcmp(key, c->gkey, sizeof key) && c->genc == d_enc && c->gctx == d_ctx_ids &&
-                   c->gtgt == d_tgt_ids && c->gout == d_out;
-  if (!hit) {
-    if (c->gexec) {
-      cudaGraphExecDestroy(c->gexec);
-      c->gexec = nullptr;
-    }
-    cudaGraph_t graph = nullptr;
-    CUDA_TRY(cudaStreamBeginCapture(c->stream, cudaStreamCaptureModeThreadLocal));
-    st = pred_launch(c, d_enc, B, n_enc, d_ctx_ids, n_ctx, d_tgt_ids, n_tgt, gt, gh, gw, d_out);
-    const cudaError_t e = cudaStreamEndCapture(c->stream, &graph);
-    if (st != JEPA_OK) {
-      if (graph) cudaGraphDestroy(graph);
-      return st;
-    }
-    if (e != cudaSuccess) return fail(JEPA_E_CUDA, "predictor graph capture: %s", cudaGetErrorString(e));
-    const cudaError_t ei = cudaGraphInstantiate(&c->gexec, graph, 0);
-    cudaGraphDestroy(graph);
-    if (ei != cudaSuccess) return fail(JEPA_E_CUDA, "predictor graph instantiate: %s", cudaGetErrorString(ei));
-    memcpy(c->gkey, key, sizeof key);
-    c->genc = d_enc;
-    c->gctx = d_ctx_ids;
-    c->gtgt = d_tgt_ids;
-    c->gout = d_out;
-  }
-  CUDA_TRY(cudaGraphLaunch(c->gexec, c->stream));
-  return JEPA_OK;
+  const std::vector<uintptr_t> key = {(uintptr_t)B, (uintptr_t)n_enc, (uintptr_t)n_ctx, (uintptr_t)n_tgt,
+                                     (uintptr_t)gt, (uintptr_t)gh, (uintptr_t)gw, (uintptr_t)d_enc,
+                                     (uintptr_t)d_ctx_ids, (uintptr_t)d_tgt_ids, (uintptr_t)d_out};
+  return c->run.run(key, [&] { return pred_launch(c, d_enc, B, n_enc, d_ctx_ids, n_ctx, d_tgt_ids, n_tgt, gt, gh, gw,
+                                                  d_out); }, "jepa_predict");
 }
 
 extern "C" jepa_status jepa_pred_context_sync(jepa_pred_context* c) {
   if (!c) return fail(JEPA_E_INVALID_ARG, "jepa_pred_context_sync: null context");
   CUDA_TRY(cudaSetDevice(c->p->device));
-  CUDA_TRY(cudaStreamSynchronize(c->stream));
-  int h_err = 0;
-  CUDA_TRY(cudaMemcpy(&h_err, c->err, sizeof(int), cudaMemcpyDeviceToHost));
-  if (h_err) {
-    CUDA_TRY(cudaMemset(c->err, 0, sizeof(int)));
-    if (h_err & kErrBadIds)
-      return fail(JEPA_E_INVALID_ARG, "jepa_predict: a context or target id was outside its range (replaced by 0)");
-    return fail(JEPA_E_TIMEOUT, "a device-side wait gave up (error word %d)", h_err);
-  }
-  return JEPA_OK;
+  return c->run.sync(c->err, "jepa_predict");
 }
 
 extern "C" jepa_status jepa_pred_context_profile(jepa_pred_context* c, jepa_kernel_stat* out, int32_t max,
                                                  int32_t* n_out, int32_t reset) {
   if (!c || !n_out || (max > 0 && !out)) return fail(JEPA_E_INVALID_ARG, "jepa_pred_context_profile: null argument");
   CUDA_TRY(cudaSetDevice(c->p->device));
-  CUDA_TRY(cudaStreamSynchronize(c->stream));
-  for (const auto& r : c->recs) {
-    float ms = 0.0f;
-    CUDA_TRY(cudaEventElapsedTime(&ms, c->ev[r.e0], c->ev[r.e1]));
-    c->prof_launches[r.cls] += 1;
-    c->prof_ms[r.cls] += ms;
-    c->prof_flops[r.cls] += r.flops;
-    c->prof_bytes[r.cls] += r.bytes;
-  }
-  c->recs.clear();
-  c->ev_used = 0;
-  int n = 0;
-  for (int k = 0; k < kQClasses; ++k) {
-    if (!c->prof_launches[k]) continue;
-    if (n < max) {
-      jepa_kernel_stat& st = out[n];
-      memset(&st, 0, sizeof st);
-      snprintf(st.name, sizeof st.name, "%s", kQNames[k]);
-      st.launches = c->prof_launches[k];
-      st.total_ms = (float)c->prof_ms[k];
-      st.flops = c->prof_flops[k];
-      st.bytes = c->prof_bytes[k];
-    }
-    ++n;
-  }
-  *n_out = n;
-  if (reset) {
-    for (int k = 0; k < kQClasses; ++k) {
-      c->prof_launches[k] = 0;
-      c->prof_ms[k] = c->prof_flops[k] = c->prof_bytes[k] = 0.0;
-    }
-  }
-  return JEPA_OK;
+  return c->run.profile(kQNames, out, max, n_out, reset);
 }

@@ -68,3 +68,10 @@ from oracle import PredConfig  # noqa: E402
 PRED_VJEPA2_L16 = PredConfig(embed_dim=384, n_layer=12, n_head=12, ffn_dim=1536, enc_dim=1024, out_dim=1024,
                              n_mask_tokens=10, mask_index=1)
 PRED_WORKLOAD = dict(grid=(8, 16, 16), n_ctx=1024, n_tgt=1024, batches=(1, 8))
+
+# The V-JEPA 2 ViT-L SSv2 classifier head (jepa.head.*): 3 pooler layers, 174 classes, over the
+# 2048 tokens of a 16 x 256^2 clip's encoder output.
+from oracle import HeadConfig  # noqa: E402
+
+HEAD_VJEPA2_L16_SSV2 = HeadConfig(embed_dim=1024, n_head=16, ffn_dim=4096, n_pool_layers=3, n_classes=174)
+HEAD_WORKLOAD = dict(tokens=2048, batches=(1, 8))

@@ -83,6 +83,23 @@ def test_predictor_preset_matches_its_config():
     expect(L.jepa_predict(None, None, 1, 1, None, 0, None, 1, 1, 1, 1, None), _lib.E_INVALID_ARG)
 
 
+def test_head_preset_matches_its_config():
+    from configs import HEAD_VJEPA2_L16_SSV2
+    hp = jv.head_preset("vjepa2_vitl16_ssv2")
+    for k in ("embed_dim", "n_head", "ffn_dim", "n_pool_layers", "n_classes"):
+        assert getattr(hp, k) == getattr(HEAD_VJEPA2_L16_SSV2, k), k
+    L = jv.lib()
+    assert L.jepa_head_hparams_validate(ctypes.byref(hp)) == 0
+    for kw, frag in [(dict(n_head=7), "not divisible"), (dict(n_classes=0), "n_classes"),
+                     (dict(n_pool_layers=-1), "n_pool_layers"), (dict(ln_eps=-1.0), "ln_eps")]:
+        bad = jv.head_preset("vjepa2_vitl16_ssv2")
+        for k, v in kw.items():
+            setattr(bad, k, v)
+        expect(L.jepa_head_hparams_validate(ctypes.byref(bad)), _lib.E_INVALID_ARG, frag)
+    expect(L.jepa_head_forward(None, None, 1, 1, None, None), _lib.E_INVALID_ARG)
+    expect(L.jepa_op_pool(0, None, 1, 1, 4, 0, None, None), _lib.E_INVALID_ARG)
+
+
 def test_token_counts():
     assert jv.n_tokens(jv.preset("vjepa2_vitg16"), 64, 256, 256) == 8192
     hp = jv.preset("levjepa_vitl16")
