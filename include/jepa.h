@@ -131,6 +131,26 @@ jepa_status jepa_model_load(const jepa_hparams* hp, uint64_t seed, int32_t dtype
 void jepa_model_free(jepa_model* m);
 jepa_status jepa_model_hparams(const jepa_model* m, jepa_hparams* out);
 
+/* Read the encoder of a GGUF file (v2 / v3; the jepa.* keys and enc.* tensors of "GGUF schema
+ * (v1)") and check it as the pages' loader does ("Architecture", Robustness: what the loader
+ * validates), without loading any weight: header counts and lengths in range; every tensor's
+ * bytes inside the file; general.architecture = jepa and a known jepa.family; every jepa.enc.*
+ * integer in its range and every float finite and in range; enum strings known (act, pos_type,
+ * rope_freq_layout, attn_mode); block_causal only on levjepa; the derived invariants of
+ * jepa_hparams_validate; every required enc.* tensor present, f32 for the operands the graph adds
+ * (norms, biases, tokens, tables) and f32 / f16 / bf16 for the matrices, each shape matching the
+ * hyper-parameters (a learned table's rows are taken from the tensor). Absent flags (cls_token,
+ * modality_embed, rope_interpolate, layer_scale) are off; an absent attn_mode is full (the pages:
+ * no existing file carries it); qkv_fused false takes attn_q / attn_k / attn_v and fuses them.
+ * Refused by name: JEPA_E_INVALID_ARG for a malformed or inconsistent file; JEPA_E_UNSUPPORTED for
+ * a valid file this build cannot run (family lewm, act other than gelu_erf, register tokens, layer
+ * scale, quantized weights). Host only: no CUDA call. */
+jepa_status jepa_gguf_hparams(const char* path, jepa_hparams* out);
+/* jepa_gguf_hparams, then load the file's enc.* tensors as a model on `device` (dtype as
+ * jepa_model_load: bf16 rounds the matrices to nearest even; the file's position table is used
+ * as stored, and resized for other grids). */
+jepa_status jepa_model_load_gguf(const char* path, int32_t dtype, int32_t device, jepa_model** out);
+
 /* Copy the enc.* tensor `name` (e.g. "enc.blk.3.attn_qkv.weight") to host memory as float:
  * n_elems must equal the tensor's element count (shape per the GGUF schema, PyTorch row-major).
  * Synchronous. Unknown name -> JEPA_E_INVALID_ARG. */

@@ -10,6 +10,7 @@ CUDA kernels. Importing works without a GPU; calls that launch kernels need one.
     tokens = ctx.encode(pixels)          # pixels: float32 CUDA tensor [B, T, 3, H, W]
 """
 import ctypes
+import os
 
 import torch
 
@@ -20,7 +21,7 @@ from ._lib import (ATTN_BLOCK_CAUSAL, ATTN_FULL, BF16, EPI_BIAS, EPI_BIAS_GELU, 
                    ROPE_TILED, POOL_CLS, POOL_MEAN, Epilogue, HeadHParams, HParams, JepaError, PredHParams, check,
                    lib)
 
-__all__ = ["Model", "Context", "HParams", "JepaError", "preset", "hparams", "n_tokens", "ops", "lib", "Predictor",
+__all__ = ["Model", "Context", "HParams", "JepaError", "preset", "hparams", "gguf_hparams", "n_tokens", "ops", "lib", "Predictor",
            "PredContext", "PredHParams", "pred_preset", "Head", "HeadContext", "HeadHParams", "head_preset"]
 
 PRESETS = ("hfvit_ti14", "vjepa2_vitl16", "vjepa2_1_vitl16", "levjepa_vitl16", "vjepa2_vitg16", "vjepa_vitl16",
@@ -38,6 +39,13 @@ def _dtype_code(dtype) -> int:
 def preset(name: str) -> HParams:
     hp = HParams()
     check(lib().jepa_preset(name.encode(), ctypes.byref(hp)))
+    return hp
+
+
+def gguf_hparams(path: str) -> HParams:
+    """The checked encoder hyper-parameters of a GGUF file (no weights are read; no GPU needed)."""
+    hp = HParams()
+    check(lib().jepa_gguf_hparams(os.fsencode(path), ctypes.byref(hp)))
     return hp
 
 
@@ -83,6 +91,19 @@ class Model:
         h = ctypes.c_void_p()
         check(lib().jepa_model_load(ctypes.byref(hp), seed, self.dtype, device, ctypes.byref(h)))
         self._h = h
+
+    @classmethod
+    def from_gguf(cls, path: str, dtype="bf16", device: int = 0):
+        """An encoder loaded from a GGUF file (checked as jepa_gguf_hparams describes)."""
+        self = cls.__new__(cls)
+        self.hp = gguf_hparams(path)
+        self.seed = None
+        self.dtype = _dtype_code(dtype)
+        self.device = device
+        h = ctypes.c_void_p()
+        check(lib().jepa_model_load_gguf(os.fsencode(path), self.dtype, device, ctypes.byref(h)))
+        self._h = h
+        return self
 
     @classmethod
     def preset(cls, name: str, seed: int = 0, dtype="bf16", device: int = 0, **overrides):

@@ -84,6 +84,8 @@ SIGNATURES = {
     "jepa_n_tokens": (_I, [_HP, _I, _I, _I, ctypes.POINTER(ctypes.c_int32)]),
     "jepa_model_load": (_I, [_HP, _U64, _I, _I, ctypes.POINTER(_P)]),
     "jepa_model_free": (None, [_P]),
+    "jepa_gguf_hparams": (_I, [ctypes.c_char_p, _HP]),
+    "jepa_model_load_gguf": (_I, [ctypes.c_char_p, _I, _I, ctypes.POINTER(_P)]),
     "jepa_model_hparams": (_I, [_P, _HP]),
     "jepa_model_tensor": (_I, [_P, ctypes.c_char_p, _P, _SZ]),
     "jepa_context_new": (_I, [_P, _I, _I, _I, _I, _SZ, ctypes.POINTER(_P)]),

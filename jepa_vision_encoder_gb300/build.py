@@ -1,6 +1,6 @@
 """Build libjepa_gb300.so in place with nvcc for sm_103a (no cmake, one -gencode).
 
-Each .cu translation unit compiles in parallel to an object under _build/, then one link
+Each translation unit (.cu, and the host-only .cpp) compiles in parallel to an object under _build/, then one link
 step writes jepa_vision_encoder_gb300/libjepa_gb300.so. Host code is compiled with
 floating-point contraction off so that the seeded weight generator (synth/jepa_synth.h)
 produces the same bits on x86-64 and aarch64.
@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libjepa_gb300.so")
 SOURCES = ["runtime.cu", "gemm_tc.cu", "gemm_tc2.cu", "attention_tc.cu", "simt.cu", "rowops.cu", "postab.cu",
-           "predictor.cu", "head.cu"]
+           "predictor.cu", "head.cu", "gguf.cpp"]
 HEADERS = ["ptx.cuh", "epilogue.cuh", "kernels.h", "internal.h", "seq.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -53,7 +53,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     objs, jobs = [], []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD, src.replace(".cu", ".o"))
+        o = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
         objs.append(o)
         if force or _stale(o, [s] + deps):
             jobs.append([nvcc()] + _flags() + list(extra_flags) + ["-c", s, "-o", o])

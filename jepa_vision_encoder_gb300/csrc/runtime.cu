@@ -17,6 +17,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <functional>
 #include <mutex>
 #include <string>
 #include <thread>
@@ -189,7 +190,60 @@ struct TensorRec {
   size_t n;
   bool bf16;
   bool fixed;     // computed by a kernel (sin-cos table), not drawn from the generator
+  bool matrix;    // a weight matrix; every other tensor is an fp32 operand (norm, bias, token, table)
+  std::vector<uint64_t> shape;  // PyTorch order
 };
+
+// The enc.* tensors of an encoder, in GGUF names and PyTorch row-major shapes ("GGUF schema (v1)",
+// Encoder tensors). bake_sincos marks a sin-cos table as computed on the device.
+std::vector<TensorRec> encoder_tensors(const jepa_hparams& hp, bool bf, bool bake_sincos) {
+  const uint64_t D = hp.embed_dim, F = hp.ffn_dim;
+  const uint64_t K = (uint64_t)hp.in_chans * hp.tubelet_size * hp.patch_size * hp.patch_size;
+  std::vector<TensorRec> ts;
+  auto add = [&](const std::string& name, std::vector<uint64_t> shape, bool matrix, bool fixed = false) {
+    TensorRec r;
+    r.name = name;
+    r.n = 1;
+    for (uint64_t d : shape) r.n *= d;
+    r.bf16 = bf && matrix;
+    r.fixed = fixed;
+    r.matrix = matrix;
+    r.shape = std::move(shape);
+    r.offset = 0;
+    ts.push_back(std::move(r));
+  };
+  add("enc.patch_embed.weight", {D, K}, true);
+  add("enc.patch_embed.bias", {D}, false);
+  if (hp.pos_type == JEPA_POS_LEARNED) add("enc.pos_embed", {(uint64_t)hp.n_pos_rows, D}, false);
+  if (hp.pos_type == JEPA_POS_SINCOS2D || hp.pos_type == JEPA_POS_SINCOS3D) {
+    const uint64_t gt = hp.pos_type == JEPA_POS_SINCOS3D ? hp.n_frames / hp.tubelet_size : 1;
+    const uint64_t g = hp.img_size / hp.patch_size;
+    add("enc.pos_embed", {gt * g * g, D}, false, bake_sincos);
+  }
+  if (hp.cls_token) add("enc.cls_token", {D}, false);
+  if (hp.modality_embed) add("enc.mod_embed_video", {D}, false);
+  for (int l = 0; l < hp.n_layer; ++l) {
+    const std::string p = "enc.blk." + std::to_string(l) + ".";
+    add(p + "ln1.weight", {D}, false);
+    add(p + "ln1.bias", {D}, false);
+    add(p + "attn_qkv.weight", {3 * D, D}, true);
+    add(p + "attn_qkv.bias", {3 * D}, false);
+    add(p + "attn_out.weight", {D, D}, true);
+    add(p + "attn_out.bias", {D}, false);
+    add(p + "ln2.weight", {D}, false);
+    add(p + "ln2.bias", {D}, false);
+    add(p + "ffn_up.weight", {F, D}, true);
+    add(p + "ffn_up.bias", {F}, false);
+    add(p + "ffn_down.weight", {D, F}, true);
+    add(p + "ffn_down.bias", {D}, false);
+  }
+  add("enc.norm.weight", {D}, false);
+  add("enc.norm.bias", {D}, false);
+  return ts;
+}
+
+// Fills n floats of tensor `name`; the model's synthetic weights or a file's.
+using TensorFill = std::function<jepa_status(const TensorRec& t, float* dst)>;
 struct LayerW {
   const float *ln1_w, *ln1_b, *b_qkv, *b_out, *ln2_w, *ln2_b, *b_up, *b_down;
   const void *w_qkv, *w_out, *w_up, *w_down;
@@ -236,8 +290,12 @@ void jepa::synth_parallel(uint64_t seed, const std::string& name, int bf16_matri
   for (auto& x : th) x.join();
 }
 
-extern "C" jepa_status jepa_model_load(const jepa_hparams* hp, uint64_t seed, int32_t dtype, int32_t device,
-                                       jepa_model** out) {
+namespace {
+// Builds a model: the tensor table, one arena, every tensor filled (fill == nullptr: the synthetic
+// recipe of `seed`, sin-cos tables baked on the device; otherwise `fill`, tables included) and
+// uploaded (bf16 matrices rounded to nearest even), then the weight tensor maps.
+jepa_status model_create(const jepa_hparams* hp, uint64_t seed, int32_t dtype, int32_t device, const TensorFill* fill,
+                         jepa_model** out) {
   if (!hp || !out) return fail(JEPA_E_INVALID_ARG, "jepa_model_load: null argument");
   *out = nullptr;
   jepa_status st = jepa_hparams_validate(hp);
@@ -265,43 +323,9 @@ extern "C" jepa_status jepa_model_load(const jepa_hparams* hp, uint64_t seed, in
   m->seed = seed;
   m->K = K;
   const bool bf = dtype == JEPA_BF16;
-  // tensor table, in GGUF enc.* names and PyTorch row-major shapes
-  auto add = [&](const std::string& name, size_t n, bool matrix, bool fixed = false) {
-    TensorRec r;
-    r.name = name;
-    r.n = n;
-    r.bf16 = bf && matrix;
-    r.fixed = fixed;
-    r.offset = 0;
-    m->tensors.push_back(r);
-  };
-  add("enc.patch_embed.weight", (size_t)D * K, true);
-  add("enc.patch_embed.bias", D, false);
-  if (hp->pos_type == JEPA_POS_LEARNED) add("enc.pos_embed", (size_t)hp->n_pos_rows * D, false);
+  m->tensors = encoder_tensors(*hp, bf, fill == nullptr);
   int pgt = 0, pgh = 0, pgw = 0;  // training grid of a sin-cos table
-  if (is_sincos(*hp)) {
-    sincos_train_grid(*hp, &pgt, &pgh, &pgw);
-    add("enc.pos_embed", (size_t)pgt * pgh * pgw * D, false, true);
-  }
-  if (hp->cls_token) add("enc.cls_token", D, false);
-  if (hp->modality_embed) add("enc.mod_embed_video", D, false);
-  for (int l = 0; l < L; ++l) {
-    const std::string p = "enc.blk." + std::to_string(l) + ".";
-    add(p + "ln1.weight", D, false);
-    add(p + "ln1.bias", D, false);
-    add(p + "attn_qkv.weight", (size_t)3 * D * D, true);
-    add(p + "attn_qkv.bias", (size_t)3 * D, false);
-    add(p + "attn_out.weight", (size_t)D * D, true);
-    add(p + "attn_out.bias", D, false);
-    add(p + "ln2.weight", D, false);
-    add(p + "ln2.bias", D, false);
-    add(p + "ffn_up.weight", (size_t)F * D, true);
-    add(p + "ffn_up.bias", F, false);
-    add(p + "ffn_down.weight", (size_t)D * F, true);
-    add(p + "ffn_down.bias", D, false);
-  }
-  add("enc.norm.weight", D, false);
-  add("enc.norm.bias", D, false);
+  if (is_sincos(*hp)) sincos_train_grid(*hp, &pgt, &pgh, &pgw);
   size_t off = 0, largest = 0;
   for (auto& t : m->tensors) {
     t.offset = off;
@@ -318,7 +342,15 @@ extern "C" jepa_status jepa_model_load(const jepa_hparams* hp, uint64_t seed, in
   std::vector<uint16_t> hbits;
   for (const auto& t : m->tensors) {
     if (t.fixed) continue;
-    synth_parallel(seed, t.name, bf ? 1 : 0, t.n, host.data());
+    if (fill) {
+      const jepa_status fs = (*fill)(t, host.data());
+      if (fs != JEPA_OK) {
+        jepa_model_free(m);
+        return fs;
+      }
+    } else {
+      synth_parallel(seed, t.name, bf ? 1 : 0, t.n, host.data());
+    }
     if (t.bf16) {
       hbits.resize(t.n);
       for (size_t i = 0; i < t.n; ++i) hbits[i] = jsynth_f32_to_bf16_bits(host[i]);
@@ -336,7 +368,7 @@ extern "C" jepa_status jepa_model_load(const jepa_hparams* hp, uint64_t seed, in
   m->w_patch = ptr("enc.patch_embed.weight");
   m->b_patch = fptr("enc.patch_embed.bias");
   if (hp->pos_type == JEPA_POS_LEARNED) m->pos = fptr("enc.pos_embed");
-  if (is_sincos(*hp)) {  // the converter's table of the training grid, baked here on the device
+  if (is_sincos(*hp) && !fill) {  // the converter's table of the training grid, baked here on the device
     float* tab = reinterpret_cast<float*>(ptr("enc.pos_embed"));
     e = sincos_table_launch(hp->pos_type == JEPA_POS_SINCOS3D ? 1 : 0, pgt, pgh, pgw, D, hp->sincos_w_first,
                             hp->sincos_uniform_power, tab, nullptr);
@@ -347,6 +379,7 @@ extern "C" jepa_status jepa_model_load(const jepa_hparams* hp, uint64_t seed, in
     }
     m->pos = tab;
   }
+  if (is_sincos(*hp) && fill) m->pos = fptr("enc.pos_embed");  // the file's table
   if (hp->cls_token) m->cls = fptr("enc.cls_token");
   if (hp->modality_embed) m->mod = fptr("enc.mod_embed_video");
   m->norm_w = fptr("enc.norm.weight");
@@ -383,6 +416,232 @@ extern "C" jepa_status jepa_model_load(const jepa_hparams* hp, uint64_t seed, in
   }
   *out = m;
   return JEPA_OK;
+}
+
+// ---- GGUF encoder files ("Architecture", Robustness: what the loader validates)
+bool gguf_is_int(const GgufValue& v) { return v.type <= 5 || v.type == 10 || v.type == 11; }  // u8..i32, u64, i64
+
+jepa_status gguf_int(const GgufFile& g, const char* key, bool required, int64_t lo, int64_t hi, int32_t dflt,
+                     int32_t* out) {
+  const GgufValue* v = g.get(key);
+  if (!v) {
+    if (required) return fail(JEPA_E_INVALID_ARG, "gguf: required key %s is missing", key);
+    *out = dflt;
+    return JEPA_OK;
+  }
+  if (!gguf_is_int(*v)) return fail(JEPA_E_INVALID_ARG, "gguf: %s is not an integer (type %u)", key, v->type);
+  const bool neg = (v->type == 1 || v->type == 3 || v->type == 5 || v->type == 11) && v->i < 0;
+  if (neg || (!neg && v->u > (uint64_t)hi) || v->i < lo)
+    return fail(JEPA_E_INVALID_ARG, "gguf: %s = %lld outside [%lld, %lld]", key, (long long)v->i, (long long)lo,
+                (long long)hi);
+  *out = (int32_t)v->i;
+  return JEPA_OK;
+}
+
+jepa_status gguf_float(const GgufFile& g, const char* key, bool required, float dflt, float* out) {
+  const GgufValue* v = g.get(key);
+  if (!v) {
+    if (required) return fail(JEPA_E_INVALID_ARG, "gguf: required key %s is missing", key);
+    *out = dflt;
+    return JEPA_OK;
+  }
+  if (v->type != 6 && v->type != 12) return fail(JEPA_E_INVALID_ARG, "gguf: %s is not a float (type %u)", key, v->type);
+  if (!std::isfinite(v->f)) return fail(JEPA_E_INVALID_ARG, "gguf: %s is not finite", key);
+  *out = (float)v->f;
+  return JEPA_OK;
+}
+
+jepa_status gguf_bool(const GgufFile& g, const char* key, bool* out) {
+  const GgufValue* v = g.get(key);
+  *out = false;  // a flag the file does not set is off
+  if (!v) return JEPA_OK;
+  if (v->type != 7) return fail(JEPA_E_INVALID_ARG, "gguf: %s is not a bool (type %u)", key, v->type);
+  *out = v->u != 0;
+  return JEPA_OK;
+}
+
+jepa_status gguf_str(const GgufFile& g, const char* key, bool required, const char* dflt, std::string* out) {
+  const GgufValue* v = g.get(key);
+  if (!v) {
+    if (required) return fail(JEPA_E_INVALID_ARG, "gguf: required key %s is missing", key);
+    *out = dflt;
+    return JEPA_OK;
+  }
+  if (v->type != 8) return fail(JEPA_E_INVALID_ARG, "gguf: %s is not a string (type %u)", key, v->type);
+  *out = v->s;
+  return JEPA_OK;
+}
+
+// Dims of a GGUF tensor in PyTorch order, without ggml's trailing unit dimensions.
+std::vector<uint64_t> torch_shape(const GgufTensor& t) {
+  std::vector<uint64_t> d(t.dims.rbegin(), t.dims.rend());
+  while (d.size() > 1 && d.front() == 1) d.erase(d.begin());
+  return d;
+}
+
+std::string shape_str(const std::vector<uint64_t>& d) {
+  std::string s = "[";
+  for (size_t i = 0; i < d.size(); ++i) s += (i ? ", " : "") + std::to_string(d[i]);
+  return s + "]";
+}
+
+// The encoder of a GGUF file: its jepa.* keys as hyper-parameters, checked as the pages' loader
+// checks them, and its tensors against those hyper-parameters (presence, dtype, shape).
+jepa_status gguf_encoder(const GgufFile& g, jepa_hparams* hp, bool* qkv_fused) {
+  std::string s;
+  jepa_status st = gguf_str(g, "general.architecture", true, "", &s);
+  if (st != JEPA_OK) return st;
+  if (s != "jepa") return fail(JEPA_E_INVALID_ARG, "gguf: general.architecture is '%s', not jepa", s.c_str());
+  std::string family;
+  if ((st = gguf_str(g, "jepa.family", true, "", &family)) != JEPA_OK) return st;
+  const char* families[] = {"ijepa", "vjepa", "vjepa2", "vjepa2_1", "levjepa", "hfvit", "lewm"};
+  bool known = false;
+  for (const char* f : families) known |= family == f;
+  if (!known) return fail(JEPA_E_INVALID_ARG, "gguf: jepa.family '%s' is not one of the seven families", family.c_str());
+  if (family == "lewm") return fail(JEPA_E_UNSUPPORTED, "gguf: family lewm (its projector is not built here)");
+  jepa_hparams h;
+  memset(&h, 0, sizeof h);
+  struct IntKey { const char* key; int64_t lo, hi; int32_t* dst; };
+  const IntKey ints[] = {
+      {"jepa.enc.embed_dim", 1, 65536, &h.embed_dim},   {"jepa.enc.n_layer", 1, 1024, &h.n_layer},
+      {"jepa.enc.n_head", 1, 1024, &h.n_head},          {"jepa.enc.ffn_dim", 1, 1 << 20, &h.ffn_dim},
+      {"jepa.enc.patch_size", 1, 1024, &h.patch_size},  {"jepa.enc.tubelet_size", 1, 1024, &h.tubelet_size},
+      {"jepa.enc.img_size", 1, 65536, &h.img_size},     {"jepa.enc.n_frames", 1, 65536, &h.n_frames},
+      {"jepa.enc.in_chans", 1, 1024, &h.in_chans}};
+  for (const auto& k : ints)
+    if ((st = gguf_int(g, k.key, true, k.lo, k.hi, 0, k.dst)) != JEPA_OK) return st;
+  if ((st = gguf_float(g, "jepa.enc.ln_eps", true, 0.0f, &h.ln_eps)) != JEPA_OK) return st;
+  std::string act, pos, layout, mode;
+  if ((st = gguf_str(g, "jepa.enc.act", true, "", &act)) != JEPA_OK) return st;
+  if (act == "gelu_tanh" || act == "silu")
+    return fail(JEPA_E_UNSUPPORTED, "gguf: jepa.enc.act %s (this build runs gelu_erf)", act.c_str());
+  if (act != "gelu_erf") return fail(JEPA_E_INVALID_ARG, "gguf: jepa.enc.act '%s' unknown", act.c_str());
+  if ((st = gguf_str(g, "jepa.enc.pos_type", true, "", &pos)) != JEPA_OK) return st;
+  if (pos == "sincos2d") h.pos_type = JEPA_POS_SINCOS2D;
+  else if (pos == "sincos3d") h.pos_type = JEPA_POS_SINCOS3D;
+  else if (pos == "learned") h.pos_type = JEPA_POS_LEARNED;
+  else if (pos == "rope3d") h.pos_type = JEPA_POS_ROPE3D;
+  else return fail(JEPA_E_INVALID_ARG, "gguf: jepa.enc.pos_type '%s' unknown", pos.c_str());
+  // the pages: attn_mode is absent from every existing file and the loader defaults it to full
+  if ((st = gguf_str(g, "jepa.enc.attn_mode", false, "full", &mode)) != JEPA_OK) return st;
+  if (mode == "block_causal") {
+    if (family != "levjepa")
+      return fail(JEPA_E_INVALID_ARG, "gguf: attn_mode block_causal on family %s, whose graph has no mask", family.c_str());
+    h.attn_mode = JEPA_ATTN_BLOCK_CAUSAL;
+  } else if (mode != "full") {
+    return fail(JEPA_E_INVALID_ARG, "gguf: jepa.enc.attn_mode '%s' unknown", mode.c_str());
+  }
+  bool interp = false, cls = false, fused = false, mod = false, ls = false;
+  if ((st = gguf_bool(g, "jepa.enc.cls_token", &cls)) != JEPA_OK) return st;
+  if ((st = gguf_bool(g, "jepa.enc.modality_embed", &mod)) != JEPA_OK) return st;
+  if ((st = gguf_bool(g, "jepa.enc.layer_scale", &ls)) != JEPA_OK) return st;
+  if (ls) return fail(JEPA_E_UNSUPPORTED, "gguf: layer scale (ls1 / ls2) is not built here");
+  fused = true;
+  if (g.get("jepa.enc.qkv_fused") && (st = gguf_bool(g, "jepa.enc.qkv_fused", &fused)) != JEPA_OK) return st;
+  int32_t n_reg = 0;
+  if ((st = gguf_int(g, "jepa.enc.n_registers", false, 0, 1 << 16, 0, &n_reg)) != JEPA_OK) return st;
+  if (n_reg) return fail(JEPA_E_UNSUPPORTED, "gguf: %d register tokens (not built here)", n_reg);
+  h.cls_token = cls;
+  h.modality_embed = mod;
+  if (h.pos_type == JEPA_POS_ROPE3D) {
+    if ((st = gguf_float(g, "jepa.enc.rope_theta", true, 0.0f, &h.rope_theta)) != JEPA_OK) return st;
+    if ((st = gguf_str(g, "jepa.enc.rope_freq_layout", true, "", &layout)) != JEPA_OK) return st;
+    if (layout == "tiled") h.rope_layout = JEPA_ROPE_TILED;
+    else if (layout == "interleaved") h.rope_layout = JEPA_ROPE_INTERLEAVED;
+    else return fail(JEPA_E_INVALID_ARG, "gguf: jepa.enc.rope_freq_layout '%s' unknown", layout.c_str());
+    if ((st = gguf_bool(g, "jepa.enc.rope_interpolate", &interp)) != JEPA_OK) return st;
+    h.rope_interpolate = interp;
+    if ((st = gguf_int(g, "jepa.enc.rope_ref_grid", false, 0, 65536, 0, &h.rope_ref_grid)) != JEPA_OK) return st;
+  } else {
+    h.rope_theta = 10000.0f;  // unused without RoPE
+  }
+  if (h.pos_type == JEPA_POS_LEARNED) {  // the table's rows come from the tensor itself
+    const GgufTensor* t = g.find("enc.pos_embed");
+    if (!t) return fail(JEPA_E_INVALID_ARG, "gguf: required tensor enc.pos_embed is missing");
+    const std::vector<uint64_t> d = torch_shape(*t);
+    if (d.size() != 2 || d[0] > (1u << 22))
+      return fail(JEPA_E_INVALID_ARG, "gguf: enc.pos_embed has shape %s", shape_str(d).c_str());
+    h.n_pos_rows = (int32_t)d[0];
+  }
+  if ((st = jepa_hparams_validate(&h)) != JEPA_OK) return st;
+  // tensors: present, f32 for every operand the graph adds, a float type for the matrices, shapes
+  std::vector<TensorRec> want = encoder_tensors(h, false, false);
+  if (!fused) {  // separate q / k / v projections, fused at load
+    std::vector<TensorRec> w2;
+    for (const auto& t : want) {
+      const size_t at = t.name.find("attn_qkv.");
+      if (at == std::string::npos) {
+        w2.push_back(t);
+        continue;
+      }
+      const bool weight = t.name.compare(at + 9, std::string::npos, "weight") == 0;
+      for (const char* part : {"attn_q.", "attn_k.", "attn_v."}) {
+        TensorRec r = t;
+        r.name = t.name.substr(0, at) + part + (weight ? "weight" : "bias");
+        r.shape = weight ? std::vector<uint64_t>{(uint64_t)h.embed_dim, (uint64_t)h.embed_dim}
+                         : std::vector<uint64_t>{(uint64_t)h.embed_dim};
+        r.n = t.n / 3;
+        w2.push_back(r);
+      }
+    }
+    want.swap(w2);
+  }
+  for (const auto& t : want) {
+    const GgufTensor* gt = g.find(t.name);
+    if (!gt) return fail(JEPA_E_INVALID_ARG, "gguf: required tensor %s is missing", t.name.c_str());
+    if (!t.matrix && gt->type != 0)
+      return fail(JEPA_E_INVALID_ARG, "gguf: %s is %s; norms, biases, tokens and tables must be f32", t.name.c_str(),
+                  gguf_type_name(gt->type));
+    if (torch_shape(*gt) != t.shape)
+      return fail(JEPA_E_INVALID_ARG, "gguf: %s has shape %s, the hyper-parameters give %s", t.name.c_str(),
+                  shape_str(torch_shape(*gt)).c_str(), shape_str(t.shape).c_str());
+    if (t.matrix && gt->type != 0 && gt->type != 1 && gt->type != 30)
+      return fail(JEPA_E_UNSUPPORTED, "gguf: %s is %s; this build reads f32, f16 and bf16 weights", t.name.c_str(),
+                  gguf_type_name(gt->type));
+  }
+  *hp = h;
+  *qkv_fused = fused;
+  return JEPA_OK;
+}
+}  // namespace
+
+extern "C" jepa_status jepa_model_load(const jepa_hparams* hp, uint64_t seed, int32_t dtype, int32_t device,
+                                       jepa_model** out) {
+  return model_create(hp, seed, dtype, device, nullptr, out);
+}
+
+extern "C" jepa_status jepa_gguf_hparams(const char* path, jepa_hparams* out) {
+  if (!path || !out) return fail(JEPA_E_INVALID_ARG, "jepa_gguf_hparams: null argument");
+  GgufFile g;
+  jepa_status st = gguf_open(path, &g);
+  if (st != JEPA_OK) return st;
+  bool fused = true;
+  return gguf_encoder(g, out, &fused);
+}
+
+extern "C" jepa_status jepa_model_load_gguf(const char* path, int32_t dtype, int32_t device, jepa_model** out) {
+  if (!path || !out) return fail(JEPA_E_INVALID_ARG, "jepa_model_load_gguf: null argument");
+  *out = nullptr;
+  GgufFile g;
+  jepa_status st = gguf_open(path, &g);
+  if (st != JEPA_OK) return st;
+  jepa_hparams hp;
+  bool fused = true;
+  if ((st = gguf_encoder(g, &hp, &fused)) != JEPA_OK) return st;
+  const TensorFill fill = [&](const TensorRec& t, float* dst) -> jepa_status {
+    const size_t at = t.name.find("attn_qkv.");
+    if (fused || at == std::string::npos) return gguf_read_f32(g, *g.find(t.name), dst);
+    const bool weight = t.name.compare(at + 9, std::string::npos, "weight") == 0;
+    const size_t part = t.n / 3;  // rows [q; k; v]
+    const char* names[3] = {"attn_q.", "attn_k.", "attn_v."};
+    for (int i = 0; i < 3; ++i) {
+      const std::string n = t.name.substr(0, at) + names[i] + (weight ? "weight" : "bias");
+      const jepa_status s2 = gguf_read_f32(g, *g.find(n), dst + i * part);
+      if (s2 != JEPA_OK) return s2;
+    }
+    return JEPA_OK;
+  };
+  return model_create(&hp, 0, dtype, device, &fill, out);
 }
 
 extern "C" void jepa_model_free(jepa_model* m) {
