@@ -10,8 +10,9 @@
 //   ln2 LN -> MLP up (GELU) -> MLP down (+ residual) = pooled -> classifier -> logits
 //
 // After the self-attention layers everything works on one row per item: those steps run on
-// small SIMT kernels (a warp per output feature; the weights are read once), in fp32 with bf16
-// weights.
+// small SIMT kernels (a warp per output feature, the rows staged in shared memory, so the weights
+// and the rows are read once per CTA), in fp32 with bf16 weights; the cross attention splits each
+// item's keys over CTAs and merges their partial softmax sums.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -43,50 +44,69 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 w, float (&f)[8]) {
   }
 }
 
-// y[r, n] = act(sum_k x[r, k] W[n, k] + b[n]) (+ res[r, n]) for the R rows of x, one warp per output
-// feature n (grid-stride), the rows in groups of 8. x fp32 [R, K], W bf16 [N, K], K % 8 == 0; res may
-// be y itself (each element is read and written by the same lane).
+// y[r, n] = act(sum_k x[r, k] W[n, k] + b[n]) (+ res[r, n]) for the R rows of x: a CTA of 8 warps
+// takes 8 output features (warp w: feature n0 + w) and stages x in shared memory, 8 rows by 1024
+// columns at a time, so each weight row is read once and x once per CTA. x fp32 [R, K], W bf16
+// [N, K], K % 8 == 0; res may be y itself (each element is read and written by the same lane).
+constexpr int kRvWarps = 8, kRvRows = 8, kRvChunk = 1024;
 template <bool GELU>
-__global__ void rowvec_linear_kernel(const float* __restrict__ x, int R, int K, const __nv_bfloat16* __restrict__ W,
-                                     int N, const float* __restrict__ bias, const float* res, float* y) {
+__global__ void __launch_bounds__(32 * kRvWarps) rowvec_linear_kernel(const float* __restrict__ x, int R, int K,
+                                                                      const __nv_bfloat16* __restrict__ W, int N,
+                                                                      const float* __restrict__ bias, const float* res,
+                                                                      float* y) {
   pdl_trigger();
   pdl_wait();
-  const int lane = threadIdx.x & 31;
-  const int warps = (int)((gridDim.x * blockDim.x) >> 5);
-  for (int n = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5); n < N; n += warps) {
-    const __nv_bfloat16* w = W + (size_t)n * K;
-    for (int r0 = 0; r0 < R; r0 += 8) {
-      float acc[8];
+  __shared__ __align__(16) float xs[kRvRows][kRvChunk];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int n0 = blockIdx.x * kRvWarps; n0 < N; n0 += gridDim.x * kRvWarps) {  // uniform across the CTA
+    const int n = n0 + warp;
+    for (int r0 = 0; r0 < R; r0 += kRvRows) {
+      const int rows = min(kRvRows, R - r0);
+      float acc[kRvRows];
 #pragma unroll
-      for (int r = 0; r < 8; ++r) acc[r] = 0.0f;
-      for (int k = lane * 8; k < K; k += 256) {
-        float wf[8];
-        bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(w + k)), wf);
+      for (int r = 0; r < kRvRows; ++r) acc[r] = 0.0f;
+      for (int k0 = 0; k0 < K; k0 += kRvChunk) {
+        const int kc = min(kRvChunk, K - k0), kc4 = kc / 4;
+        __syncthreads();  // the previous chunk is no longer read
+        for (int i = threadIdx.x; i < rows * kc4; i += blockDim.x) {
+          const int r = i / kc4, c4 = i - r * kc4;
+          reinterpret_cast<float4*>(xs[r])[c4] = __ldg(reinterpret_cast<const float4*>(x + (size_t)(r0 + r) * K + k0) + c4);
+        }
+        __syncthreads();
+        if (n < N) {
+          const __nv_bfloat16* w = W + (size_t)n * K + k0;
+#pragma unroll 4  // several weight loads in flight per warp (one CTA per SM: latency-bound otherwise)
+          for (int k = lane * 8; k < kc; k += 256) {
+            float wf[8];
+            bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(w + k)), wf);
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
-          if (r0 + r < R) {
-            const float4* xr = reinterpret_cast<const float4*>(x + (size_t)(r0 + r) * K + k);
-            const float4 a = __ldg(xr), c = __ldg(xr + 1);
-            acc[r] = fmaf(a.x, wf[0], acc[r]);
-            acc[r] = fmaf(a.y, wf[1], acc[r]);
-            acc[r] = fmaf(a.z, wf[2], acc[r]);
-            acc[r] = fmaf(a.w, wf[3], acc[r]);
-            acc[r] = fmaf(c.x, wf[4], acc[r]);
-            acc[r] = fmaf(c.y, wf[5], acc[r]);
-            acc[r] = fmaf(c.z, wf[6], acc[r]);
-            acc[r] = fmaf(c.w, wf[7], acc[r]);
+            for (int r = 0; r < kRvRows; ++r) {
+              if (r < rows) {
+                const float4 a = *reinterpret_cast<const float4*>(&xs[r][k]);
+                const float4 c = *reinterpret_cast<const float4*>(&xs[r][k + 4]);
+                float t = acc[r];
+                t = fmaf(a.x, wf[0], t);
+                t = fmaf(a.y, wf[1], t);
+                t = fmaf(a.z, wf[2], t);
+                t = fmaf(a.w, wf[3], t);
+                t = fmaf(c.x, wf[4], t);
+                t = fmaf(c.y, wf[5], t);
+                t = fmaf(c.z, wf[6], t);
+                acc[r] = fmaf(c.w, wf[7], t);
+              }
+            }
           }
         }
       }
 #pragma unroll
-      for (int r = 0; r < 8; ++r)
+      for (int r = 0; r < kRvRows; ++r)
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], o);
-      if (lane == 0) {
+      if (lane == 0 && n < N) {
         const float bn = __ldg(bias + n);
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
-          if (r0 + r < R) {
+        for (int r = 0; r < kRvRows; ++r) {
+          if (r < rows) {
             float v = acc[r] + bn;
             if (GELU) v = gelu_erf(v);
             if (res) v += res[(size_t)(r0 + r) * N + n];
@@ -98,76 +118,98 @@ __global__ void rowvec_linear_kernel(const float* __restrict__ x, int R, int K, 
   }
 }
 
-// Cross attention of one query row per head over the N tokens of one item: CTA (h, b). q fp32 [D]
-// (projected query), kv bf16 [B*N, 2D] (keys in columns [0, D), values in [D, 2D)), hd in {32, 64,
-// 128}. out[b, h*hd + d] = query[h*hd + d] + o[d] (no output projection: the raw query is the
-// residual). Scores in shared memory: N floats.
-constexpr int kXThreads = 256;
-__global__ void xattn_kernel(const float* __restrict__ q, const float* __restrict__ query,
-                             const __nv_bfloat16* __restrict__ kv, int N, int D, int hd, float* __restrict__ out) {
+// Cross attention of one query row per head over the N tokens of each item, in two kernels. Part:
+// CTA (h, b, s) takes keys [256 s, 256 s + 256) of item b: scores (eight lanes per key row, 16
+// bytes each, so a warp reads four whole rows per load), their max m, p = exp(score - m), the sum
+// l and o = sum p v; it writes (m, l, o[hd]). Combine: CTA (h, b) merges the S parts,
+// O = sum_s o_s exp(m_s - M) / sum_s l_s exp(m_s - M) with M = max_s m_s, and writes
+// out[b, h*hd + d] = query[h*hd + d] + O[d] (no output projection: the raw query is the residual).
+// q fp32 [D] (projected query), kv bf16 [B*N, 2D] (keys in columns [0, D), values in [D, 2D)),
+// hd in {32, 64, 128}.
+constexpr int kXThreads = 256, kXKeys = 256;
+__global__ void __launch_bounds__(kXThreads) xattn_part_kernel(const float* __restrict__ q,
+                                                               const __nv_bfloat16* __restrict__ kv, int N, int D,
+                                                               int hd, float* __restrict__ part) {
   pdl_trigger();
   pdl_wait();
-  extern __shared__ float sm[];
-  float* s = sm;                       // [N] scores, then probabilities
-  float* qh = sm + N;                  // [hd] scaled query of this head
-  float* red = qh + 128;               // [kXThreads] reductions and partial outputs
-  const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const float scale = rsqrtf((float)hd);
-  if (tid < hd) qh[tid] = q[h * hd + tid] * scale;
+  __shared__ float qh[128];
+  __shared__ float sc[kXKeys];
+  __shared__ float red[kXThreads];
+  const int h = blockIdx.x, b = blockIdx.y, sidx = blockIdx.z, S = gridDim.z;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int j0 = sidx * kXKeys, cnt = min(kXKeys, N - j0);
+  if (tid < hd) qh[tid] = q[h * hd + tid] * rsqrtf((float)hd);
   __syncthreads();
-  const __nv_bfloat16* base = kv + (size_t)b * N * 2 * D + (size_t)h * hd;
-  float mx = -INFINITY;
-  for (int j = tid; j < N; j += kXThreads) {
-    const uint4* kr = reinterpret_cast<const uint4*>(base + (size_t)j * 2 * D);
+  const __nv_bfloat16* base = kv + ((size_t)b * N + j0) * 2 * D + (size_t)h * hd;
+  const int c = lane & 7;  // 16-byte chunk of the row: dims [8c, 8c + 8) (+ 64 for hd 128)
+  for (int j = warp * 4 + (lane >> 3); j < kXKeys; j += kXThreads / 8) {
     float acc = 0.0f;
-    for (int c = 0; c < hd; c += 8) {
-      float kf[8];
-      bf16x8_to_f32(__ldg(kr + c / 8), kf);
+    if (j < cnt) {
+      const uint4* kr = reinterpret_cast<const uint4*>(base + (size_t)j * 2 * D);
+      for (int cc = c; cc * 8 < hd; cc += 8) {
+        float kf[8];
+        bf16x8_to_f32(__ldg(kr + cc), kf);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) acc = fmaf(qh[c + e], kf[e], acc);
+        for (int e = 0; e < 8; ++e) acc = fmaf(qh[cc * 8 + e], kf[e], acc);
+      }
     }
-    s[j] = acc;
-    mx = fmaxf(mx, acc);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+    if (c == 0) sc[j] = j < cnt ? acc : -INFINITY;
   }
+  __syncthreads();
+  // max, then p = exp(s - m) and its sum, over the 256 slots (one per thread)
+  float v = sc[tid], mx = v;
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
   if (lane == 0) red[warp] = mx;
   __syncthreads();
-  if (tid < 32) {
-    float m = tid < kXThreads / 32 ? red[tid] : -INFINITY;
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (tid == 0) red[32] = m;
-  }
-  __syncthreads();
-  const float m = red[32];
-  float sum = 0.0f;
-  for (int j = tid; j < N; j += kXThreads) {
-    const float p = expf(s[j] - m);
-    s[j] = p;
-    sum += p;
-  }
+  float m = red[0];
+  for (int w = 1; w < kXThreads / 32; ++w) m = fmaxf(m, red[w]);
+  const float p = tid < cnt ? expf(v - m) : 0.0f;
+  float sum = p;
   for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-  __syncthreads();  // red[32] read by every thread above before the slots are reused
+  __syncthreads();  // red[] read by every thread above before it is reused
+  sc[tid] = p;
   if (lane == 0) red[warp] = sum;
   __syncthreads();
-  if (tid < 32) {
-    float t = tid < kXThreads / 32 ? red[tid] : 0.0f;
-    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-    if (tid == 0) red[32] = t;
-  }
+  float l = 0.0f;
+  for (int w = 0; w < kXThreads / 32; ++w) l += red[w];
   __syncthreads();
-  const float inv = 1.0f / red[32];
-  __syncthreads();
-  // P V: thread (g, d) sums the keys j = g mod G for value dim d; the G partials are then added
-  const int G = kXThreads / hd, g = tid / hd, d = tid % hd;
+  // o = sum p v: thread (g, d) takes keys g, g + G, ... for value dim d (a row's dims are adjacent)
+  const int G = kXThreads / hd, g = tid / hd, d = tid - g * hd;
   float acc = 0.0f;
-  for (int j = g; j < N; j += G) acc = fmaf(s[j], __bfloat162float(base[(size_t)j * 2 * D + D + d]), acc);
+  for (int j = g; j < cnt; j += G) acc = fmaf(sc[j], __bfloat162float(base[(size_t)j * 2 * D + D + d]), acc);
   red[tid] = acc;
   __syncthreads();
+  float* out = part + (((size_t)b * gridDim.x + h) * S + sidx) * (hd + 2);
   if (tid < hd) {
     float o = 0.0f;
     for (int k = 0; k < G; ++k) o += red[k * hd + tid];
-    out[(size_t)b * D + h * hd + tid] = query[h * hd + tid] + o * inv;
+    out[2 + tid] = o;
   }
+  if (tid == 0) {
+    out[0] = m;
+    out[1] = l;
+  }
+}
+
+__global__ void xattn_combine_kernel(const float* __restrict__ part, int S, int hd, int D,
+                                     const float* __restrict__ query, float* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
+  const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
+  const float* pp = part + ((size_t)b * gridDim.x + h) * S * (hd + 2);
+  float M = -INFINITY;
+  for (int s = 0; s < S; ++s) M = fmaxf(M, pp[(size_t)s * (hd + 2)]);
+  float L = 0.0f, O = 0.0f;
+  for (int s = 0; s < S; ++s) {
+    const float* ps = pp + (size_t)s * (hd + 2);
+    const float w = expf(ps[0] - M);
+    L = fmaf(ps[1], w, L);
+    O = fmaf(ps[2 + d], w, O);
+  }
+  out[(size_t)b * D + h * hd + d] = query[h * hd + d] + O / L;
 }
 
 // out[b, :] = mean of rows [prefix, N) of item b (mode 0) or row 0 (mode 1); CTA (column block of
@@ -218,26 +260,16 @@ int blocks_for(long long work, int threads) {
 
 cudaError_t rowvec_launch(const float* x, int R, int K, const void* W, int N, const float* bias, const float* res,
                           float* y, bool gelu, cudaStream_t s) {
-  const int warps_per_block = 8;
-  const int grid = std::max(1, std::min((N + warps_per_block - 1) / warps_per_block, num_sms() * 8));
+  const int grid = std::max(1, std::min((N + kRvWarps - 1) / kRvWarps, num_sms() * 8));
   const __nv_bfloat16* w = reinterpret_cast<const __nv_bfloat16*>(W);
-  return gelu ? launch_kernel(rowvec_linear_kernel<true>, dim3(grid), dim3(32 * warps_per_block), 0, s, x, R, K, w, N,
-                              bias, res, y)
-              : launch_kernel(rowvec_linear_kernel<false>, dim3(grid), dim3(32 * warps_per_block), 0, s, x, R, K, w, N,
-                              bias, res, y);
+  return gelu ? launch_kernel(rowvec_linear_kernel<true>, dim3(grid), dim3(32 * kRvWarps), 0, s, x, R, K, w, N, bias,
+                              res, y)
+              : launch_kernel(rowvec_linear_kernel<false>, dim3(grid), dim3(32 * kRvWarps), 0, s, x, R, K, w, N, bias,
+                              res, y);
 }
 
 constexpr int kXMaxTokens = 32768;
-size_t xattn_smem(int N) { return ((size_t)N + 128 + kXThreads) * sizeof(float); }
-
-cudaError_t head_kernels_init() {
-  static std::once_flag once;
-  static cudaError_t result = cudaSuccess;
-  std::call_once(once, [] {
-    result = cudaFuncSetAttribute(xattn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)xattn_smem(kXMaxTokens));
-  });
-  return result;
-}
+int xattn_splits(int N) { return (N + kXKeys - 1) / kXKeys; }
 
 struct Rec {
   std::string name;
@@ -281,7 +313,7 @@ struct jepa_head_context {
   int max_B = 0, max_N = 0;
   uint8_t* ws = nullptr;
   size_t ws_bytes = 0;
-  float *X = nullptr, *qv = nullptr, *x1 = nullptr, *y = nullptr, *u = nullptr, *pooled = nullptr;
+  float *X = nullptr, *qv = nullptr, *x1 = nullptr, *y = nullptr, *u = nullptr, *pooled = nullptr, *part = nullptr;
   void *Xn = nullptr, *qkv = nullptr, *ao = nullptr, *Hh = nullptr;
   int* err = nullptr;
   int kB = -1, kN = -1;
@@ -495,7 +527,9 @@ size_t head_ws_layout(const jepa_head* h, long long B, long long N, jepa_head_co
   const size_t oX = take(blocks ? rows * D * 4 : 0), oXn = take(rows * D * 2), oQ = take(rows * 3 * D * 2),
                oA = take(blocks ? rows * D * 2 : 0), oH = take(blocks ? rows * F * 2 : 0), oq = take(D * 4),
                o1 = take((size_t)B * D * 4), oy = take((size_t)B * D * 4), ou = take((size_t)B * F * 4),
-               op = take((size_t)B * D * 4), oE = take(sizeof(int));
+               op = take((size_t)B * D * 4),
+               oP = take((size_t)B * h->hp.n_head * xattn_splits((int)N) * (D / h->hp.n_head + 2) * 4),
+               oE = take(sizeof(int));
   if (c) {
     c->X = reinterpret_cast<float*>(c->ws + oX);
     c->Xn = c->ws + oXn;
@@ -507,14 +541,15 @@ size_t head_ws_layout(const jepa_head* h, long long B, long long N, jepa_head_co
     c->y = reinterpret_cast<float*>(c->ws + oy);
     c->u = reinterpret_cast<float*>(c->ws + ou);
     c->pooled = reinterpret_cast<float*>(c->ws + op);
+    c->part = reinterpret_cast<float*>(c->ws + oP);
     c->err = reinterpret_cast<int*>(c->ws + oE);
   }
   return off;
 }
 
-// kernels of one forward: 7 per pooler layer; ln_kv, K|V GEMM, query, cross attention, ln2, up, down;
+// kernels of one forward: 7 per pooler layer; ln_kv, K|V GEMM, query, cross attention (two), ln2, up, down;
 // the classifier when logits are asked for (the token copy before the layers is not a kernel)
-int head_launches(const jepa_head_hparams& hp, bool logits) { return 7 * hp.n_pool_layers + 7 + (logits ? 1 : 0); }
+int head_launches(const jepa_head_hparams& hp, bool logits) { return 7 * hp.n_pool_layers + 8 + (logits ? 1 : 0); }
 }  // namespace
 
 extern "C" jepa_status jepa_head_context_new(const jepa_head* h, int32_t max_batch, int32_t max_tokens,
@@ -531,7 +566,6 @@ extern "C" jepa_status jepa_head_context_new(const jepa_head* h, int32_t max_bat
                 max_batch, max_tokens, budget);
   CUDA_TRY(cudaSetDevice(h->device));
   CUDA_TRY(tc_kernels_init());
-  CUDA_TRY(head_kernels_init());
   jepa_head_context* c = new jepa_head_context();
   c->h = h;
   c->max_B = max_batch;
@@ -686,9 +720,14 @@ jepa_status head_launch(jepa_head_context* c, const float* tokens, int B, int N,
   }));
   CUDA_TRY(timed(kHQuery, 2.0 * dD * dD, dD * dD * 2.0,
                  [&] { return rowvec_launch(h->query, 1, D, h->w_q, D, h->b_q, nullptr, c->qv, false, s); }));
+  const int S = xattn_splits(N);
   CUDA_TRY(timed(kHXattn, 4.0 * dD * B * N, (double)M * 2 * D * 2.0, [&] {
-    return launch_kernel(xattn_kernel, dim3(NH, B), dim3(kXThreads), xattn_smem(N), s, (const float*)c->qv, h->query,
-                         reinterpret_cast<const __nv_bfloat16*>(c->qkv), N, D, hd, c->x1);
+    return launch_kernel(xattn_part_kernel, dim3(NH, B, S), dim3(kXThreads), 0, s, (const float*)c->qv,
+                         reinterpret_cast<const __nv_bfloat16*>(c->qkv), N, D, hd, c->part);
+  }));
+  CUDA_TRY(timed(kHXattn, 0.0, (double)B * NH * S * (hd + 2) * 4.0, [&] {
+    return launch_kernel(xattn_combine_kernel, dim3(NH, B), dim3(hd), 0, s, (const float*)c->part, S, hd, D, h->query,
+                         c->x1);
   }));
   CUDA_TRY(timed(kHLn2, 0.0, (double)B * D * 8.0,
                  [&] { return layernorm_launch(c->x1, B, D, h->l2_w, h->l2_b, hp.ln_eps, false, c->y, s); }));
