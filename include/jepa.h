@@ -257,11 +257,8 @@ typedef struct {
   const float* d_pos;         /* [rows_per_item, N] learned table (rows = [prefix; patches]) or NULL */
   const float* d_vec;         /* [N] vector added to every patch row (modality) or NULL */
   /* QKV_ROPE, optional: d_rope_ids [M] gives every row's patch index (its position in d_rope's
-   * grid) in place of its place in its item (token sequences that are not the grid in order);
-   * qkv_pad64 (bf16, head_dim 32 only) stores head h of q, k and v at columns 64h .. 64h+31 of
-   * a [M, 3*n_head*64] output whose other columns the caller keeps at zero. */
+   * grid) in place of its place in its item (token sequences that are not the grid in order). */
   const int32_t* d_rope_ids;
-  int32_t qkv_pad64;
 } jepa_epilogue;
 
 /* out = epilogue(x w^T): d_x [M, K], d_w [N, K] (PyTorch Linear layout), both fp32 (dtype
@@ -303,10 +300,7 @@ jepa_status jepa_op_pos_resize(const float* d_src, int32_t st, int32_t sh, int32
 /* Softmax attention per (item, head): o = softmax(q k^T / sqrt(head_dim) + mask) v.
  * d_qkv: [B*N, 3*n_head*head_dim] ([q | k | v] columns, heads contiguous), d_out: [B*N, n_head*head_dim];
  * fp32 (dtype JEPA_FP32) or bf16 (JEPA_BF16: tcgen05 flash kernel); head_dim 64.
- * bf16 also takes head_dim 32 (the masked predictor's heads) in a zero-padded layout: d_qkv is
- * [B*N, 3*n_head*64] with head h of q, k and v in columns 64h .. 64h+31 of its third and zeros in
- * 64h+32 .. 64h+63 (the layout a QKV_ROPE epilogue with qkv_pad64 writes); d_out stays compact,
- * [B*N, n_head*32]; the scale is 1/sqrt(32).
+ * bf16 also takes head_dim 32 (the masked predictor's heads; 64-byte tiles, scale 1/sqrt(32)).
  * attn_mode JEPA_ATTN_BLOCK_CAUSAL: the first `prefix` rows see every key, prefix columns are
  * closed to the other rows, and patch key j is visible to patch query i iff
  * (i - prefix) / frame_tokens >= (j - prefix) / frame_tokens. */

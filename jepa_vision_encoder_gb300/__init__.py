@@ -496,7 +496,7 @@ class ops:
     def linear(x: torch.Tensor, w: torch.Tensor, bias: torch.Tensor, out: torch.Tensor, kind: int = EPI_BIAS,
                rope: torch.Tensor = None, rows_per_item: int = 1, prefix: int = 0, n_head: int = 0,
                head_dim: int = 0, rope_layout: int = 0, patches_per_item: int = 1, pos: torch.Tensor = None,
-               vec: torch.Tensor = None, rope_ids: torch.Tensor = None, qkv_pad64: bool = False):
+               vec: torch.Tensor = None, rope_ids: torch.Tensor = None):
         M, K = x.shape
         N = w.shape[0]
         code = BF16 if x.dtype == torch.bfloat16 else FP32
@@ -514,7 +514,6 @@ class ops:
         e.d_pos = pos.data_ptr() if pos is not None else None
         e.d_vec = vec.data_ptr() if vec is not None else None
         e.d_rope_ids = rope_ids.data_ptr() if rope_ids is not None else None
-        e.qkv_pad64 = int(qkv_pad64)
         check(lib().jepa_op_linear(code, _ptr(x), M, K, _ptr(w), N, ctypes.byref(e), _stream_ptr()))
         return out
 

@@ -44,7 +44,7 @@ class Epilogue(ctypes.Structure):
         ("d_rope", ctypes.c_void_p), ("rows_per_item", ctypes.c_int32), ("prefix", ctypes.c_int32),
         ("n_head", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("rope_layout", ctypes.c_int32),
         ("patches_per_item", ctypes.c_int32), ("d_pos", ctypes.c_void_p), ("d_vec", ctypes.c_void_p),
-        ("d_rope_ids", ctypes.c_void_p), ("qkv_pad64", ctypes.c_int32),
+        ("d_rope_ids", ctypes.c_void_p),
     ]
 
 

@@ -1,5 +1,6 @@
-// attention_tc.cu -- tcgen05 flash attention for sm_103a, head_dim 64, bf16 in / bf16 out,
-// fp32 softmax and accumulation: o = softmax(q k^T / sqrt(64) + mask) v per (item, head)
+// attention_tc.cu -- tcgen05 flash attention for sm_103a, head_dim 64 (or 32: the masked
+// predictor's heads, in 64-byte-swizzled tiles), bf16 in / bf16 out, fp32 softmax and
+// accumulation: o = softmax(q k^T / sqrt(head_dim) + mask) v per (item, head)
 // ("Architecture", Attention and precision; Block-causal attention).
 //
 // One CTA = two tiles of 128 queries (Q0, Q1) of one (item, head), one CTA per SM:
@@ -14,9 +15,9 @@
 //   warp 9      MMA, per key tile j: S_g(j+1) = Q_g K(j+1)^T for both tiles as soon as warpgroup g
 //               has read S_g(j) into registers (so the next scores are ready when its softmax
 //               ends), then O_g += P_g(j) V(j) for both tiles once P_g(j) is in TMEM.
-//               S = Q K^T: M128 N128 K16 x4 (both K-major); O += P V: M128 N64 K16 x8 with P
-//               read from TMEM and V MN-major in shared memory.
-// TMEM (512 columns): S0 [0,128) S1 [128,256) P0 [256,320) P1 [320,384) O0 [384,448) O1 [448,512).
+//               S = Q K^T: M128 N128 K16 x (HD/16) (both K-major); O += P V: M128 N(HD) K16 x8
+//               with P read from TMEM and V MN-major in shared memory.
+// TMEM (512 columns): S0 [0,128) S1 [128,256) P0 [256,320) P1 [320,384) O0, O1 from 384 (HD each).
 // Block-causal: a CTA only visits keys below the last frame its rows can see, and the per-element
 // predicate runs only on tiles that straddle a frame edge, the CLS row/column or N.
 #include <cuda_bf16.h>
@@ -32,19 +33,24 @@ namespace {
 
 constexpr int kQT = 128;  // queries per tile (per softmax warpgroup)
 constexpr int kKT = 128;  // keys per tile
-constexpr int kHD = 64;
-constexpr int kTileBytes = kQT * kHD * 2;  // 16 KB: one 128 x 64 bf16 tile
 constexpr int kKvStages = 3;
-constexpr int kSmemBytes = 1024 + kTileBytes * (2 + 2 * kKvStages) + 256;
+// Per head width HD (64, or 32 for the masked predictor): a 128-row tile of q, k or v is
+// 128 x HD bf16 with HD x 2 bytes per row, stored in the TMA / UMMA swizzle of that row length.
+template <int HD>
+struct Width {
+  static constexpr int kTileBytes = kQT * HD * 2;  // 16 KB (HD 64) or 8 KB (HD 32)
+  static constexpr int kSmemBytes = 1024 + kTileBytes * (2 + 2 * kKvStages) + 256;
+  static constexpr uint32_t kRowBytes = HD * 2;    // 128 or 64: the swizzle span
+};
 constexpr int kThreads = 320;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColP = 256, kColO = 384;  // + 128 / 64 / 64 per tile
+constexpr uint32_t kColS = 0, kColP = 256, kColO = 384;  // + 128 / 64 / HD per tile
 constexpr float kRescaleThreshold = 8.0f;                 // log2 units: p stays below 2^8 between rescales
 
 struct AttnDev {
   int N, H, D;
   int attn_mode, prefix, frame_tokens;
-  int out_hd;  // output columns per head (64, or 32 for zero-padded heads of width 32)
+  int out_hd;  // output columns per head: the head width
   __nv_bfloat16* out;
   float scale_log2;
   int* err;
@@ -70,7 +76,19 @@ __device__ __forceinline__ int keys_needed(const AttnDev& a, int q_begin, int q_
   return min(a.N, a.prefix + ((q_last - a.prefix) / a.frame_tokens + 1) * a.frame_tokens);
 }
 
+// Shared-memory descriptor of a 128 x HD tile: 128-byte swizzle (8-row groups 1024 bytes apart)
+// for HD 64, 64-byte swizzle (groups 512 bytes apart) for HD 32; K-major for q and k, MN-major
+// for v; the leading offset is unused (one swizzle atom across the row).
+template <int HD>
+__device__ __forceinline__ uint64_t tile_desc(uint32_t saddr) {
+  if constexpr (HD == 64) return smem_desc_sw128(saddr, 1024, 1024);
+  else return smem_desc_sw64(saddr, 512, 512);
+}
+
+template <int HD>
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_constant__ CUtensorMap tm, AttnDev a) {
+  constexpr int kHD = HD;
+  constexpr int kTileBytes = Width<HD>::kTileBytes;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
@@ -153,9 +171,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, kHD, 0, 1);
       // descriptors built once; a K step or a stage only moves the start address (the issue
       // loop stays short enough to keep the tensor pipe fed with these small MMAs)
-      const uint64_t q_desc = smem_desc_sw128(smem_u32(sQ), 1024, 1024);
-      const uint64_t k_desc = smem_desc_sw128(smem_u32(sK), 1024, 1024);
-      const uint64_t v_desc = smem_desc_sw128(smem_u32(sV), 1024, 1024);
+      const uint64_t q_desc = tile_desc<HD>(smem_u32(sQ));
+      const uint64_t k_desc = tile_desc<HD>(smem_u32(sK));
+      const uint64_t v_desc = tile_desc<HD>(smem_u32(sV));
       auto issue_s = [&](int g, int st) {
         const uint64_t qd = desc_advance(q_desc, g * kTileBytes), kd = desc_advance(k_desc, st * kTileBytes);
         const uint32_t d = tmem + kColS + g * 128;
@@ -165,10 +183,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       };
       auto issue_pv = [&](int g, int st, int j) {
         const uint64_t vd = desc_advance(v_desc, st * kTileBytes);
-        const uint32_t d = tmem + kColO + g * 64, p = tmem + kColP + g * 64;
+        const uint32_t d = tmem + kColO + g * kHD, p = tmem + kColP + g * 64;
 #pragma unroll
-        for (int k = 0; k < kKT / 16; ++k)
-          mma_ts(d, p + k * 8, desc_advance(vd, k * 2048), idesc_o, (j > 0 || k > 0) ? 1u : 0u);
+        for (int k = 0; k < kKT / 16; ++k)  // 16 keys = 16 rows of V per K step
+          mma_ts(d, p + k * 8, desc_advance(vd, k * 16 * Width<HD>::kRowBytes), idesc_o, (j > 0 || k > 0) ? 1u : 0u);
         mma_commit(smem_u32(o_done + g));
       };
       bool ok = num_kt > 0 && mbar_wait(smem_u32(q_full), 0, wc) && mbar_wait(smem_u32(kv_full), 0, wc);
@@ -218,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const uint32_t tS = tmem + lane_off + kColS + g * 128;
     const uint32_t tP = tmem + lane_off + kColP + g * 64;
-    const uint32_t tO = tmem + lane_off + kColO + g * 64;
+    const uint32_t tO = tmem + lane_off + kColO + g * kHD;
     int lo, hi;
     row_window(a, q, lo, hi);
     const float sc = a.scale_log2;
@@ -269,30 +287,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       const float m_tile = fmax3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3])) * sc;
       float m_new = m_run;
       if (j == 0 || m_tile > m_run + kRescaleThreshold) m_new = fmaxf(m_run, m_tile);
-      if (j > 0) {
-        // O and P of this tile are free once its previous P V has completed
-        if (!mbar_wait(smem_u32(o_done + g), (uint32_t)((j - 1) & 1), wc)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        // The rescale is decided per row, but the TMEM ld/st are warp-collective (.sync.aligned):
-        // the whole warp rescales when any of its rows needs it, the others with alpha = 1.
-        const bool need = m_new > m_run;
-        const float alpha = need ? ex2_approx(m_run - m_new) : 1.0f;
-        l_run *= alpha;
-        if (__any_sync(0xffffffffu, need)) {
-#pragma unroll 1
-          for (int c = 0; c < kHD / 16; ++c) {
-            uint32_t ov[16];
-            tmem_ld16(tO + c * 16, ov);
-            tmem_ld_wait(ov);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-            tmem_st16(tO + c * 16, ov);
-          }
-        }
-      }
+      const bool need = j > 0 && m_new > m_run;  // O (and l) of this row move to the new max
+      const float alpha = need ? ex2_approx(m_run - m_new) : 1.0f;
       m_run = m_new;
       const float base = (m_run == -INFINITY) ? 0.0f : m_run;
       // p = 2^(s*sc - m) two keys at a time, as bf16 pairs into the P columns
@@ -311,6 +307,29 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           pk[c * 16 + (e >> 1)] = pack_bf16x2(p.x, p.y);
         }
       }
+      if (j > 0) {
+        // P and O of this tile are free once its previous P V has completed: the exponentials
+        // above did not need to wait for it, only the P store and the rescale of O do
+        if (!mbar_wait(smem_u32(o_done + g), (uint32_t)((j - 1) & 1), wc)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // The rescale is decided per row, but the TMEM ld/st are warp-collective (.sync.aligned):
+        // the whole warp rescales when any of its rows needs it, the others with alpha = 1.
+        if (__any_sync(0xffffffffu, need)) {
+#pragma unroll 1
+          for (int c = 0; c < kHD / 16; ++c) {
+            uint32_t ov[16];
+            tmem_ld16(tO + c * 16, ov);
+            tmem_ld_wait(ov);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+            tmem_st16(tO + c * 16, ov);
+          }
+        }
+      }
+      l_run *= alpha;
       tmem_st64(tP, pk);
       const float2 l01 = __fadd2_rn(ls2[0], ls2[1]), l23 = __fadd2_rn(ls2[2], ls2[3]);
       l_run += (l01.x + l23.x) + (l01.y + l23.y);
@@ -360,29 +379,35 @@ cudaError_t tc_kernels_init() {
   std::call_once(once, [] {
     result = gemm_tc_init_attributes();
     if (result == cudaSuccess)
-      result = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+      result = cudaFuncSetAttribute(attn_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    Width<64>::kSmemBytes);
+    if (result == cudaSuccess)
+      result = cudaFuncSetAttribute(attn_tc_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    Width<32>::kSmemBytes);
   });
   return result;
 }
 
 cudaError_t attention_tc_launch(const CUtensorMap& tmQKV, const AttnParams& p, int* err, uint64_t limit_ns,
                                 cudaStream_t s) {
-  if (p.head_dim != kHD || (p.real_hd != 64 && p.real_hd != 32)) return cudaErrorInvalidValue;
+  if (p.head_dim != 64 && p.head_dim != 32) return cudaErrorInvalidValue;
   if (p.B <= 0 || p.N <= 0) return cudaSuccess;
   AttnDev a;
   a.N = p.N;
   a.H = p.H;
-  a.D = p.H * kHD;
+  a.D = p.H * p.head_dim;
   a.attn_mode = p.attn_mode;
   a.prefix = p.prefix;
   a.frame_tokens = p.frame_tokens > 0 ? p.frame_tokens : 1;
   a.out = reinterpret_cast<__nv_bfloat16*>(p.out);
-  a.out_hd = p.real_hd;
-  a.scale_log2 = 1.4426950408889634f / sqrtf((float)p.real_hd);  // log2(e) / sqrt(head width)
+  a.out_hd = p.head_dim;
+  a.scale_log2 = 1.4426950408889634f / sqrtf((float)p.head_dim);  // log2(e) / sqrt(head width)
   a.err = err;
   a.limit_ns = limit_ns;
   dim3 grid((p.N + 2 * kQT - 1) / (2 * kQT), p.H, p.B);
-  return launch_kernel(attn_tc_kernel, grid, dim3(kThreads), kSmemBytes, s, tmQKV, a);
+  if (p.head_dim == 32)
+    return launch_kernel(attn_tc_kernel<32>, grid, dim3(kThreads), Width<32>::kSmemBytes, s, tmQKV, a);
+  return launch_kernel(attn_tc_kernel<64>, grid, dim3(kThreads), Width<64>::kSmemBytes, s, tmQKV, a);
 }
 
 }  // namespace jepa

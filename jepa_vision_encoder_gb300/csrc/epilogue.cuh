@@ -30,9 +30,6 @@ struct EpiArgs {
   // optional: the patch position id of every output row m (rope_ids[m]), for token sequences that
   // are not the patch grid in order (the masked predictor's context and target tokens)
   const int* rope_ids;
-  // head_dim 32 only: store each 32-column head at a 64-column pitch (the upper 32 columns of a
-  // head stay as they are: zero), the layout the width-64 attention kernel reads
-  int qkv_pad64;
   // patch embedding: input row m = patch i of item b (i = m % patches_per_item)
   int patches_per_item;
   const float* pos;       // [rows_per_item, N] or null
@@ -380,8 +377,7 @@ __device__ __forceinline__ void epi_chunk_tc(const EpiArgs& a, const CUtensorMap
       uint32_t w[16];
 #pragma unroll
       for (int e = 0; e < 16; ++e) w[e] = pack_bf16x2(v[2 * e], v[2 * e + 1]);
-      // a padded QKV output puts head n0 / 32 (width 32) at column 64 * (n0 / 32)
-      st.put(lane, w, tm_out, (EK == kEpiQkvRope && a.qkv_pad64) ? (n0 >> 5) << 6 : n0, y0, false);
+      st.put(lane, w, tm_out, n0, y0, false);
     }
   }
 }
@@ -471,8 +467,7 @@ __device__ __forceinline__ void rope_hd32_regs(float (&v)[32], const float2 (&cs
 }
 
 // QKV epilogue of a warp for heads of width 32 (every 32-column chunk is one head): the row's 15
-// (cos, sin) values are loaded once per tile, each q / k chunk rotates from registers, and a
-// padded output puts head n0 / 32 at column 64 * (n0 / 32).
+// (cos, sin) values are loaded once per tile and each q / k chunk rotates from registers.
 template <int NCHUNK>
 __device__ __forceinline__ void epi_warp_qkv_hd32(const EpiArgs& a, const CUtensorMap* tm, EpiStage& st, int lane,
                                                   uint32_t trow, int y0, int n_tile0, int half) {
@@ -514,7 +509,7 @@ __device__ __forceinline__ void epi_warp_qkv_hd32(const EpiArgs& a, const CUtens
     uint32_t w[16];
 #pragma unroll
     for (int e = 0; e < 16; ++e) w[e] = pack_bf16x2(v[2 * e], v[2 * e + 1]);
-    st.put(lane, w, tm, a.qkv_pad64 ? (n0 >> 5) << 6 : n0, y0, false);
+    st.put(lane, w, tm, n0, y0, false);
   }
 }
 

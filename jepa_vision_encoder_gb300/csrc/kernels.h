@@ -39,8 +39,10 @@ bool make_tmap_2d_bf16(CUtensorMap* tm, const void* ptr, uint64_t rows, uint64_t
 // GEMM output map: row-major [rows, cols] of bf16 (elem_bytes 2) or fp32 (4), box 32 rows x 64
 // bytes with the 64-byte swizzle (the epilogue's staging layout).
 bool make_tmap_2d_out(CUtensorMap* tm, const void* ptr, uint64_t rows, uint64_t cols, int elem_bytes);
-// 3-D map of a [B][N][cols] bf16 array with box 64 x box_rows x 1 (attention Q/K/V tiles).
-bool make_tmap_3d_bf16(CUtensorMap* tm, const void* ptr, uint64_t B, uint64_t N, uint64_t cols, uint32_t box_rows);
+// 3-D map of a [B][N][cols] bf16 array with box box_cols x box_rows x 1 (attention Q/K/V tiles of
+// one head): box_cols 64 with the 128-byte swizzle, or 32 with the 64-byte swizzle.
+bool make_tmap_3d_bf16(CUtensorMap* tm, const void* ptr, uint64_t B, uint64_t N, uint64_t cols, uint32_t box_rows,
+                       uint32_t box_cols = 64);
 
 int num_sms();
 // Sets the dynamic shared-memory limits of the tcgen05 kernels (once per process; call before
@@ -69,11 +71,7 @@ cudaError_t gemm_simt_launch(const float* A, const float* Bw, const EpiArgs& epi
 struct AttnParams {
   int B, N, H, head_dim;
   int attn_mode, prefix, frame_tokens;
-  void* out;  // [B*N, H*real_hd]
-  // Heads narrower than the kernel's 64 columns arrive zero-padded to 64 (q, k and v of head h at
-  // columns 64h .. 64h+63, the first real_hd of them real): the scores are scaled by
-  // 1/sqrt(real_hd) and only the real_hd output columns of each head are written.
-  int real_hd = 64;
+  void* out;  // [B*N, H*head_dim]
 };
 cudaError_t attention_tc_launch(const CUtensorMap& tmQKV, const AttnParams& p, int* err, uint64_t limit_ns,
                                 cudaStream_t s);

@@ -4,8 +4,8 @@
 //
 //   ids (checked)  ->  gather the context rows of the encoder output (bf16)
 //   -> pred.embed GEMM (+bias) into rows [0, n_ctx) of each item  ->  mask token into the target rows
-//   per layer: LN1 -> QKV GEMM (+bias, 3-D RoPE at the ids' positions; head_dim 32 stored at a
-//              64-column pitch) -> attention (the width-64 kernel on the zero-padded heads)
+//   per layer: LN1 -> QKV GEMM (+bias, 3-D RoPE at the ids' positions) -> attention (head_dim
+//              32 in 64-byte-swizzled tiles)
 //              -> out GEMM (+bias, +=X) -> LN2 -> up GEMM (+bias, GELU) -> down GEMM (+bias, +=X)
 //   pred.norm LN -> gather the target rows -> pred.proj GEMM (+bias) -> [B, n_tgt, out_dim] fp32
 //
@@ -355,11 +355,8 @@ extern "C" jepa_status jepa_pred_tensor(const jepa_predictor* p, const char* nam
 
 // ------------------------------------------------------------------ context
 namespace {
-// qkv columns of the workspace: width-32 heads take 64 columns each (zero-padded).
-int qkv_cols(const jepa_pred_hparams& hp) {
-  const int hd = hp.embed_dim / hp.n_head;
-  return hd == 32 ? 3 * hp.n_head * 64 : 3 * hp.embed_dim;
-}
+// qkv columns of the workspace: [q | k | v], n_head heads of head_dim each.
+int qkv_cols(const jepa_pred_hparams& hp) { return 3 * hp.embed_dim; }
 
 size_t pred_ws_layout(const jepa_predictor* p, long long B, long long n_ctx, long long n_tgt, int rope_rows,
                       jepa_pred_context* c) {
@@ -419,7 +416,6 @@ extern "C" jepa_status jepa_pred_context_new(const jepa_predictor* p, int32_t ma
   }
   c->ws_bytes = need;
   pred_ws_layout(p, max_batch, max_ctx, max_tgt, kMaxRopeRows, c);
-  // the padded head columns of qkv are never written: they stay zero from here on
   e = cudaMemset(c->ws, 0, need);
   if (e != cudaSuccess) {
     cudaFree(c->ws);
@@ -480,7 +476,7 @@ jepa_status pred_prepare(jepa_pred_context* c, int B, int n_ctx, int n_tgt, int 
   ok &= make_tmap_2d_bf16(&c->tm_ao, c->ao, M, P, 128);
   ok &= make_tmap_2d_bf16(&c->tm_Hh, c->Hh, M, F, 128);
   ok &= make_tmap_2d_bf16(&c->tm_Y, c->Y, Mt, P, 128);
-  ok &= make_tmap_3d_bf16(&c->tm_qkv3, c->qkv, B, n_ctx + n_tgt, qkv_cols(hp), 128);
+  ok &= make_tmap_3d_bf16(&c->tm_qkv3, c->qkv, B, n_ctx + n_tgt, qkv_cols(hp), 128, hp.embed_dim / hp.n_head);
   ok &= make_tmap_2d_out(&c->tm_o_qkv, c->qkv, M, qkv_cols(hp), 2);
   ok &= make_tmap_2d_out(&c->tm_o_hh, c->Hh, M, F, 2);
   ok &= make_tmap_2d_out(&c->tm_o_x, c->X, M, P, 4);
@@ -556,8 +552,7 @@ jepa_status pred_launch(jepa_pred_context* c, const float* enc, int B, int n_enc
   ap.B = B;
   ap.N = n_total;
   ap.H = NH;
-  ap.head_dim = 64;
-  ap.real_hd = hd;
+  ap.head_dim = hd;  // width-32 heads in their own 64-byte tiles
   ap.attn_mode = 0;
   ap.prefix = 0;
   ap.frame_tokens = 1;
@@ -576,7 +571,6 @@ jepa_status pred_launch(jepa_pred_context* c, const float* enc, int B, int n_enc
     qe.rope_gh = gh;
     qe.rope_gw = gw;
     qe.rope_ids = c->ids;
-    qe.qkv_pad64 = hd == 32 ? 1 : 0;
     EpiArgs oe = epi_of(kEpiResidual, M, P, w.b_out, c->X);
     EpiArgs ue = epi_of(kEpiGelu, M, F, w.b_up, c->Hh);
     EpiArgs de = epi_of(kEpiResidual, M, P, w.b_down, c->X);

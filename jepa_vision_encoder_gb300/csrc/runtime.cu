@@ -1279,9 +1279,6 @@ extern "C" jepa_status jepa_op_linear(int32_t dtype, const void* d_x, int32_t M,
       return fail(JEPA_E_INVALID_ARG, "QKV_ROPE epilogue: inconsistent heads/rows");
     e.rope = reinterpret_cast<const float2*>(epi->d_rope);
     e.rope_ids = epi->d_rope_ids;
-    e.qkv_pad64 = epi->qkv_pad64 ? 1 : 0;
-    if (e.qkv_pad64 && (dtype != JEPA_BF16 || epi->head_dim != 32))
-      return fail(JEPA_E_INVALID_ARG, "QKV_ROPE epilogue: qkv_pad64 needs the bf16 path and head_dim 32");
     e.rows_per_item = epi->rows_per_item;
     e.prefix = epi->prefix;
     e.n_head = epi->n_head;
@@ -1322,8 +1319,7 @@ extern "C" jepa_status jepa_op_linear(int32_t dtype, const void* d_x, int32_t M,
   const bool patch_tma = e.kind == kEpiPatch && e.prefix == 0 && e.rows_per_item == e.patches_per_item;
   if (e.kind != kEpiPatch || patch_tma) {
     if (reinterpret_cast<uintptr_t>(e.out) & 15) return fail(JEPA_E_INVALID_ARG, "bf16 GEMM output must be 16-byte aligned");
-    const int out_cols = e.qkv_pad64 ? 3 * e.n_head * 64 : N;  // padded heads: 64 columns each
-    if (!make_tmap_2d_out(&to, e.out, M, out_cols, (e.kind == kEpiResidual || e.kind == kEpiPatch) ? 4 : 2))
+    if (!make_tmap_2d_out(&to, e.out, M, N, (e.kind == kEpiResidual || e.kind == kEpiPatch) ? 4 : 2))
       return fail(JEPA_E_CUDA, "cuTensorMapEncodeTiled refused the output");
   }
   CUDA_TRY(gemm_tc_launch(ta, tb, to, bn, e, M, N, K, err, default_wait_limit_ns(), s));
@@ -1385,14 +1381,12 @@ extern "C" jepa_status jepa_op_attention(int32_t dtype, const void* d_qkv, int32
   if (attn_mode != 0 && attn_mode != 1) return fail(JEPA_E_INVALID_ARG, "attn_mode %d unknown", attn_mode);
   if (attn_mode == 1 && (frame_tokens <= 0 || prefix < 0)) return fail(JEPA_E_INVALID_ARG, "block-causal needs frame_tokens > 0");
   if (head_dim != 64 && !(head_dim == 32 && dtype == JEPA_BF16))
-    return fail(JEPA_E_UNSUPPORTED, "attention kernels are built for head_dim 64 (32 zero-padded in bf16; got %d)",
-                head_dim);
+    return fail(JEPA_E_UNSUPPORTED, "attention kernels are built for head_dim 64 (and 32 in bf16; got %d)", head_dim);
   AttnParams p;
   p.B = B;
   p.N = N;
   p.H = n_head;
-  p.head_dim = 64;
-  p.real_hd = head_dim;
+  p.head_dim = head_dim;
   p.attn_mode = attn_mode;
   p.prefix = prefix;
   p.frame_tokens = frame_tokens;
@@ -1409,7 +1403,8 @@ extern "C" jepa_status jepa_op_attention(int32_t dtype, const void* d_qkv, int32
   jepa_status st = op_err_word(&err);
   if (st != JEPA_OK) return st;
   CUtensorMap tm;
-  if (!make_tmap_3d_bf16(&tm, d_qkv, B, N, 3 * n_head * 64, 128)) return fail(JEPA_E_CUDA, "cuTensorMapEncodeTiled refused qkv");
+  if (!make_tmap_3d_bf16(&tm, d_qkv, B, N, 3 * n_head * head_dim, 128, head_dim))
+    return fail(JEPA_E_CUDA, "cuTensorMapEncodeTiled refused qkv");
   CUDA_TRY(attention_tc_launch(tm, p, err, default_wait_limit_ns(), s));
   return JEPA_OK;
 }

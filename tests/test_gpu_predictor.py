@@ -1,9 +1,8 @@
 """The masked-latent predictor on the GPU, against the oracle (GPU only).
 
 Stage tests feed seeded inputs to one kernel through the C ABI: the QKV epilogue with per-row
-position ids and head_dim 32 stored at a 64-column pitch (pads must stay zero), and the flash
-attention on zero-padded width-32 heads (scale 1/sqrt(32), compact output), with sharp scores so
-that a wrong position, scale or pad shows. Whole-predictor tests compare with oracle.predict
+position ids and head_dim 32, and the flash attention on width-32 heads (64-byte tiles, scale
+1/sqrt(32)), with sharp scores so that a wrong position or scale shows. Whole-predictor tests compare with oracle.predict
 (fp64, the same bf16 weights): per-token cosine >= 0.9999 and max |d| <= 3e-2 * max |ref| (the
 encoder's bf16 bar, relative because the projected outputs are not unit-scale). Full size: the
 V-JEPA 2 ViT-L predictor over a 16 x 256^2 clip's 2048 tokens against tests/golden/
@@ -47,7 +46,7 @@ def positions(ids, gh, gw):
 
 # ------------------------------------------------------------------ stages
 @pytest.mark.parametrize("layout", [0, 1])
-def test_qkv_epilogue_with_position_ids_and_padded_heads(layout):
+def test_qkv_epilogue_with_position_ids_and_width_32_heads(layout):
     n_head, hd, M = 4, 32, 300                       # ragged: 300 rows = 2 tiles + 44
     P = n_head * hd
     gt, gh, gw = 3, 5, 7
@@ -59,14 +58,12 @@ def test_qkv_epilogue_with_position_ids_and_padded_heads(layout):
     hp = jv.hparams(embed_dim=P, n_layer=1, n_head=n_head, ffn_dim=64, patch_size=16, tubelet_size=2,
                     pos_type=jv.POS_ROPE3D, rope_layout=layout)
     table = jv.ops.rope_table(hp, 2 * gt, 16 * gh, 16 * gw)      # per-token table of the whole grid
-    out = torch.zeros((M, 3 * n_head * 64), dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros((M, 3 * P), dtype=torch.bfloat16, device="cuda")
     xt, wt = bf16_exact(x), bf16_exact(w)
     jv.ops.linear(xt.cuda(), wt.cuda(), torch.from_numpy(b).cuda(), out, jv.EPI_QKV_ROPE, rope=table,
                   rows_per_item=M, n_head=n_head, head_dim=hd, rope_layout=layout,
-                  rope_ids=torch.from_numpy(ids).cuda(), qkv_pad64=True)
-    got = f64(out).reshape(M, 3, n_head, 64)
-    assert np.all(got[..., 32:] == 0.0)                          # the pads stay zero
-    got = got[..., :32].reshape(M, 3 * P)
+                  rope_ids=torch.from_numpy(ids).cuda())
+    got = f64(out)
     qkv = oracle.linear(f64(xt), f64(wt), b)
     c, s = oracle.rope_tables_pos(hd, 10000.0, layout, positions(ids, gh, gw))
     ref = np.concatenate([oracle.rope_apply(qkv[:, :P], n_head, c, s), oracle.rope_apply(qkv[:, P:2 * P], n_head, c, s),
@@ -80,25 +77,22 @@ def test_qkv_epilogue_with_position_ids_and_padded_heads(layout):
 
 
 @pytest.mark.parametrize("B,N,H", [(1, 128, 2), (2, 300, 3), (1, 1100, 12)])
-def test_attention_on_zero_padded_width_32_heads(B, N, H):
+def test_attention_on_width_32_heads(B, N, H):
     rng = np.random.default_rng(40 + N)
     sharp = 3.0   # score std of q.k / sqrt(32)
-    q = rng.standard_normal((B * N, H, 32)) * np.sqrt(sharp)
-    k = rng.standard_normal((B * N, H, 32)) * np.sqrt(sharp)
-    v = rng.standard_normal((B * N, H, 32))
-    pad = np.zeros((B * N, 3, H, 64), dtype=np.float32)
-    pad[:, 0, :, :32], pad[:, 1, :, :32], pad[:, 2, :, :32] = q, k, v
-    qkv = bf16_exact(pad.reshape(B * N, 3 * H * 64))
-    got = f64(jv.ops.attention(qkv.cuda(), B, N, H, head_dim=32)).reshape(B * N, H * 32)
-    e = f64(qkv).reshape(B * N, 3, H, 64)[..., :32]
-    ref = np.concatenate([oracle.attention(e[b * N:(b + 1) * N, 0].reshape(N, H * 32),
-                                           e[b * N:(b + 1) * N, 1].reshape(N, H * 32),
-                                           e[b * N:(b + 1) * N, 2].reshape(N, H * 32), H) for b in range(B)])
-    assert np.abs(got - ref).max() <= 0.01 * np.abs(e[..., 2, :, :]).max()
+    q = rng.standard_normal((B * N, H * 32)) * np.sqrt(sharp)
+    k = rng.standard_normal((B * N, H * 32)) * np.sqrt(sharp)
+    v = rng.standard_normal((B * N, H * 32))
+    qkv = bf16_exact(np.concatenate([q, k, v], axis=1))
+    got = f64(jv.ops.attention(qkv.cuda(), B, N, H, head_dim=32))
+    e = f64(qkv)
+    P = H * 32
+    ref = np.concatenate([oracle.attention(e[b * N:(b + 1) * N, :P], e[b * N:(b + 1) * N, P:2 * P],
+                                           e[b * N:(b + 1) * N, 2 * P:], H) for b in range(B)])
+    assert np.abs(got - ref).max() <= 0.01 * np.abs(e[:, 2 * P:]).max()
     # the width-64 scale (1/8 instead of 1/sqrt(32)) would not pass
-    wrong = np.concatenate([oracle.attention(e[b * N:(b + 1) * N, 0].reshape(N, H * 32) / np.sqrt(2.0),
-                                             e[b * N:(b + 1) * N, 1].reshape(N, H * 32),
-                                             e[b * N:(b + 1) * N, 2].reshape(N, H * 32), H) for b in range(B)])
+    wrong = np.concatenate([oracle.attention(e[b * N:(b + 1) * N, :P] / np.sqrt(2.0), e[b * N:(b + 1) * N, P:2 * P],
+                                             e[b * N:(b + 1) * N, 2 * P:], H) for b in range(B)])
     assert np.abs(got - wrong).max() > 0.05
 
 
