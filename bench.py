@@ -65,12 +65,12 @@ FLUSH_BYTES = 256 << 20  # > 129 MB of L2
 # captures of the 2048-token clips at 8 per GPU; `sha1` is the hash of the class's source files when
 # the counters were taken (a changed kernel reports traffic null until it is captured again).
 NCU_TRAFFIC = {  # (workload, kernel class, clips per GPU): bytes per launch, source hash at capture
-    (HEADLINE, "attention", 8): {"bytes_per_launch": 112.78e6, "sha1": "58a1e95f818e157373e6c71370eda112659e7ff6"},
-    (HEADLINE, "layernorm", 8): {"bytes_per_launch": 68.98e6, "sha1": "39f959c935d12366f5b46a566e219d3edf4e75d6"},
-    (HEADLINE, "gemm_qkv", 8): {"bytes_per_launch": 85.51e6, "sha1": "492471294b0890c32ea3405750fc2b5f7a07768d"},
-    (HEADLINE, "gemm_out", 8): {"bytes_per_launch": 102.86e6, "sha1": "492471294b0890c32ea3405750fc2b5f7a07768d"},
-    (HEADLINE, "gemm_up", 8): {"bytes_per_launch": 120.41e6, "sha1": "492471294b0890c32ea3405750fc2b5f7a07768d"},
-    (HEADLINE, "gemm_down", 8): {"bytes_per_launch": 217.99e6, "sha1": "492471294b0890c32ea3405750fc2b5f7a07768d"},
+    (HEADLINE, "attention", 8): {"bytes_per_launch": 113.11e6, "sha1": "284bf62672e153c93d435f630c09da64e7814781"},
+    (HEADLINE, "layernorm", 8): {"bytes_per_launch": 69.09e6, "sha1": "f6fdfd512fe984c74807e382dff942f891e2d951"},
+    (HEADLINE, "gemm_qkv", 8): {"bytes_per_launch": 85.33e6, "sha1": "3576f000a50f3a6b97bd825d9625e6fccf4c81c3"},
+    (HEADLINE, "gemm_out", 8): {"bytes_per_launch": 102.92e6, "sha1": "3576f000a50f3a6b97bd825d9625e6fccf4c81c3"},
+    (HEADLINE, "gemm_up", 8): {"bytes_per_launch": 120.46e6, "sha1": "3576f000a50f3a6b97bd825d9625e6fccf4c81c3"},
+    (HEADLINE, "gemm_down", 8): {"bytes_per_launch": 217.94e6, "sha1": "3576f000a50f3a6b97bd825d9625e6fccf4c81c3"},
 }
 
 
