@@ -12,9 +12,10 @@
 //               warp rescales its O rows in TMEM. At the end o = O / l is stored as bf16.
 //   warp 8      TMA: Q0 and Q1 once, then K and V tiles of 128 keys into a 3-stage ring
 //               (3-D tensor map over qkv [B][N][3D]: rows beyond N read as zeros).
-//   warp 9      MMA, per key tile j: S_g(j+1) = Q_g K(j+1)^T for both tiles as soon as warpgroup g
-//               has read S_g(j) into registers (so the next scores are ready when its softmax
-//               ends), then O_g += P_g(j) V(j) for both tiles once P_g(j) is in TMEM.
+//   warp 9      MMA (the whole warp runs the loop, an elected lane issues), per key tile j:
+//               S_g(j+1) = Q_g K(j+1)^T for both tiles as soon as warpgroup g has read S_g(j)
+//               into registers (so the next scores are ready when its softmax ends), then
+//               O_g += P_g(j) V(j) for both tiles once P_g(j) is in TMEM.
 //               S = Q K^T: M128 N128 K16 x (HD/16) (both K-major); O += P V: M128 N(HD) K16 x8
 //               with P read from TMEM and V MN-major in shared memory.
 // TMEM (512 columns): S0 [0,128) S1 [128,256) P0 [256,320) P1 [320,384) O0, O1 from 384 (HD each).
@@ -166,67 +167,69 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         if (armed & (1u << s)) mbar_drain(smem_u32(kv_full + s), (armed_phase >> s) & 1u, a.limit_ns, a.err);
     }
   } else if (warp == 9) {
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, kKT, 0, 0);
-      constexpr uint32_t idesc_o = idesc_bf16_f32(128, kHD, 0, 1);
-      // descriptors built once; a K step or a stage only moves the start address (the issue
-      // loop stays short enough to keep the tensor pipe fed with these small MMAs)
-      const uint64_t q_desc = tile_desc<HD>(smem_u32(sQ));
-      const uint64_t k_desc = tile_desc<HD>(smem_u32(sK));
-      const uint64_t v_desc = tile_desc<HD>(smem_u32(sV));
-      auto issue_s = [&](int g, int st) {
-        const uint64_t qd = desc_advance(q_desc, g * kTileBytes), kd = desc_advance(k_desc, st * kTileBytes);
-        const uint32_t d = tmem + kColS + g * 128;
+    // the whole warp runs the issue loop (waits and descriptor arithmetic warp-uniform); one
+    // elected lane issues each MMA and commit
+    constexpr uint32_t idesc_s = idesc_bf16_f32(128, kKT, 0, 0);
+    constexpr uint32_t idesc_o = idesc_bf16_f32(128, kHD, 0, 1);
+    // descriptors built once; a K step or a stage only moves the start address
+    const uint64_t q_desc = tile_desc<HD>(smem_u32(sQ));
+    const uint64_t k_desc = tile_desc<HD>(smem_u32(sK));
+    const uint64_t v_desc = tile_desc<HD>(smem_u32(sV));
+    auto wait = [&](const uint64_t* bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, mbar_wait(smem_u32(bar), parity, wc));
+    };
+    auto issue_s = [&](int g, int st) {
+      const uint64_t qd = desc_advance(q_desc, g * kTileBytes), kd = desc_advance(k_desc, st * kTileBytes);
+      const uint32_t d = tmem + kColS + g * 128;
 #pragma unroll
-        for (int k = 0; k < kHD / 16; ++k) mma_ss(d, desc_advance(qd, k * 32), desc_advance(kd, k * 32), idesc_s, k != 0);
-        mma_commit(smem_u32(s_full + g));
-      };
-      auto issue_pv = [&](int g, int st, int j) {
-        const uint64_t vd = desc_advance(v_desc, st * kTileBytes);
-        const uint32_t d = tmem + kColO + g * kHD, p = tmem + kColP + g * 64;
+      for (int k = 0; k < kHD / 16; ++k) mma_ss_warp(d, desc_advance(qd, k * 32), desc_advance(kd, k * 32), idesc_s, k != 0);
+      mma_commit_warp(smem_u32(s_full + g));
+    };
+    auto issue_pv = [&](int g, int st, int j) {
+      const uint64_t vd = desc_advance(v_desc, st * kTileBytes);
+      const uint32_t d = tmem + kColO + g * kHD, p = tmem + kColP + g * 64;
 #pragma unroll
-        for (int k = 0; k < kKT / 16; ++k)  // 16 keys = 16 rows of V per K step
-          mma_ts(d, p + k * 8, desc_advance(vd, k * 16 * Width<HD>::kRowBytes), idesc_o, (j > 0 || k > 0) ? 1u : 0u);
-        mma_commit(smem_u32(o_done + g));
-      };
-      bool ok = num_kt > 0 && mbar_wait(smem_u32(q_full), 0, wc) && mbar_wait(smem_u32(kv_full), 0, wc);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0, 0);
-        issue_s(1, 0);
-      }
-      int stage = 0;
-      uint32_t phase = 0;
-      for (int j = 0; j < num_kt && ok; ++j) {
-        const int nst = (stage + 1 == kKvStages) ? 0 : stage + 1;
-        const uint32_t nph = (stage + 1 == kKvStages) ? (phase ^ 1u) : phase;
-        const bool more = j + 1 < num_kt;
-        // S_g(j+1) as soon as warpgroup g holds S_g(j) in registers (while it computes P), for
-        // both tiles, then P_g(j) V(j) once P is in TMEM: neither tile's next scores wait
-        // behind the other tile's softmax
-        if (more) {
-          ok = mbar_wait(smem_u32(kv_full + nst), nph, wc);
-#pragma unroll
-          for (int g = 0; g < 2 && ok; ++g) {
-            if (!(ok = mbar_wait(smem_u32(s_free + g), (uint32_t)(j & 1), wc))) break;
-            tc_fence_after();
-            issue_s(g, nst);
-          }
-        }
+      for (int k = 0; k < kKT / 16; ++k)  // 16 keys = 16 rows of V per K step
+        mma_ts_warp(d, p + k * 8, desc_advance(vd, k * 16 * Width<HD>::kRowBytes), idesc_o, (j > 0 || k > 0) ? 1u : 0u);
+      mma_commit_warp(smem_u32(o_done + g));
+    };
+    bool ok = num_kt > 0 && wait(q_full, 0) && wait(kv_full, 0);
+    if (ok) {
+      tc_fence_after();
+      issue_s(0, 0);
+      issue_s(1, 0);
+    }
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int j = 0; j < num_kt && ok; ++j) {
+      const int nst = (stage + 1 == kKvStages) ? 0 : stage + 1;
+      const uint32_t nph = (stage + 1 == kKvStages) ? (phase ^ 1u) : phase;
+      const bool more = j + 1 < num_kt;
+      // S_g(j+1) as soon as warpgroup g holds S_g(j) in registers (while it computes P), for
+      // both tiles, then P_g(j) V(j) once P is in TMEM: neither tile's next scores wait
+      // behind the other tile's softmax
+      if (more) {
+        ok = wait(kv_full + nst, nph);
 #pragma unroll
         for (int g = 0; g < 2 && ok; ++g) {
-          if (!(ok = mbar_wait(smem_u32(p_full + g), (uint32_t)(j & 1), wc))) break;
+          if (!(ok = wait(s_free + g, (uint32_t)(j & 1)))) break;
           tc_fence_after();
-          issue_pv(g, stage, j);
+          issue_s(g, nst);
         }
-        if (!ok) break;
-        mma_commit(smem_u32(kv_empty + stage));  // K(j), V(j) no longer read once these complete
-        stage = nst;
-        phase = nph;
       }
-      mma_commit(smem_u32(mma_done));
-      mbar_drain(smem_u32(mma_done), 0, a.limit_ns, a.err);
+#pragma unroll
+      for (int g = 0; g < 2 && ok; ++g) {
+        if (!(ok = wait(p_full + g, (uint32_t)(j & 1)))) break;
+        tc_fence_after();
+        issue_pv(g, stage, j);
+      }
+      if (!ok) break;
+      mma_commit_warp(smem_u32(kv_empty + stage));  // K(j), V(j) no longer read once these complete
+      stage = nst;
+      phase = nph;
     }
+    mma_commit_warp(smem_u32(mma_done));
+    mbar_drain(smem_u32(mma_done), 0, a.limit_ns, a.err);
   } else {
     const int g = warp >> 2;                 // which query tile
     const int quarter = warp & 3;

@@ -140,8 +140,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (armed & (1u << s)) mbar_drain(smem_u32(full + s), (armed_phase >> s) & 1u, limit_ns, err);
     }
   } else if (warp == 1) {
-    if (lane == 0 && rank == 0) {
-      // even CTA: the MMA issuer of the pair
+    if (rank == 0) {
+      // even CTA: the MMA issuer of the pair. The whole warp runs the issue loop (waits and
+      // descriptor arithmetic warp-uniform); one elected lane issues each MMA and commit.
       constexpr uint32_t idesc = idesc_bf16_f32(kTileM, kTileN, 0, 0);
       const uint64_t a_desc = smem_desc_sw128(smem_u32(sA), 1024, 1024);  // stage 0; stages and K
       const uint64_t b_desc = smem_desc_sw128(smem_u32(sB), 1024, 1024);  // steps move the address
@@ -149,11 +150,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
       for (int tile = pair; tile < num_tiles && ok; tile += num_pairs) {
-        if (!mbar_wait(smem_u32(tempty + acc), acc_phase ^ 1u, wc)) break;
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(tempty + acc), acc_phase ^ 1u, wc))) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kTileN);
         for (int kb = 0; kb < num_k; ++kb) {
-          if (!mbar_wait(smem_u32(full + stage), phase, wc)) {
+          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(full + stage), phase, wc))) {
             ok = false;
             break;
           }
@@ -161,21 +162,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint64_t ad = desc_advance(a_desc, stage * C::kABytes), bd = desc_advance(b_desc, stage * C::kBBytes);
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k)
-            mma_ss_pair(d_tmem, desc_advance(ad, k * 32), desc_advance(bd, k * 32), idesc, (kb | k) != 0 ? 1u : 0u);
-          mma_commit_pair_mc(smem_u32(empty + stage), 0x3);
+            mma_ss_pair_warp(d_tmem, desc_advance(ad, k * 32), desc_advance(bd, k * 32), idesc, (kb | k) != 0 ? 1u : 0u);
+          mma_commit_pair_mc_warp(smem_u32(empty + stage), 0x3);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        mma_commit_pair_mc(smem_u32(tfull + acc), 0x3);
+        mma_commit_pair_mc_warp(smem_u32(tfull + acc), 0x3);
         if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1u;
         }
       }
-      mma_commit_pair_mc(smem_u32(mma_done), 0x1);
+      mma_commit_pair_mc_warp(smem_u32(mma_done), 0x1);
       mbar_drain(smem_u32(mma_done), 0, limit_ns, err);
     }
   } else {
