@@ -12,12 +12,15 @@
 //               warp rescales its O rows in TMEM. At the end o = O / l is stored as bf16.
 //   warp 8      TMA: Q0 and Q1 once, then K and V tiles of 128 keys into a 3-stage ring
 //               (3-D tensor map over qkv [B][N][3D]: rows beyond N read as zeros).
-//   warp 9      MMA (the whole warp runs the loop, an elected lane issues), per key tile j:
+//   warps 10-11 MMA, taking the key tiles in turn (each warp runs its loop whole, an elected
+//               lane issues); per key tile j:
 //               S_g(j+1) = Q_g K(j+1)^T for both tiles as soon as warpgroup g has read S_g(j)
 //               into registers (so the next scores are ready when its softmax ends), then
 //               O_g += P_g(j) V(j) for both tiles once P_g(j) is in TMEM.
 //               S = Q K^T: M128 N128 K16 x (HD/16) (both K-major); O += P V: M128 N(HD) K16 x8
 //               with P read from TMEM and V MN-major in shared memory.
+//   warp 9      idle: the third warpgroup is whole so that it can hand registers to the softmax
+//               warpgroups (setmaxnreg: 200 per softmax thread, 104 in warpgroup 2).
 // TMEM (512 columns): S0 [0,128) S1 [128,256) P0 [256,320) P1 [320,384) O0, O1 from 384 (HD each).
 // Block-causal: a CTA only visits keys below the last frame its rows can see, and the per-element
 // predicate runs only on tiles that straddle a frame edge, the CLS row/column or N.
@@ -35,6 +38,9 @@ namespace {
 constexpr int kQT = 128;  // queries per tile (per softmax warpgroup)
 constexpr int kKT = 128;  // keys per tile
 constexpr int kKvStages = 3;
+constexpr int kIssuers = 2, kFirstIssuer = 10;  // MMA issuing warps 10 and 11
+// barriers (q_full, kv_full, kv_empty, s_full, o_done, mma_done, p_full, s_free), TMEM slot, abort flag
+static_assert((1 + 2 * kKvStages + 5 + 4 * kIssuers) * 8 + 8 <= 256, "barrier area");
 // Per head width HD (64, or 32 for the masked predictor): a 128-row tile of q, k or v is
 // 128 x HD bf16 with HD x 2 bytes per row, stored in the TMA / UMMA swizzle of that row length.
 template <int HD>
@@ -43,7 +49,12 @@ struct Width {
   static constexpr int kSmemBytes = 1024 + kTileBytes * (2 + 2 * kKvStages) + 256;
   static constexpr uint32_t kRowBytes = HD * 2;    // 128 or 64: the swizzle span
 };
-constexpr int kThreads = 320;
+// softmax warpgroups 0 and 1; warpgroup 2: TMA warp 8, idle warp 9, MMA warps 10 and 11
+constexpr int kThreads = 384;
+// Register budgets after the split: 200 per softmax thread, 104 in warpgroup 2; launched with 168
+// per thread (384 x 168 = 64512 >= 256 x 200 + 128 x 104 = 64512).
+constexpr uint32_t kSoftmaxRegs = 200, kProducerRegs = 104, kLaunchRegs = 168;
+static_assert(256 * kSoftmaxRegs + 128 * kProducerRegs <= kThreads * kLaunchRegs, "register split exceeds the launch");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColP = 256, kColO = 384;  // + 128 / 64 / HD per tile
 constexpr float kRescaleThreshold = 8.0f;                 // log2 units: p stays below 2^8 between rescales
@@ -101,11 +112,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   uint64_t* kv_full = bars + 1;
   uint64_t* kv_empty = bars + 1 + kKvStages;
   uint64_t* s_full = bars + 1 + 2 * kKvStages;  // [2]
-  uint64_t* p_full = s_full + 2;                // [2]
-  uint64_t* o_done = s_full + 4;                // [2]
-  uint64_t* mma_done = s_full + 6;
-  uint64_t* s_free = s_full + 7;                // [2]: the warpgroup has read S into registers
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 9);
+  uint64_t* o_done = s_full + 2;                // [2]
+  uint64_t* mma_done = s_full + 4;
+  // Per issuer (key tile j on [g][j % kIssuers]), so that each barrier's phases are waited in
+  // order by one warp: a parity wait cannot tell a phase two ahead from the one before.
+  uint64_t* p_full = s_full + 5;                // [2][kIssuers]: P_g(j) is in TMEM
+  uint64_t* s_free = p_full + 2 * kIssuers;     // [2][kIssuers]: the warpgroup has read S_g(j)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_free + 2 * kIssuers);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -120,11 +133,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     }
     for (int g = 0; g < 2; ++g) {
       mbar_init(smem_u32(s_full + g), 1);
-      mbar_init(smem_u32(p_full + g), 128);
       mbar_init(smem_u32(o_done + g), 1);
-      mbar_init(smem_u32(s_free + g), 4);
+      for (int w = 0; w < kIssuers; ++w) {
+        mbar_init(smem_u32(p_full + g * kIssuers + w), 128);
+        mbar_init(smem_u32(s_free + g * kIssuers + w), 4);
+      }
     }
-    mbar_init(smem_u32(mma_done), 1);
+    mbar_init(smem_u32(mma_done), kIssuers);  // each issuer's last commit
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tm);
@@ -140,7 +155,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   const WaitCtl wc{abort_flag, a.err, a.limit_ns};
   pdl_trigger();
   pdl_wait();  // qkv comes from the previous kernel; the output may still be read by older ones
-
+  if (warp >= 8) {
+  // warpgroup 2 gives registers back to the softmax warpgroups (each branch is entered by a
+  // whole warpgroup, which executes its register budget change together)
+  warpgroup_regs_dec<kProducerRegs>();
   if (warp == 8) {
     if (lane == 0) {
       const uint32_t qb = smem_u32(q_full);
@@ -166,9 +184,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       for (int s = 0; s < kKvStages; ++s)
         if (armed & (1u << s)) mbar_drain(smem_u32(kv_full + s), (armed_phase >> s) & 1u, a.limit_ns, a.err);
     }
-  } else if (warp == 9) {
-    // the whole warp runs the issue loop (waits and descriptor arithmetic warp-uniform); one
-    // elected lane issues each MMA and commit
+  } else if (warp >= kFirstIssuer && warp < kFirstIssuer + kIssuers) {
+    // Warps 10 and 11 take the key tiles in turn (tile j by warp 10 + j % 2, tile 0's scores by
+    // warp 10): issuing MMAs slows the other warps of the issuer's sub-partition, and a tile's
+    // softmax ends with its slowest lane quarter, so the cost is shared by two sub-partitions.
+    // The issuers need no ordering among themselves: S_g(j+1) follows s_free_g(j), and P_g(j) V(j)
+    // follows p_full_g(j), which the softmax arrives on only after o_done_g(j-1).
+    // Each warp runs its loop whole (waits and descriptor arithmetic warp-uniform); one elected
+    // lane issues each MMA and commit.
+    const int me = warp - kFirstIssuer;
     constexpr uint32_t idesc_s = idesc_bf16_f32(128, kKT, 0, 0);
     constexpr uint32_t idesc_o = idesc_bf16_f32(128, kHD, 0, 1);
     // descriptors built once; a K step or a stage only moves the start address
@@ -193,44 +217,47 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         mma_ts_warp(d, p + k * 8, desc_advance(vd, k * 16 * Width<HD>::kRowBytes), idesc_o, (j > 0 || k > 0) ? 1u : 0u);
       mma_commit_warp(smem_u32(o_done + g));
     };
-    bool ok = num_kt > 0 && wait(q_full, 0) && wait(kv_full, 0);
-    if (ok) {
-      tc_fence_after();
-      issue_s(0, 0);
-      issue_s(1, 0);
+    bool ok = num_kt > 0;
+    if (me == 0 && ok) {
+      ok = wait(q_full, 0) && wait(kv_full, 0);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0, 0);
+        issue_s(1, 0);
+      }
     }
-    int stage = 0;
-    uint32_t phase = 0;
-    for (int j = 0; j < num_kt && ok; ++j) {
-      const int nst = (stage + 1 == kKvStages) ? 0 : stage + 1;
-      const uint32_t nph = (stage + 1 == kKvStages) ? (phase ^ 1u) : phase;
+    for (int j = me; j < num_kt && ok; j += kIssuers) {
+      const int stage = j % kKvStages, nst = (j + 1) % kKvStages;
+      const uint32_t nph = (uint32_t)(((j + 1) / kKvStages) & 1);
       const bool more = j + 1 < num_kt;
       // S_g(j+1) as soon as warpgroup g holds S_g(j) in registers (while it computes P), for
       // both tiles, then P_g(j) V(j) once P is in TMEM: neither tile's next scores wait
       // behind the other tile's softmax
       if (more) {
-        ok = wait(kv_full + nst, nph);
 #pragma unroll
         for (int g = 0; g < 2 && ok; ++g) {
-          if (!(ok = wait(s_free + g, (uint32_t)(j & 1)))) break;
+          if (!(ok = wait(s_free + g * kIssuers + me, (uint32_t)((j / kIssuers) & 1)))) break;
+          // K(j+1) after s_free_0(j): that implies S(j) has run, so tile j-2 (the stage's previous
+          // load, whose wait another issuer may have done) is complete and the parity cannot alias
+          if (g == 0 && !(ok = wait(kv_full + nst, nph))) break;
           tc_fence_after();
           issue_s(g, nst);
         }
       }
 #pragma unroll
       for (int g = 0; g < 2 && ok; ++g) {
-        if (!(ok = wait(p_full + g, (uint32_t)(j & 1)))) break;
+        if (!(ok = wait(p_full + g * kIssuers + me, (uint32_t)((j / kIssuers) & 1)))) break;
         tc_fence_after();
         issue_pv(g, stage, j);
       }
       if (!ok) break;
       mma_commit_warp(smem_u32(kv_empty + stage));  // K(j), V(j) no longer read once these complete
-      stage = nst;
-      phase = nph;
     }
     mma_commit_warp(smem_u32(mma_done));
     mbar_drain(smem_u32(mma_done), 0, a.limit_ns, a.err);
+  }
   } else {
+    warpgroup_regs_inc<kSoftmaxRegs>();
     const int g = warp >> 2;                 // which query tile
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;       // query row inside the tile = TMEM lane
@@ -268,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       uint32_t (&s)[kKT / 32][32] = *reinterpret_cast<uint32_t (*)[kKT / 32][32]>(&sr);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(s_free + g));  // the MMA warp may overwrite S now
+      if (lane == 0) mbar_arrive(smem_u32(s_free + g * kIssuers + j % kIssuers));  // S may be overwritten now
       if (masked) {  // invisible keys score -inf: they lose the max and give p = 0
 #pragma unroll
         for (int c = 0; c < kKT / 32; ++c)
@@ -338,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       l_run += (l01.x + l23.x) + (l01.y + l23.y);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(smem_u32(p_full + g));
+      mbar_arrive(smem_u32(p_full + g * kIssuers + j % kIssuers));
     }
     bool store = ok && num_kt > 0 && mbar_wait(smem_u32(o_done + g), (uint32_t)((num_kt - 1) & 1), wc);
     store = __all_sync(0xffffffffu, store);  // the TMEM loads below are warp-collective

@@ -57,6 +57,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The same with a suspend-time hint: a thread whose phase has not completed may sleep in the
+// barrier for up to hint_ns (it resumes as soon as the phase completes), so that a waiting warp
+// does not take issue slots from the warps of its sub-partition that it is waiting for.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+constexpr uint32_t kWaitSleepNs = 1000;  // per suspension; the time limit is still checked between them
+
 // Shared state of the bounded waits of one CTA.
 struct WaitCtl {
   volatile int* abort_flag;  // shared memory: set once any role gives up
@@ -70,7 +86,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
     if (*w.abort_flag) return false;
     if (global_timer_ns() - t0 > w.limit_ns) {
       *w.abort_flag = 1;
@@ -265,6 +281,18 @@ __device__ __forceinline__ void mma_commit_warp(uint32_t bar) {
       "elect.sync _|e, 0xffffffff;\n\t"
       "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
       : "memory");
+}
+
+// Per-warpgroup register budgets (executed by all four warps of a warpgroup together). The
+// increases draw on the registers the CTA was launched with, which the decreases return: the
+// sum over warpgroups after both must not exceed threads x registers-per-thread at launch.
+template <uint32_t kRegs>
+__device__ __forceinline__ void warpgroup_regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <uint32_t kRegs>
+__device__ __forceinline__ void warpgroup_regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
 }
 
 // ---------------------------------------------------------------- 2-CTA (cluster pair) forms
