@@ -65,12 +65,12 @@ FLUSH_BYTES = 256 << 20  # > 129 MB of L2
 # captures of the 2048-token clips at 8 per GPU; `sha1` is the hash of the class's source files when
 # the counters were taken (a changed kernel reports traffic null until it is captured again).
 NCU_TRAFFIC = {  # (workload, kernel class, clips per GPU): bytes per launch, source hash at capture
-    (HEADLINE, "attention", 8): {"bytes_per_launch": 113.11e6, "sha1": "284bf62672e153c93d435f630c09da64e7814781"},
-    (HEADLINE, "layernorm", 8): {"bytes_per_launch": 69.09e6, "sha1": "f6fdfd512fe984c74807e382dff942f891e2d951"},
-    (HEADLINE, "gemm_qkv", 8): {"bytes_per_launch": 85.33e6, "sha1": "3576f000a50f3a6b97bd825d9625e6fccf4c81c3"},
-    (HEADLINE, "gemm_out", 8): {"bytes_per_launch": 102.92e6, "sha1": "3576f000a50f3a6b97bd825d9625e6fccf4c81c3"},
-    (HEADLINE, "gemm_up", 8): {"bytes_per_launch": 120.46e6, "sha1": "3576f000a50f3a6b97bd825d9625e6fccf4c81c3"},
-    (HEADLINE, "gemm_down", 8): {"bytes_per_launch": 217.94e6, "sha1": "3576f000a50f3a6b97bd825d9625e6fccf4c81c3"},
+    (HEADLINE, "attention", 8): {"bytes_per_launch": 112.97e6, "sha1": "c3ea96cde7113f36aa824c2a3c2c97a1ef011005"},
+    (HEADLINE, "layernorm", 8): {"bytes_per_launch": 68.89e6, "sha1": "bb9dc2d3ba2669d1d4fc0c56aa91f83c297e13cc"},
+    (HEADLINE, "gemm_qkv", 8): {"bytes_per_launch": 85.49e6, "sha1": "8efbd5e9fbf917cb3d824db549cee4fd2f037b5a"},
+    (HEADLINE, "gemm_out", 8): {"bytes_per_launch": 103.15e6, "sha1": "8efbd5e9fbf917cb3d824db549cee4fd2f037b5a"},
+    (HEADLINE, "gemm_up", 8): {"bytes_per_launch": 120.79e6, "sha1": "8efbd5e9fbf917cb3d824db549cee4fd2f037b5a"},
+    (HEADLINE, "gemm_down", 8): {"bytes_per_launch": 218.81e6, "sha1": "8efbd5e9fbf917cb3d824db549cee4fd2f037b5a"},
 }
 
 
