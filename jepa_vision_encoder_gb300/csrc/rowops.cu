@@ -105,26 +105,27 @@ cudaError_t patchify_launch(const float* pix, int B, int T, int C, int H, int W,
 // ------------------------------------------------------------------ LayerNorm
 // One warp per row, the row held in registers (D <= 2048): mean, then the centred sum of
 // squares (two passes over registers, no E[x^2] - mean^2), eps inside the square root.
+// Persistent: the grid is what fits on the GPU at once and each warp strides over the rows,
+// loading its next row into a second register set before normalising the current one, so that
+// every SM keeps a row per warp in flight and no partial last wave idles the memory system.
 namespace {
 
-template <int V, bool BF16>
-__global__ void __launch_bounds__(256) layernorm_kernel(const float* __restrict__ x, int M, int D,
-                                                        const float* __restrict__ g, const float* __restrict__ bta,
-                                                        float eps, void* __restrict__ y) {
-  pdl_trigger();
-  pdl_wait();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x * 8 + warp;
-  if (row >= M) return;
+template <int V>
+__device__ __forceinline__ void ln_load(const float* __restrict__ x, int row, int D, int lane, float4 (&v)[V]) {
   const float* xr = x + (size_t)row * D;
-  float4 v[V];
-  float sum = 0.0f;
 #pragma unroll
   for (int i = 0; i < V; ++i) {
     const int c = (lane + 32 * i) * 4;
     v[i] = (c < D) ? __ldg(reinterpret_cast<const float4*>(xr + c)) : make_float4(0.f, 0.f, 0.f, 0.f);
-    sum += (v[i].x + v[i].y) + (v[i].z + v[i].w);
   }
+}
+
+template <int V, bool BF16>
+__device__ __forceinline__ void ln_row(const float4 (&v)[V], int row, int D, int lane, const float* __restrict__ g,
+                                       const float* __restrict__ bta, float eps, void* __restrict__ y) {
+  float sum = 0.0f;
+#pragma unroll
+  for (int i = 0; i < V; ++i) sum += (v[i].x + v[i].y) + (v[i].z + v[i].w);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
   const float mu = sum / (float)D;
@@ -161,10 +162,50 @@ __global__ void __launch_bounds__(256) layernorm_kernel(const float* __restrict_
   }
 }
 
+template <int V, bool BF16>
+__global__ void __launch_bounds__(256, 2) layernorm_kernel(const float* __restrict__ x, int M, int D,
+                                                        const float* __restrict__ g, const float* __restrict__ bta,
+                                                        float eps, void* __restrict__ y) {
+  pdl_trigger();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int stride = gridDim.x * 8;  // warps in the grid
+  int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+  float4 a[V], b[V];  // the current row and the next one, alternating
+  if (row < M) ln_load<V>(x, row, D, lane, a);
+  while (row < M) {
+    const int r1 = row + stride;
+    if (r1 < M) ln_load<V>(x, r1, D, lane, b);
+    ln_row<V, BF16>(a, row, D, lane, g, bta, eps, y);
+    if (r1 >= M) break;
+    const int r2 = r1 + stride;
+    if (r2 < M) ln_load<V>(x, r2, D, lane, a);
+    ln_row<V, BF16>(b, r1, D, lane, g, bta, eps, y);
+    row = r2;
+  }
+}
+
+template <int V, bool BF16>
+int ln_resident_blocks() {
+  static int cached = 0;
+  if (cached == 0) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, layernorm_kernel<V, BF16>, 256, 0) != cudaSuccess ||
+        per_sm <= 0) {
+      cudaGetLastError();
+      per_sm = 1;
+    }
+    cached = per_sm * num_sms();
+  }
+  return cached;
+}
+
 template <int V>
 cudaError_t ln_v(const float* x, int M, int D, const float* g, const float* b, float eps, bool bf16, void* y,
                  cudaStream_t s) {
-  const int grid = (M + 7) / 8;
+  const int rows_blocks = (M + 7) / 8;
+  const int fit = bf16 ? ln_resident_blocks<V, true>() : ln_resident_blocks<V, false>();
+  const int grid = rows_blocks < fit ? rows_blocks : fit;
   return launch_kernel(bf16 ? layernorm_kernel<V, true> : layernorm_kernel<V, false>, dim3(grid), dim3(256), 0, s, x,
                        M, D, g, b, eps, y);
 }
