@@ -39,23 +39,24 @@ struct EpiArgs {
 __device__ __forceinline__ float gelu_erf(float x) { return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f)); }
 
 // GELU of the bf16 tensor-core epilogue, two values at a time in packed fp32 arithmetic.
-// q = Phi(-|x|) = erfc(z) / 2 with z = |x| / sqrt(2) is evaluated as exp(-z^2) * sum_k c_k z^k, a
-// fit of the scaled complementary error function (gelu_fit.py in this directory prints the
-// coefficients and the bound |q - Phi(-|x|)| <= 1.1e-6, far below bf16 rounding); z is clamped
-// at 7.5, where exp(-z^2) < 1e-24. Then GELU(x) = x (1 - q) for x >= 0 and x q for x < 0.
+// q = Phi(-|x|) = erfc(|x| / sqrt(2)) / 2 is evaluated as exp(-x^2 / 2) * sum_k c_k a^k with
+// a = min(|x|, 16), a fit of the scaled complementary error function (gelu_fit.py in this
+// directory prints the coefficients and the bound |q - Phi(-|x|)| <= 1.8e-5, so the GELU is
+// within 1.8e-5 |x|, far below bf16 rounding); past |x| = 16 the exponential is below the smallest
+// normal float and q is 0. Then GELU(x) = x Phi(x) = x / 2 + |x| (1/2 - q).
 __device__ __forceinline__ float2 gelu_fast2(float2 x) {
-  constexpr float c[9] = {5.0000000000e-01f, -5.6412470331e-01f, 4.9878799230e-01f, -3.6839867682e-01f,
-                          2.2596099097e-01f, -1.0779897437e-01f, 3.5892620358e-02f, -7.1522320417e-03f,
-                          6.2728129318e-04f};
-  constexpr float kRsqrt2 = 0.70710678118654752f, kNegLog2e = -1.4426950408889634f;
-  const float2 z = make_float2(fminf(fabsf(x.x) * kRsqrt2, 7.5f), fminf(fabsf(x.y) * kRsqrt2, 7.5f));
-  const float2 zz = __fmul2_rn(z, z);
-  float2 p = make_float2(c[8], c[8]);
+  constexpr float c[7] = {5.0000000000e-01f, -3.9842587502e-01f, 2.4521308688e-01f, -1.1811391615e-01f,
+                          4.0482376797e-02f, -8.2998320074e-03f, 7.3464815428e-04f};
+  constexpr float kNegHalfLog2e = -0.72134752044448170f;  // -log2(e) / 2
+  const float2 ax = make_float2(fabsf(x.x), fabsf(x.y));
+  const float2 a = make_float2(fminf(ax.x, 16.0f), fminf(ax.y, 16.0f));
+  const float2 t = __fmul2_rn(__fmul2_rn(x, x), make_float2(kNegHalfLog2e, kNegHalfLog2e));
+  float2 p = make_float2(c[6], c[6]);
 #pragma unroll
-  for (int k = 7; k >= 0; --k) p = __ffma2_rn(p, z, make_float2(c[k], c[k]));
-  const float2 q = __fmul2_rn(p, make_float2(ex2_approx(zz.x * kNegLog2e), ex2_approx(zz.y * kNegLog2e)));
-  const float2 f = make_float2(x.x >= 0.0f ? 1.0f - q.x : q.x, x.y >= 0.0f ? 1.0f - q.y : q.y);
-  return __fmul2_rn(x, f);
+  for (int k = 5; k >= 0; --k) p = __ffma2_rn(p, a, make_float2(c[k], c[k]));
+  const float2 q = __fmul2_rn(p, make_float2(ex2_approx(t.x), ex2_approx(t.y)));
+  const float2 h = __ffma2_rn(q, make_float2(-1.0f, -1.0f), make_float2(0.5f, 0.5f));  // 1/2 - q
+  return __ffma2_rn(ax, h, __fmul2_rn(x, make_float2(0.5f, 0.5f)));
 }
 
 // The (cos, sin) rows (dh entries each) of the t, h and w axes of output row m, row p of its item.
