@@ -66,11 +66,11 @@ FLUSH_BYTES = 256 << 20  # > 129 MB of L2
 # the counters were taken (a changed kernel reports traffic null until it is captured again).
 NCU_TRAFFIC = {  # (workload, kernel class, clips per GPU): bytes per launch, source hash at capture
     (HEADLINE, "attention", 8): {"bytes_per_launch": 112.97e6, "sha1": "c3ea96cde7113f36aa824c2a3c2c97a1ef011005"},
-    (HEADLINE, "layernorm", 8): {"bytes_per_launch": 68.89e6, "sha1": "bb9dc2d3ba2669d1d4fc0c56aa91f83c297e13cc"},
-    (HEADLINE, "gemm_qkv", 8): {"bytes_per_launch": 85.49e6, "sha1": "8efbd5e9fbf917cb3d824db549cee4fd2f037b5a"},
-    (HEADLINE, "gemm_out", 8): {"bytes_per_launch": 103.15e6, "sha1": "8efbd5e9fbf917cb3d824db549cee4fd2f037b5a"},
-    (HEADLINE, "gemm_up", 8): {"bytes_per_launch": 120.79e6, "sha1": "8efbd5e9fbf917cb3d824db549cee4fd2f037b5a"},
-    (HEADLINE, "gemm_down", 8): {"bytes_per_launch": 218.81e6, "sha1": "8efbd5e9fbf917cb3d824db549cee4fd2f037b5a"},
+    (HEADLINE, "layernorm", 8): {"bytes_per_launch": 69.09e6, "sha1": "b53000d930718a6c2dd65abaa989ac2de36953e9"},
+    (HEADLINE, "gemm_qkv", 8): {"bytes_per_launch": 85.63e6, "sha1": "dd86544a515733d19bbea5190dd57560c8e166be"},
+    (HEADLINE, "gemm_out", 8): {"bytes_per_launch": 103.07e6, "sha1": "dd86544a515733d19bbea5190dd57560c8e166be"},
+    (HEADLINE, "gemm_up", 8): {"bytes_per_launch": 120.52e6, "sha1": "dd86544a515733d19bbea5190dd57560c8e166be"},
+    (HEADLINE, "gemm_down", 8): {"bytes_per_launch": 219.05e6, "sha1": "dd86544a515733d19bbea5190dd57560c8e166be"},
 }
 
 
