@@ -195,8 +195,19 @@ jepa_status jepa_encode(jepa_context* c, const float* d_pixels, int32_t B, int32
 jepa_status jepa_encode_host(jepa_context* c, const float* h_pixels, int32_t B, int32_t T, int32_t H,
                              int32_t W, int32_t layout, float* h_tokens);
 
-/* Wait for the context stream and report device-side errors (JEPA_E_TIMEOUT) raised since the
- * last check. */
+/* Pipelined form of jepa_encode_host for streams of clips: enqueues the upload of h_pixels, the
+ * encode and the download of the tokens into h_tokens, and returns without waiting. The context
+ * holds two device slots for uploads and two for downloads on streams of their own, so the copies
+ * of one call run under the encodes of its neighbours (pinned host memory is needed for that
+ * overlap; pageable memory works but serialises). Both host buffers must stay valid and
+ * untouched until jepa_context_sync returns; the tokens are bit-identical to jepa_encode_host's.
+ * Argument errors are returned at once and enqueue nothing; JEPA_E_OOM if the four slots
+ * (2 x (max pixels + max tokens) floats, allocated by the first call) do not fit. */
+jepa_status jepa_encode_host_async(jepa_context* c, const float* h_pixels, int32_t B, int32_t T, int32_t H,
+                                   int32_t W, int32_t layout, float* h_tokens);
+
+/* Wait for the context stream (and the copies of jepa_encode_host_async) and report device-side
+ * errors (JEPA_E_TIMEOUT) raised since the last check. */
 jepa_status jepa_context_sync(jepa_context* c);
 
 /* Per-kernel timing of the encode launch sequence (the measurement side of "Architecture",

@@ -216,6 +216,16 @@ class Context:
         check(lib().jepa_encode_host(self._h, _ptr(pixels), B, T, H, W, layout, _ptr(out)))
         return out
 
+    def encode_host_async(self, pixels: torch.Tensor, out: torch.Tensor, layout: int = LAYOUT_TCHW) -> torch.Tensor:
+        """Pipelined host encode: enqueues upload, encode and download and returns at once; the copies
+        overlap the neighbouring calls' encodes (pinned buffers). `pixels` and `out` must stay alive
+        and untouched until sync()."""
+        assert not pixels.is_cuda and pixels.dtype == torch.float32 and pixels.is_contiguous()
+        assert not out.is_cuda and out.dtype == torch.float32 and out.is_contiguous()
+        B, T, H, W = _clip_dims(pixels, layout)
+        check(lib().jepa_encode_host_async(self._h, _ptr(pixels), B, T, H, W, layout, _ptr(out)))
+        return out
+
     def sync(self):
         check(lib().jepa_context_sync(self._h))
 

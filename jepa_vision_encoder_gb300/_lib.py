@@ -97,6 +97,7 @@ SIGNATURES = {
     "jepa_context_launches": (_I, [_P, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_int32)]),
     "jepa_encode": (_I, [_P, _P, _I, _I, _I, _I, _I, _P]),
     "jepa_encode_host": (_I, [_P, _P, _I, _I, _I, _I, _I, _P]),
+    "jepa_encode_host_async": (_I, [_P, _P, _I, _I, _I, _I, _I, _P]),
     "jepa_context_sync": (_I, [_P]),
     "jepa_context_set_profiling": (_I, [_P, _I]),
     "jepa_context_profile": (_I, [_P, ctypes.POINTER(KernelStat), _I, ctypes.POINTER(ctypes.c_int32), _I]),

@@ -716,6 +716,15 @@ struct jepa_context {
   std::vector<Rec> grecs;
   int prof_launches[16] = {};
   double prof_ms[16] = {}, prof_flops[16] = {}, prof_bytes[16] = {};
+  // pipelined host encodes: two device slots each for the pixels coming in and the tokens going
+  // out, uploads and downloads on their own streams, so a step's copies overlap other steps'
+  // encodes (allocated by the first jepa_encode_host_async)
+  bool hp_ready = false;
+  float* hp_pix[2] = {nullptr, nullptr};
+  float* hp_tok[2] = {nullptr, nullptr};
+  cudaStream_t hp_up = nullptr, hp_down = nullptr;
+  cudaEvent_t hp_uploaded[2] = {}, hp_pix_free[2] = {}, hp_tok_ready[2] = {}, hp_downloaded[2] = {};
+  long long hp_step = 0;
 };
 
 namespace {
@@ -803,6 +812,20 @@ extern "C" void jepa_context_free(jepa_context* c) {
   if (!c) return;
   cudaSetDevice(c->m->device);
   if (c->stream) cudaStreamSynchronize(c->stream);
+  if (c->hp_ready) {
+    cudaStreamSynchronize(c->hp_up);
+    cudaStreamSynchronize(c->hp_down);
+    for (int s = 0; s < 2; ++s) {
+      cudaFree(c->hp_pix[s]);
+      cudaFree(c->hp_tok[s]);
+      cudaEventDestroy(c->hp_uploaded[s]);
+      cudaEventDestroy(c->hp_pix_free[s]);
+      cudaEventDestroy(c->hp_tok_ready[s]);
+      cudaEventDestroy(c->hp_downloaded[s]);
+    }
+    cudaStreamDestroy(c->hp_up);
+    cudaStreamDestroy(c->hp_down);
+  }
   if (c->gexec) cudaGraphExecDestroy(c->gexec);
   for (cudaEvent_t e : c->ev_pool) cudaEventDestroy(e);
   for (cudaEvent_t e : c->gev) cudaEventDestroy(e);
@@ -1170,10 +1193,79 @@ extern "C" jepa_status jepa_encode_host(jepa_context* c, const float* h_pixels, 
   return jepa_context_sync(c);
 }
 
+namespace {
+jepa_status host_pipeline_init(jepa_context* c) {
+  if (c->hp_ready) return JEPA_OK;
+  const size_t pix_bytes = (size_t)c->max_pix * sizeof(float);
+  const size_t tok_bytes = (size_t)c->max_rows * c->m->hp.embed_dim * sizeof(float);
+  for (int s = 0; s < 2; ++s) {
+    if (cudaMalloc(&c->hp_pix[s], pix_bytes) != cudaSuccess || cudaMalloc(&c->hp_tok[s], tok_bytes) != cudaSuccess) {
+      cudaGetLastError();
+      for (int t = 0; t <= s; ++t) {
+        cudaFree(c->hp_pix[t]);
+        cudaFree(c->hp_tok[t]);
+        c->hp_pix[t] = c->hp_tok[t] = nullptr;
+      }
+      return fail(JEPA_E_OOM, "pipelined host encode: cudaMalloc of 2 x (%zu + %zu) bytes failed", pix_bytes,
+                  tok_bytes);
+    }
+  }
+  CUDA_TRY(cudaStreamCreateWithFlags(&c->hp_up, cudaStreamNonBlocking));
+  CUDA_TRY(cudaStreamCreateWithFlags(&c->hp_down, cudaStreamNonBlocking));
+  for (int s = 0; s < 2; ++s) {
+    CUDA_TRY(cudaEventCreateWithFlags(&c->hp_uploaded[s], cudaEventDisableTiming));
+    CUDA_TRY(cudaEventCreateWithFlags(&c->hp_pix_free[s], cudaEventDisableTiming));
+    CUDA_TRY(cudaEventCreateWithFlags(&c->hp_tok_ready[s], cudaEventDisableTiming));
+    CUDA_TRY(cudaEventCreateWithFlags(&c->hp_downloaded[s], cudaEventDisableTiming));
+    // recorded once on the idle streams so that the first waits on them pass
+    CUDA_TRY(cudaEventRecord(c->hp_pix_free[s], c->stream));
+    CUDA_TRY(cudaEventRecord(c->hp_downloaded[s], c->hp_down));
+  }
+  c->hp_ready = true;
+  return JEPA_OK;
+}
+}  // namespace
+
+extern "C" jepa_status jepa_encode_host_async(jepa_context* c, const float* h_pixels, int32_t B, int32_t T,
+                                              int32_t H, int32_t W, int32_t layout, float* h_tokens) {
+  if (!c) return fail(JEPA_E_INVALID_ARG, "jepa_encode_host_async: null context");
+  Geo g;
+  jepa_status st = check_shape(c, h_pixels, B, T, H, W, layout, h_tokens, &g);
+  if (st != JEPA_OK) return st;
+  CUDA_TRY(cudaSetDevice(c->m->device));
+  st = host_pipeline_init(c);
+  if (st != JEPA_OK) return st;
+  const int s = (int)(c->hp_step & 1);
+  const size_t pix_bytes = (size_t)B * T * c->m->hp.in_chans * H * W * sizeof(float);
+  const size_t tok_bytes = (size_t)B * g.N * c->m->hp.embed_dim * sizeof(float);
+  // upload into slot s once the encode two steps back has taken its pixels out of it
+  CUDA_TRY(cudaStreamWaitEvent(c->hp_up, c->hp_pix_free[s], 0));
+  CUDA_TRY(cudaMemcpyAsync(c->hp_pix[s], h_pixels, pix_bytes, cudaMemcpyHostToDevice, c->hp_up));
+  CUDA_TRY(cudaEventRecord(c->hp_uploaded[s], c->hp_up));
+  // the encode reads its own staging buffers (one captured graph serves every step)
+  CUDA_TRY(cudaStreamWaitEvent(c->stream, c->hp_uploaded[s], 0));
+  CUDA_TRY(cudaMemcpyAsync(c->pix_stage, c->hp_pix[s], pix_bytes, cudaMemcpyDeviceToDevice, c->stream));
+  CUDA_TRY(cudaEventRecord(c->hp_pix_free[s], c->stream));
+  st = jepa_encode(c, c->pix_stage, B, T, H, W, layout, c->tok_stage);
+  if (st != JEPA_OK) return st;
+  CUDA_TRY(cudaStreamWaitEvent(c->stream, c->hp_downloaded[s], 0));  // slot s's last download is done
+  CUDA_TRY(cudaMemcpyAsync(c->hp_tok[s], c->tok_stage, tok_bytes, cudaMemcpyDeviceToDevice, c->stream));
+  CUDA_TRY(cudaEventRecord(c->hp_tok_ready[s], c->stream));
+  CUDA_TRY(cudaStreamWaitEvent(c->hp_down, c->hp_tok_ready[s], 0));
+  CUDA_TRY(cudaMemcpyAsync(h_tokens, c->hp_tok[s], tok_bytes, cudaMemcpyDeviceToHost, c->hp_down));
+  CUDA_TRY(cudaEventRecord(c->hp_downloaded[s], c->hp_down));
+  ++c->hp_step;
+  return JEPA_OK;
+}
+
 extern "C" jepa_status jepa_context_sync(jepa_context* c) {
   if (!c) return fail(JEPA_E_INVALID_ARG, "jepa_context_sync: null context");
   CUDA_TRY(cudaSetDevice(c->m->device));
   CUDA_TRY(cudaStreamSynchronize(c->stream));
+  if (c->hp_ready) {
+    CUDA_TRY(cudaStreamSynchronize(c->hp_up));
+    CUDA_TRY(cudaStreamSynchronize(c->hp_down));
+  }
   int h_err = 0;
   CUDA_TRY(cudaMemcpy(&h_err, c->err, sizeof(int), cudaMemcpyDeviceToHost));
   if (h_err) {

@@ -117,6 +117,29 @@ def test_graph_replay_and_host_api_match_eager():
     assert torch.equal(host, eager.cpu())
 
 
+def test_pipelined_host_encodes_match_the_synchronous_ones():
+    """Several jepa_encode_host_async calls in flight (uploads and downloads overlapping other
+    calls' encodes, the two device slots each reused) give the synchronous call's bits, per call."""
+    name = "vjepa2_vitl16_16x256"
+    cfg, dtype, (T, H, W) = small(name)
+    model, ctx = make(name, n_layer=2, batch=2, T=T, H=H, W=W)
+    ctx.set_graph(True)
+    clips = [torch.from_numpy(synth.pixels(20 + i, (2, T, 3, H, W))).pin_memory() for i in range(5)]
+    ref = [ctx.encode_host(c).clone() for c in clips]
+    outs = [torch.empty_like(r).pin_memory() for r in ref]
+    for c, o in zip(clips, outs):
+        ctx.encode_host_async(c, o)
+    ctx.sync()
+    for i, (o, r) in enumerate(zip(outs, ref)):
+        assert torch.equal(o, r), f"call {i}"
+    # one clip of a different batch size through the same slots, then the first clip again
+    small_out = torch.empty((1,) + ref[0].shape[1:]).pin_memory()
+    ctx.encode_host_async(clips[1][:1].contiguous().pin_memory(), small_out)
+    ctx.encode_host_async(clips[0], outs[0])
+    ctx.sync()
+    assert torch.equal(small_out, ref[1][:1]) and torch.equal(outs[0], ref[0])
+
+
 @pytest.mark.parametrize("name", ["vjepa2_vitl16_16x256", "hfvit_ti14_224"])
 def test_programmatic_launches_change_nothing(name):
     # the same kernels with and without programmatic dependent launch, eager and graph replay
