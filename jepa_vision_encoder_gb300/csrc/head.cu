@@ -251,13 +251,6 @@ __global__ void pool_kernel(const float* __restrict__ x, int N, int D, int prefi
   }
 }
 
-int blocks_for(long long work, int threads) {
-  long long b = (work + threads - 1) / threads;
-  const long long cap = (long long)num_sms() * 16;
-  if (b > cap) b = cap;
-  return (int)(b < 1 ? 1 : b);
-}
-
 cudaError_t rowvec_launch(const float* x, int R, int K, const void* W, int N, const float* bias, const float* res,
                           float* y, bool gelu, cudaStream_t s) {
   const int grid = std::max(1, std::min((N + kRvWarps - 1) / kRvWarps, num_sms() * 8));
