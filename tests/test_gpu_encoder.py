@@ -140,6 +140,25 @@ def test_pipelined_host_encodes_match_the_synchronous_ones():
     assert torch.equal(small_out, ref[1][:1]) and torch.equal(outs[0], ref[0])
 
 
+def test_pipelined_host_refusals_and_mixing_with_the_synchronous_call():
+    name = "vjepa2_vitl16_16x256"
+    cfg, dtype, (T, H, W) = small(name)
+    model, ctx = make(name, n_layer=1, batch=2, T=T, H=H, W=W)
+    clip = torch.from_numpy(synth.pixels(30, (2, T, 3, H, W))).pin_memory()
+    ref = ctx.encode_host(clip).clone()
+    too_big = torch.from_numpy(synth.pixels(31, (3, T, 3, H, W))).pin_memory()
+    out3 = torch.empty((3,) + ref.shape[1:]).pin_memory()
+    with pytest.raises(jv.JepaError) as e:
+        ctx.encode_host_async(too_big, out3)  # over the context's batch: refused, nothing enqueued
+    assert e.value.status == jv._lib.E_BUDGET
+    a, b = torch.empty_like(ref).pin_memory(), torch.empty_like(ref).pin_memory()
+    ctx.encode_host_async(clip, a)
+    mid = ctx.encode_host(clip)            # a synchronous call between pipelined ones
+    ctx.encode_host_async(clip, b)
+    ctx.sync()
+    assert torch.equal(a, ref) and torch.equal(mid, ref) and torch.equal(b, ref)
+
+
 @pytest.mark.parametrize("name", ["vjepa2_vitl16_16x256", "hfvit_ti14_224"])
 def test_programmatic_launches_change_nothing(name):
     # the same kernels with and without programmatic dependent launch, eager and graph replay
