@@ -67,10 +67,10 @@ FLUSH_BYTES = 256 << 20  # > 129 MB of L2
 NCU_TRAFFIC = {  # (workload, kernel class, clips per GPU): bytes per launch, source hash at capture
     (HEADLINE, "attention", 8): {"bytes_per_launch": 112.97e6, "sha1": "c3ea96cde7113f36aa824c2a3c2c97a1ef011005"},
     (HEADLINE, "layernorm", 8): {"bytes_per_launch": 69.09e6, "sha1": "b53000d930718a6c2dd65abaa989ac2de36953e9"},
-    (HEADLINE, "gemm_qkv", 8): {"bytes_per_launch": 85.53e6, "sha1": "570a8f2459946cf21770f5576f8b2be2435571ee"},
-    (HEADLINE, "gemm_out", 8): {"bytes_per_launch": 103.15e6, "sha1": "570a8f2459946cf21770f5576f8b2be2435571ee"},
-    (HEADLINE, "gemm_up", 8): {"bytes_per_launch": 120.62e6, "sha1": "570a8f2459946cf21770f5576f8b2be2435571ee"},
-    (HEADLINE, "gemm_down", 8): {"bytes_per_launch": 219.59e6, "sha1": "570a8f2459946cf21770f5576f8b2be2435571ee"},
+    (HEADLINE, "gemm_qkv", 8): {"bytes_per_launch": 85.63e6, "sha1": "dd86544a515733d19bbea5190dd57560c8e166be"},
+    (HEADLINE, "gemm_out", 8): {"bytes_per_launch": 103.07e6, "sha1": "dd86544a515733d19bbea5190dd57560c8e166be"},
+    (HEADLINE, "gemm_up", 8): {"bytes_per_launch": 120.52e6, "sha1": "dd86544a515733d19bbea5190dd57560c8e166be"},
+    (HEADLINE, "gemm_down", 8): {"bytes_per_launch": 219.05e6, "sha1": "dd86544a515733d19bbea5190dd57560c8e166be"},
 }
 
 

@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Returns 64, 128, 256, or kPairTile for the 2-SM kernel.
 int gemm_tc_pick_bn(int M, int N) {
   const int sms = num_sms();
-  const int num_m = (M + kBM - 1) / kBM;
+  const int num_m = (M + kBM - 1) / kBM, num_m2 = (M + 2 * kBM - 1) / (2 * kBM);
   int best = 0;
   double best_cost = 1e30;
   const struct { int bn; double eff; } one[] = {{256, 0.62}, {128, 0.48}, {64, 0.29}};
@@ -213,19 +213,15 @@ int gemm_tc_pick_bn(int M, int N) {
     if (cost < best_cost) best_cost = cost, best = c.bn;
   }
   if (N % 256 == 0 && sms >= 2) {
-    // full waves of 256 x 256 tiles, plus a last wave of halves (taken as 0.65 of a tile: half
-    // the work at the 256 x 128 shape's lower rate) or of whole tiles
-    const PairPlan pl = gemm_tc2_plan(M, N);
+    const long long pair_tiles = (long long)num_m2 * (N / 256);
     const int pairs = gemm_tc2_max_pairs();
-    const double tail = pl.units > pl.first_half ? 0.65 : 0.0;
-    const double cost = ((double)(pl.first_half / pairs) + (pl.first_half % pairs ? 1.0 : 0.0) + tail) * 256 / 0.75;
+    const double cost = (double)((pair_tiles + pairs - 1) / pairs) * 256 / 0.75;
     if (cost < best_cost) best_cost = cost, best = kPairTile;
   }
   return best ? best : 64;
 }
 
-// The pair kernel loads its 128 B rows per CTA as two 64-row boxes (one for a half tile).
-int gemm_tc_b_box(int bn) { return bn == kPairTile ? 64 : bn; }
+int gemm_tc_b_box(int bn) { return bn == kPairTile ? 128 : bn; }
 
 template <int BN, int EK>
 static cudaError_t launch_bn(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmO,

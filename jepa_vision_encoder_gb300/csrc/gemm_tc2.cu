@@ -8,9 +8,6 @@
 // peer's). (A 256 x 128 pair tile, measured, was slower than both this and the 1-SM tiles at
 // every encoder shape.) Tiles are numbered N-fastest: the pairs working at the same time share rows of A (read from
 // HBM once) and sweep the weights B, which stay in L2.
-// A last wave that would leave more than half of the pairs idle (256 tiles over 76 pairs: 3.37
-// waves) is cut into 256 x 128 halves, one per pair: every output element still takes its whole
-// K range in one accumulator, in the same order, so results do not depend on the plan.
 //
 // Per CTA (320 threads, one CTA per SM, grid = 2 x pairs, tiles strided over pairs):
 //   warp 0      TMA producer of this CTA's halves; every copy of the pair completes on the even
@@ -36,7 +33,6 @@ constexpr int kBK = 64;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kEpiBytes = kEpiWarps * 4096;          // two 2 KB staging buffers per epilogue warp
-constexpr uint32_t kBBoxBytes = 64 * kBK * 2;        // one 64-row box of B: 8 KB
 
 template <int TN>
 struct PairCfg {
@@ -49,23 +45,11 @@ struct PairCfg {
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kEpiBytes + 512;
 };
 
-// Work unit u of a plan: a 256 x 256 tile (u < first_half) or one 256 x 128 half of tile
-// first_half + (u - first_half) / 2.
-struct Unit {
-  int m_blk, n0, wide;
-};
-__device__ __forceinline__ Unit unit_of(int u, int first_half, int num_n) {
-  if (u < first_half) return {u / num_n, (u % num_n) * 256, 1};
-  const int h = u - first_half, t = first_half + (h >> 1);
-  return {t / num_n, (t % num_n) * 256 + (h & 1) * 128, 0};
-}
-
 template <int TN, int EK>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const __grid_constant__ CUtensorMap tmO, EpiArgs epi, int M, int N, int K, int num_units,
-                    int first_half, int* err, uint64_t limit_ns) {
-  static_assert(TN == 256, "the unit plan assumes 256-column tiles");
+                    const __grid_constant__ CUtensorMap tmO, EpiArgs epi, int M, int N, int K, int* err,
+                    uint64_t limit_ns) {
   using C = PairCfg<TN>;
   constexpr int kStages = C::kStages, kTileN = TN;
   extern __shared__ uint8_t smem_raw[];
@@ -87,7 +71,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
   const int pair = blockIdx.x >> 1, num_pairs = gridDim.x >> 1;
-  const int num_n = N / kTileN, num_k = K / kBK;
+  const int num_m = (M + kTileM - 1) / kTileM, num_n = N / kTileN, num_k = K / kBK;
+  const int num_tiles = num_m * num_n;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -127,27 +112,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0, armed = 0, armed_phase = 0;
       bool ok = true;
-      for (int u = pair; u < num_units && ok; u += num_pairs) {
-        const Unit un = unit_of(u, first_half, num_n);
-        // B rows of this CTA: 128 (two 64-row boxes) of a whole tile, 64 of a half
-        const int m0 = un.m_blk * kTileM + (int)rank * 128, n0 = un.n0 + (int)rank * (un.wide ? 128 : 64);
-        const uint32_t bytes = 2u * (C::kABytes + (un.wide ? 2 : 1) * kBBoxBytes);
+      for (int tile = pair; tile < num_tiles && ok; tile += num_pairs) {
+        const int m0 = (tile / num_n) * kTileM + (int)rank * 128, n0 = (tile % num_n) * kTileN + (int)rank * C::kBRows;
         for (int kb = 0; kb < num_k; ++kb) {
           if (!mbar_wait(smem_u32(empty + stage), phase ^ 1u, wc)) {
             ok = false;
             break;
           }
           const uint32_t fb_even = mapa_shared(smem_u32(full + stage), 0);
-          if (rank == 0) mbar_arrive_expect_tx(smem_u32(full + stage), bytes);
+          if (rank == 0) mbar_arrive_expect_tx(smem_u32(full + stage), 2 * C::kStageBytes);
           if (EK == kEpiResidual)  // A (attention output, FFN hidden) is read once: let it go first
             tma_load_2d_pair_hint(smem_u32(sA + stage * C::kABytes), &tmA, fb_even, kb * kBK, m0, a_policy);
           else
             tma_load_2d_pair(smem_u32(sA + stage * C::kABytes), &tmA, fb_even, kb * kBK, m0);
-          // weights: every M tile reads them. Two 64-row boxes stacked make the 128-row
-          // swizzled layout of one (8-row groups 1024 bytes apart).
-          const uint32_t sb = smem_u32(sB + stage * C::kBBytes);
-          tma_load_2d_pair_hint(sb, &tmB, fb_even, kb * kBK, n0, b_policy);
-          if (un.wide) tma_load_2d_pair_hint(sb + kBBoxBytes, &tmB, fb_even, kb * kBK, n0 + 64, b_policy);
+          tma_load_2d_pair_hint(smem_u32(sB + stage * C::kBBytes), &tmB, fb_even, kb * kBK, n0, b_policy);  // weights: every M tile
           armed |= 1u << stage;
           armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
           if (++stage == kStages) {
@@ -165,15 +143,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (rank == 0) {
       // even CTA: the MMA issuer of the pair. The whole warp runs the issue loop (waits and
       // descriptor arithmetic warp-uniform); one elected lane issues each MMA and commit.
-      constexpr uint32_t idesc_wide = idesc_bf16_f32(kTileM, kTileN, 0, 0);
-      constexpr uint32_t idesc_half = idesc_bf16_f32(kTileM, kTileN / 2, 0, 0);
+      constexpr uint32_t idesc = idesc_bf16_f32(kTileM, kTileN, 0, 0);
       const uint64_t a_desc = smem_desc_sw128(smem_u32(sA), 1024, 1024);  // stage 0; stages and K
       const uint64_t b_desc = smem_desc_sw128(smem_u32(sB), 1024, 1024);  // steps move the address
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      for (int u = pair; u < num_units && ok; u += num_pairs) {
-        const uint32_t idesc = unit_of(u, first_half, num_n).wide ? idesc_wide : idesc_half;
+      for (int tile = pair; tile < num_tiles && ok; tile += num_pairs) {
         if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(tempty + acc), acc_phase ^ 1u, wc))) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kTileN);
@@ -206,23 +182,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else {
     const int q = warp & 3;                    // TMEM lane quarter this warp may access
     constexpr int kChunks = kTileN / 32 / 2;   // 32-column chunks per warp (half the columns)
-    constexpr int kHalfChunks = kChunks / 2;   // the same for a 128-column half tile
     const int half = (warp - 2) >> 2;  // which of the two warps on this lane quarter
     const uint32_t tempty_even = mapa_shared(smem_u32(tempty), 0);
     EpiStage stage{sEpi + (warp - 2) * 4096, 0};
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int u = pair; u < num_units; u += num_pairs) {
-      const Unit un = unit_of(u, first_half, num_n);
-      const int m0 = un.m_blk * kTileM + (int)rank * 128;
+    for (int tile = pair; tile < num_tiles; tile += num_pairs) {
+      const int m0 = (tile / num_n) * kTileM + (int)rank * 128, n0 = (tile % num_n) * kTileN;
       if (!mbar_wait(smem_u32(tfull + acc), acc_phase, wc)) break;
       tc_fence_after();
       const int y0 = m0 + q * 32;
       const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kTileN);
-      if (un.wide)
-        epi_warp_tile<EK, kChunks>(epi, &tmO, stage, lane, trow, y0, un.n0, half);
-      else
-        epi_warp_tile<EK, kHalfChunks>(epi, &tmO, stage, lane, trow, y0, un.n0, half);
+      epi_warp_tile<EK, kChunks>(epi, &tmO, stage, lane, trow, y0, n0, half);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(tempty_even + (uint32_t)(acc * sizeof(uint64_t)));
@@ -260,9 +231,11 @@ cudaError_t set_pair_attrs() {
 template <int TN, int EK>
 cudaError_t launch_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmO, const EpiArgs& epi,
                         int M, int N, int K, int* err, uint64_t limit_ns, cudaStream_t s) {
-  const PairPlan pl = gemm_tc2_plan(M, N);
-  return launch_kernel(gemm_tc2_kernel<TN, EK>, dim3(2 * pl.pairs), dim3(kThreads), PairCfg<TN>::kSmemBytes, s, tmA,
-                       tmB, tmO, epi, M, N, K, pl.units, pl.first_half, err, limit_ns);
+  const int tiles = ((M + kTileM - 1) / kTileM) * (N / TN);
+  const int max_pairs = gemm_tc2_max_pairs();
+  const int pairs = tiles < max_pairs ? tiles : max_pairs;
+  return launch_kernel(gemm_tc2_kernel<TN, EK>, dim3(2 * pairs), dim3(kThreads), PairCfg<TN>::kSmemBytes, s, tmA, tmB,
+                       tmO, epi, M, N, K, err, limit_ns);
 }
 
 template <int TN>
@@ -298,19 +271,6 @@ int gemm_tc2_max_pairs() {
     cached = n < num_sms() / 2 ? n : num_sms() / 2;
   }
   return cached;
-}
-
-PairPlan gemm_tc2_plan(int M, int N) {
-  const int full = ((M + kTileM - 1) / kTileM) * (N / 256);
-  const int P = gemm_tc2_max_pairs();
-  const int rest = full % P;  // tiles of the last wave (all of them when full < P)
-  PairPlan pl{full, full, 0};
-  if (rest > 0 && 2 * rest <= P) {
-    pl.first_half = full - rest;
-    pl.units = full + rest;
-  }
-  pl.pairs = pl.units < P ? pl.units : P;
-  return pl;
 }
 
 cudaError_t gemm_tc2_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmO,

@@ -274,7 +274,7 @@ struct HeadLayer {
   const void *w_qkv, *w_out, *w_up, *w_down;
   CUtensorMap tm_qkv[3], tm_out[3], tm_up[3], tm_down[3];
 };
-int slot(int bn) { return gemm_tc_b_slot(bn); }
+int slot(int bn) { return bn == 64 ? 0 : ((bn == 128 || bn == kPairTile) ? 1 : 2); }
 
 enum HeadClass { kHLn, kHQkv, kHAttn, kHOut, kHUp, kHDown, kHLnKv, kHKv, kHQuery, kHXattn, kHLn2, kHMlpUp, kHMlpDown,
                  kHCls, kHClasses };

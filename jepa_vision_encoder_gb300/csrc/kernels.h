@@ -52,25 +52,12 @@ uint64_t default_wait_limit_ns();
 
 // tcgen05 GEMM: out = epilogue(A[M,K] * B[N,K]^T), bf16 operands. tmA box 128x64, tmB box
 // gemm_tc_b_box(BN) x 64 where BN = gemm_tc_pick_bn(M, N); BN == kPairTile selects the 2-SM
-// (cluster pair) kernel with 256 x 256 tiles (256 x 128 halves in a short last wave). tmO =
-// make_tmap_2d_out over epi.out (bf16 for BIAS / GELU / QKV_ROPE, fp32 for RESIDUAL; unused for
-// PATCH, which stores from registers).
+// (cluster pair) kernel with 256 x 256 tiles. tmO = make_tmap_2d_out over epi.out (bf16 for
+// BIAS / GELU / QKV_ROPE, fp32 for RESIDUAL; unused for PATCH, which stores from registers).
 constexpr int kPairTile = 512;
 int gemm_tc_pick_bn(int M, int N);
 int gemm_tc_b_box(int bn);
-// Index of the B box among the weight maps a model keeps per matrix (box rows 64 / 128 / 256).
-inline int gemm_tc_b_slot(int bn) {
-  const int box = gemm_tc_b_box(bn);
-  return box == 64 ? 0 : (box == 128 ? 1 : 2);
-}
 int gemm_tc2_max_pairs();
-// Work plan of the pair kernel for an M x N output: `units` work units, the first `first_half`
-// of them 256 x 256 tiles and the rest 256 x 128 halves of the last `units - first_half` / 2
-// tiles. A last wave that would keep at most half of the pairs busy is split into halves.
-struct PairPlan {
-  int units, first_half, pairs;
-};
-PairPlan gemm_tc2_plan(int M, int N);
 cudaError_t gemm_tc2_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmO,
                             const EpiArgs& epi, int M, int N, int K, int* err, uint64_t limit_ns, cudaStream_t s);
 cudaError_t gemm_tc_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmO, int BN,

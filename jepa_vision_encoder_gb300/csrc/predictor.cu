@@ -125,7 +125,7 @@ struct PredLayer {
   const void *w_qkv, *w_out, *w_up, *w_down;
   CUtensorMap tm_qkv[3], tm_out[3], tm_up[3], tm_down[3];  // B boxes of 64 / 128 / 256 rows
 };
-int slot(int bn) { return gemm_tc_b_slot(bn); }
+int slot(int bn) { return bn == 64 ? 0 : ((bn == 128 || bn == kPairTile) ? 1 : 2); }
 }  // namespace
 
 struct jepa_predictor {

@@ -249,7 +249,7 @@ struct LayerW {
   const void *w_qkv, *w_out, *w_up, *w_down;
   CUtensorMap tm_qkv[3], tm_out[3], tm_up[3], tm_down[3];  // box rows 64 / 128 / 256
 };
-int bn_slot(int bn) { return gemm_tc_b_slot(bn); }
+int bn_slot(int bn) { return bn == 64 ? 0 : ((bn == 128 || bn == kPairTile) ? 1 : 2); }
 }  // namespace
 
 struct jepa_model {
