@@ -694,6 +694,7 @@ struct jepa_context {
   // per-shape state
   int kB = -1, kT = -1, kH = -1, kW = -1;
   CUtensorMap tm_Pm, tm_Xn, tm_ao, tm_Hh, tm_qkv3;
+  CUtensorMap tm_Pm64, tm_Xn64, tm_ao64, tm_Hh64;  // 64-row boxes: A quarters of the 4-CTA GEMM
   CUtensorMap tm_o_qkv, tm_o_hh, tm_o_x;  // GEMM outputs: qkv and Hh (bf16), X (fp32 residual adds)
   int bn_patch = 0, bn_qkv = 0, bn_out = 0, bn_up = 0, bn_down = 0;
   // graph replay
@@ -903,6 +904,10 @@ jepa_status prepare_shape(jepa_context* c, int B, int T, int H, int W, const Geo
     ok &= make_tmap_2d_bf16(&c->tm_Xn, c->Xn, M, D, 128);
     ok &= make_tmap_2d_bf16(&c->tm_ao, c->ao, M, D, 128);
     ok &= make_tmap_2d_bf16(&c->tm_Hh, c->Hh, M, F, 128);
+    ok &= make_tmap_2d_bf16(&c->tm_Pm64, c->Pm, Mp, m->K, 64);
+    ok &= make_tmap_2d_bf16(&c->tm_Xn64, c->Xn, M, D, 64);
+    ok &= make_tmap_2d_bf16(&c->tm_ao64, c->ao, M, D, 64);
+    ok &= make_tmap_2d_bf16(&c->tm_Hh64, c->Hh, M, F, 64);
     ok &= make_tmap_3d_bf16(&c->tm_qkv3, c->qkv, B, g.N, 3 * D, 128);
     ok &= make_tmap_2d_out(&c->tm_o_qkv, c->qkv, M, 3 * D, 2);
     ok &= make_tmap_2d_out(&c->tm_o_hh, c->Hh, M, F, 2);
@@ -1040,7 +1045,7 @@ jepa_status launch_encode(jepa_context* c, const float* pix, int B, int T, int H
   pe.pos = c->pos_clip;
   pe.vec = m->mod;
   CUDA_TRY(prof(c, kPGemmPatch, 2.0 * dMp * dD * dK, 0.0, [&] {
-    return bf ? gemm_tc_launch(c->tm_Pm, m->tm_patch[bn_slot(c->bn_patch)], c->tm_o_x, c->bn_patch, pe, Mp, D, m->K, c->err, lim, s)
+    return bf ? gemm_tc_launch(c->tm_Pm, m->tm_patch[bn_slot(c->bn_patch)], c->tm_o_x, c->bn_patch, pe, Mp, D, m->K, c->err, lim, s, &c->tm_Pm64)
               : gemm_simt_launch(reinterpret_cast<const float*>(c->Pm), reinterpret_cast<const float*>(m->w_patch), pe,
                                  Mp, D, m->K, s);
   }));
@@ -1078,7 +1083,7 @@ jepa_status launch_encode(jepa_context* c, const float* pix, int B, int T, int H
     EpiArgs de = make_epi(kEpiResidual, M, D, w.b_down, c->X);
     const float* Xn = reinterpret_cast<const float*>(c->Xn);
     CUDA_TRY(prof(c, kPGemmQkv, 2.0 * dM * 3.0 * dD * dD, 0.0, [&] {
-      return bf ? gemm_tc_launch(c->tm_Xn, w.tm_qkv[bn_slot(c->bn_qkv)], c->tm_o_qkv, c->bn_qkv, qe, M, 3 * D, D, c->err, lim, s)
+      return bf ? gemm_tc_launch(c->tm_Xn, w.tm_qkv[bn_slot(c->bn_qkv)], c->tm_o_qkv, c->bn_qkv, qe, M, 3 * D, D, c->err, lim, s, &c->tm_Xn64)
                 : gemm_simt_launch(Xn, reinterpret_cast<const float*>(w.w_qkv), qe, M, 3 * D, D, s);
     }));
     CUDA_TRY(prof(c, kPAttention, attn_flops, 0.0, [&] {
@@ -1086,18 +1091,18 @@ jepa_status launch_encode(jepa_context* c, const float* pix, int B, int T, int H
                 : attention_simt_launch(reinterpret_cast<const float*>(c->qkv), ap, s);
     }));
     CUDA_TRY(prof(c, kPGemmOut, 2.0 * dM * dD * dD, 0.0, [&] {
-      return bf ? gemm_tc_launch(c->tm_ao, w.tm_out[bn_slot(c->bn_out)], c->tm_o_x, c->bn_out, oe, M, D, D, c->err, lim, s)
+      return bf ? gemm_tc_launch(c->tm_ao, w.tm_out[bn_slot(c->bn_out)], c->tm_o_x, c->bn_out, oe, M, D, D, c->err, lim, s, &c->tm_ao64)
                 : gemm_simt_launch(reinterpret_cast<const float*>(c->ao), reinterpret_cast<const float*>(w.w_out), oe,
                                    M, D, D, s);
     }));
     CUDA_TRY(prof(c, kPLn, 0.0, ln_bytes,
                   [&] { return layernorm_launch(c->X, M, D, w.ln2_w, w.ln2_b, hp.ln_eps, bf, c->Xn, s); }));
     CUDA_TRY(prof(c, kPGemmUp, 2.0 * dM * dF * dD, 0.0, [&] {
-      return bf ? gemm_tc_launch(c->tm_Xn, w.tm_up[bn_slot(c->bn_up)], c->tm_o_hh, c->bn_up, ue, M, F, D, c->err, lim, s)
+      return bf ? gemm_tc_launch(c->tm_Xn, w.tm_up[bn_slot(c->bn_up)], c->tm_o_hh, c->bn_up, ue, M, F, D, c->err, lim, s, &c->tm_Xn64)
                 : gemm_simt_launch(Xn, reinterpret_cast<const float*>(w.w_up), ue, M, F, D, s);
     }));
     CUDA_TRY(prof(c, kPGemmDown, 2.0 * dM * dD * dF, 0.0, [&] {
-      return bf ? gemm_tc_launch(c->tm_Hh, w.tm_down[bn_slot(c->bn_down)], c->tm_o_x, c->bn_down, de, M, D, F, c->err, lim, s)
+      return bf ? gemm_tc_launch(c->tm_Hh, w.tm_down[bn_slot(c->bn_down)], c->tm_o_x, c->bn_down, de, M, D, F, c->err, lim, s, &c->tm_Hh64)
                 : gemm_simt_launch(reinterpret_cast<const float*>(c->Hh), reinterpret_cast<const float*>(w.w_down), de,
                                    M, D, F, s);
     }));
@@ -1403,8 +1408,9 @@ extern "C" jepa_status jepa_op_linear(int32_t dtype, const void* d_x, int32_t M,
   jepa_status st = op_err_word(&err);
   if (st != JEPA_OK) return st;
   const int bn = gemm_tc_pick_bn(M, N);
-  CUtensorMap ta, tb, to;
-  if (!make_tmap_2d_bf16(&ta, d_x, M, K, 128) || !make_tmap_2d_bf16(&tb, d_w, N, K, gemm_tc_b_box(bn)))
+  CUtensorMap ta, ta64, tb, to;
+  if (!make_tmap_2d_bf16(&ta, d_x, M, K, 128) || !make_tmap_2d_bf16(&ta64, d_x, M, K, 64) ||
+      !make_tmap_2d_bf16(&tb, d_w, N, K, gemm_tc_b_box(bn)))
     return fail(JEPA_E_CUDA, "cuTensorMapEncodeTiled refused an operand");
   memset(&to, 0, sizeof to);
   // the patch embedding stores through TMA too when its rows are the patch rows themselves
@@ -1414,7 +1420,7 @@ extern "C" jepa_status jepa_op_linear(int32_t dtype, const void* d_x, int32_t M,
     if (!make_tmap_2d_out(&to, e.out, M, N, (e.kind == kEpiResidual || e.kind == kEpiPatch) ? 4 : 2))
       return fail(JEPA_E_CUDA, "cuTensorMapEncodeTiled refused the output");
   }
-  CUDA_TRY(gemm_tc_launch(ta, tb, to, bn, e, M, N, K, err, default_wait_limit_ns(), s));
+  CUDA_TRY(gemm_tc_launch(ta, tb, to, bn, e, M, N, K, err, default_wait_limit_ns(), s, &ta64));
   return JEPA_OK;
 }
 
