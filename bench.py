@@ -65,12 +65,12 @@ FLUSH_BYTES = 256 << 20  # > 129 MB of L2
 # captures of the 2048-token clips at 8 per GPU; `sha1` is the hash of the class's source files when
 # the counters were taken (a changed kernel reports traffic null until it is captured again).
 NCU_TRAFFIC = {  # (workload, kernel class, clips per GPU): bytes per launch, source hash at capture
-    (HEADLINE, "attention", 8): {"bytes_per_launch": 112.97e6, "sha1": "c3ea96cde7113f36aa824c2a3c2c97a1ef011005"},
-    (HEADLINE, "layernorm", 8): {"bytes_per_launch": 69.09e6, "sha1": "b53000d930718a6c2dd65abaa989ac2de36953e9"},
-    (HEADLINE, "gemm_qkv", 8): {"bytes_per_launch": 85.63e6, "sha1": "dd86544a515733d19bbea5190dd57560c8e166be"},
-    (HEADLINE, "gemm_out", 8): {"bytes_per_launch": 103.07e6, "sha1": "dd86544a515733d19bbea5190dd57560c8e166be"},
-    (HEADLINE, "gemm_up", 8): {"bytes_per_launch": 120.52e6, "sha1": "dd86544a515733d19bbea5190dd57560c8e166be"},
-    (HEADLINE, "gemm_down", 8): {"bytes_per_launch": 219.05e6, "sha1": "dd86544a515733d19bbea5190dd57560c8e166be"},
+    (HEADLINE, "attention", 8): {"bytes_per_launch": 112.97e6, "sha1": "1b19c1524880125ffbc3c4cc1311b596f3d8cbfa"},
+    (HEADLINE, "layernorm", 8): {"bytes_per_launch": 69.09e6, "sha1": "a2ea4531106105c660f8d1b0a216f48845cb0f45"},
+    (HEADLINE, "gemm_qkv", 8): {"bytes_per_launch": 85.91e6, "sha1": "46959bf9d3e82d5d3ed1f392803cba2db5e0baca"},
+    (HEADLINE, "gemm_out", 8): {"bytes_per_launch": 103.05e6, "sha1": "46959bf9d3e82d5d3ed1f392803cba2db5e0baca"},
+    (HEADLINE, "gemm_up", 8): {"bytes_per_launch": 120.51e6, "sha1": "46959bf9d3e82d5d3ed1f392803cba2db5e0baca"},
+    (HEADLINE, "gemm_down", 8): {"bytes_per_launch": 215.07e6, "sha1": "46959bf9d3e82d5d3ed1f392803cba2db5e0baca"},
 }
 
 
