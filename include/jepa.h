@@ -177,16 +177,19 @@ jepa_status jepa_context_set_graph(jepa_context* c, int32_t enable);
  * change. Launches are ordinary while per-kernel profiling is on. */
 jepa_status jepa_context_set_pdl(jepa_context* c, int32_t enable);
 jepa_status jepa_context_workspace_bytes(const jepa_context* c, size_t* out);
-/* Kernel launches one jepa_encode of this shape issues (graph replay counts the kernels inside). */
+/* Kernel launches one jepa_encode of this shape issues (graph replay counts the kernels inside; a
+ * batch that runs as two halves counts each half's). */
 jepa_status jepa_context_launches(const jepa_context* c, int32_t B, int32_t T, int32_t H, int32_t W,
                                   int32_t* n_out);
 
 /* Encode B clips. d_pixels: float [B,T,C,H,W] (layout JEPA_LAYOUT_TCHW) or [B,C,T,H,W]
  * (JEPA_LAYOUT_CTHW, the NCTHW tensor of "Architecture", Video ingest), already normalised.
  * d_tokens: float [B, N, embed_dim], N from jepa_n_tokens, after the final norm. Items never
- * mix ("Architecture", Batching). Asynchronous on the context stream. Shapes beyond the context's
- * max -> JEPA_E_BUDGET; not divisible -> JEPA_E_INVALID_ARG. A 16-byte aligned d_pixels takes the
- * vectorised rearrangement. */
+ * mix ("Architecture", Batching). Asynchronous on the context stream. In bf16, a batch of 4 or more
+ * items runs as two halves, the second on a side stream the context owns, forked from and joined
+ * back into the context stream (work queued after the call waits for both; each row's result is
+ * the same as in one pass). Shapes beyond the context's max -> JEPA_E_BUDGET; not divisible ->
+ * JEPA_E_INVALID_ARG. A 16-byte aligned d_pixels takes the vectorised rearrangement. */
 jepa_status jepa_encode(jepa_context* c, const float* d_pixels, int32_t B, int32_t T, int32_t H, int32_t W,
                         int32_t layout, float* d_tokens);
 

@@ -676,6 +676,9 @@ extern "C" jepa_status jepa_model_tensor(const jepa_model* m, const char* name, 
 }
 
 // ------------------------------------------------------------------ context
+// Batches of this many items or more (bf16) encode as two halves on two streams.
+static constexpr int kSplitMin = 4;
+
 struct jepa_context {
   const jepa_model* m = nullptr;
   cudaStream_t stream = nullptr;
@@ -693,10 +696,26 @@ struct jepa_context {
   int* err = nullptr;
   // per-shape state
   int kB = -1, kT = -1, kH = -1, kW = -1;
-  CUtensorMap tm_Pm, tm_Xn, tm_ao, tm_Hh, tm_qkv3;
-  CUtensorMap tm_Pm64, tm_Xn64, tm_ao64, tm_Hh64;  // 64-row boxes: A quarters of the 4-CTA GEMM
-  CUtensorMap tm_o_qkv, tm_o_hh, tm_o_x;  // GEMM outputs: qkv and Hh (bf16), X (fp32 residual adds)
-  int bn_patch = 0, bn_qkv = 0, bn_out = 0, bn_up = 0, bn_down = 0;
+  // A lane: the items [item0, item0 + B) of the batch, their rows of every workspace buffer, the
+  // tensor maps over those rows and the GEMM tile widths for their row count. lanes[0] is the
+  // whole batch; a batch of kSplitMin or more items (bf16, no per-kernel profiling) runs as
+  // lanes[1] and lanes[2], its two halves, on the context stream and a side stream (fork and join
+  // through events): the kernels of one half fill the SMs that the other half's persistent grids
+  // leave idle in their last rounds (8 clips: 11.0 -> 10.8 ms). Each row's arithmetic is the same
+  // either way.
+  struct Lane {
+    int item0 = 0, B = 0;
+    float* X = nullptr;
+    void *Xn = nullptr, *qkv = nullptr, *ao = nullptr, *Hh = nullptr, *Pm = nullptr;
+    CUtensorMap tm_Pm, tm_Xn, tm_ao, tm_Hh, tm_qkv3;
+    CUtensorMap tm_Pm64, tm_Xn64, tm_ao64, tm_Hh64;  // 64-row boxes: A quarters of the 4-CTA GEMM
+    CUtensorMap tm_o_qkv, tm_o_hh, tm_o_x;  // GEMM outputs: qkv and Hh (bf16), X (fp32 residual adds)
+    int bn_patch = 0, bn_qkv = 0, bn_out = 0, bn_up = 0, bn_down = 0;
+  };
+  Lane lanes[3];
+  bool halves = false;  // lanes[1] and lanes[2] are set up for the current shape
+  cudaStream_t side = nullptr;  // the second half's stream (owned)
+  cudaEvent_t fork_ev = nullptr, join_ev = nullptr;
   // graph replay
   bool use_graph = false;
   bool use_pdl = true;  // programmatic dependent launches in the encode sequence
@@ -804,6 +823,18 @@ extern "C" jepa_status jepa_context_new(const jepa_model* m, int32_t max_batch, 
     return fail(JEPA_E_CUDA, "cudaStreamCreate: %s", cudaGetErrorString(e));
   }
   c->own_stream = true;
+  // the side stream of the two-half encode; without it every batch runs as one lane
+  if (m->dtype == JEPA_BF16 && max_batch >= kSplitMin) {
+    if (cudaStreamCreateWithFlags(&c->side, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&c->fork_ev, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&c->join_ev, cudaEventDisableTiming) != cudaSuccess) {
+      cudaGetLastError();
+      if (c->side) cudaStreamDestroy(c->side);
+      if (c->fork_ev) cudaEventDestroy(c->fork_ev);
+      c->side = nullptr;
+      c->fork_ev = c->join_ev = nullptr;
+    }
+  }
   cudaMemset(c->err, 0, sizeof(int));
   *out = c;
   return JEPA_OK;
@@ -830,6 +861,12 @@ extern "C" void jepa_context_free(jepa_context* c) {
   if (c->gexec) cudaGraphExecDestroy(c->gexec);
   for (cudaEvent_t e : c->ev_pool) cudaEventDestroy(e);
   for (cudaEvent_t e : c->gev) cudaEventDestroy(e);
+  if (c->side) {
+    cudaStreamSynchronize(c->side);
+    cudaStreamDestroy(c->side);
+    cudaEventDestroy(c->fork_ev);
+    cudaEventDestroy(c->join_ev);
+  }
   if (c->own_stream && c->stream) cudaStreamDestroy(c->stream);
   if (c->ws) cudaFree(c->ws);
   delete c;
@@ -892,33 +929,58 @@ jepa_status check_shape(jepa_context* c, const float* pix, int B, int T, int H, 
 }
 
 // Per-shape set-up: tensor maps over the workspace, GEMM tile widths, the RoPE table.
+// The rows of items [item0, item0 + B) in every workspace buffer, tensor maps over them and the
+// GEMM tile widths for their row count.
+bool build_lane(jepa_context* c, jepa_context::Lane* ln, int item0, int B, const Geo& g) {
+  const jepa_model* m = c->m;
+  const int D = m->hp.embed_dim, F = m->hp.ffn_dim;
+  const size_t es = m->dtype == JEPA_BF16 ? 2 : 4;
+  const long long r0 = (long long)item0 * g.N, p0 = (long long)item0 * g.Np;
+  const long long M = (long long)B * g.N, Mp = (long long)B * g.Np;
+  ln->item0 = item0;
+  ln->B = B;
+  ln->X = c->X + r0 * D;
+  ln->Xn = static_cast<uint8_t*>(c->Xn) + r0 * D * es;
+  ln->qkv = static_cast<uint8_t*>(c->qkv) + r0 * 3 * D * es;
+  ln->ao = static_cast<uint8_t*>(c->ao) + r0 * D * es;
+  ln->Hh = static_cast<uint8_t*>(c->Hh) + r0 * F * es;
+  ln->Pm = static_cast<uint8_t*>(c->Pm) + p0 * m->K * es;
+  if (m->dtype != JEPA_BF16) return true;
+  bool ok = true;
+  ok &= make_tmap_2d_bf16(&ln->tm_Pm, ln->Pm, Mp, m->K, 128);
+  ok &= make_tmap_2d_bf16(&ln->tm_Xn, ln->Xn, M, D, 128);
+  ok &= make_tmap_2d_bf16(&ln->tm_ao, ln->ao, M, D, 128);
+  ok &= make_tmap_2d_bf16(&ln->tm_Hh, ln->Hh, M, F, 128);
+  ok &= make_tmap_2d_bf16(&ln->tm_Pm64, ln->Pm, Mp, m->K, 64);
+  ok &= make_tmap_2d_bf16(&ln->tm_Xn64, ln->Xn, M, D, 64);
+  ok &= make_tmap_2d_bf16(&ln->tm_ao64, ln->ao, M, D, 64);
+  ok &= make_tmap_2d_bf16(&ln->tm_Hh64, ln->Hh, M, F, 64);
+  ok &= make_tmap_3d_bf16(&ln->tm_qkv3, ln->qkv, B, g.N, 3 * D, 128);
+  ok &= make_tmap_2d_out(&ln->tm_o_qkv, ln->qkv, M, 3 * D, 2);
+  ok &= make_tmap_2d_out(&ln->tm_o_hh, ln->Hh, M, F, 2);
+  ok &= make_tmap_2d_out(&ln->tm_o_x, ln->X, M, D, 4);
+  ln->bn_patch = gemm_tc_pick_bn((int)Mp, D);
+  ln->bn_qkv = gemm_tc_pick_bn((int)M, 3 * D);
+  ln->bn_out = gemm_tc_pick_bn((int)M, D);
+  ln->bn_up = gemm_tc_pick_bn((int)M, F);
+  ln->bn_down = gemm_tc_pick_bn((int)M, D);
+  return ok;
+}
+
 jepa_status prepare_shape(jepa_context* c, int B, int T, int H, int W, const Geo& g) {
   if (c->kB == B && c->kT == T && c->kH == H && c->kW == W) return JEPA_OK;
   const jepa_model* m = c->m;
   const jepa_hparams& hp = m->hp;
-  const int D = hp.embed_dim, F = hp.ffn_dim;
-  const long long M = (long long)B * g.N, Mp = (long long)B * g.Np;
-  if (m->dtype == JEPA_BF16) {
-    bool ok = true;
-    ok &= make_tmap_2d_bf16(&c->tm_Pm, c->Pm, Mp, m->K, 128);
-    ok &= make_tmap_2d_bf16(&c->tm_Xn, c->Xn, M, D, 128);
-    ok &= make_tmap_2d_bf16(&c->tm_ao, c->ao, M, D, 128);
-    ok &= make_tmap_2d_bf16(&c->tm_Hh, c->Hh, M, F, 128);
-    ok &= make_tmap_2d_bf16(&c->tm_Pm64, c->Pm, Mp, m->K, 64);
-    ok &= make_tmap_2d_bf16(&c->tm_Xn64, c->Xn, M, D, 64);
-    ok &= make_tmap_2d_bf16(&c->tm_ao64, c->ao, M, D, 64);
-    ok &= make_tmap_2d_bf16(&c->tm_Hh64, c->Hh, M, F, 64);
-    ok &= make_tmap_3d_bf16(&c->tm_qkv3, c->qkv, B, g.N, 3 * D, 128);
-    ok &= make_tmap_2d_out(&c->tm_o_qkv, c->qkv, M, 3 * D, 2);
-    ok &= make_tmap_2d_out(&c->tm_o_hh, c->Hh, M, F, 2);
-    ok &= make_tmap_2d_out(&c->tm_o_x, c->X, M, D, 4);
-    if (!ok) return fail(JEPA_E_CUDA, "cuTensorMapEncodeTiled refused a workspace tensor map");
-    c->bn_patch = gemm_tc_pick_bn((int)Mp, D);
-    c->bn_qkv = gemm_tc_pick_bn((int)M, 3 * D);
-    c->bn_out = gemm_tc_pick_bn((int)M, D);
-    c->bn_up = gemm_tc_pick_bn((int)M, F);
-    c->bn_down = gemm_tc_pick_bn((int)M, D);
+  const int D = hp.embed_dim;
+  c->kB = -1;  // set again once everything below has succeeded
+  bool ok = build_lane(c, &c->lanes[0], 0, B, g);
+  c->halves = m->dtype == JEPA_BF16 && c->side != nullptr && B >= kSplitMin;
+  if (c->halves) {
+    const int B1 = (B + 1) / 2;
+    ok &= build_lane(c, &c->lanes[1], 0, B1, g);
+    ok &= build_lane(c, &c->lanes[2], B1, B - B1, g);
   }
+  if (!ok) return fail(JEPA_E_CUDA, "cuTensorMapEncodeTiled refused a workspace tensor map");
   if (hp.pos_type == JEPA_POS_ROPE3D) {
     CUDA_TRY(rope_axes_launch(g.gt, g.gh, g.gw, D / hp.n_head, hp.rope_theta, hp.rope_interpolate,
                               hp.rope_ref_grid, c->rope, c->stream));
@@ -1014,44 +1076,39 @@ double visible_pairs(int attn_mode, int prefix, int frames, int frame_tokens, in
 }
 
 // The launch sequence of one encode (no host synchronisation inside: graph-capturable).
-jepa_status launch_encode(jepa_context* c, const float* pix, int B, int T, int H, int W, int layout, float* tok,
-                          const Geo& g) {
+// The encode of one lane (its items' pixels in, their tokens out) on stream s.
+jepa_status encode_lane(jepa_context* c, const jepa_context::Lane& ln, cudaStream_t s, const float* pix, int T, int H,
+                        int W, int layout, float* tok, const Geo& g) {
   const jepa_model* m = c->m;
+  const int B = ln.B;
   const jepa_hparams& hp = m->hp;
   const bool bf = m->dtype == JEPA_BF16;
   const int D = hp.embed_dim, F = hp.ffn_dim, L = hp.n_layer, NH = hp.n_head, hd = D / NH;
   const int M = B * g.N, Mp = B * g.Np;
-  cudaStream_t s = c->stream;
   const uint64_t lim = default_wait_limit_ns();
   const double es = bf ? 2.0 : 4.0;                       // bytes of a GEMM operand element
-  // programmatic launches for this sequence (not between profiling events)
-  struct PdlScope {
-    bool prev;
-    explicit PdlScope(bool on) : prev(pdl_launches()) { pdl_launches() = on; }
-    ~PdlScope() { pdl_launches() = prev; }
-  } pdl_scope(c->use_pdl && !c->profiling);
   const double dM = M, dMp = Mp, dD = D, dF = F, dK = m->K;
   const double ln_bytes = dM * dD * (4.0 + es);           // read X fp32, write the normalised rows
   const double attn_flops = 4.0 * hd * NH * B *
                             visible_pairs(hp.attn_mode, g.prefix, g.gt, g.gh * g.gw, g.N);
 
   CUDA_TRY(prof(c, kPPatchify, 0.0, (double)B * T * hp.in_chans * H * W * 4.0 + dMp * dK * es, [&] {
-    return patchify_launch(pix, B, T, hp.in_chans, H, W, hp.tubelet_size, hp.patch_size, layout, bf, c->Pm, s);
+    return patchify_launch(pix, B, T, hp.in_chans, H, W, hp.tubelet_size, hp.patch_size, layout, bf, ln.Pm, s);
   }));
-  EpiArgs pe = make_epi(kEpiPatch, Mp, D, m->b_patch, c->X);
+  EpiArgs pe = make_epi(kEpiPatch, Mp, D, m->b_patch, ln.X);
   pe.patches_per_item = g.Np;
   pe.rows_per_item = g.N;
   pe.prefix = g.prefix;
   pe.pos = c->pos_clip;
   pe.vec = m->mod;
   CUDA_TRY(prof(c, kPGemmPatch, 2.0 * dMp * dD * dK, 0.0, [&] {
-    return bf ? gemm_tc_launch(c->tm_Pm, m->tm_patch[bn_slot(c->bn_patch)], c->tm_o_x, c->bn_patch, pe, Mp, D, m->K, c->err, lim, s, &c->tm_Pm64)
-              : gemm_simt_launch(reinterpret_cast<const float*>(c->Pm), reinterpret_cast<const float*>(m->w_patch), pe,
+    return bf ? gemm_tc_launch(ln.tm_Pm, m->tm_patch[bn_slot(ln.bn_patch)], ln.tm_o_x, ln.bn_patch, pe, Mp, D, m->K, c->err, lim, s, &ln.tm_Pm64)
+              : gemm_simt_launch(reinterpret_cast<const float*>(ln.Pm), reinterpret_cast<const float*>(m->w_patch), pe,
                                  Mp, D, m->K, s);
   }));
   if (g.prefix)
     CUDA_TRY(prof(c, kPPrefix, 0.0, (double)B * D * 4.0,
-                  [&] { return prefix_rows_launch(c->X, B, g.N, D, m->cls, m->pos, m->mod, s); }));
+                  [&] { return prefix_rows_launch(ln.X, B, g.N, D, m->cls, m->pos, m->mod, s); }));
 
   AttnParams ap;
   ap.B = B;
@@ -1061,13 +1118,13 @@ jepa_status launch_encode(jepa_context* c, const float* pix, int B, int T, int H
   ap.attn_mode = hp.attn_mode;
   ap.prefix = g.prefix;
   ap.frame_tokens = g.gh * g.gw;
-  ap.out = c->ao;
+  ap.out = ln.ao;
 
   for (int l = 0; l < L; ++l) {
     const LayerW& w = m->layers[l];
     CUDA_TRY(prof(c, kPLn, 0.0, ln_bytes,
-                  [&] { return layernorm_launch(c->X, M, D, w.ln1_w, w.ln1_b, hp.ln_eps, bf, c->Xn, s); }));
-    EpiArgs qe = make_epi(kEpiQkvRope, M, 3 * D, w.b_qkv, c->qkv);
+                  [&] { return layernorm_launch(ln.X, M, D, w.ln1_w, w.ln1_b, hp.ln_eps, bf, ln.Xn, s); }));
+    EpiArgs qe = make_epi(kEpiQkvRope, M, 3 * D, w.b_qkv, ln.qkv);
     qe.rows_per_item = g.N;
     qe.prefix = g.prefix;
     qe.n_head = NH;
@@ -1078,39 +1135,66 @@ jepa_status launch_encode(jepa_context* c, const float* pix, int B, int T, int H
     qe.rope_gt = g.gt;
     qe.rope_gh = g.gh;
     qe.rope_gw = g.gw;
-    EpiArgs oe = make_epi(kEpiResidual, M, D, w.b_out, c->X);
-    EpiArgs ue = make_epi(kEpiGelu, M, F, w.b_up, c->Hh);
-    EpiArgs de = make_epi(kEpiResidual, M, D, w.b_down, c->X);
-    const float* Xn = reinterpret_cast<const float*>(c->Xn);
+    EpiArgs oe = make_epi(kEpiResidual, M, D, w.b_out, ln.X);
+    EpiArgs ue = make_epi(kEpiGelu, M, F, w.b_up, ln.Hh);
+    EpiArgs de = make_epi(kEpiResidual, M, D, w.b_down, ln.X);
+    const float* Xn = reinterpret_cast<const float*>(ln.Xn);
     CUDA_TRY(prof(c, kPGemmQkv, 2.0 * dM * 3.0 * dD * dD, 0.0, [&] {
-      return bf ? gemm_tc_launch(c->tm_Xn, w.tm_qkv[bn_slot(c->bn_qkv)], c->tm_o_qkv, c->bn_qkv, qe, M, 3 * D, D, c->err, lim, s, &c->tm_Xn64)
+      return bf ? gemm_tc_launch(ln.tm_Xn, w.tm_qkv[bn_slot(ln.bn_qkv)], ln.tm_o_qkv, ln.bn_qkv, qe, M, 3 * D, D, c->err, lim, s, &ln.tm_Xn64)
                 : gemm_simt_launch(Xn, reinterpret_cast<const float*>(w.w_qkv), qe, M, 3 * D, D, s);
     }));
     CUDA_TRY(prof(c, kPAttention, attn_flops, 0.0, [&] {
-      return bf ? attention_tc_launch(c->tm_qkv3, ap, c->err, lim, s)
-                : attention_simt_launch(reinterpret_cast<const float*>(c->qkv), ap, s);
+      return bf ? attention_tc_launch(ln.tm_qkv3, ap, c->err, lim, s)
+                : attention_simt_launch(reinterpret_cast<const float*>(ln.qkv), ap, s);
     }));
     CUDA_TRY(prof(c, kPGemmOut, 2.0 * dM * dD * dD, 0.0, [&] {
-      return bf ? gemm_tc_launch(c->tm_ao, w.tm_out[bn_slot(c->bn_out)], c->tm_o_x, c->bn_out, oe, M, D, D, c->err, lim, s, &c->tm_ao64)
-                : gemm_simt_launch(reinterpret_cast<const float*>(c->ao), reinterpret_cast<const float*>(w.w_out), oe,
+      return bf ? gemm_tc_launch(ln.tm_ao, w.tm_out[bn_slot(ln.bn_out)], ln.tm_o_x, ln.bn_out, oe, M, D, D, c->err, lim, s, &ln.tm_ao64)
+                : gemm_simt_launch(reinterpret_cast<const float*>(ln.ao), reinterpret_cast<const float*>(w.w_out), oe,
                                    M, D, D, s);
     }));
     CUDA_TRY(prof(c, kPLn, 0.0, ln_bytes,
-                  [&] { return layernorm_launch(c->X, M, D, w.ln2_w, w.ln2_b, hp.ln_eps, bf, c->Xn, s); }));
+                  [&] { return layernorm_launch(ln.X, M, D, w.ln2_w, w.ln2_b, hp.ln_eps, bf, ln.Xn, s); }));
     CUDA_TRY(prof(c, kPGemmUp, 2.0 * dM * dF * dD, 0.0, [&] {
-      return bf ? gemm_tc_launch(c->tm_Xn, w.tm_up[bn_slot(c->bn_up)], c->tm_o_hh, c->bn_up, ue, M, F, D, c->err, lim, s, &c->tm_Xn64)
+      return bf ? gemm_tc_launch(ln.tm_Xn, w.tm_up[bn_slot(ln.bn_up)], ln.tm_o_hh, ln.bn_up, ue, M, F, D, c->err, lim, s, &ln.tm_Xn64)
                 : gemm_simt_launch(Xn, reinterpret_cast<const float*>(w.w_up), ue, M, F, D, s);
     }));
     CUDA_TRY(prof(c, kPGemmDown, 2.0 * dM * dD * dF, 0.0, [&] {
-      return bf ? gemm_tc_launch(c->tm_Hh, w.tm_down[bn_slot(c->bn_down)], c->tm_o_x, c->bn_down, de, M, D, F, c->err, lim, s, &c->tm_Hh64)
-                : gemm_simt_launch(reinterpret_cast<const float*>(c->Hh), reinterpret_cast<const float*>(w.w_down), de,
+      return bf ? gemm_tc_launch(ln.tm_Hh, w.tm_down[bn_slot(ln.bn_down)], ln.tm_o_x, ln.bn_down, de, M, D, F, c->err, lim, s, &ln.tm_Hh64)
+                : gemm_simt_launch(reinterpret_cast<const float*>(ln.Hh), reinterpret_cast<const float*>(w.w_down), de,
                                    M, D, F, s);
     }));
   }
   CUDA_TRY(prof(c, kPLnFinal, 0.0, dM * dD * 8.0,
-                [&] { return layernorm_launch(c->X, M, D, m->norm_w, m->norm_b, hp.ln_eps, false, tok, s); }));
+                [&] { return layernorm_launch(ln.X, M, D, m->norm_w, m->norm_b, hp.ln_eps, false, tok, s); }));
   return JEPA_OK;
 }
+
+jepa_status launch_encode(jepa_context* c, const float* pix, int B, int T, int H, int W, int layout, float* tok,
+                          const Geo& g) {
+  // programmatic launches for this sequence (not between profiling events)
+  struct PdlScope {
+    bool prev;
+    explicit PdlScope(bool on) : prev(pdl_launches()) { pdl_launches() = on; }
+    ~PdlScope() { pdl_launches() = prev; }
+  } pdl_scope(c->use_pdl && !c->profiling);
+  (void)B;  // the lanes were set up for this batch by prepare_shape
+  if (!c->halves || c->profiling) return encode_lane(c, c->lanes[0], c->stream, pix, T, H, W, layout, tok, g);
+  // two halves: the second on the side stream, forked from and joined back into the context
+  // stream (inside a capture the side stream joins the capture through the fork event)
+  const size_t pix_item = (size_t)T * c->m->hp.in_chans * H * W;
+  const size_t tok_item = (size_t)g.N * c->m->hp.embed_dim;
+  const jepa_context::Lane& b = c->lanes[2];
+  CUDA_TRY(cudaEventRecord(c->fork_ev, c->stream));
+  CUDA_TRY(cudaStreamWaitEvent(c->side, c->fork_ev, 0));
+  jepa_status st = encode_lane(c, c->lanes[1], c->stream, pix, T, H, W, layout, tok, g);
+  const jepa_status st2 =
+      encode_lane(c, b, c->side, pix + b.item0 * pix_item, T, H, W, layout, tok + b.item0 * tok_item, g);
+  // join even after a failed launch, so that a capture in progress can end
+  CUDA_TRY(cudaEventRecord(c->join_ev, c->side));
+  CUDA_TRY(cudaStreamWaitEvent(c->stream, c->join_ev, 0));
+  return st != JEPA_OK ? st : st2;
+}
+
 }  // namespace
 
 extern "C" jepa_status jepa_context_launches(const jepa_context* c, int32_t B, int32_t T, int32_t H, int32_t W,
@@ -1120,7 +1204,9 @@ extern "C" jepa_status jepa_context_launches(const jepa_context* c, int32_t B, i
   Geo g;
   jepa_status st = geometry(&c->m->hp, T, H, W, &g);
   if (st != JEPA_OK) return st;
-  *n_out = launches_per_encode(c->m);
+  // a batch that runs as two halves launches every kernel of the sequence once per half
+  const bool halves = c->m->dtype == JEPA_BF16 && c->side != nullptr && B >= kSplitMin && !c->profiling;
+  *n_out = launches_per_encode(c->m) * (halves ? 2 : 1);
   return JEPA_OK;
 }
 
