@@ -87,11 +87,12 @@ def test_layouts_agree_bit_exact():
     assert torch.equal(a, b)
 
 
+# B = 5 (bf16) runs as two uneven halves (3 + 2 items) on two streams; graph replay captures both
+@pytest.mark.parametrize("B,graph", [(3, False), (5, False), (5, True)])
 @pytest.mark.parametrize("name", ["vjepa2_vitl16_16x256", "levjepa_vitl16_16x256", "hfvit_ti14_224"])
-def test_batch_items_equal_single_calls(name):
+def test_batch_items_equal_single_calls(name, B, graph):
     cfg, dtype, (T, H, W) = small(name)
-    B = 3
-    model, ctx = make(name, n_layer=2, batch=B, T=T, H=H, W=W)
+    model, ctx = make(name, n_layer=2, batch=B, T=T, H=H, W=W, graph=graph)
     pix = torch.from_numpy(synth.pixels(2, (B, T, 3, H, W))).cuda()
     full = ctx.encode(pix).clone()
     for b in range(B):
