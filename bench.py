@@ -572,7 +572,7 @@ KERNEL_SOURCES = {
     "layernorm": ("rowops.cu", "ptx.cuh"), "layernorm_final": ("rowops.cu", "ptx.cuh"),
     "patchify": ("rowops.cu", "ptx.cuh"),
 }
-GEMM_SOURCES = ("gemm_tc.cu", "gemm_tc2.cu", "gemm_tc4.cu", "epilogue.cuh", "ptx.cuh")
+GEMM_SOURCES = ("gemm_tc.cu", "gemm_tc2.cu", "epilogue.cuh", "ptx.cuh")
 
 
 def source_sha1(kernel_class: str):

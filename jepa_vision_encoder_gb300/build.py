@@ -16,7 +16,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libjepa_gb300.so")
-SOURCES = ["runtime.cu", "gemm_tc.cu", "gemm_tc2.cu", "gemm_tc4.cu", "attention_tc.cu", "simt.cu", "rowops.cu", "postab.cu",
+SOURCES = ["runtime.cu", "gemm_tc.cu", "gemm_tc2.cu", "attention_tc.cu", "simt.cu", "rowops.cu", "postab.cu",
            "predictor.cu", "head.cu", "gguf.cpp"]
 HEADERS = ["ptx.cuh", "epilogue.cuh", "kernels.h", "internal.h", "seq.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

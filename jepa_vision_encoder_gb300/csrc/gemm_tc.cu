@@ -261,11 +261,9 @@ static cudaError_t set_smem_attr() {
 }
 
 cudaError_t gemm_tc2_init_attributes();
-cudaError_t gemm_tc4_init_attributes();
 
 cudaError_t gemm_tc_init_attributes() {
   cudaError_t e = gemm_tc2_init_attributes();
-  if (e == cudaSuccess) e = gemm_tc4_init_attributes();
   if (e == cudaSuccess) e = set_smem_attr<256>();
   if (e == cudaSuccess) e = set_smem_attr<128>();
   if (e == cudaSuccess) e = set_smem_attr<64>();
@@ -273,18 +271,8 @@ cudaError_t gemm_tc_init_attributes() {
 }
 
 cudaError_t gemm_tc_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmO, int BN,
-                           const EpiArgs& epi, int M, int N, int K, int* err, uint64_t limit_ns, cudaStream_t s,
-                           const CUtensorMap* tmA64) {
+                           const EpiArgs& epi, int M, int N, int K, int* err, uint64_t limit_ns, cudaStream_t s) {
   if (M <= 0) return cudaSuccess;
-  if (BN == kPairTile && tmA64 != nullptr && N % 512 == 0 && gemm_tc4_max_clusters() > 0) {
-    // The 4-CTA kernel when it needs no more rounds of tiles than the pair kernel: fewer SMs hold
-    // clusters of four (36 of them, 144 SMs, against 76 pairs), and the shared A makes a tile only
-    // a little faster (FFN-down 96.2 -> 94.0 us at 8 clips; FFN-up, 15 rounds against 14, 87.0 -> 90.7).
-    const long long units = (long long)((M + 255) / 256) * (N / 512);
-    const long long clusters = gemm_tc4_max_clusters(), pairs = gemm_tc2_max_pairs();
-    if ((units + clusters - 1) / clusters <= (2 * units + pairs - 1) / pairs)
-      return gemm_tc4_launch(*tmA64, tmB, tmO, epi, M, N, K, err, limit_ns, s);
-  }
   if (BN == kPairTile) return gemm_tc2_launch(tmA, tmB, tmO, epi, M, N, K, err, limit_ns, s);
   switch (BN) {
     case 256: return launch_kind<256>(tmA, tmB, tmO, epi, M, N, K, err, limit_ns, s);

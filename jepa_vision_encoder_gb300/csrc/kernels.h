@@ -60,17 +60,8 @@ int gemm_tc_b_box(int bn);
 int gemm_tc2_max_pairs();
 cudaError_t gemm_tc2_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmO,
                             const EpiArgs& epi, int M, int N, int K, int* err, uint64_t limit_ns, cudaStream_t s);
-// The 4-CTA form of the pair kernel (two pairs side by side along N sharing A by multicast):
-// tmA64 is A with 64-row boxes; N a multiple of 512. gemm_tc4_max_clusters() is 0 where clusters
-// of four cannot be resident.
-int gemm_tc4_max_clusters();
-cudaError_t gemm_tc4_launch(const CUtensorMap& tmA64, const CUtensorMap& tmB, const CUtensorMap& tmO,
-                            const EpiArgs& epi, int M, int N, int K, int* err, uint64_t limit_ns, cudaStream_t s);
-// tmA64 (optional, A with 64-row boxes): lets a kPairTile GEMM with N a multiple of 512 run on the
-// 4-CTA kernel.
 cudaError_t gemm_tc_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmO, int BN,
-                           const EpiArgs& epi, int M, int N, int K, int* err, uint64_t limit_ns, cudaStream_t s,
-                           const CUtensorMap* tmA64 = nullptr);
+                           const EpiArgs& epi, int M, int N, int K, int* err, uint64_t limit_ns, cudaStream_t s);
 
 // fp32 SIMT GEMM with the same epilogues.
 cudaError_t gemm_simt_launch(const float* A, const float* Bw, const EpiArgs& epi, int M, int N, int K,

@@ -708,7 +708,6 @@ struct jepa_context {
     float* X = nullptr;
     void *Xn = nullptr, *qkv = nullptr, *ao = nullptr, *Hh = nullptr, *Pm = nullptr;
     CUtensorMap tm_Pm, tm_Xn, tm_ao, tm_Hh, tm_qkv3;
-    CUtensorMap tm_Pm64, tm_Xn64, tm_ao64, tm_Hh64;  // 64-row boxes: A quarters of the 4-CTA GEMM
     CUtensorMap tm_o_qkv, tm_o_hh, tm_o_x;  // GEMM outputs: qkv and Hh (bf16), X (fp32 residual adds)
     int bn_patch = 0, bn_qkv = 0, bn_out = 0, bn_up = 0, bn_down = 0;
   };
@@ -951,10 +950,6 @@ bool build_lane(jepa_context* c, jepa_context::Lane* ln, int item0, int B, const
   ok &= make_tmap_2d_bf16(&ln->tm_Xn, ln->Xn, M, D, 128);
   ok &= make_tmap_2d_bf16(&ln->tm_ao, ln->ao, M, D, 128);
   ok &= make_tmap_2d_bf16(&ln->tm_Hh, ln->Hh, M, F, 128);
-  ok &= make_tmap_2d_bf16(&ln->tm_Pm64, ln->Pm, Mp, m->K, 64);
-  ok &= make_tmap_2d_bf16(&ln->tm_Xn64, ln->Xn, M, D, 64);
-  ok &= make_tmap_2d_bf16(&ln->tm_ao64, ln->ao, M, D, 64);
-  ok &= make_tmap_2d_bf16(&ln->tm_Hh64, ln->Hh, M, F, 64);
   ok &= make_tmap_3d_bf16(&ln->tm_qkv3, ln->qkv, B, g.N, 3 * D, 128);
   ok &= make_tmap_2d_out(&ln->tm_o_qkv, ln->qkv, M, 3 * D, 2);
   ok &= make_tmap_2d_out(&ln->tm_o_hh, ln->Hh, M, F, 2);
@@ -1102,7 +1097,7 @@ jepa_status encode_lane(jepa_context* c, const jepa_context::Lane& ln, cudaStrea
   pe.pos = c->pos_clip;
   pe.vec = m->mod;
   CUDA_TRY(prof(c, kPGemmPatch, 2.0 * dMp * dD * dK, 0.0, [&] {
-    return bf ? gemm_tc_launch(ln.tm_Pm, m->tm_patch[bn_slot(ln.bn_patch)], ln.tm_o_x, ln.bn_patch, pe, Mp, D, m->K, c->err, lim, s, &ln.tm_Pm64)
+    return bf ? gemm_tc_launch(ln.tm_Pm, m->tm_patch[bn_slot(ln.bn_patch)], ln.tm_o_x, ln.bn_patch, pe, Mp, D, m->K, c->err, lim, s)
               : gemm_simt_launch(reinterpret_cast<const float*>(ln.Pm), reinterpret_cast<const float*>(m->w_patch), pe,
                                  Mp, D, m->K, s);
   }));
@@ -1140,7 +1135,7 @@ jepa_status encode_lane(jepa_context* c, const jepa_context::Lane& ln, cudaStrea
     EpiArgs de = make_epi(kEpiResidual, M, D, w.b_down, ln.X);
     const float* Xn = reinterpret_cast<const float*>(ln.Xn);
     CUDA_TRY(prof(c, kPGemmQkv, 2.0 * dM * 3.0 * dD * dD, 0.0, [&] {
-      return bf ? gemm_tc_launch(ln.tm_Xn, w.tm_qkv[bn_slot(ln.bn_qkv)], ln.tm_o_qkv, ln.bn_qkv, qe, M, 3 * D, D, c->err, lim, s, &ln.tm_Xn64)
+      return bf ? gemm_tc_launch(ln.tm_Xn, w.tm_qkv[bn_slot(ln.bn_qkv)], ln.tm_o_qkv, ln.bn_qkv, qe, M, 3 * D, D, c->err, lim, s)
                 : gemm_simt_launch(Xn, reinterpret_cast<const float*>(w.w_qkv), qe, M, 3 * D, D, s);
     }));
     CUDA_TRY(prof(c, kPAttention, attn_flops, 0.0, [&] {
@@ -1148,18 +1143,18 @@ jepa_status encode_lane(jepa_context* c, const jepa_context::Lane& ln, cudaStrea
                 : attention_simt_launch(reinterpret_cast<const float*>(ln.qkv), ap, s);
     }));
     CUDA_TRY(prof(c, kPGemmOut, 2.0 * dM * dD * dD, 0.0, [&] {
-      return bf ? gemm_tc_launch(ln.tm_ao, w.tm_out[bn_slot(ln.bn_out)], ln.tm_o_x, ln.bn_out, oe, M, D, D, c->err, lim, s, &ln.tm_ao64)
+      return bf ? gemm_tc_launch(ln.tm_ao, w.tm_out[bn_slot(ln.bn_out)], ln.tm_o_x, ln.bn_out, oe, M, D, D, c->err, lim, s)
                 : gemm_simt_launch(reinterpret_cast<const float*>(ln.ao), reinterpret_cast<const float*>(w.w_out), oe,
                                    M, D, D, s);
     }));
     CUDA_TRY(prof(c, kPLn, 0.0, ln_bytes,
                   [&] { return layernorm_launch(ln.X, M, D, w.ln2_w, w.ln2_b, hp.ln_eps, bf, ln.Xn, s); }));
     CUDA_TRY(prof(c, kPGemmUp, 2.0 * dM * dF * dD, 0.0, [&] {
-      return bf ? gemm_tc_launch(ln.tm_Xn, w.tm_up[bn_slot(ln.bn_up)], ln.tm_o_hh, ln.bn_up, ue, M, F, D, c->err, lim, s, &ln.tm_Xn64)
+      return bf ? gemm_tc_launch(ln.tm_Xn, w.tm_up[bn_slot(ln.bn_up)], ln.tm_o_hh, ln.bn_up, ue, M, F, D, c->err, lim, s)
                 : gemm_simt_launch(Xn, reinterpret_cast<const float*>(w.w_up), ue, M, F, D, s);
     }));
     CUDA_TRY(prof(c, kPGemmDown, 2.0 * dM * dD * dF, 0.0, [&] {
-      return bf ? gemm_tc_launch(ln.tm_Hh, w.tm_down[bn_slot(ln.bn_down)], ln.tm_o_x, ln.bn_down, de, M, D, F, c->err, lim, s, &ln.tm_Hh64)
+      return bf ? gemm_tc_launch(ln.tm_Hh, w.tm_down[bn_slot(ln.bn_down)], ln.tm_o_x, ln.bn_down, de, M, D, F, c->err, lim, s)
                 : gemm_simt_launch(reinterpret_cast<const float*>(ln.Hh), reinterpret_cast<const float*>(w.w_down), de,
                                    M, D, F, s);
     }));
@@ -1494,8 +1489,8 @@ extern "C" jepa_status jepa_op_linear(int32_t dtype, const void* d_x, int32_t M,
   jepa_status st = op_err_word(&err);
   if (st != JEPA_OK) return st;
   const int bn = gemm_tc_pick_bn(M, N);
-  CUtensorMap ta, ta64, tb, to;
-  if (!make_tmap_2d_bf16(&ta, d_x, M, K, 128) || !make_tmap_2d_bf16(&ta64, d_x, M, K, 64) ||
+  CUtensorMap ta, tb, to;
+  if (!make_tmap_2d_bf16(&ta, d_x, M, K, 128) ||
       !make_tmap_2d_bf16(&tb, d_w, N, K, gemm_tc_b_box(bn)))
     return fail(JEPA_E_CUDA, "cuTensorMapEncodeTiled refused an operand");
   memset(&to, 0, sizeof to);
@@ -1506,7 +1501,7 @@ extern "C" jepa_status jepa_op_linear(int32_t dtype, const void* d_x, int32_t M,
     if (!make_tmap_2d_out(&to, e.out, M, N, (e.kind == kEpiResidual || e.kind == kEpiPatch) ? 4 : 2))
       return fail(JEPA_E_CUDA, "cuTensorMapEncodeTiled refused the output");
   }
-  CUDA_TRY(gemm_tc_launch(ta, tb, to, bn, e, M, N, K, err, default_wait_limit_ns(), s, &ta64));
+  CUDA_TRY(gemm_tc_launch(ta, tb, to, bn, e, M, N, K, err, default_wait_limit_ns(), s));
   return JEPA_OK;
 }
 

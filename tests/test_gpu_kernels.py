@@ -98,8 +98,8 @@ def bf16_bound(ref, K):
     return 2.0 ** -8 * np.abs(ref) + 1e-5 * np.sqrt(K) * np.abs(ref).max() + 1e-6
 
 
-# (M, N, K): tile widths 256 (many tiles, > 1 per CTA), 128, 64; ragged M. (2125, 3072) and
-# (4099, 4096) run on the 4-CTA kernel (N a multiple of 512), (4099, 768) on the 2-SM pair kernel.
+# (M, N, K): tile widths 256 (many tiles, > 1 per CTA), 128, 64; ragged M. (2125, 3072), (4099, 4096)
+# and (4099, 768) run on the 2-SM pair kernel.
 GEMM_SHAPES = [(2048 + 77, 3072, 256), (2048, 1024, 1024), (257, 256, 128), (128, 64, 64), (4096 + 3, 4096, 128),
                (4096 + 3, 768, 128)]
 
