@@ -346,9 +346,7 @@ def run_sequence(args, wl, make):
     import torch
     import torch.distributed as dist
 
-    rank, world, local = dist_env()
-    if world > 1:
-        dist.init_process_group(backend="nccl" if torch.cuda.is_available() else "gloo")
+    rank, world, local = init_ranks()
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU")
     torch.cuda.set_device(local)
@@ -649,9 +647,7 @@ def run_ours(args):
     import torch
     import torch.distributed as dist
 
-    rank, world, local = dist_env()
-    if world > 1:
-        dist.init_process_group(backend="nccl" if torch.cuda.is_available() else "gloo")
+    rank, world, local = init_ranks()
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU")
     torch.cuda.set_device(local)
@@ -831,8 +827,42 @@ def run_ours(args):
     return 0
 
 
+def free_port() -> int:
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def spawn_ranks(n: int, argv) -> int:
+    """`python bench.py --gpus N` without torchrun: start N ranks, one process per GPU, through
+    torch.distributed.run on 127.0.0.1 with the same arguments, and return their exit status."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", "--master-port", str(free_port()), os.path.abspath(__file__)] + list(argv)
+    return subprocess.call(cmd)
+
+
+def init_ranks():
+    """Process group of a multi-rank run (NCCL on GPUs, gloo on a CPU-only host); returns the
+    (rank, world, local rank) triple and reports it on stderr."""
+    import torch
+    import torch.distributed as dist
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group(backend="nccl" if torch.cuda.is_available() else "gloo")
+        print(f"bench.py: rank {rank} of {world} (local GPU {local})", file=sys.stderr, flush=True)
+    return rank, world, local
+
+
 def main(argv=None):
+    argv = sys.argv[1:] if argv is None else list(argv)
     args = parse_args(argv)
+    if args.gpus < 1:
+        raise SystemExit(f"bench.py: --gpus {args.gpus} must be at least 1")
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        return spawn_ranks(args.gpus, argv)
+    if dist_env()[1] != args.gpus:
+        raise SystemExit(f"bench.py: --gpus {args.gpus} but the launcher started {dist_env()[1]} ranks")
     if args.impl == "reference":
         return run_reference(args)
     if args.workload == PREDICTOR:

@@ -177,6 +177,11 @@ jepa_status jepa_context_set_graph(jepa_context* c, int32_t enable);
  * change. Launches are ordinary while per-kernel profiling is on. */
 jepa_status jepa_context_set_pdl(jepa_context* c, int32_t enable);
 jepa_status jepa_context_workspace_bytes(const jepa_context* c, size_t* out);
+/* The largest number of items one jepa_encode call of this context folds into its launch sequence
+ * ("Architecture", Batching: the encode folds up to jepa_context_max_batch() items, which never
+ * mix): the max_batch given to jepa_context_new. A caller with more items splits them into calls
+ * of at most this many. Null argument -> JEPA_E_INVALID_ARG. */
+jepa_status jepa_context_max_batch(const jepa_context* c, int32_t* out);
 /* Kernel launches one jepa_encode of this shape issues (graph replay counts the kernels inside; a
  * batch that runs as two halves counts each half's). */
 jepa_status jepa_context_launches(const jepa_context* c, int32_t B, int32_t T, int32_t H, int32_t W,

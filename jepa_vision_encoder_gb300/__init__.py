@@ -189,6 +189,13 @@ class Context:
         check(lib().jepa_context_workspace_bytes(self._h, ctypes.byref(n)))
         return n.value
 
+    @property
+    def max_batch(self) -> int:
+        """Items one encode call folds together at most (the max_batch the context was made for)."""
+        n = ctypes.c_int32()
+        check(lib().jepa_context_max_batch(self._h, ctypes.byref(n)))
+        return n.value
+
     def launches(self, B, T, H, W) -> int:
         n = ctypes.c_int32()
         check(lib().jepa_context_launches(self._h, B, T, H, W, ctypes.byref(n)))

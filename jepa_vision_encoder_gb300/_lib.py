@@ -94,6 +94,7 @@ SIGNATURES = {
     "jepa_context_set_graph": (_I, [_P, _I]),
     "jepa_context_set_pdl": (_I, [_P, _I]),
     "jepa_context_workspace_bytes": (_I, [_P, ctypes.POINTER(_SZ)]),
+    "jepa_context_max_batch": (_I, [_P, ctypes.POINTER(_I)]),
     "jepa_context_launches": (_I, [_P, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_int32)]),
     "jepa_encode": (_I, [_P, _P, _I, _I, _I, _I, _I, _P]),
     "jepa_encode_host": (_I, [_P, _P, _I, _I, _I, _I, _I, _P]),

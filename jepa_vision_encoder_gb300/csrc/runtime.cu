@@ -762,7 +762,8 @@ size_t ws_layout(const jepa_model* m, long long rows, long long prows, long long
                oA = take(rows * D * es), oH = take(rows * F * es), oP = take(prows * K * es),
                oR = take((size_t)np * 3 * std::max(dh, 1) * sizeof(float2)),
                oPos = take(is_sincos(hp) ? (size_t)np * D * 4 : 0), oPix = take(pix * 4),
-               oTok = take(rows * D * 4), oErr = take(sizeof(int));
+               oTok = take(pix > 0 ? rows * D * 4 : 0),  // host staging only where pixels are staged too
+               oErr = take(sizeof(int));
   if (c) {
     c->X = reinterpret_cast<float*>(c->ws + oX);
     c->Xn = c->ws + oXn;
@@ -772,8 +773,8 @@ size_t ws_layout(const jepa_model* m, long long rows, long long prows, long long
     c->Pm = c->ws + oP;
     c->rope = reinterpret_cast<float2*>(c->ws + oR);
     c->pos_buf = is_sincos(hp) ? reinterpret_cast<float*>(c->ws + oPos) : nullptr;
-    c->pix_stage = reinterpret_cast<float*>(c->ws + oPix);
-    c->tok_stage = reinterpret_cast<float*>(c->ws + oTok);
+    c->pix_stage = pix > 0 ? reinterpret_cast<float*>(c->ws + oPix) : nullptr;
+    c->tok_stage = pix > 0 ? reinterpret_cast<float*>(c->ws + oTok) : nullptr;
     c->err = reinterpret_cast<int*>(c->ws + oErr);
   }
   return off;
@@ -900,6 +901,12 @@ extern "C" jepa_status jepa_context_set_pdl(jepa_context* c, int32_t enable) {
 extern "C" jepa_status jepa_context_workspace_bytes(const jepa_context* c, size_t* out) {
   if (!c || !out) return fail(JEPA_E_INVALID_ARG, "jepa_context_workspace_bytes: null argument");
   *out = c->ws_bytes;
+  return JEPA_OK;
+}
+
+extern "C" jepa_status jepa_context_max_batch(const jepa_context* c, int32_t* out) {
+  if (!c || !out) return fail(JEPA_E_INVALID_ARG, "jepa_context_max_batch: null argument");
+  *out = c->max_B;
   return JEPA_OK;
 }
 

@@ -59,3 +59,34 @@ def test_measured_peaks_and_defaults():
     assert p["bf16_tflops"] > 100 and p["hbm_gbs"] > 1000
     a = bench.parse_args([])
     assert a.gpus == 1 and a.steps >= 1 and a.warmup >= 3 and a.impl == "ours"
+
+
+def test_gpus_flag_starts_that_many_ranks():
+    """`bench.py --gpus 2` without a launcher starts two ranks through torch.distributed.run; on
+    this CPU-only host both reach the multi-rank set-up (gloo) and then stop for lack of a GPU, so
+    the run exits non-zero and never prints a one-GPU line."""
+    import subprocess
+    import sys
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "MASTER_ADDR",
+                                                            "MASTER_PORT")}
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    r = subprocess.run([sys.executable, bench.__file__, "--gpus", "2", "--steps", "1", "--warmup", "3",
+                        "--no-cpu-baseline"], capture_output=True, text=True, timeout=300, env=env)
+    assert r.returncode != 0
+    assert '"n_gpus": 1' not in r.stdout
+    assert "rank 0 of 2" in r.stderr and "rank 1 of 2" in r.stderr, r.stderr[-2000:]
+
+
+def test_gpus_flag_must_match_the_launcher():
+    env_keep = {k: os.environ.get(k) for k in ("WORLD_SIZE",)}
+    os.environ["WORLD_SIZE"] = "3"
+    try:
+        with pytest.raises(SystemExit) as e:
+            bench.main(["--gpus", "2"])
+        assert "3 ranks" in str(e.value)
+    finally:
+        for k, v in env_keep.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v

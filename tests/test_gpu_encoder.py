@@ -204,7 +204,8 @@ def test_refusals():
         jv.Context(model, 64, 64, 512, 512, max_workspace_bytes=1 << 30)
     assert e.value.status == jv._lib.E_BUDGET
     ctx = jv.Context(model, 1, 4, 64, 64)
-    with pytest.raises(jv.JepaError) as e:
+    assert ctx.max_batch == 1 and jv.Context(model, 3, 4, 64, 64).max_batch == 3
+    with pytest.raises(jv.JepaError) as e:   # more items than jepa_context_max_batch
         ctx.encode(torch.zeros((2, 4, 3, 64, 64), dtype=torch.float32, device="cuda"))
     assert e.value.status == jv._lib.E_BUDGET
     with pytest.raises(jv.JepaError) as e:

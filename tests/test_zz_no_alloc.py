@@ -1,13 +1,19 @@
 """Allocation-free encode against the context encode (GPU only).
 
-jepa_encode_noalloc runs the encoder with a fixed scratch array compiled into the library as its
-workspace. Two calls in a row must each agree with jepa_encode on the same clip within the
-encoder's parity bar (fp32: max |y - ref| / max |ref| <= 1e-4; bf16: per-token cosine >= 0.9999
-and max |y - ref| <= 3e-2), the second call must leave the device's free memory unchanged, and a
-batch whose workspace does not fit in the array is refused before anything is launched.
+jepa_encode_noalloc is for callers that must not allocate device memory: code running inside
+another framework's memory pool, a fixed-budget embedded service, or a loop where a cudaMalloc
+(which can synchronise the device) is not allowed. It runs the encoder with a fixed scratch
+array compiled into the library as its workspace.
+
+The test makes one set-up call (the first call on a device looks up the array's address; the
+first launches of each kernel may also load its module), then two calls in a row on two other
+clips. Each of the two must equal jepa_encode on the same clip bit for bit: both run the same
+launch sequence (one lane, the same tile widths, the same kernels), so any difference would mean
+stale or aliased scratch. The device's free memory must be the same before the first of the two
+calls and after the second: nothing is allocated and kept by either call. A batch whose
+workspace does not fit in the array is refused before anything is launched.
 The file name sorts last so that it also runs after every other GPU test.
 """
-import numpy as np
 import pytest
 import torch
 
@@ -15,18 +21,6 @@ import synth
 
 jv = pytest.importorskip("jepa_vision_encoder_gb300")
 pytestmark = pytest.mark.gpu
-
-
-def bar(got, ref, dtype, what):
-    got = got.double().cpu().numpy().reshape(-1, got.shape[-1])
-    ref = ref.double().cpu().numpy().reshape(-1, ref.shape[-1])
-    err = np.abs(got - ref)
-    if dtype == "fp32":
-        assert err.max() / np.abs(ref).max() <= 1e-4, f"{what}: max rel err {err.max() / np.abs(ref).max():.3e}"
-    else:
-        cos = (got * ref).sum(-1) / (np.linalg.norm(got, axis=-1) * np.linalg.norm(ref, axis=-1))
-        assert cos.min() >= 0.9999, f"{what}: min token cosine {cos.min():.7f}"
-        assert err.max() <= 3e-2, f"{what}: max abs err {err.max():.3e}"
 
 
 def clip(seed, B, T, H, W):
@@ -49,23 +43,21 @@ def test_two_calls_match_context_encode(case):
     ctx = jv.Context(model, B, T, H, W)
     N = model.n_tokens(T, H, W)
     D = model.hp.embed_dim
-    outs, refs = [], []
-    for seed in (11, 12):
-        px = clip(seed, B, T, H, W)
-        refs.append(ctx.encode(px).clone())
-        out = torch.empty((B, N, D), dtype=torch.float32, device="cuda")
-        torch.cuda.synchronize()
-        free0 = torch.cuda.mem_get_info()[0]
-        model.encode_noalloc(px, out)
-        free1 = torch.cuda.mem_get_info()[0]
-        if seed == 12:  # the first call may include the one-time look-up of the array
-            assert free1 == free0, f"device free memory moved by {free0 - free1} bytes"
-        outs.append(out)
+    clips = [clip(seed, B, T, H, W) for seed in (10, 11, 12)]
+    refs = [ctx.encode(px).clone() for px in clips[1:]]
+    outs = [torch.full((B, N, D), float("nan"), dtype=torch.float32, device="cuda") for _ in range(3)]
+    model.encode_noalloc(clips[0], outs[0])   # set-up call
     torch.cuda.synchronize()
-    for i, (o, r) in enumerate(zip(outs, refs)):
-        assert torch.isfinite(o).all()
-        bar(o, r, dtype, f"{name} call {i + 1}")
-    assert not torch.equal(outs[0], outs[1])  # two clips, two results
+    free_before = torch.cuda.mem_get_info()[0]
+    model.encode_noalloc(clips[1], outs[1])
+    model.encode_noalloc(clips[2], outs[2])
+    torch.cuda.synchronize()
+    free_after = torch.cuda.mem_get_info()[0]
+    assert free_after == free_before, f"device free memory moved by {free_before - free_after} bytes"
+    for i, (o, r) in enumerate(zip(outs[1:], refs)):
+        assert torch.isfinite(o).all(), f"{name} call {i + 1}"
+        assert torch.equal(o, r), f"{name} call {i + 1}: max |d| {(o - r).abs().max().item():.3e}"
+    assert not torch.equal(outs[1], outs[2])  # two clips, two results
     assert jv.ops.device_status() == 0
 
 
