@@ -18,6 +18,12 @@ whose 3-D sin-cos table is baked for 16 x 224 x 224 and resized (trilinear), or 
 ViT-L/16 256 x 256 images whose 2-D table is baked for 224 x 224 and resized (bicubic). Their
 lines add the one-off table kernels' times ("pos_table").
 
+--workload also times the other encoder workloads, one line each: hfvit_ti14_224 (ViT-Ti/14 224^2
+image, fp32 SIMT path, roofline against the fp32 FFMA peak), vjepa2_1_vitl16_16x384 (4608 tokens,
+interleaved RoPE rescaled 15/23, modality vector), levjepa_vitl16_16x256 (4097 tokens, CLS,
+block-causal, two clips; the line adds the same clips with full attention, which shows what
+skipping the masked key tiles saves) and vjepa2_vitg16_64x256 (ViT-g/16, 8192 tokens).
+
     python bench.py [--gpus N --steps K --warmup W] [--batch B] [--workload NAME] [--impl reference]
 
 Timing: W untimed steps, then K steps replaying one CUDA graph of the encode, each bracketed by
@@ -58,6 +64,21 @@ PREDICTOR = "vjepa2_vitl16_predictor"
 HEADW = "vjepa2_vitl16_ssv2_head"
 HEAD_METRIC = "attentive-pool head tokens/s and TFLOP/s, V-JEPA 2 ViT-L SSv2 classifier head over 16×256² clips"
 PRED_METRIC = "masked predictor tokens/s and TFLOP/s, V-JEPA 2 ViT-L predictor over 16×256² clips"
+BENCH_WORKLOADS.update({
+    "hfvit_ti14_224": dict(preset="hfvit_ti14", T=1, H=224, W=224, batch=1, dtype="fp32",
+                           metric="encoder tokens/s and fraction of fp32 FFMA peak, hfvit ViT-Ti/14 224² image (fp32)",
+                           label="hfvit ViT-Ti/14 224x224 image (CLS, learned positions), fp32 SIMT path"),
+    "vjepa2_1_vitl16_16x384": dict(preset="vjepa2_1_vitl16", T=16, H=384, W=384, batch=1,
+                                   metric="encoder tokens/s and TFLOP/s, V-JEPA 2.1 ViT-L/16 16×384² video",
+                                   label="V-JEPA 2.1 ViT-L/16 16x384x384 clip (interleaved RoPE rescaled 15/23, "
+                                         "modality vector)"),
+    "levjepa_vitl16_16x256": dict(preset="levjepa_vitl16", T=16, H=256, W=256, batch=2, full_attention_control=True,
+                                  metric="encoder tokens/s and TFLOP/s, LeVJEPA ViT-L/16 16×256² video, block-causal",
+                                  label="LeVJEPA ViT-L/16 16x256x256 clip (tubelet 1, CLS, block-causal attention)"),
+    "vjepa2_vitg16_64x256": dict(preset="vjepa2_vitg16", T=64, H=256, W=256, batch=1,
+                                 metric="encoder tokens/s and TFLOP/s, V-JEPA 2 ViT-g/16 64×256² video",
+                                 label="V-JEPA 2 ViT-g/16 64x256x256 clip"),
+})
 HEADLINE = "vjepa2_vitl16_16x256"
 FLUSH_BYTES = 256 << 20  # > 129 MB of L2
 
@@ -176,32 +197,42 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ oracle timing (host cores)
-def oracle_layer_times(workload=HEADLINE):
-    """Time the oracle on the workload clip with 1 and 2 transformer layers; returns
-    (t1, t2, tokens, threads). Full-depth time = t1 + (L - 1) (t2 - t1)."""
-    import numpy as np
+def oracle_layer_times(workload=HEADLINE, layers=(0, 1)):
+    """Time the oracle on one item of the workload with each depth in `layers`; returns
+    (times, tokens, threads, full depth)."""
     from dataclasses import replace
     import oracle
     import synth
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     from configs import WORKLOADS
-    cfg, _, _, (T, H, W) = WORKLOADS[workload]
+    cfg, dtype, _, (T, H, W) = WORKLOADS[workload]
     pix = synth.pixels(0, (1, T, 3, H, W))
     times = []
-    for nl in (1, 2):
+    for nl in layers:
         t0 = time.perf_counter()
-        oracle.encode(replace(cfg, n_layer=nl), 0, True, pix)
+        oracle.encode(replace(cfg, n_layer=nl), 0, dtype == "bf16", pix)
         times.append(time.perf_counter() - t0)
-    return times[0], times[1], oracle.n_tokens(cfg, T, H, W), oracle.num_threads(), cfg.n_layer
+    return times, oracle.n_tokens(cfg, T, H, W), oracle.num_threads(), cfg.n_layer
 
 
-def cpu_baseline(workload=HEADLINE):
-    t1, t2, N, threads, L = oracle_layer_times(workload)
-    per_layer = max(t2 - t1, 1e-9)
-    full = t1 + (L - 1) * per_layer
+def cpu_baseline(workload=HEADLINE, full_depth_budget_s=20.0):
+    """The oracle on the host cores: the embedding + final norm alone (0 layers) and with one
+    layer; the full depth is then measured directly when it should take under the budget, else
+    extrapolated linearly per layer (the layers are identical in cost)."""
+    (t0, t1), N, threads, L = oracle_layer_times(workload)
+    per_layer = max(t1 - t0, 1e-9)
+    est = t0 + L * per_layer
+    if est <= full_depth_budget_s:
+        reps = max(1, min(9, int(5.0 / max(est, 1e-3))))   # short runs: the median of several
+        (*fulls,), _, _, _ = oracle_layer_times(workload, layers=(L,) * reps)
+        full = statistics.median(fulls)
+        how = f"measured at full depth ({full:.2f} s, median of {reps})"
+    else:
+        full = est
+        how = f"full-depth time {full:.1f} s extrapolated linearly per layer"
     return {"value": N / full, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-            "sample": f"fp64 oracle encodes of the same {N}-token item with 1 and 2 of the {L} layers "
-                      f"({t1:.2f} s, {t2:.2f} s); full-depth time {full:.1f} s extrapolated linearly per layer"}
+            "sample": f"fp64 oracle on one {N}-token item with 0 and 1 of the {L} layers ({t0:.2f} s, {t1:.2f} s); "
+                      + how}
 
 
 def pred_inputs(B, seed=0):
@@ -531,19 +562,20 @@ def run_reference(args):
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     from configs import WORKLOADS
     wl = BENCH_WORKLOADS[args.workload]
-    cfg, _, _, (T, H, W) = WORKLOADS[args.workload]
+    cfg, dtype, _, (T, H, W) = WORKLOADS[args.workload]
+    bf16 = dtype == "bf16"
     pix = synth.pixels(0, (1, T, 3, H, W))
     one = replace(cfg, n_layer=1)
-    # calibration: the per-layer cost (2 layers minus 1 layer)
-    t1, t2, N, threads, L = oracle_layer_times(args.workload)
-    per_layer = max(t2 - t1, 1e-9)
+    # calibration: the per-layer cost (1 layer minus the embedding and final norm alone)
+    (t0_, t1_), N, threads, L = oracle_layer_times(args.workload)
+    per_layer = max(t1_ - t0_, 1e-9)
     for _ in range(args.warmup):
-        oracle.encode(one, 0, True, pix)
+        oracle.encode(one, 0, bf16, pix)
     full_times = []
     t_start = time.perf_counter()
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        oracle.encode(one, 0, True, pix)
+        oracle.encode(one, 0, bf16, pix)
         full_times.append((time.perf_counter() - t0) + (L - 1) * per_layer)
     wall = time.perf_counter() - t_start
     mean_full = statistics.mean(full_times)
@@ -643,6 +675,72 @@ def time_pos_tables(jv, model, T, H, W, reps=20):
                     "both tables fit in L2, timed back to back without a flush"}
 
 
+def fp32_ffma_peak_tflops():
+    """Dense fp32 FFMA peak of this GPU: SMs x 128 FP32 lanes x 2 flops per FMA x the maximum SM
+    clock (the measured-peaks file's, else 2070 MHz)."""
+    import torch
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            mhz = float(json.load(f).get("sm_max_mhz", 2070.0))
+    except (OSError, ValueError):
+        mhz = 2070.0
+    return sms * 128 * 2 * mhz * 1e6 / 1e12, sms, mhz
+
+
+def profile_classes(jv, ctx, pix, out, flush, steps, warmup, stream):
+    """Per-kernel-class durations: `steps` encodes with the library's event hook (events captured
+    inside the graph; eager launches if the driver cannot time those). Returns (classes, ms per
+    step of the profiled pass, launch mode, clock summary)."""
+    import torch
+    ctx.set_profiling(True)
+    launch_mode = "CUDA graph replay of the encode"
+    try:
+        for _ in range(2):
+            ctx.encode(pix, out)
+        ctx.sync()
+        ctx.profile(reset=True)
+    except jv.JepaError:
+        ctx.set_graph(False)
+        launch_mode = "CUDA graph replay of the encode (per-kernel events: eager launches)"
+    for _ in range(warmup):
+        flush.zero_()
+        ctx.encode(pix, out)
+    ctx.sync()
+    ctx.profile(reset=True)
+    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        p0.record(stream)
+        for _ in range(steps):
+            flush.zero_()
+            ctx.encode(pix, out)
+        p1.record(stream)
+        torch.cuda.synchronize()
+    ctx.sync()
+    prof = ctx.profile(reset=True)
+    ctx.set_profiling(False)
+    return prof, p0.elapsed_time(p1) / steps, launch_mode, clk.summary()
+
+
+def full_attention_control(jv, wl, B, steps, warmup, flush, rank, local):
+    """The same clips through the same encoder with full attention instead of the block-causal
+    mask: what skipping the masked key tiles saves (step time and attention kernel time)."""
+    import torch
+    import synth
+    T, H, W = wl["T"], wl["H"], wl["W"]
+    model = jv.Model.preset(wl["preset"], seed=0, dtype="bf16", device=local, attn_mode=jv.ATTN_FULL)
+    ms = time_graph_steps(jv, model, wl, B, steps, warmup, flush, rank)
+    ctx = jv.Context(model, B, T, H, W, graph=True)
+    pix = torch.from_numpy(synth.pixels(rank, (B, T, 3, H, W))).cuda()
+    out = torch.empty((B, model.n_tokens(T, H, W), model.hp.embed_dim), dtype=torch.float32, device="cuda")
+    with torch.cuda.stream(ctx.stream):
+        prof, _, _, _ = profile_classes(jv, ctx, pix, out, flush, min(steps, 10), warmup, ctx.stream)
+    ctx.close()
+    att = prof["attention"]
+    return {"ms_per_step": ms, "attention_avg_us": 1e3 * att["total_ms"] / att["launches"],
+            "attention_tflops_all_pairs": att["flops"] / (att["total_ms"] / 1e3) / 1e12}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -656,7 +754,8 @@ def run_ours(args):
 
     wl = BENCH_WORKLOADS[args.workload]
     B, T, H, W = args.batch or wl["batch"], wl["T"], wl["H"], wl["W"]
-    model = jv.Model.preset(wl["preset"], seed=0, dtype="bf16", device=local)
+    dtype = wl.get("dtype", "bf16")
+    model = jv.Model.preset(wl["preset"], seed=0, dtype=dtype, device=local)
     ctx = jv.Context(model, B, T, H, W)
     N = model.n_tokens(T, H, W)
     D = model.hp.embed_dim
@@ -694,32 +793,8 @@ def run_ours(args):
         # per-kernel durations: the same K steps again with the library's event hook (events
         # captured inside the graph; eager launches if the driver cannot time those). The events
         # between kernels lengthen the step, so the headline above is taken without them.
-        ctx.set_profiling(True)
-        launch_mode = "CUDA graph replay of the encode"
-        try:
-            for _ in range(2):
-                ctx.encode(pix, out)
-            ctx.sync()
-            ctx.profile(reset=True)
-        except jv.JepaError:
-            ctx.set_graph(False)
-            launch_mode = "CUDA graph replay of the encode (per-kernel events: eager launches)"
-        for _ in range(args.warmup):
-            flush.zero_()
-            ctx.encode(pix, out)
-        ctx.sync()
-        ctx.profile(reset=True)
-        p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with ClockSampler(local) as clk_prof:
-            p0.record(stream)
-            for i in range(args.steps):
-                flush.zero_()
-                ctx.encode(pix, out)
-            p1.record(stream)
-            torch.cuda.synchronize()
-        ctx.sync()
-        prof = ctx.profile(reset=True)
-        ctx.set_profiling(False)
+        prof, prof_ms, launch_mode, clk_prof = profile_classes(jv, ctx, pix, out, flush, args.steps, args.warmup,
+                                                               stream)
 
         # the same step with eager launches, for comparison (not the headline)
         ctx.set_graph(False)
@@ -747,7 +822,13 @@ def run_ours(args):
     # dominant kernel class of the timed region
     name, st = max(prof.items(), key=lambda kv: kv[1]["total_ms"])
     avg_ms = st["total_ms"] / st["launches"]
-    if st["flops"] > 0:
+    fp32_peak, n_sms, max_mhz = fp32_ffma_peak_tflops()
+    if st["flops"] > 0 and dtype == "fp32":
+        achieved = st["flops"] / st["launches"] / (avg_ms / 1e3) / 1e12
+        roof = {"bound": "alu", "achieved": achieved, "peak": fp32_peak, "unit": "TFLOP/s",
+                "frac": achieved / fp32_peak, "kernel": name,
+                "peak_derivation": f"{n_sms} SMs x 128 fp32 FMA lanes x 2 flops x {max_mhz:.0f} MHz"}
+    elif st["flops"] > 0:
         achieved = st["flops"] / st["launches"] / (avg_ms / 1e3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": achieved / peaks["bf16_tflops"], "kernel": name,
@@ -800,6 +881,16 @@ def run_ours(args):
         b1 = {"ms_per_step": ms1, "value": world * N / (ms1 / 1e3), "unit": "tokens/s",
               "tflops": world * fl1 / (ms1 / 1e3) / 1e12,
               "frac_of_bf16_peak": fl1 / (ms1 / 1e3) / 1e12 / peaks["bf16_tflops"]}
+    control = None
+    if wl.get("full_attention_control"):
+        control = full_attention_control(jv, wl, B, min(args.steps, 20), args.warmup, flush, rank, local)
+        att = prof["attention"]
+        att_us = 1e3 * att["total_ms"] / att["launches"]
+        control.update({"block_causal_ms_per_step": ms_per_step, "block_causal_attention_avg_us": att_us,
+                        "step_speedup": control["ms_per_step"] / ms_per_step,
+                        "attention_speedup": control["attention_avg_us"] / att_us,
+                        "note": "same weights and clips, attn_mode full: every key tile visited; the "
+                                "block-causal run visits only tiles with a visible pair"})
     pos_table = time_pos_tables(jv, model, T, H, W) if model.hp.pos_type in (jv.POS_SINCOS2D, jv.POS_SINCOS3D) else None
     line = None
     if rank == 0:
@@ -810,13 +901,18 @@ def run_ours(args):
                            "tokens_per_step": tokens_per_step, "global_batch": world * B, "seq_len": N,
                            "parallelism": f"replicas x{world} (independent clips, no collective)",
                            "l2": "flushed (256 MiB write) between steps", "weights": "seeded synthetic"},
-                "tflops": tflops, "frac_of_bf16_peak": tflops / (world * peaks["bf16_tflops"]),
-                "eager_ms_per_step": eager_ms, "launch_mode": launch_mode,
+                "tflops": tflops, "eager_ms_per_step": eager_ms, "launch_mode": launch_mode,
                 "roofline": roof, "kernels": kernels,
                 "e2e": e2e, "gpu_launches": launches * args.steps, "batch1": b1,
                 "clocks": {k: v for k, v in clk.summary().items()},
-                "profiled_pass": {"ms_per_step": p0.elapsed_time(p1) / args.steps,
-                                  "clocks": clk_prof.summary()}}
+                "profiled_pass": {"ms_per_step": prof_ms, "clocks": clk_prof}}
+        if dtype == "fp32":
+            line["dtype"] = "f32"
+            line["frac_of_fp32_peak"] = tflops / (world * fp32_peak)
+        else:
+            line["frac_of_bf16_peak"] = tflops / (world * peaks["bf16_tflops"])
+        if control:
+            line["full_attention_control"] = control
         if pos_table:
             line["pos_table"] = pos_table
         if world == 1 and not args.no_cpu_baseline:

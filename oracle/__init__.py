@@ -30,6 +30,7 @@ class OracleHParams(ctypes.Structure):
         ("rope_ref_grid", ctypes.c_int), ("cls_token", ctypes.c_int), ("modality_embed", ctypes.c_int),
         ("attn_mode", ctypes.c_int), ("n_pos_rows", ctypes.c_int), ("img_size", ctypes.c_int),
         ("n_frames", ctypes.c_int), ("sincos_w_first", ctypes.c_int), ("sincos_uniform_power", ctypes.c_int),
+        ("q_weight_scale", ctypes.c_double), ("k_weight_scale", ctypes.c_double),
     ]
 
 
@@ -57,6 +58,10 @@ class Config:
     n_frames: int = 0
     sincos_w_first: int = 0    # sincos2d halves [w | h] (HF I-JEPA order)
     sincos_uniform_power: int = 0
+    # test input option, not part of the method: the synthetic q / k rows of every attn_qkv.weight
+    # are multiplied by these factors (powers of two keep bf16 weights exact), for peaked attention
+    q_weight_scale: float = 1.0
+    k_weight_scale: float = 1.0
 
     def struct(self) -> OracleHParams:
         return OracleHParams(**asdict(self))

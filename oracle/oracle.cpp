@@ -469,10 +469,14 @@ namespace {
 // predictor blocks have the encoder's layout).
 struct BlockW {
   std::vector<double> ln1w, ln1b, wqkv, bqkv, wout, bout, ln2w, ln2b, wup, bup, wdn, bdn;
-  void gen(uint64_t seed, const std::string& p, int bf16_weights, int D, int F) {
+  void gen(uint64_t seed, const std::string& p, int bf16_weights, int D, int F, double q_scale = 1.0,
+           double k_scale = 1.0) {
     gen_param(seed, p + "ln1.weight", bf16_weights, D, ln1w);
     gen_param(seed, p + "ln1.bias", bf16_weights, D, ln1b);
     gen_param(seed, p + "attn_qkv.weight", bf16_weights, (size_t)3 * D * D, wqkv);
+    // test input option (oracle.h): scaled q and k rows
+    for (size_t i = 0; i < (size_t)D * D; ++i) wqkv[i] *= q_scale;
+    for (size_t i = (size_t)D * D; i < (size_t)2 * D * D; ++i) wqkv[i] *= k_scale;
     gen_param(seed, p + "attn_qkv.bias", bf16_weights, (size_t)3 * D, bqkv);
     gen_param(seed, p + "attn_out.weight", bf16_weights, (size_t)D * D, wout);
     gen_param(seed, p + "attn_out.bias", bf16_weights, D, bout);
@@ -591,7 +595,7 @@ int oracle_encode(const oracle_hparams* hp, uint64_t seed, int bf16_weights, con
   BlockScratch sc(N, D, F);
   for (int l = 0; l < hp->n_layer; ++l) {
     BlockW w;
-    w.gen(seed, "enc.blk." + std::to_string(l) + ".", bf16_weights, D, F);
+    w.gen(seed, "enc.blk." + std::to_string(l) + ".", bf16_weights, D, F, hp->q_weight_scale, hp->k_weight_scale);
     for (int b = 0; b < B; ++b)
       block_forward(w, X.data() + (size_t)b * MD, N, D, NH, F, hp->ln_eps, hp->pos_type == 2 ? rc.data() : nullptr,
                     rs.data(), hp->attn_mode, prefix, frame_tokens, sc);

@@ -43,6 +43,11 @@ typedef struct {
   int n_frames;         /* ... x (frames/t) positions */
   int sincos_w_first;   /* sincos2d halves ordered [w | h] (HF I-JEPA) instead of [h | w] */
   int sincos_uniform_power; /* sincos3d: three equal axis widths 2*ceil(D/6), cut to D */
+  /* Test input, not part of the method: the synthetic q rows [0, D) and k rows [D, 2D) of every
+   * enc.blk.*.attn_qkv.weight are multiplied by these factors (1 = the plain recipe). Powers of
+   * two keep bf16 weights exact; larger q, k give peaked attention, so that a test encoder's
+   * output depends strongly on the scores (RoPE layout, mask). */
+  double q_weight_scale, k_weight_scale;
 } oracle_hparams;
 
 /* Number of tokens of one item: (T/t)(H/P)(W/P) + cls. Returns -1 if a size is not divisible. */

@@ -103,8 +103,9 @@ def encoder_kvs(cfg, family=None):
 
 def encoder_tensors(cfg, seed=0, matrix_type=GGML_BF16, fused=True, pos_table=None, round_bf16=True):
     """The enc.* tensors of an oracle Config with the generator's values (matrices bf16-rounded, as
-    the bf16 model holds them, unless round_bf16 is false); pos_table: the table of a sin-cos model
-    (rows of its training grid)."""
+    the bf16 model holds them, unless round_bf16 is false; q / k rows of attn_qkv.weight scaled by
+    the Config's q_weight_scale / k_weight_scale); pos_table: the table of a sin-cos model (rows of
+    its training grid)."""
     D, F, L = cfg.embed_dim, cfg.ffn_dim, cfg.n_layer
     K = cfg.in_chans * cfg.tubelet_size * cfg.patch_size ** 2
     P = lambda name, shape: synth.param(seed, name, shape, round_bf16)  # noqa: E731
@@ -122,6 +123,9 @@ def encoder_tensors(cfg, seed=0, matrix_type=GGML_BF16, fused=True, pos_table=No
         p = f"enc.blk.{l}."
         ts += [(p + "ln1.weight", P(p + "ln1.weight", (D,)), GGML_F32), (p + "ln1.bias", P(p + "ln1.bias", (D,)), GGML_F32)]
         wqkv, bqkv = P(p + "attn_qkv.weight", (3 * D, D)), P(p + "attn_qkv.bias", (3 * D,))
+        # the oracle's test input option: q and k rows scaled (powers of two: exact in bf16)
+        wqkv[:D] *= np.float32(getattr(cfg, "q_weight_scale", 1.0))
+        wqkv[D:2 * D] *= np.float32(getattr(cfg, "k_weight_scale", 1.0))
         if fused:
             ts += [(p + "attn_qkv.weight", wqkv, matrix_type), (p + "attn_qkv.bias", bqkv, GGML_F32)]
         else:

@@ -269,6 +269,40 @@ def test_attention_bf16(B, N, H, mode, prefix, F):
         assert np.abs(got - full).max() > 1e-2 * vmax
 
 
+# The workloads' full attention geometries: V-JEPA 2.1 at 384 px (4608 tokens, 16 heads), LeVJEPA's
+# two clips of 4097 tokens (CLS + 16 frames of 256, block-causal), ViT-g/16's 8192 tokens x 22 heads.
+# Every head runs on the GPU; the oracle computes the listed heads (all queries and keys of each,
+# the last head included), compared element by element under the same bar as above.
+FULL_ATTN_CASES = [
+    # name, B, N, H, mode, prefix, frame_tokens, heads checked
+    ("vjepa2_1_16x384", 1, 4608, 16, 0, 0, 1, (0, 7, 15)),
+    ("levjepa_16x256_2clips", 2, 4097, 16, 1, 1, 256, (0, 9, 15)),
+    ("vitg16_64x256", 1, 8192, 22, 0, 0, 1, (0, 13, 21)),
+]
+
+
+def head_cols(H, heads):
+    D = H * 64
+    cols = [np.arange(h * 64, (h + 1) * 64) for h in heads]
+    one = np.concatenate(cols)
+    return one, np.concatenate([one, D + one, 2 * D + one])
+
+
+@pytest.mark.parametrize("name,B,N,H,mode,prefix,F,heads", FULL_ATTN_CASES, ids=[c[0] for c in FULL_ATTN_CASES])
+def test_attention_bf16_full_geometry(name, B, N, H, mode, prefix, F, heads):
+    qkv = bf16_exact(attn_inputs(B, N, H, 90 + H))
+    got = f64(jv.ops.attention(qkv.to(DEV), B, N, H, 64, mode, prefix, F))
+    out_cols, in_cols = head_cols(H, heads)
+    x = f64(qkv)[:, in_cols]
+    ref = ref_attention(x, B, N, len(heads), mode, prefix, F)
+    vmax = np.abs(x[:, 2 * len(heads) * 64:]).max()
+    err = np.abs(got[:, out_cols] - ref).max()
+    assert err <= 1e-2 * vmax, f"{name}: max |d| {err:.3e} against 1 % of max |v| {vmax:.3f}"
+    if mode == 1:   # control: the unmasked result is outside the bar
+        full = ref_attention(x, B, N, len(heads), 0, prefix, F)
+        assert np.abs(got[:, out_cols] - full).max() > 1e-2 * vmax
+
+
 @pytest.mark.parametrize("B,N,H,mode,prefix,F", [(1, 257, 3, 0, 0, 1), (2, 1 + 3 * 50, 2, 1, 1, 50),
                                                  (1, 300, 2, 1, 0, 75)])
 def test_attention_fp32(B, N, H, mode, prefix, F):

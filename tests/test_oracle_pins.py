@@ -407,7 +407,10 @@ def torch_encoder(cfg: Config, seed, bf16, pix):
     for l in range(cfg.n_layer):
         p = f"enc.blk.{l}."
         h = torch.nn.functional.layer_norm(x, (D,), prm(p + "ln1.weight", (D,)), prm(p + "ln1.bias", (D,)), cfg.ln_eps)
-        qkv = h @ prm(p + "attn_qkv.weight", (3 * D, D)).T + prm(p + "attn_qkv.bias", (3 * D,))
+        wqkv = prm(p + "attn_qkv.weight", (3 * D, D))
+        wqkv[:D] *= cfg.q_weight_scale     # test input option: scaled q and k rows
+        wqkv[D:2 * D] *= cfg.k_weight_scale
+        qkv = h @ wqkv.T + prm(p + "attn_qkv.bias", (3 * D,))
         q, k, v = (qkv[..., i * D:(i + 1) * D].reshape(B, N, NH, hd).transpose(1, 2) for i in range(3))
         if cfg.pos_type == 2:
             q, k = rope(q), rope(k)
@@ -429,6 +432,9 @@ ENC_CASES = {
                                        rope_ref_grid=4, modality_embed=1), (4, 12, 20)),
     "levjepa_block_causal": (tiny_video(embed_dim=128, n_head=2, ffn_dim=96, tubelet_size=1, cls_token=1,
                                         attn_mode=1), (3, 12, 8)),
+    # peaked attention: the q / k rows of attn_qkv.weight scaled by 4 and 2 (a test input option)
+    "levjepa_peaked": (tiny_video(embed_dim=128, n_head=2, ffn_dim=96, tubelet_size=1, cls_token=1, attn_mode=1,
+                                  q_weight_scale=4.0, k_weight_scale=2.0), (3, 12, 8)),
 }
 
 
@@ -460,3 +466,16 @@ def test_batch_items_are_independent():
     out = oracle.encode(cfg, 5, True, pix)
     for b in range(3):
         assert np.array_equal(out[b], oracle.encode(cfg, 5, True, pix[b:b + 1])[0])
+
+
+def test_qk_weight_scale_touches_only_the_q_and_k_rows():
+    """The scale option multiplies the q rows by its first factor and the k rows by its second:
+    (a, b) and (b, a) swap nothing for scores (q.k scales by a*b either way) but do change the
+    tokens, since the biases are not scaled; (1, 1) is the plain recipe."""
+    cfg, (T, H, W) = ENC_CASES["vjepa2_tiled"]
+    pix = synth.pixels(6, (1, T, 3, H, W))
+    plain = oracle.encode(cfg, 6, True, pix)
+    assert np.array_equal(oracle.encode(replace(cfg, q_weight_scale=1.0, k_weight_scale=1.0), 6, True, pix), plain)
+    a = oracle.encode(replace(cfg, q_weight_scale=4.0, k_weight_scale=2.0), 6, True, pix)
+    b = oracle.encode(replace(cfg, q_weight_scale=2.0, k_weight_scale=4.0), 6, True, pix)
+    assert np.abs(a - plain).max() > 1e-3 and np.abs(a - b).max() > 1e-6
