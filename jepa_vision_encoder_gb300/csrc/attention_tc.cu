@@ -22,8 +22,14 @@
 //   warp 9      idle: the third warpgroup is whole so that it can hand registers to the softmax
 //               warpgroups (setmaxnreg: 200 per softmax thread, 104 in warpgroup 2).
 // TMEM (512 columns): S0 [0,128) S1 [128,256) P0 [256,320) P1 [320,384) O0, O1 from 384 (HD each).
-// Block-causal: a CTA only visits keys below the last frame its rows can see, and the per-element
-// predicate runs only on tiles that straddle a frame edge, the CLS row/column or N.
+// Block-causal: a CTA only visits keys below the last frame its rows can see, and a query tile
+// that sees none of a key tile's keys writes P = 0 without computing exponentials. When a frame is
+// a whole number of 128-row tiles, the query and key tiles start at the first patch row (after the
+// CLS prefix), so every tile lies inside one frame and no tile needs the per-element predicate
+// (except the ragged end at N); the CTAs covering one frame's rows (heaviest frames first) see
+// key tiles 0 .. the end of that frame. The prefix rows, which see every key, are one extra CTA per
+// (item, head) computing them in fp32 on the CUDA cores. Otherwise the tiles start at row 0 and
+// tiles that straddle a frame edge, the CLS row/column or N take the per-element predicate.
 #include <cuda_bf16.h>
 
 #include <mutex>
@@ -64,9 +70,14 @@ struct AttnDev {
   int attn_mode, prefix, frame_tokens;
   int out_hd;  // output columns per head: the head width
   __nv_bfloat16* out;
+  const __nv_bfloat16* qkv;  // [B*N, 3D]: read by the prefix-row CTAs
   float scale_log2;
   int* err;
   uint64_t limit_ns;
+  // frame-aligned block-causal tiling: tiles start at row k_origin (= prefix), the first
+  // n_prefix_ctas CTAs of each (head, item) compute the prefix rows, the next n_main CTAs take the
+  // 256-row query blocks, last block first
+  int aligned, k_origin, n_prefix_ctas, n_main;
 };
 
 // Visible keys of query row q are [lo, hi).
@@ -97,7 +108,92 @@ __device__ __forceinline__ uint64_t tile_desc(uint32_t saddr) {
   else return smem_desc_sw64(saddr, 512, 512);
 }
 
+// The prefix (CLS) rows of one (item, head) under the block-causal mask: each sees every key, so
+// this is full attention of `prefix` query rows over N keys, in fp32 on the CUDA cores: scores of
+// all keys into shared memory (one key row per thread at a time), their max, p = 2^(s - max) and
+// the sum, then o = sum_k p_k v_k with each warp taking every twelfth key and each lane HD/32 of
+// the columns, the warps' partial rows added in shared memory. sm holds N + (kThreads/32 + 1) * HD + 64
+// floats.
 template <int HD>
+__device__ __forceinline__ void attn_prefix_rows(const AttnDev& a, int h, int b, float* sm) {
+  constexpr int kWarps = kThreads / 32, kPer = HD / 32;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const size_t ld = 3 * (size_t)a.D;
+  const __nv_bfloat16* rows = a.qkv + (size_t)b * a.N * ld;
+  float* sc = sm;                        // [N] scores, then p
+  float* part = sm + ((a.N + 3) & ~3);   // [kWarps][HD] partial outputs
+  float* qv = part + kWarps * HD;        // [HD] the query row
+  float* red = qv + HD;                  // [2 * kWarps] reductions
+  for (int r = 0; r < a.prefix; ++r) {
+    if (tid < HD) qv[tid] = __bfloat162float(rows[(size_t)r * ld + h * HD + tid]);
+    __syncthreads();
+    float mx = -INFINITY;
+    for (int k = tid; k < a.N; k += kThreads) {
+      const uint4* kr = reinterpret_cast<const uint4*>(rows + (size_t)k * ld + a.D + h * HD);
+      float dot = 0.0f;
+#pragma unroll
+      for (int u = 0; u < HD / 8; ++u) {
+        const uint4 w = __ldg(kr + u);
+        const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[t]));
+          dot = fmaf(qv[u * 8 + 2 * t], f.x, dot);
+          dot = fmaf(qv[u * 8 + 2 * t + 1], f.y, dot);
+        }
+      }
+      const float sv = dot * a.scale_log2;
+      sc[k] = sv;
+      mx = fmaxf(mx, sv);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) red[warp] = mx;
+    __syncthreads();
+    mx = red[0];
+    for (int w = 1; w < kWarps; ++w) mx = fmaxf(mx, red[w]);
+    float sum = 0.0f;
+    for (int k = tid; k < a.N; k += kThreads) {
+      const float pv = ex2_approx(sc[k] - mx);
+      sc[k] = pv;
+      sum += pv;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (lane == 0) red[kWarps + warp] = sum;
+    __syncthreads();  // every p is in sc and every partial sum in red
+    float acc[kPer];
+#pragma unroll
+    for (int t = 0; t < kPer; ++t) acc[t] = 0.0f;
+    for (int k = warp; k < a.N; k += kWarps) {
+      const float pv = sc[k];
+      const __nv_bfloat16* vr = rows + (size_t)k * ld + 2 * a.D + h * HD + lane * kPer;
+      if constexpr (kPer == 2) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(vr));
+        acc[0] = fmaf(pv, f.x, acc[0]);
+        acc[1] = fmaf(pv, f.y, acc[1]);
+      } else {
+        acc[0] = fmaf(pv, __bfloat162float(*vr), acc[0]);
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < kPer; ++t) part[warp * HD + lane * kPer + t] = acc[t];
+    __syncthreads();
+    if (tid < HD) {
+      float l = 0.0f, o = 0.0f;
+      for (int w = 0; w < kWarps; ++w) {
+        l += red[kWarps + w];
+        o += part[w * HD + tid];
+      }
+      a.out[((size_t)b * a.N + r) * (a.H * a.out_hd) + h * a.out_hd + tid] = __float2bfloat16_rn(o / l);
+    }
+    __syncthreads();  // sc, part, qv and red are reused by the next prefix row
+  }
+}
+
+// BC: the block-causal form (per-row key windows, tiles without visible keys skipped, the
+// frame-aligned tiling and the prefix-row CTAs); the full-attention form compiles without them.
+template <int HD, bool BC>
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_constant__ CUtensorMap tm, AttnDev a) {
   constexpr int kHD = HD;
   constexpr int kTileBytes = Width<HD>::kTileBytes;
@@ -122,8 +218,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int q0 = blockIdx.x * 2 * kQT, h = blockIdx.y, b = blockIdx.z;
-  const int num_kt = (keys_needed(a, q0, q0 + 2 * kQT) + kKT - 1) / kKT;
+  // the aligned form's grid is (head, item, job) so that jobs run heaviest first over all (item,
+  // head) pairs: job 0 the prefix rows, then the query blocks from the last frame back
+  const bool aligned = BC && a.aligned;
+  const int k_origin = BC ? a.k_origin : 0;
+  const int h = aligned ? blockIdx.x : blockIdx.y, b = aligned ? blockIdx.y : blockIdx.z;
+  const int job = aligned ? (int)blockIdx.z : (int)blockIdx.x;
+  if (aligned && job < a.n_prefix_ctas) {
+    pdl_trigger();
+    pdl_wait();  // qkv comes from the previous kernel
+    attn_prefix_rows<HD>(a, h, b, reinterpret_cast<float*>(smem));
+    return;
+  }
+  // first query row of the CTA: 256-row blocks from k_origin, in the aligned form last block first
+  const int q0 = aligned ? k_origin + (a.n_main - 1 - (job - a.n_prefix_ctas)) * 2 * kQT : job * 2 * kQT;
+  const int num_kt = BC ? (keys_needed(a, q0, q0 + 2 * kQT) - k_origin + kKT - 1) / kKT : (a.N + kKT - 1) / kKT;
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(q_full), 1);
@@ -171,8 +280,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         if (!mbar_wait(smem_u32(kv_empty + stage), phase ^ 1u, wc)) break;
         const uint32_t fb = smem_u32(kv_full + stage);
         mbar_arrive_expect_tx(fb, 2 * kTileBytes);
-        tma_load_3d(smem_u32(sK + stage * kTileBytes), &tm, fb, a.D + h * kHD, j * kKT, b);
-        tma_load_3d(smem_u32(sV + stage * kTileBytes), &tm, fb, 2 * a.D + h * kHD, j * kKT, b);
+        tma_load_3d(smem_u32(sK + stage * kTileBytes), &tm, fb, a.D + h * kHD, k_origin + j * kKT, b);
+        tma_load_3d(smem_u32(sV + stage * kTileBytes), &tm, fb, 2 * a.D + h * kHD, k_origin + j * kKT, b);
         armed |= 1u << stage;
         armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
         if (++stage == kKvStages) {
@@ -272,13 +381,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     const float sc = a.scale_log2;
     // uniform per warpgroup: the tile's query span for the mask classification
     const int q_first = max(qt0, a.prefix), q_last = min(qt0 + kQT - 1, a.N - 1);
-    const int f_min = (a.attn_mode == 1 && q_last >= q_first) ? (q_first - a.prefix) / a.frame_tokens : 0;
+    const int f_min = (BC && q_last >= q_first) ? (q_first - a.prefix) / a.frame_tokens : 0;
+    // key tiles this tile's rows can see at all; past them the group writes P = 0 (no exponentials)
+    const int kt_vis = BC ? (keys_needed(a, qt0, qt0 + kQT) - k_origin + kKT - 1) / kKT : num_kt;
     float m_run = -INFINITY, l_run = 0.0f;
     bool ok = true;
     for (int j = 0; j < num_kt; ++j) {
-      const int k0 = j * kKT;
+      const int k0 = k_origin + j * kKT;
+      const bool none = BC && j >= kt_vis;  // uniform over the warpgroup
       bool masked = (k0 + kKT > a.N);
-      if (a.attn_mode == 1) {
+      if (BC && !aligned) {
         const int k_last = min(k0 + kKT - 1, a.N - 1);
         const int fk_max = (k_last - a.prefix) / a.frame_tokens;
         masked = masked || qt0 < a.prefix || k0 < a.prefix || fk_max > f_min || q_last < q_first;
@@ -296,6 +408,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(s_free + g * kIssuers + j % kIssuers));  // S may be overwritten now
+      if (none) {  // no key of this tile is visible to these rows: P = 0, m and l unchanged
+        if (j > 0) {
+          if (!mbar_wait(smem_u32(o_done + g), (uint32_t)((j - 1) & 1), wc)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        uint32_t zero[kKT / 2];
+#pragma unroll
+        for (int e = 0; e < kKT / 2; ++e) zero[e] = 0u;
+        tmem_st64(tP, zero);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(smem_u32(p_full + g * kIssuers + j % kIssuers));
+        continue;
+      }
       if (masked) {  // invisible keys score -inf: they lose the max and give p = 0
 #pragma unroll
         for (int c = 0; c < kKT / 32; ++c)
@@ -408,12 +537,13 @@ cudaError_t tc_kernels_init() {
   static cudaError_t result = cudaSuccess;
   std::call_once(once, [] {
     result = gemm_tc_init_attributes();
-    if (result == cudaSuccess)
-      result = cudaFuncSetAttribute(attn_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    Width<64>::kSmemBytes);
-    if (result == cudaSuccess)
-      result = cudaFuncSetAttribute(attn_tc_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    Width<32>::kSmemBytes);
+    auto set = [&](const void* f, int bytes) {
+      if (result == cudaSuccess) result = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    };
+    set((const void*)attn_tc_kernel<64, false>, Width<64>::kSmemBytes);
+    set((const void*)attn_tc_kernel<64, true>, Width<64>::kSmemBytes);
+    set((const void*)attn_tc_kernel<32, false>, Width<32>::kSmemBytes);
+    set((const void*)attn_tc_kernel<32, true>, Width<32>::kSmemBytes);
   });
   return result;
 }
@@ -430,14 +560,27 @@ cudaError_t attention_tc_launch(const CUtensorMap& tmQKV, const AttnParams& p, i
   a.prefix = p.prefix;
   a.frame_tokens = p.frame_tokens > 0 ? p.frame_tokens : 1;
   a.out = reinterpret_cast<__nv_bfloat16*>(p.out);
+  a.qkv = reinterpret_cast<const __nv_bfloat16*>(p.qkv);
   a.out_hd = p.head_dim;
   a.scale_log2 = 1.4426950408889634f / sqrtf((float)p.head_dim);  // log2(e) / sqrt(head width)
   a.err = err;
   a.limit_ns = limit_ns;
-  dim3 grid((p.N + 2 * kQT - 1) / (2 * kQT), p.H, p.B);
+  // Frame-aligned block-causal tiling when frames are whole tiles: the patch rows N - prefix are
+  // frames of frame_tokens rows; the prefix rows' scores must fit the shared memory.
+  const int smem_bytes = p.head_dim == 32 ? Width<32>::kSmemBytes : Width<64>::kSmemBytes;
+  const long long prefix_smem = 4LL * (((long long)p.N + 3) & ~3LL) + 4LL * (kThreads / 32 + 1) * p.head_dim + 4LL * 64;
+  a.aligned = p.attn_mode == 1 && p.frame_tokens % kKT == 0 && (p.N - p.prefix) % p.frame_tokens == 0 &&
+              p.prefix <= 8 && (p.prefix == 0 || (p.qkv != nullptr && prefix_smem <= smem_bytes - 1024));
+  a.k_origin = a.aligned ? p.prefix : 0;
+  a.n_prefix_ctas = (a.aligned && p.prefix > 0) ? 1 : 0;
+  a.n_main = a.aligned ? (p.N - p.prefix + 2 * kQT - 1) / (2 * kQT) : (p.N + 2 * kQT - 1) / (2 * kQT);
+  const dim3 grid = a.aligned ? dim3(p.H, p.B, a.n_prefix_ctas + a.n_main) : dim3(a.n_main, p.H, p.B);
+  const bool bc = p.attn_mode == 1;
   if (p.head_dim == 32)
-    return launch_kernel(attn_tc_kernel<32>, grid, dim3(kThreads), Width<32>::kSmemBytes, s, tmQKV, a);
-  return launch_kernel(attn_tc_kernel<64>, grid, dim3(kThreads), Width<64>::kSmemBytes, s, tmQKV, a);
+    return launch_kernel(bc ? attn_tc_kernel<32, true> : attn_tc_kernel<32, false>, grid, dim3(kThreads),
+                         Width<32>::kSmemBytes, s, tmQKV, a);
+  return launch_kernel(bc ? attn_tc_kernel<64, true> : attn_tc_kernel<64, false>, grid, dim3(kThreads),
+                       Width<64>::kSmemBytes, s, tmQKV, a);
 }
 
 }  // namespace jepa

@@ -71,7 +71,8 @@ cudaError_t gemm_simt_launch(const float* A, const float* Bw, const EpiArgs& epi
 struct AttnParams {
   int B, N, H, head_dim;
   int attn_mode, prefix, frame_tokens;
-  void* out;  // [B*N, H*head_dim]
+  void* out;                  // [B*N, H*head_dim]
+  const void* qkv = nullptr;  // [B*N, 3*H*head_dim]: read directly by the block-causal prefix rows
 };
 cudaError_t attention_tc_launch(const CUtensorMap& tmQKV, const AttnParams& p, int* err, uint64_t limit_ns,
                                 cudaStream_t s);

@@ -1121,6 +1121,7 @@ jepa_status encode_lane(jepa_context* c, const jepa_context::Lane& ln, cudaStrea
   ap.prefix = g.prefix;
   ap.frame_tokens = g.gh * g.gw;
   ap.out = ln.ao;
+  ap.qkv = ln.qkv;
 
   for (int l = 0; l < L; ++l) {
     const LayerW& w = m->layers[l];
@@ -1577,6 +1578,7 @@ extern "C" jepa_status jepa_op_attention(int32_t dtype, const void* d_qkv, int32
   p.prefix = prefix;
   p.frame_tokens = frame_tokens;
   p.out = d_out;
+  p.qkv = d_qkv;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (dtype == JEPA_FP32) {
     CUDA_TRY(attention_simt_launch(reinterpret_cast<const float*>(d_qkv), p, s));

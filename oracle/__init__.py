@@ -59,7 +59,8 @@ class Config:
     sincos_w_first: int = 0    # sincos2d halves [w | h] (HF I-JEPA order)
     sincos_uniform_power: int = 0
     # test input option, not part of the method: the synthetic q / k rows of every attn_qkv.weight
-    # are multiplied by these factors (powers of two keep bf16 weights exact), for peaked attention
+    # are multiplied by these factors in float (bf16 weights: rounded to bf16 again), for peaked
+    # attention
     q_weight_scale: float = 1.0
     k_weight_scale: float = 1.0
 

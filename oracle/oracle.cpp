@@ -474,9 +474,14 @@ struct BlockW {
     gen_param(seed, p + "ln1.weight", bf16_weights, D, ln1w);
     gen_param(seed, p + "ln1.bias", bf16_weights, D, ln1b);
     gen_param(seed, p + "attn_qkv.weight", bf16_weights, (size_t)3 * D * D, wqkv);
-    // test input option (oracle.h): scaled q and k rows
-    for (size_t i = 0; i < (size_t)D * D; ++i) wqkv[i] *= q_scale;
-    for (size_t i = (size_t)D * D; i < (size_t)2 * D * D; ++i) wqkv[i] *= k_scale;
+    // test input option (oracle.h): scaled q and k rows; with bf16 weights the scaled value is
+    // rounded to bf16 again (exact for powers of two), as a bf16 model holds a file's f32 value
+    if (q_scale != 1.0 || k_scale != 1.0) {
+      for (size_t i = 0; i < (size_t)2 * D * D; ++i) {
+        const float v = (float)(wqkv[i] * (i < (size_t)D * D ? q_scale : k_scale));
+        wqkv[i] = bf16_weights ? (double)jsynth_round_bf16(v) : (double)v;
+      }
+    }
     gen_param(seed, p + "attn_qkv.bias", bf16_weights, (size_t)3 * D, bqkv);
     gen_param(seed, p + "attn_out.weight", bf16_weights, (size_t)D * D, wout);
     gen_param(seed, p + "attn_out.bias", bf16_weights, D, bout);

@@ -44,9 +44,10 @@ typedef struct {
   int sincos_w_first;   /* sincos2d halves ordered [w | h] (HF I-JEPA) instead of [h | w] */
   int sincos_uniform_power; /* sincos3d: three equal axis widths 2*ceil(D/6), cut to D */
   /* Test input, not part of the method: the synthetic q rows [0, D) and k rows [D, 2D) of every
-   * enc.blk.*.attn_qkv.weight are multiplied by these factors (1 = the plain recipe). Powers of
-   * two keep bf16 weights exact; larger q, k give peaked attention, so that a test encoder's
-   * output depends strongly on the scores (RoPE layout, mask). */
+   * enc.blk.*.attn_qkv.weight are multiplied by these factors (1 = the plain recipe), in float,
+   * and with bf16 weights rounded to bf16 again (round to nearest even), which is the value a bf16
+   * model holds when a file stores the scaled weight in f32. Larger q, k give peaked attention, so
+   * that a test encoder's output depends strongly on the scores (RoPE layout, mask). */
   double q_weight_scale, k_weight_scale;
 } oracle_hparams;
 

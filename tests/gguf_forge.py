@@ -123,7 +123,8 @@ def encoder_tensors(cfg, seed=0, matrix_type=GGML_BF16, fused=True, pos_table=No
         p = f"enc.blk.{l}."
         ts += [(p + "ln1.weight", P(p + "ln1.weight", (D,)), GGML_F32), (p + "ln1.bias", P(p + "ln1.bias", (D,)), GGML_F32)]
         wqkv, bqkv = P(p + "attn_qkv.weight", (3 * D, D)), P(p + "attn_qkv.bias", (3 * D,))
-        # the oracle's test input option: q and k rows scaled (powers of two: exact in bf16)
+        # the oracle's test input option: q and k rows scaled in float (a bf16 model rounds the
+        # file's f32 value to bf16 at load, as the oracle does)
         wqkv[:D] *= np.float32(getattr(cfg, "q_weight_scale", 1.0))
         wqkv[D:2 * D] *= np.float32(getattr(cfg, "k_weight_scale", 1.0))
         if fused:

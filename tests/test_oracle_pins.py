@@ -362,6 +362,12 @@ def test_attention_special_cases():
 
 
 # ---------------------------------------------------------------- whole encoder
+def bf16_round(a: np.ndarray) -> np.ndarray:
+    """float32 -> nearest bf16 (ties to even), as float32 (finite values)."""
+    bits = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    return (((bits + 0x7FFF + ((bits >> 16) & 1)) >> 16) << 16).astype(np.uint32).view(np.float32)
+
+
 def torch_encoder(cfg: Config, seed, bf16, pix):
     """Independent composition of library routines (conv3d, layer_norm, sdpa, F.gelu) with the
     RoPE written as the pages' expansion; weights drawn from the shared generator."""
@@ -408,8 +414,11 @@ def torch_encoder(cfg: Config, seed, bf16, pix):
         p = f"enc.blk.{l}."
         h = torch.nn.functional.layer_norm(x, (D,), prm(p + "ln1.weight", (D,)), prm(p + "ln1.bias", (D,)), cfg.ln_eps)
         wqkv = prm(p + "attn_qkv.weight", (3 * D, D))
-        wqkv[:D] *= cfg.q_weight_scale     # test input option: scaled q and k rows
-        wqkv[D:2 * D] *= cfg.k_weight_scale
+        if cfg.q_weight_scale != 1.0 or cfg.k_weight_scale != 1.0:   # test input option: scaled q, k rows
+            sc = np.ones((3 * D, 1), dtype=np.float32)
+            sc[:D], sc[D:2 * D] = cfg.q_weight_scale, cfg.k_weight_scale
+            w32 = (wqkv.numpy().astype(np.float32) * sc).astype(np.float32)
+            wqkv = torch.from_numpy((bf16_round(w32) if bf16 else w32).astype(np.float64))
         qkv = h @ wqkv.T + prm(p + "attn_qkv.bias", (3 * D,))
         q, k, v = (qkv[..., i * D:(i + 1) * D].reshape(B, N, NH, hd).transpose(1, 2) for i in range(3))
         if cfg.pos_type == 2:
@@ -434,7 +443,7 @@ ENC_CASES = {
                                         attn_mode=1), (3, 12, 8)),
     # peaked attention: the q / k rows of attn_qkv.weight scaled by 4 and 2 (a test input option)
     "levjepa_peaked": (tiny_video(embed_dim=128, n_head=2, ffn_dim=96, tubelet_size=1, cls_token=1, attn_mode=1,
-                                  q_weight_scale=4.0, k_weight_scale=2.0), (3, 12, 8)),
+                                  q_weight_scale=2.5, k_weight_scale=2.0), (3, 12, 8)),
 }
 
 
