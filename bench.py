@@ -83,15 +83,14 @@ HEADLINE = "vjepa2_vitl16_16x256"
 FLUSH_BYTES = 256 << 20  # > 129 MB of L2
 
 # Per-launch DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of a kernel class, from ncu
-# captures of the 2048-token clips at 8 per GPU; `sha1` is the hash of the class's source files when
-# the counters were taken (a changed kernel reports traffic null until it is captured again).
+# captures; `sha1` is the hash of the class's source files when the counters were taken (a changed
+# kernel reports traffic null until it is captured again). The 8-clip attention figure is a 4-clip
+# launch of the two-half encode (50.39 MB read + 0.29 MB written) times two: attention reads each
+# clip's q, k, v once, so its traffic grows with the clips.
 NCU_TRAFFIC = {  # (workload, kernel class, clips per GPU): bytes per launch, source hash at capture
-    (HEADLINE, "attention", 8): {"bytes_per_launch": 112.97e6, "sha1": "1b19c1524880125ffbc3c4cc1311b596f3d8cbfa"},
-    (HEADLINE, "layernorm", 8): {"bytes_per_launch": 69.09e6, "sha1": "a2ea4531106105c660f8d1b0a216f48845cb0f45"},
-    (HEADLINE, "gemm_qkv", 8): {"bytes_per_launch": 85.91e6, "sha1": "46959bf9d3e82d5d3ed1f392803cba2db5e0baca"},
-    (HEADLINE, "gemm_out", 8): {"bytes_per_launch": 103.05e6, "sha1": "46959bf9d3e82d5d3ed1f392803cba2db5e0baca"},
-    (HEADLINE, "gemm_up", 8): {"bytes_per_launch": 120.51e6, "sha1": "46959bf9d3e82d5d3ed1f392803cba2db5e0baca"},
-    (HEADLINE, "gemm_down", 8): {"bytes_per_launch": 215.07e6, "sha1": "46959bf9d3e82d5d3ed1f392803cba2db5e0baca"},
+    (HEADLINE, "attention", 8): {"bytes_per_launch": 2 * 50.682368e6, "sha1": "37bf648cbb1a95c30d1d700e58d969a6f012719f"},
+    ("levjepa_vitl16_16x256", "attention", 2): {"bytes_per_launch": 51.048448e6,
+                                                "sha1": "37bf648cbb1a95c30d1d700e58d969a6f012719f"},
 }
 
 
