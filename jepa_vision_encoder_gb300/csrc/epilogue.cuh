@@ -314,9 +314,10 @@ struct EpiStage {
     }
     ++n;
   }
-  // Every store of this warp complete (before the kernel exits).
+  // Every store of this warp done reading shared memory (before the CTA exits; the global writes
+  // complete with the grid, before any dependent grid passes its wait).
   __device__ __forceinline__ void finish(int lane) {
-    if (lane == 0) bulk_wait_all();
+    if (lane == 0) bulk_wait_read<0>();
     __syncwarp();
   }
 };

@@ -94,28 +94,41 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
   const WaitCtl wc{abort_flag, err, limit_ns};
   pdl_trigger();
-  pdl_wait();  // A and the residual stream come from earlier kernels
 
   if (warp == 0) {
     if (lane == 0) {
       const uint64_t a_policy = l2_policy_evict_first(), b_policy = l2_policy_evict_last();
-      int stage = 0;
+      // The weights are written by no kernel of the sequence: the first tile's first S stages of
+      // B are requested (and their stages armed) before waiting for the previous kernel, whose
+      // tail this CTA may overlap; A and the residual stream come from earlier kernels.
+      // The loop's first S waits for a free stage pass at once (fresh barriers), so every stage
+      // armed here also gets its A copy.
+      const int pre = blockIdx.x < num_tiles ? (num_k < S ? num_k : S) : 0;
       uint32_t phase = 0, armed = 0, armed_phase = 0;
+      for (int kb = 0; kb < pre; ++kb) {
+        const uint32_t fb = smem_u32(full + kb);
+        mbar_arrive_expect_tx(fb, C::kStageBytes);
+        tma_load_2d_hint(smem_u32(sB + kb * C::kBBytes), &tmB, fb, kb * kBK, (blockIdx.x % num_n) * BN, b_policy);
+        armed |= 1u << kb;
+      }
+      pdl_wait();
+      int stage = 0, it = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
         const int m0 = (tile / num_n) * kBM, n0 = (tile % num_n) * BN;
-        for (int kb = 0; kb < num_k; ++kb) {
+        for (int kb = 0; kb < num_k; ++kb, ++it) {
           if (!mbar_wait(smem_u32(empty + stage), phase ^ 1u, wc)) {
             ok = false;
             break;
           }
           const uint32_t fb = smem_u32(full + stage);
-          mbar_arrive_expect_tx(fb, C::kStageBytes);
+          if (it >= pre) mbar_arrive_expect_tx(fb, C::kStageBytes);
           if (EK == kEpiResidual)  // A (attention output, FFN hidden) is read once: let it go first
             tma_load_2d_hint(smem_u32(sA + stage * C::kABytes), &tmA, fb, kb * kBK, m0, a_policy);
           else
             tma_load_2d(smem_u32(sA + stage * C::kABytes), &tmA, fb, kb * kBK, m0);
-          tma_load_2d_hint(smem_u32(sB + stage * C::kBBytes), &tmB, fb, kb * kBK, n0, b_policy);  // weights: every M tile
+          if (it >= pre)  // weights: every M tile reads them, keep them in L2
+            tma_load_2d_hint(smem_u32(sB + stage * C::kBBytes), &tmB, fb, kb * kBK, n0, b_policy);
           armed |= 1u << stage;
           armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
           if (++stage == S) {
@@ -128,6 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (armed & (1u << s)) mbar_drain(smem_u32(full + s), (armed_phase >> s) & 1u, limit_ns, err);
     }
   } else if (warp == 1) {
+    pdl_wait();
     // the whole warp runs the issue loop (waits and descriptor arithmetic warp-uniform); one
     // elected lane issues each MMA and commit
     constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN, 0, 0);
@@ -166,6 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mma_commit_warp(smem_u32(mma_done));
     mbar_drain(smem_u32(mma_done), 0, limit_ns, err);
   } else {
+    pdl_wait();  // the epilogue writes (or adds into) buffers that earlier kernels use
     const int q = warp & 3;                        // TMEM lane quarter this warp may access
     constexpr int kChunks = BN / 32 / 2;           // 32-column chunks per warp (half the tile)
     const int half = (warp - 2) >> 2;              // which of the two warps on this lane quarter

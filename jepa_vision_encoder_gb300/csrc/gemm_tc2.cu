@@ -101,7 +101,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
   const WaitCtl wc{abort_flag, err, limit_ns};
   pdl_trigger();
-  pdl_wait();  // A and the residual stream come from earlier kernels
 
   if (warp == 0) {
     if (lane == 0) {
@@ -109,23 +108,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // which the even CTA arms with the bytes of both halves (tx-count may run ahead of the
       // arm within a phase: the phase cannot complete before the even CTA's arrive).
       const uint64_t a_policy = l2_policy_evict_first(), b_policy = l2_policy_evict_last();
-      int stage = 0;
+      // The weights are written by no kernel of the sequence: the first tile's first stages of
+      // B are requested (and, on the even CTA, armed) before waiting for the previous kernel,
+      // whose tail this CTA may overlap; A and the residual stream come from earlier kernels.
+      // The loop's first kStages waits for a free stage pass at once (fresh barriers), so every
+      // stage armed here also gets its A copies.
+      const int pre = pair < num_tiles ? (num_k < kStages ? num_k : kStages) : 0;
       uint32_t phase = 0, armed = 0, armed_phase = 0;
+      for (int kb = 0; kb < pre; ++kb) {
+        const uint32_t fb_even = mapa_shared(smem_u32(full + kb), 0);
+        if (rank == 0) mbar_arrive_expect_tx(smem_u32(full + kb), 2 * C::kStageBytes);
+        tma_load_2d_pair_hint(smem_u32(sB + kb * C::kBBytes), &tmB, fb_even, kb * kBK,
+                              (pair % num_n) * kTileN + (int)rank * C::kBRows, b_policy);
+        armed |= 1u << kb;
+      }
+      pdl_wait();
+      int stage = 0, it = 0;
       bool ok = true;
       for (int tile = pair; tile < num_tiles && ok; tile += num_pairs) {
         const int m0 = (tile / num_n) * kTileM + (int)rank * 128, n0 = (tile % num_n) * kTileN + (int)rank * C::kBRows;
-        for (int kb = 0; kb < num_k; ++kb) {
+        for (int kb = 0; kb < num_k; ++kb, ++it) {
           if (!mbar_wait(smem_u32(empty + stage), phase ^ 1u, wc)) {
             ok = false;
             break;
           }
           const uint32_t fb_even = mapa_shared(smem_u32(full + stage), 0);
-          if (rank == 0) mbar_arrive_expect_tx(smem_u32(full + stage), 2 * C::kStageBytes);
+          if (rank == 0 && it >= pre) mbar_arrive_expect_tx(smem_u32(full + stage), 2 * C::kStageBytes);
           if (EK == kEpiResidual)  // A (attention output, FFN hidden) is read once: let it go first
             tma_load_2d_pair_hint(smem_u32(sA + stage * C::kABytes), &tmA, fb_even, kb * kBK, m0, a_policy);
           else
             tma_load_2d_pair(smem_u32(sA + stage * C::kABytes), &tmA, fb_even, kb * kBK, m0);
-          tma_load_2d_pair_hint(smem_u32(sB + stage * C::kBBytes), &tmB, fb_even, kb * kBK, n0, b_policy);  // weights: every M tile
+          if (it >= pre)  // weights: every M tile reads them, keep them in L2
+            tma_load_2d_pair_hint(smem_u32(sB + stage * C::kBBytes), &tmB, fb_even, kb * kBK, n0, b_policy);
           armed |= 1u << stage;
           armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
           if (++stage == kStages) {
@@ -140,6 +154,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (armed & (1u << s)) mbar_drain(smem_u32(full + s), (armed_phase >> s) & 1u, limit_ns, err);
     }
   } else if (warp == 1) {
+    pdl_wait();
     if (rank == 0) {
       // even CTA: the MMA issuer of the pair. The whole warp runs the issue loop (waits and
       // descriptor arithmetic warp-uniform); one elected lane issues each MMA and commit.
@@ -180,6 +195,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_drain(smem_u32(mma_done), 0, limit_ns, err);
     }
   } else {
+    pdl_wait();  // the epilogue writes (or adds into) buffers that earlier kernels use
     const int q = warp & 3;                    // TMEM lane quarter this warp may access
     constexpr int kChunks = kTileN / 32 / 2;   // 32-column chunks per warp (half the columns)
     const int half = (warp - 2) >> 2;  // which of the two warps on this lane quarter
