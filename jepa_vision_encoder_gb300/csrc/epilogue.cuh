@@ -245,18 +245,16 @@ __device__ __forceinline__ void epi_fragment(const EpiArgs& a, int m, int n0, fl
 // The tcgen05 GEMMs take the epilogue kind as a template argument (EK) so each kernel holds only
 // its own arithmetic. epi_math_tc applies the bias and then GELU or 3-D RoPE to 32 consecutive
 // columns n0.. of row m; the caller stages the result in shared memory and stores it with TMA.
+// The bias of a warp's 32-column chunk is held one value per lane (lane e: column n0 + e), loaded
+// while the tile's main loop still runs (epi_bias_lanes), and handed to every row by shuffles.
 template <int EK>
-__device__ __forceinline__ void epi_math_tc(const EpiArgs& a, int m, int n0, float (&v)[32]) {
-  const float4* b4 = reinterpret_cast<const float4*>(a.bias + n0);  // n0 is warp-uniform: broadcast
+__device__ __forceinline__ void epi_math_tc(const EpiArgs& a, int m, int n0, float (&v)[32], float blane) {
 #pragma unroll
-  for (int e = 0; e < 32; e += 4) {
-    const float4 b = __ldg(b4 + e / 4);
-    const float2 lo = __fadd2_rn(make_float2(v[e], v[e + 1]), make_float2(b.x, b.y));
-    const float2 hi = __fadd2_rn(make_float2(v[e + 2], v[e + 3]), make_float2(b.z, b.w));
-    v[e] = lo.x;
-    v[e + 1] = lo.y;
-    v[e + 2] = hi.x;
-    v[e + 3] = hi.y;
+  for (int e = 0; e < 32; e += 2) {
+    const float2 b = make_float2(__shfl_sync(0xffffffffu, blane, e), __shfl_sync(0xffffffffu, blane, e + 1));
+    const float2 r = __fadd2_rn(make_float2(v[e], v[e + 1]), b);
+    v[e] = r.x;
+    v[e + 1] = r.y;
   }
   if constexpr (EK == kEpiGelu) {
 #pragma unroll
@@ -326,12 +324,12 @@ struct EpiStage {
 // math, then staged store (bf16: one piece) or staged fp32 add into the residual stream (two).
 template <int EK>
 __device__ __forceinline__ void epi_chunk_tc(const EpiArgs& a, const CUtensorMap* tm_out, EpiStage& st, int lane,
-                                             int y0, int n0, float (&v)[32]) {
+                                             int y0, int n0, float (&v)[32], float blane) {
   if constexpr (EK == kEpiPatch) {
     if (a.prefix == 0 && a.rows_per_item == a.patches_per_item) {
       // output rows are the patch rows (no CLS): bias (+ position row) (+ modality vector), then
       // the same staged TMA store as the other epilogues, in fp32
-      epi_math_tc<EK>(a, y0 + lane, n0, v);
+      epi_math_tc<EK>(a, y0 + lane, n0, v, blane);
       if (a.pos != nullptr) {  // row i of the item's table (a fixed table: patch rows only)
         const float4* p4 =
             reinterpret_cast<const float4*>(a.pos + (size_t)((y0 + lane) % a.patches_per_item) * a.N + n0);
@@ -366,7 +364,7 @@ __device__ __forceinline__ void epi_chunk_tc(const EpiArgs& a, const CUtensorMap
       epi_fragment<32, false>(a, y0 + lane, n0, v);  // rows remapped per item: stores from registers
     }
   } else {
-    epi_math_tc<EK>(a, y0 + lane, n0, v);
+    epi_math_tc<EK>(a, y0 + lane, n0, v, blane);
     if constexpr (EK == kEpiResidual) {
       uint32_t w[16];
 #pragma unroll
@@ -408,7 +406,7 @@ __device__ __forceinline__ void rope_hd64_regs(float (&v)[32], const float2 (&cs
 // chunk rotates from registers.
 template <int J0, int NCHUNK>
 __device__ __forceinline__ void epi_warp_qkv_hd64(const EpiArgs& a, const CUtensorMap* tm, EpiStage& st, int lane,
-                                                  uint32_t trow, int y0, int n_tile0) {
+                                                  uint32_t trow, int y0, int n_tile0, const float (&bl)[NCHUNK]) {
   constexpr int kA0 = J0 == 0 ? 0 : 1;  // axes touched by this half: t, h (J0 = 0) or h, w (J0 = 32)
   const int p = (y0 + lane) % a.rows_per_item;
   const bool rot = (a.rope != nullptr || a.rope_axes != nullptr) && p >= a.prefix;
@@ -437,7 +435,7 @@ __device__ __forceinline__ void epi_warp_qkv_hd64(const EpiArgs& a, const CUtens
 #pragma unroll
     for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[i & 1][e]);
     const int n0 = n_tile0 + c * 32;
-    epi_math_tc<kEpiBias>(a, y0 + lane, n0, v);
+    epi_math_tc<kEpiBias>(a, y0 + lane, n0, v, bl[i]);
     if (n0 < qk_cols) {  // q and k columns rotate (warp-uniform); v columns pass
       if (a.rope_layout == 0)
         rope_hd64_regs<J0, 0>(v, cs);
@@ -472,7 +470,8 @@ __device__ __forceinline__ void rope_hd32_regs(float (&v)[32], const float2 (&cs
 // (cos, sin) values are loaded once per tile and each q / k chunk rotates from registers.
 template <int NCHUNK>
 __device__ __forceinline__ void epi_warp_qkv_hd32(const EpiArgs& a, const CUtensorMap* tm, EpiStage& st, int lane,
-                                                  uint32_t trow, int y0, int n_tile0, int half) {
+                                                  uint32_t trow, int y0, int n_tile0, int half,
+                                                  const float (&bl)[NCHUNK]) {
   const int m = y0 + lane;
   const int p = m % a.rows_per_item;
   const bool rot = (a.rope != nullptr || a.rope_axes != nullptr) && p >= a.prefix;
@@ -501,7 +500,7 @@ __device__ __forceinline__ void epi_warp_qkv_hd32(const EpiArgs& a, const CUtens
 #pragma unroll
     for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[i & 1][e]);
     const int n0 = n_tile0 + (c0 + i) * 32;
-    epi_math_tc<kEpiBias>(a, m, n0, v);
+    epi_math_tc<kEpiBias>(a, m, n0, v, bl[i]);
     if (n0 < qk_cols) {  // q and k heads rotate (warp-uniform); v heads pass
       if (a.rope_layout == 0)
         rope_hd32_regs<0>(v, cs);
@@ -515,22 +514,38 @@ __device__ __forceinline__ void epi_warp_qkv_hd32(const EpiArgs& a, const CUtens
   }
 }
 
+// Column of chunk i of a warp's share of a tile: QKV with width-64 heads takes every other 32-column
+// chunk (the head half `half`), the other kinds the warp's contiguous half of the tile.
+template <int EK, int NCHUNK>
+__device__ __forceinline__ int epi_chunk_col(const EpiArgs& a, int i, int half) {
+  return (EK == kEpiQkvRope && a.head_dim == 64) ? (2 * i + half) * 32 : (half * NCHUNK + i) * 32;
+}
+
+// The bias of the warp's chunks of the tile at column n_tile0, one value per lane per chunk,
+// requested before the accumulator is ready so that no chunk waits on a load from L2.
+template <int EK, int NCHUNK>
+__device__ __forceinline__ void epi_bias_lanes(const EpiArgs& a, int lane, int n_tile0, int half, float (&bl)[NCHUNK]) {
+#pragma unroll
+  for (int i = 0; i < NCHUNK; ++i) bl[i] = __ldg(a.bias + n_tile0 + epi_chunk_col<EK, NCHUNK>(a, i, half) + lane);
+}
+
 // The epilogue of one warp for one accumulator tile: NCHUNK 32-column chunks of its 32 TMEM lanes
 // (rows y0 .. y0+31), the next tcgen05.ld in flight while a chunk is processed. half selects which
-// chunks: 0 or 1 of the warp pair sharing the lane quarter.
+// chunks: 0 or 1 of the warp pair sharing the lane quarter; bl = epi_bias_lanes of the tile.
 template <int EK, int NCHUNK>
 __device__ __forceinline__ void epi_warp_tile(const EpiArgs& a, const CUtensorMap* tm, EpiStage& st, int lane,
-                                              uint32_t trow, int y0, int n_tile0, int half) {
+                                              uint32_t trow, int y0, int n_tile0, int half,
+                                              const float (&bl)[NCHUNK]) {
   if constexpr (EK == kEpiQkvRope) {
     if (a.head_dim == 64) {  // heads never straddle a 64-column boundary: chunk parity = head half
       if (half == 0)
-        epi_warp_qkv_hd64<0, NCHUNK>(a, tm, st, lane, trow, y0, n_tile0);
+        epi_warp_qkv_hd64<0, NCHUNK>(a, tm, st, lane, trow, y0, n_tile0, bl);
       else
-        epi_warp_qkv_hd64<32, NCHUNK>(a, tm, st, lane, trow, y0, n_tile0);
+        epi_warp_qkv_hd64<32, NCHUNK>(a, tm, st, lane, trow, y0, n_tile0, bl);
       return;
     }
     if (a.head_dim == 32) {
-      epi_warp_qkv_hd32<NCHUNK>(a, tm, st, lane, trow, y0, n_tile0, half);
+      epi_warp_qkv_hd32<NCHUNK>(a, tm, st, lane, trow, y0, n_tile0, half, bl);
       return;
     }
   }
@@ -544,7 +559,7 @@ __device__ __forceinline__ void epi_warp_tile(const EpiArgs& a, const CUtensorMa
     float v[32];
 #pragma unroll
     for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[i & 1][e]);
-    epi_chunk_tc<EK>(a, tm, st, lane, y0, n_tile0 + (c0 + i) * 32, v);
+    epi_chunk_tc<EK>(a, tm, st, lane, y0, n_tile0 + (c0 + i) * 32, v, bl[i]);
   }
 }
 
