@@ -402,27 +402,23 @@ __device__ __forceinline__ void rope_hd64_regs(float (&v)[32], const float2 (&cs
 }
 
 // QKV epilogue of a warp whose chunks are all head halves J0 (chunks 2i + J0/32 of the tile): the
-// row's (cos, sin) values for the two axes those dims use are loaded once per tile, then every
-// chunk rotates from registers.
+// row's (cos, sin) values for the two axes those dims use come from epi_prepare (loaded once per
+// tile, before the accumulator is ready), and every chunk rotates from registers.
+template <int EK, int NCHUNK>
+struct EpiPre;
+
 template <int J0, int NCHUNK>
 __device__ __forceinline__ void epi_warp_qkv_hd64(const EpiArgs& a, const CUtensorMap* tm, EpiStage& st, int lane,
-                                                  uint32_t trow, int y0, int n_tile0, const float (&bl)[NCHUNK]) {
+                                                  uint32_t trow, int y0, int n_tile0,
+                                                  const EpiPre<kEpiQkvRope, NCHUNK>& pre) {
   constexpr int kA0 = J0 == 0 ? 0 : 1;  // axes touched by this half: t, h (J0 = 0) or h, w (J0 = 32)
-  const int p = (y0 + lane) % a.rows_per_item;
-  const bool rot = (a.rope != nullptr || a.rope_axes != nullptr) && p >= a.prefix;
   float2 cs[3][10];
 #pragma unroll
   for (int ax = 0; ax < 3; ++ax)
 #pragma unroll
-    for (int k = 0; k < 10; ++k) cs[ax][k] = make_float2(1.0f, 0.0f);
-  if (rot) {
-    const float2* rows[3];
-    rope_axis_rows(a, y0 + lane, p, 10, rows);
-#pragma unroll
-    for (int ax = kA0; ax < kA0 + 2; ++ax)
-#pragma unroll
-      for (int k = 0; k < 10; ++k) cs[ax][k] = __ldg(rows[ax] + k);
-  }
+    for (int k = 0; k < 10; ++k)
+      cs[ax][k] = (ax == kA0 || ax == kA0 + 1) ? pre.cs[ax == kA0 ? 0 : 1][k] : make_float2(1.0f, 0.0f);
+  const float (&bl)[NCHUNK] = pre.bl;
   const int qk_cols = 2 * a.n_head * 64;
   uint32_t r[2][32];
   tmem_ld32(trow + (J0 / 32) * 32, r[0]);
@@ -529,19 +525,53 @@ __device__ __forceinline__ void epi_bias_lanes(const EpiArgs& a, int lane, int n
   for (int i = 0; i < NCHUNK; ++i) bl[i] = __ldg(a.bias + n_tile0 + epi_chunk_col<EK, NCHUNK>(a, i, half) + lane);
 }
 
+// What a warp's epilogue of one tile reads besides the accumulator, requested while the tile's
+// main loop runs so that no chunk waits on L2: the bias (one value per lane per chunk) and, for QKV
+// with width-64 heads, the row's (cos, sin) values of the two axes its head half rotates.
+template <int EK, int NCHUNK>
+struct EpiPre {
+  float bl[NCHUNK];
+  float2 cs[2][10];
+};
+
+template <int EK, int NCHUNK>
+__device__ __forceinline__ void epi_prepare(const EpiArgs& a, int lane, int y0, int n_tile0, int half,
+                                            EpiPre<EK, NCHUNK>& pre) {
+  epi_bias_lanes<EK, NCHUNK>(a, lane, n_tile0, half, pre.bl);
+  if constexpr (EK == kEpiQkvRope) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int k = 0; k < 10; ++k) pre.cs[j][k] = make_float2(1.0f, 0.0f);
+    const int m = y0 + lane, p = m % a.rows_per_item;
+    if (a.head_dim == 64 && (a.rope != nullptr || a.rope_axes != nullptr) && p >= a.prefix) {
+      const float2* rows[3];
+      rope_axis_rows(a, m, p, 10, rows);
+      const float2* r0 = half ? rows[1] : rows[0];  // axes t, h (half 0) or h, w (half 1)
+      const float2* r1 = half ? rows[2] : rows[1];
+#pragma unroll
+      for (int k = 0; k < 10; ++k) {
+        pre.cs[0][k] = __ldg(r0 + k);
+        pre.cs[1][k] = __ldg(r1 + k);
+      }
+    }
+  }
+}
+
 // The epilogue of one warp for one accumulator tile: NCHUNK 32-column chunks of its 32 TMEM lanes
 // (rows y0 .. y0+31), the next tcgen05.ld in flight while a chunk is processed. half selects which
-// chunks: 0 or 1 of the warp pair sharing the lane quarter; bl = epi_bias_lanes of the tile.
+// chunks: 0 or 1 of the warp pair sharing the lane quarter; pre = epi_prepare of the tile.
 template <int EK, int NCHUNK>
 __device__ __forceinline__ void epi_warp_tile(const EpiArgs& a, const CUtensorMap* tm, EpiStage& st, int lane,
                                               uint32_t trow, int y0, int n_tile0, int half,
-                                              const float (&bl)[NCHUNK]) {
+                                              const EpiPre<EK, NCHUNK>& pre) {
+  const float (&bl)[NCHUNK] = pre.bl;
   if constexpr (EK == kEpiQkvRope) {
     if (a.head_dim == 64) {  // heads never straddle a 64-column boundary: chunk parity = head half
       if (half == 0)
-        epi_warp_qkv_hd64<0, NCHUNK>(a, tm, st, lane, trow, y0, n_tile0, bl);
+        epi_warp_qkv_hd64<0, NCHUNK>(a, tm, st, lane, trow, y0, n_tile0, pre);
       else
-        epi_warp_qkv_hd64<32, NCHUNK>(a, tm, st, lane, trow, y0, n_tile0, bl);
+        epi_warp_qkv_hd64<32, NCHUNK>(a, tm, st, lane, trow, y0, n_tile0, pre);
       return;
     }
     if (a.head_dim == 32) {

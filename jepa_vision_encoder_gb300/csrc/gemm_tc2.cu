@@ -205,13 +205,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     for (int tile = pair; tile < num_tiles; tile += num_pairs) {
       const int m0 = (tile / num_n) * kTileM + (int)rank * 128, n0 = (tile % num_n) * kTileN;
-      float bl[kChunks];  // this warp's bias, requested while the main loop runs
-      epi_bias_lanes<EK, kChunks>(epi, lane, n0, half, bl);
+      EpiPre<EK, kChunks> pre;  // requested while the main loop runs
+      epi_prepare<EK, kChunks>(epi, lane, m0 + q * 32, n0, half, pre);
       if (!mbar_wait(smem_u32(tfull + acc), acc_phase, wc)) break;
       tc_fence_after();
       const int y0 = m0 + q * 32;
       const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kTileN);
-      epi_warp_tile<EK, kChunks>(epi, &tmO, stage, lane, trow, y0, n0, half, bl);
+      epi_warp_tile<EK, kChunks>(epi, &tmO, stage, lane, trow, y0, n0, half, pre);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(tempty_even + (uint32_t)(acc * sizeof(uint64_t)));
