@@ -318,7 +318,8 @@ jepa_status jepa_op_pos_resize(const float* d_src, int32_t st, int32_t sh, int32
 
 /* Softmax attention per (item, head): o = softmax(q k^T / sqrt(head_dim) + mask) v.
  * d_qkv: [B*N, 3*n_head*head_dim] ([q | k | v] columns, heads contiguous), d_out: [B*N, n_head*head_dim];
- * fp32 (dtype JEPA_FP32) or bf16 (JEPA_BF16: tcgen05 flash kernel); head_dim 64.
+ * fp32 (dtype JEPA_FP32) or bf16 (JEPA_BF16: tcgen05 flash kernel); head_dim 64; d_qkv (and in fp32
+ * d_out) 16-byte aligned, else JEPA_E_INVALID_ARG.
  * bf16 also takes head_dim 32 (the masked predictor's heads; 64-byte tiles, scale 1/sqrt(32)).
  * attn_mode JEPA_ATTN_BLOCK_CAUSAL: the first `prefix` rows see every key, prefix columns are
  * closed to the other rows, and patch key j is visible to patch query i iff

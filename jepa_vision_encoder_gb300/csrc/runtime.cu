@@ -1581,6 +1581,8 @@ extern "C" jepa_status jepa_op_attention(int32_t dtype, const void* d_qkv, int32
   p.qkv = d_qkv;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (dtype == JEPA_FP32) {
+    if ((reinterpret_cast<uintptr_t>(d_qkv) | reinterpret_cast<uintptr_t>(d_out)) & 15)
+      return fail(JEPA_E_INVALID_ARG, "fp32 attention: qkv and out must be 16-byte aligned");
     CUDA_TRY(attention_simt_launch(reinterpret_cast<const float*>(d_qkv), p, s));
     return JEPA_OK;
   }

@@ -1,4 +1,4 @@
-// simt.cu -- the fp32 path: a tiled FFMA GEMM with the shared epilogues and an fp32 flash
+// simt.cu -- the fp32 path: a split-K tiled FFMA GEMM with the shared epilogues and an fp32 flash
 // attention (online softmax). Used when the model is loaded in fp32 (the hfvit Ti/14 image
 // encoder workload), where every operation keeps fp32 precision end to end.
 #include <cuda_bf16.h>
@@ -10,120 +10,214 @@ namespace jepa {
 
 namespace {
 
-// C[M,N] = A[M,K] B[N,K]^T. 64x64 tile, BK 16, 256 threads, a 4x4 micro-tile per thread
-// (4 consecutive columns, so RoPE pairs stay inside one thread's fragment).
-constexpr int kTM = 64, kTN = 64, kTK = 16;
+// C[M,N] = A[M,K] B[N,K]^T for the small fp32 shapes (one image of 257 tokens: every GEMM has a
+// few dozen 32 x 32 output tiles). A CTA of 8 warps computes one 32 x 32 tile; each warp takes
+// one eighth of the K steps (so a CTA's dependent chain of global loads is K / 8 long), stages
+// its 32 x 16 slices of A and B in its own shared memory with the next step's loads in flight, and
+// accumulates a 4 x 8 micro-tile per lane; the eight partial tiles are then summed in a fixed
+// order (the same order for every batch size) and passed to the epilogue four columns at a time.
+constexpr int kTM = 32, kTN = 32, kTK = 16, kKS = 8, kLd = 36;  // kLd: padded row (16-byte aligned)
 
 __global__ void __launch_bounds__(256) gemm_simt_kernel(const float* __restrict__ A, const float* __restrict__ Bw,
                                                         EpiArgs epi, int M, int N, int K) {
-  __shared__ float As[kTK][kTM + 4];
-  __shared__ float Bs[kTK][kTN + 4];
+  __shared__ __align__(16) float sm[kKS * 2 * kTK * kLd];  // per warp A and B slices; then the partial tiles
+  static_assert(kKS * 2 * kTK * kLd >= kKS * kTM * kTN, "partial tiles fit the staging area");
   pdl_trigger();
   pdl_wait();
-  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.y * kTM, n0 = blockIdx.x * kTN;
-  float acc[4][4] = {};
-  for (int k0 = 0; k0 < K; k0 += kTK) {
-    // 64 rows x 16 k of A and of B: 1024 floats each, 4 per thread
+  float* As = sm + warp * 2 * kTK * kLd;  // [kTK][kLd]: As[kk][row]
+  float* Bs = As + kTK * kLd;             // [kTK][kLd]: Bs[kk][col]
+  const int steps = (K + kTK - 1) / kTK, per = (steps + kKS - 1) / kKS;
+  const int s_begin = warp * per, s_end = min(steps, s_begin + per);
+  const int r0 = (lane >> 2) * 4, c0 = (lane & 3) * 8;  // this lane's 4 x 8 outputs
+  float acc[4][8] = {};
+  float ra[16], rb[16];  // one step of A and B (32 x 16 each), 16 values per lane
+  auto load = [&](int st) {
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      const int idx = threadIdx.x + t * 256;
-      const int row = idx / kTK, kk = idx % kTK;
-      const int gm = m0 + row, gn = n0 + row, gk = k0 + kk;
-      As[kk][row] = (gm < M && gk < K) ? A[(size_t)gm * K + gk] : 0.0f;
-      Bs[kk][row] = (gn < N && gk < K) ? Bw[(size_t)gn * K + gk] : 0.0f;
+    for (int t = 0; t < 16; ++t) {
+      const int idx = lane + 32 * t, row = idx / kTK, kk = idx % kTK, gk = st * kTK + kk;
+      ra[t] = (m0 + row < M && gk < K) ? __ldg(A + (size_t)(m0 + row) * K + gk) : 0.0f;
+      rb[t] = (n0 + row < N && gk < K) ? __ldg(Bw + (size_t)(n0 + row) * K + gk) : 0.0f;
     }
-    __syncthreads();
+  };
+  if (s_begin < s_end) load(s_begin);
+  for (int st = s_begin; st < s_end; ++st) {
+    __syncwarp();  // the previous step's shared-memory reads are done
+#pragma unroll
+    for (int t = 0; t < 16; ++t) {
+      const int idx = lane + 32 * t, row = idx / kTK, kk = idx % kTK;
+      As[kk * kLd + row] = ra[t];
+      Bs[kk * kLd + row] = rb[t];
+    }
+    __syncwarp();
+    if (st + 1 < s_end) load(st + 1);  // in flight during this step's FMAs
 #pragma unroll
     for (int kk = 0; kk < kTK; ++kk) {
-      float a[4], b[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx * 4 + j];
+      const float4 a4 = *reinterpret_cast<const float4*>(As + kk * kLd + r0);
+      const float4 b0 = *reinterpret_cast<const float4*>(Bs + kk * kLd + c0);
+      const float4 b1 = *reinterpret_cast<const float4*>(Bs + kk * kLd + c0 + 4);
+      const float a[4] = {a4.x, a4.y, a4.z, a4.w};
+      const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
     }
-    __syncthreads();
   }
+  __syncthreads();  // every warp is done with its staging area
+  float* red = sm;  // [kKS][kTM * kTN]
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int m = m0 + ty * 4 + i;
-    const int n = n0 + tx * 4;
-    if (m < M && n < N) epi_fragment<4, false>(epi, m, n, acc[i]);
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; j += 4)
+      *reinterpret_cast<float4*>(red + warp * kTM * kTN + (r0 + i) * kTN + c0 + j) =
+          make_float4(acc[i][j], acc[i][j + 1], acc[i][j + 2], acc[i][j + 3]);
+  __syncthreads();
+  const int o = threadIdx.x * 4, row = o / kTN, col = o % kTN;
+  float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+  for (int w = 0; w < kKS; ++w) {
+    const float4 x = *reinterpret_cast<const float4*>(red + w * kTM * kTN + o);
+    v[0] += x.x;
+    v[1] += x.y;
+    v[2] += x.z;
+    v[3] += x.w;
   }
+  const int m = m0 + row, n = n0 + col;
+  if (m < M && n < N) epi_fragment<4, false>(epi, m, n, v);
 }
 
-// fp32 attention: one thread per query row, K/V tiles of 64 keys staged in shared memory.
-constexpr int kSQ = 128, kSK = 64, kSHD = 64;
+// fp32 attention ("Architecture", attention): a CTA per (8 query rows, head, item), 8 threads per
+// query row, the row's scaled q in registers. Keys come in chunks of 32 staged in shared memory
+// (the next chunk's loads in flight while one is scored); thread `sub` of a row scores keys sub,
+// sub + 8, sub + 16 and sub + 24 of the chunk (64-wide dot products, conflict-free 16-byte reads),
+// the row's 8 threads combine the chunk maximum and sum by shuffles (online softmax: earlier sums
+// and outputs rescaled when the maximum moves), and each accumulates 8 of the row's 64 output
+// columns over the chunk's keys.
+constexpr int kSQ = 8, kSK = 32, kSHD = 64, kKLd = kSHD + 4;
+constexpr int kAThreads = kSQ * 8, kALoads = kSK * (kSHD / 4) / kAThreads;  // float4 of K (and of V) per thread
 
-__global__ void __launch_bounds__(kSQ) attn_simt_kernel(const float* __restrict__ qkv, AttnParams p) {
-  __shared__ float Ks[kSK][kSHD];
-  __shared__ float Vs[kSK][kSHD];
+__global__ void __launch_bounds__(kAThreads) attn_simt_kernel(const float* __restrict__ qkv, AttnParams p) {
+  __shared__ __align__(16) float Ks[kSK][kKLd];
+  __shared__ __align__(16) float Vs[kSK][kSHD];
+  __shared__ float Ps[kSQ][kSK + 1];
   pdl_trigger();
   pdl_wait();
   const int h = blockIdx.y, b = blockIdx.z;
   const int D = p.H * kSHD, ld = 3 * D;
-  const int q = blockIdx.x * kSQ + threadIdx.x;
-  const bool valid = q < p.N;
-  float qv[kSHD], o[kSHD];
-  const float* qrow = qkv + ((size_t)b * p.N + (valid ? q : 0)) * ld + h * kSHD;
+  const int q0 = blockIdx.x * kSQ;
+  const int r = threadIdx.x >> 3, sub = threadIdx.x & 7;  // query row of the CTA, its eighth
+  const int q = q0 + r;
+  const float* base = qkv + (size_t)b * p.N * ld + h * kSHD;
+  float qv[kSHD];
+  {
+    const float4* qr = reinterpret_cast<const float4*>(base + (size_t)(q < p.N ? q : 0) * ld);
 #pragma unroll
-  for (int c = 0; c < kSHD; ++c) {
-    qv[c] = qrow[c] * 0.125f;  // 1/sqrt(64), exact
-    o[c] = 0.0f;
+    for (int c = 0; c < kSHD; c += 4) {
+      const float4 x = __ldg(qr + c / 4);
+      qv[c] = x.x * 0.125f;  // 1/sqrt(64), exact
+      qv[c + 1] = x.y * 0.125f;
+      qv[c + 2] = x.z * 0.125f;
+      qv[c + 3] = x.w * 0.125f;
+    }
   }
-  int lo = 0, hi = p.N;
+  int lo = 0, hi = p.N;  // visible keys of this row
   if (p.attn_mode == 1 && q >= p.prefix) {
     lo = p.prefix;
     hi = min(p.N, p.prefix + ((q - p.prefix) / p.frame_tokens + 1) * p.frame_tokens);
   }
-  // keys the whole block needs
-  int kv_end = p.N;
-  const int q0 = blockIdx.x * kSQ;
+  int kv_end = p.N;  // keys any row of the CTA sees
   if (p.attn_mode == 1 && q0 >= p.prefix) {
     const int q_last = min(q0 + kSQ - 1, p.N - 1);
     kv_end = min(p.N, p.prefix + ((q_last - p.prefix) / p.frame_tokens + 1) * p.frame_tokens);
   }
-  float m = -INFINITY, l = 0.0f;
-  for (int k0 = 0; k0 < kv_end; k0 += kSK) {
-    for (int idx = threadIdx.x; idx < kSK * kSHD; idx += kSQ) {
-      const int kr = idx / kSHD, c = idx % kSHD;
-      const int key = k0 + kr;
-      const float* base = qkv + ((size_t)b * p.N + (key < p.N ? key : 0)) * ld + h * kSHD + c;
-      Ks[kr][c] = key < p.N ? base[D] : 0.0f;
-      Vs[kr][c] = key < p.N ? base[2 * D] : 0.0f;
-    }
-    __syncthreads();
-    const int kn = min(kSK, kv_end - k0);
-    for (int kr = 0; kr < kn; ++kr) {
-      const int key = k0 + kr;
-      if (key < lo || key >= hi) continue;
-      float s = 0.0f;
+  // chunk staging: this thread's float4 of K and of V (rows idx / 16, columns (idx % 16) * 4)
+  float4 rk[kALoads], rv[kALoads];
+  auto load = [&](int k0) {
 #pragma unroll
-      for (int c = 0; c < kSHD; ++c) s = fmaf(qv[c], Ks[kr][c], s);
-      if (s > m) {
-        const float alpha = expf(m - s);  // 0 on the first visible key (m = -inf)
-        l *= alpha;
-#pragma unroll
-        for (int c = 0; c < kSHD; ++c) o[c] *= alpha;
-        m = s;
+    for (int t = 0; t < kALoads; ++t) {
+      const int idx = threadIdx.x + kAThreads * t, kr = idx >> 4, c = (idx & 15) * 4, key = k0 + kr;
+      rk[t] = rv[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (key < p.N) {
+        rk[t] = __ldg(reinterpret_cast<const float4*>(base + (size_t)key * ld + D + c));
+        rv[t] = __ldg(reinterpret_cast<const float4*>(base + (size_t)key * ld + 2 * D + c));
       }
-      const float pw = expf(s - m);
-      l += pw;
+    }
+  };
+  float m_run = -INFINITY, l_run = 0.0f, o[8] = {};
+  if (kv_end > 0) load(0);
+  for (int k0 = 0; k0 < kv_end; k0 += kSK) {
+    __syncthreads();  // the previous chunk's K / V reads are done
 #pragma unroll
-      for (int c = 0; c < kSHD; ++c) o[c] = fmaf(pw, Vs[kr][c], o[c]);
+    for (int t = 0; t < kALoads; ++t) {
+      const int idx = threadIdx.x + kAThreads * t, kr = idx >> 4, c = (idx & 15) * 4;
+      *reinterpret_cast<float4*>(&Ks[kr][c]) = rk[t];
+      *reinterpret_cast<float4*>(&Vs[kr][c]) = rv[t];
     }
     __syncthreads();
-  }
-  if (valid) {
-    float* dst = reinterpret_cast<float*>(p.out) + ((size_t)b * p.N + q) * D + h * kSHD;
-    const float inv = 1.0f / l;
+    if (k0 + kSK < kv_end) load(k0 + kSK);  // in flight while this chunk is used
+    float s[4];
 #pragma unroll
-    for (int c = 0; c < kSHD; c += 4)
-      *reinterpret_cast<float4*>(dst + c) = make_float4(o[c] * inv, o[c + 1] * inv, o[c + 2] * inv, o[c + 3] * inv);
+    for (int j = 0; j < 4; ++j) {
+      const int kr = sub + 8 * j, key = k0 + kr;
+      float d0 = 0.0f, d1 = 0.0f;
+#pragma unroll
+      for (int c = 0; c < kSHD; c += 8) {
+        const float4 x = *reinterpret_cast<const float4*>(&Ks[kr][c]);
+        const float4 y = *reinterpret_cast<const float4*>(&Ks[kr][c + 4]);
+        d0 = fmaf(qv[c], x.x, d0);
+        d0 = fmaf(qv[c + 1], x.y, d0);
+        d0 = fmaf(qv[c + 2], x.z, d0);
+        d0 = fmaf(qv[c + 3], x.w, d0);
+        d1 = fmaf(qv[c + 4], y.x, d1);
+        d1 = fmaf(qv[c + 5], y.y, d1);
+        d1 = fmaf(qv[c + 6], y.z, d1);
+        d1 = fmaf(qv[c + 7], y.w, d1);
+      }
+      s[j] = (key >= lo && key < hi) ? d0 + d1 : -INFINITY;
+    }
+    float cm = fmaxf(fmaxf(s[0], s[1]), fmaxf(s[2], s[3]));
+#pragma unroll
+    for (int off = 4; off > 0; off >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, off));
+    const float m_new = fmaxf(m_run, cm);
+    // nothing visible yet: p = 0 and nothing to rescale
+    const float alpha = (m_new == -INFINITY) ? 1.0f : expf(m_run - m_new);
+    float ps = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float pj = (m_new == -INFINITY) ? 0.0f : expf(s[j] - m_new);
+      Ps[r][sub + 8 * j] = pj;
+      ps += pj;
+    }
+#pragma unroll
+    for (int off = 4; off > 0; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
+    l_run = l_run * alpha + ps;
+    m_run = m_new;
+    __syncwarp();  // the row's probabilities (written by its 8 threads, one warp) are visible
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[e] *= alpha;
+#pragma unroll 8
+    for (int kr = 0; kr < kSK; ++kr) {
+      const float pk = Ps[r][kr];
+      const float4 v0 = *reinterpret_cast<const float4*>(&Vs[kr][sub * 8]);
+      const float4 v1 = *reinterpret_cast<const float4*>(&Vs[kr][sub * 8 + 4]);
+      o[0] = fmaf(pk, v0.x, o[0]);
+      o[1] = fmaf(pk, v0.y, o[1]);
+      o[2] = fmaf(pk, v0.z, o[2]);
+      o[3] = fmaf(pk, v0.w, o[3]);
+      o[4] = fmaf(pk, v1.x, o[4]);
+      o[5] = fmaf(pk, v1.y, o[5]);
+      o[6] = fmaf(pk, v1.z, o[6]);
+      o[7] = fmaf(pk, v1.w, o[7]);
+    }
+    __syncwarp();  // Ps of this row is read before the next chunk overwrites it
+  }
+  if (q < p.N) {
+    float* dst = reinterpret_cast<float*>(p.out) + ((size_t)b * p.N + q) * D + h * kSHD + sub * 8;
+    const float inv = l_run > 0.0f ? 1.0f / l_run : 0.0f;
+    *reinterpret_cast<float4*>(dst) = make_float4(o[0] * inv, o[1] * inv, o[2] * inv, o[3] * inv);
+    *reinterpret_cast<float4*>(dst + 4) = make_float4(o[4] * inv, o[5] * inv, o[6] * inv, o[7] * inv);
   }
 }
 
@@ -142,7 +236,7 @@ cudaError_t attention_simt_launch(const float* qkv, const AttnParams& p, cudaStr
   AttnParams q = p;
   if (q.frame_tokens <= 0) q.frame_tokens = 1;
   dim3 grid((p.N + kSQ - 1) / kSQ, p.H, p.B);
-  return launch_kernel(attn_simt_kernel, grid, dim3(kSQ), 0, s, qkv, q);
+  return launch_kernel(attn_simt_kernel, grid, dim3(kAThreads), 0, s, qkv, q);
 }
 
 }  // namespace jepa
