@@ -120,9 +120,10 @@ __device__ __forceinline__ void ln_load(const float* __restrict__ x, int row, in
   }
 }
 
+// g, bta: gamma and beta as staged in the block's shared memory.
 template <int V, bool BF16>
-__device__ __forceinline__ void ln_row(const float4 (&v)[V], int row, int D, int lane, const float* __restrict__ g,
-                                       const float* __restrict__ bta, float eps, void* __restrict__ y) {
+__device__ __forceinline__ void ln_row(const float4 (&v)[V], int row, int D, int lane, const float* g,
+                                       const float* bta, float eps, void* __restrict__ y) {
   float sum = 0.0f;
 #pragma unroll
   for (int i = 0; i < V; ++i) sum += (v[i].x + v[i].y) + (v[i].z + v[i].w);
@@ -145,8 +146,8 @@ __device__ __forceinline__ void ln_row(const float4 (&v)[V], int row, int D, int
   for (int i = 0; i < V; ++i) {
     const int c = (lane + 32 * i) * 4;
     if (c >= D) continue;
-    const float4 gg = __ldg(reinterpret_cast<const float4*>(g + c));
-    const float4 bb = __ldg(reinterpret_cast<const float4*>(bta + c));
+    const float4 gg = *reinterpret_cast<const float4*>(g + c);
+    const float4 bb = *reinterpret_cast<const float4*>(bta + c);
     const float o0 = (v[i].x - mu) * rstd * gg.x + bb.x;
     const float o1 = (v[i].y - mu) * rstd * gg.y + bb.y;
     const float o2 = (v[i].z - mu) * rstd * gg.z + bb.z;
@@ -166,6 +167,14 @@ template <int V, bool BF16>
 __global__ void __launch_bounds__(256, 2) layernorm_kernel(const float* __restrict__ x, int M, int D,
                                                         const float* __restrict__ g, const float* __restrict__ bta,
                                                         float eps, void* __restrict__ y) {
+  // gamma and beta are weights, written by no kernel of the sequence: staged in shared memory
+  // before waiting for the previous kernel
+  __shared__ __align__(16) float sg[V * 128], sb[V * 128];
+  for (int c = threadIdx.x * 4; c < D; c += 256 * 4) {
+    *reinterpret_cast<float4*>(sg + c) = __ldg(reinterpret_cast<const float4*>(g + c));
+    *reinterpret_cast<float4*>(sb + c) = __ldg(reinterpret_cast<const float4*>(bta + c));
+  }
+  __syncthreads();
   pdl_trigger();
   pdl_wait();
   const int lane = threadIdx.x & 31;
@@ -176,11 +185,11 @@ __global__ void __launch_bounds__(256, 2) layernorm_kernel(const float* __restri
   while (row < M) {
     const int r1 = row + stride;
     if (r1 < M) ln_load<V>(x, r1, D, lane, b);
-    ln_row<V, BF16>(a, row, D, lane, g, bta, eps, y);
+    ln_row<V, BF16>(a, row, D, lane, sg, sb, eps, y);
     if (r1 >= M) break;
     const int r2 = r1 + stride;
     if (r2 < M) ln_load<V>(x, r2, D, lane, a);
-    ln_row<V, BF16>(b, r1, D, lane, g, bta, eps, y);
+    ln_row<V, BF16>(b, r1, D, lane, sg, sb, eps, y);
     row = r2;
   }
 }
