@@ -25,24 +25,24 @@ __device__ __forceinline__ size_t pix_index(int layout, int T, int C, int H, int
                      : ((((size_t)b * C + c) * T + f) * H + y) * (size_t)W + x;
 }
 
-// Vectorised path: each thread writes 8 consecutive elements (16 bytes of bf16) read as two float4.
-// Needs P % 8 == 0 and W % 4 == 0 (16-byte aligned pixel runs).
+// Vectorised path: one CTA per patch row (persistent over rows when there are more rows than the
+// grid), one thread per 8 consecutive elements of the row (16 bytes of bf16, read as two float4 of
+// one pixel row). A thread's element offset within the row, and so its (channel, frame offset,
+// dy, dx) and pixel offset, is the same for every row and is computed once; each row adds the
+// patch's own (item, frame, y, x) origin. Needs P % 8 == 0, W % 4 == 0 and K / 8 <= 1024.
 __global__ void patchify_bf16_v8_kernel(const float* __restrict__ pix, int B, int T, int C, int H, int W, int t,
                                         int P, int layout, __nv_bfloat16* __restrict__ out) {
   pdl_trigger();
   pdl_wait();
   const int gt = T / t, gh = H / P, gw = W / P;
-  const int K = C * t * P * P;
-  const int chunks_per_row = K / 8;
-  const long long total = (long long)B * gt * gh * gw * chunks_per_row;
-  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
-       idx += (long long)gridDim.x * blockDim.x) {
-    const long long row = idx / chunks_per_row;
-    const int k = (int)(idx % chunks_per_row) * 8;
-    const int b = (int)(row / ((long long)gt * gh * gw));
-    const int i = (int)(row % ((long long)gt * gh * gw));
-    const int tt = i / (gh * gw), hh = (i % (gh * gw)) / gw, ww = i % gw;
-    const int dx = k % P, dy = (k / P) % P, dt = (k / (P * P)) % t, c = k / (P * P * t);
+  const int K = C * t * P * P, np = gt * gh * gw;
+  const int k = threadIdx.x * 8;
+  if (k >= K) return;
+  const int dx = k % P, dy = (k / P) % P, dt = (k / (P * P)) % t, c = k / (P * P * t);
+  const long long rows = (long long)B * np;
+  for (long long row = blockIdx.x; row < rows; row += gridDim.x) {
+    const int b = (int)(row / np), i = (int)(row % np);
+    const int tt = i / (gh * gw), hw = i % (gh * gw), hh = hw / gw, ww = hw % gw;
     const float4* src = reinterpret_cast<const float4*>(
         pix + pix_index(layout, T, C, H, W, b, tt * t + dt, c, hh * P + dy, ww * P + dx));
     const float4 u = __ldg(src), v = __ldg(src + 1);
@@ -94,9 +94,12 @@ cudaError_t patchify_launch(const float* pix, int B, int T, int C, int H, int W,
   const long long rows = (long long)B * (T / t) * (H / P) * (W / P);
   const int K = C * t * P * P;
   if (rows <= 0) return cudaSuccess;
-  if (out_bf16 && P % 8 == 0 && W % 4 == 0 && (reinterpret_cast<uintptr_t>(pix) & 15) == 0) {
-    return launch_kernel(patchify_bf16_v8_kernel, dim3(grid_for(rows * (K / 8), 256)), dim3(256), 0, s, pix, B, T, C,
-                         H, W, t, P, layout, reinterpret_cast<__nv_bfloat16*>(out));
+  if (out_bf16 && P % 8 == 0 && W % 4 == 0 && K / 8 <= 1024 && (reinterpret_cast<uintptr_t>(pix) & 15) == 0) {
+    const int threads = ((K / 8 + 31) / 32) * 32;
+    const long long cap = (long long)num_sms() * (2048 / threads);
+    const int grid = (int)(rows < cap ? rows : cap);
+    return launch_kernel(patchify_bf16_v8_kernel, dim3(grid), dim3(threads), 0, s, pix, B, T, C, H, W, t, P, layout,
+                         reinterpret_cast<__nv_bfloat16*>(out));
   }
   return launch_kernel(out_bf16 ? patchify_scalar_kernel<true> : patchify_scalar_kernel<false>,
                        dim3(grid_for(rows * K, 256)), dim3(256), 0, s, pix, B, T, C, H, W, t, P, layout, out);
