@@ -54,6 +54,8 @@ uint64_t default_wait_limit_ns();
 // gemm_tc_b_box(BN) x 64 where BN = gemm_tc_pick_bn(M, N); BN == kPairTile selects the 2-SM
 // (cluster pair) kernel with 256 x 256 tiles. tmO = make_tmap_2d_out over epi.out (bf16 for
 // BIAS / GELU / QKV_ROPE, fp32 for RESIDUAL; unused for PATCH, which stores from registers).
+// B holds weights: in a programmatic launch sequence its first stages are requested before the
+// wait on the previous kernel, so no kernel of the sequence may write it.
 constexpr int kPairTile = 512;
 int gemm_tc_pick_bn(int M, int N);
 int gemm_tc_b_box(int bn);
@@ -63,7 +65,8 @@ cudaError_t gemm_tc2_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, cons
 cudaError_t gemm_tc_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmO, int BN,
                            const EpiArgs& epi, int M, int N, int K, int* err, uint64_t limit_ns, cudaStream_t s);
 
-// fp32 SIMT GEMM with the same epilogues.
+// fp32 SIMT GEMM with the same epilogues. In a programmatic launch sequence its first B (weight)
+// step is read before the wait on the previous kernel, like the tcgen05 GEMMs' first weight stages.
 cudaError_t gemm_simt_launch(const float* A, const float* Bw, const EpiArgs& epi, int M, int N, int K,
                              cudaStream_t s);
 

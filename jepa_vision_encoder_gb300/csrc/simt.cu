@@ -23,7 +23,6 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const float* __restrict_
   __shared__ __align__(16) float sm[kKS * 2 * kTK * kLd];  // per warp A and B slices; then the partial tiles
   static_assert(kKS * 2 * kTK * kLd >= kKS * kTM * kTN, "partial tiles fit the staging area");
   pdl_trigger();
-  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.y * kTM, n0 = blockIdx.x * kTN;
   float* As = sm + warp * 2 * kTK * kLd;  // [kTK][kLd]: As[kk][row]
@@ -33,15 +32,25 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const float* __restrict_
   const int r0 = (lane >> 2) * 4, c0 = (lane & 3) * 8;  // this lane's 4 x 8 outputs
   float acc[4][8] = {};
   float ra[16], rb[16];  // one step of A and B (32 x 16 each), 16 values per lane
-  auto load = [&](int st) {
+  auto load_a = [&](int st) {
 #pragma unroll
     for (int t = 0; t < 16; ++t) {
       const int idx = lane + 32 * t, row = idx / kTK, kk = idx % kTK, gk = st * kTK + kk;
       ra[t] = (m0 + row < M && gk < K) ? __ldg(A + (size_t)(m0 + row) * K + gk) : 0.0f;
+    }
+  };
+  auto load_b = [&](int st) {
+#pragma unroll
+    for (int t = 0; t < 16; ++t) {
+      const int idx = lane + 32 * t, row = idx / kTK, kk = idx % kTK, gk = st * kTK + kk;
       rb[t] = (n0 + row < N && gk < K) ? __ldg(Bw + (size_t)(n0 + row) * K + gk) : 0.0f;
     }
   };
-  if (s_begin < s_end) load(s_begin);
+  // B holds weights, written by no kernel of the sequence: its first step is requested before
+  // waiting for the kernel that produced A
+  if (s_begin < s_end) load_b(s_begin);
+  pdl_wait();
+  if (s_begin < s_end) load_a(s_begin);
   for (int st = s_begin; st < s_end; ++st) {
     __syncwarp();  // the previous step's shared-memory reads are done
 #pragma unroll
@@ -51,7 +60,10 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const float* __restrict_
       Bs[kk * kLd + row] = rb[t];
     }
     __syncwarp();
-    if (st + 1 < s_end) load(st + 1);  // in flight during this step's FMAs
+    if (st + 1 < s_end) {  // in flight during this step's FMAs
+      load_a(st + 1);
+      load_b(st + 1);
+    }
 #pragma unroll
     for (int kk = 0; kk < kTK; ++kk) {
       const float4 a4 = *reinterpret_cast<const float4*>(As + kk * kLd + r0);
