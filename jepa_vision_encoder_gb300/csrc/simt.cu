@@ -100,15 +100,15 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const float* __restrict_
   if (m < M && n < N) epi_fragment<4, false>(epi, m, n, v);
 }
 
-// fp32 attention ("Architecture", attention): a CTA per (8 query rows, head, item), 8 threads per
-// query row, the row's scaled q in registers. Keys come in chunks of 32 staged in shared memory
+// fp32 attention ("Architecture", attention): a CTA per (8 query rows, head, item), kTpr threads
+// per query row, the row's scaled q in registers. Keys come in chunks of 32 staged in shared memory
 // (the next chunk's loads in flight while one is scored); thread `sub` of a row scores keys sub,
-// sub + 8, sub + 16 and sub + 24 of the chunk (64-wide dot products, conflict-free 16-byte reads),
-// the row's 8 threads combine the chunk maximum and sum by shuffles (online softmax: earlier sums
-// and outputs rescaled when the maximum moves), and each accumulates 8 of the row's 64 output
-// columns over the chunk's keys.
-constexpr int kSQ = 8, kSK = 32, kSHD = 64, kKLd = kSHD + 4;
-constexpr int kAThreads = kSQ * 8, kALoads = kSK * (kSHD / 4) / kAThreads;  // float4 of K (and of V) per thread
+// sub + kTpr, ... of the chunk (64-wide dot products from 16-byte shared-memory reads), the row's
+// threads combine the chunk maximum and sum by shuffles (online softmax: earlier sums and outputs
+// rescaled when the maximum moves), and each accumulates 64 / kTpr of the row's output columns.
+constexpr int kSQ = 8, kSK = 32, kSHD = 64, kKLd = kSHD + 4, kTpr = 16;
+constexpr int kAThreads = kSQ * kTpr, kALoads = kSK * (kSHD / 4) / kAThreads;  // float4 of K (and of V) per thread
+constexpr int kKpt = kSK / kTpr, kOpt = kSHD / kTpr;  // keys scored, output columns per thread
 
 __global__ void __launch_bounds__(kAThreads) attn_simt_kernel(const float* __restrict__ qkv, AttnParams p) {
   __shared__ __align__(16) float Ks[kSK][kKLd];
@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(kAThreads) attn_simt_kernel(const float* __res
   const int h = blockIdx.y, b = blockIdx.z;
   const int D = p.H * kSHD, ld = 3 * D;
   const int q0 = blockIdx.x * kSQ;
-  const int r = threadIdx.x >> 3, sub = threadIdx.x & 7;  // query row of the CTA, its eighth
+  const int r = threadIdx.x / kTpr, sub = threadIdx.x % kTpr;  // query row of the CTA, its share
   const int q = q0 + r;
   const float* base = qkv + (size_t)b * p.N * ld + h * kSHD;
   float qv[kSHD];
@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(kAThreads) attn_simt_kernel(const float* __res
       }
     }
   };
-  float m_run = -INFINITY, l_run = 0.0f, o[8] = {};
+  float m_run = -INFINITY, l_run = 0.0f, o[kOpt] = {};
   if (kv_end > 0) load(0);
   for (int k0 = 0; k0 < kv_end; k0 += kSK) {
     __syncthreads();  // the previous chunk's K / V reads are done
@@ -169,10 +169,10 @@ __global__ void __launch_bounds__(kAThreads) attn_simt_kernel(const float* __res
     }
     __syncthreads();
     if (k0 + kSK < kv_end) load(k0 + kSK);  // in flight while this chunk is used
-    float s[4];
+    float s[kKpt];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int kr = sub + 8 * j, key = k0 + kr;
+    for (int j = 0; j < kKpt; ++j) {
+      const int kr = sub + kTpr * j, key = k0 + kr;
       float d0 = 0.0f, d1 = 0.0f;
 #pragma unroll
       for (int c = 0; c < kSHD; c += 8) {
@@ -189,47 +189,48 @@ __global__ void __launch_bounds__(kAThreads) attn_simt_kernel(const float* __res
       }
       s[j] = (key >= lo && key < hi) ? d0 + d1 : -INFINITY;
     }
-    float cm = fmaxf(fmaxf(s[0], s[1]), fmaxf(s[2], s[3]));
+    float cm = s[0];
 #pragma unroll
-    for (int off = 4; off > 0; off >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, off));
+    for (int j = 1; j < kKpt; ++j) cm = fmaxf(cm, s[j]);
+#pragma unroll
+    for (int off = kTpr / 2; off > 0; off >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, off));
     const float m_new = fmaxf(m_run, cm);
     // nothing visible yet: p = 0 and nothing to rescale
     const float alpha = (m_new == -INFINITY) ? 1.0f : expf(m_run - m_new);
     float ps = 0.0f;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < kKpt; ++j) {
       const float pj = (m_new == -INFINITY) ? 0.0f : expf(s[j] - m_new);
-      Ps[r][sub + 8 * j] = pj;
+      Ps[r][sub + kTpr * j] = pj;
       ps += pj;
     }
 #pragma unroll
-    for (int off = 4; off > 0; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
+    for (int off = kTpr / 2; off > 0; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
     l_run = l_run * alpha + ps;
     m_run = m_new;
-    __syncwarp();  // the row's probabilities (written by its 8 threads, one warp) are visible
+    __syncwarp();  // the row's probabilities (written by its threads, all in this warp) are visible
 #pragma unroll
-    for (int e = 0; e < 8; ++e) o[e] *= alpha;
+    for (int e = 0; e < kOpt; ++e) o[e] *= alpha;
 #pragma unroll 8
     for (int kr = 0; kr < kSK; ++kr) {
       const float pk = Ps[r][kr];
-      const float4 v0 = *reinterpret_cast<const float4*>(&Vs[kr][sub * 8]);
-      const float4 v1 = *reinterpret_cast<const float4*>(&Vs[kr][sub * 8 + 4]);
-      o[0] = fmaf(pk, v0.x, o[0]);
-      o[1] = fmaf(pk, v0.y, o[1]);
-      o[2] = fmaf(pk, v0.z, o[2]);
-      o[3] = fmaf(pk, v0.w, o[3]);
-      o[4] = fmaf(pk, v1.x, o[4]);
-      o[5] = fmaf(pk, v1.y, o[5]);
-      o[6] = fmaf(pk, v1.z, o[6]);
-      o[7] = fmaf(pk, v1.w, o[7]);
+#pragma unroll
+      for (int e = 0; e < kOpt; e += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(&Vs[kr][sub * kOpt + e]);
+        o[e] = fmaf(pk, v.x, o[e]);
+        o[e + 1] = fmaf(pk, v.y, o[e + 1]);
+        o[e + 2] = fmaf(pk, v.z, o[e + 2]);
+        o[e + 3] = fmaf(pk, v.w, o[e + 3]);
+      }
     }
     __syncwarp();  // Ps of this row is read before the next chunk overwrites it
   }
   if (q < p.N) {
-    float* dst = reinterpret_cast<float*>(p.out) + ((size_t)b * p.N + q) * D + h * kSHD + sub * 8;
+    float* dst = reinterpret_cast<float*>(p.out) + ((size_t)b * p.N + q) * D + h * kSHD + sub * kOpt;
     const float inv = l_run > 0.0f ? 1.0f / l_run : 0.0f;
-    *reinterpret_cast<float4*>(dst) = make_float4(o[0] * inv, o[1] * inv, o[2] * inv, o[3] * inv);
-    *reinterpret_cast<float4*>(dst + 4) = make_float4(o[4] * inv, o[5] * inv, o[6] * inv, o[7] * inv);
+#pragma unroll
+    for (int e = 0; e < kOpt; e += 4)
+      *reinterpret_cast<float4*>(dst + e) = make_float4(o[e] * inv, o[e + 1] * inv, o[e + 2] * inv, o[e + 3] * inv);
   }
 }
 
