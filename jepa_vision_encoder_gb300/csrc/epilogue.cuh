@@ -431,6 +431,7 @@ __device__ __forceinline__ void epi_warp_qkv_hd64(const EpiArgs& a, const CUtens
 #pragma unroll
     for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[i & 1][e]);
     const int n0 = n_tile0 + c * 32;
+    if (n0 >= a.N) continue;  // past the last column (a ragged last tile): nothing to store
     epi_math_tc<kEpiBias>(a, y0 + lane, n0, v, bl[i]);
     if (n0 < qk_cols) {  // q and k columns rotate (warp-uniform); v columns pass
       if (a.rope_layout == 0)
@@ -496,6 +497,7 @@ __device__ __forceinline__ void epi_warp_qkv_hd32(const EpiArgs& a, const CUtens
 #pragma unroll
     for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[i & 1][e]);
     const int n0 = n_tile0 + (c0 + i) * 32;
+    if (n0 >= a.N) continue;  // past the last column (a ragged last tile): nothing to store
     epi_math_tc<kEpiBias>(a, m, n0, v, bl[i]);
     if (n0 < qk_cols) {  // q and k heads rotate (warp-uniform); v heads pass
       if (a.rope_layout == 0)
@@ -522,7 +524,10 @@ __device__ __forceinline__ int epi_chunk_col(const EpiArgs& a, int i, int half) 
 template <int EK, int NCHUNK>
 __device__ __forceinline__ void epi_bias_lanes(const EpiArgs& a, int lane, int n_tile0, int half, float (&bl)[NCHUNK]) {
 #pragma unroll
-  for (int i = 0; i < NCHUNK; ++i) bl[i] = __ldg(a.bias + n_tile0 + epi_chunk_col<EK, NCHUNK>(a, i, half) + lane);
+  for (int i = 0; i < NCHUNK; ++i) {
+    const int n = n_tile0 + epi_chunk_col<EK, NCHUNK>(a, i, half) + lane;
+    bl[i] = n < a.N ? __ldg(a.bias + n) : 0.0f;  // columns past N: a ragged last tile
+  }
 }
 
 // What a warp's epilogue of one tile reads besides the accumulator, requested while the tile's
@@ -589,6 +594,7 @@ __device__ __forceinline__ void epi_warp_tile(const EpiArgs& a, const CUtensorMa
     float v[32];
 #pragma unroll
     for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[i & 1][e]);
+    if (n_tile0 + (c0 + i) * 32 >= a.N) continue;  // past the last column (a ragged last tile)
     epi_chunk_tc<EK>(a, tm, st, lane, y0, n_tile0 + (c0 + i) * 32, v, bl[i]);
   }
 }

@@ -229,8 +229,11 @@ int gemm_tc_pick_bn(int M, int N) {
     const double cost = (double)((tiles + sms - 1) / sms) * c.bn / c.eff;
     if (cost < best_cost) best_cost = cost, best = c.bn;
   }
-  if (N % 256 == 0 && sms >= 2) {
-    const long long pair_tiles = (long long)num_m2 * (N / 256);
+  // a last column tile that reaches past N computes zeros there (not stored): taken only while that
+  // waste stays under a tenth of the columns computed
+  const int n_pad = ((N + 255) / 256) * 256;
+  if (N % 64 == 0 && 10 * (n_pad - N) < n_pad && sms >= 2) {
+    const long long pair_tiles = (long long)num_m2 * (n_pad / 256);
     const int pairs = gemm_tc2_max_pairs();
     const double cost = (double)((pair_tiles + pairs - 1) / pairs) * 256 / 0.75;
     if (cost < best_cost) best_cost = cost, best = kPairTile;

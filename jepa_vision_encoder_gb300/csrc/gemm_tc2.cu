@@ -71,7 +71,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
   const int pair = blockIdx.x >> 1, num_pairs = gridDim.x >> 1;
-  const int num_m = (M + kTileM - 1) / kTileM, num_n = N / kTileN, num_k = K / kBK;
+  // N need not be a multiple of the tile: the last column tile's rows of B past N load as zeros
+  // (TMA fill) and its columns past N are not stored
+  const int num_m = (M + kTileM - 1) / kTileM, num_n = (N + kTileN - 1) / kTileN, num_k = K / kBK;
   const int num_tiles = num_m * num_n;
 
   if (threadIdx.x == 0) {
@@ -249,7 +251,7 @@ cudaError_t set_pair_attrs() {
 template <int TN, int EK>
 cudaError_t launch_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmO, const EpiArgs& epi,
                         int M, int N, int K, int* err, uint64_t limit_ns, cudaStream_t s) {
-  const int tiles = ((M + kTileM - 1) / kTileM) * (N / TN);
+  const int tiles = ((M + kTileM - 1) / kTileM) * ((N + TN - 1) / TN);
   const int max_pairs = gemm_tc2_max_pairs();
   const int pairs = tiles < max_pairs ? tiles : max_pairs;
   return launch_kernel(gemm_tc2_kernel<TN, EK>, dim3(2 * pairs), dim3(kThreads), PairCfg<TN>::kSmemBytes, s, tmA, tmB,
@@ -294,7 +296,7 @@ int gemm_tc2_max_pairs() {
 cudaError_t gemm_tc2_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmO,
                             const EpiArgs& epi, int M, int N, int K, int* err, uint64_t limit_ns, cudaStream_t s) {
   if (M <= 0) return cudaSuccess;
-  if (N % 256 || K % kBK) return cudaErrorInvalidValue;
+  if (N % 64 || K % kBK) return cudaErrorInvalidValue;
   return launch_pair_kind<256>(tmA, tmB, tmO, epi, M, N, K, err, limit_ns, s);
 }
 

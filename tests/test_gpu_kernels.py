@@ -99,9 +99,10 @@ def bf16_bound(ref, K):
 
 
 # (M, N, K): tile widths 256 (many tiles, > 1 per CTA), 128, 64; ragged M. (2125, 3072), (4099, 4096)
-# and (4099, 768) run on the 2-SM pair kernel.
+# and (4099, 768) run on the 2-SM pair kernel; (4099, 1408) and (4099, 2368) on the pair kernel with a
+# ragged last column tile (N % 256 = 128 and 64: the columns past N are loaded as zeros, not stored).
 GEMM_SHAPES = [(2048 + 77, 3072, 256), (2048, 1024, 1024), (257, 256, 128), (128, 64, 64), (4096 + 3, 4096, 128),
-               (4096 + 3, 768, 128)]
+               (4096 + 3, 768, 128), (4096 + 3, 1408, 128), (4096 + 3, 2368, 64)]
 
 
 @pytest.mark.parametrize("M,N,K", GEMM_SHAPES)
@@ -167,13 +168,11 @@ def test_rope_table(case):
 
 @pytest.mark.parametrize("case", list(ROPE_CASES))
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
-def test_qkv_rope_epilogue(case, dtype):
+def test_qkv_rope_epilogue(case, dtype, n_head=4, B=2):
     extra, (T, H, W) = ROPE_CASES[case]
-    n_head = 4
     cfg, hp = rope_cfgs(extra, n_head)
     D = 64 * n_head
     N = oracle.n_tokens(cfg, T, H, W)
-    B = 2
     M, K = B * N, 128
     x, w, bias = rnd((M, K), 12), rnd((3 * D, K), 13, 0.1), rnd(3 * D, 14, 0.1)
     if dtype == "bf16":
@@ -198,6 +197,12 @@ def test_qkv_rope_epilogue(case, dtype):
     wrong = ref_epilogue(jv.EPI_QKV_ROPE, acc, bias, n_head=n_head, head_dim=64, rows_per_item=N,
                          tables=oracle.rope_tables(other, T, H, W))
     assert np.abs(got - wrong).max() > 0.05 * np.abs(ref).max()
+
+
+def test_qkv_rope_epilogue_ragged_pair_tile():
+    # ViT-g's 22 heads: N = 3 * 1408 = 4224 = 16.5 pair tiles; 200 items of 24 tokens make M large
+    # enough for the pair kernel, whose last column tile is half past N
+    test_qkv_rope_epilogue("tiled", "bf16", n_head=22, B=200)
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
