@@ -4,13 +4,15 @@
 //
 // Warp roles (320 threads, one CTA per SM, grid = min(tiles, SMs), tiles strided over CTAs and
 // numbered N-fastest, so the CTAs working at the same time share rows of A and sweep the weights):
-//   warp 0      TMA producer: A tile 128x64 and B tile BNx64 per stage (128-byte swizzle)
+//   warp 0      TMA producer: A tile 128x64 and B tile BNx64 per stage (128-byte swizzle); the
+//               first tile's weight stages go out before the wait on the previous kernel
 //   warp 1      MMA issuer: 4 x tcgen05.mma (M=128, N=BN, K=16) per stage into one of two
 //               TMEM accumulators (2 x BN columns), so the epilogue of tile i overlaps the
 //               main loop of tile i+1
 //   warps 2..9  epilogue: two warps per TMEM lane quarter, each taking half of the tile's columns
 //               (for QKV, alternate 32-column chunks, so a warp meets one half of every head and
-//               keeps that half's RoPE (cos, sin) row in registers), 32 columns at a time (the
+//               keeps that half's RoPE (cos, sin) row in registers; bias and RoPE values are
+//               requested before the accumulator is ready), 32 columns at a time (the
 //               next tcgen05.ld in flight while one chunk is processed), then
 //               the fused bias / GELU / RoPE of epilogue.cuh; each 32-row x 64-byte piece goes
 //               through a per-warp pair of swizzled shared-memory buffers to a TMA store (bf16
