@@ -246,6 +246,8 @@ ATTN_CASES = [
     (1, 1 + 3 * 256, 2, 1, 1, 256),    # frames of two tiles each, shifted by the CLS row
     (1, 5 * 96, 2, 1, 0, 96),          # block-causal without a prefix
     (1, 1 + 200, 1, 1, 1, 200),        # one frame: full attention with the CLS column closed
+    (1, 2 + 2 * 256, 2, 1, 2, 256),    # two prefix rows
+    (1, 1 + 32 * 256, 1, 1, 1, 256),   # 8193 tokens: the prefix row over 65 key tiles
 ]
 
 

@@ -96,6 +96,26 @@ def test_attention_on_width_32_heads(B, N, H):
     assert np.abs(got - wrong).max() > 0.05
 
 
+def test_block_causal_on_width_32_heads():
+    # CLS + three frames of 256 rows (two tiles each): the frame-aligned tiling on 64-byte-swizzled
+    # tiles and the prefix-row CTA on width-32 heads
+    B, N, H, F = 1, 1 + 3 * 256, 2, 256
+    rng = np.random.default_rng(44)
+    q = rng.standard_normal((N, H * 32)) * np.sqrt(3.0)
+    k = rng.standard_normal((N, H * 32)) * np.sqrt(3.0)
+    v = rng.standard_normal((N, H * 32))
+    qkv = bf16_exact(np.concatenate([q, k, v], axis=1))
+    got = f64(jv.ops.attention(qkv.cuda(), B, N, H, 32, 1, 1, F))
+    e = f64(qkv)
+    P = H * 32
+    ref = oracle.attention(e[:, :P], e[:, P:2 * P], e[:, 2 * P:], H, 1, 1, F)
+    vmax = np.abs(e[:, 2 * P:]).max()
+    assert np.abs(got - ref).max() <= 0.01 * vmax
+    assert np.abs(got[:1] - ref[:1]).max() <= 0.01 * vmax  # the CLS row, which sees every key
+    full = oracle.attention(e[:, :P], e[:, P:2 * P], e[:, 2 * P:], H)
+    assert np.abs(got - full).max() > 0.01 * vmax
+
+
 # ------------------------------------------------------------------ whole predictor
 def check_pred(got, ref, what):
     got = np.asarray(got, dtype=np.float64).reshape(-1, ref.shape[-1])
