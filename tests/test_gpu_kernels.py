@@ -61,7 +61,7 @@ def test_patchify_bit_exact(t, P, T, H, W, layout, dtype):
 
 
 # ------------------------------------------------------------------ layernorm
-@pytest.mark.parametrize("M,D", [(333, 192), (257, 1024), (130, 1408), (5, 2048)])
+@pytest.mark.parametrize("M,D", [(333, 192), (257, 1024), (130, 1408), (5, 2048), (1, 1024)])
 def test_layernorm(M, D):
     x = rnd((M, D), 1, scale=3.0, offset=20.0)  # large offset: a one-pass variance would fail
     g, b = rnd(D, 2, 0.1, 1.0), rnd(D, 3, 0.01)
@@ -102,7 +102,8 @@ def bf16_bound(ref, K):
 # and (4099, 768) run on the 2-SM pair kernel; (4099, 1408) and (4099, 2368) on the pair kernel with a
 # ragged last column tile (N % 256 = 128 and 64: the columns past N are loaded as zeros, not stored).
 GEMM_SHAPES = [(2048 + 77, 3072, 256), (2048, 1024, 1024), (257, 256, 128), (128, 64, 64), (4096 + 3, 4096, 128),
-               (4096 + 3, 768, 128), (4096 + 3, 1408, 128), (4096 + 3, 2368, 64)]
+               (4096 + 3, 768, 128), (4096 + 3, 1408, 128), (4096 + 3, 2368, 64),
+               (1, 1024, 128), (129, 512, 64)]  # one row; one row past a tile
 
 
 @pytest.mark.parametrize("M,N,K", GEMM_SHAPES)
@@ -239,6 +240,8 @@ def attn_inputs(B, N, H, seed, sharp=3.0):
 ATTN_CASES = [
     # B, N, H, mode, prefix, frame_tokens
     (1, 128, 2, 0, 0, 1),
+    (3, 1, 2, 0, 0, 1),                # one token: the output is its own value row
+    (1, 129, 1, 0, 0, 1),              # one key past a tile
     (2, 257, 3, 0, 0, 1),
     (1, 1000, 2, 0, 0, 1),
     (1, 2048, 2, 0, 0, 1),
