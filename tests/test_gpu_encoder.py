@@ -69,6 +69,22 @@ def test_small_encoder_matches_oracle(name):
     check_bar(out.cpu().numpy(), ref, dtype, name)
 
 
+# The degenerate clips: one patch per frame (one token per tubelet; with a CLS row, two tokens),
+# so every kernel runs on a single row tile with one valid row and a 1 x 1 position grid.
+@pytest.mark.parametrize("name,T,H,W", [("vjepa2_vitl16_16x256", 2, 16, 16), ("vjepa2_1_vitl16_16x384", 2, 16, 16),
+                                        ("levjepa_vitl16_16x256", 1, 16, 16), ("levjepa_vitl16_16x256", 3, 16, 16)])
+def test_one_patch_clips_match_oracle(name, T, H, W):
+    cfg, dtype, _ = small(name)
+    B = 2
+    model, ctx = make(name, n_layer=cfg.n_layer, batch=B, T=T, H=H, W=W, cfg=cfg)
+    pix = synth.pixels(5, (B, T, 3, H, W))
+    out = ctx.encode(torch.from_numpy(pix).cuda())
+    ctx.sync()
+    ref = oracle.encode(cfg, 0, dtype == "bf16", pix)
+    assert out.shape == ref.shape
+    check_bar(out.cpu().numpy(), ref, dtype, f"{name} {T}x{H}x{W}")
+
+
 def test_weights_are_the_generator_bits():
     model = jv.Model.preset("vjepa2_vitl16", seed=0, dtype="bf16", n_layer=1)
     for name, shape in [("enc.blk.0.attn_qkv.weight", (3072, 1024)), ("enc.blk.0.ln1.weight", (1024,)),
